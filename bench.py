@@ -1,0 +1,418 @@
+"""Benchmark of the DSpark draft-sample -> schedule -> verify hot path.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload dspark5]
+
+One step = one decoding round for the whole batch: draft sampling of all G
+positions, calibration + prefix scheduling, and verification, on inputs
+already resident in HBM.  `value` is verified draft positions (sum of the
+scheduled verify lengths) per second over all ranks; the HBM figure is the
+algorithmic bytes of the round over the step time.  The e2e figure is the
+same metric with the per-round inputs copied from pinned host memory and the
+emitted tokens copied back inside the timed region.  Multi-GPU runs are
+independent replicas (one batch per rank, weak scaling, no collective on the
+data path); `--impl reference` times the CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "verified draft positions/sec & achieved HBM GB/s at V=129280, B=256, γ=5"
+UNIT = "positions/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[3:7]):
+                if p.lower() == "active":
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+def _dist_init(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# CPU oracle leg (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, h, seed, budget_s=12.0, threads=None):
+    """Time the oracle on a growing sample of requests of workload ``w``."""
+    import oracle
+    oracle.build()
+    threads = threads or len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    sch = oracle.schedule(h["conf_logits"], h["pos_temp"], h["sps"], w.L_min, w.G) if w.scheduler else None
+    t_sched = time.perf_counter() - t0
+    vl_all = sch["verify_len"] if sch is not None else np.full(w.B, w.G, np.int32)
+    n = min(w.B, max(threads, 8))
+    elapsed, done, positions = 0.0, 0, 0
+    rid_all = h["request_id"].numpy().astype(np.uint32)
+    e_in, w_out = oracle._f64(h["e_in"]), oracle._f64(h["w_out"])
+    while done < w.B:
+        reqs = np.arange(done, min(w.B, done + n))
+        t0 = time.perf_counter()
+        d = oracle.draft_sample_parallel(h["base"][reqs], e_in, w_out, h["anchor"][reqs],
+                                         h["temperature"][reqs], rid_all[reqs], seed, threads=threads)
+        oracle.verify_parallel(h["target"][reqs], h["base"][reqs], e_in, w_out, h["anchor"][reqs],
+                               d["tokens"], vl_all[reqs], h["temperature"][reqs], rid_all[reqs], seed,
+                               threads=threads)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done += len(reqs)
+        positions += int(vl_all[reqs].sum())
+        if elapsed >= budget_s:
+            break
+        remaining = budget_s - elapsed
+        per_req = dt / len(reqs)
+        n = int(max(1, min(w.B - done, remaining / max(per_req, 1e-9))))
+    total = elapsed + t_sched
+    return dict(value=positions / total, unit=UNIT, cores=threads, kind="oracle",
+                sample="%d of %d requests of one %s round (draft + verify per request, scheduler on "
+                       "all requests), %.1f s" % (done, w.B, w.name, total),
+                seconds=total, positions=positions)
+
+
+def run_reference(args, w):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from speculative_decoding_draft_head_gb300.synth import make_inputs
+    h = make_inputs(w, args.seed, device="cpu")
+    vals = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        budget = max(2.0, 60.0 / max(1, args.warmup + args.steps))
+        r = oracle_sample(w, h, args.seed, budget_s=budget)
+        if i >= args.warmup:
+            vals.append(r["value"])
+            info = r
+    value = float(np.mean(vals))
+    line = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=1000.0 * info["seconds"],
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                config=_config(w),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=info["cores"], kind="oracle",
+                                  sample=info["sample"]),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line))
+
+
+def _config(w):
+    return dict(workload="%s: B=%d, gamma=%d, V=%d, r=%d, %s logits" % (w.name, w.B, w.G, w.V, w.r, w.dtype),
+                B=w.B, gamma=w.G, V=w.V, r=w.r, storage=w.dtype, scheduler=w.scheduler,
+                l2="inputs larger than L2 (base and target logits > 129 MB); W_out stays L2-resident")
+
+
+# --------------------------------------------------------------------------
+# GPU leg
+# --------------------------------------------------------------------------
+
+def run_ours(args, w):
+    from speculative_decoding_draft_head_gb300 import binding
+    from speculative_decoding_draft_head_gb300.synth import make_inputs
+
+    rank, world, local = _dist_init(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load()
+    inp = make_inputs(w, args.seed + rank, device=dev, request_id_base=rank * w.B)
+    stream = torch.cuda.current_stream(dev)
+    s_ = 2 if w.dtype == "bf16" else 4
+    B, G, V, r = w.B, w.G, w.V, w.r
+
+    ws_d = binding.default_workspace(binding.WS_DRAFT, B, G, V, r, dev)
+    ws_s = binding.default_workspace(binding.WS_SCHEDULE, B, G, 8, 1, dev)
+    ws_v = binding.default_workspace(binding.WS_VERIFY, B, G, V, r, dev)
+    d_out = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
+                 lse=torch.empty((B, G), dtype=torch.float32, device=dev),
+                 logq=torch.empty((B, G), dtype=torch.float32, device=dev))
+    s_out = dict(conf=torch.empty((B, G), dtype=torch.float32, device=dev),
+                 cum_conf=torch.empty((B, G), dtype=torch.float32, device=dev),
+                 verify_len=torch.full((B,), G, dtype=torch.int32, device=dev),
+                 theta=torch.empty((1,), dtype=torch.float64, device=dev))
+    v_out = dict(accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                 out_tokens=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
+                 num_out=torch.empty((B,), dtype=torch.int32, device=dev),
+                 target_lse=torch.empty((B, G + 1), dtype=torch.float32, device=dev),
+                 logp=torch.empty((B, G), dtype=torch.float32, device=dev))
+
+    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for k in ("draft", "sched", "verify")}
+    call_ms = {k: [] for k in ev}
+
+    def step(x, timed=False):
+        if timed:
+            ev["draft"][0].record(stream)
+        binding.draft_sample(x["base"], x["e_in"], x["w_out"], x["anchor"], x["temperature"],
+                             x["request_id"], args.seed, out=d_out, workspace=ws_d, stream=stream)
+        if timed:
+            ev["draft"][1].record(stream)
+            ev["sched"][0].record(stream)
+        vl = None
+        if w.scheduler:
+            binding.schedule_prefix(x["conf_logits"], x["pos_temp"], x["sps"], w.L_min, G, out=s_out,
+                                    workspace=ws_s, stream=stream)
+            vl = s_out["verify_len"]
+        if timed:
+            ev["sched"][1].record(stream)
+            ev["verify"][0].record(stream)
+        binding.verify(x["target"], x["base"], x["e_in"], x["w_out"], x["anchor"], d_out, vl,
+                       x["temperature"], x["request_id"], args.seed, out=v_out, workspace=ws_v,
+                       stream=stream)
+        if timed:
+            ev["verify"][1].record(stream)
+
+    for _ in range(args.warmup):
+        step(inp)
+    torch.cuda.synchronize()
+    vl_host = s_out["verify_len"].cpu().numpy() if w.scheduler else np.full(B, G)
+    positions = int(vl_host.sum())
+    n_rej = int((v_out["accept_len"] < (s_out["verify_len"] if w.scheduler else G)).sum().item())
+
+    # per-call timing (events around each call), then the whole-step timing
+    for _ in range(max(3, min(args.steps, 20))):
+        step(inp, timed=True)
+        torch.cuda.synchronize()
+        for k in ev:
+            call_ms[k].append(ev[k][0].elapsed_time(ev[k][1]))
+
+    clocks = ClockSampler(dev.index)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(inp)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    ms = t0.elapsed_time(t1) / args.steps
+    clk = clocks.stop() if rank == 0 else None
+    ms_max = _max_over_ranks(ms, world)
+    total_positions = _sum_over_ranks(positions, world)
+    value = total_positions / (ms_max / 1000.0)
+
+    # end to end: per-round inputs from pinned host memory, emitted tokens back
+    per_round = ("base", "target", "anchor", "temperature", "request_id", "conf_logits")
+    host = {k: inp[k].cpu().pin_memory() for k in per_round}
+    dev_in = dict(inp)
+    out_host = dict(out_tokens=torch.empty((B, G + 1), dtype=torch.int32).pin_memory(),
+                    num_out=torch.empty((B,), dtype=torch.int32).pin_memory())
+    h2d = sum(host[k].numel() * host[k].element_size() for k in per_round)
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    def e2e_step():
+        for k in per_round:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        step(dev_in)
+        out_host["out_tokens"].copy_(v_out["out_tokens"], non_blocking=True)
+        out_host["num_out"].copy_(v_out["num_out"], non_blocking=True)
+
+    dev_in = {k: (inp[k].clone() if k in per_round else inp[k]) for k in inp}
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, args.steps // 4)
+    _barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    e_ms = _max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
+    e_value = total_positions / (e_ms / 1000.0)
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    # algorithmic bytes of one round
+    draft_bytes = B * G * V * s_ + r * V * s_ + B * G * r * s_
+    verify_bytes = int((vl_host + 1).sum()) * V * s_
+    residual_bytes = n_rej * V * s_ * 2
+    round_bytes = draft_bytes + verify_bytes + residual_bytes
+    d_ms = statistics.median(call_ms["draft"])
+    v_ms = statistics.median(call_ms["verify"])
+    s_ms = statistics.median(call_ms["sched"])
+    dominant = "draft" if d_ms >= v_ms else "verify"
+    dom_bytes = draft_bytes if dominant == "draft" else verify_bytes + residual_bytes
+    dom_ms = d_ms if dominant == "draft" else v_ms
+    launches_per_call = 2 * G if dominant == "draft" else 4
+    achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
+    bias_flops = 2.0 * B * G * V * r
+    traffic = _read_traffic(w, dominant)
+    line = dict(
+        metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=ms_max, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f32",
+        data="synthetic", config=_config(w),
+        hbm_gbs=round_bytes / (ms / 1000.0) / 1e9,
+        positions_per_step=positions,
+        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                      frac=achieved / peaks["hbm_gbs"], traffic=traffic,
+                      kernel="%s call (%d launches per call)" % (dominant, launches_per_call),
+                      peak_source=peaks["source"]),
+        calls_ms=dict(draft=d_ms, schedule=s_ms, verify=v_ms),
+        bias_gemm=dict(flops_per_round=bias_flops,
+                       tflops_over_draft_time=bias_flops / (d_ms / 1000.0) / 1e12,
+                       peak_tflops=peaks["bf16_tflops_sustained"]),
+        e2e=dict(value=e_value, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
+                 ms_per_step=e_ms),
+        gpu_launches=args.steps * (2 * G + (1 if w.scheduler else 0) + 4),
+        clocks=clk,
+    )
+    if not args.no_cpu_baseline and world == 1:
+        h = {k: t.cpu() for k, t in inp.items()}
+        cb = oracle_sample(w, h, args.seed, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = dict(value=cb["value"], unit=UNIT, cores=cb["cores"], kind="oracle",
+                                    sample=cb["sample"])
+    print(json.dumps(line))
+
+
+def _read_traffic(w, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if one matches."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get("%s/%s" % (w.name, kernel))
+    return None if e is None else e.get("dram_bytes_per_call")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dspark5")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from speculative_decoding_draft_head_gb300.synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,214 @@
+/*
+ * dspark.h -- C ABI of libdspark: the data-parallel hot path of DSpark-style
+ * speculative decoding on one GB300 (sm_103a) GPU.
+ *
+ * One decoding round for a batch of B requests with block length G over a
+ * vocabulary of V tokens is three calls:
+ *
+ *   dspark_draft_sample     draft G tokens per request with the
+ *                           semi-autoregressive Markov head;
+ *   dspark_schedule_prefix  calibrate per-position confidences and choose how
+ *                           many draft tokens of each request to verify;
+ *   dspark_verify           lossless rejection-sampling verification against
+ *                           the target logits, with residual resampling or a
+ *                           bonus token.
+ *
+ * Conventions shared by every entry point
+ *  - Every array argument is a DEVICE pointer owned by the caller, row-major
+ *    and contiguous (the last index is contiguous).  The library never
+ *    allocates or frees memory.  Pointers to logits, E_in and W_out must be
+ *    16-byte aligned; V must be a multiple of 8.
+ *  - "dtype" arrays hold bf16 (DSPARK_BF16) or fp32 (DSPARK_F32) values; all
+ *    arithmetic is fp32 on the device (the scheduler uses fp64).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls only enqueue work: they do not synchronise.
+ *  - `workspace` is caller-owned device scratch memory of at least
+ *    dspark_workspace_bytes(...) bytes, 256-byte aligned.  One workspace must
+ *    not be shared by two calls that may run concurrently.
+ *  - Host-side argument errors return DSPARK_ERR_INVALID_ARG before any launch
+ *    and leave the outputs untouched.  CUDA launch errors return
+ *    DSPARK_ERR_CUDA.  The message of the last failure on the calling thread
+ *    is available from dspark_last_error().
+ *  - Device-resident inputs (token ids, temperatures, verify lengths) are
+ *    checked by the kernels: a request with an out-of-range value gets -1 in
+ *    its output tokens and sets a bit in the workspace's flag word, which
+ *    dspark_read_device_flags() returns.  Kernels never read out of bounds.
+ *  - Randomness: Philox4x32-10 (Salmon et al., SC'11) with key =
+ *    (seed mod 2^32, seed >> 32) and counter = (v >> 2, j, request_id,
+ *    stream), output word v & 3; u = ((w >> 9) + 0.5) * 2^-23.  Streams:
+ *    0 draft Gumbel noise, 1 acceptance uniform, 2 residual Gumbel noise,
+ *    3 bonus Gumbel noise.  A call is reproducible from (seed, request ids).
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dspark_status {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARG = 1,   /* bad size, pointer, alignment or workspace */
+    DSPARK_ERR_UNSUPPORTED = 2,   /* valid request the library does not handle */
+    DSPARK_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    DSPARK_ERR_TIMEOUT = 4        /* a bounded device-side wait gave up */
+} dspark_status;
+
+typedef enum dspark_dtype {
+    DSPARK_BF16 = 0,
+    DSPARK_F32 = 1
+} dspark_dtype;
+
+/* which workspace: argument of dspark_workspace_bytes */
+enum {
+    DSPARK_WS_DRAFT = 0,
+    DSPARK_WS_SCHEDULE = 1,
+    DSPARK_WS_VERIFY = 2
+};
+
+/* bits of the device flag word */
+enum {
+    DSPARK_FLAG_BAD_TOKEN = 1u,        /* an anchor or draft token outside [0, V) */
+    DSPARK_FLAG_BAD_TEMPERATURE = 2u,  /* a temperature that is negative, NaN or inf */
+    DSPARK_FLAG_BAD_VERIFY_LEN = 4u,   /* a verify length outside [0, G] */
+    DSPARK_FLAG_BAD_POS_TEMP = 8u      /* a calibration temperature <= 0 or NaN */
+};
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+DSPARK_API int dspark_version(void);
+
+/* Message of the last failed call on the calling thread ("" if none). */
+DSPARK_API const char *dspark_last_error(void);
+
+/* Bytes of workspace needed by one call of the given kind (DSPARK_WS_*), for
+ * B requests, block length G, vocabulary V, Markov rank r.  Returns 0 for
+ * invalid sizes. */
+DSPARK_API size_t dspark_workspace_bytes(int which, int B, int G, int V, int r);
+
+/*
+ * Draft sampling with the semi-autoregressive Markov head.
+ *
+ * Defined by "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
+ * "Un po' di autoregressione basta", equation for p_k: the draft distribution
+ * of position j is softmax(U_j + B_j) where the bias B_j = E_in[x_{j-1}] W_out
+ * is the rank-r Markov head (B = W1 W2) driven by the previous token (the
+ * anchor x_0 for the first position), and tokens are drawn left to right so
+ * each keeps an explicit softmax probability.
+ *
+ * For each request b and j = 0 .. G-1, with prev = anchor[b] (j = 0) or
+ * draft_tokens[b][j-1]:
+ *   z[v]  = base_logits[b][j][v] + sum_k e_in[prev][k] * w_out[k][v]   (fp32)
+ *   T > 0: s = z / T, lse = log sum exp s, x_j = argmax_v s[v] + g_v with
+ *          g_v = -ln(-ln u(seed, request_id[b], j, v, stream 0)),
+ *          logq = s[x_j] - lse
+ *   T = 0: x_j = argmax_v z[v] (lowest id on ties), lse = max z, logq = 0
+ *
+ * base_logits [B][G][V] dtype   e_in [V][r] dtype   w_out [r][V] dtype
+ * anchor [B] int32              temperature [B] fp32 (>= 0)
+ * request_id [B] uint32 or NULL (then request b uses id b)
+ * outputs: draft_tokens [B][G] int32, draft_lse [B][G] fp32,
+ *          draft_logq [B][G] fp32, draft_logits [B][G][V] fp32 z or NULL.
+ * Limits: 1 <= B, 1 <= G <= 64, 8 <= V < 2^31 with V % 8 == 0,
+ *         16 <= r <= 256 with r % 16 == 0 (bf16) or 1 <= r <= 256 (fp32).
+ */
+DSPARK_API dspark_status dspark_draft_sample(
+    const void *base_logits, const void *e_in, const void *w_out,
+    const int32_t *anchor, const float *temperature, const uint32_t *request_id,
+    int B, int G, int V, int r, dspark_dtype dtype, uint64_t seed,
+    int32_t *draft_tokens, float *draft_lse, float *draft_logq, float *draft_logits,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Confidence calibration and the load-aware prefix scheduler.
+ *
+ * Defined by "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
+ * "Verificare meglio, non di piu'": c = per-position temperature-scaled
+ * confidence, a_{b,j} = prod_{i<=j} c_{b,i}, Theta = tau * SPS(B); candidates
+ * of all requests are admitted in decreasing a while Theta grows, stopping at
+ * the first one that does not raise it.
+ *
+ *   c[b][j]   = 1 / (1 + exp(-conf_logits[b][j] / pos_temp[j]))
+ *   a[b][j]   = prod_{i <= j} c[b][i]
+ *   start:    L_b = L_min, tau = sum_b (1 + sum_{j < L_b} a[b][j]),
+ *             n = sum_b (L_b + 1) batch tokens
+ *   candidates (b, j), L_min <= j < L_max, in order (a desc, j asc, b asc):
+ *             admit (L_b = j + 1) while (tau + a) * sps[n + 1] > tau * sps[n]
+ *
+ * conf_logits [B][G] fp32, pos_temp [G] fp32 (> 0), sps [sps_len] fp32 with
+ * sps[n] = engine steps per second at n batch tokens, sps_len >=
+ * B * (L_max + 1) + 1.  Outputs: conf, cum_conf [B][G] fp32, verify_len [B]
+ * int32, theta_out [1] fp64 (final Theta) or NULL.
+ * Limits: 0 <= L_min <= L_max <= G <= 64, B * G <= 16384.
+ * Confidences and Theta are computed in fp64.
+ */
+DSPARK_API dspark_status dspark_schedule_prefix(
+    const float *conf_logits, const float *pos_temp, const float *sps, int sps_len,
+    int B, int G, int L_min, int L_max,
+    float *conf, float *cum_conf, int32_t *verify_len, double *theta_out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Lossless rejection-sampling verification of one block per request.
+ *
+ * Defined by "Les mathematiques derriere l'acceleration : comment le decodage
+ * speculatif masque la latence sans modifier les sorties" (seventnews.com),
+ * section "La garantie de l'echantillonnage par rejet" (accept x with
+ * probability min(1, p(x)/q(x)), stop at the first rejection and resample that
+ * token from the residual distribution), and "DeepSeek发布DSpark"
+ * (learnblockchain.cn), section "DSpark 是什么？" (a bonus token is appended
+ * when the whole block is accepted).
+ *
+ * For request b with L = verify_len[b] (G if verify_len is NULL) and T > 0:
+ *   row j < L of target_logits is the target's logits for draft position j;
+ *   p_j = softmax(target[b][j] / T), q_j = the draft distribution (from the
+ *   draft's logq and lse);
+ *   accept x_j while u(seed, id, j, 0, stream 1) < min(1, p_j(x_j)/q_j(x_j));
+ *   at the first rejection d: y = argmax over {v : p_d(v) > q_d(v)} of
+ *   ln(p_d(v) - q_d(v)) + g(u(seed, id, d, v, stream 2))  (the draft logits
+ *   of row d are recomputed from base_logits, e_in and w_out, or read from
+ *   draft_logits when it is not NULL);
+ *   if all L are accepted: y = argmax_v target[b][L][v] / T +
+ *   g(u(seed, id, L, v, stream 3)).
+ * T = 0: accept while x_j == argmax target[b][j]; y = that argmax at the first
+ * mismatch, else argmax target[b][L].
+ *
+ * target_logits [B][G+1][V] dtype; base_logits, e_in, w_out as for
+ * dspark_draft_sample (may be NULL when draft_logits is given);
+ * draft_logits [B][G][V] fp32 or NULL; anchor [B]; draft_tokens, draft_lse,
+ * draft_logq [B][G] from dspark_draft_sample; verify_len [B] or NULL;
+ * temperature [B]; request_id [B] or NULL.
+ * Outputs: accept_len [B] int32; out_tokens [B][G+1] int32 = accepted draft
+ * tokens then the resampled or bonus token, padded with -1; num_out [B] =
+ * accept_len + 1; target_lse [B][G+1] fp32 or NULL (lse of rows j < L at
+ * T > 0, max of the row at T = 0; NaN where not computed); logp_sel [B][G]
+ * fp32 or NULL (log p_j(x_j) of the tested rows, NaN elsewhere).
+ */
+DSPARK_API dspark_status dspark_verify(
+    const void *target_logits, const void *base_logits, const void *e_in, const void *w_out,
+    const float *draft_logits,
+    const int32_t *anchor, const int32_t *draft_tokens, const float *draft_lse,
+    const float *draft_logq, const int32_t *verify_len,
+    const float *temperature, const uint32_t *request_id,
+    int B, int G, int V, int r, dspark_dtype dtype, uint64_t seed,
+    int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
+    float *target_lse, float *logp_sel,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Copy the device flag word of a workspace to *flags (waits for `stream`).
+ * Returns DSPARK_OK or DSPARK_ERR_CUDA. */
+DSPARK_API dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

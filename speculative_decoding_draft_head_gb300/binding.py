@@ -1,0 +1,261 @@
+"""Thin ctypes binding of libdspark (argument marshalling only).
+
+Every function checks shapes, dtypes, devices and contiguity of torch tensors,
+allocates missing outputs and workspaces with torch, and calls the C entry
+point of the same name on the current CUDA stream.  No step of the method runs
+in Python.  If the library cannot be loaded the functions raise: there is no
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+DSPARK_OK = 0
+DSPARK_BF16 = 0
+DSPARK_F32 = 1
+WS_DRAFT, WS_SCHEDULE, WS_VERIFY = 0, 1, 2
+
+FLAG_BAD_TOKEN = 1
+FLAG_BAD_TEMPERATURE = 2
+FLAG_BAD_VERIFY_LEN = 4
+FLAG_BAD_POS_TEMP = 8
+
+EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
+           "dspark_schedule_prefix", "dspark_verify", "dspark_read_device_flags")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("dspark status %d: %s" % (status, message))
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libdspark.so (building it first when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            _build.build_library()
+        if not os.path.exists(path):
+            raise RuntimeError("libdspark.so not built: run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        vp, i32, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+        L.dspark_version.restype = ctypes.c_int
+        L.dspark_version.argtypes = []
+        L.dspark_last_error.restype = ctypes.c_char_p
+        L.dspark_last_error.argtypes = []
+        L.dspark_workspace_bytes.restype = sz
+        L.dspark_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        L.dspark_draft_sample.restype = ctypes.c_int
+        L.dspark_draft_sample.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, u64,
+                                          vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_schedule_prefix.restype = ctypes.c_int
+        L.dspark_schedule_prefix.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                             vp, sz, vp]
+        L.dspark_verify.restype = ctypes.c_int
+        L.dspark_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                    i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_read_device_flags.restype = ctypes.c_int
+        L.dspark_read_device_flags.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        _lib = L
+        return L
+
+
+def _check(status):
+    if status != DSPARK_OK:
+        raise DSparkError(status, load().dspark_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return DSPARK_BF16
+    if t.dtype == torch.float32:
+        return DSPARK_F32
+    raise TypeError("logits must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _need(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        raise ValueError("%s is required" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def _rid(request_id, B, device):
+    if request_id is None:
+        return None
+    rid = request_id
+    if rid.dtype not in (torch.int32,):
+        raise TypeError("request_id must be int32 storage of uint32 ids")
+    return _need(rid, "request_id", shape=(B,), device=device)
+
+
+def version() -> int:
+    return int(load().dspark_version())
+
+
+def workspace_bytes(which: int, B: int, G: int, V: int, r: int) -> int:
+    return int(load().dspark_workspace_bytes(which, B, G, V, r))
+
+
+class WorkspaceCache:
+    """Device scratch buffers reused across calls of the same shape."""
+
+    def __init__(self):
+        self._bufs = {}
+
+    def get(self, which, B, G, V, r, device):
+        n = workspace_bytes(which, B, G, V, r)
+        if n == 0:
+            raise ValueError("invalid sizes for a workspace")
+        key = (which, device)
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < n:
+            buf = torch.empty(n + 256, dtype=torch.uint8, device=device)
+            self._bufs[key] = buf
+        off = (-buf.data_ptr()) % 256
+        return buf[off:off + n]
+
+
+_default_ws = WorkspaceCache()
+
+
+def draft_sample(base, e_in, w_out, anchor, temperature, request_id=None, seed=0, *,
+                 out=None, store_logits=False, workspace=None, stream=None):
+    """Draft one block per request.  Returns dict(tokens, lse, logq[, logits])."""
+    lib = load()
+    B, G, V = base.shape
+    r = e_in.shape[1]
+    dev = base.device
+    _need(base, "base", shape=(B, G, V), device=dev)
+    _need(e_in, "e_in", dtype=base.dtype, shape=(V, r), device=dev)
+    _need(w_out, "w_out", dtype=base.dtype, shape=(r, V), device=dev)
+    _need(anchor, "anchor", dtype=torch.int32, shape=(B,), device=dev)
+    _need(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
+    rid = _rid(request_id, B, dev)
+    if out is None:
+        out = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
+                   lse=torch.empty((B, G), dtype=torch.float32, device=dev),
+                   logq=torch.empty((B, G), dtype=torch.float32, device=dev))
+        if store_logits:
+            out["logits"] = torch.empty((B, G, V), dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else _default_ws.get(WS_DRAFT, B, G, V, r, dev)
+    _check(lib.dspark_draft_sample(
+        _ptr(base), _ptr(e_in), _ptr(w_out), _ptr(anchor), _ptr(temperature), _ptr(rid),
+        B, G, V, r, _dtype_code(base), int(seed) & 0xFFFFFFFFFFFFFFFF,
+        _ptr(out["tokens"]), _ptr(out["lse"]), _ptr(out["logq"]), _ptr(out.get("logits")),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def schedule_prefix(conf_logits, pos_temp, sps, L_min, L_max, *, out=None, workspace=None,
+                    stream=None):
+    """Calibrate confidences and choose verify lengths.
+
+    Returns dict(conf, cum_conf, verify_len, theta)."""
+    lib = load()
+    B, G = conf_logits.shape
+    dev = conf_logits.device
+    _need(conf_logits, "conf_logits", dtype=torch.float32, device=dev)
+    _need(pos_temp, "pos_temp", dtype=torch.float32, shape=(G,), device=dev)
+    _need(sps, "sps", dtype=torch.float32, device=dev)
+    if out is None:
+        out = dict(conf=torch.empty((B, G), dtype=torch.float32, device=dev),
+                   cum_conf=torch.empty((B, G), dtype=torch.float32, device=dev),
+                   verify_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                   theta=torch.empty((1,), dtype=torch.float64, device=dev))
+    ws = workspace if workspace is not None else _default_ws.get(WS_SCHEDULE, B, G, 8, 1, dev)
+    _check(lib.dspark_schedule_prefix(
+        _ptr(conf_logits), _ptr(pos_temp), _ptr(sps), sps.numel(), B, G, int(L_min), int(L_max),
+        _ptr(out["conf"]), _ptr(out["cum_conf"]), _ptr(out["verify_len"]), _ptr(out.get("theta")),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, request_id=None,
+           seed=0, *, draft_logits=None, out=None, workspace=None, stream=None):
+    """Verify one drafted block per request.
+
+    ``draft`` is the dict returned by :func:`draft_sample`.  Returns
+    dict(accept_len, out_tokens, num_out, target_lse, logp)."""
+    lib = load()
+    B, G1, V = target.shape
+    G = G1 - 1
+    dev = target.device
+    _need(target, "target", device=dev)
+    if draft_logits is None:
+        _need(base, "base", dtype=target.dtype, shape=(B, G, V), device=dev)
+        _need(e_in, "e_in", dtype=target.dtype, device=dev)
+        _need(w_out, "w_out", dtype=target.dtype, device=dev)
+        r = e_in.shape[1]
+    else:
+        _need(draft_logits, "draft_logits", dtype=torch.float32, shape=(B, G, V), device=dev)
+        r = e_in.shape[1] if e_in is not None else 16
+    _need(anchor, "anchor", dtype=torch.int32, shape=(B,), device=dev)
+    for k in ("tokens", "lse", "logq"):
+        _need(draft[k], "draft." + k, shape=(B, G), device=dev)
+    if verify_len is not None:
+        _need(verify_len, "verify_len", dtype=torch.int32, shape=(B,), device=dev)
+    _need(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
+    rid = _rid(request_id, B, dev)
+    if out is None:
+        out = dict(accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
+                   num_out=torch.empty((B,), dtype=torch.int32, device=dev),
+                   target_lse=torch.empty((B, G + 1), dtype=torch.float32, device=dev),
+                   logp=torch.empty((B, G), dtype=torch.float32, device=dev))
+    ws = workspace if workspace is not None else _default_ws.get(WS_VERIFY, B, G, V, r, dev)
+    _check(lib.dspark_verify(
+        _ptr(target), _ptr(base), _ptr(e_in), _ptr(w_out), _ptr(draft_logits), _ptr(anchor),
+        _ptr(draft["tokens"]), _ptr(draft["lse"]), _ptr(draft["logq"]), _ptr(verify_len),
+        _ptr(temperature), _ptr(rid), B, G, V, r, _dtype_code(target),
+        int(seed) & 0xFFFFFFFFFFFFFFFF,
+        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["num_out"]),
+        _ptr(out.get("target_lse")), _ptr(out.get("logp")), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def read_device_flags(workspace, stream=None) -> int:
+    val = ctypes.c_uint32(0)
+    _check(load().dspark_read_device_flags(_ptr(workspace), _stream(stream), ctypes.byref(val)))
+    return int(val.value)
+
+
+def default_workspace(which, B, G, V, r, device):
+    return _default_ws.get(which, B, G, V, r, device)

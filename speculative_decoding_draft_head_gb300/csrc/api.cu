@@ -1,0 +1,165 @@
+// extern "C" entry points of libdspark: argument checks, workspace planning
+// and the launch sequence of each step.  Nothing here computes on the host.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+
+namespace dspark {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+dspark_status fail(dspark_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+dspark_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(DSPARK_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+dspark_status check_common(int B, int G, int V, int r, dspark_dtype dt) {
+    if (B < 1) return fail(DSPARK_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
+    if (G < 1 || G > kMaxG) return fail(DSPARK_ERR_INVALID_ARG, "G must be in [1, %d] (got %d)", kMaxG, G);
+    if (V < 8 || V % 8 != 0) return fail(DSPARK_ERR_INVALID_ARG, "V must be a positive multiple of 8 (got %d)", V);
+    if (dt != DSPARK_BF16 && dt != DSPARK_F32) return fail(DSPARK_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+    if (r < 1 || r > 256) return fail(DSPARK_ERR_INVALID_ARG, "r must be in [1, 256] (got %d)", r);
+    if (dt == DSPARK_BF16 && r % 16 != 0) return fail(DSPARK_ERR_INVALID_ARG, "bf16 needs r %% 16 == 0 (got %d)", r);
+    if ((long)B * G * (long)V > (1L << 40)) return fail(DSPARK_ERR_INVALID_ARG, "B*G*V too large");
+    return DSPARK_OK;
+}
+
+dspark_status check_ws(void *ws, size_t have, size_t need) {
+    if (!ws) return fail(DSPARK_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(DSPARK_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (have < need) return fail(DSPARK_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", have, need);
+    return DSPARK_OK;
+}
+
+}  // namespace
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" {
+
+int dspark_version(void) { return 100; }
+
+const char *dspark_last_error(void) { return g_last_error; }
+
+size_t dspark_workspace_bytes(int which, int B, int G, int V, int r) {
+    if (B < 1 || G < 1 || G > kMaxG || V < 8 || V % 8 != 0 || r < 1 || r > 256) return 0;
+    switch (which) {
+        case DSPARK_WS_DRAFT: return plan_draft(B, G, V, r, DSPARK_BF16).ws_bytes > plan_draft(B, G, V, r, DSPARK_F32).ws_bytes
+                                         ? plan_draft(B, G, V, r, DSPARK_BF16).ws_bytes
+                                         : plan_draft(B, G, V, r, DSPARK_F32).ws_bytes;
+        case DSPARK_WS_SCHEDULE: return kFlagBytes;
+        case DSPARK_WS_VERIFY: return plan_verify(B, G, V, r).ws_bytes;
+        default: return 0;
+    }
+}
+
+dspark_status dspark_draft_sample(const void *base_logits, const void *e_in, const void *w_out,
+                                  const int32_t *anchor, const float *temperature,
+                                  const uint32_t *request_id, int B, int G, int V, int r,
+                                  dspark_dtype dtype, uint64_t seed, int32_t *draft_tokens,
+                                  float *draft_lse, float *draft_logq, float *draft_logits,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    dspark_status st = check_common(B, G, V, r, dtype);
+    if (st != DSPARK_OK) return st;
+    if (!base_logits || !e_in || !w_out || !anchor || !temperature || !draft_tokens || !draft_lse || !draft_logq)
+        return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned(base_logits, 16) || !aligned(e_in, 16) || !aligned(w_out, 16) ||
+        (draft_logits && !aligned(draft_logits, 16)))
+        return fail(DSPARK_ERR_INVALID_ARG, "logits and weights must be 16-byte aligned");
+    const DraftPlan plan = plan_draft(B, G, V, r, dtype);
+    if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    DraftArgs a{base_logits, e_in, w_out, anchor, temperature, request_id, B, G, V, r, dtype, seed,
+                draft_tokens, draft_lse, draft_logq, draft_logits, static_cast<unsigned char *>(workspace)};
+    for (int j = 0; j < G; ++j) {
+        e = plan.tensor_path ? launch_draft_tensor(a, plan, j, s) : launch_draft_simt(a, plan, j, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft sample launch");
+        e = launch_draft_finalize(a, plan, j, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
+    }
+    return DSPARK_OK;
+}
+
+dspark_status dspark_schedule_prefix(const float *conf_logits, const float *pos_temp, const float *sps,
+                                     int sps_len, int B, int G, int L_min, int L_max, float *conf,
+                                     float *cum_conf, int32_t *verify_len, double *theta_out,
+                                     void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 1 || G < 1 || G > kMaxG) return fail(DSPARK_ERR_INVALID_ARG, "bad B=%d or G=%d", B, G);
+    if (L_min < 0 || L_min > L_max || L_max > G)
+        return fail(DSPARK_ERR_INVALID_ARG, "need 0 <= L_min <= L_max <= G (got %d, %d, %d)", L_min, L_max, G);
+    if ((long)B * G > kScheduleMaxCells) return fail(DSPARK_ERR_UNSUPPORTED, "B*G > %d", kScheduleMaxCells);
+    if ((long)sps_len < (long)B * (L_max + 1) + 1)
+        return fail(DSPARK_ERR_INVALID_ARG, "sps_len must be >= B*(L_max+1)+1 = %ld", (long)B * (L_max + 1) + 1);
+    if (!conf_logits || !pos_temp || !sps || !conf || !cum_conf || !verify_len)
+        return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (schedule_smem_bytes(B, G, L_min, L_max) > 200 * 1024)
+        return fail(DSPARK_ERR_UNSUPPORTED, "too many scheduler candidates");
+    dspark_status st = check_ws(workspace, workspace_bytes, kFlagBytes);
+    if (st != DSPARK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    ScheduleArgs a{conf_logits, pos_temp, sps, sps_len, B, G, L_min, L_max, conf, cum_conf, verify_len,
+                   theta_out, static_cast<unsigned char *>(workspace)};
+    e = launch_schedule(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+    return DSPARK_OK;
+}
+
+dspark_status dspark_verify(const void *target_logits, const void *base_logits, const void *e_in,
+                            const void *w_out, const float *draft_logits, const int32_t *anchor,
+                            const int32_t *draft_tokens, const float *draft_lse, const float *draft_logq,
+                            const int32_t *verify_len, const float *temperature,
+                            const uint32_t *request_id, int B, int G, int V, int r, dspark_dtype dtype,
+                            uint64_t seed, int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
+                            float *target_lse, float *logp_sel, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    dspark_status st = check_common(B, G, V, r, dtype);
+    if (st != DSPARK_OK) return st;
+    if (!target_logits || !anchor || !draft_tokens || !draft_lse || !draft_logq || !temperature ||
+        !accept_len || !out_tokens || !num_out)
+        return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!draft_logits && (!base_logits || !e_in || !w_out))
+        return fail(DSPARK_ERR_INVALID_ARG, "need draft_logits or (base_logits, e_in, w_out)");
+    if (!aligned(target_logits, 16) || (base_logits && !aligned(base_logits, 16)) ||
+        (e_in && !aligned(e_in, 16)) || (w_out && !aligned(w_out, 16)) ||
+        (draft_logits && !aligned(draft_logits, 16)))
+        return fail(DSPARK_ERR_INVALID_ARG, "logits and weights must be 16-byte aligned");
+    const VerifyPlan plan = plan_verify(B, G, V, r);
+    if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    VerifyArgs a{target_logits, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens, draft_lse,
+                 draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype, seed, accept_len,
+                 out_tokens, num_out, target_lse, logp_sel, static_cast<unsigned char *>(workspace)};
+    e = launch_verify(a, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+    return DSPARK_OK;
+}
+
+dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags) {
+    if (!workspace || !flags) return fail(DSPARK_ERR_INVALID_ARG, "NULL workspace or flags");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the flag word");
+    return DSPARK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,212 @@
+// Draft sampling, SIMT form (fp32 weights, and any dtype when the tensor-core
+// kernel does not apply), plus the split-vocabulary merge shared by both forms.
+//
+// Method: "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
+// "Un po' di autoregressione basta", equation for p_k: position j draws from
+// softmax((U_j + E_in[x_{j-1}] W_out) / T); the drawn token feeds position j+1.
+//
+// One launch per block position.  A block owns `rows_per_block` requests and
+// one vocabulary segment: it gathers the E_in rows of the previous tokens into
+// shared memory, forms the rank-r bias with register-tiled FMAs (4 vocabulary
+// entries x rows_per_block requests per thread), adds the base logits and
+// streams every logit once through the online softmax and the Gumbel-max
+// argmax.  The per-(request, segment) partial states are merged by
+// draft_finalize, which writes the token the next position reads.
+#include <climits>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kSimtThreads = 256;
+constexpr int kSimtRows = 8;
+
+template <typename TIn>
+__global__ void __launch_bounds__(kSimtThreads)
+draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
+                  const TIn *__restrict__ w_out, const int32_t *__restrict__ anchor,
+                  const int32_t *__restrict__ tokens, const float *__restrict__ temperature,
+                  const uint32_t *__restrict__ request_id, int B, int G, int V, int r, int j,
+                  uint32_t k0, uint32_t k1, int chunk, int nsplit, RowState *__restrict__ part,
+                  uint32_t *__restrict__ flags, float *__restrict__ z_out) {
+    extern __shared__ float a_rows[];  // [kSimtRows][r]
+    __shared__ int prev_s[kSimtRows];
+    __shared__ float inv_t_s[kSimtRows];
+    __shared__ uint32_t rid_s[kSimtRows];
+    __shared__ RowState scratch[kSimtThreads / 32];
+
+    const int b0 = blockIdx.y * kSimtRows;
+    const int seg = blockIdx.x;
+    if (threadIdx.x < kSimtRows) {
+        const int b = b0 + threadIdx.x;
+        int prev = -1;
+        float inv_t = 0.f;
+        uint32_t id = 0;
+        if (b < B) {
+            prev = (j == 0) ? anchor[b] : tokens[(size_t)b * G + j - 1];
+            const float T = temperature[b];
+            id = request_id ? request_id[b] : (uint32_t)b;
+            const bool bad_prev = prev < 0 || prev >= V;
+            // an earlier position already flagged this request and wrote -1
+            if (bad_prev && (j == 0 || prev != -1) && seg == 0) atomicOr(flags, kFlagBadToken);
+            if (!(T >= 0.f) || isinf(T)) {
+                if (seg == 0 && j == 0) atomicOr(flags, kFlagBadTemperature);
+                prev = -1;
+            }
+            if (bad_prev) prev = -1;
+            inv_t = (T > 0.f) ? 1.0f / T : 0.f;
+        }
+        prev_s[threadIdx.x] = prev;
+        inv_t_s[threadIdx.x] = inv_t;
+        rid_s[threadIdx.x] = id;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kSimtRows * r; i += blockDim.x) {
+        const int rb = i / r, k = i - rb * r;
+        const int prev = prev_s[rb];
+        a_rows[i] = prev >= 0 ? to_f32(e_in[(size_t)prev * r + k]) : 0.f;
+    }
+    __syncthreads();
+
+    RowState st[kSimtRows];
+#pragma unroll
+    for (int rb = 0; rb < kSimtRows; ++rb) st[rb] = row_state_init();
+
+    const int vb = seg * chunk;
+    const int ve = min(V, vb + chunk);
+    for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kSimtThreads) {
+        float acc[kSimtRows][4];
+#pragma unroll
+        for (int rb = 0; rb < kSimtRows; ++rb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[rb][e] = 0.f;
+        for (int k = 0; k < r; ++k) {
+            const float4 w = load4(w_out + (size_t)k * V + v);
+#pragma unroll
+            for (int rb = 0; rb < kSimtRows; ++rb) {
+                const float a = a_rows[rb * r + k];
+                acc[rb][0] = fmaf(a, w.x, acc[rb][0]);
+                acc[rb][1] = fmaf(a, w.y, acc[rb][1]);
+                acc[rb][2] = fmaf(a, w.z, acc[rb][2]);
+                acc[rb][3] = fmaf(a, w.w, acc[rb][3]);
+            }
+        }
+#pragma unroll
+        for (int rb = 0; rb < kSimtRows; ++rb) {
+            const int b = b0 + rb;
+            if (b >= B || prev_s[rb] < 0) continue;
+            const size_t row = (size_t)b * G + j;
+            const float4 u4 = load4(base + row * V + v);
+            const float inv_t = inv_t_s[rb];
+            float z[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[rb][e];
+            if (z_out) *reinterpret_cast<float4 *>(z_out + row * V + v) = make_float4(z[0], z[1], z[2], z[3]);
+            if (inv_t > 0.f) {
+                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, rid_s[rb], kStreamDraft), k0, k1);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float s = z[e] * inv_t;
+                    softmax_push(st[rb], s);
+                    gumbel_push(st[rb], s, word_of(w4, e), v + e);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) argmax_push(st[rb], z[e], v + e);
+            }
+        }
+    }
+#pragma unroll
+    for (int rb = 0; rb < kSimtRows; ++rb) {
+        RowState m = block_merge(st[rb], scratch);
+        const int b = b0 + rb;
+        if (threadIdx.x == 0 && b < B) part[(size_t)b * nsplit + seg] = m;
+    }
+}
+
+// One warp per request: merge the segment partials, write token, lse, logq.
+__global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsplit,
+                                      const float *__restrict__ temperature, int B, int G, int j,
+                                      int32_t *__restrict__ tokens, float *__restrict__ lse,
+                                      float *__restrict__ logq) {
+    const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (b >= B) return;
+    RowState s = row_state_init();
+    for (int i = lane; i < nsplit; i += 32) row_state_merge(s, part[(size_t)b * nsplit + i]);
+    s = warp_merge(s);
+    if (lane != 0) return;
+    const size_t o = (size_t)b * G + j;
+    const float T = temperature[b];
+    if (s.idx == INT32_MAX) {  // request flagged invalid
+        tokens[o] = -1;
+        lse[o] = __int_as_float(0x7fc00000);
+        logq[o] = __int_as_float(0x7fc00000);
+        return;
+    }
+    tokens[o] = s.idx;
+    if (T > 0.f) {
+        const float l = s.m + logf(s.S);
+        lse[o] = l;
+        logq[o] = s.s_at - l;
+    } else {
+        lse[o] = s.key;
+        logq[o] = 0.f;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s) {
+    const dim3 grid(p.nsplit, p.row_blocks);
+    const size_t smem = sizeof(float) * kSimtRows * (size_t)a.r;
+    uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
+    RowState *part = reinterpret_cast<RowState *>(a.ws + p.partial_offset);
+    const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
+    if (a.dt == DSPARK_BF16) {
+        draft_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, smem, s>>>(
+            (const __nv_bfloat16 *)a.base, (const __nv_bfloat16 *)a.e_in, (const __nv_bfloat16 *)a.w_out,
+            a.anchor, a.tokens, a.temperature, a.request_id, a.B, a.G, a.V, a.r, j, k0, k1, p.chunk,
+            p.nsplit, part, flags, a.z_out);
+    } else {
+        draft_simt_kernel<float><<<grid, kSimtThreads, smem, s>>>(
+            (const float *)a.base, (const float *)a.e_in, (const float *)a.w_out, a.anchor, a.tokens,
+            a.temperature, a.request_id, a.B, a.G, a.V, a.r, j, k0, k1, p.chunk, p.nsplit, part, flags,
+            a.z_out);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s) {
+    const RowState *part = reinterpret_cast<const RowState *>(a.ws + p.partial_offset);
+    const int warps = 4;
+    draft_finalize_kernel<<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
+        part, p.nsplit, a.temperature, a.B, a.G, j, a.tokens, a.lse, a.logq);
+    return cudaGetLastError();
+}
+
+DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
+    DraftPlan p{};
+    (void)G;
+    (void)r;
+    (void)dt;
+    p.tensor_path = false;
+    p.rows_per_block = kSimtRows;
+    p.row_blocks = (B + kSimtRows - 1) / kSimtRows;
+    const int want_blocks = 2 * kNumSMs;
+    int nsplit = (want_blocks + p.row_blocks - 1) / p.row_blocks;
+    const int max_split = (V + 1023) / 1024;
+    if (nsplit > max_split) nsplit = max_split;
+    if (nsplit < 1) nsplit = 1;
+    int chunk = (V + nsplit - 1) / nsplit;
+    chunk = (chunk + 3) / 4 * 4;
+    p.nsplit = (V + chunk - 1) / chunk;
+    p.chunk = chunk;
+    p.partial_offset = kFlagBytes;
+    p.ws_bytes = align_up(p.partial_offset + sizeof(RowState) * (size_t)B * p.nsplit, 256);
+    return p;
+}
+
+}  // namespace dspark

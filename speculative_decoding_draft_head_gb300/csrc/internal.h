@@ -1,0 +1,106 @@
+// Host-side declarations shared by the entry points and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr int kNumSMs = 152;            // GB300: 2 dies x 76 SMs
+constexpr size_t kFlagBytes = 256;      // flag word region at the head of every workspace
+constexpr int kMaxG = 64;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- draft ----
+struct DraftPlan {
+    bool tensor_path;      // tcgen05 Markov-head kernel (bf16) vs SIMT kernel
+    int rows_per_block;    // SIMT: requests per block
+    int row_blocks;        // SIMT: ceil(B / rows_per_block); tensor path: M tiles
+    int nsplit;            // vocabulary segments per row (partials per row)
+    int chunk;             // vocabulary entries per segment (multiple of 4)
+    size_t partial_offset; // byte offset of the per-(row, segment) partials
+    size_t ws_bytes;
+};
+DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt);
+
+struct DraftArgs {
+    const void *base;
+    const void *e_in;
+    const void *w_out;
+    const int32_t *anchor;
+    const float *temperature;
+    const uint32_t *request_id;
+    int B, G, V, r;
+    dspark_dtype dt;
+    uint64_t seed;
+    int32_t *tokens;
+    float *lse;
+    float *logq;
+    float *z_out;
+    unsigned char *ws;
+};
+cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
+cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
+cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
+
+// --------------------------------------------------------------- verify ----
+struct VerifyPlan {
+    int row_split;          // segments per target row in the row pass
+    int row_chunk;
+    int res_split;          // segments per residual row
+    int res_chunk;
+    size_t row_part_offset; // [B][G+1][row_split] RowState
+    size_t res_row_offset;  // [B] int32: rejected position or -1
+    size_t lse_t_offset;    // [B] fp32: target lse of the rejected row
+    size_t res_part_offset; // [B][res_split] ResidualState
+    size_t ws_bytes;
+};
+VerifyPlan plan_verify(int B, int G, int V, int r);
+
+struct VerifyArgs {
+    const void *target;
+    const void *base;
+    const void *e_in;
+    const void *w_out;
+    const float *z_in;
+    const int32_t *anchor;
+    const int32_t *draft_tokens;
+    const float *draft_lse;
+    const float *draft_logq;
+    const int32_t *verify_len;
+    const float *temperature;
+    const uint32_t *request_id;
+    int B, G, V, r;
+    dspark_dtype dt;
+    uint64_t seed;
+    int32_t *accept_len;
+    int32_t *out_tokens;
+    int32_t *num_out;
+    float *target_lse;
+    float *logp_sel;
+    unsigned char *ws;
+};
+cudaError_t launch_verify(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s);
+
+// ------------------------------------------------------------- schedule ----
+struct ScheduleArgs {
+    const float *conf_logits;
+    const float *pos_temp;
+    const float *sps;
+    int sps_len;
+    int B, G, L_min, L_max;
+    float *conf;
+    float *cum_conf;
+    int32_t *verify_len;
+    double *theta_out;
+    unsigned char *ws;
+};
+constexpr int kScheduleMaxCells = 16384;  // B * G
+size_t schedule_smem_bytes(int B, int G, int L_min, int L_max);
+cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s);
+
+}  // namespace dspark

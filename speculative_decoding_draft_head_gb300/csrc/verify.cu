@@ -1,0 +1,402 @@
+// Rejection-sampling verification of one drafted block per request.
+//
+// Method: "Les mathematiques derriere l'acceleration" (seventnews.com),
+// section "La garantie de l'echantillonnage par rejet": accept x with
+// probability min(1, p(x)/q(x)), stop at the first rejection and draw that
+// position again from the residual distribution; "DeepSeek发布DSpark"
+// (learnblockchain.cn), section "DSpark 是什么？": a bonus token from the target
+// follows a fully accepted block.  The residual is normalise(max(0, p - q)).
+//
+// Four launches:
+//  1. verify_rows     grid (segments, B*(G+1)): streams the target rows j <= L
+//                     of every request once with 128-bit loads -- online
+//                     softmax of t/T for rows j < L, the bonus Gumbel-max for
+//                     row L, the argmax for greedy requests.
+//  2. verify_decide   one warp per request: merges the row partials, runs the
+//                     sequential acceptance scan, writes the emitted tokens and
+//                     marks the rejected row, if any.
+//  3. verify_residual grid (segments, B): for rejected requests only, rebuilds
+//                     the draft logits of the rejected row (base + Markov
+//                     bias, or the stored draft logits) and draws from
+//                     max(0, p - q) by Gumbel-max.
+//  4. verify_residual_finalize: merges the residual partials into the token.
+#include <climits>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kRowThreads = 256;
+constexpr int kResThreads = 256;
+
+struct ResidualState {
+    float key_res;  // best ln(p - q) + g over entries with p > q
+    int idx_res;
+    float key_p;    // best ln p + g (used only if no entry has p > q)
+    int idx_p;
+};
+
+__device__ __forceinline__ ResidualState residual_init() {
+    return ResidualState{-INFINITY, INT32_MAX, -INFINITY, INT32_MAX};
+}
+
+__device__ __forceinline__ void residual_merge(ResidualState &a, const ResidualState &b) {
+    if (key_better(b.key_res, b.idx_res, a.key_res, a.idx_res)) {
+        a.key_res = b.key_res;
+        a.idx_res = b.idx_res;
+    }
+    if (key_better(b.key_p, b.idx_p, a.key_p, a.idx_p)) {
+        a.key_p = b.key_p;
+        a.idx_p = b.idx_p;
+    }
+}
+
+__device__ __forceinline__ ResidualState residual_warp_merge(ResidualState s) {
+#pragma unroll
+    for (int mask = 16; mask > 0; mask >>= 1) {
+        ResidualState o;
+        o.key_res = __shfl_xor_sync(0xffffffffu, s.key_res, mask);
+        o.idx_res = __shfl_xor_sync(0xffffffffu, s.idx_res, mask);
+        o.key_p = __shfl_xor_sync(0xffffffffu, s.key_p, mask);
+        o.idx_p = __shfl_xor_sync(0xffffffffu, s.idx_p, mask);
+        residual_merge(s, o);
+    }
+    return s;
+}
+
+__device__ __forceinline__ int read_verify_len(const int32_t *verify_len, int b, int G) {
+    const int L = verify_len ? verify_len[b] : G;
+    return (L < 0 || L > G) ? -1 : L;
+}
+
+__device__ __forceinline__ bool temperature_ok(float T) { return T >= 0.f && !isinf(T); }
+
+// ---------------------------------------------------------------- pass 1 ----
+template <typename TIn>
+__global__ void __launch_bounds__(kRowThreads)
+verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ verify_len,
+                   const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
+                   int B, int G, int V, uint32_t k0, uint32_t k1, int chunk, int nsplit,
+                   RowState *__restrict__ part) {
+    __shared__ RowState scratch[kRowThreads / 32];
+    const int row = blockIdx.y;
+    const int b = row / (G + 1);
+    const int j = row - b * (G + 1);
+    const int L = read_verify_len(verify_len, b, G);
+    const float T = temperature[b];
+    if (L < 0 || j > L || !temperature_ok(T)) return;
+    const float inv_t = T > 0.f ? 1.0f / T : 0.f;
+    const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
+    const int seg = blockIdx.x;
+    const int vb = seg * chunk;
+    const int ve = min(V, vb + chunk);
+    const TIn *t_row = target + ((size_t)b * (G + 1) + j) * V;
+
+    RowState st = row_state_init();
+    if (T > 0.f && j < L) {
+        for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kRowThreads) {
+            const float4 t4 = load4(t_row + v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) softmax_push(st, elem(t4, e) * inv_t);
+        }
+    } else if (T > 0.f) {  // j == L: bonus draw
+        for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kRowThreads) {
+            const float4 t4 = load4(t_row + v);
+            const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, id, kStreamBonus), k0, k1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gumbel_push(st, elem(t4, e) * inv_t, word_of(w4, e), v + e);
+        }
+    } else {  // greedy request
+        for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kRowThreads) {
+            const float4 t4 = load4(t_row + v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) argmax_push(st, elem(t4, e), v + e);
+        }
+    }
+    st = block_merge(st, scratch);
+    if (threadIdx.x == 0) part[(size_t)row * nsplit + seg] = st;
+}
+
+// ---------------------------------------------------------------- pass 2 ----
+template <typename TIn>
+__global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowState *__restrict__ part,
+                                     int nsplit, const int32_t *__restrict__ anchor,
+                                     const int32_t *__restrict__ draft_tokens,
+                                     const float *__restrict__ draft_logq,
+                                     const int32_t *__restrict__ verify_len,
+                                     const float *__restrict__ temperature,
+                                     const uint32_t *__restrict__ request_id, int B, int G, int V,
+                                     uint32_t k0, uint32_t k1, int32_t *__restrict__ accept_len,
+                                     int32_t *__restrict__ out_tokens, int32_t *__restrict__ num_out,
+                                     float *__restrict__ target_lse, float *__restrict__ logp_sel,
+                                     int32_t *__restrict__ res_row, float *__restrict__ lse_t_row,
+                                     uint32_t *__restrict__ flags) {
+    const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (b >= B) return;
+    const float nan = __int_as_float(0x7fc00000);
+    const int L = read_verify_len(verify_len, b, G);
+    const float T = temperature[b];
+    bool bad = false;
+    if (L < 0) {
+        if (lane == 0) atomicOr(flags, kFlagBadVerifyLen);
+        bad = true;
+    }
+    if (!temperature_ok(T)) {
+        if (lane == 0) atomicOr(flags, kFlagBadTemperature);
+        bad = true;
+    }
+    if (!bad) {
+        const int an = anchor[b];
+        if (an < 0 || an >= V) bad = true;
+        for (int j = 0; j < L; ++j) {
+            const int x = draft_tokens[(size_t)b * G + j];
+            if (x < 0 || x >= V) bad = true;
+        }
+        if (bad && lane == 0) atomicOr(flags, kFlagBadToken);
+    }
+    // clear the optional per-row outputs of this request
+    for (int j = lane; j <= G; j += 32) {
+        out_tokens[(size_t)b * (G + 1) + j] = -1;
+        if (target_lse) target_lse[(size_t)b * (G + 1) + j] = nan;
+        if (logp_sel && j < G) logp_sel[(size_t)b * G + j] = nan;
+    }
+    __syncwarp();
+    if (bad) {
+        if (lane == 0) {
+            accept_len[b] = -1;
+            num_out[b] = 0;
+            res_row[b] = -1;
+        }
+        return;
+    }
+    const float inv_t = T > 0.f ? 1.0f / T : 0.f;
+    const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
+    int k = 0, y = -1, d = -1;
+    for (int j = 0; j < L; ++j) {
+        RowState s = row_state_init();
+        const RowState *pr = part + ((size_t)b * (G + 1) + j) * nsplit;
+        for (int i = lane; i < nsplit; i += 32) row_state_merge(s, pr[i]);
+        s = warp_merge(s);
+        const int x = draft_tokens[(size_t)b * G + j];
+        if (T > 0.f) {
+            const float lse_t = s.m + logf(s.S);
+            const float tx = to_f32(target[((size_t)b * (G + 1) + j) * V + x]);
+            const float logp = tx * inv_t - lse_t;
+            const float logq = draft_logq[(size_t)b * G + j];
+            const uint4 w4 = philox4x32_10(make_uint4(0u, (uint32_t)j, id, kStreamAccept), k0, k1);
+            const float u = word_to_uniform(w4.x);
+            const bool accept = u < expf(logp - logq);
+            if (lane == 0) {
+                if (target_lse) target_lse[(size_t)b * (G + 1) + j] = lse_t;
+                if (logp_sel) logp_sel[(size_t)b * G + j] = logp;
+            }
+            if (!accept) {
+                d = j;
+                if (lane == 0) lse_t_row[b] = lse_t;
+                break;
+            }
+        } else {
+            if (lane == 0) {
+                if (target_lse) target_lse[(size_t)b * (G + 1) + j] = s.key;
+                if (logp_sel) logp_sel[(size_t)b * G + j] = (s.idx == x) ? 0.f : -INFINITY;
+            }
+            if (s.idx != x) {
+                y = s.idx;
+                break;
+            }
+        }
+        ++k;
+    }
+    if (d < 0 && y < 0) {  // bonus token from row L
+        RowState s = row_state_init();
+        const RowState *pr = part + ((size_t)b * (G + 1) + L) * nsplit;
+        for (int i = lane; i < nsplit; i += 32) row_state_merge(s, pr[i]);
+        s = warp_merge(s);
+        y = s.idx;
+        if (T == 0.f && lane == 0 && target_lse) target_lse[(size_t)b * (G + 1) + L] = s.key;
+    }
+    for (int j = lane; j < k; j += 32) out_tokens[(size_t)b * (G + 1) + j] = draft_tokens[(size_t)b * G + j];
+    if (lane == 0) {
+        out_tokens[(size_t)b * (G + 1) + k] = (d >= 0) ? -1 : y;
+        accept_len[b] = k;
+        num_out[b] = k + 1;
+        res_row[b] = d;
+    }
+}
+
+// ---------------------------------------------------------------- pass 3 ----
+template <typename TIn>
+__global__ void __launch_bounds__(kResThreads)
+verify_residual_kernel(const TIn *__restrict__ target, const TIn *__restrict__ base,
+                       const TIn *__restrict__ e_in, const TIn *__restrict__ w_out,
+                       const float *__restrict__ z_in, const int32_t *__restrict__ anchor,
+                       const int32_t *__restrict__ draft_tokens, const float *__restrict__ draft_lse,
+                       const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
+                       const int32_t *__restrict__ res_row, const float *__restrict__ lse_t_row,
+                       int B, int G, int V, int r, uint32_t k0, uint32_t k1, int chunk, int nsplit,
+                       ResidualState *__restrict__ part) {
+    extern __shared__ float a_row[];  // [r]
+    __shared__ ResidualState scratch[kResThreads / 32];
+    const int b = blockIdx.y;
+    const int d = res_row[b];
+    if (d < 0) return;
+    const int seg = blockIdx.x;
+    const float inv_t = 1.0f / temperature[b];
+    const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
+    const float lse_q = draft_lse[(size_t)b * G + d];
+    const float lse_t = lse_t_row[b];
+    const int prev = (d == 0) ? anchor[b] : draft_tokens[(size_t)b * G + d - 1];
+    if (!z_in) {
+        for (int k = threadIdx.x; k < r; k += blockDim.x) a_row[k] = to_f32(e_in[(size_t)prev * r + k]);
+        __syncthreads();
+    }
+    const size_t drow = (size_t)b * G + d;
+    const TIn *t_row = target + ((size_t)b * (G + 1) + d) * V;
+    const int vb = seg * chunk;
+    const int ve = min(V, vb + chunk);
+    ResidualState st = residual_init();
+    for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kResThreads) {
+        float z[4];
+        if (z_in) {
+            const float4 z4 = *reinterpret_cast<const float4 *>(z_in + drow * V + v);
+            z[0] = z4.x; z[1] = z4.y; z[2] = z4.z; z[3] = z4.w;
+        } else {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < r; ++k) {
+                const float4 w = load4(w_out + (size_t)k * V + v);
+                const float a = a_row[k];
+                acc[0] = fmaf(a, w.x, acc[0]);
+                acc[1] = fmaf(a, w.y, acc[1]);
+                acc[2] = fmaf(a, w.z, acc[2]);
+                acc[3] = fmaf(a, w.w, acc[3]);
+            }
+            const float4 u4 = load4(base + drow * V + v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[e];
+        }
+        const float4 t4 = load4(t_row + v);
+        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, kStreamResidual), k0, k1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float t = elem(t4, e);
+            const float ln_e = logf(neg_log_uniform(word_of(w4, e)));
+            // log p - log q, formed from the difference of the logits first
+            const float delta = fmaf(t - z[e], inv_t, lse_q - lse_t);
+            if (delta > 0.f) {
+                const float logq = fmaf(z[e], inv_t, -lse_q);
+                const float key = logq + logf(expm1f(delta)) - ln_e;
+                if (key_better(key, v + e, st.key_res, st.idx_res)) {
+                    st.key_res = key;
+                    st.idx_res = v + e;
+                }
+            }
+            const float key_p = t * inv_t - ln_e;
+            if (key_better(key_p, v + e, st.key_p, st.idx_p)) {
+                st.key_p = key_p;
+                st.idx_p = v + e;
+            }
+        }
+    }
+    st = residual_warp_merge(st);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) scratch[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+        st = (lane < kResThreads / 32) ? scratch[lane] : residual_init();
+        st = residual_warp_merge(st);
+        if (lane == 0) part[(size_t)b * nsplit + seg] = st;
+    }
+}
+
+__global__ void verify_residual_finalize_kernel(const ResidualState *__restrict__ part, int nsplit,
+                                                const int32_t *__restrict__ res_row,
+                                                const int32_t *__restrict__ accept_len, int B, int G,
+                                                int32_t *__restrict__ out_tokens) {
+    const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (b >= B) return;
+    const int d = res_row[b];
+    if (d < 0) return;
+    ResidualState s = residual_init();
+    for (int i = lane; i < nsplit; i += 32) residual_merge(s, part[(size_t)b * nsplit + i]);
+    s = residual_warp_merge(s);
+    if (lane == 0) {
+        const int y = (s.idx_res != INT32_MAX) ? s.idx_res : s.idx_p;
+        out_tokens[(size_t)b * (G + 1) + accept_len[b]] = y;
+    }
+}
+
+template <typename TIn>
+cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
+    uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
+    RowState *row_part = reinterpret_cast<RowState *>(a.ws + p.row_part_offset);
+    int32_t *res_row = reinterpret_cast<int32_t *>(a.ws + p.res_row_offset);
+    float *lse_t_row = reinterpret_cast<float *>(a.ws + p.lse_t_offset);
+    ResidualState *res_part = reinterpret_cast<ResidualState *>(a.ws + p.res_part_offset);
+    const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
+    const TIn *target = static_cast<const TIn *>(a.target);
+
+    verify_rows_kernel<TIn><<<dim3(p.row_split, a.B * (a.G + 1)), kRowThreads, 0, s>>>(
+        target, a.verify_len, a.temperature, a.request_id, a.B, a.G, a.V, k0, k1, p.row_chunk,
+        p.row_split, row_part);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int warps = 4;
+    verify_decide_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
+        target, row_part, p.row_split, a.anchor, a.draft_tokens, a.draft_logq, a.verify_len, a.temperature,
+        a.request_id, a.B, a.G, a.V, k0, k1, a.accept_len, a.out_tokens, a.num_out, a.target_lse,
+        a.logp_sel, res_row, lse_t_row, flags);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t smem = a.z_in ? 0 : sizeof(float) * (size_t)a.r;
+    verify_residual_kernel<TIn><<<dim3(p.res_split, a.B), kResThreads, smem, s>>>(
+        target, static_cast<const TIn *>(a.base), static_cast<const TIn *>(a.e_in),
+        static_cast<const TIn *>(a.w_out), a.z_in, a.anchor, a.draft_tokens, a.draft_lse,
+        a.temperature, a.request_id, res_row, lse_t_row, a.B, a.G, a.V, a.r, k0, k1, p.res_chunk,
+        p.res_split, res_part);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    verify_residual_finalize_kernel<<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
+        res_part, p.res_split, res_row, a.accept_len, a.B, a.G, a.out_tokens);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
+    if (a.dt == DSPARK_BF16) return launch_verify_t<__nv_bfloat16>(a, p, s);
+    return launch_verify_t<float>(a, p, s);
+}
+
+VerifyPlan plan_verify(int B, int G, int V, int r) {
+    (void)r;
+    VerifyPlan p{};
+    const long rows = (long)B * (G + 1);
+    // about 4 blocks per SM over the target rows, segments of >= 2048 entries
+    long want = (4L * kNumSMs + rows - 1) / rows;
+    int max_split = (V + 2047) / 2048;
+    int split = (int)(want < 1 ? 1 : (want > max_split ? max_split : want));
+    int chunk = ((V + split - 1) / split + 3) / 4 * 4;
+    p.row_split = (V + chunk - 1) / chunk;
+    p.row_chunk = chunk;
+    long want_r = (2L * kNumSMs + B - 1) / B;
+    int max_r = (V + 1023) / 1024;
+    int rs = (int)(want_r < 1 ? 1 : (want_r > max_r ? max_r : want_r));
+    int rchunk = ((V + rs - 1) / rs + 3) / 4 * 4;
+    p.res_split = (V + rchunk - 1) / rchunk;
+    p.res_chunk = rchunk;
+    size_t off = kFlagBytes;
+    p.row_part_offset = off;
+    off = align_up(off + sizeof(RowState) * (size_t)rows * p.row_split, 256);
+    p.res_row_offset = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)B, 256);
+    p.lse_t_offset = off;
+    off = align_up(off + sizeof(float) * (size_t)B, 256);
+    p.res_part_offset = off;
+    off = align_up(off + sizeof(ResidualState) * (size_t)B * p.res_split, 256);
+    p.ws_bytes = off;
+    return p;
+}
+
+}  // namespace dspark

@@ -1,0 +1,210 @@
+"""Helpers that run the CUDA path and the oracle on the same inputs and compare
+them under the parity contract.
+
+Contract (fp32 device arithmetic against a double-precision oracle):
+  - token ids, accepted lengths and verify lengths are bit-exact, except for a
+    decision the oracle itself places on a near-tie: a Gumbel (or greedy)
+    top-two gap <= TIE_GUMBEL * max(1, |top key|), an acceptance uniform within
+    TIE_ACCEPT of min(1, p/q), or a scheduler step whose Theta change or
+    candidate order is within TIE_THETA (relative).  Such mismatches are
+    counted; everything after a divergence in the same request is skipped.
+  - log-sum-exps and calibrated confidences agree within REL (relative, with
+    a floor of 1 on the scale); log-probabilities within REL absolute (that is,
+    probabilities within REL relative).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from speculative_decoding_draft_head_gb300 import binding
+from speculative_decoding_draft_head_gb300.synth import make_inputs
+
+REL = 1e-5
+TIE_GUMBEL = 1e-5
+TIE_ACCEPT = 1e-6
+TIE_THETA = 1e-6
+
+
+@dataclasses.dataclass
+class Tally:
+    decisions: int = 0
+    exempt: int = 0
+    failures: list = dataclasses.field(default_factory=list)
+
+    def add(self, other: "Tally"):
+        self.decisions += other.decisions
+        self.exempt += other.exempt
+        self.failures += other.failures
+
+    def check(self):
+        assert not self.failures, "\n".join(self.failures[:20])
+
+
+def to_host(d):
+    return {k: (v.detach().cpu() if torch.is_tensor(v) else v) for k, v in d.items()}
+
+
+def gpu_round(inp, w, seed, scheduler=None, store_logits=False):
+    """draft -> schedule (if the workload uses it) -> verify on the GPU."""
+    scheduler = w.scheduler if scheduler is None else scheduler
+    d = binding.draft_sample(inp["base"], inp["e_in"], inp["w_out"], inp["anchor"],
+                             inp["temperature"], inp["request_id"], seed, store_logits=store_logits)
+    sch = None
+    vl = None
+    if scheduler:
+        sch = binding.schedule_prefix(inp["conf_logits"], inp["pos_temp"], inp["sps"], w.L_min, w.G)
+        vl = sch["verify_len"]
+    v = binding.verify(inp["target"], inp["base"], inp["e_in"], inp["w_out"], inp["anchor"], d, vl,
+                       inp["temperature"], inp["request_id"], seed)
+    torch.cuda.synchronize()
+    return dict(draft=to_host(d), sched=None if sch is None else to_host(sch), verify=to_host(v))
+
+
+def oracle_round(hinp, w, seed, reqs=None, verify_len=None, threads=None):
+    """The oracle on the requests ``reqs`` (all when None)."""
+    B = w.B
+    reqs = np.arange(B) if reqs is None else np.asarray(reqs)
+    base = hinp["base"][reqs]
+    target = hinp["target"][reqs]
+    anchor = hinp["anchor"][reqs]
+    temp = hinp["temperature"][reqs]
+    rid = hinp["request_id"].numpy().astype(np.uint32)[reqs]
+    d = oracle.draft_sample_parallel(base, hinp["e_in"], hinp["w_out"], anchor, temp, rid, seed,
+                                     threads=threads)
+    sch = None
+    if w.scheduler and verify_len is None:
+        sch = oracle.schedule(hinp["conf_logits"], hinp["pos_temp"], hinp["sps"], w.L_min, w.G)
+        vl_all = sch["verify_len"]
+    else:
+        vl_all = verify_len
+    vl = None if vl_all is None else np.asarray(vl_all)[reqs]
+    v = oracle.verify_parallel(target, base, hinp["e_in"], hinp["w_out"], anchor, d["tokens"], vl,
+                               temp, rid, seed, threads=threads)
+    return dict(draft=d, sched=sch, verify=v, reqs=reqs)
+
+
+def _close(a, b, scale_floor=1.0, rel=REL):
+    return abs(a - b) <= rel * max(scale_floor, abs(b))
+
+
+def compare_draft(g, o, temps, reqs):
+    """g: GPU draft (host tensors, all B rows); o: oracle draft on ``reqs``."""
+    t = Tally()
+    G = o["tokens"].shape[1]
+    diverged = np.zeros(len(reqs), bool)
+    gt, gl, gq = g["tokens"].numpy(), g["lse"].numpy(), g["logq"].numpy()
+    for i, b in enumerate(reqs):
+        T = float(temps[b])
+        for j in range(G):
+            t.decisions += 1
+            if gt[b, j] != o["tokens"][i, j]:
+                gap, top = o["gap"][i, j], o["top"][i, j]
+                if gap <= TIE_GUMBEL * max(1.0, abs(top)):
+                    t.exempt += 1
+                    diverged[i] = True
+                    break
+                t.failures.append("draft token b=%d j=%d gpu=%d oracle=%d gap=%.3g" %
+                                  (b, j, gt[b, j], o["tokens"][i, j], gap))
+                diverged[i] = True
+                break
+            if not _close(gl[b, j], o["lse"][i, j]):
+                t.failures.append("draft lse b=%d j=%d gpu=%.9g oracle=%.9g" % (b, j, gl[b, j], o["lse"][i, j]))
+            if T > 0 and abs(gq[b, j] - o["logq"][i, j]) > REL:
+                t.failures.append("draft logq b=%d j=%d gpu=%.9g oracle=%.9g" % (b, j, gq[b, j], o["logq"][i, j]))
+            if T == 0 and gq[b, j] != 0.0:
+                t.failures.append("greedy logq b=%d j=%d is %g" % (b, j, gq[b, j]))
+    return t, diverged
+
+
+def compare_schedule(g, o):
+    t = Tally()
+    c, a = g["conf"].numpy(), g["cum_conf"].numpy()
+    if not np.allclose(c, o["conf"], rtol=REL, atol=0):
+        t.failures.append("calibrated confidences differ: max rel %.3g" %
+                          np.max(np.abs(c - o["conf"]) / np.abs(o["conf"])))
+    if not np.allclose(a, o["cum_conf"], rtol=REL, atol=0):
+        t.failures.append("cumulative confidences differ")
+    t.decisions += int(o["n_admitted"]) + 1
+    gl = g["verify_len"].numpy()
+    if not np.array_equal(gl, o["verify_len"]):
+        if min(o["min_margin"], o["min_tie"]) <= TIE_THETA:
+            t.exempt += 1
+        else:
+            t.failures.append("verify lengths differ (%d requests)" % int((gl != o["verify_len"]).sum()))
+    theta = float(g["theta"].numpy()[0])
+    if not _close(theta, o["theta"], rel=1e-9):
+        t.failures.append("theta gpu=%.12g oracle=%.12g" % (theta, o["theta"]))
+    return t
+
+
+def compare_verify(g, o, temps, reqs, skip):
+    """Compare verification outputs of requests whose drafts matched."""
+    t = Tally()
+    ga, go, gn = g["accept_len"].numpy(), g["out_tokens"].numpy(), g["num_out"].numpy()
+    glse, glp = g["target_lse"].numpy(), g["logp"].numpy()
+    for i, b in enumerate(reqs):
+        if skip[i]:
+            continue
+        T = float(temps[b])
+        ka, ko = int(ga[b]), int(o["accept_len"][i])
+        t.decisions += min(ka, ko) + 1
+        if ka != ko:
+            row = min(ka, ko)
+            m = o["accept_margin"][i, row] if T > 0 else np.nan
+            if T > 0 and not np.isnan(m) and m <= TIE_ACCEPT:
+                t.exempt += 1
+            else:
+                t.failures.append("accept_len b=%d gpu=%d oracle=%d margin=%s" % (b, ka, ko, m))
+            continue
+        t.decisions += 1
+        if gn[b] != o["num_out"][i]:
+            t.failures.append("num_out b=%d" % b)
+        if not np.array_equal(go[b, :ka], o["out_tokens"][i, :ko]):
+            t.failures.append("accepted prefix b=%d" % b)
+        if go[b, ka] != o["out_tokens"][i, ko]:
+            gap, top = o["final_gap"][i], o["final_top"][i]
+            if gap <= TIE_GUMBEL * max(1.0, abs(top)):
+                t.exempt += 1
+            else:
+                t.failures.append("final token b=%d gpu=%d oracle=%d kind=%d gap=%.3g" %
+                                  (b, go[b, ka], o["out_tokens"][i, ko], o["final_kind"][i], gap))
+        if np.any(go[b, ka + 1:] != -1):
+            t.failures.append("padding b=%d" % b)
+        for j in range(o["target_lse"].shape[1]):
+            ol = o["target_lse"][i, j]
+            if not np.isnan(ol) and not _close(glse[b, j], ol):
+                t.failures.append("target lse b=%d j=%d gpu=%.9g oracle=%.9g" % (b, j, glse[b, j], ol))
+        for j in range(o["logp"].shape[1]):
+            ol = o["logp"][i, j]
+            if np.isfinite(ol) and abs(glp[b, j] - ol) > REL:
+                t.failures.append("logp b=%d j=%d gpu=%.9g oracle=%.9g" % (b, j, glp[b, j], ol))
+    return t
+
+
+def host_inputs(inp):
+    return {k: v.detach().cpu() for k, v in inp.items()}
+
+
+def full_parity(w, seed, reqs=None, device="cuda", threads=None):
+    """Generate inputs, run both sides, compare everything; returns the Tally."""
+    inp = make_inputs(w, seed, device=device)
+    g = gpu_round(inp, w, seed)
+    h = host_inputs(inp)
+    o = oracle_round(h, w, seed, reqs=reqs, threads=threads)
+    temps = h["temperature"].numpy()
+    tally = Tally()
+    if w.scheduler:
+        tally.add(compare_schedule(g["sched"], o["sched"]))
+    td, diverged = compare_draft(g["draft"], o["draft"], temps, o["reqs"])
+    tally.add(td)
+    skip = diverged.copy()
+    if w.scheduler:
+        gl = g["sched"]["verify_len"].numpy()
+        skip |= gl[o["reqs"]] != o["sched"]["verify_len"][o["reqs"]]
+    tally.add(compare_verify(g["verify"], o["verify"], temps, o["reqs"], skip))
+    return tally, g, o, inp

@@ -1,0 +1,198 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Sizes: the tiny workload in full; every other workload scaled down in B and V
+(the oracle finishes in seconds, the vocabulary still spans several segments
+and a ragged tail); and every workload at full size with the oracle on a
+sample of requests plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_draft_head_gb300 import binding
+from speculative_decoding_draft_head_gb300.synth import WORKLOADS, make_inputs
+
+from parity import (REL, Tally, compare_draft, compare_verify, full_parity, gpu_round, host_inputs,
+                    oracle_round)
+
+pytestmark = pytest.mark.gpu
+
+SCALED = {
+    "tiny": WORKLOADS["tiny"],
+    "qwen3": WORKLOADS["qwen3"].scaled(B=12, V=8200),
+    "dspark5": WORKLOADS["dspark5"].scaled(B=64, V=8200),
+    "largev": WORKLOADS["largev"].scaled(B=16, V=16392),
+    "highconc": WORKLOADS["highconc"].scaled(B=160, V=4104),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    binding.load()
+    oracle.build()
+
+
+@pytest.mark.parametrize("name", list(SCALED))
+def test_scaled_workload_matches_oracle(name):
+    w = SCALED[name]
+    total = Tally()
+    for seed in range(3):
+        tally, g, o, _ = full_parity(w, seed)
+        total.add(tally)
+    total.check()
+    assert total.exempt <= max(1, total.decisions // 1000)
+
+
+def test_tiny_many_seeds():
+    w = SCALED["tiny"]
+    total = Tally()
+    for seed in range(40):
+        tally, *_ = full_parity(w, 1000 + seed)
+        total.add(tally)
+    total.check()
+    assert total.decisions > 600
+
+
+def _properties(w, g, inp):
+    d, v = g["draft"], g["verify"]
+    V, G, B = w.V, w.G, w.B
+    tok = d["tokens"].numpy()
+    assert tok.min() >= 0 and tok.max() < V
+    acc, out, n = v["accept_len"].numpy(), v["out_tokens"].numpy(), v["num_out"].numpy()
+    vl = g["sched"]["verify_len"].numpy() if g["sched"] is not None else np.full(B, G)
+    assert np.all(n == acc + 1) and np.all(acc >= 0) and np.all(acc <= vl)
+    for b in range(B):
+        assert np.array_equal(out[b, :acc[b]], tok[b, :acc[b]])
+        assert 0 <= out[b, acc[b]] < V
+        assert np.all(out[b, acc[b] + 1:] == -1)
+    if g["sched"] is not None:
+        assert vl.min() >= w.L_min and vl.max() <= G
+    lse = d["lse"].numpy()
+    assert np.all(np.isfinite(lse))
+    logq = d["logq"].numpy()
+    assert np.all(logq <= 1e-6)
+
+
+@pytest.mark.parametrize("name", ["qwen3", "dspark5", "largev", "highconc"])
+def test_full_size_sampled_requests(name):
+    w = WORKLOADS[name]
+    rng = np.random.default_rng(5)
+    reqs = np.sort(rng.choice(w.B, size=6, replace=False))
+    if name == "largev":  # both temperature groups
+        reqs = np.array([0, 7, 15, 16, 24, 31])
+    tally, g, o, inp = full_parity(w, 7, reqs=reqs)
+    tally.check()
+    _properties(w, g, inp)
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_verify_alone_on_oracle_drafts():
+    """Feed the oracle's draft to the CUDA verify, compare with the oracle verify."""
+    for name in ("tiny", "dspark5", "largev"):
+        w = SCALED[name]
+        inp = make_inputs(w, 3, device="cuda")
+        h = host_inputs(inp)
+        o = oracle_round(h, w, 3)
+        d = dict(tokens=torch.from_numpy(o["draft"]["tokens"]).cuda(),
+                 lse=torch.from_numpy(o["draft"]["lse"].astype(np.float32)).cuda(),
+                 logq=torch.from_numpy(o["draft"]["logq"].astype(np.float32)).cuda())
+        vl = None
+        if w.scheduler:
+            vl = torch.from_numpy(o["sched"]["verify_len"]).cuda()
+        v = binding.verify(inp["target"], inp["base"], inp["e_in"], inp["w_out"], inp["anchor"], d,
+                           vl, inp["temperature"], inp["request_id"], 3)
+        torch.cuda.synchronize()
+        g = {k: t.cpu() for k, t in v.items()}
+        t = compare_verify(g, o["verify"], h["temperature"].numpy(), np.arange(w.B),
+                           np.zeros(w.B, bool))
+        t.check()
+
+
+def test_stored_draft_logits_match_oracle_and_recompute_path():
+    w = SCALED["dspark5"]
+    inp = make_inputs(w, 4, device="cuda")
+    d = binding.draft_sample(inp["base"], inp["e_in"], inp["w_out"], inp["anchor"], inp["temperature"],
+                             inp["request_id"], 4, store_logits=True)
+    h = host_inputs(inp)
+    o = oracle.draft_sample(h["base"][:4], h["e_in"], h["w_out"], h["anchor"][:4],
+                            h["temperature"][:4], h["request_id"][:4].numpy().astype(np.uint32), 4,
+                            want_z=True)
+    z = d["logits"][:4].cpu().double().numpy()
+    same = (d["tokens"][:4].cpu().numpy() == o["tokens"]).all(axis=1)
+    for b in range(4):
+        if same[b]:
+            np.testing.assert_allclose(z[b], o["z"][b], rtol=REL, atol=REL)
+    v1 = binding.verify(inp["target"], inp["base"], inp["e_in"], inp["w_out"], inp["anchor"], d, None,
+                        inp["temperature"], inp["request_id"], 4)
+    v2 = binding.verify(inp["target"], None, inp["e_in"], None, inp["anchor"], d, None,
+                        inp["temperature"], inp["request_id"], 4, draft_logits=d["logits"])
+    torch.cuda.synchronize()
+    for k in ("accept_len", "out_tokens", "num_out"):
+        assert torch.equal(v1[k], v2[k]), k
+
+
+def test_edge_cases_lengths_and_greedy():
+    w = SCALED["dspark5"].scaled(B=9, G=5, V=1032, scheduler=False)
+    inp = make_inputs(w, 11, device="cuda")
+    h = host_inputs(inp)
+    for vl_np in (np.zeros(w.B, np.int32), np.full(w.B, w.G, np.int32),
+                  np.arange(w.B, dtype=np.int32) % (w.G + 1)):
+        for greedy in (False, True):
+            temp = inp["temperature"].clone()
+            if greedy:
+                temp.zero_()
+            inp2 = dict(inp, temperature=temp)
+            d = binding.draft_sample(inp2["base"], inp2["e_in"], inp2["w_out"], inp2["anchor"], temp,
+                                     inp2["request_id"], 11)
+            vl = torch.from_numpy(vl_np).cuda()
+            v = binding.verify(inp2["target"], inp2["base"], inp2["e_in"], inp2["w_out"], inp2["anchor"],
+                               d, vl, temp, inp2["request_id"], 11)
+            torch.cuda.synchronize()
+            h2 = dict(h, temperature=temp.cpu())
+            o = oracle_round(h2, w, 11, verify_len=vl_np)
+            td, div = compare_draft({k: t.cpu() for k, t in d.items()}, o["draft"], h2["temperature"].numpy(),
+                                    np.arange(w.B))
+            td.check()
+            tv = compare_verify({k: t.cpu() for k, t in v.items()}, o["verify"], h2["temperature"].numpy(),
+                                np.arange(w.B), div)
+            tv.check()
+
+
+def test_minimal_sizes():
+    w = WORKLOADS["tiny"].scaled(B=1, G=1, V=8, r=1)
+    tally, *_ = full_parity(w, 0)
+    tally.check()
+    w2 = WORKLOADS["dspark5"].scaled(B=1, G=1, V=8, r=16, scheduler=False)
+    tally, *_ = full_parity(w2, 0)
+    tally.check()
+
+
+def test_invalid_device_inputs_are_flagged_not_read():
+    w = SCALED["tiny"].scaled(B=4)
+    inp = make_inputs(w, 0, device="cuda")
+    anchor = inp["anchor"].clone()
+    anchor[1] = w.V + 5
+    temp = inp["temperature"].clone()
+    temp[2] = -1.0
+    ws = binding.default_workspace(binding.WS_DRAFT, w.B, w.G, w.V, w.r, anchor.device)
+    d = binding.draft_sample(inp["base"], inp["e_in"], inp["w_out"], anchor, temp, None, 0, workspace=ws)
+    flags = binding.read_device_flags(ws)
+    assert flags & binding.FLAG_BAD_TOKEN and flags & binding.FLAG_BAD_TEMPERATURE
+    tok = d["tokens"].cpu().numpy()
+    assert np.all(tok[1] == -1) and np.all(tok[2] == -1)
+    assert np.all(tok[0] >= 0) and np.all(tok[3] >= 0)
+    vl = torch.tensor([2, 9, 1, 0], dtype=torch.int32, device="cuda")
+    wsv = binding.default_workspace(binding.WS_VERIFY, w.B, w.G, w.V, w.r, anchor.device)
+    v = binding.verify(inp["target"], inp["base"], inp["e_in"], inp["w_out"], anchor, d, vl, temp, None, 0,
+                       workspace=wsv)
+    flags = binding.read_device_flags(wsv)
+    assert flags & binding.FLAG_BAD_VERIFY_LEN
+    acc = v["accept_len"].cpu().numpy()
+    assert acc[1] == -1 and acc[2] == -1 and acc[0] >= 0 and acc[3] == 0
+    cl = inp["conf_logits"]
+    pt = torch.tensor([1.0, 0.0, 1.0, 1.0], device="cuda")
+    wss = binding.default_workspace(binding.WS_SCHEDULE, w.B, w.G, 8, 1, anchor.device)
+    binding.schedule_prefix(cl, pt, inp["sps"], 1, w.G, workspace=wss)
+    assert binding.read_device_flags(wss) & binding.FLAG_BAD_POS_TEMP
