@@ -203,6 +203,41 @@ DSPARK_API dspark_status dspark_verify(
     float *target_lse, float *logp_sel,
     void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * dspark_verify without a workspace argument, for callers that cannot
+ * allocate device memory.  The paper has no counterpart: this is a deployment
+ * convenience of this library.
+ *
+ * Who needs it: runtimes that plan all device memory ahead of time and hand
+ * it out only to tensors, plugins that run inside another framework where
+ * cudaMalloc is not allowed, and foreign-function callers without an
+ * allocator.  Arguments and results are those of dspark_verify; the caller
+ * still owns every input and output buffer.
+ *
+ * Scratch: a fixed DSPARK_NOALLOC_SCRATCH_BYTES array in the library's device
+ * image, held by every GPU that loads the library until the process exits.
+ * Its device address is looked up on the first call on each device (with that
+ * device current): make that first call before any stream capture begins.
+ * Every call shares the array and finds the previous call's contents in it
+ * (the flag word is cleared on each call); calls whose GPU work overlaps
+ * (other streams, unordered host threads) race on it and must be avoided.
+ * Sizes whose verify scratch exceeds the array return DSPARK_ERR_UNSUPPORTED
+ * with a message in dspark_last_error().  No call allocates or frees memory.
+ * The device flag word can be read with dspark_read_device_flags() only
+ * through dspark_verify's own workspace, not for this entry point.
+ */
+#define DSPARK_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+DSPARK_API dspark_status dspark_verify_noalloc(
+    const void *target_logits, const void *base_logits, const void *e_in, const void *w_out,
+    const float *draft_logits,
+    const int32_t *anchor, const int32_t *draft_tokens, const float *draft_lse,
+    const float *draft_logq, const int32_t *verify_len,
+    const float *temperature, const uint32_t *request_id,
+    int B, int G, int V, int r, dspark_dtype dtype, uint64_t seed,
+    int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
+    float *target_lse, float *logp_sel, void *stream);
+
 /* Copy the device flag word of a workspace to *flags (waits for `stream`).
  * Returns DSPARK_OK or DSPARK_ERR_CUDA. */
 DSPARK_API dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags);

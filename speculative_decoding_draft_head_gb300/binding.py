@@ -27,7 +27,8 @@ FLAG_BAD_VERIFY_LEN = 4
 FLAG_BAD_POS_TEMP = 8
 
 EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
-           "dspark_schedule_prefix", "dspark_verify", "dspark_read_device_flags")
+           "dspark_schedule_prefix", "dspark_verify", "dspark_read_device_flags",
+           "dspark_verify_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -71,6 +72,9 @@ def load(build_if_missing: bool = True):
         L.dspark_verify.restype = ctypes.c_int
         L.dspark_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                     i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_verify_noalloc.restype = ctypes.c_int
+        L.dspark_verify_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp]
         L.dspark_read_device_flags.restype = ctypes.c_int
         L.dspark_read_device_flags.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         _lib = L
@@ -248,6 +252,36 @@ def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, re
         _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["num_out"]),
         _ptr(out.get("target_lse")), _ptr(out.get("logp")), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def verify_noalloc(target, base, e_in, w_out, anchor, draft, verify_len, temperature,
+                   request_id=None, seed=0, *, draft_logits=None, out=None, stream=None):
+    """:func:`verify` through ``dspark_verify_noalloc``: no workspace is passed
+    or allocated; the library uses its fixed device scratch array."""
+    lib = load()
+    B, G1, V = target.shape
+    G = G1 - 1
+    dev = target.device
+    _need(target, "target", device=dev)
+    r = e_in.shape[1] if e_in is not None else 16
+    if out is None:
+        out = dict(accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
+                   num_out=torch.empty((B,), dtype=torch.int32, device=dev),
+                   target_lse=torch.empty((B, G + 1), dtype=torch.float32, device=dev),
+                   logp=torch.empty((B, G), dtype=torch.float32, device=dev))
+    rid = _rid(request_id, B, dev)
+    _check(lib.dspark_verify_noalloc(
+        _ptr(target), _ptr(base), _ptr(e_in), _ptr(w_out), _ptr(draft_logits), _ptr(anchor),
+        _ptr(draft["tokens"]), _ptr(draft["lse"]), _ptr(draft["logq"]), _ptr(verify_len),
+        _ptr(temperature), _ptr(rid), B, G, V, r, _dtype_code(target),
+        int(seed) & 0xFFFFFFFFFFFFFFFF,
+        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["num_out"]),
+        _ptr(out.get("target_lse")), _ptr(out.get("logp")), _stream(stream)))
     return out
 
 

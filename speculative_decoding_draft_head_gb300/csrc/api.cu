@@ -11,13 +11,7 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
-dspark_status fail(dspark_status st, const char *fmt, ...) {
-    va_list ap;
-    va_start(ap, fmt);
-    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
-    va_end(ap);
-    return st;
-}
+#define fail set_last_error
 
 dspark_status cuda_fail(cudaError_t e, const char *where) {
     return fail(DSPARK_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
@@ -44,6 +38,16 @@ dspark_status check_ws(void *ws, size_t have, size_t need) {
 }
 
 }  // namespace
+}  // namespace dspark
+
+namespace dspark {
+dspark_status set_last_error(dspark_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
 }  // namespace dspark
 
 using namespace dspark;

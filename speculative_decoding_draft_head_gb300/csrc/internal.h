@@ -15,6 +15,9 @@ constexpr int kMaxG = 64;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Record the message returned by dspark_last_error() and return `st`.
+dspark_status set_last_error(dspark_status st, const char *fmt, ...);
+
 // ---------------------------------------------------------------- draft ----
 struct DraftPlan {
     bool tensor_path;      // tcgen05 Markov-head kernel (bf16) vs SIMT kernel
