@@ -80,7 +80,8 @@ enum {
     DSPARK_FLAG_BAD_TOKEN = 1u,        /* an anchor or draft token outside [0, V) */
     DSPARK_FLAG_BAD_TEMPERATURE = 2u,  /* a temperature that is negative, NaN or inf */
     DSPARK_FLAG_BAD_VERIFY_LEN = 4u,   /* a verify length outside [0, G] */
-    DSPARK_FLAG_BAD_POS_TEMP = 8u      /* a calibration temperature <= 0 or NaN */
+    DSPARK_FLAG_BAD_POS_TEMP = 8u,     /* a calibration temperature <= 0 or NaN */
+    DSPARK_FLAG_TIMEOUT = 16u          /* a bounded device-side wait gave up */
 };
 
 /* Library version, major * 10000 + minor * 100 + patch. */
@@ -100,7 +101,8 @@ DSPARK_API size_t dspark_workspace_bytes(int which, int B, int G, int V, int r);
  * Defined by "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
  * "Un po' di autoregressione basta", equation for p_k: the draft distribution
  * of position j is softmax(U_j + B_j) where the bias B_j = E_in[x_{j-1}] W_out
- * is the rank-r Markov head (B = W1 W2) driven by the previous token (the
+ * is the rank-r Markov head (B = W1 W2, with W1 = E_in and W2 = W_out^T)
+ * driven by the previous token (the
  * anchor x_0 for the first position), and tokens are drawn left to right so
  * each keeps an explicit softmax probability.
  *
@@ -112,13 +114,16 @@ DSPARK_API size_t dspark_workspace_bytes(int which, int B, int G, int V, int r);
  *          logq = s[x_j] - lse
  *   T = 0: x_j = argmax_v z[v] (lowest id on ties), lse = max z, logq = 0
  *
- * base_logits [B][G][V] dtype   e_in [V][r] dtype   w_out [r][V] dtype
+ * base_logits [B][G][V] dtype   e_in [V][r] dtype   w_out [V][r] dtype (row v
+ * scores token v, the layout of a language-model output head)
  * anchor [B] int32              temperature [B] fp32 (>= 0)
  * request_id [B] uint32 or NULL (then request b uses id b)
  * outputs: draft_tokens [B][G] int32, draft_lse [B][G] fp32,
  *          draft_logq [B][G] fp32, draft_logits [B][G][V] fp32 z or NULL.
  * Limits: 1 <= B, 1 <= G <= 64, 8 <= V < 2^31 with V % 8 == 0,
- *         16 <= r <= 256 with r % 16 == 0 (bf16) or 1 <= r <= 256 (fp32).
+ *         16 <= r <= 256 with r % 16 == 0 (bf16) or 4 <= r <= 256 with
+ *         r % 4 == 0 (fp32).  bf16 runs the bias on the tcgen05 tensor cores;
+ *         fp32 runs it with CUDA-core FMAs (no TF32 rounding).
  */
 DSPARK_API dspark_status dspark_draft_sample(
     const void *base_logits, const void *e_in, const void *w_out,

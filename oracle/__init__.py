@@ -163,7 +163,8 @@ def gumbel(seed, request_id, j, v, stream):
 def draft_sample(U, E_in, W_out, anchor, temp, rid=None, seed=0, want_z=False):
     """Draft a block for every request (see ``or_draft_sample``).
 
-    U [B,G,V], E_in [V,r], W_out [r,V], anchor [B], temp [B], rid [B] or None.
+    U [B,G,V], E_in [V,r], W_out [V,r] (row v scores token v), anchor [B], temp [B],
+    rid [B] or None.
     Returns a dict of numpy arrays: tokens, lse, logq, gap, top (all [B,G]),
     and z [B,G,V] when ``want_z``.
     """
@@ -172,7 +173,7 @@ def draft_sample(U, E_in, W_out, anchor, temp, rid=None, seed=0, want_z=False):
     W_out = _f64(W_out)
     B, G, V = U.shape
     r = E_in.shape[1]
-    assert E_in.shape == (V, r) and W_out.shape == (r, V)
+    assert E_in.shape == (V, r) and W_out.shape == (V, r)
     anchor = _i32(anchor)
     temp = _f64(temp)
     rid = _u32(rid)

@@ -31,7 +31,7 @@
  *      2 residual Gumbel, 3 bonus Gumbel.
  *  R2  u = ((w >> 9) + 1/2) * 2^-23, an exact fp32 value in (0, 1);
  *      Gumbel noise g = -ln(-ln u).
- *  R3  One low-rank factorisation B = E_in * W_out serves every block
+ *  R3  One low-rank factorisation B = E_in * W_out^T serves every block
  *      position; the bias at position j depends only on the previous token
  *      (the anchor for j = 0).
  *  R4  z = U + bias is rounded to fp32 (the value the kernels hold); all later
@@ -159,15 +159,17 @@ static int gumbel_max(const double *s, const unsigned char *allowed, int V,
 }
 
 /* [DSP-IT] "Un po' di autoregressione basta", equation for p_k, with the
- * Markov head B = W1 W2 (R3, R4):
- *   z_v = fp32( U[v] + sum_k E_in[prev, k] * W_out[k, v] ). */
+ * Markov head B = W1 W2 (R3, R4).  W1 = E_in is stored [V][r]; W2 is stored
+ * transposed as W_out [V][r] (row v scores token v), so
+ *   z_v = fp32( U[v] + sum_k E_in[prev, k] * W_out[v, k] ). */
 static void markov_logits(const double *U_row, const double *E_in, const double *W_out,
                           int prev, int V, int r, double *z)
 {
     const double *e = E_in + (size_t)prev * (size_t)r;
     for (int v = 0; v < V; ++v) {
+        const double *w = W_out + (size_t)v * (size_t)r;
         double bias = 0.0;
-        for (int k = 0; k < r; ++k) bias += e[k] * W_out[(size_t)k * (size_t)V + (size_t)v];
+        for (int k = 0; k < r; ++k) bias += e[k] * w[k];
         z[v] = (double)(float)(U_row[v] + bias);
     }
 }
@@ -177,7 +179,7 @@ static void markov_logits(const double *U_row, const double *E_in, const double 
 /* autoregressione basta": each draft token keeps an explicit softmax         */
 /* probability; the sampled token feeds the next position's bias).            */
 /*                                                                           */
-/* U [B][G][V], E_in [V][r], W_out [r][V], anchor [B], temp [B], rid [B]      */
+/* U [B][G][V], E_in [V][r], W_out [V][r], anchor [B], temp [B], rid [B]      */
 /* (NULL = 0..B-1).  Outputs [B][G]: tokens, lse (T = 0: max z), logq         */
 /* (T = 0: 0), gap / top of the deciding keys; z_out [B][G][V] optional.      */
 /* Returns 0, or -1 on an out-of-range anchor.                                */

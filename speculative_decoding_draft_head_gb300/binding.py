@@ -168,7 +168,7 @@ def draft_sample(base, e_in, w_out, anchor, temperature, request_id=None, seed=0
     dev = base.device
     _need(base, "base", shape=(B, G, V), device=dev)
     _need(e_in, "e_in", dtype=base.dtype, shape=(V, r), device=dev)
-    _need(w_out, "w_out", dtype=base.dtype, shape=(r, V), device=dev)
+    _need(w_out, "w_out", dtype=base.dtype, shape=(V, r), device=dev)
     _need(anchor, "anchor", dtype=torch.int32, shape=(B,), device=dev)
     _need(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
     rid = _rid(request_id, B, dev)

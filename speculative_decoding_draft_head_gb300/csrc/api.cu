@@ -26,6 +26,7 @@ dspark_status check_common(int B, int G, int V, int r, dspark_dtype dt) {
     if (dt != DSPARK_BF16 && dt != DSPARK_F32) return fail(DSPARK_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
     if (r < 1 || r > 256) return fail(DSPARK_ERR_INVALID_ARG, "r must be in [1, 256] (got %d)", r);
     if (dt == DSPARK_BF16 && r % 16 != 0) return fail(DSPARK_ERR_INVALID_ARG, "bf16 needs r %% 16 == 0 (got %d)", r);
+    if (dt == DSPARK_F32 && r % 4 != 0) return fail(DSPARK_ERR_INVALID_ARG, "fp32 needs r %% 4 == 0 (got %d)", r);
     if ((long)B * G * (long)V > (1L << 40)) return fail(DSPARK_ERR_INVALID_ARG, "B*G*V too large");
     return DSPARK_OK;
 }
@@ -61,11 +62,17 @@ const char *dspark_last_error(void) { return g_last_error; }
 size_t dspark_workspace_bytes(int which, int B, int G, int V, int r) {
     if (B < 1 || G < 1 || G > kMaxG || V < 8 || V % 8 != 0 || r < 1 || r > 256) return 0;
     switch (which) {
-        case DSPARK_WS_DRAFT: return plan_draft(B, G, V, r, DSPARK_BF16).ws_bytes > plan_draft(B, G, V, r, DSPARK_F32).ws_bytes
-                                         ? plan_draft(B, G, V, r, DSPARK_BF16).ws_bytes
-                                         : plan_draft(B, G, V, r, DSPARK_F32).ws_bytes;
+        case DSPARK_WS_DRAFT: {
+            const size_t a = plan_draft(B, G, V, r, DSPARK_BF16).ws_bytes;
+            const size_t b = plan_draft(B, G, V, r, DSPARK_F32).ws_bytes;
+            return a > b ? a : b;
+        }
         case DSPARK_WS_SCHEDULE: return kFlagBytes;
-        case DSPARK_WS_VERIFY: return plan_verify(B, G, V, r).ws_bytes;
+        case DSPARK_WS_VERIFY: {
+            const size_t a = plan_verify(B, G, V, r, DSPARK_BF16).ws_bytes;
+            const size_t b = plan_verify(B, G, V, r, DSPARK_F32).ws_bytes;
+            return a > b ? a : b;
+        }
         default: return 0;
     }
 }
@@ -144,7 +151,7 @@ dspark_status dspark_verify(const void *target_logits, const void *base_logits, 
         (e_in && !aligned(e_in, 16)) || (w_out && !aligned(w_out, 16)) ||
         (draft_logits && !aligned(draft_logits, 16)))
         return fail(DSPARK_ERR_INVALID_ARG, "logits and weights must be 16-byte aligned");
-    const VerifyPlan plan = plan_verify(B, G, V, r);
+    const VerifyPlan plan = plan_verify(B, G, V, r, dtype);
     if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);

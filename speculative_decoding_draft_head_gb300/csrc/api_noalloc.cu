@@ -72,7 +72,7 @@ dspark_status dspark_verify_noalloc(
                              draft_lse, draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype,
                              seed, accept_len, out_tokens, num_out, target_lse, logp_sel, nullptr, 0,
                              stream);  // reports the size error
-    const size_t need = plan_verify(B, G, V, r).ws_bytes;
+    const size_t need = plan_verify(B, G, V, r, dtype).ws_bytes;
     if (need > kNoAllocScratchBytes)
         return set_last_error(DSPARK_ERR_UNSUPPORTED,
                               "verify needs %zu bytes of scratch, more than the fixed %zu-byte array",

@@ -4,6 +4,11 @@
 // Numbers: As Easy as 1, 2, 3", SC'11) keyed by the 64-bit seed, counter =
 // (v >> 2, position, request id, stream), word v & 3; the uniform keeps the
 // top 23 bits of the word and centres it in its cell: u = (k + 1/2) 2^-23.
+//
+// Scores are kept in log2 units: s2 = z * log2(e) / T.  The online softmax
+// holds (m, S) with S = sum 2^(s2 - m), so lse = ln 2 * (m + log2 S); the
+// Gumbel-max key of token v is s2_v - log2(E_v) with E_v = -ln u_v, which
+// orders tokens exactly as the natural-log key s_v - ln(E_v) = s_v + g_v.
 #pragma once
 
 #include <cstdint>
@@ -26,6 +31,10 @@ constexpr uint32_t kFlagBadToken = 1u;
 constexpr uint32_t kFlagBadTemperature = 2u;
 constexpr uint32_t kFlagBadVerifyLen = 4u;
 constexpr uint32_t kFlagBadPosTemp = 8u;
+constexpr uint32_t kFlagTimeout = 16u;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // Ten rounds of the Philox4x32 bijection.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
@@ -51,13 +60,32 @@ __device__ __forceinline__ float word_to_uniform(uint32_t w) {
     return __uint_as_float(0x3F800000u | (w >> 9)) - 0x1.fffffep-1f;
 }
 
+// 1 - u, exact: (2 - 2^-24) - (1 + k 2^-23).
+__device__ __forceinline__ float word_to_one_minus_uniform(uint32_t w) {
+    return 0x1.fffffep+0f - __uint_as_float(0x3F800000u | (w >> 9));
+}
+
 // Exponential variate E = -ln u (relative accuracy matters: small E wins).
 __device__ __forceinline__ float neg_log_uniform(uint32_t w) {
     return -logf(word_to_uniform(w));
 }
 
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
 // Four consecutive elements starting at a 4-aligned index.
 __device__ __forceinline__ float4 load4(const float *p) {
@@ -65,23 +93,20 @@ __device__ __forceinline__ float4 load4(const float *p) {
 }
 __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
     const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(p));
-    float4 f;
-    f.x = __uint_as_float(raw.x << 16);
-    f.y = __uint_as_float(raw.x & 0xFFFF0000u);
-    f.z = __uint_as_float(raw.y << 16);
-    f.w = __uint_as_float(raw.y & 0xFFFF0000u);
-    return f;
+    return make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
 }
 __device__ __forceinline__ float elem(const float4 &f, int e) {
     return e == 0 ? f.x : (e == 1 ? f.y : (e == 2 ? f.z : f.w));
 }
 
 // Running state of one row segment: online softmax (m, S) and the best key.
+// T > 0: m = max s2, S = sum 2^(s2 - m), key = best s2 - log2(E), s_at = s2
+// at the best token.  T = 0: key = m = max z, s_at = z at the best token.
 struct RowState {
-    float m;      // max of s seen
-    float S;      // sum of exp(s - m)
-    float key;    // best key (Gumbel-perturbed s, or z when greedy)
-    float s_at;   // s at the best index
+    float m;
+    float S;
+    float key;
+    float s_at;
     int idx;      // best index, INT32_MAX if none
     int pad0, pad1, pad2;
 };
@@ -106,8 +131,8 @@ __device__ __forceinline__ bool key_better(float ka, int ia, float kb, int ib) {
 __device__ __forceinline__ void row_state_merge(RowState &a, const RowState &b) {
     const float m = fmaxf(a.m, b.m);
     if (m != -INFINITY) {
-        const float sa = (a.m == -INFINITY) ? 0.f : a.S * expf(a.m - m);
-        const float sb = (b.m == -INFINITY) ? 0.f : b.S * expf(b.m - m);
+        const float sa = (a.m == -INFINITY) ? 0.f : a.S * exp2f(a.m - m);
+        const float sb = (b.m == -INFINITY) ? 0.f : b.S * exp2f(b.m - m);
         a.S = sa + sb;
         a.m = m;
     }
@@ -138,23 +163,36 @@ __device__ __forceinline__ RowState warp_merge(RowState s) {
     return s;
 }
 
-// Online-softmax step with one value s (T > 0).
-__device__ __forceinline__ void softmax_push(RowState &st, float s) {
-    if (s > st.m) {
-        st.S = st.S * expf(st.m - s) + 1.f;
-        st.m = s;
-    } else {
-        st.S += expf(s - st.m);
+// Online-softmax step with a group of n scores (log2 units), n <= 16.
+template <int N>
+__device__ __forceinline__ void softmax_push_group(RowState &st, const float (&s2)[N], int n) {
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (i < n) cm = fmaxf(cm, s2[i]);
+    if (cm > st.m) {
+        st.S = (st.m == -INFINITY) ? 0.f : st.S * fast_exp2(st.m - cm);
+        st.m = cm;
     }
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (i < n) acc += fast_exp2(s2[i] - st.m);
+    st.S += acc;
 }
 
-// Gumbel-max step: key = s + g(u) = s - ln(E), E = -ln u.
-__device__ __forceinline__ void gumbel_push(RowState &st, float s, uint32_t word, int v) {
-    const float key = s - logf(neg_log_uniform(word));
-    if (key > st.key || (key == st.key && v < st.idx)) {
-        st.key = key;
-        st.s_at = s;
-        st.idx = v;
+// Gumbel-max step for one token: exact key s2 - log2(-ln u).  The cheap test
+// first: since -ln u >= 1 - u, the token cannot beat the current best when
+// log2(1 - u) >= s2 - best (a 1e-4 margin covers the approximate log2).
+__device__ __forceinline__ void gumbel_push(RowState &st, float s2, uint32_t word, int v) {
+    const float w1 = word_to_one_minus_uniform(word);
+    if (fast_log2(w1) < s2 - st.key + 1e-4f) {
+        const float key = s2 - fast_log2(neg_log_uniform(word));
+        if (key > st.key || (key == st.key && v < st.idx)) {
+            st.key = key;
+            st.s_at = s2;
+            st.idx = v;
+        }
     }
 }
 
@@ -166,6 +204,30 @@ __device__ __forceinline__ void argmax_push(RowState &st, float z, int v) {
         st.idx = v;
     }
     st.m = fmaxf(st.m, z);
+}
+
+// Residual draw state: best key over {p > q} and, for the degenerate case
+// where no entry has p > q, the best key of a draw from p.
+struct ResidualState {
+    float key_res;
+    int idx_res;
+    float key_p;
+    int idx_p;
+};
+
+__device__ __forceinline__ ResidualState residual_init() {
+    return ResidualState{-INFINITY, INT32_MAX, -INFINITY, INT32_MAX};
+}
+
+__device__ __forceinline__ void residual_merge(ResidualState &a, const ResidualState &b) {
+    if (key_better(b.key_res, b.idx_res, a.key_res, a.idx_res)) {
+        a.key_res = b.key_res;
+        a.idx_res = b.idx_res;
+    }
+    if (key_better(b.key_p, b.idx_p, a.key_p, a.idx_p)) {
+        a.key_p = b.key_p;
+        a.idx_p = b.idx_p;
+    }
 }
 
 // Block-wide merge of one RowState per thread; the result is valid in thread 0.

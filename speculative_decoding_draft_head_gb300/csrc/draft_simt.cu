@@ -1,17 +1,18 @@
-// Draft sampling, SIMT form (fp32 weights, and any dtype when the tensor-core
-// kernel does not apply), plus the split-vocabulary merge shared by both forms.
+// Draft sampling, SIMT form (fp32 weights), plus the split-vocabulary merge
+// shared with the tensor-core form.
 //
 // Method: "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
 // "Un po' di autoregressione basta", equation for p_k: position j draws from
-// softmax((U_j + E_in[x_{j-1}] W_out) / T); the drawn token feeds position j+1.
+// softmax((U_j + E_in[x_{j-1}] W_out^T) / T); the drawn token feeds position j+1.
 //
 // One launch per block position.  A block owns `rows_per_block` requests and
 // one vocabulary segment: it gathers the E_in rows of the previous tokens into
 // shared memory, forms the rank-r bias with register-tiled FMAs (4 vocabulary
-// entries x rows_per_block requests per thread), adds the base logits and
-// streams every logit once through the online softmax and the Gumbel-max
-// argmax.  The per-(request, segment) partial states are merged by
-// draft_finalize, which writes the token the next position reads.
+// entries x rows_per_block requests per thread, W_out rows read along r), adds
+// the base logits and streams every logit once through the online softmax and
+// the Gumbel-max argmax.  The per-(request, segment) partial states are merged
+// by draft_finalize, which writes the token the next position reads.  bf16
+// weights take the tensor-core kernel (markov_tc.cu) instead.
 #include <climits>
 
 #include "device_common.cuh"
@@ -33,7 +34,7 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
                   uint32_t *__restrict__ flags, float *__restrict__ z_out) {
     extern __shared__ float a_rows[];  // [kSimtRows][r]
     __shared__ int prev_s[kSimtRows];
-    __shared__ float inv_t_s[kSimtRows];
+    __shared__ float c2_s[kSimtRows];
     __shared__ uint32_t rid_s[kSimtRows];
     __shared__ RowState scratch[kSimtThreads / 32];
 
@@ -42,7 +43,7 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
     if (threadIdx.x < kSimtRows) {
         const int b = b0 + threadIdx.x;
         int prev = -1;
-        float inv_t = 0.f;
+        float c2 = 0.f;
         uint32_t id = 0;
         if (b < B) {
             prev = (j == 0) ? anchor[b] : tokens[(size_t)b * G + j - 1];
@@ -51,15 +52,13 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
             const bool bad_prev = prev < 0 || prev >= V;
             // an earlier position already flagged this request and wrote -1
             if (bad_prev && (j == 0 || prev != -1) && seg == 0) atomicOr(flags, kFlagBadToken);
-            if (!(T >= 0.f) || isinf(T)) {
-                if (seg == 0 && j == 0) atomicOr(flags, kFlagBadTemperature);
-                prev = -1;
-            }
-            if (bad_prev) prev = -1;
-            inv_t = (T > 0.f) ? 1.0f / T : 0.f;
+            const bool t_ok = T >= 0.f && !isinf(T);
+            if (!t_ok && seg == 0 && j == 0) atomicOr(flags, kFlagBadTemperature);
+            if (bad_prev || !t_ok) prev = -1;
+            c2 = (T > 0.f) ? kLog2e / T : 0.f;
         }
         prev_s[threadIdx.x] = prev;
-        inv_t_s[threadIdx.x] = inv_t;
+        c2_s[threadIdx.x] = c2;
         rid_s[threadIdx.x] = id;
     }
     __syncthreads();
@@ -82,15 +81,22 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
         for (int rb = 0; rb < kSimtRows; ++rb)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[rb][e] = 0.f;
-        for (int k = 0; k < r; ++k) {
-            const float4 w = load4(w_out + (size_t)k * V + v);
+        for (int k = 0; k < r; k += 4) {
+            float4 w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = load4(w_out + (size_t)(v + e) * r + k);
 #pragma unroll
             for (int rb = 0; rb < kSimtRows; ++rb) {
-                const float a = a_rows[rb * r + k];
-                acc[rb][0] = fmaf(a, w.x, acc[rb][0]);
-                acc[rb][1] = fmaf(a, w.y, acc[rb][1]);
-                acc[rb][2] = fmaf(a, w.z, acc[rb][2]);
-                acc[rb][3] = fmaf(a, w.w, acc[rb][3]);
+                const float4 a = *reinterpret_cast<const float4 *>(a_rows + rb * r + k);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float t = acc[rb][e];
+                    t = fmaf(a.x, w[e].x, t);
+                    t = fmaf(a.y, w[e].y, t);
+                    t = fmaf(a.z, w[e].z, t);
+                    t = fmaf(a.w, w[e].w, t);
+                    acc[rb][e] = t;
+                }
             }
         }
 #pragma unroll
@@ -99,19 +105,19 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
             if (b >= B || prev_s[rb] < 0) continue;
             const size_t row = (size_t)b * G + j;
             const float4 u4 = load4(base + row * V + v);
-            const float inv_t = inv_t_s[rb];
+            const float c2 = c2_s[rb];
             float z[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[rb][e];
             if (z_out) *reinterpret_cast<float4 *>(z_out + row * V + v) = make_float4(z[0], z[1], z[2], z[3]);
-            if (inv_t > 0.f) {
+            if (c2 > 0.f) {
+                float s2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s2[e] = z[e] * c2;
+                softmax_push_group<4>(st[rb], s2, 4);
                 const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, rid_s[rb], kStreamDraft), k0, k1);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float s = z[e] * inv_t;
-                    softmax_push(st[rb], s);
-                    gumbel_push(st[rb], s, word_of(w4, e), v + e);
-                }
+                for (int e = 0; e < 4; ++e) gumbel_push(st[rb], s2[e], word_of(w4, e), v + e);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) argmax_push(st[rb], z[e], v + e);
@@ -148,9 +154,9 @@ __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsp
     }
     tokens[o] = s.idx;
     if (T > 0.f) {
-        const float l = s.m + logf(s.S);
-        lse[o] = l;
-        logq[o] = s.s_at - l;
+        const float l2 = log2f(s.S);
+        lse[o] = kLn2 * (s.m + l2);
+        logq[o] = kLn2 * ((s.s_at - s.m) - l2);
     } else {
         lse[o] = s.key;
         logq[o] = 0.f;
@@ -188,23 +194,30 @@ cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j,
 }
 
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
-    DraftPlan p{};
     (void)G;
     (void)r;
-    (void)dt;
-    p.tensor_path = false;
-    p.rows_per_block = kSimtRows;
-    p.row_blocks = (B + kSimtRows - 1) / kSimtRows;
-    const int want_blocks = 2 * kNumSMs;
-    int nsplit = (want_blocks + p.row_blocks - 1) / p.row_blocks;
-    const int max_split = (V + 1023) / 1024;
-    if (nsplit > max_split) nsplit = max_split;
-    if (nsplit < 1) nsplit = 1;
-    int chunk = (V + nsplit - 1) / nsplit;
-    chunk = (chunk + 3) / 4 * 4;
-    p.nsplit = (V + chunk - 1) / chunk;
-    p.chunk = chunk;
+    DraftPlan p{};
     p.partial_offset = kFlagBytes;
+    if (dt == DSPARK_BF16) {
+        p.tensor_path = true;
+        p.rows_per_block = 128;
+        p.row_blocks = tc_row_blocks(B);
+        p.nsplit = tc_segments(B, V);
+        p.chunk = 0;
+    } else {
+        p.tensor_path = false;
+        p.rows_per_block = kSimtRows;
+        p.row_blocks = (B + kSimtRows - 1) / kSimtRows;
+        const int want_blocks = 2 * kNumSMs;
+        int nsplit = (want_blocks + p.row_blocks - 1) / p.row_blocks;
+        const int max_split = (V + 1023) / 1024;
+        if (nsplit > max_split) nsplit = max_split;
+        if (nsplit < 1) nsplit = 1;
+        int chunk = (V + nsplit - 1) / nsplit;
+        chunk = (chunk + 3) / 4 * 4;
+        p.nsplit = (V + chunk - 1) / chunk;
+        p.chunk = chunk;
+    }
     p.ws_bytes = align_up(p.partial_offset + sizeof(RowState) * (size_t)B * p.nsplit, 256);
     return p;
 }

@@ -50,19 +50,46 @@ cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cud
 cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
 cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
 
+// tensor-core kernel geometry (bf16): 128-request row blocks x vocabulary segments
+int tc_row_blocks(int B);
+int tc_segments(int B, int V);
+size_t tc_residual_state_bytes();
+
+// residual resampling of the rejected rows on the tensor cores
+struct ResidualArgs {
+    const void *target;
+    const void *base;
+    const void *e_in;
+    const void *w_out;
+    const int32_t *anchor;
+    const int32_t *tokens;
+    const float *temperature;
+    const uint32_t *request_id;
+    const int32_t *res_row;    // [B] rejected position or -1
+    const float *lse_t_row;    // [B] target lse of that row, log2 units
+    const float *draft_lse;    // [B][G] natural log
+    int B, G, V, r, nseg;
+    uint64_t seed;
+    void *rpart;               // [B][nseg] residual partials
+    uint32_t *flags;
+};
+cudaError_t launch_residual_tensor(const ResidualArgs &a, cudaStream_t s);
+
 // --------------------------------------------------------------- verify ----
 struct VerifyPlan {
+    bool tensor_residual;   // residual rows rebuilt on the tensor cores (bf16)
     int row_split;          // segments per target row in the row pass
     int row_chunk;
-    int res_split;          // segments per residual row
-    int res_chunk;
+    int res_split;          // segments per residual row, SIMT kernel
+    int res_chunk;          // entries per segment, SIMT kernel
+    int res_split_tc;       // segments per residual row, tensor-core kernel (0 = unused)
     size_t row_part_offset; // [B][G+1][row_split] RowState
     size_t res_row_offset;  // [B] int32: rejected position or -1
     size_t lse_t_offset;    // [B] fp32: target lse of the rejected row
     size_t res_part_offset; // [B][res_split] ResidualState
     size_t ws_bytes;
 };
-VerifyPlan plan_verify(int B, int G, int V, int r);
+VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt);
 
 struct VerifyArgs {
     const void *target;

@@ -1,0 +1,576 @@
+// Markov-head logits on the tcgen05 tensor cores, fused with sampling.
+//
+// Method: "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
+// "Un po' di autoregressione basta": position j draws from
+// softmax((U_j + E_in[x_{j-1}] W_out^T) / T), a rank-r bias driven by the
+// previous token.  The bias is a dense contraction (128 requests x 64 tokens x
+// r per tile), so it runs on the tensor cores; everything after it -- base
+// logits, temperature, online softmax, Philox Gumbel-max -- is fused into the
+// TMEM epilogue so that each logit is produced and consumed on chip.
+//
+// Two uses share the kernel:
+//  - draft:    rows = 128 requests at block position j; reads the base logits
+//              tile by TMA; writes per-(request, segment) softmax/argmax
+//              partials (draft_finalize merges them and writes x_j, which the
+//              next position's launch gathers);
+//  - residual: rows = 128 requests, each at its own rejected position d_b
+//              (rows without a rejection idle); reads base and target logits
+//              directly and draws from max(0, p - q) by Gumbel-max.
+//
+// CTA layout (one CTA per SM, 576 threads, ~196 KB shared memory):
+//   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant of
+//               rows) and columns 16*(w/4).. of each 64-column tile;
+//   warp 16     TMA producer: W_out tiles (64 tokens x r, 128-byte swizzle,
+//               L2 evict-last) and base-logit tiles (evict-first);
+//   warp 17     TMEM allocator and UMMA issuer (M=128, N=64, K=16 steps).
+// The A operand (the 128 gathered E_in rows, 128 x r bf16) is built once per
+// CTA in the 128-byte swizzled K-major layout.  Rings: 2 W stages, 3 base
+// stages, 4 TMEM accumulators of 64 columns.  Every wait is bounded; a timeout
+// sets the timeout bit of the flag word and the CTA unwinds.
+#include <climits>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "tc_primitives.cuh"
+
+namespace dspark {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;
+constexpr int BN = 64;
+constexpr int kEpiWarps = 16;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 18 * 32;
+constexpr int kWStages = 2;
+constexpr int kUStages = 3;
+constexpr int kAccBufs = 4;
+constexpr uint32_t kTmemCols = kAccBufs * BN;  // 256
+constexpr uint32_t kAtomA = BM * 128;          // one 64-wide K atom of A: 16 KB
+constexpr uint32_t kAtomW = BN * 128;          // one 64-wide K atom of a W tile: 8 KB
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffW = kOffA + 4 * kAtomA;
+constexpr uint32_t kOffU = kOffW + kWStages * 4 * kAtomW;
+constexpr uint32_t kUBytes = BM * BN * 2;
+constexpr uint32_t kOffMerge = kOffU + kUStages * kUBytes;
+constexpr uint32_t kMergeBytes = BM * 4 * 32;
+constexpr uint32_t kOffBar = kOffMerge + kMergeBytes;
+constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kMiscBytes = 16 + BM * 16;
+constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of clock cycles
+
+struct TcParams {
+    const __nv_bfloat16 *e_in;
+    const __nv_bfloat16 *base;
+    const __nv_bfloat16 *target;
+    const int32_t *anchor;
+    const int32_t *tokens;
+    const float *temperature;
+    const uint32_t *request_id;
+    const int32_t *res_row;
+    const float *lse_t_row;   // log2 units
+    const float *draft_lse;   // natural log
+    int B, G, V, r, j, nseg;
+    uint32_t k0, k1;
+    RowState *part;
+    ResidualState *rpart;
+    uint32_t *flags;
+    float *z_out;
+};
+
+__device__ __forceinline__ int seg_begin(int s, int nseg, int V) {
+    if (s >= nseg) return V;
+    return (int)(((long long)s * V / nseg) & ~7LL);
+}
+
+__device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    bool ok = mbar_wait(bar, parity, abort, kSpinLimit);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <bool kResidual>
+__global__ void __launch_bounds__(kThreads, 1)
+markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
+                 const TcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg = blockIdx.x;
+    const int m0 = blockIdx.y * BM;
+    const int vb = seg_begin(seg, p.nseg, p.V);
+    const int ve = seg_begin(seg + 1, p.nseg, p.V);
+    const int ntiles = (ve - vb + BN - 1) / BN;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
+    auto full_w = [&](int s) { return bar(s); };
+    auto empty_w = [&](int s) { return bar(2 + s); };
+    auto full_u = [&](int s) { return bar(4 + s); };
+    auto empty_u = [&](int s) { return bar(7 + s); };
+    auto tfull = [&](int a) { return bar(10 + a); };
+    auto tempty = [&](int a) { return bar(14 + a); };
+
+    int *misc = reinterpret_cast<int *>(smem + kOffMisc);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
+    volatile int *abort = misc + 1;
+    int *row_prev = misc + 4;
+    float *row_c2 = reinterpret_cast<float *>(misc + 4 + BM);
+    uint32_t *row_rid = reinterpret_cast<uint32_t *>(misc + 4 + 2 * BM);
+    int *row_aux = misc + 4 + 3 * BM;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(full_w(s), 1);
+            mbar_init(empty_w(s), 1);
+        }
+        for (int s = 0; s < kUStages; ++s) {
+            mbar_init(full_u(s), 1);
+            mbar_init(empty_u(s), kEpiWarps);
+        }
+        for (int a = 0; a < kAccBufs; ++a) {
+            mbar_init(tfull(a), 1);
+            mbar_init(tempty(a), kEpiWarps);
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&map_w);
+        if (!kResidual) tma_prefetch_desc(&map_u);
+    }
+    if (threadIdx.x < BM) {
+        const int b = m0 + threadIdx.x;
+        int prev = -1, aux = -1;
+        float c2 = 0.f;
+        uint32_t id = 0;
+        if (b < p.B) {
+            const float T = p.temperature[b];
+            id = p.request_id ? p.request_id[b] : (uint32_t)b;
+            const bool t_ok = T >= 0.f && !isinf(T);
+            if (!kResidual) {
+                prev = (p.j == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + p.j - 1];
+                const bool bad = prev < 0 || prev >= p.V;
+                if (bad && (p.j == 0 || prev != -1) && seg == 0) atomicOr(p.flags, kFlagBadToken);
+                if (!t_ok && p.j == 0 && seg == 0) atomicOr(p.flags, kFlagBadTemperature);
+                if (bad || !t_ok) prev = -1;
+                c2 = (T > 0.f) ? kLog2e / T : 0.f;
+            } else {
+                const int d = p.res_row[b];
+                if (d >= 0) {  // validated by the decide kernel
+                    prev = (d == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + d - 1];
+                    aux = d;
+                    c2 = kLog2e / T;
+                }
+            }
+        }
+        row_prev[threadIdx.x] = prev;
+        row_c2[threadIdx.x] = c2;
+        row_rid[threadIdx.x] = id;
+        row_aux[threadIdx.x] = aux;
+    }
+    __syncthreads();
+
+    // A operand: gathered E_in rows, 128-byte swizzled K-major atoms of 64 K.
+    if (warp < kEpiWarps) {
+        const int nchunk = p.r >> 3;  // 16-byte chunks per row
+        for (int i = threadIdx.x; i < BM * nchunk; i += kEpiWarps * 32) {
+            const int row = i / nchunk, c = i - row * nchunk;
+            const int prev = row_prev[row];
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (prev >= 0) val = __ldg(reinterpret_cast<const uint4 *>(p.e_in + (size_t)prev * p.r) + c);
+            const int atom = c >> 3, cc = c & 7;
+            st_shared_v4(sbase + kOffA + atom * kAtomA + row * 128 + ((cc ^ (row & 7)) << 4), val);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_katoms = (p.r + 63) >> 6;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_last();
+            const uint64_t pol_u = policy_evict_first();
+            for (int t = 0; t < ntiles; ++t) {
+                const int v0 = vb + t * BN;
+                const int ws = t % kWStages;
+                const uint32_t wph = (uint32_t)(t / kWStages) & 1u;
+                if (t >= kWStages && !mbar_wait(empty_w(ws), wph ^ 1u, abort, kSpinLimit)) {
+                    *abort = 1;
+                    atomicOr(p.flags, kFlagTimeout);
+                    break;
+                }
+                mbar_arrive_expect_tx(full_w(ws), n_katoms * kAtomW);
+                for (int kb = 0; kb < n_katoms; ++kb)
+                    tma_load_2d(sbase + kOffW + ws * 4 * kAtomW + kb * kAtomW, &map_w, full_w(ws), kb * 64, v0,
+                                pol_w);
+                if (!kResidual) {
+                    const int us = t % kUStages;
+                    const uint32_t uph = (uint32_t)(t / kUStages) & 1u;
+                    if (t >= kUStages && !mbar_wait(empty_u(us), uph ^ 1u, abort, kSpinLimit)) {
+                        *abort = 1;
+                        atomicOr(p.flags, kFlagTimeout);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_u(us), kUBytes);
+                    tma_load_3d(sbase + kOffU + us * kUBytes, &map_u, full_u(us), v0, p.j, m0, pol_u);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(BM, BN);
+            const int ksteps = p.r >> 4;
+            for (int t = 0; t < ntiles; ++t) {
+                const int ws = t % kWStages;
+                const uint32_t wph = (uint32_t)(t / kWStages) & 1u;
+                const int a = t % kAccBufs;
+                const uint32_t aph = (uint32_t)(t / kAccBufs) & 1u;
+                if (!mbar_wait(full_w(ws), wph, abort, kSpinLimit) ||
+                    (t >= kAccBufs && !mbar_wait(tempty(a), aph ^ 1u, abort, kSpinLimit))) {
+                    *abort = 1;
+                    atomicOr(p.flags, kFlagTimeout);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + a * BN;
+                for (int s = 0; s < ksteps; ++s) {
+                    const uint32_t kb = (uint32_t)s >> 2, ko = ((uint32_t)s & 3u) * 32u;
+                    const uint64_t ad = sw128_kmajor_desc(sbase + kOffA + kb * kAtomA + ko);
+                    const uint64_t bd = sw128_kmajor_desc(sbase + kOffW + ws * 4 * kAtomW + kb * kAtomW + ko);
+                    umma_bf16(d_tmem, ad, bd, idesc, s > 0 ? 1u : 0u);
+                }
+                umma_commit(empty_w(ws));
+                umma_commit(tfull(a));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ epilogue ----
+        const int q = warp & 3, slice = warp >> 2;
+        const int row = q * 32 + lane;
+        const int b = m0 + row;
+        const int prev = row_prev[row];
+        const float c2 = row_c2[row];
+        const uint32_t rid = row_rid[row];
+        const int d = row_aux[row];
+        const bool active = kResidual ? (d >= 0) : (prev >= 0);
+        RowState st = row_state_init();
+        ResidualState rs = residual_init();
+        float lse_q2 = 0.f, lse_t2 = 0.f;
+        if (kResidual && active) {
+            lse_q2 = p.draft_lse[(size_t)b * p.G + d] * kLog2e;
+            lse_t2 = p.lse_t_row[b];
+        }
+        const uint32_t pos = kResidual ? (uint32_t)(d < 0 ? 0 : d) : (uint32_t)p.j;
+        for (int t = 0; t < ntiles; ++t) {
+            const int a = t % kAccBufs;
+            const uint32_t aph = (uint32_t)(t / kAccBufs) & 1u;
+            if (!uniform_wait(tfull(a), aph, abort)) {
+                if (lane == 0) {
+                    *abort = 1;
+                    atomicOr(p.flags, kFlagTimeout);
+                }
+                break;
+            }
+            tc_fence_after();
+            uint32_t acc[16];
+            tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 16, acc);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(a));
+
+            const int v = vb + t * BN + slice * 16;
+            const int n = min(16, ve - v);
+            float u[16];
+            if (!kResidual) {
+                const int us = t % kUStages;
+                const uint32_t uph = (uint32_t)(t / kUStages) & 1u;
+                if (!uniform_wait(full_u(us), uph, abort)) {
+                    if (lane == 0) {
+                        *abort = 1;
+                        atomicOr(p.flags, kFlagTimeout);
+                    }
+                    break;
+                }
+                const uint32_t ub = sbase + kOffU + us * kUBytes + row * 128;
+                const uint4 lo = ld_shared_v4(ub + ((uint32_t)((2 * slice) ^ (row & 7)) << 4));
+                const uint4 hi = ld_shared_v4(ub + ((uint32_t)((2 * slice + 1) ^ (row & 7)) << 4));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_u(us));
+                const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    u[2 * i] = bf16_lo(wv[i]);
+                    u[2 * i + 1] = bf16_hi(wv[i]);
+                }
+            }
+            if (!active || n <= 0) continue;
+
+            if (!kResidual) {
+                float z[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) z[i] = u[i] + __uint_as_float(acc[i]);
+                if (p.z_out) {
+                    float *zo = p.z_out + ((size_t)b * p.G + p.j) * p.V + v;
+                    if (n == 16) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(zo + i) = make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
+                    } else {
+                        for (int i = 0; i < n; ++i) zo[i] = z[i];
+                    }
+                }
+                if (c2 == 0.f) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i < n) argmax_push(st, z[i], v + i);
+                } else {
+                    float s2[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) s2[i] = z[i] * c2;
+                    softmax_push_group<16>(st, s2, n);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (4 * g < n) {
+                            const uint4 w4 = philox4x32_10(
+                                make_uint4(((uint32_t)v >> 2) + g, pos, rid, kStreamDraft), p.k0, p.k1);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (4 * g + e < n) gumbel_push(st, s2[4 * g + e], word_of(w4, e), v + 4 * g + e);
+                        }
+                    }
+                }
+            } else {
+                const size_t rowoff = ((size_t)b * p.G + d) * p.V + v;
+                const size_t trowoff = ((size_t)b * (p.G + 1) + d) * p.V + v;
+                float tt[16];
+                if (n == 16) {
+                    const uint4 *ub4 = reinterpret_cast<const uint4 *>(p.base + rowoff);
+                    const uint4 *tb4 = reinterpret_cast<const uint4 *>(p.target + trowoff);
+                    const uint4 u0 = __ldg(ub4), u1 = __ldg(ub4 + 1), t0 = __ldg(tb4), t1 = __ldg(tb4 + 1);
+                    const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    const uint32_t tw[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        u[2 * i] = bf16_lo(uw[i]);
+                        u[2 * i + 1] = bf16_hi(uw[i]);
+                        tt[2 * i] = bf16_lo(tw[i]);
+                        tt[2 * i + 1] = bf16_hi(tw[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        u[i] = (i < n) ? __bfloat162float(p.base[rowoff + i]) : 0.f;
+                        tt[i] = (i < n) ? __bfloat162float(p.target[trowoff + i]) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (4 * g < n) {
+                        const uint4 w4 = philox4x32_10(
+                            make_uint4(((uint32_t)v >> 2) + g, pos, rid, kStreamResidual), p.k0, p.k1);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * g + e;
+                            if (i >= n) continue;
+                            const float z = u[i] + __uint_as_float(acc[i]);
+                            const uint32_t word = word_of(w4, e);
+                            const float lw = fast_log2(word_to_one_minus_uniform(word));
+                            // log2 p - log2 q, from the logit difference first
+                            const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
+                            if (delta2 > 0.f) {
+                                // log2(2^delta - 1); for delta > 20 it equals delta within 2^-20
+                                const float l1 = delta2 > 20.f ? delta2 : fast_log2(expm1f(delta2 * kLn2));
+                                const float base_r = fmaf(z, c2, -lse_q2) + l1;
+                                if (lw < base_r - rs.key_res + 1e-4f) {
+                                    const float key = base_r - fast_log2(neg_log_uniform(word));
+                                    if (key > rs.key_res) {
+                                        rs.key_res = key;
+                                        rs.idx_res = v + i;
+                                    }
+                                }
+                            }
+                            const float base_p = tt[i] * c2;
+                            if (lw < base_p - rs.key_p + 1e-4f) {
+                                const float key = base_p - fast_log2(neg_log_uniform(word));
+                                if (key > rs.key_p) {
+                                    rs.key_p = key;
+                                    rs.idx_p = v + i;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        // merge the four column slices of each row
+        if (!kResidual) {
+            RowState *ms = reinterpret_cast<RowState *>(smem + kOffMerge);
+            ms[row * 4 + slice] = st;
+        } else {
+            ResidualState *ms = reinterpret_cast<ResidualState *>(smem + kOffMerge);
+            ms[row * 4 + slice] = rs;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        if (slice == 0 && b < p.B) {
+            if (!kResidual) {
+                const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
+                for (int s = 1; s < 4; ++s) row_state_merge(st, ms[row * 4 + s]);
+                p.part[(size_t)b * p.nseg + seg] = st;
+            } else if (active) {
+                const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);
+                for (int s = 1; s < 4; ++s) residual_merge(rs, ms[row * 4 + s]);
+                p.rpart[(size_t)b * p.nseg + seg] = rs;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host ----
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+cudaError_t make_w_map(CUtensorMap *m, const void *w_out, int V, int r) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)V};
+    cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)BN};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w_out), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)G, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)G * V * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BN, 1, (cuuint32_t)BM};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool kResidual>
+cudaError_t set_smem_attr() {
+    static cudaError_t once = cudaFuncSetAttribute(markov_tc_kernel<kResidual>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    return once;
+}
+
+}  // namespace
+
+int tc_row_blocks(int B) { return (B + BM - 1) / BM; }
+
+int tc_segments(int B, int V) {
+    const int mb = tc_row_blocks(B);
+    int nseg = kNumSMs / mb;
+    if (nseg < 1) nseg = 1;
+    const int max_seg = V / BN;
+    if (nseg > max_seg) nseg = max_seg < 1 ? 1 : max_seg;
+    return nseg;
+}
+
+size_t tc_residual_state_bytes() { return sizeof(ResidualState); }
+
+cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, cudaStream_t s) {
+    CUtensorMap mw, mu;
+    cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
+    if (e != cudaSuccess) return e;
+    if ((e = make_u_map(&mu, a.base, a.B, a.G, a.V)) != cudaSuccess) return e;
+    if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
+    TcParams p{};
+    p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
+    p.base = static_cast<const __nv_bfloat16 *>(a.base);
+    p.anchor = a.anchor;
+    p.tokens = a.tokens;
+    p.temperature = a.temperature;
+    p.request_id = a.request_id;
+    p.B = a.B;
+    p.G = a.G;
+    p.V = a.V;
+    p.r = a.r;
+    p.j = j;
+    p.nseg = pl.nsplit;
+    p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFu);
+    p.k1 = (uint32_t)(a.seed >> 32);
+    p.part = reinterpret_cast<RowState *>(a.ws + pl.partial_offset);
+    p.flags = reinterpret_cast<uint32_t *>(a.ws);
+    p.z_out = a.z_out;
+    markov_tc_kernel<false><<<dim3(pl.nsplit, pl.row_blocks), kThreads, kSmemBytes, s>>>(mw, mu, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_residual_tensor(const ResidualArgs &a, cudaStream_t s) {
+    CUtensorMap mw;
+    cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
+    if (e != cudaSuccess) return e;
+    if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
+    TcParams p{};
+    p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
+    p.base = static_cast<const __nv_bfloat16 *>(a.base);
+    p.target = static_cast<const __nv_bfloat16 *>(a.target);
+    p.anchor = a.anchor;
+    p.tokens = a.tokens;
+    p.temperature = a.temperature;
+    p.request_id = a.request_id;
+    p.res_row = a.res_row;
+    p.lse_t_row = a.lse_t_row;
+    p.draft_lse = a.draft_lse;
+    p.B = a.B;
+    p.G = a.G;
+    p.V = a.V;
+    p.r = a.r;
+    p.j = 0;
+    p.nseg = a.nseg;
+    p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFu);
+    p.k1 = (uint32_t)(a.seed >> 32);
+    p.rpart = reinterpret_cast<ResidualState *>(a.rpart);
+    p.flags = a.flags;
+    // the residual kernel has no base-logit tiles to load: map_u is unused
+    markov_tc_kernel<true><<<dim3(a.nseg, tc_row_blocks(a.B)), kThreads, kSmemBytes, s>>>(mw, mw, p);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

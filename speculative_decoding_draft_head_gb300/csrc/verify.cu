@@ -9,16 +9,16 @@
 //
 // Four launches:
 //  1. verify_rows     grid (segments, B*(G+1)): streams the target rows j <= L
-//                     of every request once with 128-bit loads -- online
+//                     of every request once with 16-byte loads -- online
 //                     softmax of t/T for rows j < L, the bonus Gumbel-max for
 //                     row L, the argmax for greedy requests.
 //  2. verify_decide   one warp per request: merges the row partials, runs the
 //                     sequential acceptance scan, writes the emitted tokens and
 //                     marks the rejected row, if any.
-//  3. verify_residual grid (segments, B): for rejected requests only, rebuilds
-//                     the draft logits of the rejected row (base + Markov
-//                     bias, or the stored draft logits) and draws from
-//                     max(0, p - q) by Gumbel-max.
+//  3. residual        rejected requests only: rebuilds the draft logits of the
+//                     rejected row (base + Markov bias on the tensor cores for
+//                     bf16 weights, SIMT for fp32, or the stored draft logits)
+//                     and draws from max(0, p - q) by Gumbel-max.
 //  4. verify_residual_finalize: merges the residual partials into the token.
 #include <climits>
 
@@ -30,28 +30,6 @@ namespace {
 
 constexpr int kRowThreads = 256;
 constexpr int kResThreads = 256;
-
-struct ResidualState {
-    float key_res;  // best ln(p - q) + g over entries with p > q
-    int idx_res;
-    float key_p;    // best ln p + g (used only if no entry has p > q)
-    int idx_p;
-};
-
-__device__ __forceinline__ ResidualState residual_init() {
-    return ResidualState{-INFINITY, INT32_MAX, -INFINITY, INT32_MAX};
-}
-
-__device__ __forceinline__ void residual_merge(ResidualState &a, const ResidualState &b) {
-    if (key_better(b.key_res, b.idx_res, a.key_res, a.idx_res)) {
-        a.key_res = b.key_res;
-        a.idx_res = b.idx_res;
-    }
-    if (key_better(b.key_p, b.idx_p, a.key_p, a.idx_p)) {
-        a.key_p = b.key_p;
-        a.idx_p = b.idx_p;
-    }
-}
 
 __device__ __forceinline__ ResidualState residual_warp_merge(ResidualState s) {
 #pragma unroll
@@ -73,6 +51,18 @@ __device__ __forceinline__ int read_verify_len(const int32_t *verify_len, int b,
 
 __device__ __forceinline__ bool temperature_ok(float T) { return T >= 0.f && !isinf(T); }
 
+// Eight consecutive elements (16 bytes of bf16, 32 bytes of fp32).
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 r = __ldg(reinterpret_cast<const uint4 *>(p));
+    x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x); x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
+    x[4] = bf16_lo(r.z); x[5] = bf16_hi(r.z); x[6] = bf16_lo(r.w); x[7] = bf16_hi(r.w);
+}
+__device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
 // ---------------------------------------------------------------- pass 1 ----
 template <typename TIn>
 __global__ void __launch_bounds__(kRowThreads)
@@ -87,7 +77,7 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
     const int L = read_verify_len(verify_len, b, G);
     const float T = temperature[b];
     if (L < 0 || j > L || !temperature_ok(T)) return;
-    const float inv_t = T > 0.f ? 1.0f / T : 0.f;
+    const float c2 = T > 0.f ? kLog2e / T : 0.f;
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     const int seg = blockIdx.x;
     const int vb = seg * chunk;
@@ -96,23 +86,44 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
 
     RowState st = row_state_init();
     if (T > 0.f && j < L) {
-        for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kRowThreads) {
-            const float4 t4 = load4(t_row + v);
+        int v = vb + 8 * threadIdx.x;
+        for (; v + 8 * kRowThreads < ve; v += 16 * kRowThreads) {  // two loads in flight
+            float x[8], y[8];
+            load8(t_row + v, x);
+            load8(t_row + v + 8 * kRowThreads, y);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) softmax_push(st, elem(t4, e) * inv_t);
+            for (int e = 0; e < 8; ++e) {
+                x[e] *= c2;
+                y[e] *= c2;
+            }
+            softmax_push_group<8>(st, x, 8);
+            softmax_push_group<8>(st, y, 8);
+        }
+        if (v < ve) {
+            float x[8];
+            load8(t_row + v, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] *= c2;
+            softmax_push_group<8>(st, x, 8);
         }
     } else if (T > 0.f) {  // j == L: bonus draw
-        for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kRowThreads) {
-            const float4 t4 = load4(t_row + v);
-            const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, id, kStreamBonus), k0, k1);
+        for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {
+            float x[8];
+            load8(t_row + v, x);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) gumbel_push(st, elem(t4, e) * inv_t, word_of(w4, e), v + e);
+            for (int h = 0; h < 2; ++h) {
+                const uint4 w4 = philox4x32_10(
+                    make_uint4(((uint32_t)v >> 2) + h, (uint32_t)j, id, kStreamBonus), k0, k1);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) gumbel_push(st, x[4 * h + e] * c2, word_of(w4, e), v + 4 * h + e);
+            }
         }
     } else {  // greedy request
-        for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kRowThreads) {
-            const float4 t4 = load4(t_row + v);
+        for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {
+            float x[8];
+            load8(t_row + v, x);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) argmax_push(st, elem(t4, e), v + e);
+            for (int e = 0; e < 8; ++e) argmax_push(st, x[e], v + e);
         }
     }
     st = block_merge(st, scratch);
@@ -157,7 +168,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         }
         if (bad && lane == 0) atomicOr(flags, kFlagBadToken);
     }
-    // clear the optional per-row outputs of this request
+    // clear the per-row outputs of this request
     for (int j = lane; j <= G; j += 32) {
         out_tokens[(size_t)b * (G + 1) + j] = -1;
         if (target_lse) target_lse[(size_t)b * (G + 1) + j] = nan;
@@ -172,7 +183,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         }
         return;
     }
-    const float inv_t = T > 0.f ? 1.0f / T : 0.f;
+    const float c2 = T > 0.f ? kLog2e / T : 0.f;
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     int k = 0, y = -1, d = -1;
     for (int j = 0; j < L; ++j) {
@@ -182,20 +193,20 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         s = warp_merge(s);
         const int x = draft_tokens[(size_t)b * G + j];
         if (T > 0.f) {
-            const float lse_t = s.m + logf(s.S);
+            const float lse2 = s.m + log2f(s.S);
             const float tx = to_f32(target[((size_t)b * (G + 1) + j) * V + x]);
-            const float logp = tx * inv_t - lse_t;
+            const float logp = kLn2 * (fmaf(tx, c2, -s.m) - log2f(s.S));
             const float logq = draft_logq[(size_t)b * G + j];
             const uint4 w4 = philox4x32_10(make_uint4(0u, (uint32_t)j, id, kStreamAccept), k0, k1);
             const float u = word_to_uniform(w4.x);
             const bool accept = u < expf(logp - logq);
             if (lane == 0) {
-                if (target_lse) target_lse[(size_t)b * (G + 1) + j] = lse_t;
+                if (target_lse) target_lse[(size_t)b * (G + 1) + j] = kLn2 * lse2;
                 if (logp_sel) logp_sel[(size_t)b * G + j] = logp;
             }
             if (!accept) {
                 d = j;
-                if (lane == 0) lse_t_row[b] = lse_t;
+                if (lane == 0) lse_t_row[b] = lse2;
                 break;
             }
         } else {
@@ -227,27 +238,29 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
     }
 }
 
-// ---------------------------------------------------------------- pass 3 ----
+// ------------------------------------------------- pass 3 (SIMT / stored) ----
+// Residual draw with the draft logits of the rejected row taken from the
+// stored draft logits (any dtype) or rebuilt with CUDA-core FMAs (fp32).
 template <typename TIn>
 __global__ void __launch_bounds__(kResThreads)
-verify_residual_kernel(const TIn *__restrict__ target, const TIn *__restrict__ base,
-                       const TIn *__restrict__ e_in, const TIn *__restrict__ w_out,
-                       const float *__restrict__ z_in, const int32_t *__restrict__ anchor,
-                       const int32_t *__restrict__ draft_tokens, const float *__restrict__ draft_lse,
-                       const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
-                       const int32_t *__restrict__ res_row, const float *__restrict__ lse_t_row,
-                       int B, int G, int V, int r, uint32_t k0, uint32_t k1, int chunk, int nsplit,
-                       ResidualState *__restrict__ part) {
+verify_residual_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__ base,
+                            const TIn *__restrict__ e_in, const TIn *__restrict__ w_out,
+                            const float *__restrict__ z_in, const int32_t *__restrict__ anchor,
+                            const int32_t *__restrict__ draft_tokens, const float *__restrict__ draft_lse,
+                            const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
+                            const int32_t *__restrict__ res_row, const float *__restrict__ lse_t_row,
+                            int B, int G, int V, int r, uint32_t k0, uint32_t k1, int chunk, int nsplit,
+                            ResidualState *__restrict__ part) {
     extern __shared__ float a_row[];  // [r]
     __shared__ ResidualState scratch[kResThreads / 32];
     const int b = blockIdx.y;
     const int d = res_row[b];
     if (d < 0) return;
     const int seg = blockIdx.x;
-    const float inv_t = 1.0f / temperature[b];
+    const float c2 = kLog2e / temperature[b];
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
-    const float lse_q = draft_lse[(size_t)b * G + d];
-    const float lse_t = lse_t_row[b];
+    const float lse_q2 = draft_lse[(size_t)b * G + d] * kLog2e;
+    const float lse_t2 = lse_t_row[b];
     const int prev = (d == 0) ? anchor[b] : draft_tokens[(size_t)b * G + d - 1];
     if (!z_in) {
         for (int k = threadIdx.x; k < r; k += blockDim.x) a_row[k] = to_f32(e_in[(size_t)prev * r + k]);
@@ -265,13 +278,18 @@ verify_residual_kernel(const TIn *__restrict__ target, const TIn *__restrict__ b
             z[0] = z4.x; z[1] = z4.y; z[2] = z4.z; z[3] = z4.w;
         } else {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < r; ++k) {
-                const float4 w = load4(w_out + (size_t)k * V + v);
-                const float a = a_row[k];
-                acc[0] = fmaf(a, w.x, acc[0]);
-                acc[1] = fmaf(a, w.y, acc[1]);
-                acc[2] = fmaf(a, w.z, acc[2]);
-                acc[3] = fmaf(a, w.w, acc[3]);
+            for (int k = 0; k < r; k += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(a_row + k);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 w = load4(w_out + (size_t)(v + e) * r + k);
+                    float t = acc[e];
+                    t = fmaf(a.x, w.x, t);
+                    t = fmaf(a.y, w.y, t);
+                    t = fmaf(a.z, w.z, t);
+                    t = fmaf(a.w, w.w, t);
+                    acc[e] = t;
+                }
             }
             const float4 u4 = load4(base + drow * V + v);
 #pragma unroll
@@ -282,21 +300,28 @@ verify_residual_kernel(const TIn *__restrict__ target, const TIn *__restrict__ b
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float t = elem(t4, e);
-            const float ln_e = logf(neg_log_uniform(word_of(w4, e)));
-            // log p - log q, formed from the difference of the logits first
-            const float delta = fmaf(t - z[e], inv_t, lse_q - lse_t);
-            if (delta > 0.f) {
-                const float logq = fmaf(z[e], inv_t, -lse_q);
-                const float key = logq + logf(expm1f(delta)) - ln_e;
-                if (key_better(key, v + e, st.key_res, st.idx_res)) {
-                    st.key_res = key;
-                    st.idx_res = v + e;
+            const uint32_t word = word_of(w4, e);
+            const float lw = fast_log2(word_to_one_minus_uniform(word));
+            // log2 p - log2 q, from the logit difference first
+            const float delta2 = fmaf(t - z[e], c2, lse_q2 - lse_t2);
+            if (delta2 > 0.f) {
+                const float l1 = delta2 > 20.f ? delta2 : fast_log2(expm1f(delta2 * kLn2));
+                const float base_r = fmaf(z[e], c2, -lse_q2) + l1;
+                if (lw < base_r - st.key_res + 1e-4f) {
+                    const float key = base_r - fast_log2(neg_log_uniform(word));
+                    if (key_better(key, v + e, st.key_res, st.idx_res)) {
+                        st.key_res = key;
+                        st.idx_res = v + e;
+                    }
                 }
             }
-            const float key_p = t * inv_t - ln_e;
-            if (key_better(key_p, v + e, st.key_p, st.idx_p)) {
-                st.key_p = key_p;
-                st.idx_p = v + e;
+            const float base_p = t * c2;
+            if (lw < base_p - st.key_p + 1e-4f) {
+                const float key = base_p - fast_log2(neg_log_uniform(word));
+                if (key_better(key, v + e, st.key_p, st.idx_p)) {
+                    st.key_p = key;
+                    st.idx_p = v + e;
+                }
             }
         }
     }
@@ -350,15 +375,25 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
         a.request_id, a.B, a.G, a.V, k0, k1, a.accept_len, a.out_tokens, a.num_out, a.target_lse,
         a.logp_sel, res_row, lse_t_row, flags);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t smem = a.z_in ? 0 : sizeof(float) * (size_t)a.r;
-    verify_residual_kernel<TIn><<<dim3(p.res_split, a.B), kResThreads, smem, s>>>(
-        target, static_cast<const TIn *>(a.base), static_cast<const TIn *>(a.e_in),
-        static_cast<const TIn *>(a.w_out), a.z_in, a.anchor, a.draft_tokens, a.draft_lse,
-        a.temperature, a.request_id, res_row, lse_t_row, a.B, a.G, a.V, a.r, k0, k1, p.res_chunk,
-        p.res_split, res_part);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const bool tensor = p.tensor_residual && !a.z_in;
+    const int res_nsplit = tensor ? p.res_split_tc : p.res_split;
+    if (tensor) {
+        ResidualArgs ra{a.target, a.base, a.e_in, a.w_out, a.anchor, a.draft_tokens, a.temperature,
+                        a.request_id, res_row, lse_t_row, a.draft_lse, a.B, a.G, a.V, a.r, res_nsplit,
+                        a.seed, res_part, flags};
+        e = launch_residual_tensor(ra, s);
+    } else {
+        const size_t smem = a.z_in ? 0 : sizeof(float) * (size_t)a.r;
+        verify_residual_simt_kernel<TIn><<<dim3(p.res_split, a.B), kResThreads, smem, s>>>(
+            target, static_cast<const TIn *>(a.base), static_cast<const TIn *>(a.e_in),
+            static_cast<const TIn *>(a.w_out), a.z_in, a.anchor, a.draft_tokens, a.draft_lse,
+            a.temperature, a.request_id, res_row, lse_t_row, a.B, a.G, a.V, a.r, k0, k1, p.res_chunk,
+            p.res_split, res_part);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     verify_residual_finalize_kernel<<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
-        res_part, p.res_split, res_row, a.accept_len, a.B, a.G, a.out_tokens);
+        res_part, res_nsplit, res_row, a.accept_len, a.B, a.G, a.out_tokens);
     return cudaGetLastError();
 }
 
@@ -369,23 +404,28 @@ cudaError_t launch_verify(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t
     return launch_verify_t<float>(a, p, s);
 }
 
-VerifyPlan plan_verify(int B, int G, int V, int r) {
+VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {
     (void)r;
     VerifyPlan p{};
     const long rows = (long)B * (G + 1);
-    // about 4 blocks per SM over the target rows, segments of >= 2048 entries
-    long want = (4L * kNumSMs + rows - 1) / rows;
-    int max_split = (V + 2047) / 2048;
+    // target rows: aim for ~8 blocks per SM among the rows that are read
+    // (about half of them with scheduled lengths), segments >= 4096 entries
+    long want = (16L * kNumSMs + rows - 1) / rows;
+    int max_split = (V + 4095) / 4096;
     int split = (int)(want < 1 ? 1 : (want > max_split ? max_split : want));
-    int chunk = ((V + split - 1) / split + 3) / 4 * 4;
+    int chunk = ((V + split - 1) / split + 7) / 8 * 8;
     p.row_split = (V + chunk - 1) / chunk;
     p.row_chunk = chunk;
+    // residual rows: the tensor-core kernel's segments (bf16), else SIMT segments
+    p.tensor_residual = (dt == DSPARK_BF16);
     long want_r = (2L * kNumSMs + B - 1) / B;
     int max_r = (V + 1023) / 1024;
     int rs = (int)(want_r < 1 ? 1 : (want_r > max_r ? max_r : want_r));
     int rchunk = ((V + rs - 1) / rs + 3) / 4 * 4;
-    p.res_split = (V + rchunk - 1) / rchunk;
     p.res_chunk = rchunk;
+    p.res_split = (V + rchunk - 1) / rchunk;
+    p.res_split_tc = p.tensor_residual ? tc_segments(B, V) : 0;
+    const int res_slots = p.res_split > p.res_split_tc ? p.res_split : p.res_split_tc;
     size_t off = kFlagBytes;
     p.row_part_offset = off;
     off = align_up(off + sizeof(RowState) * (size_t)rows * p.row_split, 256);
@@ -394,7 +434,7 @@ VerifyPlan plan_verify(int B, int G, int V, int r) {
     p.lse_t_offset = off;
     off = align_up(off + sizeof(float) * (size_t)B, 256);
     p.res_part_offset = off;
-    off = align_up(off + sizeof(ResidualState) * (size_t)B * p.res_split, 256);
+    off = align_up(off + sizeof(ResidualState) * (size_t)B * res_slots, 256);
     p.ws_bytes = off;
     return p;
 }

@@ -11,7 +11,7 @@ distributions follow the five workloads the library is measured on:
   highconc   B=1024 G=4   V=129280  r=256  bf16  T~U[0.3,1.2], t=U+N(0,sigma_b^2),
                                                   sigma_b~U[0.2,2], scheduler on
 
-E_in (V x r) and W_out (r x V) are N(0, 0.02^2).  Confidence logits are
+E_in and W_out (both V x r; W_out row v scores token v) are N(0, 0.02^2).  Confidence logits are
 N(1, 1); the per-position calibration temperatures are evenly spaced in
 [1, 2]; the batch-token throughput table is SPS(n) = 1 / (1 + n / 512).
 """
@@ -70,7 +70,7 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", request_id_base: int =
     """Draw one block's inputs for every request of workload ``w``.
 
     Returns a dict of tensors on ``device``:
-      base [B,G,V], target [B,G+1,V], e_in [V,r], w_out [r,V] (workload dtype),
+      base [B,G,V], target [B,G+1,V], e_in [V,r], w_out [V,r] (workload dtype),
       anchor [B] i32, temperature [B] f32, request_id [B] u32 (as int32 storage),
       conf_logits [B,G] f32, pos_temp [G] f32, sps [B*(G+1)+1] f32.
     """
@@ -96,7 +96,7 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", request_id_base: int =
     del base_ext
 
     e_in = (torch.randn((V, r), generator=g, device=device, dtype=f32) * 0.02).to(dt).contiguous()
-    w_out = (torch.randn((r, V), generator=g, device=device, dtype=f32) * 0.02).to(dt).contiguous()
+    w_out = (torch.randn((V, r), generator=g, device=device, dtype=f32) * 0.02).to(dt).contiguous()
     anchor = torch.randint(0, V, (B,), generator=g, device=device, dtype=torch.int32)
 
     if w.temp == "one":

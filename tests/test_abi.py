@@ -64,6 +64,7 @@ def _call_draft(**over):
     (dict(r=0), "r must be"),
     (dict(dt=0, r=24), "r % 16"),
     (dict(dt=5), "unknown dtype"),
+    (dict(dt=1, r=6), "r % 4"),
     (dict(base=None), "NULL"),
     (dict(base=(1 << 12) + 4), "aligned"),
     (dict(ws=None), "workspace is NULL"),

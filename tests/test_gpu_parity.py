@@ -161,7 +161,7 @@ def test_edge_cases_lengths_and_greedy():
 
 
 def test_minimal_sizes():
-    w = WORKLOADS["tiny"].scaled(B=1, G=1, V=8, r=1)
+    w = WORKLOADS["tiny"].scaled(B=1, G=1, V=8, r=4)
     tally, *_ = full_parity(w, 0)
     tally.check()
     w2 = WORKLOADS["dspark5"].scaled(B=1, G=1, V=8, r=16, scheduler=False)

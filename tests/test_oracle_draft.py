@@ -30,7 +30,7 @@ def test_constant_row_closed_form():
     V, r = 1000, 4
     U = np.full((1, 1, V), 2.5)
     E = np.zeros((V, r))
-    W = np.zeros((r, V))
+    W = np.zeros((V, r))
     d = oracle.draft_sample(U, E, W, [0], [1.0])
     assert d["lse"][0, 0] == pytest.approx(2.5 + math.log(V), abs=1e-12)
     assert d["logq"][0, 0] == pytest.approx(-math.log(V), abs=1e-12)
@@ -41,7 +41,7 @@ def test_single_spike_dominates_at_low_temperature():
     U = np.zeros((3, 1, V))
     for b, spike in enumerate((7, 300, 511)):
         U[b, 0, spike] = 5.0
-    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((r, V)), [0, 0, 0], [0.05, 0.05, 0.05])
+    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((V, r)), [0, 0, 0], [0.05, 0.05, 0.05])
     assert list(d["tokens"][:, 0]) == [7, 300, 511]
     # logq = -log(1 + (V-1) exp(-100)) ~ 0
     assert np.all(np.abs(d["logq"]) < 1e-30)
@@ -52,25 +52,25 @@ def test_greedy_ties_take_lowest_id():
     U = np.zeros((1, 2, V))
     U[0, 0, [5, 9, 40]] = 3.0
     U[0, 1, [63, 2]] = 1.0
-    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((r, V)), [1], [0.0])
+    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((V, r)), [1], [0.0])
     assert list(d["tokens"][0]) == [5, 2]
     assert d["lse"][0, 0] == 3.0 and d["logq"][0, 0] == 0.0
     assert d["gap"][0, 0] == 0.0
 
 
 def test_markov_logits_equal_library_matmul():
-    # z = fp32(U + E_in[prev] @ W_out), prev = anchor then the drawn tokens
+    # z = fp32(U + W_out @ E_in[prev]), prev = anchor then the drawn tokens
     rng = np.random.default_rng(3)
     B, G, V, r = 3, 4, 97, 8
     U = rng.normal(0, 2, (B, G, V))
     E = rng.normal(0, 0.3, (V, r))
-    W = rng.normal(0, 0.3, (r, V))
+    W = rng.normal(0, 0.3, (V, r))
     anchor = np.array([0, 50, 96])
     d = oracle.draft_sample(U, E, W, anchor, [1.0, 0.0, 0.7], seed=9, want_z=True)
     for b in range(B):
         prev = anchor[b]
         for j in range(G):
-            want = (U[b, j] + np.matmul(E[prev], W)).astype(np.float32).astype(np.float64)
+            want = (U[b, j] + np.matmul(W, E[prev])).astype(np.float32).astype(np.float64)
             np.testing.assert_allclose(d["z"][b, j], want, rtol=0, atol=1e-6)
             prev = d["tokens"][b, j]
 
@@ -80,7 +80,7 @@ def test_gumbel_max_matches_softmax_distribution():
     rng = np.random.default_rng(4)
     row = rng.normal(0, 1.5, V)
     U = np.broadcast_to(row, (N, 1, V)).copy()
-    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((r, V)), np.zeros(N, np.int32),
+    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((V, r)), np.zeros(N, np.int32),
                             np.full(N, T), rid=np.arange(N), seed=11)
     counts = np.bincount(d["tokens"][:, 0], minlength=V)
     ok, chi2 = _chi2_ok(counts, _softmax(row / T), N)
@@ -96,20 +96,20 @@ def test_second_position_conditions_on_first_draw():
     row0 = rng.normal(0, 1, V)
     row1 = rng.normal(0, 1, V)
     E = rng.normal(0, 1.0, (V, r))
-    W = rng.normal(0, 1.0, (r, V))
+    W = rng.normal(0, 1.0, (V, r))
     U = np.empty((N, 2, V))
     U[:, 0] = row0
     U[:, 1] = row1
     anchor = np.full(N, 2, np.int32)
     d = oracle.draft_sample(U, E, W, anchor, np.full(N, T), rid=np.arange(N), seed=21)
     x0, x1 = d["tokens"][:, 0], d["tokens"][:, 1]
-    ok, chi2 = _chi2_ok(np.bincount(x0, minlength=V), _softmax((row0 + E[2] @ W) / T), N)
+    ok, chi2 = _chi2_ok(np.bincount(x0, minlength=V), _softmax((row0 + W @ E[2]) / T), N)
     assert ok, chi2
     for a in range(V):
         sel = x0 == a
         if sel.sum() < 2000:
             continue
-        want = _softmax((row1 + E[a] @ W) / T)
+        want = _softmax((row1 + W @ E[a]) / T)
         ok, chi2 = _chi2_ok(np.bincount(x1[sel], minlength=V), want, sel.sum())
         assert ok, (a, chi2)
 
@@ -117,7 +117,7 @@ def test_second_position_conditions_on_first_draw():
 def test_request_id_and_seed_select_independent_streams():
     V, r = 256, 2
     U = np.zeros((2, 3, V))
-    kw = dict(E_in=np.zeros((V, r)), W_out=np.zeros((r, V)), anchor=[0, 0], temp=[1.0, 1.0])
+    kw = dict(E_in=np.zeros((V, r)), W_out=np.zeros((V, r)), anchor=[0, 0], temp=[1.0, 1.0])
     a = oracle.draft_sample(U, rid=[5, 5], seed=1, **kw)["tokens"]
     b = oracle.draft_sample(U, rid=[5, 6], seed=1, **kw)["tokens"]
     c = oracle.draft_sample(U, rid=[5, 5], seed=2, **kw)["tokens"]

@@ -56,7 +56,7 @@ def _run(p_rows, q_rows, N, seed, temp=1.0, L=None):
     U = np.broadcast_to(np.log(np.asarray(q_rows)) * temp, (N, G, V)).copy()
     tgt = np.broadcast_to(np.log(np.asarray(p_rows)) * temp, (N, G + 1, V)).copy()
     E = np.zeros((V, r))
-    W = np.zeros((r, V))
+    W = np.zeros((V, r))
     anchor = np.zeros(N, np.int32)
     temps = np.full(N, temp)
     rid = np.arange(N)
@@ -164,12 +164,12 @@ def test_oracle_output_is_distributed_as_target():
     """End to end through the oracle: Markov draft, prefix-dependent target."""
     V, N, T, seed = 4, 400000, 1.0, 17
     p0, p1, p2, q0, q1 = _toy_tables(11, V)
-    # draft: U row 0 = log q0; row 1 = 0 plus bias E_in[x0] @ W_out = log q1[x0]
+    # draft: U row 0 = log q0; row 1 = 0 plus bias W_out @ E_in[x0] = log q1[x0]
     r = V
     E = np.eye(V)
-    W = np.log(q1)
+    W = np.log(q1).T          # W_out[v, k] = log q1[k][v]
     U = np.zeros((N, 2, V))
-    U[:, 0] = np.log(q0) - (E[0] @ W)      # position 0 is biased by the anchor (token 0)
+    U[:, 0] = np.log(q0) - (W @ E[0])      # position 0 is biased by the anchor (token 0)
     anchor = np.zeros(N, np.int32)
     temps = np.full(N, T)
     rid = np.arange(N)
@@ -218,7 +218,7 @@ def test_greedy_limit_is_argmax_prefix_match():
     # request 2: verify length 2; bonus from row 2 (argmax 6)
     for j, tok in enumerate((3, 5, 6, 0, 0)):
         tgt[2, j, tok] = 2.0
-    E, W = np.zeros((V, r)), np.zeros((r, V))
+    E, W = np.zeros((V, r)), np.zeros((V, r))
     anchor = np.zeros(3, np.int32)
     temps = np.zeros(3)
     d = oracle.draft_sample(U, E, W, anchor, temps)
@@ -238,7 +238,7 @@ def test_verify_length_zero_emits_one_target_token():
     p = _softmax(rng.normal(0, 1, V))
     U = np.zeros((N, G, V))
     tgt = np.broadcast_to(np.log(p), (N, G + 1, V)).copy()
-    E, W = np.zeros((V, r)), np.zeros((r, V))
+    E, W = np.zeros((V, r)), np.zeros((V, r))
     anchor = np.zeros(N, np.int32)
     temps = np.ones(N)
     d = oracle.draft_sample(U, E, W, anchor, temps, rid=np.arange(N), seed=2)
@@ -258,14 +258,14 @@ def test_markov_head_fixes_the_multimodal_collision():
     for head in ("parallel", "markov"):
         r = V
         E = np.eye(V)
-        W = np.zeros((r, V))
+        W = np.zeros((V, r))
         if head == "markov":
-            W[0] = [0.0, big / 2, 0.0, -big / 2]
-            W[2] = [0.0, -big / 2, 0.0, big / 2]
+            W[:, 0] = [0.0, big / 2, 0.0, -big / 2]
+            W[:, 2] = [0.0, -big / 2, 0.0, big / 2]
         U = np.zeros((N, 2, V))
         U[:, 0] = p0
         U[:, 1] = [-big, 0.0, -big, 0.0]
-        anchor = np.full(N, 1, np.int32)     # the anchor token adds no bias (W[1] = 0)
+        anchor = np.full(N, 1, np.int32)     # the anchor token adds no bias (W[:, 1] = 0)
         temps = np.ones(N)
         rid = np.arange(N)
         d = oracle.draft_sample(U, E, W, anchor, temps, rid=rid, seed=4)
