@@ -19,7 +19,8 @@
  *    allocates or frees memory.  Pointers to logits, E_in and W_out must be
  *    16-byte aligned; V must be a multiple of 8.
  *  - "dtype" arrays hold bf16 (DSPARK_BF16) or fp32 (DSPARK_F32) values; all
- *    arithmetic is fp32 on the device (the scheduler uses fp64).
+ *    arithmetic is fp32 on the device (the scheduler sums tau and Theta in
+ *    fp64).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Calls only enqueue work: they do not synchronise.
  *  - `workspace` is caller-owned device scratch memory of at least
@@ -153,7 +154,7 @@ DSPARK_API dspark_status dspark_draft_sample(
  * B * (L_max + 1) + 1.  Outputs: conf, cum_conf [B][G] fp32, verify_len [B]
  * int32, theta_out [1] fp64 (final Theta) or NULL.
  * Limits: 0 <= L_min <= L_max <= G <= 64, B * G <= 16384.
- * Confidences and Theta are computed in fp64.
+ * c and a are computed in fp32; tau and Theta are accumulated in fp64.
  */
 DSPARK_API dspark_status dspark_schedule_prefix(
     const float *conf_logits, const float *pos_temp, const float *sps, int sps_len,

@@ -51,6 +51,34 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
+// Philox4x32-10 round keys: k0 + r W0, k1 + r W1 for r = 0..9.
+struct PhiloxRoundKeys {
+    uint32_t k0[10];
+    uint32_t k1[10];
+};
+
+// Philox4x32-10 for counter (x0, pos, rid, stream) with the parts of round 1
+// that do not depend on x0 precomputed per request:
+//   y0c = hi(M1 rid) ^ pos ^ k0[0],  y1c = lo(M1 rid),  sk = stream ^ k1[0].
+// Same words as philox4x32_10(make_uint4(x0, pos, rid, stream), k0, k1).
+__device__ __forceinline__ uint4 philox_folded(uint32_t x0, uint32_t y0c, uint32_t y1c, uint32_t sk,
+                                               const PhiloxRoundKeys &K) {
+    const uint64_t p = (uint64_t)kPhiloxM0 * x0;
+    uint32_t c0 = y0c, c1 = y1c, c2 = (uint32_t)(p >> 32) ^ sk, c3 = (uint32_t)p;
+#pragma unroll
+    for (int r = 1; r < 10; ++r) {
+        const uint64_t pa = (uint64_t)kPhiloxM0 * c0;
+        const uint64_t pb = (uint64_t)kPhiloxM1 * c2;
+        const uint32_t n0 = (uint32_t)(pb >> 32) ^ c1 ^ K.k0[r];
+        const uint32_t n2 = (uint32_t)(pa >> 32) ^ c3 ^ K.k1[r];
+        c1 = (uint32_t)pb;
+        c3 = (uint32_t)pa;
+        c0 = n0;
+        c2 = n2;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &w, int e) {
     return e == 0 ? w.x : (e == 1 ? w.y : (e == 2 ? w.z : w.w));
 }
@@ -63,6 +91,14 @@ __device__ __forceinline__ float word_to_uniform(uint32_t w) {
 // 1 - u, exact: (2 - 2^-24) - (1 + k 2^-23).
 __device__ __forceinline__ float word_to_one_minus_uniform(uint32_t w) {
     return 0x1.fffffep+0f - __uint_as_float(0x3F800000u | (w >> 9));
+}
+
+// f1 = 1 + k' 2^-23 with k' = 0x7FFFFF - (w >> 9), which equals
+// (1 - u) + 1 - 2^-24 exactly.  The test f1 < fl(t + 1) is a conservative form
+// of (1 - u) < t: fl(t + 1) >= t + 1 - 2^-24 whenever t < 1 (round to
+// nearest), and for t >= 1 both sides pass, so no true "yes" is lost.
+__device__ __forceinline__ float one_minus_uniform_plus_one(uint32_t w) {
+    return __uint_as_float(0x3F800000u | ((~w) >> 9));
 }
 
 // Exponential variate E = -ln u (relative accuracy matters: small E wins).

@@ -55,8 +55,10 @@ int tc_row_blocks(int B);
 int tc_segments(int B, int V);
 size_t tc_residual_state_bytes();
 
-// residual resampling of the rejected rows on the tensor cores
-struct ResidualArgs {
+// final draw of verification on the tensor cores: residual rows (rejected at
+// position d, draft logits rebuilt with the Markov bias) and bonus rows
+// (fully accepted, Gumbel-max over target row L)
+struct FinalArgs {
     const void *target;
     const void *base;
     const void *e_in;
@@ -65,15 +67,15 @@ struct ResidualArgs {
     const int32_t *tokens;
     const float *temperature;
     const uint32_t *request_id;
-    const int32_t *res_row;    // [B] rejected position or -1
-    const float *lse_t_row;    // [B] target lse of that row, log2 units
+    const int32_t *final_code; // [B]: -1, (1 << 16) | d residual, (2 << 16) | L bonus
+    const float *lse_t_row;    // [B] target lse of the rejected row, log2 units
     const float *draft_lse;    // [B][G] natural log
     int B, G, V, r, nseg;
     uint64_t seed;
-    void *rpart;               // [B][nseg] residual partials
+    void *rpart;               // [B][nseg] final-draw partials
     uint32_t *flags;
 };
-cudaError_t launch_residual_tensor(const ResidualArgs &a, cudaStream_t s);
+cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s);
 
 // --------------------------------------------------------------- verify ----
 struct VerifyPlan {

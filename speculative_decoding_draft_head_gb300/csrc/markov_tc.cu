@@ -9,13 +9,16 @@
 // TMEM epilogue so that each logit is produced and consumed on chip.
 //
 // Two uses share the kernel:
-//  - draft:    rows = 128 requests at block position j; reads the base logits
-//              tile by TMA; writes per-(request, segment) softmax/argmax
-//              partials (draft_finalize merges them and writes x_j, which the
-//              next position's launch gathers);
-//  - residual: rows = 128 requests, each at its own rejected position d_b
-//              (rows without a rejection idle); reads base and target logits
-//              directly and draws from max(0, p - q) by Gumbel-max.
+//  - draft: rows = 128 requests at block position j; base-logit tiles come
+//    by TMA; the kernel writes per-(request, segment) softmax/argmax partials
+//    (draft_finalize merges them and writes x_j, which the next position's
+//    launch gathers);
+//  - final draw of verification ("Les mathematiques derriere l'acceleration",
+//    section "La garantie de l'echantillonnage par rejet", and "DeepSeek发布
+//    DSpark", section "DSpark 是什么？"): each row is a request that either
+//    rejected at position d (draw from max(0, p_d - q_d), q rebuilt from base
+//    logits + Markov bias) or accepted its whole block (bonus draw from p_L);
+//    other rows idle.  Base and target rows are read directly, one tile ahead.
 //
 // CTA layout (one CTA per SM, 576 threads, ~196 KB shared memory):
 //   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant of
@@ -27,6 +30,12 @@
 // CTA in the 128-byte swizzled K-major layout.  Rings: 2 W stages, 3 base
 // stages, 4 TMEM accumulators of 64 columns.  Every wait is bounded; a timeout
 // sets the timeout bit of the flag word and the CTA unwinds.
+//
+// Gumbel-max without a logarithm per token: token v beats the running best
+// key K iff E_v < 2^(s2_v - K) = e_v * 2^(m - K), where e_v = 2^(s2_v - m) is
+// the softmax term already computed and E_v = -ln u_v >= 1 - u_v.  So the test
+// (1 - u_v) < e_v * Q with Q = 2^(m - K) (plus a 1e-4 margin) rejects almost
+// every token exactly; only the survivors evaluate -ln u_v and the exact key.
 #include <climits>
 #include <mutex>
 
@@ -67,6 +76,8 @@ constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of clock cycles
+constexpr float kQMax = 0x1p126f;
+constexpr float kMargin = 1.0001f;
 
 struct TcParams {
     const __nv_bfloat16 *e_in;
@@ -76,11 +87,11 @@ struct TcParams {
     const int32_t *tokens;
     const float *temperature;
     const uint32_t *request_id;
-    const int32_t *res_row;
-    const float *lse_t_row;   // log2 units
-    const float *draft_lse;   // natural log
+    const int32_t *final_code;  // [B]: -1, or (kind << 16) | position
+    const float *lse_t_row;     // [B] target lse of the rejected row, log2 units
+    const float *draft_lse;     // [B][G] natural log
     int B, G, V, r, j, nseg;
-    uint32_t k0, k1;
+    PhiloxRoundKeys keys;
     RowState *part;
     ResidualState *rpart;
     uint32_t *flags;
@@ -97,10 +108,86 @@ __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, vola
     return __all_sync(0xffffffffu, ok);
 }
 
-template <bool kResidual>
+__device__ __forceinline__ void unpack16(const uint4 &lo, const uint4 &hi, float (&x)[16]) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w[i]);
+        x[2 * i + 1] = bf16_hi(w[i]);
+    }
+}
+
+// 16 bf16 values starting at p (n valid; the rest read as 0).
+__device__ __forceinline__ void load16_bf16(const __nv_bfloat16 *p, int n, uint4 &lo, uint4 &hi) {
+    if (n >= 16) {
+        lo = __ldg(reinterpret_cast<const uint4 *>(p));
+        hi = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+    } else {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = (2 * i < n) ? (uint32_t)__bfloat16_as_ushort(p[2 * i]) : 0u;
+            const uint32_t b = (2 * i + 1 < n) ? (uint32_t)__bfloat16_as_ushort(p[2 * i + 1]) : 0u;
+            w[i] = a | (b << 16);
+        }
+        lo = make_uint4(w[0], w[1], w[2], w[3]);
+        hi = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+// Draft epilogue for 16 logits of one row (T > 0).
+__device__ __forceinline__ void draft_sample16(RowState &st, float &Q, const float (&z)[16], float c2, int n, int v,
+                                               uint32_t y0c, uint32_t y1c, uint32_t sk, const PhiloxRoundKeys &K) {
+    float s2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s2[i] = z[i] * c2;
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (i < n) cm = fmaxf(cm, s2[i]);
+    if (cm > st.m) {
+        st.S *= fast_exp2(st.m - cm);
+        st.m = cm;
+        Q = fminf(fast_exp2(cm - st.key), kQMax) * kMargin;
+    }
+    float e[16];
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        e[i] = (i < n) ? fast_exp2(s2[i] - st.m) : 0.f;
+        sum += e[i];
+    }
+    st.S += sum;
+    uint4 w[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)v >> 2) + g, y0c, y1c, sk, K);
+    bool cand[16];
+    bool any = false;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        cand[i] = one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(e[i], Q, 1.f);
+        any |= cand[i];
+    }
+    if (any) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (cand[i]) {
+                const float key = s2[i] - fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
+                if (key > st.key) {
+                    st.key = key;
+                    st.s_at = s2[i];
+                    st.idx = v + i;
+                    Q = fminf(fast_exp2(st.m - key), kQMax) * kMargin;
+                }
+            }
+        }
+    }
+}
+
+template <bool kFinal>
 __global__ void __launch_bounds__(kThreads, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
-                 const TcParams p) {
+                 const __grid_constant__ TcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -126,7 +213,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     int *row_prev = misc + 4;
     float *row_c2 = reinterpret_cast<float *>(misc + 4 + BM);
     uint32_t *row_rid = reinterpret_cast<uint32_t *>(misc + 4 + 2 * BM);
-    int *row_aux = misc + 4 + 3 * BM;
+    int *row_code = misc + 4 + 3 * BM;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWStages; ++s) {
@@ -150,18 +237,18 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     }
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&map_w);
-        if (!kResidual) tma_prefetch_desc(&map_u);
+        if (!kFinal) tma_prefetch_desc(&map_u);
     }
     if (threadIdx.x < BM) {
         const int b = m0 + threadIdx.x;
-        int prev = -1, aux = -1;
+        int prev = -1, code = -1;
         float c2 = 0.f;
         uint32_t id = 0;
         if (b < p.B) {
             const float T = p.temperature[b];
             id = p.request_id ? p.request_id[b] : (uint32_t)b;
             const bool t_ok = T >= 0.f && !isinf(T);
-            if (!kResidual) {
+            if (!kFinal) {
                 prev = (p.j == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + p.j - 1];
                 const bool bad = prev < 0 || prev >= p.V;
                 if (bad && (p.j == 0 || prev != -1) && seg == 0) atomicOr(p.flags, kFlagBadToken);
@@ -169,10 +256,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 if (bad || !t_ok) prev = -1;
                 c2 = (T > 0.f) ? kLog2e / T : 0.f;
             } else {
-                const int d = p.res_row[b];
-                if (d >= 0) {  // validated by the decide kernel
-                    prev = (d == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + d - 1];
-                    aux = d;
+                code = p.final_code[b];  // validated by the decide kernel
+                if (code >= 0) {
+                    const int d = code & 0xFFFF;
+                    if ((code >> 16) == 1) prev = (d == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + d - 1];
                     c2 = kLog2e / T;
                 }
             }
@@ -180,7 +267,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         row_prev[threadIdx.x] = prev;
         row_c2[threadIdx.x] = c2;
         row_rid[threadIdx.x] = id;
-        row_aux[threadIdx.x] = aux;
+        row_code[threadIdx.x] = code;
     }
     __syncthreads();
 
@@ -220,7 +307,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 for (int kb = 0; kb < n_katoms; ++kb)
                     tma_load_2d(sbase + kOffW + ws * 4 * kAtomW + kb * kAtomW, &map_w, full_w(ws), kb * 64, v0,
                                 pol_w);
-                if (!kResidual) {
+                if (!kFinal) {
                     const int us = t % kUStages;
                     const uint32_t uph = (uint32_t)(t / kUStages) & 1u;
                     if (t >= kUStages && !mbar_wait(empty_u(us), uph ^ 1u, abort, kSpinLimit)) {
@@ -270,16 +357,41 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const int prev = row_prev[row];
         const float c2 = row_c2[row];
         const uint32_t rid = row_rid[row];
-        const int d = row_aux[row];
-        const bool active = kResidual ? (d >= 0) : (prev >= 0);
+        const int code = row_code[row];
+        const int kind = kFinal ? (code >= 0 ? (code >> 16) : 0) : 0;
+        const int fpos = kFinal ? (code & 0xFFFF) : 0;
+        const bool active = kFinal ? (kind != 0) : (prev >= 0);
+        const uint32_t pos = kFinal ? (uint32_t)fpos : (uint32_t)p.j;
+        const uint32_t stream = kFinal ? (kind == 1 ? kStreamResidual : kStreamBonus) : kStreamDraft;
+        // round-1 constants of Philox for this request and position
+        const uint32_t y0c = __umulhi(kPhiloxM1, rid) ^ pos ^ p.keys.k0[0];
+        const uint32_t y1c = kPhiloxM1 * rid;
+        const uint32_t sk = stream ^ p.keys.k1[0];
+
         RowState st = row_state_init();
+        float Q = kQMax;
+        float Qr = kQMax;  // 2^-K for the residual candidate test (with margin)
         ResidualState rs = residual_init();
         float lse_q2 = 0.f, lse_t2 = 0.f;
-        if (kResidual && active) {
-            lse_q2 = p.draft_lse[(size_t)b * p.G + d] * kLog2e;
-            lse_t2 = p.lse_t_row[b];
+        const __nv_bfloat16 *urow = nullptr, *trow = nullptr;
+        if (kFinal && active) {
+            trow = p.target + ((size_t)b * (p.G + 1) + fpos) * p.V;
+            if (kind == 1) {
+                urow = p.base + ((size_t)b * p.G + fpos) * p.V;
+                lse_q2 = p.draft_lse[(size_t)b * p.G + fpos] * kLog2e;
+                lse_t2 = p.lse_t_row[b];
+            }
         }
-        const uint32_t pos = kResidual ? (uint32_t)(d < 0 ? 0 : d) : (uint32_t)p.j;
+        // final draw: this thread's base / target values, one tile ahead
+        uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
+        if (kFinal && active && ntiles > 0) {
+            const int v = vb + slice * 16;
+            const int n = min(16, ve - v);
+            if (n > 0) {
+                load16_bf16(trow + v, n, nt_lo, nt_hi);
+                if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
+            }
+        }
         for (int t = 0; t < ntiles; ++t) {
             const int a = t % kAccBufs;
             const uint32_t aph = (uint32_t)(t / kAccBufs) & 1u;
@@ -300,8 +412,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 
             const int v = vb + t * BN + slice * 16;
             const int n = min(16, ve - v);
-            float u[16];
-            if (!kResidual) {
+            if (!kFinal) {
                 const int us = t % kUStages;
                 const uint32_t uph = (uint32_t)(t / kUStages) & 1u;
                 if (!uniform_wait(full_u(us), uph, abort)) {
@@ -316,19 +427,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 const uint4 hi = ld_shared_v4(ub + ((uint32_t)((2 * slice + 1) ^ (row & 7)) << 4));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_u(us));
-                const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    u[2 * i] = bf16_lo(wv[i]);
-                    u[2 * i + 1] = bf16_hi(wv[i]);
-                }
-            }
-            if (!active || n <= 0) continue;
-
-            if (!kResidual) {
+                if (!active || n <= 0) continue;
                 float z[16];
+                unpack16(lo, hi, z);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) z[i] = u[i] + __uint_as_float(acc[i]);
+                for (int i = 0; i < 16; ++i) z[i] += __uint_as_float(acc[i]);
                 if (p.z_out) {
                     float *zo = p.z_out + ((size_t)b * p.G + p.j) * p.V + v;
                     if (n == 16) {
@@ -344,86 +447,79 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     for (int i = 0; i < 16; ++i)
                         if (i < n) argmax_push(st, z[i], v + i);
                 } else {
-                    float s2[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) s2[i] = z[i] * c2;
-                    softmax_push_group<16>(st, s2, n);
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (4 * g < n) {
-                            const uint4 w4 = philox4x32_10(
-                                make_uint4(((uint32_t)v >> 2) + g, pos, rid, kStreamDraft), p.k0, p.k1);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (4 * g + e < n) gumbel_push(st, s2[4 * g + e], word_of(w4, e), v + 4 * g + e);
-                        }
-                    }
+                    draft_sample16(st, Q, z, c2, n, v, y0c, y1c, sk, p.keys);
                 }
             } else {
-                const size_t rowoff = ((size_t)b * p.G + d) * p.V + v;
-                const size_t trowoff = ((size_t)b * (p.G + 1) + d) * p.V + v;
-                float tt[16];
-                if (n == 16) {
-                    const uint4 *ub4 = reinterpret_cast<const uint4 *>(p.base + rowoff);
-                    const uint4 *tb4 = reinterpret_cast<const uint4 *>(p.target + trowoff);
-                    const uint4 u0 = __ldg(ub4), u1 = __ldg(ub4 + 1), t0 = __ldg(tb4), t1 = __ldg(tb4 + 1);
-                    const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                    const uint32_t tw[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                if (!active || n <= 0) continue;
+                float u[16], tt[16];
+                unpack16(nu_lo, nu_hi, u);
+                unpack16(nt_lo, nt_hi, tt);
+                {   // prefetch the next tile's values
+                    const int vn = v + BN;
+                    const int nn = min(16, ve - vn);
+                    if (t + 1 < ntiles && nn > 0) {
+                        load16_bf16(trow + vn, nn, nt_lo, nt_hi);
+                        if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
+                    }
+                }
+                uint4 w[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        u[2 * i] = bf16_lo(uw[i]);
-                        u[2 * i + 1] = bf16_hi(uw[i]);
-                        tt[2 * i] = bf16_lo(tw[i]);
-                        tt[2 * i + 1] = bf16_hi(tw[i]);
+                for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)v >> 2) + g, y0c, y1c, sk, p.keys);
+                // Candidate test: the key of token v is log2(r_v) - log2(E_v) with
+                // r_v = p_v - q_v (residual) or 2^(t_v c2) (bonus, unnormalised);
+                // it can beat the best key K only if (1 - u_v) < r_v 2^-K.
+                bool cand[16];
+                bool any = false;
+                if (kind == 1) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float z = u[i] + __uint_as_float(acc[i]);
+                        const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
+                        const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
+                        // upper bound of p - q under the approximate exponentials
+                        const float rb = (pv - qv) + 4e-7f * (pv + qv);
+                        // rb <= 0 gives a threshold <= 1 <= f1: no candidate
+                        cand[i] = (i < n) &&
+                                  one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rb, Qr, 1.f);
+                        any |= cand[i];
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        u[i] = (i < n) ? __bfloat162float(p.base[rowoff + i]) : 0.f;
-                        tt[i] = (i < n) ? __bfloat162float(p.target[trowoff + i]) : 0.f;
+                        const float rb = fast_exp2(fmaf(tt[i], c2, -rs.key_res)) * kMargin;
+                        cand[i] = (i < n) &&
+                                  one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rb, 1.f, 1.f);
+                        any |= cand[i];
                     }
                 }
+                if (any) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    if (4 * g < n) {
-                        const uint4 w4 = philox4x32_10(
-                            make_uint4(((uint32_t)v >> 2) + g, pos, rid, kStreamResidual), p.k0, p.k1);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 4 * g + e;
-                            if (i >= n) continue;
+                    for (int i = 0; i < 16; ++i) {
+                        if (!cand[i]) continue;
+                        const float ln_e = fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
+                        float base;
+                        if (kind == 1) {
                             const float z = u[i] + __uint_as_float(acc[i]);
-                            const uint32_t word = word_of(w4, e);
-                            const float lw = fast_log2(word_to_one_minus_uniform(word));
-                            // log2 p - log2 q, from the logit difference first
+                            // log2 p - log2 q from the logit difference, then log2(p - q)
                             const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
-                            if (delta2 > 0.f) {
-                                // log2(2^delta - 1); for delta > 20 it equals delta within 2^-20
-                                const float l1 = delta2 > 20.f ? delta2 : fast_log2(expm1f(delta2 * kLn2));
-                                const float base_r = fmaf(z, c2, -lse_q2) + l1;
-                                if (lw < base_r - rs.key_res + 1e-4f) {
-                                    const float key = base_r - fast_log2(neg_log_uniform(word));
-                                    if (key > rs.key_res) {
-                                        rs.key_res = key;
-                                        rs.idx_res = v + i;
-                                    }
-                                }
-                            }
-                            const float base_p = tt[i] * c2;
-                            if (lw < base_p - rs.key_p + 1e-4f) {
-                                const float key = base_p - fast_log2(neg_log_uniform(word));
-                                if (key > rs.key_p) {
-                                    rs.key_p = key;
-                                    rs.idx_p = v + i;
-                                }
-                            }
+                            if (!(delta2 > 0.f)) continue;
+                            const float l1 = delta2 > 20.f ? delta2 : fast_log2(expm1f(delta2 * kLn2));
+                            base = fmaf(z, c2, -lse_q2) + l1;
+                        } else {
+                            base = tt[i] * c2;
+                        }
+                        const float key = base - ln_e;
+                        if (key > rs.key_res) {
+                            rs.key_res = key;
+                            rs.idx_res = v + i;
+                            if (kind == 1) Qr = fminf(fast_exp2(-key), kQMax) * kMargin;
                         }
                     }
                 }
             }
         }
         // merge the four column slices of each row
-        if (!kResidual) {
+        if (!kFinal) {
             RowState *ms = reinterpret_cast<RowState *>(smem + kOffMerge);
             ms[row * 4 + slice] = st;
         } else {
@@ -432,7 +528,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
         if (slice == 0 && b < p.B) {
-            if (!kResidual) {
+            if (!kFinal) {
                 const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
                 for (int s = 1; s < 4; ++s) row_state_merge(st, ms[row * 4 + s]);
                 p.part[(size_t)b * p.nseg + seg] = st;
@@ -492,11 +588,23 @@ cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V) {
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kResidual>
+template <bool kFinal>
 cudaError_t set_smem_attr() {
-    static cudaError_t once = cudaFuncSetAttribute(markov_tc_kernel<kResidual>,
+    static cudaError_t once = cudaFuncSetAttribute(markov_tc_kernel<kFinal>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     return once;
+}
+
+PhiloxRoundKeys round_keys(uint64_t seed) {
+    PhiloxRoundKeys K;
+    uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFu), k1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        K.k0[r] = k0;
+        K.k1[r] = k1;
+        k0 += kPhiloxW0;
+        k1 += kPhiloxW1;
+    }
+    return K;
 }
 
 }  // namespace
@@ -533,8 +641,7 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, 
     p.r = a.r;
     p.j = j;
     p.nseg = pl.nsplit;
-    p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFu);
-    p.k1 = (uint32_t)(a.seed >> 32);
+    p.keys = round_keys(a.seed);
     p.part = reinterpret_cast<RowState *>(a.ws + pl.partial_offset);
     p.flags = reinterpret_cast<uint32_t *>(a.ws);
     p.z_out = a.z_out;
@@ -542,7 +649,7 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_residual_tensor(const ResidualArgs &a, cudaStream_t s) {
+cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     CUtensorMap mw;
     cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
     if (e != cudaSuccess) return e;
@@ -555,7 +662,7 @@ cudaError_t launch_residual_tensor(const ResidualArgs &a, cudaStream_t s) {
     p.tokens = a.tokens;
     p.temperature = a.temperature;
     p.request_id = a.request_id;
-    p.res_row = a.res_row;
+    p.final_code = a.final_code;
     p.lse_t_row = a.lse_t_row;
     p.draft_lse = a.draft_lse;
     p.B = a.B;
@@ -564,11 +671,10 @@ cudaError_t launch_residual_tensor(const ResidualArgs &a, cudaStream_t s) {
     p.r = a.r;
     p.j = 0;
     p.nseg = a.nseg;
-    p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFu);
-    p.k1 = (uint32_t)(a.seed >> 32);
+    p.keys = round_keys(a.seed);
     p.rpart = reinterpret_cast<ResidualState *>(a.rpart);
     p.flags = a.flags;
-    // the residual kernel has no base-logit tiles to load: map_u is unused
+    // the final draw reads its base rows directly: map_u is unused
     markov_tc_kernel<true><<<dim3(a.nseg, tc_row_blocks(a.B)), kThreads, kSmemBytes, s>>>(mw, mw, p);
     return cudaGetLastError();
 }

@@ -8,10 +8,10 @@
 // stopping at the first candidate that does not raise it.
 //
 // One block of 1024 threads (the work is at most a few thousand candidates):
-//  1. c, a per request in fp64 (a fixed left-to-right product), fp32 copies out;
+//  1. c, a per request in fp32 (a fixed left-to-right product);
 //  2. tau_0 and the candidate list (a, j, b) for L_min <= j < L_max;
 //  3. bitonic sort in shared memory by (a desc, j asc, b asc);
-//  4. block prefix sum of a, Theta before / after each admission, the first
+//  4. block prefix sum of a in fp64, Theta before / after each admission, the first
 //     candidate whose admission does not raise Theta (block min);
 //  5. scatter the admitted counts into the verify lengths.
 #include <climits>
@@ -24,8 +24,11 @@ namespace {
 
 constexpr int kSchedThreads = 1024;
 
-__device__ __forceinline__ bool cand_before(double ka, int pa, double kb, int pb) {
-    return ka > kb || (ka == kb && pa < pb);
+// Sort key of a candidate: a >= 0 is fp32, so its bit pattern orders like
+// its value; (~bits) puts larger a first, the payload j * B + b breaks ties
+// by position, then request.
+__device__ __forceinline__ unsigned long long cand_key(float a, int pay) {
+    return ((unsigned long long)(~__float_as_uint(a)) << 32) | (unsigned int)pay;
 }
 
 __device__ double block_sum(double v, double *red) {
@@ -69,10 +72,9 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
                 float *__restrict__ conf, float *__restrict__ cum_conf,
                 int32_t *__restrict__ verify_len, double *__restrict__ theta_out,
                 uint32_t *__restrict__ flags) {
-    extern __shared__ double smem[];
-    double *key = smem;                                   // [npow2]
-    int *pay = reinterpret_cast<int *>(key + npow2);      // [npow2]: j * B + b
-    int *len_s = pay + npow2;                             // [B]
+    extern __shared__ unsigned long long smem[];
+    unsigned long long *key = smem;                       // [npow2] sort keys
+    int *len_s = reinterpret_cast<int *>(key + npow2);    // [B]
     __shared__ double red[32];
     __shared__ int first_fail;
     __shared__ int bad_temp;
@@ -104,28 +106,21 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
     // 1-2. calibrated confidences, prefix products, tau_0, candidates
     double tau_part = 0.0;
     for (int b = tid; b < B; b += blockDim.x) {
-        double prod = 1.0;
+        float prod = 1.f;
         double t = 1.0;
         for (int j = 0; j < G; ++j) {
-            const double l = (double)conf_logits[(size_t)b * G + j];
-            const double c = 1.0 / (1.0 + exp(-l / (double)pos_temp[j]));
+            const float l = conf_logits[(size_t)b * G + j];
+            const float c = 1.f / (1.f + expf(-l / pos_temp[j]));
             prod *= c;
-            conf[(size_t)b * G + j] = (float)c;
-            cum_conf[(size_t)b * G + j] = (float)prod;
-            if (j < L_min) t += prod;
-            if (j >= L_min && j < L_max) {
-                const int i = b * width + (j - L_min);
-                key[i] = prod;
-                pay[i] = j * B + b;
-            }
+            conf[(size_t)b * G + j] = c;
+            cum_conf[(size_t)b * G + j] = prod;
+            if (j < L_min) t += (double)prod;
+            if (j >= L_min && j < L_max) key[b * width + (j - L_min)] = cand_key(prod, j * B + b);
         }
         tau_part += t;
         len_s[b] = L_min;
     }
-    for (int i = ncand + tid; i < npow2; i += blockDim.x) {
-        key[i] = -1.0;
-        pay[i] = INT_MAX;
-    }
+    for (int i = ncand + tid; i < npow2; i += blockDim.x) key[i] = ~0ull;
     const double tau0 = block_sum(tau_part, red);
     __syncthreads();
 
@@ -135,13 +130,11 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
             for (int i = tid; i < npow2; i += blockDim.x) {
                 const int ixj = i ^ jj;
                 if (ixj > i) {
-                    const double ki = key[i], kx = key[ixj];
-                    const int pi = pay[i], px = pay[ixj];
+                    const unsigned long long ki = key[i], kx = key[ixj];
                     const bool up = (i & k) == 0;
-                    const bool swap = up ? cand_before(kx, px, ki, pi) : cand_before(ki, pi, kx, px);
-                    if (swap) {
-                        key[i] = kx; key[ixj] = ki;
-                        pay[i] = px; pay[ixj] = pi;
+                    if (up ? (kx < ki) : (ki < kx)) {
+                        key[i] = kx;
+                        key[ixj] = ki;
                     }
                 }
             }
@@ -153,28 +146,30 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
     const long n0 = (long)B * (L_min + 1);
     const int per = (ncand + blockDim.x - 1) / blockDim.x;
     const int lo = min(ncand, tid * per), hi = min(ncand, lo + per);
+    auto a_of = [&](int i) { return (double)__uint_as_float(~(unsigned int)(key[i] >> 32)); };
     double local = 0.0;
-    for (int i = lo; i < hi; ++i) local += key[i];
+    for (int i = lo; i < hi; ++i) local += a_of(i);
     const double before = block_exclusive_scan(local, red);
     double run = tau0 + before;  // tau before candidate lo
     for (int i = lo; i < hi; ++i) {
+        const double a = a_of(i);
         const double th_before = run * (double)sps[n0 + i];
-        const double th_after = (run + key[i]) * (double)sps[n0 + i + 1];
+        const double th_after = (run + a) * (double)sps[n0 + i + 1];
         if (!(th_after > th_before)) {
             atomicMin(&first_fail, i);
             break;
         }
-        run += key[i];
+        run += a;
     }
     __syncthreads();
     const int nstar = first_fail;
     // tau after the admitted prefix, for Theta
     double adm = 0.0;
-    for (int i = lo; i < min(hi, nstar); ++i) adm += key[i];
+    for (int i = lo; i < min(hi, nstar); ++i) adm += a_of(i);
     const double tau_final = tau0 + block_sum(adm, red);
 
     // 5. verify lengths
-    for (int i = tid; i < nstar; i += blockDim.x) atomicAdd(&len_s[pay[i] % B], 1);
+    for (int i = tid; i < nstar; i += blockDim.x) atomicAdd(&len_s[(int)(key[i] & 0xFFFFFFFFu) % B], 1);
     __syncthreads();
     for (int b = tid; b < B; b += blockDim.x) verify_len[b] = len_s[b];
     if (tid == 0 && theta_out) *theta_out = tau_final * (double)sps[n0 + nstar];
@@ -187,7 +182,7 @@ size_t schedule_smem_bytes(int B, int G, int L_min, int L_max) {
     const long ncand = (long)B * (L_max - L_min);
     long npow2 = 1;
     while (npow2 < ncand) npow2 <<= 1;
-    return (size_t)npow2 * (sizeof(double) + sizeof(int)) + sizeof(int) * (size_t)B;
+    return (size_t)npow2 * sizeof(unsigned long long) + sizeof(int) * (size_t)B;
 }
 
 cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {

@@ -8,18 +8,19 @@
 // follows a fully accepted block.  The residual is normalise(max(0, p - q)).
 //
 // Four launches:
-//  1. verify_rows     grid (segments, B*(G+1)): streams the target rows j <= L
-//                     of every request once with 16-byte loads -- online
-//                     softmax of t/T for rows j < L, the bonus Gumbel-max for
-//                     row L, the argmax for greedy requests.
+//  1. verify_rows     grid (segments, B*(G+1)): streams the target rows j < L
+//                     of every sampled request once with 16-byte loads
+//                     (online softmax of t/T), and rows j <= L of greedy
+//                     requests (argmax);
 //  2. verify_decide   one warp per request: merges the row partials, runs the
 //                     sequential acceptance scan, writes the emitted tokens and
-//                     marks the rejected row, if any.
-//  3. residual        rejected requests only: rebuilds the draft logits of the
-//                     rejected row (base + Markov bias on the tensor cores for
-//                     bf16 weights, SIMT for fp32, or the stored draft logits)
-//                     and draws from max(0, p - q) by Gumbel-max.
-//  4. verify_residual_finalize: merges the residual partials into the token.
+//                     marks the final draw: a residual at the rejected row or a
+//                     bonus from row L (sampled requests only);
+//  3. final draw      residual rows rebuild the draft logits of the rejected
+//                     row (base + Markov bias on the tensor cores for bf16
+//                     weights, CUDA cores for fp32, or the stored draft logits)
+//                     and draw from max(0, p - q); bonus rows draw from p_L;
+//  4. verify_final_merge: merges the final-draw partials into the token.
 #include <climits>
 
 #include "device_common.cuh"
@@ -67,8 +68,7 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
 template <typename TIn>
 __global__ void __launch_bounds__(kRowThreads)
 verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ verify_len,
-                   const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
-                   int B, int G, int V, uint32_t k0, uint32_t k1, int chunk, int nsplit,
+                   const float *__restrict__ temperature, int B, int G, int V, int chunk, int nsplit,
                    RowState *__restrict__ part) {
     __shared__ RowState scratch[kRowThreads / 32];
     const int row = blockIdx.y;
@@ -76,16 +76,17 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
     const int j = row - b * (G + 1);
     const int L = read_verify_len(verify_len, b, G);
     const float T = temperature[b];
-    if (L < 0 || j > L || !temperature_ok(T)) return;
+    // sampled requests read rows j < L here (row L only for a bonus draw, in
+    // the final pass); greedy requests read rows j <= L
+    if (L < 0 || !temperature_ok(T) || j > L || (T > 0.f && j == L)) return;
     const float c2 = T > 0.f ? kLog2e / T : 0.f;
-    const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     const int seg = blockIdx.x;
     const int vb = seg * chunk;
     const int ve = min(V, vb + chunk);
     const TIn *t_row = target + ((size_t)b * (G + 1) + j) * V;
 
     RowState st = row_state_init();
-    if (T > 0.f && j < L) {
+    if (T > 0.f) {
         int v = vb + 8 * threadIdx.x;
         for (; v + 8 * kRowThreads < ve; v += 16 * kRowThreads) {  // two loads in flight
             float x[8], y[8];
@@ -105,18 +106,6 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] *= c2;
             softmax_push_group<8>(st, x, 8);
-        }
-    } else if (T > 0.f) {  // j == L: bonus draw
-        for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {
-            float x[8];
-            load8(t_row + v, x);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint4 w4 = philox4x32_10(
-                    make_uint4(((uint32_t)v >> 2) + h, (uint32_t)j, id, kStreamBonus), k0, k1);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) gumbel_push(st, x[4 * h + e] * c2, word_of(w4, e), v + 4 * h + e);
-            }
         }
     } else {  // greedy request
         for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {
@@ -142,7 +131,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
                                      uint32_t k0, uint32_t k1, int32_t *__restrict__ accept_len,
                                      int32_t *__restrict__ out_tokens, int32_t *__restrict__ num_out,
                                      float *__restrict__ target_lse, float *__restrict__ logp_sel,
-                                     int32_t *__restrict__ res_row, float *__restrict__ lse_t_row,
+                                     int32_t *__restrict__ final_code, float *__restrict__ lse_t_row,
                                      uint32_t *__restrict__ flags) {
     const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -179,7 +168,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         if (lane == 0) {
             accept_len[b] = -1;
             num_out[b] = 0;
-            res_row[b] = -1;
+            final_code[b] = -1;
         }
         return;
     }
@@ -221,87 +210,109 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         }
         ++k;
     }
-    if (d < 0 && y < 0) {  // bonus token from row L
+    int code = -1;
+    if (d >= 0) {
+        code = (1 << 16) | d;              // residual draw at the rejected row
+    } else if (y < 0 && T > 0.f) {
+        code = (2 << 16) | L;              // bonus draw from row L
+    } else if (y < 0) {                    // greedy bonus: argmax of row L
         RowState s = row_state_init();
         const RowState *pr = part + ((size_t)b * (G + 1) + L) * nsplit;
         for (int i = lane; i < nsplit; i += 32) row_state_merge(s, pr[i]);
         s = warp_merge(s);
         y = s.idx;
-        if (T == 0.f && lane == 0 && target_lse) target_lse[(size_t)b * (G + 1) + L] = s.key;
+        if (lane == 0 && target_lse) target_lse[(size_t)b * (G + 1) + L] = s.key;
     }
     for (int j = lane; j < k; j += 32) out_tokens[(size_t)b * (G + 1) + j] = draft_tokens[(size_t)b * G + j];
     if (lane == 0) {
-        out_tokens[(size_t)b * (G + 1) + k] = (d >= 0) ? -1 : y;
+        out_tokens[(size_t)b * (G + 1) + k] = (code >= 0) ? -1 : y;
         accept_len[b] = k;
         num_out[b] = k + 1;
-        res_row[b] = d;
+        final_code[b] = code;
     }
 }
 
 // ------------------------------------------------- pass 3 (SIMT / stored) ----
-// Residual draw with the draft logits of the rejected row taken from the
-// stored draft logits (any dtype) or rebuilt with CUDA-core FMAs (fp32).
+// Final draw with CUDA cores: residual rows take the draft logits of the
+// rejected row from the stored draft logits (any dtype) or rebuild them with
+// FMAs (fp32 weights); bonus rows draw from the target row L.
 template <typename TIn>
 __global__ void __launch_bounds__(kResThreads)
-verify_residual_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__ base,
-                            const TIn *__restrict__ e_in, const TIn *__restrict__ w_out,
-                            const float *__restrict__ z_in, const int32_t *__restrict__ anchor,
-                            const int32_t *__restrict__ draft_tokens, const float *__restrict__ draft_lse,
-                            const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
-                            const int32_t *__restrict__ res_row, const float *__restrict__ lse_t_row,
-                            int B, int G, int V, int r, uint32_t k0, uint32_t k1, int chunk, int nsplit,
-                            ResidualState *__restrict__ part) {
+verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__ base,
+                         const TIn *__restrict__ e_in, const TIn *__restrict__ w_out,
+                         const float *__restrict__ z_in, const int32_t *__restrict__ anchor,
+                         const int32_t *__restrict__ draft_tokens, const float *__restrict__ draft_lse,
+                         const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
+                         const int32_t *__restrict__ final_code, const float *__restrict__ lse_t_row,
+                         int B, int G, int V, int r, uint32_t k0, uint32_t k1, int chunk, int nsplit,
+                         ResidualState *__restrict__ part) {
     extern __shared__ float a_row[];  // [r]
     __shared__ ResidualState scratch[kResThreads / 32];
     const int b = blockIdx.y;
-    const int d = res_row[b];
-    if (d < 0) return;
+    const int code = final_code[b];
+    if (code < 0) return;
+    const int kind = code >> 16, d = code & 0xFFFF;
     const int seg = blockIdx.x;
     const float c2 = kLog2e / temperature[b];
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
-    const float lse_q2 = draft_lse[(size_t)b * G + d] * kLog2e;
-    const float lse_t2 = lse_t_row[b];
-    const int prev = (d == 0) ? anchor[b] : draft_tokens[(size_t)b * G + d - 1];
-    if (!z_in) {
+    const bool residual = (kind == 1);
+    const float lse_q2 = residual ? draft_lse[(size_t)b * G + d] * kLog2e : 0.f;
+    const float lse_t2 = residual ? lse_t_row[b] : 0.f;
+    if (residual && !z_in) {
+        const int prev = (d == 0) ? anchor[b] : draft_tokens[(size_t)b * G + d - 1];
         for (int k = threadIdx.x; k < r; k += blockDim.x) a_row[k] = to_f32(e_in[(size_t)prev * r + k]);
-        __syncthreads();
     }
+    __syncthreads();
     const size_t drow = (size_t)b * G + d;
     const TIn *t_row = target + ((size_t)b * (G + 1) + d) * V;
+    const uint32_t stream = residual ? kStreamResidual : kStreamBonus;
     const int vb = seg * chunk;
     const int ve = min(V, vb + chunk);
     ResidualState st = residual_init();
     for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kResThreads) {
-        float z[4];
-        if (z_in) {
-            const float4 z4 = *reinterpret_cast<const float4 *>(z_in + drow * V + v);
-            z[0] = z4.x; z[1] = z4.y; z[2] = z4.z; z[3] = z4.w;
-        } else {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < r; k += 4) {
-                const float4 a = *reinterpret_cast<const float4 *>(a_row + k);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 w = load4(w_out + (size_t)(v + e) * r + k);
-                    float t = acc[e];
-                    t = fmaf(a.x, w.x, t);
-                    t = fmaf(a.y, w.y, t);
-                    t = fmaf(a.z, w.z, t);
-                    t = fmaf(a.w, w.w, t);
-                    acc[e] = t;
-                }
-            }
-            const float4 u4 = load4(base + drow * V + v);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[e];
-        }
         const float4 t4 = load4(t_row + v);
-        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, kStreamResidual), k0, k1);
+        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, stream), k0, k1);
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
+        if (residual) {
+            if (z_in) {
+                const float4 z4 = *reinterpret_cast<const float4 *>(z_in + drow * V + v);
+                z[0] = z4.x; z[1] = z4.y; z[2] = z4.z; z[3] = z4.w;
+            } else {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int k = 0; k < r; k += 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(a_row + k);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 w = load4(w_out + (size_t)(v + e) * r + k);
+                        float t = acc[e];
+                        t = fmaf(a.x, w.x, t);
+                        t = fmaf(a.y, w.y, t);
+                        t = fmaf(a.z, w.z, t);
+                        t = fmaf(a.w, w.w, t);
+                        acc[e] = t;
+                    }
+                }
+                const float4 u4 = load4(base + drow * V + v);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[e];
+            }
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float t = elem(t4, e);
             const uint32_t word = word_of(w4, e);
             const float lw = fast_log2(word_to_one_minus_uniform(word));
+            const float base_p = t * c2;
+            if (!residual) {  // bonus: Gumbel-max over t / T
+                if (lw < base_p - st.key_res + 1e-4f) {
+                    const float key = base_p - fast_log2(neg_log_uniform(word));
+                    if (key_better(key, v + e, st.key_res, st.idx_res)) {
+                        st.key_res = key;
+                        st.idx_res = v + e;
+                    }
+                }
+                continue;
+            }
             // log2 p - log2 q, from the logit difference first
             const float delta2 = fmaf(t - z[e], c2, lse_q2 - lse_t2);
             if (delta2 > 0.f) {
@@ -315,7 +326,6 @@ verify_residual_simt_kernel(const TIn *__restrict__ target, const TIn *__restric
                     }
                 }
             }
-            const float base_p = t * c2;
             if (lw < base_p - st.key_p + 1e-4f) {
                 const float key = base_p - fast_log2(neg_log_uniform(word));
                 if (key_better(key, v + e, st.key_p, st.idx_p)) {
@@ -336,64 +346,89 @@ verify_residual_simt_kernel(const TIn *__restrict__ target, const TIn *__restric
     }
 }
 
-__global__ void verify_residual_finalize_kernel(const ResidualState *__restrict__ part, int nsplit,
-                                                const int32_t *__restrict__ res_row,
-                                                const int32_t *__restrict__ accept_len, int B, int G,
-                                                int32_t *__restrict__ out_tokens) {
+// One warp per request with a final draw: merge the partials, emit the token.
+// If a residual row had no entry with p > q at all (impossible in exact
+// arithmetic after a rejection), the token is drawn from p with the residual
+// stream instead, scanning the target row here.
+template <typename TIn>
+__global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part, int nsplit,
+                                          const int32_t *__restrict__ final_code,
+                                          const int32_t *__restrict__ accept_len,
+                                          const TIn *__restrict__ target, const float *__restrict__ temperature,
+                                          const uint32_t *__restrict__ request_id, int B, int G, int V,
+                                          uint32_t k0, uint32_t k1, int32_t *__restrict__ out_tokens) {
     const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
-    const int d = res_row[b];
-    if (d < 0) return;
+    const int code = final_code[b];
+    if (code < 0) return;
     ResidualState s = residual_init();
     for (int i = lane; i < nsplit; i += 32) residual_merge(s, part[(size_t)b * nsplit + i]);
     s = residual_warp_merge(s);
-    if (lane == 0) {
-        const int y = (s.idx_res != INT32_MAX) ? s.idx_res : s.idx_p;
-        out_tokens[(size_t)b * (G + 1) + accept_len[b]] = y;
+    int y = (s.idx_res != INT32_MAX) ? s.idx_res : s.idx_p;
+    if (y == INT32_MAX) {  // degenerate residual: draw from p
+        const int d = code & 0xFFFF;
+        const float c2 = kLog2e / temperature[b];
+        const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
+        const TIn *t_row = target + ((size_t)b * (G + 1) + d) * V;
+        ResidualState f = residual_init();
+        for (int v = 4 * lane; v < V; v += 128) {
+            const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, kStreamResidual), k0, k1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float key = to_f32(t_row[v + e]) * c2 - fast_log2(neg_log_uniform(word_of(w4, e)));
+                if (key_better(key, v + e, f.key_p, f.idx_p)) {
+                    f.key_p = key;
+                    f.idx_p = v + e;
+                }
+            }
+        }
+        f = residual_warp_merge(f);
+        y = f.idx_p;
     }
+    if (lane == 0) out_tokens[(size_t)b * (G + 1) + accept_len[b]] = y;
 }
 
 template <typename TIn>
 cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
     uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
     RowState *row_part = reinterpret_cast<RowState *>(a.ws + p.row_part_offset);
-    int32_t *res_row = reinterpret_cast<int32_t *>(a.ws + p.res_row_offset);
+    int32_t *final_code = reinterpret_cast<int32_t *>(a.ws + p.res_row_offset);
     float *lse_t_row = reinterpret_cast<float *>(a.ws + p.lse_t_offset);
     ResidualState *res_part = reinterpret_cast<ResidualState *>(a.ws + p.res_part_offset);
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
     const TIn *target = static_cast<const TIn *>(a.target);
 
     verify_rows_kernel<TIn><<<dim3(p.row_split, a.B * (a.G + 1)), kRowThreads, 0, s>>>(
-        target, a.verify_len, a.temperature, a.request_id, a.B, a.G, a.V, k0, k1, p.row_chunk,
-        p.row_split, row_part);
+        target, a.verify_len, a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split, row_part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int warps = 4;
     verify_decide_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
         target, row_part, p.row_split, a.anchor, a.draft_tokens, a.draft_logq, a.verify_len, a.temperature,
         a.request_id, a.B, a.G, a.V, k0, k1, a.accept_len, a.out_tokens, a.num_out, a.target_lse,
-        a.logp_sel, res_row, lse_t_row, flags);
+        a.logp_sel, final_code, lse_t_row, flags);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const bool tensor = p.tensor_residual && !a.z_in;
     const int res_nsplit = tensor ? p.res_split_tc : p.res_split;
     if (tensor) {
-        ResidualArgs ra{a.target, a.base, a.e_in, a.w_out, a.anchor, a.draft_tokens, a.temperature,
-                        a.request_id, res_row, lse_t_row, a.draft_lse, a.B, a.G, a.V, a.r, res_nsplit,
-                        a.seed, res_part, flags};
-        e = launch_residual_tensor(ra, s);
+        FinalArgs fa{a.target, a.base, a.e_in, a.w_out, a.anchor, a.draft_tokens, a.temperature,
+                     a.request_id, final_code, lse_t_row, a.draft_lse, a.B, a.G, a.V, a.r, res_nsplit,
+                     a.seed, res_part, flags};
+        e = launch_final_tensor(fa, s);
     } else {
-        const size_t smem = a.z_in ? 0 : sizeof(float) * (size_t)a.r;
-        verify_residual_simt_kernel<TIn><<<dim3(p.res_split, a.B), kResThreads, smem, s>>>(
+        const size_t smem = sizeof(float) * (size_t)a.r;
+        verify_final_simt_kernel<TIn><<<dim3(p.res_split, a.B), kResThreads, smem, s>>>(
             target, static_cast<const TIn *>(a.base), static_cast<const TIn *>(a.e_in),
             static_cast<const TIn *>(a.w_out), a.z_in, a.anchor, a.draft_tokens, a.draft_lse,
-            a.temperature, a.request_id, res_row, lse_t_row, a.B, a.G, a.V, a.r, k0, k1, p.res_chunk,
+            a.temperature, a.request_id, final_code, lse_t_row, a.B, a.G, a.V, a.r, k0, k1, p.res_chunk,
             p.res_split, res_part);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    verify_residual_finalize_kernel<<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
-        res_part, res_nsplit, res_row, a.accept_len, a.B, a.G, a.out_tokens);
+    verify_final_merge_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
+        res_part, res_nsplit, final_code, a.accept_len, target, a.temperature, a.request_id, a.B, a.G,
+        a.V, k0, k1, a.out_tokens);
     return cudaGetLastError();
 }
 

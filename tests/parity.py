@@ -137,7 +137,7 @@ def compare_schedule(g, o):
         else:
             t.failures.append("verify lengths differ (%d requests)" % int((gl != o["verify_len"]).sum()))
     theta = float(g["theta"].numpy()[0])
-    if not _close(theta, o["theta"], rel=1e-9):
+    if not _close(theta, o["theta"]):
         t.failures.append("theta gpu=%.12g oracle=%.12g" % (theta, o["theta"]))
     return t
 
