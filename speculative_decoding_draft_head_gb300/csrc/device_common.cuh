@@ -242,6 +242,22 @@ __device__ __forceinline__ void argmax_push(RowState &st, float z, int v) {
     st.m = fmaxf(st.m, z);
 }
 
+// Float keys as unsigned integers whose order is the float order, so that a
+// row-wide running best can be kept with atomicMax.  0 encodes "none" (-inf).
+__device__ __forceinline__ uint32_t key_to_ordered(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ordered_to_key(uint32_t o) {
+    if (o == 0u) return -INFINITY;
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+__device__ __forceinline__ uint32_t load_relaxed(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 // Residual draw state: best key over {p > q} and, for the degenerate case
 // where no entry has p > q, the best key of a draw from p.
 struct ResidualState {

@@ -194,7 +194,6 @@ cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j,
 }
 
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
-    (void)G;
     (void)r;
     DraftPlan p{};
     p.partial_offset = kFlagBytes;
@@ -218,7 +217,8 @@ DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
         p.nsplit = (V + chunk - 1) / chunk;
         p.chunk = chunk;
     }
-    p.ws_bytes = align_up(p.partial_offset + sizeof(RowState) * (size_t)B * p.nsplit, 256);
+    p.row_best_offset = align_up(p.partial_offset + sizeof(RowState) * (size_t)B * p.nsplit, 256);
+    p.ws_bytes = align_up(p.row_best_offset + sizeof(uint32_t) * (size_t)B * (size_t)G, 256);
     return p;
 }
 

@@ -26,6 +26,7 @@ struct DraftPlan {
     int nsplit;            // vocabulary segments per row (partials per row)
     int chunk;             // vocabulary entries per segment (multiple of 4)
     size_t partial_offset; // byte offset of the per-(row, segment) partials
+    size_t row_best_offset;// [G][B] uint32 row-wide best keys (tensor path), zeroed per call
     size_t ws_bytes;
 };
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt);
@@ -71,6 +72,7 @@ struct FinalArgs {
     const float *lse_t_row;    // [B] target lse of the rejected row, log2 units
     const float *draft_lse;    // [B][G] natural log
     int B, G, V, r, nseg;
+    int pass;                  // traversal direction of the vocabulary segments (odd: backwards)
     uint64_t seed;
     void *rpart;               // [B][nseg] final-draw partials
     uint32_t *flags;

@@ -20,14 +20,14 @@
 //    logits + Markov bias) or accepted its whole block (bonus draw from p_L);
 //    other rows idle.  Base and target rows are read directly, one tile ahead.
 //
-// CTA layout (one CTA per SM, 576 threads, ~196 KB shared memory):
+// CTA layout (one CTA per SM, 576 threads, ~212 KB shared memory):
 //   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant of
 //               rows) and columns 16*(w/4).. of each 64-column tile;
 //   warp 16     TMA producer: W_out tiles (64 tokens x r, 128-byte swizzle,
 //               L2 evict-last) and base-logit tiles (evict-first);
 //   warp 17     TMEM allocator and UMMA issuer (M=128, N=64, K=16 steps).
 // The A operand (the 128 gathered E_in rows, 128 x r bf16) is built once per
-// CTA in the 128-byte swizzled K-major layout.  Rings: 2 W stages, 3 base
+// CTA in the 128-byte swizzled K-major layout.  Rings: 3 W stages, 3 base
 // stages, 4 TMEM accumulators of 64 columns.  Every wait is bounded; a timeout
 // sets the timeout bit of the flag word and the CTA unwinds.
 //
@@ -57,7 +57,7 @@ constexpr int kEpiWarps = 16;
 constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
 constexpr int kThreads = 18 * 32;
-constexpr int kWStages = 2;
+constexpr int kWStages = 3;
 constexpr int kUStages = 3;
 constexpr int kAccBufs = 4;
 constexpr uint32_t kTmemCols = kAccBufs * BN;  // 256
@@ -67,9 +67,13 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffW = kOffA + 4 * kAtomA;
 constexpr uint32_t kOffU = kOffW + kWStages * 4 * kAtomW;
 constexpr uint32_t kUBytes = BM * BN * 2;
-constexpr uint32_t kOffMerge = kOffU + kUStages * kUBytes;
+// the slice merge after the last tile reuses the W ring (all UMMAs are done)
+constexpr uint32_t kOffMerge = kOffW;
 constexpr uint32_t kMergeBytes = BM * 4 * 32;
-constexpr uint32_t kOffBar = kOffMerge + kMergeBytes;
+static_assert(kMergeBytes <= kWStages * 4 * kAtomW, "merge scratch fits in the W ring");
+constexpr uint32_t kOffBar = kOffU + kUStages * kUBytes;
+constexpr int kNumBars = 2 * kWStages + 2 * kUStages + 2 * kAccBufs;
+static_assert(kNumBars * 8 <= 256, "barrier region");
 constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kMiscBytes = 16 + BM * 16;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
@@ -91,8 +95,10 @@ struct TcParams {
     const float *lse_t_row;     // [B] target lse of the rejected row, log2 units
     const float *draft_lse;     // [B][G] natural log
     int B, G, V, r, j, nseg;
+    int pass;                   // launch counter: odd passes walk the segment backwards
     PhiloxRoundKeys keys;
     RowState *part;
+    uint32_t *row_best;         // [G][B] draft / [B] final: row-wide best key (ordered encoding)
     ResidualState *rpart;
     uint32_t *flags;
     float *z_out;
@@ -135,55 +141,96 @@ __device__ __forceinline__ void load16_bf16(const __nv_bfloat16 *p, int n, uint4
     }
 }
 
-// Draft epilogue for 16 logits of one row (T > 0).
-__device__ __forceinline__ void draft_sample16(RowState &st, float &Q, const float (&z)[16], float c2, int n, int v,
-                                               uint32_t y0c, uint32_t y1c, uint32_t sk, const PhiloxRoundKeys &K) {
-    float s2[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s2[i] = z[i] * c2;
-    float cm = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if (i < n) cm = fmaxf(cm, s2[i]);
-    if (cm > st.m) {
-        st.S *= fast_exp2(st.m - cm);
-        st.m = cm;
-        Q = fminf(fast_exp2(cm - st.key), kQMax) * kMargin;
-    }
+// Draft epilogue for 16 logits of one row (T > 0).  Every lane of the warp
+// calls it together (it votes across the warp); `on` is false for rows that
+// are greedy or inactive, which then change nothing.
+//
+// The softmax keeps a running reference m that may lag the true maximum:
+// terms 2^(s2 - m) above 1 are fine, and a batch whose sum exceeds 2^64 (or
+// overflows) is redone against its own maximum.  The candidate test runs per
+// Philox group of four tokens: the group's largest e against its smallest
+// 1 - u (largest word); only passing groups test their tokens one by one.
+//
+// kbest is the best key known for the whole row: this thread's, or a larger
+// one another thread published in row_best (any token that cannot beat an
+// achieved key cannot be the row's Gumbel argmax, so it is skipped exactly).
+// A new best is published with atomicMax; readers see it a tile later.
+__device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kbest, const float (&s2)[16], int n,
+                                               int v, bool on, uint32_t *row_best, uint32_t y0c, uint32_t y1c,
+                                               uint32_t sk, const PhiloxRoundKeys &K) {
+    const bool full = (n == 16);  // warp-uniform
     float e[16];
-    float sum = 0.f;
+    if (on) {
+        if (st.m == -INFINITY) {  // first batch of this row segment: take its maximum
+            float cm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        e[i] = (i < n) ? fast_exp2(s2[i] - st.m) : 0.f;
-        sum += e[i];
+            for (int i = 0; i < 16; ++i)
+                if (full || i < n) cm = fmaxf(cm, s2[i]);
+            st.m = cm;
+            Q = fminf(fast_exp2(cm - kbest), kQMax) * kMargin;
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            e[i] = (full || i < n) ? fast_exp2(s2[i] - st.m) : 0.f;
+            sum += e[i];
+        }
+        if (!(sum <= 0x1p64f)) {  // far above the reference (or overflow): renormalise
+            float cm = st.m;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (full || i < n) cm = fmaxf(cm, s2[i]);
+            st.S *= fast_exp2(st.m - cm);
+            st.m = cm;
+            Q = fminf(fast_exp2(cm - kbest), kQMax) * kMargin;
+            sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                e[i] = (full || i < n) ? fast_exp2(s2[i] - st.m) : 0.f;
+                sum += e[i];
+            }
+        }
+        st.S += sum;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) e[i] = 0.f;  // threshold 1 <= f1: no candidate
     }
-    st.S += sum;
     uint4 w[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)v >> 2) + g, y0c, y1c, sk, K);
-    bool cand[16];
+    bool gc[4];
     bool any = false;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        cand[i] = one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(e[i], Q, 1.f);
-        any |= cand[i];
+    for (int g = 0; g < 4; ++g) {
+        const float emax = fmaxf(fmaxf(e[4 * g], e[4 * g + 1]), fmaxf(e[4 * g + 2], e[4 * g + 3]));
+        const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
+        gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(emax, Q, 1.f);
+        any |= gc[g];
     }
-    if (any) {
+    if (__any_sync(0xffffffffu, any)) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (cand[i]) {
-                const float key = s2[i] - fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
-                if (key > st.key) {
+        for (int g = 0; g < 4; ++g) {
+            if (!(__any_sync(0xffffffffu, gc[g]) && gc[g])) continue;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = 4 * g + c;
+                const uint32_t word = word_of(w[g], c);
+                if (!(one_minus_uniform_plus_one(word) < fmaf(e[i], Q, 1.f))) continue;
+                const float key = s2[i] - fast_log2(neg_log_uniform(word));
+                if (key > kbest) {
                     st.key = key;
                     st.s_at = s2[i];
                     st.idx = v + i;
-                    Q = fminf(fast_exp2(st.m - key), kQMax) * kMargin;
+                    kbest = key;
+                    atomicMax(row_best, key_to_ordered(key));
                 }
             }
         }
+        if (on) Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
     }
 }
 
+// 18 warps: 5 share one SM sub-partition's 16K registers, so at most 96 each.
 template <bool kFinal>
 __global__ void __launch_bounds__(kThreads, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
@@ -198,14 +245,18 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     const int vb = seg_begin(seg, p.nseg, p.V);
     const int ve = seg_begin(seg + 1, p.nseg, p.V);
     const int ntiles = (ve - vb + BN - 1) / BN;
+    // Odd launches walk the segment backwards: each launch then starts on
+    // the W_out tiles the previous launch touched last, which are still in L2.
+    const bool reverse = (p.pass & 1) != 0;
+    auto tile_col = [&](int t) { return vb + (reverse ? (ntiles - 1 - t) : t) * BN; };
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
     auto full_w = [&](int s) { return bar(s); };
-    auto empty_w = [&](int s) { return bar(2 + s); };
-    auto full_u = [&](int s) { return bar(4 + s); };
-    auto empty_u = [&](int s) { return bar(7 + s); };
-    auto tfull = [&](int a) { return bar(10 + a); };
-    auto tempty = [&](int a) { return bar(14 + a); };
+    auto empty_w = [&](int s) { return bar(kWStages + s); };
+    auto full_u = [&](int s) { return bar(2 * kWStages + s); };
+    auto empty_u = [&](int s) { return bar(2 * kWStages + kUStages + s); };
+    auto tfull = [&](int a) { return bar(2 * kWStages + 2 * kUStages + a); };
+    auto tempty = [&](int a) { return bar(2 * kWStages + 2 * kUStages + kAccBufs + a); };
 
     int *misc = reinterpret_cast<int *>(smem + kOffMisc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
@@ -295,7 +346,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             const uint64_t pol_w = policy_evict_last();
             const uint64_t pol_u = policy_evict_first();
             for (int t = 0; t < ntiles; ++t) {
-                const int v0 = vb + t * BN;
+                const int v0 = tile_col(t);
                 const int ws = t % kWStages;
                 const uint32_t wph = (uint32_t)(t / kWStages) & 1u;
                 if (t >= kWStages && !mbar_wait(empty_w(ws), wph ^ 1u, abort, kSpinLimit)) {
@@ -370,6 +421,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 
         RowState st = row_state_init();
         float Q = kQMax;
+        float kbest = -INFINITY;  // best key of the row known to this thread
+        uint32_t *row_best = (kFinal || b >= p.B) ? nullptr : p.row_best + (size_t)p.j * p.B + b;
         float Qr = kQMax;  // 2^-K for the residual candidate test (with margin)
         ResidualState rs = residual_init();
         float lse_q2 = 0.f, lse_t2 = 0.f;
@@ -380,12 +433,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 urow = p.base + ((size_t)b * p.G + fpos) * p.V;
                 lse_q2 = p.draft_lse[(size_t)b * p.G + fpos] * kLog2e;
                 lse_t2 = p.lse_t_row[b];
+            } else {
+                lse_q2 = INFINITY;  // q = 0
+                lse_t2 = 0.f;       // unnormalised p: the same argmax
             }
         }
         // final draw: this thread's base / target values, one tile ahead
         uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
         if (kFinal && active && ntiles > 0) {
-            const int v = vb + slice * 16;
+            const int v = tile_col(0) + slice * 16;
             const int n = min(16, ve - v);
             if (n > 0) {
                 load16_bf16(trow + v, n, nt_lo, nt_hi);
@@ -404,13 +460,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             }
             tc_fence_after();
             uint32_t acc[16];
-            tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 16, acc);
-            tmem_ld_wait();
+            tmem_ld16_sync(tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 16, acc);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(a));
 
-            const int v = vb + t * BN + slice * 16;
+            const int v = tile_col(t) + slice * 16;
             const int n = min(16, ve - v);
             if (!kFinal) {
                 const int us = t % kUStages;
@@ -425,14 +480,17 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 const uint32_t ub = sbase + kOffU + us * kUBytes + row * 128;
                 const uint4 lo = ld_shared_v4(ub + ((uint32_t)((2 * slice) ^ (row & 7)) << 4));
                 const uint4 hi = ld_shared_v4(ub + ((uint32_t)((2 * slice + 1) ^ (row & 7)) << 4));
+                // the refill of this stage is an async-proxy (TMA) write: order
+                // these generic-proxy reads before it, then release the stage
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_u(us));
-                if (!active || n <= 0) continue;
+                if (n <= 0) continue;  // warp-uniform: n depends on the tile and slice only
                 float z[16];
                 unpack16(lo, hi, z);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) z[i] += __uint_as_float(acc[i]);
-                if (p.z_out) {
+                if (p.z_out && active) {
                     float *zo = p.z_out + ((size_t)b * p.G + p.j) * p.V + v;
                     if (n == 16) {
 #pragma unroll
@@ -442,79 +500,84 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         for (int i = 0; i < n; ++i) zo[i] = z[i];
                     }
                 }
-                if (c2 == 0.f) {
+                if (active && c2 == 0.f) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         if (i < n) argmax_push(st, z[i], v + i);
-                } else {
-                    draft_sample16(st, Q, z, c2, n, v, y0c, y1c, sk, p.keys);
                 }
+                float s2[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) s2[i] = z[i] * c2;
+                const bool on = active && c2 > 0.f;
+                if (on) {
+                    const float kg = ordered_to_key(load_relaxed(row_best));
+                    if (kg > kbest) {
+                        kbest = kg;
+                        Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
+                    }
+                }
+                draft_sample16(st, Q, kbest, s2, n, v, on, row_best, y0c, y1c, sk, p.keys);
             } else {
-                if (!active || n <= 0) continue;
+                // take this tile's prefetched values, then prefetch the next tile's
+                // (before any skip: the skipped tile may come first when walking
+                // the segment backwards)
                 float u[16], tt[16];
                 unpack16(nu_lo, nu_hi, u);
                 unpack16(nt_lo, nt_hi, tt);
-                {   // prefetch the next tile's values
-                    const int vn = v + BN;
+                {
+                    const int vn = (t + 1 < ntiles) ? tile_col(t + 1) + slice * 16 : ve;
                     const int nn = min(16, ve - vn);
-                    if (t + 1 < ntiles && nn > 0) {
+                    if (active && t + 1 < ntiles && nn > 0) {
                         load16_bf16(trow + vn, nn, nt_lo, nt_hi);
                         if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
                     }
                 }
+                if (n <= 0) continue;  // warp-uniform
                 uint4 w[4];
 #pragma unroll
                 for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)v >> 2) + g, y0c, y1c, sk, p.keys);
-                // Candidate test: the key of token v is log2(r_v) - log2(E_v) with
-                // r_v = p_v - q_v (residual) or 2^(t_v c2) (bonus, unnormalised);
-                // it can beat the best key K only if (1 - u_v) < r_v 2^-K.
-                bool cand[16];
+                // Token v's key is log2(r_v) - log2(E_v) with r_v = p_v - q_v; a
+                // bonus row is a residual row with q = 0 and unnormalised p
+                // (lse_q2 = +inf, lse_t2 = 0).  It can beat the best key K only
+                // if (1 - u_v) < r_v 2^-K.
+                // upper bound of p - q under the approximate exponentials;
+                // rb <= 0 gives a threshold <= 1 <= f1: no candidate
+                auto rbound = [&](int i) -> float {
+                    const float z = u[i] + __uint_as_float(acc[i]);
+                    const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
+                    const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
+                    return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
+                };
+                bool gc[4];
                 bool any = false;
-                if (kind == 1) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float z = u[i] + __uint_as_float(acc[i]);
-                        const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
-                        const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
-                        // upper bound of p - q under the approximate exponentials
-                        const float rb = (pv - qv) + 4e-7f * (pv + qv);
-                        // rb <= 0 gives a threshold <= 1 <= f1: no candidate
-                        cand[i] = (i < n) &&
-                                  one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rb, Qr, 1.f);
-                        any |= cand[i];
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float rb = fast_exp2(fmaf(tt[i], c2, -rs.key_res)) * kMargin;
-                        cand[i] = (i < n) &&
-                                  one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rb, 1.f, 1.f);
-                        any |= cand[i];
-                    }
+                for (int g = 0; g < 4; ++g) {
+                    const float rmax = fmaxf(fmaxf(rbound(4 * g), rbound(4 * g + 1)),
+                                             fmaxf(rbound(4 * g + 2), rbound(4 * g + 3)));
+                    const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
+                    gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f);
+                    any |= gc[g];
                 }
-                if (any) {
+                if (__any_sync(0xffffffffu, any)) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        if (!cand[i]) continue;
-                        const float ln_e = fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
-                        float base;
-                        if (kind == 1) {
-                            const float z = u[i] + __uint_as_float(acc[i]);
-                            // log2 p - log2 q from the logit difference, then log2(p - q)
-                            const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
-                            if (!(delta2 > 0.f)) continue;
-                            const float l1 = delta2 > 20.f ? delta2 : fast_log2(expm1f(delta2 * kLn2));
-                            base = fmaf(z, c2, -lse_q2) + l1;
-                        } else {
-                            base = tt[i] * c2;
-                        }
-                        const float key = base - ln_e;
+                        if (!(__any_sync(0xffffffffu, gc[i >> 2]) && gc[i >> 2])) continue;
+                        if (!(one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rbound(i), Qr, 1.f)))
+                            continue;
+                        // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
+                        // log2 q formed from the logit difference first (+inf for bonus rows)
+                        const float z = u[i] + __uint_as_float(acc[i]);
+                        const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
+                        if (!(delta2 > 0.f)) continue;
+                        const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
+                        const float key = fmaf(tt[i], c2, -lse_t2) + l1 -
+                                          fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
                         if (key > rs.key_res) {
                             rs.key_res = key;
                             rs.idx_res = v + i;
-                            if (kind == 1) Qr = fminf(fast_exp2(-key), kQMax) * kMargin;
                         }
                     }
+                    Qr = fminf(fast_exp2(-rs.key_res), kQMax) * kMargin;
                 }
             }
         }
@@ -575,15 +638,18 @@ cudaError_t make_w_map(CUtensorMap *m, const void *w_out, int V, int r) {
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V) {
+// Base logits [B][G][V] as a 3-D tensor (V, G, B), boxes of BN columns x
+// 128 requests in the 128-byte swizzled layout.
+cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, int box_cols = BN) {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)G, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)G * V * 2};
-    cuuint32_t box[3] = {(cuuint32_t)BN, 1, (cuuint32_t)BM};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)BM};
     cuuint32_t estr[3] = {1, 1, 1};
+    const bool tile = (box_cols == BN);
     CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, tile ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -626,7 +692,7 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, 
     CUtensorMap mw, mu;
     cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
     if (e != cudaSuccess) return e;
-    if ((e = make_u_map(&mu, a.base, a.B, a.G, a.V)) != cudaSuccess) return e;
+    if ((e = make_u_map(&mu, a.base, a.B, a.G, a.V, BN)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
     TcParams p{};
     p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
@@ -640,9 +706,11 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, 
     p.V = a.V;
     p.r = a.r;
     p.j = j;
+    p.pass = j;
     p.nseg = pl.nsplit;
     p.keys = round_keys(a.seed);
     p.part = reinterpret_cast<RowState *>(a.ws + pl.partial_offset);
+    p.row_best = reinterpret_cast<uint32_t *>(a.ws + pl.row_best_offset);
     p.flags = reinterpret_cast<uint32_t *>(a.ws);
     p.z_out = a.z_out;
     markov_tc_kernel<false><<<dim3(pl.nsplit, pl.row_blocks), kThreads, kSmemBytes, s>>>(mw, mu, p);
@@ -670,6 +738,7 @@ cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     p.V = a.V;
     p.r = a.r;
     p.j = 0;
+    p.pass = a.pass;
     p.nseg = a.nseg;
     p.keys = round_keys(a.seed);
     p.rpart = reinterpret_cast<ResidualState *>(a.rpart);

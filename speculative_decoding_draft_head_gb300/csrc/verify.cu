@@ -412,9 +412,10 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     const bool tensor = p.tensor_residual && !a.z_in;
     const int res_nsplit = tensor ? p.res_split_tc : p.res_split;
     if (tensor) {
+        // the last draft launch (position G-1) walked in direction G-1: continue from its end
         FinalArgs fa{a.target, a.base, a.e_in, a.w_out, a.anchor, a.draft_tokens, a.temperature,
                      a.request_id, final_code, lse_t_row, a.draft_lse, a.B, a.G, a.V, a.r, res_nsplit,
-                     a.seed, res_part, flags};
+                     a.G, a.seed, res_part, flags};
         e = launch_final_tensor(fa, s);
     } else {
         const size_t smem = sizeof(float) * (size_t)a.r;
