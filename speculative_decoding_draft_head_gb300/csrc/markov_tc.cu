@@ -20,16 +20,29 @@
 //    logits + Markov bias) or accepted its whole block (bonus draw from p_L);
 //    other rows idle.  Base and target rows are read directly, one tile ahead.
 //
-// CTA layout (one CTA per SM, 576 threads, ~212 KB shared memory):
+// CTA layout (one CTA per SM, 608 threads, ~199 KB shared memory):
 //   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant of
-//               rows) and columns 16*(w/4).. of each 64-column tile;
-//   warp 16     TMA producer: W_out tiles (64 tokens x r, 128-byte swizzle,
-//               L2 evict-last) and base-logit tiles (evict-first);
-//   warp 17     TMEM allocator and UMMA issuer (M=128, N=64, K=16 steps).
-// The A operand (the 128 gathered E_in rows, 128 x r bf16) is built once per
-// CTA in the 128-byte swizzled K-major layout.  Rings: 3 W stages, 3 base
-// stages, 4 TMEM accumulators of 64 columns.  Every wait is bounded; a timeout
-// sets the timeout bit of the flag word and the CTA unwinds.
+//               rows) and columns 32*(w/4).. of each 128-column tile, as two
+//               16-column sub-slices;
+//   warp 16     TMA producer: W_out chunks (128 tokens x 64 of r, 128-byte
+//               swizzle, L2 evict-last) and base-logit tiles (two boxes of
+//               128 requests x 64 tokens, evict-first);
+//   warps 17-18 UMMA issuers for even / odd tiles (M=128, N=128, K=16 steps);
+//               warp 17 also allocates TMEM.
+// The A operand (the 128 gathered E_in rows, 128 x r bf16) is written once per
+// CTA into TMEM (columns 384..) and read from there by the bias UMMAs, which
+// leaves shared memory to the streams.  Rings: 8 W chunks (two tiles), 2 base
+// tiles (tile slots), 3 TMEM accumulators of 128 columns.  Tiles are as wide as a single
+// UMMA allows at this shape because every tcgen05.mma costs a roughly fixed
+// issue time whatever its N: wide tiles cut the instructions per token.  In
+// the draft the base-logit tile joins the contraction: after the r/16 bias
+// steps, eight N=16 UMMAs multiply 16-token slices of the tile (128 requests
+// x 128 tokens, already in the K-major A layout as TMA writes it) by a 16 x 16
+// identity into the matching accumulator columns, so TMEM holds z = U + bias
+// and the epilogue reads nothing from shared memory.  (U * 1 and U * 0 are
+// exact; base logits must be finite, since inf * 0 would poison the other
+// columns of its 16-wide step.)  Every wait is bounded; a timeout sets the
+// timeout bit of the flag word and the CTA unwinds.
 //
 // Gumbel-max without a logarithm per token: token v beats the running best
 // key K iff E_v < 2^(s2_v - K) = e_v * 2^(m - K), where e_v = 2^(s2_v - m) is
@@ -52,32 +65,37 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128;
-constexpr int BN = 64;
+constexpr int BN = 128;                  // tokens per tile: the UMMA N
 constexpr int kEpiWarps = 16;
 constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kThreads = 18 * 32;
-constexpr int kWStages = 3;
-constexpr int kUStages = 3;
-constexpr int kAccBufs = 4;
-constexpr uint32_t kTmemCols = kAccBufs * BN;  // 256
-constexpr uint32_t kAtomA = BM * 128;          // one 64-wide K atom of A: 16 KB
-constexpr uint32_t kAtomW = BN * 128;          // one 64-wide K atom of a W tile: 8 KB
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffW = kOffA + 4 * kAtomA;
-constexpr uint32_t kOffU = kOffW + kWStages * 4 * kAtomW;
-constexpr uint32_t kUBytes = BM * BN * 2;
+constexpr int kMmaWarp = 17;              // and kMmaWarp + 1: even / odd tiles
+constexpr int kThreads = 19 * 32;
+constexpr int kWStages = 8;              // W ring: one 64-wide K atom of one tile per stage
+constexpr int kUStages = 2;              // = tile slots: tile t fills slot t % 2
+constexpr int kAccBufs = 3;
+constexpr uint32_t kTmemCols = 512;      // 3 x 128 accumulator columns + A, power-of-two allocation
+constexpr uint32_t kTmemA = kAccBufs * BN;  // A operand: columns 384.. (r/2 columns, <= 128)
+constexpr uint32_t kWChunk = BN * 128;   // 128 tokens x 64 of r: 16 KB
+constexpr uint32_t kUHalf = BM * 128;    // 128 requests x 64 tokens: 16 KB (one TMA box)
+constexpr uint32_t kUBytes = 2 * kUHalf;
+constexpr uint32_t kOffW = 0;
+constexpr uint32_t kOffU = kOffW + kWStages * kWChunk;
+// 16 x 16 bf16 identity in the B-operand layout: eight N = 16 UMMAs per tile
+// add the base-logit tile (as an A operand) onto the bias accumulator
+constexpr uint32_t kOffI = kOffU + kUStages * kUBytes;
+constexpr uint32_t kIBytes = 16 * 128;
 // the slice merge after the last tile reuses the W ring (all UMMAs are done)
 constexpr uint32_t kOffMerge = kOffW;
 constexpr uint32_t kMergeBytes = BM * 4 * 32;
-static_assert(kMergeBytes <= kWStages * 4 * kAtomW, "merge scratch fits in the W ring");
-constexpr uint32_t kOffBar = kOffU + kUStages * kUBytes;
-constexpr int kNumBars = 2 * kWStages + 2 * kUStages + 2 * kAccBufs;
+static_assert(kMergeBytes <= kWStages * kWChunk, "merge scratch fits in the W ring");
+constexpr uint32_t kOffBar = kOffI + kIBytes;
+constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs;
 static_assert(kNumBars * 8 <= 256, "barrier region");
 constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kMiscBytes = 16 + BM * 16;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kTmemA + 128 <= kTmemCols, "TMEM accumulators and A operand");
 
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of clock cycles
 constexpr float kQMax = 0x1p126f;
@@ -141,63 +159,84 @@ __device__ __forceinline__ void load16_bf16(const __nv_bfloat16 *p, int n, uint4
     }
 }
 
-// Draft epilogue for 16 logits of one row (T > 0).  Every lane of the warp
-// calls it together (it votes across the warp); `on` is false for rows that
-// are greedy or inactive, which then change nothing.
+// Pairwise sum of 16 terms (short dependency chains).
+__device__ __forceinline__ float sum16(const float (&e)[16]) {
+    float s8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s8[i] = e[2 * i] + e[2 * i + 1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s8[i] += s8[i + 4];
+    return (s8[0] + s8[2]) + (s8[1] + s8[3]);
+}
+
+// Draft epilogue for 16 logits z of one row (T > 0, c2 = log2(e) / T), with
+// the draft-stream Philox words w of those tokens.  Every
+// lane of the warp calls it together (it votes across the warp); `on` is false
+// for rows that are greedy or inactive, which then change nothing.
 //
-// The softmax keeps a running reference m that may lag the true maximum:
-// terms 2^(s2 - m) above 1 are fine, and a batch whose sum exceeds 2^64 (or
-// overflows) is redone against its own maximum.  The candidate test runs per
-// Philox group of four tokens: the group's largest e against its smallest
-// 1 - u (largest word); only passing groups test their tokens one by one.
+// The softmax keeps a running reference m (log2 units) that may lag the true
+// maximum: terms 2^(z c2 - m) above 1 are fine, and a batch whose sum exceeds
+// 2^64 (or overflows) is redone against its own maximum.  The first batch of a
+// row segment takes its maximum as m and the exact key of that token as the
+// first best key, so later tokens face a tight threshold at once.  The
+// candidate test runs per Philox group of four tokens: the group's largest e
+// against its smallest 1 - u (largest word); only passing groups test their
+// tokens one by one.
 //
 // kbest is the best key known for the whole row: this thread's, or a larger
 // one another thread published in row_best (any token that cannot beat an
 // achieved key cannot be the row's Gumbel argmax, so it is skipped exactly).
 // A new best is published with atomicMax; readers see it a tile later.
-__device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kbest, const float (&s2)[16], int n,
-                                               int v, bool on, uint32_t *row_best, uint32_t y0c, uint32_t y1c,
-                                               uint32_t sk, const PhiloxRoundKeys &K) {
+__device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
+                                               int n, int v, bool on, uint32_t *row_best, const uint4 (&w)[4]) {
     const bool full = (n == 16);  // warp-uniform
     float e[16];
     if (on) {
-        if (st.m == -INFINITY) {  // first batch of this row segment: take its maximum
-            float cm = -INFINITY;
+        if (st.m == -INFINITY) {
+            float zm = z[0];
+            int im = 0;
+#pragma unroll
+            for (int i = 1; i < 16; ++i)
+                if ((full || i < n) && z[i] > zm) {
+                    zm = z[i];
+                    im = i;
+                }
+            st.m = zm * c2;  // c2 > 0: the rounded product is monotone in z
+            uint32_t word = 0;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                if (full || i < n) cm = fmaxf(cm, s2[i]);
-            st.m = cm;
-            Q = fminf(fast_exp2(cm - kbest), kQMax) * kMargin;
+                if (i == im) word = word_of(w[i >> 2], i & 3);
+            const float key = st.m - fast_log2(neg_log_uniform(word));
+            if (key > kbest) {
+                st.key = key;
+                st.s_at = st.m;
+                st.idx = v + im;
+                kbest = key;
+                atomicMax(row_best, key_to_ordered(key));
+            }
+            Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
-        float sum = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            e[i] = (full || i < n) ? fast_exp2(s2[i] - st.m) : 0.f;
-            sum += e[i];
-        }
+        for (int i = 0; i < 16; ++i) e[i] = (full || i < n) ? fast_exp2(fmaf(z[i], c2, -st.m)) : 0.f;
+        float sum = sum16(e);
         if (!(sum <= 0x1p64f)) {  // far above the reference (or overflow): renormalise
-            float cm = st.m;
+            float zm = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                if (full || i < n) cm = fmaxf(cm, s2[i]);
+                if (full || i < n) zm = fmaxf(zm, z[i]);
+            const float cm = fmaxf(st.m, zm * c2);
             st.S *= fast_exp2(st.m - cm);
             st.m = cm;
             Q = fminf(fast_exp2(cm - kbest), kQMax) * kMargin;
-            sum = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                e[i] = (full || i < n) ? fast_exp2(s2[i] - st.m) : 0.f;
-                sum += e[i];
-            }
+            for (int i = 0; i < 16; ++i) e[i] = (full || i < n) ? fast_exp2(fmaf(z[i], c2, -st.m)) : 0.f;
+            sum = sum16(e);
         }
         st.S += sum;
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) e[i] = 0.f;  // threshold 1 <= f1: no candidate
     }
-    uint4 w[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)v >> 2) + g, y0c, y1c, sk, K);
     bool gc[4];
     bool any = false;
 #pragma unroll
@@ -216,10 +255,11 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
                 const int i = 4 * g + c;
                 const uint32_t word = word_of(w[g], c);
                 if (!(one_minus_uniform_plus_one(word) < fmaf(e[i], Q, 1.f))) continue;
-                const float key = s2[i] - fast_log2(neg_log_uniform(word));
+                const float s2 = z[i] * c2;
+                const float key = s2 - fast_log2(neg_log_uniform(word));
                 if (key > kbest) {
                     st.key = key;
-                    st.s_at = s2[i];
+                    st.s_at = s2;
                     st.idx = v + i;
                     kbest = key;
                     atomicMax(row_best, key_to_ordered(key));
@@ -231,8 +271,9 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
 }
 
 // 18 warps: 5 share one SM sub-partition's 16K registers, so at most 96 each.
+// 19 warps: five share some SM sub-partition's 16K registers, so at most 96 each.
 template <bool kFinal>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(96)
 markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
                  const __grid_constant__ TcParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -251,12 +292,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     auto tile_col = [&](int t) { return vb + (reverse ? (ntiles - 1 - t) : t) * BN; };
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
-    auto full_w = [&](int s) { return bar(s); };
-    auto empty_w = [&](int s) { return bar(kWStages + s); };
-    auto full_u = [&](int s) { return bar(2 * kWStages + s); };
-    auto empty_u = [&](int s) { return bar(2 * kWStages + kUStages + s); };
-    auto tfull = [&](int a) { return bar(2 * kWStages + 2 * kUStages + a); };
-    auto tempty = [&](int a) { return bar(2 * kWStages + 2 * kUStages + kAccBufs + a); };
+    // full_tile(slot): every W chunk and the base-logit tile of one tile have
+    // landed; empty_w(stage): a W chunk was read; slot_free(slot): every UMMA
+    // of the slot's tile is done (its base tile is free and its full_tile
+    // phase has been consumed, so the slot may be armed again)
+    auto empty_w = [&](int s) { return bar(s); };
+    auto full_tile = [&](int s) { return bar(kWStages + s); };
+    auto slot_free = [&](int s) { return bar(kWStages + kUStages + s); };
+    auto tfull = [&](int a) { return bar(kWStages + 2 * kUStages + a); };
+    auto tempty = [&](int a) { return bar(kWStages + 2 * kUStages + kAccBufs + a); };
 
     int *misc = reinterpret_cast<int *>(smem + kOffMisc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
@@ -267,13 +311,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     int *row_code = misc + 4 + 3 * BM;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kWStages; ++s) {
-            mbar_init(full_w(s), 1);
-            mbar_init(empty_w(s), 1);
-        }
+        for (int s = 0; s < kWStages; ++s) mbar_init(empty_w(s), 1);  // released by the UMMAs
         for (int s = 0; s < kUStages; ++s) {
-            mbar_init(full_u(s), 1);
-            mbar_init(empty_u(s), kEpiWarps);
+            mbar_init(full_tile(s), 1);
+            mbar_init(slot_free(s), 1);
         }
         for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(tfull(a), 1);
@@ -285,6 +326,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
+        tc_fence_before();
     }
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&map_w);
@@ -321,82 +363,142 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         row_code[threadIdx.x] = code;
     }
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
 
-    // A operand: gathered E_in rows, 128-byte swizzled K-major atoms of 64 K.
+    // A operand in TMEM: lane = request row, K in pairs per 32-bit column.
+    // Warp w writes K elements 64 (w / 4) .. + 63 of the rows of its quadrant.
     if (warp < kEpiWarps) {
-        const int nchunk = p.r >> 3;  // 16-byte chunks per row
-        for (int i = threadIdx.x; i < BM * nchunk; i += kEpiWarps * 32) {
-            const int row = i / nchunk, c = i - row * nchunk;
+        const int q = warp & 3, cc = warp >> 2;
+        const int row = q * 32 + lane;
+        const int k0 = cc * 64;
+        if (k0 < p.r) {
             const int prev = row_prev[row];
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (prev >= 0) val = __ldg(reinterpret_cast<const uint4 *>(p.e_in + (size_t)prev * p.r) + c);
-            const int atom = c >> 3, cc = c & 7;
-            st_shared_v4(sbase + kOffA + atom * kAtomA + row * 128 + ((cc ^ (row & 7)) << 4), val);
+            const int nk = min(64, p.r - k0);  // a multiple of 16
+            uint32_t av[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                if (prev >= 0 && 8 * i < nk) val = __ldg(reinterpret_cast<const uint4 *>(p.e_in + (size_t)prev * p.r + k0) + i);
+                av[4 * i] = val.x;
+                av[4 * i + 1] = val.y;
+                av[4 * i + 2] = val.z;
+                av[4 * i + 3] = val.w;
+            }
+            tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(cc * 32), av);
+            tmem_st_wait();
+        }
+        if (!kFinal && threadIdx.x < 16 * 8) {
+            // identity row n (16 rows of 128 bytes): a single 1.0 at k = n;
+            // 16-byte chunk c of row n sits at position c ^ (n & 7)
+            const int n = threadIdx.x >> 3, pos = threadIdx.x & 7, c = pos ^ (n & 7);
+            const uint32_t one = (c == (n >> 3)) ? ((n & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
+            const int wsel = (n & 7) >> 1;
+            st_shared_v4(sbase + kOffI + n * 128 + (pos << 4),
+                         make_uint4(wsel == 0 ? one : 0u, wsel == 1 ? one : 0u, wsel == 2 ? one : 0u,
+                                    wsel == 3 ? one : 0u));
         }
         fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
     const int n_katoms = (p.r + 63) >> 6;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_last();
             const uint64_t pol_u = policy_evict_first();
-            for (int t = 0; t < ntiles; ++t) {
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
                 const int v0 = tile_col(t);
-                const int ws = t % kWStages;
-                const uint32_t wph = (uint32_t)(t / kWStages) & 1u;
-                if (t >= kWStages && !mbar_wait(empty_w(ws), wph ^ 1u, abort, kSpinLimit)) {
-                    *abort = 1;
-                    atomicOr(p.flags, kFlagTimeout);
-                    break;
-                }
-                mbar_arrive_expect_tx(full_w(ws), n_katoms * kAtomW);
-                for (int kb = 0; kb < n_katoms; ++kb)
-                    tma_load_2d(sbase + kOffW + ws * 4 * kAtomW + kb * kAtomW, &map_w, full_w(ws), kb * 64, v0,
-                                pol_w);
-                if (!kFinal) {
-                    const int us = t % kUStages;
-                    const uint32_t uph = (uint32_t)(t / kUStages) & 1u;
-                    if (t >= kUStages && !mbar_wait(empty_u(us), uph ^ 1u, abort, kSpinLimit)) {
-                        *abort = 1;
-                        atomicOr(p.flags, kFlagTimeout);
+                const int slot = t % kUStages;
+                // the second 64-token box lies past the vocabulary only at its end
+                const bool two = v0 + 64 < p.V;
+                const uint32_t u_bytes = kFinal ? 0u : (two ? kUBytes : kUHalf);
+                for (int kb = 0; kb < n_katoms; ++kb) {
+                    const int c = t * n_katoms + kb;
+                    const int ws = c % kWStages;
+                    const uint32_t wph = (uint32_t)(c / kWStages) & 1u;
+                    if (c >= kWStages && !mbar_wait(empty_w(ws), wph ^ 1u, abort, kSpinLimit)) {
+                        ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_u(us), kUBytes);
-                    tma_load_3d(sbase + kOffU + us * kUBytes, &map_u, full_u(us), v0, p.j, m0, pol_u);
+                    if (kb == 0) {
+                        if (t >= kUStages &&
+                            !mbar_wait(slot_free(slot), ((uint32_t)(t / kUStages) & 1u) ^ 1u, abort, kSpinLimit)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full_tile(slot), n_katoms * kWChunk + u_bytes);
+                    }
+                    tma_load_2d(sbase + kOffW + ws * kWChunk, &map_w, full_tile(slot), kb * 64, v0, pol_w);
                 }
+                if (ok && !kFinal) {
+                    tma_load_3d(sbase + kOffU + slot * kUBytes, &map_u, full_tile(slot), v0, p.j, m0, pol_u);
+                    if (two)
+                        tma_load_3d(sbase + kOffU + slot * kUBytes + kUHalf, &map_u, full_tile(slot), v0 + 64, p.j, m0,
+                                    pol_u);
+                }
+            }
+            if (!ok) {
+                *abort = 1;
+                atomicOr(p.flags, kFlagTimeout);
             }
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // two issuers, even and odd tiles: a tcgen05.mma costs a roughly fixed
+        // issue time, so one thread alone cannot keep the tensor core busy
+        // while the epilogue warps share its sub-partition
         if (lane == 0) {
+            const int par = warp - kMmaWarp;
             const uint32_t idesc = idesc_bf16_f32(BM, BN);
+            const uint32_t idesc16 = idesc_bf16_f32(BM, 16);
             const int ksteps = p.r >> 4;
-            for (int t = 0; t < ntiles; ++t) {
-                const int ws = t % kWStages;
-                const uint32_t wph = (uint32_t)(t / kWStages) & 1u;
+            // descriptors step in 16-byte units in their low word: K-step s of a
+            // 64-wide atom sits at byte 32 (s % 4) of each 128-byte swizzled row
+            const uint64_t d_w = sw128_kmajor_desc(sbase + kOffW);
+            const uint32_t w_lo0 = (uint32_t)d_w, desc_hi = (uint32_t)(d_w >> 32);
+            const uint32_t u_lo0 = (uint32_t)sw128_kmajor_desc(sbase + kOffU);
+            const uint32_t i_lo = (uint32_t)sw128_kmajor_desc(sbase + kOffI);
+            bool ok = true;
+            for (int t = par; t < ntiles; t += 2) {
                 const int a = t % kAccBufs;
-                const uint32_t aph = (uint32_t)(t / kAccBufs) & 1u;
-                if (!mbar_wait(full_w(ws), wph, abort, kSpinLimit) ||
-                    (t >= kAccBufs && !mbar_wait(tempty(a), aph ^ 1u, abort, kSpinLimit))) {
-                    *abort = 1;
-                    atomicOr(p.flags, kFlagTimeout);
+                const int slot = t % kUStages;  // = par
+                if ((t >= kAccBufs &&
+                     !mbar_wait(tempty(a), ((uint32_t)(t / kAccBufs) & 1u) ^ 1u, abort, kSpinLimit)) ||
+                    !mbar_wait(full_tile(slot), (uint32_t)(t / kUStages) & 1u, abort, kSpinLimit)) {
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + a * BN;
-                for (int s = 0; s < ksteps; ++s) {
-                    const uint32_t kb = (uint32_t)s >> 2, ko = ((uint32_t)s & 3u) * 32u;
-                    const uint64_t ad = sw128_kmajor_desc(sbase + kOffA + kb * kAtomA + ko);
-                    const uint64_t bd = sw128_kmajor_desc(sbase + kOffW + ws * 4 * kAtomW + kb * kAtomW + ko);
-                    umma_bf16(d_tmem, ad, bd, idesc, s > 0 ? 1u : 0u);
+                for (int kb = 0; kb < n_katoms; ++kb) {
+                    const int ws = (t * n_katoms + kb) % kWStages;
+                    const uint32_t w_lo = w_lo0 + ws * (kWChunk >> 4);
+                    // K-step s = 4 kb + k4: A columns 8 s .. 8 s + 7 of the TMEM copy
+                    const uint32_t a_tm = tmem_base + kTmemA + (uint32_t)(32 * kb);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        if (4 * kb + k4 < ksteps)
+                            umma_bf16_ts(d_tmem, a_tm + 8 * k4, w_lo + 2 * k4, desc_hi, idesc, (kb | k4) ? 1u : 0u);
+                    umma_commit(empty_w(ws));
                 }
-                umma_commit(empty_w(ws));
+                if (!kFinal) {
+                    // + base-logit tile: columns 16 s .. 16 s + 15 get U x identity
+                    const uint32_t u_lo = u_lo0 + slot * (kUBytes >> 4);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        umma_bf16_w(d_tmem + 16 * s, u_lo + (s >> 2) * (kUHalf >> 4) + 2 * (s & 3), i_lo, desc_hi,
+                                    idesc16, 1u);
+                }
+                umma_commit(slot_free(slot));
                 umma_commit(tfull(a));
+            }
+            if (!ok) {
+                *abort = 1;
+                atomicOr(p.flags, kFlagTimeout);
             }
         }
         __syncwarp();
@@ -423,6 +525,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         float Q = kQMax;
         float kbest = -INFINITY;  // best key of the row known to this thread
         uint32_t *row_best = (kFinal || b >= p.B) ? nullptr : p.row_best + (size_t)p.j * p.B + b;
+        uint32_t kg_next = 0u;  // "none"
         float Qr = kQMax;  // 2^-K for the residual candidate test (with margin)
         ResidualState rs = residual_init();
         float lse_q2 = 0.f, lse_t2 = 0.f;
@@ -438,146 +541,148 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 lse_t2 = 0.f;       // unnormalised p: the same argmax
             }
         }
-        // final draw: this thread's base / target values, one tile ahead
+        // this thread's 16-token sub-slice h of tile t
+        auto sub_col = [&](int t, int h) { return tile_col(t) + slice * 32 + h * 16; };
+        // final draw: this thread's base / target values, one sub-slice ahead
         uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
         if (kFinal && active && ntiles > 0) {
-            const int v = tile_col(0) + slice * 16;
+            const int v = sub_col(0, 0);
             const int n = min(16, ve - v);
             if (n > 0) {
                 load16_bf16(trow + v, n, nt_lo, nt_hi);
                 if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
             }
         }
-        for (int t = 0; t < ntiles; ++t) {
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
             const int a = t % kAccBufs;
             const uint32_t aph = (uint32_t)(t / kAccBufs) & 1u;
-            if (!uniform_wait(tfull(a), aph, abort)) {
-                if (lane == 0) {
-                    *abort = 1;
-                    atomicOr(p.flags, kFlagTimeout);
-                }
-                break;
-            }
-            tc_fence_after();
-            uint32_t acc[16];
-            tmem_ld16_sync(tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 16, acc);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty(a));
-
-            const int v = tile_col(t) + slice * 16;
-            const int n = min(16, ve - v);
-            if (!kFinal) {
-                const int us = t % kUStages;
-                const uint32_t uph = (uint32_t)(t / kUStages) & 1u;
-                if (!uniform_wait(full_u(us), uph, abort)) {
-                    if (lane == 0) {
-                        *abort = 1;
-                        atomicOr(p.flags, kFlagTimeout);
-                    }
-                    break;
-                }
-                const uint32_t ub = sbase + kOffU + us * kUBytes + row * 128;
-                const uint4 lo = ld_shared_v4(ub + ((uint32_t)((2 * slice) ^ (row & 7)) << 4));
-                const uint4 hi = ld_shared_v4(ub + ((uint32_t)((2 * slice + 1) ^ (row & 7)) << 4));
-                // the refill of this stage is an async-proxy (TMA) write: order
-                // these generic-proxy reads before it, then release the stage
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_u(us));
-                if (n <= 0) continue;  // warp-uniform: n depends on the tile and slice only
-                float z[16];
-                unpack16(lo, hi, z);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) z[i] += __uint_as_float(acc[i]);
-                if (p.z_out && active) {
-                    float *zo = p.z_out + ((size_t)b * p.G + p.j) * p.V + v;
-                    if (n == 16) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<float4 *>(zo + i) = make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
-                    } else {
-                        for (int i = 0; i < n; ++i) zo[i] = z[i];
-                    }
-                }
-                if (active && c2 == 0.f) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (i < n) argmax_push(st, z[i], v + i);
-                }
-                float s2[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) s2[i] = z[i] * c2;
-                const bool on = active && c2 > 0.f;
-                if (on) {
-                    const float kg = ordered_to_key(load_relaxed(row_best));
-                    if (kg > kbest) {
-                        kbest = kg;
-                        Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
-                    }
-                }
-                draft_sample16(st, Q, kbest, s2, n, v, on, row_best, y0c, y1c, sk, p.keys);
-            } else {
-                // take this tile's prefetched values, then prefetch the next tile's
-                // (before any skip: the skipped tile may come first when walking
-                // the segment backwards)
-                float u[16], tt[16];
-                unpack16(nu_lo, nu_hi, u);
-                unpack16(nt_lo, nt_hi, tt);
-                {
-                    const int vn = (t + 1 < ntiles) ? tile_col(t + 1) + slice * 16 : ve;
-                    const int nn = min(16, ve - vn);
-                    if (active && t + 1 < ntiles && nn > 0) {
-                        load16_bf16(trow + vn, nn, nt_lo, nt_hi);
-                        if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
-                    }
-                }
-                if (n <= 0) continue;  // warp-uniform
+            for (int h = 0; h < 2; ++h) {
+                // the Philox words need nothing from the tensor cores: draw them
+                // first, while the tile's UMMAs may still be running
                 uint4 w[4];
+                {
+                    const int vw = sub_col(t, h);
+                    if (vw < ve) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)v >> 2) + g, y0c, y1c, sk, p.keys);
-                // Token v's key is log2(r_v) - log2(E_v) with r_v = p_v - q_v; a
-                // bonus row is a residual row with q = 0 and unnormalised p
-                // (lse_q2 = +inf, lse_t2 = 0).  It can beat the best key K only
-                // if (1 - u_v) < r_v 2^-K.
-                // upper bound of p - q under the approximate exponentials;
-                // rb <= 0 gives a threshold <= 1 <= f1: no candidate
-                auto rbound = [&](int i) -> float {
-                    const float z = u[i] + __uint_as_float(acc[i]);
-                    const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
-                    const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
-                    return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
-                };
-                bool gc[4];
-                bool any = false;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const float rmax = fmaxf(fmaxf(rbound(4 * g), rbound(4 * g + 1)),
-                                             fmaxf(rbound(4 * g + 2), rbound(4 * g + 3)));
-                    const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
-                    gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f);
-                    any |= gc[g];
+                        for (int g = 0; g < 4; ++g)
+                            w[g] = philox_folded(((uint32_t)vw >> 2) + g, y0c, y1c, sk, p.keys);
+                    }
                 }
-                if (__any_sync(0xffffffffu, any)) {
+                if (h == 0) {
+                    if (!uniform_wait(tfull(a), aph, abort)) {
+                        if (lane == 0) {
+                            *abort = 1;
+                            atomicOr(p.flags, kFlagTimeout);
+                        }
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                uint32_t acc[16];
+                tmem_ld16_sync(tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 32 + h * 16, acc);
+                if (h == 1) {  // both halves are in registers: hand the accumulator back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty(a));
+                }
+                const int v = sub_col(t, h);
+                const int n = min(16, ve - v);
+                if (!kFinal) {
+                    if (n <= 0) continue;  // warp-uniform: n depends on the tile and slice only
+                    float z[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (!(__any_sync(0xffffffffu, gc[i >> 2]) && gc[i >> 2])) continue;
-                        if (!(one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rbound(i), Qr, 1.f)))
-                            continue;
-                        // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
-                        // log2 q formed from the logit difference first (+inf for bonus rows)
-                        const float z = u[i] + __uint_as_float(acc[i]);
-                        const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
-                        if (!(delta2 > 0.f)) continue;
-                        const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
-                        const float key = fmaf(tt[i], c2, -lse_t2) + l1 -
-                                          fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
-                        if (key > rs.key_res) {
-                            rs.key_res = key;
-                            rs.idx_res = v + i;
+                    for (int i = 0; i < 16; ++i) z[i] = __uint_as_float(acc[i]);
+                    if (p.z_out && active) {
+                        float *zo = p.z_out + ((size_t)b * p.G + p.j) * p.V + v;
+                        if (n == 16) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4)
+                                *reinterpret_cast<float4 *>(zo + i) = make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (i < n) zo[i] = z[i];  // static index: z stays in registers
                         }
                     }
-                    Qr = fminf(fast_exp2(-rs.key_res), kQMax) * kMargin;
+                    if (active && c2 == 0.f) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (i < n) argmax_push(st, z[i], v + i);
+                    }
+                    const bool on = active && c2 > 0.f;
+                    if (on) {
+                        // the row-wide best key loaded one tile earlier; reload for the next
+                        const float kg = ordered_to_key(kg_next);
+                        kg_next = load_relaxed(row_best);
+                        if (kg > kbest) {
+                            kbest = kg;
+                            Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
+                        }
+                    }
+                    draft_sample16(st, Q, kbest, z, c2, n, v, on, row_best, w);
+                } else {
+                    // take this sub-slice's prefetched values, then prefetch the next
+                    // one's (before any skip: the skipped sub-slice may come first
+                    // when walking the segment backwards)
+                    float u[16], tt[16];
+                    unpack16(nu_lo, nu_hi, u);
+                    unpack16(nt_lo, nt_hi, tt);
+                    {
+                        const int tn = t + h, hn = h ^ 1;  // the next sub-slice
+                        const int vn = (tn < ntiles) ? sub_col(tn, hn) : ve;
+                        const int nn = min(16, ve - vn);
+                        if (active && tn < ntiles && nn > 0) {
+                            load16_bf16(trow + vn, nn, nt_lo, nt_hi);
+                            if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
+                        }
+                    }
+                    if (n <= 0) continue;  // warp-uniform
+                    // Token v's key is log2(r_v) - log2(E_v) with r_v = p_v - q_v; a
+                    // bonus row is a residual row with q = 0 and unnormalised p
+                    // (lse_q2 = +inf, lse_t2 = 0).  It can beat the best key K only
+                    // if (1 - u_v) < r_v 2^-K.
+                    // upper bound of p - q under the approximate exponentials;
+                    // rb <= 0 gives a threshold <= 1 <= f1: no candidate
+                    auto rbound = [&](int i) -> float {
+                        const float z = u[i] + __uint_as_float(acc[i]);
+                        const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
+                        const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
+                        return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
+                    };
+                    bool gc[4];
+                    bool any = false;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const float rmax = fmaxf(fmaxf(rbound(4 * g), rbound(4 * g + 1)),
+                                                 fmaxf(rbound(4 * g + 2), rbound(4 * g + 3)));
+                        const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
+                        gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f);
+                        any |= gc[g];
+                    }
+                    if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (!(__any_sync(0xffffffffu, gc[i >> 2]) && gc[i >> 2])) continue;
+                            if (!(one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rbound(i), Qr, 1.f)))
+                                continue;
+                            // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
+                            // log2 q formed from the logit difference first (+inf for bonus rows)
+                            const float z = u[i] + __uint_as_float(acc[i]);
+                            const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
+                            if (!(delta2 > 0.f)) continue;
+                            const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
+                            const float key = fmaf(tt[i], c2, -lse_t2) + l1 -
+                                              fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
+                            if (key > rs.key_res) {
+                                rs.key_res = key;
+                                rs.idx_res = v + i;
+                            }
+                        }
+                        Qr = fminf(fast_exp2(-rs.key_res), kQMax) * kMargin;
+                    }
                 }
             }
         }
@@ -638,16 +743,16 @@ cudaError_t make_w_map(CUtensorMap *m, const void *w_out, int V, int r) {
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Base logits [B][G][V] as a 3-D tensor (V, G, B), boxes of BN columns x
-// 128 requests in the 128-byte swizzled layout.
-cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, int box_cols = BN) {
+// Base logits [B][G][V] as a 3-D tensor (V, G, B), boxes of 64 columns x
+// 128 requests in the 128-byte swizzled layout (two boxes per tile).
+cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, int box_cols = 64) {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)G, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)G * V * 2};
     cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)BM};
     cuuint32_t estr[3] = {1, 1, 1};
-    const bool tile = (box_cols == BN);
+    const bool tile = (box_cols == 64);
     CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, tile ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -692,7 +797,7 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, 
     CUtensorMap mw, mu;
     cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
     if (e != cudaSuccess) return e;
-    if ((e = make_u_map(&mu, a.base, a.B, a.G, a.V, BN)) != cudaSuccess) return e;
+    if ((e = make_u_map(&mu, a.base, a.B, a.G, a.V, 64)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
     TcParams p{};
     p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
