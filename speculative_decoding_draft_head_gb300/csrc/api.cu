@@ -95,17 +95,24 @@ dspark_status dspark_draft_sample(const void *base_logits, const void *e_in, con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
-    if (plan.tensor_path) {
-        e = cudaMemsetAsync(static_cast<unsigned char *>(workspace) + plan.row_best_offset, 0,
-                            sizeof(uint32_t) * (size_t)B * (size_t)G, s);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the row-wide best keys");
-    }
     DraftArgs a{base_logits, e_in, w_out, anchor, temperature, request_id, B, G, V, r, dtype, seed,
                 draft_tokens, draft_lse, draft_logq, draft_logits, static_cast<unsigned char *>(workspace)};
-    for (int j = 0; j < G; ++j) {
-        e = plan.tensor_path ? launch_draft_tensor(a, plan, j, s) : launch_draft_simt(a, plan, j, s);
+    if (plan.tensor_path) {
+        e = cudaMemsetAsync(static_cast<unsigned char *>(workspace) + plan.best_offset, 0,
+                            sizeof(unsigned long long) * (size_t)B * (size_t)G, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the row-wide best words");
+        // the tokens feed the next position through the best words; the
+        // partials of every position are merged once at the end
+        e = launch_draft_tensor(a, plan, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft sample launch");
-        e = launch_draft_finalize(a, plan, j, s);
+        e = launch_draft_finalize(a, plan, 0, G, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
+        return DSPARK_OK;
+    }
+    for (int j = 0; j < G; ++j) {
+        e = launch_draft_simt(a, plan, j, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft sample launch");
+        e = launch_draft_finalize(a, plan, j, 1, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
     }
     return DSPARK_OK;

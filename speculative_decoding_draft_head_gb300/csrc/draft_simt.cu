@@ -132,16 +132,19 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
     }
 }
 
-// One warp per request: merge the segment partials, write token, lse, logq.
-__global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsplit,
-                                      const float *__restrict__ temperature, int B, int G, int j,
+// One warp per (request, position): merge the segment partials, write token,
+// lse, logq.  Position j0 + k reads its partials at part + k * pos_stride.
+__global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsplit, size_t pos_stride,
+                                      const float *__restrict__ temperature, int B, int G, int j0, int npos,
                                       int32_t *__restrict__ tokens, float *__restrict__ lse,
                                       float *__restrict__ logq) {
-    const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (b >= B) return;
+    if (gw >= B * npos) return;
+    const int k = gw / B, b = gw - k * B, j = j0 + k;
+    const RowState *pr = part + (size_t)k * pos_stride;
     RowState s = row_state_init();
-    for (int i = lane; i < nsplit; i += 32) row_state_merge(s, part[(size_t)b * nsplit + i]);
+    for (int i = lane; i < nsplit; i += 32) row_state_merge(s, pr[(size_t)b * nsplit + i]);
     s = warp_merge(s);
     if (lane != 0) return;
     const size_t o = (size_t)b * G + j;
@@ -185,11 +188,16 @@ cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cud
     return cudaGetLastError();
 }
 
-cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s) {
+cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, int npos, cudaStream_t s) {
+    // the tensor path keeps every position's partials ([G][B][nsplit]); the
+    // SIMT path reuses one [B][nsplit] array per position
     const RowState *part = reinterpret_cast<const RowState *>(a.ws + p.partial_offset);
+    const size_t pos_stride = p.tensor_path ? (size_t)a.B * p.nsplit : 0;
+    if (p.tensor_path) part += (size_t)j * pos_stride;
     const int warps = 4;
-    draft_finalize_kernel<<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
-        part, p.nsplit, a.temperature, a.B, a.G, j, a.tokens, a.lse, a.logq);
+    const int rows = a.B * npos;
+    draft_finalize_kernel<<<(rows + warps - 1) / warps, 32 * warps, 0, s>>>(
+        part, p.nsplit, pos_stride, a.temperature, a.B, a.G, j, npos, a.tokens, a.lse, a.logq);
     return cudaGetLastError();
 }
 
@@ -217,8 +225,10 @@ DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
         p.nsplit = (V + chunk - 1) / chunk;
         p.chunk = chunk;
     }
-    p.row_best_offset = align_up(p.partial_offset + sizeof(RowState) * (size_t)B * p.nsplit, 256);
-    p.ws_bytes = align_up(p.row_best_offset + sizeof(uint32_t) * (size_t)B * (size_t)G, 256);
+    const size_t npart = (size_t)B * p.nsplit * (p.tensor_path ? (size_t)G : 1);
+    p.best_offset = align_up(p.partial_offset + sizeof(RowState) * npart, 256);
+    p.ws_bytes = align_up(p.best_offset + (p.tensor_path ? sizeof(unsigned long long) * (size_t)B * (size_t)G : 0),
+                          256);
     return p;
 }
 

@@ -11,6 +11,7 @@ namespace dspark {
 
 constexpr int kNumSMs = 152;            // GB300: 2 dies x 76 SMs
 constexpr size_t kFlagBytes = 256;      // flag word region at the head of every workspace
+constexpr size_t kGridBarOffset = 64;   // grid-barrier counter of the draft kernel, inside the flag region
 constexpr int kMaxG = 64;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -25,8 +26,8 @@ struct DraftPlan {
     int row_blocks;        // SIMT: ceil(B / rows_per_block); tensor path: M tiles
     int nsplit;            // vocabulary segments per row (partials per row)
     int chunk;             // vocabulary entries per segment (multiple of 4)
-    size_t partial_offset; // byte offset of the per-(row, segment) partials
-    size_t row_best_offset;// [G][B] uint32 row-wide best keys (tensor path), zeroed per call
+    size_t partial_offset; // byte offset of the per-(row, segment) partials ([G][B][nsplit] on the tensor path)
+    size_t best_offset;    // [G][B] 64-bit row-wide best (key, token) words (tensor path), zeroed per call
     size_t ws_bytes;
 };
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt);
@@ -48,8 +49,10 @@ struct DraftArgs {
     unsigned char *ws;
 };
 cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
-cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
-cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
+// merges the partials of positions j .. j + npos - 1 into tokens, lse and log q
+cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, int npos, cudaStream_t s);
+// every block position (one cooperative launch, else one launch per position)
+cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &p, cudaStream_t s);
 
 // tensor-core kernel geometry (bf16): 128-request row blocks x vocabulary segments
 int tc_row_blocks(int B);

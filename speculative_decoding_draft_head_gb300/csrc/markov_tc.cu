@@ -84,12 +84,12 @@ constexpr uint32_t kOffU = kOffW + kWStages * kWChunk;
 // add the base-logit tile (as an A operand) onto the bias accumulator
 constexpr uint32_t kOffI = kOffU + kUStages * kUBytes;
 constexpr uint32_t kIBytes = 16 * 128;
-// the slice merge after the last tile reuses the W ring (all UMMAs are done)
-constexpr uint32_t kOffMerge = kOffW;
+// per-row merge of the four column slices (the W ring keeps streaming the
+// next block position meanwhile)
+constexpr uint32_t kOffMerge = kOffI + kIBytes;
 constexpr uint32_t kMergeBytes = BM * 4 * 32;
-static_assert(kMergeBytes <= kWStages * kWChunk, "merge scratch fits in the W ring");
-constexpr uint32_t kOffBar = kOffI + kIBytes;
-constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs;
+constexpr uint32_t kOffBar = kOffMerge + kMergeBytes;
+constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs + 1;
 static_assert(kNumBars * 8 <= 256, "barrier region");
 constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kMiscBytes = 16 + BM * 16;
@@ -112,15 +112,54 @@ struct TcParams {
     const int32_t *final_code;  // [B]: -1, or (kind << 16) | position
     const float *lse_t_row;     // [B] target lse of the rejected row, log2 units
     const float *draft_lse;     // [B][G] natural log
-    int B, G, V, r, j, nseg;
-    int pass;                   // launch counter: odd passes walk the segment backwards
+    int B, G, V, r;
+    int j, j_end;               // draft: block positions j .. j_end - 1 in this launch
+    int nseg;
+    int pass;                   // final draw: odd passes walk the segment backwards
     PhiloxRoundKeys keys;
-    RowState *part;
-    uint32_t *row_best;         // [G][B] draft / [B] final: row-wide best key (ordered encoding)
+    RowState *part;             // draft: [G][B][nseg] softmax / key partials
+    unsigned long long *best;   // draft: [G][B] row-wide best (key, token), see best_encode
+    unsigned int *grid_bar;     // draft, several positions: arrival counter of the grid barrier
     ResidualState *rpart;
     uint32_t *flags;
     float *z_out;
 };
+
+// Row-wide best draw of a block position as one 64-bit word: the key's
+// order-preserving encoding above the complemented token id, so that
+// atomicMax keeps the largest key and, on an exact tie, the lowest id (the
+// merge rule of the partial states).  0 means "none".
+__device__ __forceinline__ unsigned long long best_encode(float key, int idx) {
+    return ((unsigned long long)key_to_ordered(key) << 32) | (unsigned long long)(~(uint32_t)idx);
+}
+__device__ __forceinline__ int best_token(unsigned long long w) { return w ? (int)~(uint32_t)w : -1; }
+__device__ __forceinline__ unsigned long long load_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned int load_acquire_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier between block positions (one thread per CTA; the launch
+// is cooperative, so every CTA is resident).  Bounded: gives up after about
+// `limit` cycles or when this CTA has aborted.
+__device__ __forceinline__ bool grid_sync(unsigned int *ctr, unsigned int target, volatile int *abort,
+                                          long long limit) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const long long t0 = clock64();
+    while (load_acquire_u32(ctr) < target) {
+        if (*abort) return false;
+        if (clock64() - t0 > limit) return false;
+        __nanosleep(64);
+    }
+    __threadfence();
+    return true;
+}
 
 __device__ __forceinline__ int seg_begin(int s, int nseg, int V) {
     if (s >= nseg) return V;
@@ -184,11 +223,12 @@ __device__ __forceinline__ float sum16(const float (&e)[16]) {
 // tokens one by one.
 //
 // kbest is the best key known for the whole row: this thread's, or a larger
-// one another thread published in row_best (any token that cannot beat an
+// one another thread published in the row's best word (any token that cannot beat an
 // achieved key cannot be the row's Gumbel argmax, so it is skipped exactly).
 // A new best is published with atomicMax; readers see it a tile later.
 __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
-                                               int n, int v, bool on, uint32_t *row_best, const uint4 (&w)[4]) {
+                                               int n, int v, bool on, unsigned long long *best,
+                                               const uint4 (&w)[4]) {
     const bool full = (n == 16);  // warp-uniform
     float e[16];
     if (on) {
@@ -212,7 +252,7 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
                 st.s_at = st.m;
                 st.idx = v + im;
                 kbest = key;
-                atomicMax(row_best, key_to_ordered(key));
+                atomicMax(best, best_encode(key, v + im));
             }
             Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
@@ -262,7 +302,7 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
                     st.s_at = s2;
                     st.idx = v + i;
                     kbest = key;
-                    atomicMax(row_best, key_to_ordered(key));
+                    atomicMax(best, best_encode(key, v + i));
                 }
             }
         }
@@ -272,6 +312,14 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
 
 // 18 warps: 5 share one SM sub-partition's 16K registers, so at most 96 each.
 // 19 warps: five share some SM sub-partition's 16K registers, so at most 96 each.
+//
+// The draft form walks block positions p.j .. p.j_end - 1 in one launch when
+// the launch is cooperative: between positions every CTA publishes its rows'
+// best (key, token) words and meets the others at a grid barrier; then the
+// epilogue warps read x_j, gather the E_in rows of the next position into the
+// TMEM A operand and release the MMA warps (a_ready), while the producer has
+// already been streaming the next position's W_out and base-logit tiles.
+// Tile, ring and accumulator counters run on across positions.
 template <bool kFinal>
 __global__ void __maxnreg__(96)
 markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
@@ -286,29 +334,37 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     const int vb = seg_begin(seg, p.nseg, p.V);
     const int ve = seg_begin(seg + 1, p.nseg, p.V);
     const int ntiles = (ve - vb + BN - 1) / BN;
-    // Odd launches walk the segment backwards: each launch then starts on
-    // the W_out tiles the previous launch touched last, which are still in L2.
-    const bool reverse = (p.pass & 1) != 0;
-    auto tile_col = [&](int t) { return vb + (reverse ? (ntiles - 1 - t) : t) * BN; };
+    const int npos = kFinal ? 1 : p.j_end - p.j;
+    const int total = npos * ntiles;  // tiles of all positions, in order
+    // Odd positions (odd passes of the final draw) walk the segment backwards:
+    // each then starts on the W_out tiles the previous one touched last, which
+    // are still in L2.
+    auto tile_col = [&](int tg) {
+        const int pi = tg / ntiles, t = tg - pi * ntiles;
+        const bool reverse = (((kFinal ? p.pass : p.j + pi)) & 1) != 0;
+        return vb + (reverse ? (ntiles - 1 - t) : t) * BN;
+    };
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
     // full_tile(slot): every W chunk and the base-logit tile of one tile have
     // landed; empty_w(stage): a W chunk was read; slot_free(slot): every UMMA
     // of the slot's tile is done (its base tile is free and its full_tile
-    // phase has been consumed, so the slot may be armed again)
+    // phase has been consumed, so the slot may be armed again); a_ready: the
+    // A operand of the next position is in TMEM.
     auto empty_w = [&](int s) { return bar(s); };
     auto full_tile = [&](int s) { return bar(kWStages + s); };
     auto slot_free = [&](int s) { return bar(kWStages + kUStages + s); };
     auto tfull = [&](int a) { return bar(kWStages + 2 * kUStages + a); };
     auto tempty = [&](int a) { return bar(kWStages + 2 * kUStages + kAccBufs + a); };
+    const uint32_t a_ready = bar(kWStages + 2 * kUStages + 2 * kAccBufs);
 
     int *misc = reinterpret_cast<int *>(smem + kOffMisc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     volatile int *abort = misc + 1;
-    int *row_prev = misc + 4;
+    int *row_prev = misc + 4;  // final draw: the row's previous token
     float *row_c2 = reinterpret_cast<float *>(misc + 4 + BM);
     uint32_t *row_rid = reinterpret_cast<uint32_t *>(misc + 4 + 2 * BM);
-    int *row_code = misc + 4 + 3 * BM;
+    int *row_code = misc + 4 + 3 * BM;  // final draw: kind << 16 | position; draft: temperature valid
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWStages; ++s) mbar_init(empty_w(s), 1);  // released by the UMMAs
@@ -320,6 +376,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             mbar_init(tfull(a), 1);
             mbar_init(tempty(a), kEpiWarps);
         }
+        mbar_init(a_ready, kEpiWarps);
         *abort = 0;
         fence_mbar_init();
     }
@@ -334,7 +391,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     }
     if (threadIdx.x < BM) {
         const int b = m0 + threadIdx.x;
-        int prev = -1, code = -1;
+        int prev = -1, code = 0;
         float c2 = 0.f;
         uint32_t id = 0;
         if (b < p.B) {
@@ -342,11 +399,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             id = p.request_id ? p.request_id[b] : (uint32_t)b;
             const bool t_ok = T >= 0.f && !isinf(T);
             if (!kFinal) {
-                prev = (p.j == 0) ? p.anchor[b] : p.tokens[(size_t)b * p.G + p.j - 1];
-                const bool bad = prev < 0 || prev >= p.V;
-                if (bad && (p.j == 0 || prev != -1) && seg == 0) atomicOr(p.flags, kFlagBadToken);
-                if (!t_ok && p.j == 0 && seg == 0) atomicOr(p.flags, kFlagBadTemperature);
-                if (bad || !t_ok) prev = -1;
+                if (p.j == 0 && seg == 0) {
+                    const int x0 = p.anchor[b];
+                    if (x0 < 0 || x0 >= p.V) atomicOr(p.flags, kFlagBadToken);
+                    if (!t_ok) atomicOr(p.flags, kFlagBadTemperature);
+                }
+                code = t_ok ? 1 : 0;
                 c2 = (T > 0.f) ? kLog2e / T : 0.f;
             } else {
                 code = p.final_code[b];  // validated by the decide kernel
@@ -356,53 +414,28 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     c2 = kLog2e / T;
                 }
             }
+        } else if (kFinal) {
+            code = -1;
         }
         row_prev[threadIdx.x] = prev;
         row_c2[threadIdx.x] = c2;
         row_rid[threadIdx.x] = id;
         row_code[threadIdx.x] = code;
     }
+    if (!kFinal && warp < kEpiWarps && threadIdx.x < 16 * 8) {
+        // identity row n (16 rows of 128 bytes): a single 1.0 at k = n;
+        // 16-byte chunk c of row n sits at position c ^ (n & 7)
+        const int n = threadIdx.x >> 3, pos = threadIdx.x & 7, c = pos ^ (n & 7);
+        const uint32_t one = (c == (n >> 3)) ? ((n & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
+        const int wsel = (n & 7) >> 1;
+        st_shared_v4(sbase + kOffI + n * 128 + (pos << 4),
+                     make_uint4(wsel == 0 ? one : 0u, wsel == 1 ? one : 0u, wsel == 2 ? one : 0u,
+                                wsel == 3 ? one : 0u));
+        fence_proxy_async_smem();
+    }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
-    // A operand in TMEM: lane = request row, K in pairs per 32-bit column.
-    // Warp w writes K elements 64 (w / 4) .. + 63 of the rows of its quadrant.
-    if (warp < kEpiWarps) {
-        const int q = warp & 3, cc = warp >> 2;
-        const int row = q * 32 + lane;
-        const int k0 = cc * 64;
-        if (k0 < p.r) {
-            const int prev = row_prev[row];
-            const int nk = min(64, p.r - k0);  // a multiple of 16
-            uint32_t av[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                if (prev >= 0 && 8 * i < nk) val = __ldg(reinterpret_cast<const uint4 *>(p.e_in + (size_t)prev * p.r + k0) + i);
-                av[4 * i] = val.x;
-                av[4 * i + 1] = val.y;
-                av[4 * i + 2] = val.z;
-                av[4 * i + 3] = val.w;
-            }
-            tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(cc * 32), av);
-            tmem_st_wait();
-        }
-        if (!kFinal && threadIdx.x < 16 * 8) {
-            // identity row n (16 rows of 128 bytes): a single 1.0 at k = n;
-            // 16-byte chunk c of row n sits at position c ^ (n & 7)
-            const int n = threadIdx.x >> 3, pos = threadIdx.x & 7, c = pos ^ (n & 7);
-            const uint32_t one = (c == (n >> 3)) ? ((n & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
-            const int wsel = (n & 7) >> 1;
-            st_shared_v4(sbase + kOffI + n * 128 + (pos << 4),
-                         make_uint4(wsel == 0 ? one : 0u, wsel == 1 ? one : 0u, wsel == 2 ? one : 0u,
-                                    wsel == 3 ? one : 0u));
-        }
-        fence_proxy_async_smem();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const int n_katoms = (p.r + 63) >> 6;
 
     if (warp == kProducerWarp) {
@@ -410,14 +443,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             const uint64_t pol_w = policy_evict_last();
             const uint64_t pol_u = policy_evict_first();
             bool ok = true;
-            for (int t = 0; t < ntiles && ok; ++t) {
-                const int v0 = tile_col(t);
-                const int slot = t % kUStages;
+            for (int tg = 0; tg < total && ok; ++tg) {
+                const int v0 = tile_col(tg);
+                const int jj = p.j + tg / ntiles;
+                const int slot = tg % kUStages;
                 // the second 64-token box lies past the vocabulary only at its end
                 const bool two = v0 + 64 < p.V;
                 const uint32_t u_bytes = kFinal ? 0u : (two ? kUBytes : kUHalf);
                 for (int kb = 0; kb < n_katoms; ++kb) {
-                    const int c = t * n_katoms + kb;
+                    const int c = tg * n_katoms + kb;
                     const int ws = c % kWStages;
                     const uint32_t wph = (uint32_t)(c / kWStages) & 1u;
                     if (c >= kWStages && !mbar_wait(empty_w(ws), wph ^ 1u, abort, kSpinLimit)) {
@@ -425,8 +459,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         break;
                     }
                     if (kb == 0) {
-                        if (t >= kUStages &&
-                            !mbar_wait(slot_free(slot), ((uint32_t)(t / kUStages) & 1u) ^ 1u, abort, kSpinLimit)) {
+                        if (tg >= kUStages &&
+                            !mbar_wait(slot_free(slot), ((uint32_t)(tg / kUStages) & 1u) ^ 1u, abort, kSpinLimit)) {
                             ok = false;
                             break;
                         }
@@ -435,9 +469,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     tma_load_2d(sbase + kOffW + ws * kWChunk, &map_w, full_tile(slot), kb * 64, v0, pol_w);
                 }
                 if (ok && !kFinal) {
-                    tma_load_3d(sbase + kOffU + slot * kUBytes, &map_u, full_tile(slot), v0, p.j, m0, pol_u);
+                    tma_load_3d(sbase + kOffU + slot * kUBytes, &map_u, full_tile(slot), v0, jj, m0, pol_u);
                     if (two)
-                        tma_load_3d(sbase + kOffU + slot * kUBytes + kUHalf, &map_u, full_tile(slot), v0 + 64, p.j, m0,
+                        tma_load_3d(sbase + kOffU + slot * kUBytes + kUHalf, &map_u, full_tile(slot), v0 + 64, jj, m0,
                                     pol_u);
                 }
             }
@@ -463,19 +497,30 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             const uint32_t u_lo0 = (uint32_t)sw128_kmajor_desc(sbase + kOffU);
             const uint32_t i_lo = (uint32_t)sw128_kmajor_desc(sbase + kOffI);
             bool ok = true;
-            for (int t = par; t < ntiles; t += 2) {
-                const int a = t % kAccBufs;
-                const int slot = t % kUStages;  // = par
-                if ((t >= kAccBufs &&
-                     !mbar_wait(tempty(a), ((uint32_t)(t / kAccBufs) & 1u) ^ 1u, abort, kSpinLimit)) ||
-                    !mbar_wait(full_tile(slot), (uint32_t)(t / kUStages) & 1u, abort, kSpinLimit)) {
+            int last_pi = -1;
+            for (int tg = par; tg < total; tg += 2) {
+                const int pi = tg / ntiles;
+                const int a = tg % kAccBufs;
+                const int slot = tg % kUStages;  // = par
+                // the A operand of this position is in TMEM.  Every phase of
+                // a_ready is waited for in order, also those of positions with no
+                // tile of this warp (one tile per segment): a parity wait more
+                // than one phase ahead would see an older phase as complete.
+                while (last_pi < pi && ok) {
+                    ++last_pi;
+                    ok = mbar_wait(a_ready, (uint32_t)last_pi & 1u, abort, kSpinLimit);
+                }
+                if (!ok) break;
+                if ((tg >= kAccBufs &&
+                     !mbar_wait(tempty(a), ((uint32_t)(tg / kAccBufs) & 1u) ^ 1u, abort, kSpinLimit)) ||
+                    !mbar_wait(full_tile(slot), (uint32_t)(tg / kUStages) & 1u, abort, kSpinLimit)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + a * BN;
                 for (int kb = 0; kb < n_katoms; ++kb) {
-                    const int ws = (t * n_katoms + kb) % kWStages;
+                    const int ws = (tg * n_katoms + kb) % kWStages;
                     const uint32_t w_lo = w_lo0 + ws * (kWChunk >> 4);
                     // K-step s = 4 kb + k4: A columns 8 s .. 8 s + 7 of the TMEM copy
                     const uint32_t a_tm = tmem_base + kTmemA + (uint32_t)(32 * kb);
@@ -507,203 +552,265 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const int q = warp & 3, slice = warp >> 2;
         const int row = q * 32 + lane;
         const int b = m0 + row;
-        const int prev = row_prev[row];
         const float c2 = row_c2[row];
         const uint32_t rid = row_rid[row];
         const int code = row_code[row];
         const int kind = kFinal ? (code >= 0 ? (code >> 16) : 0) : 0;
         const int fpos = kFinal ? (code & 0xFFFF) : 0;
-        const bool active = kFinal ? (kind != 0) : (prev >= 0);
-        const uint32_t pos = kFinal ? (uint32_t)fpos : (uint32_t)p.j;
         const uint32_t stream = kFinal ? (kind == 1 ? kStreamResidual : kStreamBonus) : kStreamDraft;
-        // round-1 constants of Philox for this request and position
-        const uint32_t y0c = __umulhi(kPhiloxM1, rid) ^ pos ^ p.keys.k0[0];
         const uint32_t y1c = kPhiloxM1 * rid;
         const uint32_t sk = stream ^ p.keys.k1[0];
-
-        RowState st = row_state_init();
-        float Q = kQMax;
-        float kbest = -INFINITY;  // best key of the row known to this thread
-        uint32_t *row_best = (kFinal || b >= p.B) ? nullptr : p.row_best + (size_t)p.j * p.B + b;
-        uint32_t kg_next = 0u;  // "none"
-        float Qr = kQMax;  // 2^-K for the residual candidate test (with margin)
-        ResidualState rs = residual_init();
-        float lse_q2 = 0.f, lse_t2 = 0.f;
-        const __nv_bfloat16 *urow = nullptr, *trow = nullptr;
-        if (kFinal && active) {
-            trow = p.target + ((size_t)b * (p.G + 1) + fpos) * p.V;
-            if (kind == 1) {
-                urow = p.base + ((size_t)b * p.G + fpos) * p.V;
-                lse_q2 = p.draft_lse[(size_t)b * p.G + fpos] * kLog2e;
-                lse_t2 = p.lse_t_row[b];
-            } else {
-                lse_q2 = INFINITY;  // q = 0
-                lse_t2 = 0.f;       // unnormalised p: the same argmax
-            }
-        }
-        // this thread's 16-token sub-slice h of tile t
-        auto sub_col = [&](int t, int h) { return tile_col(t) + slice * 32 + h * 16; };
-        // final draw: this thread's base / target values, one sub-slice ahead
-        uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
-        if (kFinal && active && ntiles > 0) {
-            const int v = sub_col(0, 0);
-            const int n = min(16, ve - v);
-            if (n > 0) {
-                load16_bf16(trow + v, n, nt_lo, nt_hi);
-                if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
-            }
-        }
         bool ok = true;
-        for (int t = 0; t < ntiles && ok; ++t) {
-            const int a = t % kAccBufs;
-            const uint32_t aph = (uint32_t)(t / kAccBufs) & 1u;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                // the Philox words need nothing from the tensor cores: draw them
-                // first, while the tile's UMMAs may still be running
-                uint4 w[4];
-                {
-                    const int vw = sub_col(t, h);
-                    if (vw < ve) {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            w[g] = philox_folded(((uint32_t)vw >> 2) + g, y0c, y1c, sk, p.keys);
-                    }
-                }
-                if (h == 0) {
-                    if (!uniform_wait(tfull(a), aph, abort)) {
-                        if (lane == 0) {
-                            *abort = 1;
-                            atomicOr(p.flags, kFlagTimeout);
-                        }
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                uint32_t acc[16];
-                tmem_ld16_sync(tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 32 + h * 16, acc);
-                if (h == 1) {  // both halves are in registers: hand the accumulator back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty(a));
-                }
-                const int v = sub_col(t, h);
-                const int n = min(16, ve - v);
-                if (!kFinal) {
-                    if (n <= 0) continue;  // warp-uniform: n depends on the tile and slice only
-                    float z[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) z[i] = __uint_as_float(acc[i]);
-                    if (p.z_out && active) {
-                        float *zo = p.z_out + ((size_t)b * p.G + p.j) * p.V + v;
-                        if (n == 16) {
-#pragma unroll
-                            for (int i = 0; i < 16; i += 4)
-                                *reinterpret_cast<float4 *>(zo + i) = make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (i < n) zo[i] = z[i];  // static index: z stays in registers
-                        }
-                    }
-                    if (active && c2 == 0.f) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (i < n) argmax_push(st, z[i], v + i);
-                    }
-                    const bool on = active && c2 > 0.f;
-                    if (on) {
-                        // the row-wide best key loaded one tile earlier; reload for the next
-                        const float kg = ordered_to_key(kg_next);
-                        kg_next = load_relaxed(row_best);
-                        if (kg > kbest) {
-                            kbest = kg;
-                            Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
-                        }
-                    }
-                    draft_sample16(st, Q, kbest, z, c2, n, v, on, row_best, w);
+        for (int pi = 0; pi < npos && ok; ++pi) {
+            const int jj = kFinal ? 0 : p.j + pi;
+            // ---- A operand of this position: TMEM lane = request row, K in
+            // pairs per 32-bit column; warp w writes K elements 64 (w / 4) .. + 63
+            // of the rows of its quadrant.  Every UMMA of the previous position
+            // is done: this warp has seen the tfull of its last tile.
+            int prev = -1;
+            if (kFinal) {
+                prev = row_prev[row];
+            } else if (b < p.B && code) {
+                if (jj == 0) {
+                    prev = p.anchor[b];
+                    if (prev < 0 || prev >= p.V) prev = -1;
                 } else {
-                    // take this sub-slice's prefetched values, then prefetch the next
-                    // one's (before any skip: the skipped sub-slice may come first
-                    // when walking the segment backwards)
-                    float u[16], tt[16];
-                    unpack16(nu_lo, nu_hi, u);
-                    unpack16(nt_lo, nt_hi, tt);
-                    {
-                        const int tn = t + h, hn = h ^ 1;  // the next sub-slice
-                        const int vn = (tn < ntiles) ? sub_col(tn, hn) : ve;
-                        const int nn = min(16, ve - vn);
-                        if (active && tn < ntiles && nn > 0) {
-                            load16_bf16(trow + vn, nn, nt_lo, nt_hi);
-                            if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
+                    prev = best_token(load_relaxed_u64(p.best + (size_t)(jj - 1) * p.B + b));
+                }
+            }
+            {
+                const int k0 = slice * 64;
+                if (k0 < p.r) {
+                    const int nk = min(64, p.r - k0);  // a multiple of 16
+                    uint32_t av[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                        if (prev >= 0 && 8 * i < nk)
+                            val = __ldg(reinterpret_cast<const uint4 *>(p.e_in + (size_t)prev * p.r + k0) + i);
+                        av[4 * i] = val.x;
+                        av[4 * i + 1] = val.y;
+                        av[4 * i + 2] = val.z;
+                        av[4 * i + 3] = val.w;
+                    }
+                    tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(slice * 32), av);
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(a_ready);
+            }
+            const bool active = kFinal ? (kind != 0) : (prev >= 0);
+            const uint32_t pos = kFinal ? (uint32_t)fpos : (uint32_t)jj;
+            // round-1 constant of Philox for this request and position
+            const uint32_t y0c = __umulhi(kPhiloxM1, rid) ^ pos ^ p.keys.k0[0];
+
+            RowState st = row_state_init();
+            float Q = kQMax;
+            float kbest = -INFINITY;  // best key of the row known to this thread
+            unsigned long long *best = (kFinal || b >= p.B) ? nullptr : p.best + (size_t)jj * p.B + b;
+            uint32_t kg_next = 0u;  // "none"
+            float Qr = kQMax;       // 2^-K for the residual candidate test (with margin)
+            ResidualState rs = residual_init();
+            float lse_q2 = 0.f, lse_t2 = 0.f;
+            const __nv_bfloat16 *urow = nullptr, *trow = nullptr;
+            if (kFinal && active) {
+                trow = p.target + ((size_t)b * (p.G + 1) + fpos) * p.V;
+                if (kind == 1) {
+                    urow = p.base + ((size_t)b * p.G + fpos) * p.V;
+                    lse_q2 = p.draft_lse[(size_t)b * p.G + fpos] * kLog2e;
+                    lse_t2 = p.lse_t_row[b];
+                } else {
+                    lse_q2 = INFINITY;  // q = 0
+                    lse_t2 = 0.f;       // unnormalised p: the same argmax
+                }
+            }
+            // this thread's 16-token sub-slice h of tile t of this position
+            auto sub_col = [&](int t, int h) { return tile_col(pi * ntiles + t) + slice * 32 + h * 16; };
+            // final draw: this thread's base / target values, one sub-slice ahead
+            uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
+            if (kFinal && active && ntiles > 0) {
+                const int v = sub_col(0, 0);
+                const int n = min(16, ve - v);
+                if (n > 0) {
+                    load16_bf16(trow + v, n, nt_lo, nt_hi);
+                    if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
+                }
+            }
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int tg = pi * ntiles + t;
+                const int a = tg % kAccBufs;
+                const uint32_t aph = (uint32_t)(tg / kAccBufs) & 1u;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // The Philox words need nothing from the tensor cores.  The first
+                    // sub-slice draws them while the tile's UMMAs may still run; the
+                    // second issues its TMEM load first and draws them under its latency.
+                    uint4 w[4];
+                    uint32_t acc[16];
+                    const int vw = sub_col(t, h);
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 32 + h * 16;
+                    if (h == 0) {
+                        if (vw < ve) {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g)
+                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, y0c, y1c, sk, p.keys);
+                        }
+                        if (!uniform_wait(tfull(a), aph, abort)) {
+                            if (lane == 0) {
+                                *abort = 1;
+                                atomicOr(p.flags, kFlagTimeout);
+                            }
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        tmem_ld16(taddr, acc);
+                    } else {
+                        tmem_ld16(taddr, acc);
+                        if (vw < ve) {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g)
+                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, y0c, y1c, sk, p.keys);
                         }
                     }
-                    if (n <= 0) continue;  // warp-uniform
-                    // Token v's key is log2(r_v) - log2(E_v) with r_v = p_v - q_v; a
-                    // bonus row is a residual row with q = 0 and unnormalised p
-                    // (lse_q2 = +inf, lse_t2 = 0).  It can beat the best key K only
-                    // if (1 - u_v) < r_v 2^-K.
-                    // upper bound of p - q under the approximate exponentials;
-                    // rb <= 0 gives a threshold <= 1 <= f1: no candidate
-                    auto rbound = [&](int i) -> float {
-                        const float z = u[i] + __uint_as_float(acc[i]);
-                        const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
-                        const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
-                        return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
-                    };
-                    bool gc[4];
-                    bool any = false;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const float rmax = fmaxf(fmaxf(rbound(4 * g), rbound(4 * g + 1)),
-                                                 fmaxf(rbound(4 * g + 2), rbound(4 * g + 3)));
-                        const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
-                        gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f);
-                        any |= gc[g];
+                    tmem_ld_wait16(acc);
+                    if (h == 1) {  // both halves are in registers: hand the accumulator back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty(a));
                     }
-                    if (__any_sync(0xffffffffu, any)) {
+                    const int v = vw;
+                    const int n = min(16, ve - v);
+                    if (!kFinal) {
+                        if (n <= 0) continue;  // warp-uniform: n depends on the tile and slice only
+                        float z[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (!(__any_sync(0xffffffffu, gc[i >> 2]) && gc[i >> 2])) continue;
-                            if (!(one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rbound(i), Qr, 1.f)))
-                                continue;
-                            // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
-                            // log2 q formed from the logit difference first (+inf for bonus rows)
-                            const float z = u[i] + __uint_as_float(acc[i]);
-                            const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
-                            if (!(delta2 > 0.f)) continue;
-                            const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
-                            const float key = fmaf(tt[i], c2, -lse_t2) + l1 -
-                                              fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
-                            if (key > rs.key_res) {
-                                rs.key_res = key;
-                                rs.idx_res = v + i;
+                        for (int i = 0; i < 16; ++i) z[i] = __uint_as_float(acc[i]);
+                        if (p.z_out && active) {
+                            float *zo = p.z_out + ((size_t)b * p.G + jj) * p.V + v;
+                            if (n == 16) {
+#pragma unroll
+                                for (int i = 0; i < 16; i += 4)
+                                    *reinterpret_cast<float4 *>(zo + i) = make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (i < n) zo[i] = z[i];  // static index: z stays in registers
                             }
                         }
-                        Qr = fminf(fast_exp2(-rs.key_res), kQMax) * kMargin;
+                        if (active && c2 == 0.f) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (i < n) argmax_push(st, z[i], v + i);
+                        }
+                        const bool on = active && c2 > 0.f;
+                        if (on) {
+                            // the row-wide best key loaded one sub-slice earlier (the high
+                            // word of the row's best); reload it for the next
+                            const float kg = ordered_to_key(kg_next);
+                            kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
+                            if (kg > kbest) {
+                                kbest = kg;
+                                Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
+                            }
+                        }
+                        draft_sample16(st, Q, kbest, z, c2, n, v, on, best, w);
+                    } else {
+                        // take this sub-slice's prefetched values, then prefetch the next
+                        // one's (before any skip: the skipped sub-slice may come first
+                        // when walking the segment backwards)
+                        float u[16], tt[16];
+                        unpack16(nu_lo, nu_hi, u);
+                        unpack16(nt_lo, nt_hi, tt);
+                        {
+                            const int tn = t + h, hn = h ^ 1;  // the next sub-slice
+                            const int vn = (tn < ntiles) ? sub_col(tn, hn) : ve;
+                            const int nn = min(16, ve - vn);
+                            if (active && tn < ntiles && nn > 0) {
+                                load16_bf16(trow + vn, nn, nt_lo, nt_hi);
+                                if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
+                            }
+                        }
+                        if (n <= 0) continue;  // warp-uniform
+                        // Token v's key is log2(r_v) - log2(E_v) with r_v = p_v - q_v; a
+                        // bonus row is a residual row with q = 0 and unnormalised p
+                        // (lse_q2 = +inf, lse_t2 = 0).  It can beat the best key K only
+                        // if (1 - u_v) < r_v 2^-K.
+                        // upper bound of p - q under the approximate exponentials;
+                        // rb <= 0 gives a threshold <= 1 <= f1: no candidate
+                        auto rbound = [&](int i) -> float {
+                            const float z = u[i] + __uint_as_float(acc[i]);
+                            const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
+                            const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
+                            return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
+                        };
+                        bool gc[4];
+                        bool any = false;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const float rmax = fmaxf(fmaxf(rbound(4 * g), rbound(4 * g + 1)),
+                                                     fmaxf(rbound(4 * g + 2), rbound(4 * g + 3)));
+                            const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
+                            gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f);
+                            any |= gc[g];
+                        }
+                        if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (!(__any_sync(0xffffffffu, gc[i >> 2]) && gc[i >> 2])) continue;
+                                if (!(one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rbound(i), Qr, 1.f)))
+                                    continue;
+                                // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
+                                // log2 q formed from the logit difference first (+inf for bonus rows)
+                                const float z = u[i] + __uint_as_float(acc[i]);
+                                const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
+                                if (!(delta2 > 0.f)) continue;
+                                const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
+                                const float key = fmaf(tt[i], c2, -lse_t2) + l1 -
+                                                  fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
+                                if (key > rs.key_res) {
+                                    rs.key_res = key;
+                                    rs.idx_res = v + i;
+                                }
+                            }
+                            Qr = fminf(fast_exp2(-rs.key_res), kQMax) * kMargin;
+                        }
                     }
                 }
             }
-        }
-        // merge the four column slices of each row
-        if (!kFinal) {
-            RowState *ms = reinterpret_cast<RowState *>(smem + kOffMerge);
-            ms[row * 4 + slice] = st;
-        } else {
-            ResidualState *ms = reinterpret_cast<ResidualState *>(smem + kOffMerge);
-            ms[row * 4 + slice] = rs;
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-        if (slice == 0 && b < p.B) {
+            // merge the four column slices of each row
             if (!kFinal) {
-                const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
-                for (int s = 1; s < 4; ++s) row_state_merge(st, ms[row * 4 + s]);
-                p.part[(size_t)b * p.nseg + seg] = st;
-            } else if (active) {
-                const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);
-                for (int s = 1; s < 4; ++s) residual_merge(rs, ms[row * 4 + s]);
-                p.rpart[(size_t)b * p.nseg + seg] = rs;
+                RowState *ms = reinterpret_cast<RowState *>(smem + kOffMerge);
+                ms[row * 4 + slice] = st;
+            } else {
+                ResidualState *ms = reinterpret_cast<ResidualState *>(smem + kOffMerge);
+                ms[row * 4 + slice] = rs;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+            if (slice == 0 && b < p.B) {
+                if (!kFinal) {
+                    const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
+                    for (int s2 = 1; s2 < 4; ++s2) row_state_merge(st, ms[row * 4 + s2]);
+                    p.part[((size_t)jj * p.B + b) * p.nseg + seg] = st;
+                    if (st.idx != INT32_MAX) atomicMax(best, best_encode(st.key, st.idx));
+                } else if (active) {
+                    const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);
+                    for (int s2 = 1; s2 < 4; ++s2) residual_merge(rs, ms[row * 4 + s2]);
+                    p.rpart[(size_t)b * p.nseg + seg] = rs;
+                }
+            }
+            if (!kFinal && pi + 1 < npos) {
+                // every CTA has published this position's rows: x_j is final
+                asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                if (threadIdx.x == 0 &&
+                    !grid_sync(p.grid_bar, (unsigned int)(pi + 1) * gridDim.x * gridDim.y, abort, kSpinLimit)) {
+                    *abort = 1;
+                    atomicOr(p.flags, kFlagTimeout);
+                }
+                asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                __threadfence();
+                if (*abort) ok = false;
             }
         }
     }
@@ -793,7 +900,36 @@ int tc_segments(int B, int V) {
 
 size_t tc_residual_state_bytes() { return sizeof(ResidualState); }
 
-cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, cudaStream_t s) {
+namespace {
+
+// CTAs of the draft kernel that can be resident at once on the current device
+// (0 if cooperative launches are unavailable).
+int coop_capacity() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static std::mutex mu;
+    static int cached[64];
+    static bool have[64];
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return 0;
+    if (!have[dev]) {
+        int coop = 0, sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, markov_tc_kernel<false>, kThreads,
+                                                                 kSmemBytes) == cudaSuccess)
+            cached[dev] = per_sm * sms;
+        else
+            cached[dev] = 0;
+        cudaGetLastError();
+        have[dev] = true;
+    }
+    return cached[dev];
+}
+
+}  // namespace
+
+cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStream_t s) {
     CUtensorMap mw, mu;
     cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
     if (e != cudaSuccess) return e;
@@ -810,16 +946,31 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, int j, 
     p.G = a.G;
     p.V = a.V;
     p.r = a.r;
-    p.j = j;
-    p.pass = j;
     p.nseg = pl.nsplit;
     p.keys = round_keys(a.seed);
     p.part = reinterpret_cast<RowState *>(a.ws + pl.partial_offset);
-    p.row_best = reinterpret_cast<uint32_t *>(a.ws + pl.row_best_offset);
+    p.best = reinterpret_cast<unsigned long long *>(a.ws + pl.best_offset);
+    p.grid_bar = reinterpret_cast<unsigned int *>(a.ws + kGridBarOffset);
     p.flags = reinterpret_cast<uint32_t *>(a.ws);
     p.z_out = a.z_out;
-    markov_tc_kernel<false><<<dim3(pl.nsplit, pl.row_blocks), kThreads, kSmemBytes, s>>>(mw, mu, p);
-    return cudaGetLastError();
+    const dim3 grid(pl.nsplit, pl.row_blocks);
+    // all positions in one cooperative launch when every CTA fits at once
+    if (a.G > 1 && (long)grid.x * grid.y <= (long)coop_capacity()) {
+        p.j = 0;
+        p.j_end = a.G;
+        void *args[] = {(void *)&mw, (void *)&mu, (void *)&p};
+        e = cudaLaunchCooperativeKernel((const void *)markov_tc_kernel<false>, grid, dim3(kThreads), args, kSmemBytes,
+                                        s);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        cudaGetLastError();  // not resident after all: one launch per position
+    }
+    for (int j = 0; j < a.G; ++j) {
+        p.j = j;
+        p.j_end = j + 1;
+        markov_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(mw, mu, p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
