@@ -71,7 +71,8 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
                    const float *__restrict__ temperature, int B, int G, int V, int chunk, int nsplit,
                    RowState *__restrict__ part) {
     __shared__ RowState scratch[kRowThreads / 32];
-    const int row = blockIdx.y;
+    // rows along x (their count B (G + 1) can pass the 65535 limit of y)
+    const int row = blockIdx.x;
     const int b = row / (G + 1);
     const int j = row - b * (G + 1);
     const int L = read_verify_len(verify_len, b, G);
@@ -80,7 +81,7 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
     // the final pass); greedy requests read rows j <= L
     if (L < 0 || !temperature_ok(T) || j > L || (T > 0.f && j == L)) return;
     const float c2 = T > 0.f ? kLog2e / T : 0.f;
-    const int seg = blockIdx.x;
+    const int seg = blockIdx.y;
     const int vb = seg * chunk;
     const int ve = min(V, vb + chunk);
     const TIn *t_row = target + ((size_t)b * (G + 1) + j) * V;
@@ -248,11 +249,11 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__
                          ResidualState *__restrict__ part) {
     extern __shared__ float a_row[];  // [r]
     __shared__ ResidualState scratch[kResThreads / 32];
-    const int b = blockIdx.y;
+    const int b = blockIdx.x;  // requests along x, segments along y
     const int code = final_code[b];
     if (code < 0) return;
     const int kind = code >> 16, d = code & 0xFFFF;
-    const int seg = blockIdx.x;
+    const int seg = blockIdx.y;
     const float c2 = kLog2e / temperature[b];
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     const bool residual = (kind == 1);
@@ -399,7 +400,7 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
     const TIn *target = static_cast<const TIn *>(a.target);
 
-    verify_rows_kernel<TIn><<<dim3(p.row_split, a.B * (a.G + 1)), kRowThreads, 0, s>>>(
+    verify_rows_kernel<TIn><<<dim3(a.B * (a.G + 1), p.row_split), kRowThreads, 0, s>>>(
         target, a.verify_len, a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split, row_part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -419,7 +420,7 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
         e = launch_final_tensor(fa, s);
     } else {
         const size_t smem = sizeof(float) * (size_t)a.r;
-        verify_final_simt_kernel<TIn><<<dim3(p.res_split, a.B), kResThreads, smem, s>>>(
+        verify_final_simt_kernel<TIn><<<dim3(a.B, p.res_split), kResThreads, smem, s>>>(
             target, static_cast<const TIn *>(a.base), static_cast<const TIn *>(a.e_in),
             static_cast<const TIn *>(a.w_out), a.z_in, a.anchor, a.draft_tokens, a.draft_lse,
             a.temperature, a.request_id, final_code, lse_t_row, a.B, a.G, a.V, a.r, k0, k1, p.res_chunk,

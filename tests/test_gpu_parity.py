@@ -88,6 +88,29 @@ def test_full_size_sampled_requests(name):
     torch.cuda.empty_cache()
 
 
+def test_draft_one_launch_per_position():
+    """More 128-request row blocks than SMs: the grid cannot be resident at
+    once, so the draft runs one launch per block position (each reading the
+    previous position's draws from the workspace) and must still match."""
+    w = WORKLOADS["qwen3"].scaled(B=157 * 128, G=3, V=1024, r=16)
+    reqs = np.array([0, 1, 5000, 12345, 20000, w.B - 1])
+    tally, g, o, inp = full_parity(w, 9, reqs=reqs)
+    tally.check()
+    del inp
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_short_blocks(G):
+    """A block of one position (a single launch) and of two."""
+    w = SCALED["qwen3"].scaled(G=G)
+    total = Tally()
+    for seed in range(3):
+        tally, *_ = full_parity(w, 40 + seed)
+        total.add(tally)
+    total.check()
+
+
 def test_verify_alone_on_oracle_drafts():
     """Feed the oracle's draft to the CUDA verify, compare with the oracle verify."""
     for name in ("tiny", "dspark5", "largev"):
