@@ -277,32 +277,35 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
 #pragma unroll
         for (int i = 0; i < 16; ++i) e[i] = 0.f;  // threshold 1 <= f1: no candidate
     }
-    bool gc[4];
-    bool any = false;
+    uint32_t gmask = 0;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         const float emax = fmaxf(fmaxf(e[4 * g], e[4 * g + 1]), fmaxf(e[4 * g + 2], e[4 * g + 3]));
         const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
-        gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(emax, Q, 1.f);
-        any |= gc[g];
+        if (one_minus_uniform_plus_one(wmax) < fmaf(emax, Q, 1.f)) gmask |= 1u << g;
     }
-    if (__any_sync(0xffffffffu, any)) {
-#pragma unroll
+    if (__any_sync(0xffffffffu, gmask != 0)) {
+        // rare: one pass per group, its values picked by value (no local memory)
+#pragma unroll 1
         for (int g = 0; g < 4; ++g) {
-            if (!(__any_sync(0xffffffffu, gc[g]) && gc[g])) continue;
+            const bool mine = (gmask >> g) & 1u;
+            if (!(__any_sync(0xffffffffu, mine) && mine)) continue;
+            const uint4 wg = g == 0 ? w[0] : (g == 1 ? w[1] : (g == 2 ? w[2] : w[3]));
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int i = 4 * g + c;
-                const uint32_t word = word_of(w[g], c);
-                if (!(one_minus_uniform_plus_one(word) < fmaf(e[i], Q, 1.f))) continue;
-                const float s2 = z[i] * c2;
+                const float ei = g == 0 ? e[c] : (g == 1 ? e[4 + c] : (g == 2 ? e[8 + c] : e[12 + c]));
+                const float zi = g == 0 ? z[c] : (g == 1 ? z[4 + c] : (g == 2 ? z[8 + c] : z[12 + c]));
+                const uint32_t word = word_of(wg, c);
+                if (!(one_minus_uniform_plus_one(word) < fmaf(ei, Q, 1.f))) continue;
+                const float s2 = zi * c2;
                 const float key = s2 - fast_log2(neg_log_uniform(word));
                 if (key > kbest) {
+                    const int idx = v + 4 * g + c;
                     st.key = key;
                     st.s_at = s2;
-                    st.idx = v + i;
+                    st.idx = idx;
                     kbest = key;
-                    atomicMax(best, best_encode(key, v + i));
+                    atomicMax(best, best_encode(key, idx));
                 }
             }
         }
@@ -641,7 +644,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 const int tg = pi * ntiles + t;
                 const int a = tg % kAccBufs;
                 const uint32_t aph = (uint32_t)(tg / kAccBufs) & 1u;
-#pragma unroll
+                // one copy of the sub-slice body (a second would overflow the
+                // instruction cache)
+#pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     // The Philox words need nothing from the tensor cores.  The first
                     // sub-slice draws them while the tile's UMMAs may still run; the
@@ -745,33 +750,43 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
                             return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
                         };
-                        bool gc[4];
-                        bool any = false;
+                        uint32_t gmask = 0;
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
                             const float rmax = fmaxf(fmaxf(rbound(4 * g), rbound(4 * g + 1)),
                                                      fmaxf(rbound(4 * g + 2), rbound(4 * g + 3)));
                             const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
-                            gc[g] = one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f);
-                            any |= gc[g];
+                            if (one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f)) gmask |= 1u << g;
                         }
-                        if (__any_sync(0xffffffffu, any)) {
+                        if (__any_sync(0xffffffffu, gmask != 0)) {
+                            // rare: one pass per group, its values picked by value
+#pragma unroll 1
+                            for (int g = 0; g < 4; ++g) {
+                                const bool mine = (gmask >> g) & 1u;
+                                if (!(__any_sync(0xffffffffu, mine) && mine)) continue;
+                                const uint4 wg = g == 0 ? w[0] : (g == 1 ? w[1] : (g == 2 ? w[2] : w[3]));
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                if (!(__any_sync(0xffffffffu, gc[i >> 2]) && gc[i >> 2])) continue;
-                                if (!(one_minus_uniform_plus_one(word_of(w[i >> 2], i & 3)) < fmaf(rbound(i), Qr, 1.f)))
-                                    continue;
-                                // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
-                                // log2 q formed from the logit difference first (+inf for bonus rows)
-                                const float z = u[i] + __uint_as_float(acc[i]);
-                                const float delta2 = fmaf(tt[i] - z, c2, lse_q2 - lse_t2);
-                                if (!(delta2 > 0.f)) continue;
-                                const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
-                                const float key = fmaf(tt[i], c2, -lse_t2) + l1 -
-                                                  fast_log2(neg_log_uniform(word_of(w[i >> 2], i & 3)));
-                                if (key > rs.key_res) {
-                                    rs.key_res = key;
-                                    rs.idx_res = v + i;
+                                for (int c = 0; c < 4; ++c) {
+                                    const int i0 = c, i1 = 4 + c, i2 = 8 + c, i3 = 12 + c;
+                                    const float ui = g == 0 ? u[i0] : (g == 1 ? u[i1] : (g == 2 ? u[i2] : u[i3]));
+                                    const float ti = g == 0 ? tt[i0] : (g == 1 ? tt[i1] : (g == 2 ? tt[i2] : tt[i3]));
+                                    const uint32_t ai = g == 0 ? acc[i0] : (g == 1 ? acc[i1] : (g == 2 ? acc[i2] : acc[i3]));
+                                    const float z = ui + __uint_as_float(ai);
+                                    const float pv = fast_exp2(fmaf(ti, c2, -lse_t2));
+                                    const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
+                                    const float rbi = (active && 4 * g + c < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
+                                    const uint32_t word = word_of(wg, c);
+                                    if (!(one_minus_uniform_plus_one(word) < fmaf(rbi, Qr, 1.f))) continue;
+                                    // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
+                                    // log2 q formed from the logit difference first (+inf for bonus rows)
+                                    const float delta2 = fmaf(ti - z, c2, lse_q2 - lse_t2);
+                                    if (!(delta2 > 0.f)) continue;
+                                    const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
+                                    const float key = fmaf(ti, c2, -lse_t2) + l1 - fast_log2(neg_log_uniform(word));
+                                    if (key > rs.key_res) {
+                                        rs.key_res = key;
+                                        rs.idx_res = v + 4 * g + c;
+                                    }
                                 }
                             }
                             Qr = fminf(fast_exp2(-rs.key_res), kQMax) * kMargin;
