@@ -93,6 +93,11 @@ def lib():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _f64p, _f64p, _i32p, _f64p, _i32p, _f64p, _f64p]
             L.or_schedule.restype = ctypes.c_int
+            L.or_schedule_policy.argtypes = [
+                _f64p, _f64p, _f64p, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                _f64p, _f64p, _i32p, _f64p, _i32p, _f64p, _f64p]
+            L.or_schedule_policy.restype = ctypes.c_int
             L.or_verify.argtypes = [
                 _f64p, _f64p, _f64p, _f64p, _i32p, _i32p, ni, _f64p, nu,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
@@ -205,6 +210,30 @@ def schedule(conf_logits, pos_temp, sps, L_min, L_max):
                            out["conf"], out["cum_conf"], out["verify_len"], theta, nadm, mm, mt)
     if rc != 0:
         raise ValueError("or_schedule failed: %d" % rc)
+    out.update(theta=float(theta[0]), n_admitted=int(nadm[0]), min_margin=float(mm[0]),
+               min_tie=float(mt[0]))
+    return out
+
+
+def schedule_policy(conf_logits, pos_temp, sps, L_min, L_max, policy, threshold=0.0):
+    """Verify lengths under one of the policies of ``or_schedule_policy``
+    (0 early stop, 1 best prefix without early stop, 2 threshold on a,
+    3 threshold on c)."""
+    cl = _f64(conf_logits)
+    B, G = cl.shape
+    pt = _f64(pos_temp)
+    sp = _f64(sps)
+    out = dict(conf=np.zeros((B, G)), cum_conf=np.zeros((B, G)),
+               verify_len=np.zeros(B, np.int32))
+    theta = np.zeros(1)
+    nadm = np.zeros(1, np.int32)
+    mm = np.zeros(1)
+    mt = np.zeros(1)
+    rc = lib().or_schedule_policy(cl, pt, sp, len(sp), B, G, int(L_min), int(L_max), int(policy),
+                                  float(threshold), out["conf"], out["cum_conf"], out["verify_len"], theta,
+                                  nadm, mm, mt)
+    if rc != 0:
+        raise ValueError("or_schedule_policy failed: %d" % rc)
     out.update(theta=float(theta[0]), n_admitted=int(nadm[0]), min_margin=float(mm[0]),
                min_tie=float(mt[0]))
     return out

@@ -317,6 +317,123 @@ int or_schedule(const double *conf_logits, const double *pos_temp, const double 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Other verify-length policies the pages describe next to the early-stop    */
+/* scheduler ([DSP-IT] "Che cosa resta da verificare": production schedules  */
+/* from confidences two rounds old and drops the early stop; "Verificare     */
+/* meglio, non di piu'" and [DSP-ZH] "置信度调度的验证": a fixed confidence     */
+/* threshold as the simpler comparator).  Readings:                           */
+/*  policy 0  the early stop above (or_schedule);                             */
+/*  policy 1  no early stop: over the same candidate order, admit the count   */
+/*            n in 0..ncand whose Theta(n) = tau_n * SPS(B_tok + n) is        */
+/*            largest (the first such n);                                    */
+/*  policy 2  threshold on the prefix survival: L_b grows from L_min while    */
+/*            a_{b,L_b} > threshold (a is non-increasing in j);              */
+/*  policy 3  threshold on the per-position confidence: L_b grows from L_min  */
+/*            while c_{b,L_b} > threshold (the leading run).                  */
+/* Theta is reported for the chosen lengths in every policy.  min_margin is   */
+/* the smallest relative gap on which a decision turned: policy 1, the best  */
+/* Theta against the runner-up; policies 2-3, |value - threshold| / threshold. */
+/* The lag itself is the caller's: the confidences passed in are the ones     */
+/* the policy is applied to.                                                  */
+/* ------------------------------------------------------------------------ */
+int or_schedule_policy(const double *conf_logits, const double *pos_temp, const double *sps, int sps_len,
+                       int B, int G, int L_min, int L_max, int policy, double threshold,
+                       double *conf, double *cum_conf, int32_t *verify_len, double *theta,
+                       int32_t *n_admitted, double *min_margin, double *min_tie)
+{
+    if (policy == 0)
+        return or_schedule(conf_logits, pos_temp, sps, sps_len, B, G, L_min, L_max, conf, cum_conf, verify_len,
+                           theta, n_admitted, min_margin, min_tie);
+    if (policy < 1 || policy > 3) return -1;
+    if (B < 0 || G < 1 || L_min < 0 || L_min > L_max || L_max > G) return -1;
+    if (sps_len < B * (L_max + 1) + 1) return -1;
+    for (int b = 0; b < B; ++b) {
+        double prod = 1.0;
+        for (int j = 0; j < G; ++j) {
+            double l = conf_logits[(size_t)b * G + j];
+            double c = 1.0 / (1.0 + exp(-l / pos_temp[j]));
+            prod *= c;
+            conf[(size_t)b * G + j] = c;
+            cum_conf[(size_t)b * G + j] = prod;
+        }
+    }
+    double mm = INFINITY, mt = INFINITY;
+    int admitted = 0;
+    if (policy == 1) {
+        double tau = 0.0;
+        long btok = 0;
+        for (int b = 0; b < B; ++b) {
+            verify_len[b] = L_min;
+            double t = 1.0;
+            for (int j = 0; j < L_min; ++j) t += cum_conf[(size_t)b * G + j];
+            tau += t;
+            btok += L_min + 1;
+        }
+        int nc = B * (L_max - L_min);
+        or_cand *cand = (or_cand *)malloc(sizeof(or_cand) * (size_t)(nc > 0 ? nc : 1));
+        if (!cand) return -2;
+        int n = 0;
+        for (int b = 0; b < B; ++b)
+            for (int j = L_min; j < L_max; ++j) {
+                cand[n].a = cum_conf[(size_t)b * G + j];
+                cand[n].j = j;
+                cand[n].b = b;
+                ++n;
+            }
+        qsort(cand, (size_t)nc, sizeof(or_cand), cand_order);
+        for (int i = 0; i + 1 < nc; ++i) {
+            double d = fabs(cand[i].a - cand[i + 1].a) / fmax(fabs(cand[i].a), 1e-300);
+            if (d < mt) mt = d;
+        }
+        /* Theta after admitting the first n candidates, n = 0..nc */
+        double best = tau * sps[btok], second = -INFINITY, run = tau;
+        int nbest = 0;
+        for (int i = 0; i < nc; ++i) {
+            run += cand[i].a;
+            double th = run * sps[btok + i + 1];
+            if (th > best) {
+                second = best;
+                best = th;
+                nbest = i + 1;
+            } else if (th > second) {
+                second = th;
+            }
+        }
+        for (int i = 0; i < nbest; ++i) verify_len[cand[i].b] = cand[i].j + 1;
+        admitted = nbest;
+        if (second > -INFINITY) mm = fabs(best - second) / fmax(fabs(best), 1e-300);
+        free(cand);
+    } else {
+        for (int b = 0; b < B; ++b) {
+            int L = L_min;
+            for (int j = L_min; j < L_max; ++j) {
+                double x = (policy == 2) ? cum_conf[(size_t)b * G + j] : conf[(size_t)b * G + j];
+                double d = fabs(x - threshold) / fmax(fabs(threshold), 1e-300);
+                if (d < mm) mm = d;
+                if (!(x > threshold)) break;
+                L = j + 1;
+            }
+            verify_len[b] = L;
+            admitted += L - L_min;
+        }
+    }
+    /* Theta of the chosen lengths */
+    double tau = 0.0;
+    long btok = 0;
+    for (int b = 0; b < B; ++b) {
+        double t = 1.0;
+        for (int j = 0; j < verify_len[b]; ++j) t += cum_conf[(size_t)b * G + j];
+        tau += t;
+        btok += verify_len[b] + 1;
+    }
+    if (theta) *theta = tau * sps[btok];
+    if (n_admitted) *n_admitted = admitted;
+    if (min_margin) *min_margin = mm;
+    if (min_tie) *min_tie = mt;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Verification by rejection sampling ([MATH-FR] "La garantie de            */
 /* l'echantillonnage par rejet": accept x with probability min(1, p/q), stop */
 /* at the first rejection and resample from the residual distribution;       */
