@@ -8,7 +8,8 @@
  *   dspark_draft_sample     draft G tokens per request with the
  *                           semi-autoregressive Markov head;
  *   dspark_schedule_prefix  calibrate per-position confidences and choose how
- *                           many draft tokens of each request to verify;
+ *                           many draft tokens of each request to verify
+ *                           (dspark_schedule_policy: other policies);
  *   dspark_verify           lossless rejection-sampling verification against
  *                           the target logits, with residual resampling or a
  *                           bonus token.
@@ -159,6 +160,42 @@ DSPARK_API dspark_status dspark_draft_sample(
 DSPARK_API dspark_status dspark_schedule_prefix(
     const float *conf_logits, const float *pos_temp, const float *sps, int sps_len,
     int B, int G, int L_min, int L_max,
+    float *conf, float *cum_conf, int32_t *verify_len, double *theta_out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Verify lengths under another policy; the early stop above is policy 0.
+ *
+ * Defined by "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
+ * "Che cosa resta da verificare" (the deployed scheduler takes confidences
+ * from two rounds earlier and drops the early stop) and section "Verificare
+ * meglio, non di piu'" (a fixed confidence threshold as the comparator):
+ *
+ *   DSPARK_SCHED_EARLY_STOP (0)  as dspark_schedule_prefix;
+ *   DSPARK_SCHED_BEST_PREFIX (1) the same candidate order, admitting the first
+ *        n whose Theta(n) = tau_n * sps[n_0 + n] is largest over n = 0 .. all
+ *        candidates (no early stop; for a fixed n the top-a set is the best
+ *        one, so this is the optimum over every vector of lengths);
+ *   DSPARK_SCHED_THRESHOLD_CUM (2)  L_b grows from L_min while
+ *        a[b][L_b] > threshold (L_b < L_max);
+ *   DSPARK_SCHED_THRESHOLD_CONF (3) the same on c[b][L_b] (a leading run).
+ *
+ * For the lagged production mode pass the confidence logits of round t - 2
+ * with policy 1 (the library keeps no history).  Arguments, outputs and
+ * limits as dspark_schedule_prefix; theta_out is Theta of the chosen lengths
+ * for every policy.  `threshold` is used by policies 2 and 3 only and must be
+ * finite.  An unknown policy returns DSPARK_ERR_INVALID_ARG.
+ */
+typedef enum {
+    DSPARK_SCHED_EARLY_STOP = 0,
+    DSPARK_SCHED_BEST_PREFIX = 1,
+    DSPARK_SCHED_THRESHOLD_CUM = 2,
+    DSPARK_SCHED_THRESHOLD_CONF = 3
+} dspark_sched_policy;
+
+DSPARK_API dspark_status dspark_schedule_policy(
+    const float *conf_logits, const float *pos_temp, const float *sps, int sps_len,
+    int B, int G, int L_min, int L_max, int policy, float threshold,
     float *conf, float *cum_conf, int32_t *verify_len, double *theta_out,
     void *workspace, size_t workspace_bytes, void *stream);
 

@@ -27,7 +27,7 @@ FLAG_BAD_VERIFY_LEN = 4
 FLAG_BAD_POS_TEMP = 8
 
 EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
-           "dspark_schedule_prefix", "dspark_verify", "dspark_read_device_flags",
+           "dspark_schedule_prefix", "dspark_schedule_policy", "dspark_verify", "dspark_read_device_flags",
            "dspark_verify_noalloc")
 
 _lib = None
@@ -69,6 +69,9 @@ def load(build_if_missing: bool = True):
         L.dspark_schedule_prefix.restype = ctypes.c_int
         L.dspark_schedule_prefix.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                              vp, sz, vp]
+        L.dspark_schedule_policy.restype = ctypes.c_int
+        L.dspark_schedule_policy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, ctypes.c_float,
+                                             vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.dspark_verify.restype = ctypes.c_int
         L.dspark_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                     i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -187,9 +190,14 @@ def draft_sample(base, e_in, w_out, anchor, temperature, request_id=None, seed=0
     return out
 
 
-def schedule_prefix(conf_logits, pos_temp, sps, L_min, L_max, *, out=None, workspace=None,
-                    stream=None):
-    """Calibrate confidences and choose verify lengths.
+# verify-length policies of dspark_schedule_policy
+SCHED_EARLY_STOP, SCHED_BEST_PREFIX, SCHED_THRESHOLD_CUM, SCHED_THRESHOLD_CONF = 0, 1, 2, 3
+
+
+def schedule_prefix(conf_logits, pos_temp, sps, L_min, L_max, *, policy=SCHED_EARLY_STOP, threshold=0.0,
+                    out=None, workspace=None, stream=None):
+    """Calibrate confidences and choose verify lengths (early stop by default;
+    ``policy`` selects another rule of dspark_schedule_policy).
 
     Returns dict(conf, cum_conf, verify_len, theta)."""
     lib = load()
@@ -204,8 +212,9 @@ def schedule_prefix(conf_logits, pos_temp, sps, L_min, L_max, *, out=None, works
                    verify_len=torch.empty((B,), dtype=torch.int32, device=dev),
                    theta=torch.empty((1,), dtype=torch.float64, device=dev))
     ws = workspace if workspace is not None else _default_ws.get(WS_SCHEDULE, B, G, 8, 1, dev)
-    _check(lib.dspark_schedule_prefix(
+    _check(lib.dspark_schedule_policy(
         _ptr(conf_logits), _ptr(pos_temp), _ptr(sps), sps.numel(), B, G, int(L_min), int(L_max),
+        int(policy), float(threshold),
         _ptr(out["conf"]), _ptr(out["cum_conf"]), _ptr(out["verify_len"]), _ptr(out.get("theta")),
         _ptr(ws), ws.numel(), _stream(stream)))
     return out

@@ -1,5 +1,6 @@
 // extern "C" entry points of libdspark: argument checks, workspace planning
 // and the launch sequence of each step.  Nothing here computes on the host.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -122,6 +123,19 @@ dspark_status dspark_schedule_prefix(const float *conf_logits, const float *pos_
                                      int sps_len, int B, int G, int L_min, int L_max, float *conf,
                                      float *cum_conf, int32_t *verify_len, double *theta_out,
                                      void *workspace, size_t workspace_bytes, void *stream) {
+    return dspark_schedule_policy(conf_logits, pos_temp, sps, sps_len, B, G, L_min, L_max,
+                                  DSPARK_SCHED_EARLY_STOP, 0.f, conf, cum_conf, verify_len, theta_out, workspace,
+                                  workspace_bytes, stream);
+}
+
+dspark_status dspark_schedule_policy(const float *conf_logits, const float *pos_temp, const float *sps,
+                                     int sps_len, int B, int G, int L_min, int L_max, int policy, float threshold,
+                                     float *conf, float *cum_conf, int32_t *verify_len, double *theta_out,
+                                     void *workspace, size_t workspace_bytes, void *stream) {
+    if (policy < DSPARK_SCHED_EARLY_STOP || policy > DSPARK_SCHED_THRESHOLD_CONF)
+        return fail(DSPARK_ERR_INVALID_ARG, "unknown scheduling policy %d", policy);
+    if (policy >= DSPARK_SCHED_THRESHOLD_CUM && !std::isfinite(threshold))
+        return fail(DSPARK_ERR_INVALID_ARG, "threshold must be finite");
     if (B < 1 || G < 1 || G > kMaxG) return fail(DSPARK_ERR_INVALID_ARG, "bad B=%d or G=%d", B, G);
     if (L_min < 0 || L_min > L_max || L_max > G)
         return fail(DSPARK_ERR_INVALID_ARG, "need 0 <= L_min <= L_max <= G (got %d, %d, %d)", L_min, L_max, G);
@@ -138,7 +152,7 @@ dspark_status dspark_schedule_prefix(const float *conf_logits, const float *pos_
     cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
     ScheduleArgs a{conf_logits, pos_temp, sps, sps_len, B, G, L_min, L_max, conf, cum_conf, verify_len,
-                   theta_out, static_cast<unsigned char *>(workspace)};
+                   theta_out, static_cast<unsigned char *>(workspace), policy, threshold};
     e = launch_schedule(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
     return DSPARK_OK;

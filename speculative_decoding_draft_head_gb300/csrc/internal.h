@@ -135,6 +135,8 @@ struct ScheduleArgs {
     int32_t *verify_len;
     double *theta_out;
     unsigned char *ws;
+    int policy;        // dspark_sched_policy
+    float threshold;   // policies 2 and 3
 };
 constexpr int kScheduleMaxCells = 16384;  // B * G
 size_t schedule_smem_bytes(int B, int G, int L_min, int L_max);

@@ -7,13 +7,24 @@
 // tokens of all requests in decreasing a while Theta = tau * SPS(B) grows,
 // stopping at the first candidate that does not raise it.
 //
+// The same page's section "Che cosa resta da verificare" says production drops
+// the early stop (and works from confidences two rounds old, which is the
+// caller's choice of input); "Verificare meglio, non di piu'" compares with a
+// fixed confidence threshold.  Policies:
+//  0  early stop (above);
+//  1  no early stop: the admitted count with the largest Theta (first on ties);
+//  2  threshold on a: L_b grows from L_min while a_{b,L_b} > threshold;
+//  3  threshold on c: the same with the per-position confidence (a leading run).
+//
 // One block of 1024 threads (the work is at most a few thousand candidates):
-//  1. c, a per request in fp32 (a fixed left-to-right product);
+//  1. c, a per request in fp32 (a fixed left-to-right product); policies 2-3
+//     decide the lengths here and skip to 5;
 //  2. tau_0 and the candidate list (a, j, b) for L_min <= j < L_max;
 //  3. bitonic sort in shared memory by (a desc, j asc, b asc);
-//  4. block prefix sum of a in fp64, Theta before / after each admission, the first
-//     candidate whose admission does not raise Theta (block min);
-//  5. scatter the admitted counts into the verify lengths.
+//  4. block prefix sum of a in fp64, Theta before / after each admission, and
+//     the first candidate whose admission does not raise Theta (policy 0,
+//     block min) or the count with the largest Theta (policy 1, block argmax);
+//  5. scatter the admitted counts into the verify lengths, Theta of the result.
 #include <climits>
 
 #include "device_common.cuh"
@@ -66,16 +77,47 @@ __device__ double block_exclusive_scan(double v, double *red) {
     return red[warp] + (incl - v);
 }
 
+// Block-wide argmax of (value, index): the larger value, on equal values the
+// smaller index.  Every thread gets the result.
+__device__ void block_argmax(double &v, int &n, double *redv, int *redn) {
+    for (int o = 16; o > 0; o >>= 1) {
+        const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const int n2 = __shfl_xor_sync(0xffffffffu, n, o);
+        if (v2 > v || (v2 == v && n2 < n)) {
+            v = v2;
+            n = n2;
+        }
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) {
+        redv[warp] = v;
+        redn[warp] = n;
+    }
+    __syncthreads();
+    v = (lane < (int)(blockDim.x >> 5)) ? redv[lane] : -INFINITY;
+    n = (lane < (int)(blockDim.x >> 5)) ? redn[lane] : INT_MAX;
+    for (int o = 16; o > 0; o >>= 1) {
+        const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const int n2 = __shfl_xor_sync(0xffffffffu, n, o);
+        if (v2 > v || (v2 == v && n2 < n)) {
+            v = v2;
+            n = n2;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kSchedThreads)
 schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__ pos_temp,
-                const float *__restrict__ sps, int B, int G, int L_min, int L_max, int npow2,
-                float *__restrict__ conf, float *__restrict__ cum_conf,
+                const float *__restrict__ sps, int B, int G, int L_min, int L_max, int npow2, int policy,
+                float threshold, float *__restrict__ conf, float *__restrict__ cum_conf,
                 int32_t *__restrict__ verify_len, double *__restrict__ theta_out,
                 uint32_t *__restrict__ flags) {
     extern __shared__ unsigned long long smem[];
     unsigned long long *key = smem;                       // [npow2] sort keys
     int *len_s = reinterpret_cast<int *>(key + npow2);    // [B]
     __shared__ double red[32];
+    __shared__ int redn[32];
     __shared__ int first_fail;
     __shared__ int bad_temp;
 
@@ -103,22 +145,41 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
         return;
     }
 
-    // 1-2. calibrated confidences, prefix products, tau_0, candidates
-    double tau_part = 0.0;
+    // 1-2. calibrated confidences, prefix products, tau_0, candidates (policies
+    // 2-3: the lengths, tau and the batch tokens of the result)
+    double tau_part = 0.0, tok_part = 0.0;
     for (int b = tid; b < B; b += blockDim.x) {
         float prod = 1.f;
         double t = 1.0;
+        int L = L_min;
+        bool run = true;
         for (int j = 0; j < G; ++j) {
             const float l = conf_logits[(size_t)b * G + j];
             const float c = 1.f / (1.f + expf(-l / pos_temp[j]));
             prod *= c;
             conf[(size_t)b * G + j] = c;
             cum_conf[(size_t)b * G + j] = prod;
-            if (j < L_min) t += (double)prod;
-            if (j >= L_min && j < L_max) key[b * width + (j - L_min)] = cand_key(prod, j * B + b);
+            if (policy >= 2) {
+                if (run && j >= L_min && j < L_max) {
+                    run = (policy == 2 ? prod : c) > threshold;
+                    if (run) L = j + 1;
+                }
+                if (j < L) t += (double)prod;
+            } else {
+                if (j < L_min) t += (double)prod;
+                if (j >= L_min && j < L_max) key[b * width + (j - L_min)] = cand_key(prod, j * B + b);
+            }
         }
         tau_part += t;
-        len_s[b] = L_min;
+        len_s[b] = L;
+        tok_part += (double)(L + 1);
+    }
+    if (policy >= 2) {
+        const double tau = block_sum(tau_part, red);
+        const double tok = block_sum(tok_part, red);
+        for (int b = tid; b < B; b += blockDim.x) verify_len[b] = len_s[b];
+        if (tid == 0 && theta_out) *theta_out = tau * (double)sps[(long)tok];
+        return;
     }
     for (int i = ncand + tid; i < npow2; i += blockDim.x) key[i] = ~0ull;
     const double tau0 = block_sum(tau_part, red);
@@ -151,18 +212,36 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
     for (int i = lo; i < hi; ++i) local += a_of(i);
     const double before = block_exclusive_scan(local, red);
     double run = tau0 + before;  // tau before candidate lo
-    for (int i = lo; i < hi; ++i) {
-        const double a = a_of(i);
-        const double th_before = run * (double)sps[n0 + i];
-        const double th_after = (run + a) * (double)sps[n0 + i + 1];
-        if (!(th_after > th_before)) {
-            atomicMin(&first_fail, i);
-            break;
+    int nstar;
+    if (policy == 0) {
+        for (int i = lo; i < hi; ++i) {
+            const double a = a_of(i);
+            const double th_before = run * (double)sps[n0 + i];
+            const double th_after = (run + a) * (double)sps[n0 + i + 1];
+            if (!(th_after > th_before)) {
+                atomicMin(&first_fail, i);
+                break;
+            }
+            run += a;
         }
-        run += a;
+        __syncthreads();
+        nstar = first_fail;
+    } else {
+        // Theta after admitting the first n candidates, n = 0 .. ncand
+        double bv = (tid == 0) ? tau0 * (double)sps[n0] : -INFINITY;
+        int bn = (tid == 0) ? 0 : INT_MAX;
+        for (int i = lo; i < hi; ++i) {
+            run += a_of(i);
+            const double th = run * (double)sps[n0 + i + 1];
+            if (th > bv) {
+                bv = th;
+                bn = i + 1;
+            }
+        }
+        block_argmax(bv, bn, red, redn);
+        nstar = bn;
+        __syncthreads();
     }
-    __syncthreads();
-    const int nstar = first_fail;
     // tau after the admitted prefix, for Theta
     double adm = 0.0;
     for (int i = lo; i < min(hi, nstar); ++i) adm += a_of(i);
@@ -186,6 +265,7 @@ size_t schedule_smem_bytes(int B, int G, int L_min, int L_max) {
 }
 
 cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
+    // (policies 2-3 do not sort, but one launch shape serves all)
     const long ncand = (long)a.B * (a.L_max - a.L_min);
     int npow2 = 1;
     while (npow2 < ncand) npow2 <<= 1;
@@ -193,8 +273,8 @@ cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     schedule_kernel<<<1, kSchedThreads, smem, s>>>(a.conf_logits, a.pos_temp, a.sps, a.B, a.G, a.L_min,
-                                                    a.L_max, npow2, a.conf, a.cum_conf, a.verify_len,
-                                                    a.theta_out, reinterpret_cast<uint32_t *>(a.ws));
+                                                    a.L_max, npow2, a.policy, a.threshold, a.conf, a.cum_conf,
+                                                    a.verify_len, a.theta_out, reinterpret_cast<uint32_t *>(a.ws));
     return cudaGetLastError();
 }
 
