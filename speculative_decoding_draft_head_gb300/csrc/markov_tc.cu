@@ -171,13 +171,20 @@ __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, vola
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void unpack16(const uint4 &lo, const uint4 &hi, float (&x)[16]) {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        x[2 * i] = bf16_lo(w[i]);
-        x[2 * i + 1] = bf16_hi(w[i]);
+// Element i (a compile-time constant after unrolling) of 16 packed bf16.
+__device__ __forceinline__ float bf16_at(const uint4 &lo, const uint4 &hi, int i) {
+    uint32_t wd;
+    switch (i >> 1) {
+        case 0: wd = lo.x; break;
+        case 1: wd = lo.y; break;
+        case 2: wd = lo.z; break;
+        case 3: wd = lo.w; break;
+        case 4: wd = hi.x; break;
+        case 5: wd = hi.y; break;
+        case 6: wd = hi.z; break;
+        default: wd = hi.w; break;
     }
+    return (i & 1) ? bf16_hi(wd) : bf16_lo(wd);
 }
 
 // 16 bf16 values starting at p (n valid; the rest read as 0).
@@ -725,9 +732,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         // take this sub-slice's prefetched values, then prefetch the next
                         // one's (before any skip: the skipped sub-slice may come first
                         // when walking the segment backwards)
-                        float u[16], tt[16];
-                        unpack16(nu_lo, nu_hi, u);
-                        unpack16(nt_lo, nt_hi, tt);
+                        // z = base + bias at once (the bias registers die), the target
+                        // kept packed as bf16 pairs
+                        float z[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) z[i] = bf16_at(nu_lo, nu_hi, i) + __uint_as_float(acc[i]);
+                        const uint4 ct_lo = nt_lo, ct_hi = nt_hi;
                         {
                             const int tn = t + h, hn = h ^ 1;  // the next sub-slice
                             const int vn = (tn < ntiles) ? sub_col(tn, hn) : ve;
@@ -745,9 +755,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         // upper bound of p - q under the approximate exponentials;
                         // rb <= 0 gives a threshold <= 1 <= f1: no candidate
                         auto rbound = [&](int i) -> float {
-                            const float z = u[i] + __uint_as_float(acc[i]);
-                            const float pv = fast_exp2(fmaf(tt[i], c2, -lse_t2));
-                            const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
+                            const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -lse_t2));
+                            const float qv = fast_exp2(fmaf(z[i], c2, -lse_q2));
                             return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
                         };
                         uint32_t gmask = 0;
@@ -768,18 +777,19 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 #pragma unroll
                                 for (int c = 0; c < 4; ++c) {
                                     const int i0 = c, i1 = 4 + c, i2 = 8 + c, i3 = 12 + c;
-                                    const float ui = g == 0 ? u[i0] : (g == 1 ? u[i1] : (g == 2 ? u[i2] : u[i3]));
-                                    const float ti = g == 0 ? tt[i0] : (g == 1 ? tt[i1] : (g == 2 ? tt[i2] : tt[i3]));
-                                    const uint32_t ai = g == 0 ? acc[i0] : (g == 1 ? acc[i1] : (g == 2 ? acc[i2] : acc[i3]));
-                                    const float z = ui + __uint_as_float(ai);
+                                    const float ti = g == 0 ? bf16_at(ct_lo, ct_hi, i0)
+                                                            : (g == 1 ? bf16_at(ct_lo, ct_hi, i1)
+                                                                      : (g == 2 ? bf16_at(ct_lo, ct_hi, i2)
+                                                                                : bf16_at(ct_lo, ct_hi, i3)));
+                                    const float zi = g == 0 ? z[i0] : (g == 1 ? z[i1] : (g == 2 ? z[i2] : z[i3]));
                                     const float pv = fast_exp2(fmaf(ti, c2, -lse_t2));
-                                    const float qv = fast_exp2(fmaf(z, c2, -lse_q2));
+                                    const float qv = fast_exp2(fmaf(zi, c2, -lse_q2));
                                     const float rbi = (active && 4 * g + c < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
                                     const uint32_t word = word_of(wg, c);
                                     if (!(one_minus_uniform_plus_one(word) < fmaf(rbi, Qr, 1.f))) continue;
                                     // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
                                     // log2 q formed from the logit difference first (+inf for bonus rows)
-                                    const float delta2 = fmaf(ti - z, c2, lse_q2 - lse_t2);
+                                    const float delta2 = fmaf(ti - zi, c2, lse_q2 - lse_t2);
                                     if (!(delta2 > 0.f)) continue;
                                     const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
                                     const float key = fmaf(ti, c2, -lse_t2) + l1 - fast_log2(neg_log_uniform(word));
