@@ -263,8 +263,13 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
             }
             Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
+        if (full) {  // warp-uniform: only segment tails are ragged
 #pragma unroll
-        for (int i = 0; i < 16; ++i) e[i] = (full || i < n) ? fast_exp2(fmaf(z[i], c2, -st.m)) : 0.f;
+            for (int i = 0; i < 16; ++i) e[i] = fast_exp2(fmaf(z[i], c2, -st.m));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) e[i] = (i < n) ? fast_exp2(fmaf(z[i], c2, -st.m)) : 0.f;
+        }
         float sum = sum16(e);
         if (!(sum <= 0x1p64f)) {  // far above the reference (or overflow): renormalise
             float zm = -INFINITY;
