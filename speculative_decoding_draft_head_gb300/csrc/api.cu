@@ -99,9 +99,8 @@ dspark_status dspark_draft_sample(const void *base_logits, const void *e_in, con
     DraftArgs a{base_logits, e_in, w_out, anchor, temperature, request_id, B, G, V, r, dtype, seed,
                 draft_tokens, draft_lse, draft_logq, draft_logits, static_cast<unsigned char *>(workspace)};
     if (plan.tensor_path) {
-        e = cudaMemsetAsync(static_cast<unsigned char *>(workspace) + plan.best_offset, 0,
-                            sizeof(unsigned long long) * (size_t)B * (size_t)G, s);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the row-wide best words");
+        e = cudaMemsetAsync(static_cast<unsigned char *>(workspace) + plan.best_offset, 0, plan.clear_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the row-wide best words and barrier counters");
         // the tokens feed the next position through the best words; the
         // partials of every position are merged once at the end
         e = launch_draft_tensor(a, plan, s);

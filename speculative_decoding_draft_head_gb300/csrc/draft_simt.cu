@@ -227,8 +227,11 @@ DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
     }
     const size_t npart = (size_t)B * p.nsplit * (p.tensor_path ? (size_t)G : 1);
     p.best_offset = align_up(p.partial_offset + sizeof(RowState) * npart, 256);
-    p.ws_bytes = align_up(p.best_offset + (p.tensor_path ? sizeof(unsigned long long) * (size_t)B * (size_t)G : 0),
-                          256);
+    const size_t words = p.tensor_path ? sizeof(unsigned long long) * (size_t)B * (size_t)G : 0;
+    p.bar_offset = p.best_offset + words;  // 8-byte aligned
+    const size_t bars = p.tensor_path ? sizeof(unsigned int) * (size_t)p.row_blocks : 0;
+    p.clear_bytes = words + bars;
+    p.ws_bytes = align_up(p.bar_offset + bars, 256);
     return p;
 }
 

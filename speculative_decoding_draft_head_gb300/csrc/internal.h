@@ -11,7 +11,6 @@ namespace dspark {
 
 constexpr int kNumSMs = 152;            // GB300: 2 dies x 76 SMs
 constexpr size_t kFlagBytes = 256;      // flag word region at the head of every workspace
-constexpr size_t kGridBarOffset = 64;   // grid-barrier counter of the draft kernel, inside the flag region
 constexpr int kMaxG = 64;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -28,6 +27,8 @@ struct DraftPlan {
     int chunk;             // vocabulary entries per segment (multiple of 4)
     size_t partial_offset; // byte offset of the per-(row, segment) partials ([G][B][nsplit] on the tensor path)
     size_t best_offset;    // [G][B] 64-bit row-wide best (key, token) words (tensor path), zeroed per call
+    size_t bar_offset;     // [row_blocks] barrier counters between positions (tensor path), zeroed per call
+    size_t clear_bytes;    // bytes from best_offset to zero per call (words + counters)
     size_t ws_bytes;
 };
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt);

@@ -119,7 +119,7 @@ struct TcParams {
     PhiloxRoundKeys keys;
     RowState *part;             // draft: [G][B][nseg] softmax / key partials
     unsigned long long *best;   // draft: [G][B] row-wide best (key, token), see best_encode
-    unsigned int *grid_bar;     // draft, several positions: arrival counter of the grid barrier
+    unsigned int *grid_bar;     // draft, several positions: [row blocks] arrival counters of the barrier
     ResidualState *rpart;
     uint32_t *flags;
     float *z_out;
@@ -831,10 +831,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 }
             }
             if (!kFinal && pi + 1 < npos) {
-                // every CTA has published this position's rows: x_j is final
+                // every CTA of this row block has published its rows: x_j is final
+                // (a row block needs only its own rows' words)
                 asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
                 if (threadIdx.x == 0 &&
-                    !grid_sync(p.grid_bar, (unsigned int)(pi + 1) * gridDim.x * gridDim.y, abort, kSpinLimit)) {
+                    !grid_sync(p.grid_bar + blockIdx.y, (unsigned int)(pi + 1) * gridDim.x, abort, kSpinLimit)) {
                     *abort = 1;
                     atomicOr(p.flags, kFlagTimeout);
                 }
@@ -980,7 +981,7 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStr
     p.keys = round_keys(a.seed);
     p.part = reinterpret_cast<RowState *>(a.ws + pl.partial_offset);
     p.best = reinterpret_cast<unsigned long long *>(a.ws + pl.best_offset);
-    p.grid_bar = reinterpret_cast<unsigned int *>(a.ws + kGridBarOffset);
+    p.grid_bar = reinterpret_cast<unsigned int *>(a.ws + pl.bar_offset);
     p.flags = reinterpret_cast<uint32_t *>(a.ws);
     p.z_out = a.z_out;
     const dim3 grid(pl.nsplit, pl.row_blocks);
