@@ -240,26 +240,40 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
     float e[16];
     if (on) {
         if (st.m == -INFINITY) {
-            float zm = z[0];
-            int im = 0;
+            // exact keys of the top token of each group of four: the best of them
+            // seeds the threshold
+            float zm = -INFINITY, kb = -INFINITY, sb = 0.f;
+            int ib = INT32_MAX;
 #pragma unroll
-            for (int i = 1; i < 16; ++i)
-                if ((full || i < n) && z[i] > zm) {
-                    zm = z[i];
-                    im = i;
+            for (int g = 0; g < 4; ++g) {
+                float zg = -INFINITY;
+                int ig = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int i = 4 * g + c;
+                    if ((full || i < n) && z[i] > zg) {
+                        zg = z[i];
+                        ig = c;
+                    }
                 }
+                if (zg == -INFINITY) continue;  // ragged tail: an empty group
+                zm = fmaxf(zm, zg);
+                const uint32_t word = ig == 0 ? w[g].x : (ig == 1 ? w[g].y : (ig == 2 ? w[g].z : w[g].w));
+                const float s2 = zg * c2;
+                const float key = s2 - fast_log2(neg_log_uniform(word));
+                if (key > kb) {
+                    kb = key;
+                    sb = s2;
+                    ib = v + 4 * g + ig;
+                }
+            }
             st.m = zm * c2;  // c2 > 0: the rounded product is monotone in z
-            uint32_t word = 0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (i == im) word = word_of(w[i >> 2], i & 3);
-            const float key = st.m - fast_log2(neg_log_uniform(word));
-            if (key > kbest) {
-                st.key = key;
-                st.s_at = st.m;
-                st.idx = v + im;
-                kbest = key;
-                atomicMax(best, best_encode(key, v + im));
+            if (kb > kbest) {
+                st.key = kb;
+                st.s_at = sb;
+                st.idx = ib;
+                kbest = kb;
+                atomicMax(best, best_encode(kb, ib));
             }
             Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
@@ -724,15 +738,18 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         const bool on = active && c2 > 0.f;
                         if (on) {
                             // the row-wide best key loaded one sub-slice earlier (the high
-                            // word of the row's best); reload it for the next
+                            // word of the row's best)
                             const float kg = ordered_to_key(kg_next);
-                            kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
                             if (kg > kbest) {
                                 kbest = kg;
                                 Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
                             }
                         }
                         draft_sample16(st, Q, kbest, z, c2, n, v, on, best, w);
+                        // reload it for the next sub-slice, after this one's publications
+                        // (at the start of a position the other threads are publishing
+                        // their first batches now)
+                        if (on) kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
                     } else {
                         // take this sub-slice's prefetched values, then prefetch the next
                         // one's (before any skip: the skipped sub-slice may come first
