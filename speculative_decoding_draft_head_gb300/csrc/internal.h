@@ -79,6 +79,7 @@ struct FinalArgs {
     int pass;                  // traversal direction of the vocabulary segments (odd: backwards)
     uint64_t seed;
     void *rpart;               // [B][nseg] final-draw partials
+    uint32_t *res_best;        // [B] row-wide best residual key (ordered encoding), zeroed by the decide pass
     uint32_t *flags;
 };
 cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s);
@@ -95,6 +96,7 @@ struct VerifyPlan {
     size_t res_row_offset;  // [B] int32: rejected position or -1
     size_t lse_t_offset;    // [B] fp32: target lse of the rejected row
     size_t res_part_offset; // [B][res_split] ResidualState
+    size_t res_best_offset; // [B] uint32 row-wide best residual key of the tensor-core final draw
     size_t ws_bytes;
 };
 VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt);

@@ -121,6 +121,7 @@ struct TcParams {
     unsigned long long *best;   // draft: [G][B] row-wide best (key, token), see best_encode
     unsigned int *grid_bar;     // draft, several positions: [row blocks] arrival counters of the barrier
     ResidualState *rpart;
+    uint32_t *res_best;         // final draw: [B] row-wide best residual key (ordered encoding)
     uint32_t *flags;
     float *z_out;
 };
@@ -640,6 +641,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             unsigned long long *best = (kFinal || b >= p.B) ? nullptr : p.best + (size_t)jj * p.B + b;
             uint32_t kg_next = 0u;  // "none"
             float Qr = kQMax;       // 2^-K for the residual candidate test (with margin)
+            float kbest_r = -INFINITY;  // best residual key of the row known to this thread
+            uint32_t kr_next = 0u;      // the row-wide word, loaded one sub-slice ahead ("none")
+            uint32_t *res_best = (kFinal && active) ? p.res_best + b : nullptr;
             ResidualState rs = residual_init();
             float lse_q2 = 0.f, lse_t2 = 0.f;
             const __nv_bfloat16 *urow = nullptr, *trow = nullptr;
@@ -781,6 +785,56 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             const float qv = fast_exp2(fmaf(z[i], c2, -lse_q2));
                             return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
                         };
+                        // exact residual key of a token with target logit ti and draft
+                        // logit zi (-inf where p <= q)
+                        auto rkey = [&](float ti, float zi, uint32_t word) -> float {
+                            // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
+                            // log2 q formed from the logit difference first (+inf for bonus rows)
+                            const float delta2 = fmaf(ti - zi, c2, lse_q2 - lse_t2);
+                            if (!(delta2 > 0.f)) return -INFINITY;
+                            const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
+                            return fmaf(ti, c2, -lse_t2) + l1 - fast_log2(neg_log_uniform(word));
+                        };
+                        if (active) {
+                            // the row-wide best key (one sub-slice old) tightens the threshold
+                            const float kg = ordered_to_key(kr_next);
+                            if (kg > kbest_r) {
+                                kbest_r = kg;
+                                Qr = fminf(fast_exp2(-kbest_r), kQMax) * kMargin;
+                            }
+                            if (rs.key_res == -INFINITY && kbest_r == -INFINITY) {
+                                // first batch: exact keys of each group's most promising
+                                // token (largest bound) seed the threshold
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) {
+                                    float rbm = 0.f, tm = 0.f, zm = 0.f;
+                                    int im = -1;
+                                    uint32_t word = 0;
+#pragma unroll
+                                    for (int c = 0; c < 4; ++c) {
+                                        const float r = rbound(4 * g + c);
+                                        if (r > rbm) {
+                                            rbm = r;
+                                            im = c;
+                                            tm = bf16_at(ct_lo, ct_hi, 4 * g + c);
+                                            zm = z[4 * g + c];
+                                            word = word_of(w[g], c);
+                                        }
+                                    }
+                                    if (im < 0) continue;
+                                    const float key = rkey(tm, zm, word);
+                                    if (key > rs.key_res) {
+                                        rs.key_res = key;
+                                        rs.idx_res = v + 4 * g + im;
+                                    }
+                                }
+                                if (rs.key_res > kbest_r) {
+                                    kbest_r = rs.key_res;
+                                    atomicMax(res_best, key_to_ordered(kbest_r));
+                                }
+                                Qr = fminf(fast_exp2(-kbest_r), kQMax) * kMargin;
+                            }
+                        }
                         uint32_t gmask = 0;
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
@@ -821,8 +875,14 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                                     }
                                 }
                             }
-                            Qr = fminf(fast_exp2(-rs.key_res), kQMax) * kMargin;
+                            if (rs.key_res > kbest_r) {
+                                kbest_r = rs.key_res;
+                                atomicMax(res_best, key_to_ordered(kbest_r));
+                            }
+                            Qr = fminf(fast_exp2(-kbest_r), kQMax) * kMargin;
                         }
+                        // the row-wide word for the next sub-slice, after this one's publication
+                        if (active) kr_next = load_relaxed(res_best);
                     }
                 }
             }
@@ -1046,6 +1106,7 @@ cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     p.nseg = a.nseg;
     p.keys = round_keys(a.seed);
     p.rpart = reinterpret_cast<ResidualState *>(a.rpart);
+    p.res_best = a.res_best;
     p.flags = a.flags;
     // the final draw reads its base rows directly: map_u is unused
     markov_tc_kernel<true><<<dim3(a.nseg, tc_row_blocks(a.B)), kThreads, kSmemBytes, s>>>(mw, mw, p);

@@ -133,7 +133,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
                                      int32_t *__restrict__ out_tokens, int32_t *__restrict__ num_out,
                                      float *__restrict__ target_lse, float *__restrict__ logp_sel,
                                      int32_t *__restrict__ final_code, float *__restrict__ lse_t_row,
-                                     uint32_t *__restrict__ flags) {
+                                     uint32_t *__restrict__ res_best, uint32_t *__restrict__ flags) {
     const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -170,6 +170,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
             accept_len[b] = -1;
             num_out[b] = 0;
             final_code[b] = -1;
+            res_best[b] = 0u;
         }
         return;
     }
@@ -230,6 +231,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         accept_len[b] = k;
         num_out[b] = k + 1;
         final_code[b] = code;
+        res_best[b] = 0u;  // "none" for the final draw's row-wide best key
     }
 }
 
@@ -397,6 +399,7 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     int32_t *final_code = reinterpret_cast<int32_t *>(a.ws + p.res_row_offset);
     float *lse_t_row = reinterpret_cast<float *>(a.ws + p.lse_t_offset);
     ResidualState *res_part = reinterpret_cast<ResidualState *>(a.ws + p.res_part_offset);
+    uint32_t *res_best = reinterpret_cast<uint32_t *>(a.ws + p.res_best_offset);
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
     const TIn *target = static_cast<const TIn *>(a.target);
 
@@ -408,7 +411,7 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     verify_decide_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
         target, row_part, p.row_split, a.anchor, a.draft_tokens, a.draft_logq, a.verify_len, a.temperature,
         a.request_id, a.B, a.G, a.V, k0, k1, a.accept_len, a.out_tokens, a.num_out, a.target_lse,
-        a.logp_sel, final_code, lse_t_row, flags);
+        a.logp_sel, final_code, lse_t_row, res_best, flags);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const bool tensor = p.tensor_residual && !a.z_in;
     const int res_nsplit = tensor ? p.res_split_tc : p.res_split;
@@ -416,7 +419,7 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
         // the last draft launch (position G-1) walked in direction G-1: continue from its end
         FinalArgs fa{a.target, a.base, a.e_in, a.w_out, a.anchor, a.draft_tokens, a.temperature,
                      a.request_id, final_code, lse_t_row, a.draft_lse, a.B, a.G, a.V, a.r, res_nsplit,
-                     a.G, a.seed, res_part, flags};
+                     a.G, a.seed, res_part, res_best, flags};
         e = launch_final_tensor(fa, s);
     } else {
         const size_t smem = sizeof(float) * (size_t)a.r;
@@ -472,6 +475,8 @@ VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {
     off = align_up(off + sizeof(float) * (size_t)B, 256);
     p.res_part_offset = off;
     off = align_up(off + sizeof(ResidualState) * (size_t)B * res_slots, 256);
+    p.res_best_offset = off;
+    off = align_up(off + sizeof(uint32_t) * (size_t)B, 256);
     p.ws_bytes = off;
     return p;
 }
