@@ -118,6 +118,7 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
     int *len_s = reinterpret_cast<int *>(key + npow2);    // [B]
     __shared__ double red[32];
     __shared__ int redn[32];
+    __shared__ unsigned long long xch[kSchedThreads];  // register-sort exchange
     __shared__ int first_fail;
     __shared__ int bad_temp;
 
@@ -185,21 +186,45 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
     const double tau0 = block_sum(tau_part, red);
     __syncthreads();
 
-    // 3. bitonic sort: highest priority first
-    for (int k = 2; k <= npow2; k <<= 1) {
-        for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            for (int i = tid; i < npow2; i += blockDim.x) {
-                const int ixj = i ^ jj;
-                if (ixj > i) {
-                    const unsigned long long ki = key[i], kx = key[ixj];
-                    const bool up = (i & k) == 0;
-                    if (up ? (kx < ki) : (ki < kx)) {
-                        key[i] = kx;
-                        key[ixj] = ki;
+    // 3. bitonic sort: highest priority first (ascending keys)
+    if (npow2 <= kSchedThreads) {
+        // one key per thread (padding sorts last): partners closer than a warp
+        // are exchanged by shuffle, the others through shared memory
+        unsigned long long kv = (tid < npow2) ? key[tid] : ~0ull;
+        for (int k = 2; k <= kSchedThreads; k <<= 1) {
+            for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                unsigned long long other;
+                if (jj >= 32) {
+                    __syncthreads();
+                    xch[tid] = kv;
+                    __syncthreads();
+                    other = xch[tid ^ jj];
+                } else {
+                    other = __shfl_xor_sync(0xffffffffu, kv, jj);
+                }
+                const bool up = (tid & k) == 0, lower = (tid & jj) == 0;
+                kv = (up == lower) ? min(kv, other) : max(kv, other);
+            }
+        }
+        __syncthreads();
+        if (tid < npow2) key[tid] = kv;
+        __syncthreads();
+    } else {
+        for (int k = 2; k <= npow2; k <<= 1) {
+            for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                for (int i = tid; i < npow2; i += blockDim.x) {
+                    const int ixj = i ^ jj;
+                    if (ixj > i) {
+                        const unsigned long long ki = key[i], kx = key[ixj];
+                        const bool up = (i & k) == 0;
+                        if (up ? (kx < ki) : (ki < kx)) {
+                            key[i] = kx;
+                            key[ixj] = ki;
+                        }
                     }
                 }
+                __syncthreads();
             }
-            __syncthreads();
         }
     }
 
