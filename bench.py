@@ -307,30 +307,52 @@ def run_ours(args, w):
     # end to end: per-round inputs from pinned host memory, emitted tokens back
     per_round = ("base", "target", "anchor", "temperature", "request_id", "conf_logits")
     host = {k: inp[k].cpu().pin_memory() for k in per_round}
-    dev_in = dict(inp)
     out_host = dict(out_tokens=torch.empty((B, G + 1), dtype=torch.int32).pin_memory(),
                     num_out=torch.empty((B,), dtype=torch.int32).pin_memory())
     h2d = sum(host[k].numel() * host[k].element_size() for k in per_round)
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
-    def e2e_step():
-        for k in per_round:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        step(dev_in)
-        out_host["out_tokens"].copy_(v_out["out_tokens"], non_blocking=True)
-        out_host["num_out"].copy_(v_out["num_out"], non_blocking=True)
+    # Double-buffered: the copies of step i + 1 run on a copy stream while step i
+    # computes (every step still copies its whole input from pinned host memory,
+    # inside the timed region; H2D is the bound at about 200 GB/s).
+    copy_stream = torch.cuda.Stream(dev)
+    bufs = [{k: (inp[k].clone() if k in per_round else inp[k]) for k in inp} for _ in range(2)]
+    ev_copied = [torch.cuda.Event() for _ in range(2)]
+    ev_used = [torch.cuda.Event() for _ in range(2)]
+    used_recorded = [False, False]
 
-    dev_in = {k: (inp[k].clone() if k in per_round else inp[k]) for k in inp}
-    for _ in range(2):
-        e2e_step()
+    def issue_copy(i, start_ev=None):
+        b = i % 2
+        with torch.cuda.stream(copy_stream):
+            if start_ev is not None:
+                copy_stream.wait_event(start_ev)
+            if used_recorded[b]:
+                copy_stream.wait_event(ev_used[b])  # step i - 2 is done with this buffer
+            for k in per_round:
+                bufs[b][k].copy_(host[k], non_blocking=True)
+            ev_copied[b].record(copy_stream)
+
+    def e2e_run(n, start_ev=None):
+        issue_copy(0, start_ev)
+        for i in range(n):
+            if i + 1 < n:
+                issue_copy(i + 1)
+            b = i % 2
+            stream.wait_event(ev_copied[b])
+            step(bufs[b])
+            ev_used[b].record(stream)
+            used_recorded[b] = True
+            out_host["out_tokens"].copy_(v_out["out_tokens"], non_blocking=True)
+            out_host["num_out"].copy_(v_out["num_out"], non_blocking=True)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     e_steps = max(3, args.steps // 4)
     _barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
+    e2e_run(e_steps, start_ev=e0)
     e1.record(stream)
     torch.cuda.synchronize()
     _barrier(world)
@@ -376,7 +398,8 @@ def run_ours(args, w):
                        tflops_over_draft_time=bias_flops / (d_ms / 1000.0) / 1e12,
                        peak_tflops=peaks["bf16_tflops_sustained"]),
         e2e=dict(value=e_value, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
-                 ms_per_step=e_ms),
+                 ms_per_step=e_ms, copies="pinned host -> device each step, overlapped with the previous "
+                                         "step's compute (two input buffers, a copy stream)"),
         gpu_launches=args.steps * (launches_draft + (1 if w.scheduler else 0) + 4),
         clocks=clk,
     )
