@@ -659,7 +659,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 }
             }
             // this thread's 16-token sub-slice h of tile t of this position
-            auto sub_col = [&](int t, int h) { return tile_col(pi * ntiles + t) + slice * 32 + h * 16; };
+            // (the direction of this position, known here: no division per sub-slice)
+            const bool rev_pos = (((kFinal ? p.pass : p.j + pi)) & 1) != 0;
+            const int col0 = vb + slice * 32;
+            auto sub_col = [&](int t, int h) { return col0 + (rev_pos ? (ntiles - 1 - t) : t) * BN + h * 16; };
             // final draw: this thread's base / target values, one sub-slice ahead
             uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
             if (kFinal && active && ntiles > 0) {
