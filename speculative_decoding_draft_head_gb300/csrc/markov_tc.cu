@@ -66,10 +66,19 @@ using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BN = 128;                  // tokens per tile: the UMMA N
-constexpr int kEpiWarps = 16;
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;              // and kMmaWarp + 1: even / odd tiles
-constexpr int kThreads = 19 * 32;
+#ifndef DSPARK_EPI_WARPS
+#define DSPARK_EPI_WARPS 16
+#endif
+constexpr int kEpiWarps = DSPARK_EPI_WARPS;  // a multiple of 4: one group per TMEM lane quadrant
+constexpr int kEpiPerQuad = kEpiWarps / 4;   // warps sharing a quadrant's 16-column sub-slices
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;      // and kMmaWarp + 1: even / odd tiles
+constexpr int kThreads = (kEpiWarps + 3) * 32;
+// registers per thread such that the warps of the busiest SM sub-partition fit its 16K
+constexpr int kMaxRegs = (16384 / (32 * ((kEpiWarps + 3 + 3) / 4))) / 8 * 8 > 96
+                             ? 96
+                             : (16384 / (32 * ((kEpiWarps + 3 + 3) / 4))) / 8 * 8;
+static_assert(kEpiWarps % 4 == 0 && kEpiPerQuad <= 8, "epilogue warps");
 constexpr int kWStages = 8;              // W ring: one 64-wide K atom of one tile per stage
 constexpr int kUStages = 2;              // = tile slots: tile t fills slot t % 2
 constexpr int kAccBufs = 3;
@@ -87,7 +96,7 @@ constexpr uint32_t kIBytes = 16 * 128;
 // per-row merge of the four column slices (the W ring keeps streaming the
 // next block position meanwhile)
 constexpr uint32_t kOffMerge = kOffI + kIBytes;
-constexpr uint32_t kMergeBytes = BM * 4 * 32;
+constexpr uint32_t kMergeBytes = BM * kEpiPerQuad * 32;
 constexpr uint32_t kOffBar = kOffMerge + kMergeBytes;
 constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs + 1;
 static_assert(kNumBars * 8 <= 256, "barrier region");
@@ -341,7 +350,7 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
 }
 
 // 18 warps: 5 share one SM sub-partition's 16K registers, so at most 96 each.
-// 19 warps: five share some SM sub-partition's 16K registers, so at most 96 each.
+// The warps of the busiest SM sub-partition share its 16K registers: kMaxRegs each.
 //
 // The draft form walks block positions p.j .. p.j_end - 1 in one launch when
 // the launch is cooperative: between positions every CTA publishes its rows'
@@ -351,7 +360,7 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
 // already been streaming the next position's W_out and base-logit tiles.
 // Tile, ring and accumulator counters run on across positions.
 template <bool kFinal>
-__global__ void __maxnreg__(96)
+__global__ void __maxnreg__(kMaxRegs)
 markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
                  const __grid_constant__ TcParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -404,7 +413,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         }
         for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), kEpiWarps);
+            mbar_init(tempty(a), 32);  // one arrival per 16-column sub-slice of each quadrant
         }
         mbar_init(a_ready, kEpiWarps);
         *abort = 0;
@@ -579,7 +588,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue ----
-        const int q = warp & 3, slice = warp >> 2;
+        const int q = warp & 3, slice = warp >> 2;  // quadrant, index within the quadrant's warps
         const int row = q * 32 + lane;
         const int b = m0 + row;
         const float c2 = row_c2[row];
@@ -658,37 +667,40 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     lse_t2 = 0.f;       // unnormalised p: the same argmax
                 }
             }
-            // this thread's 16-token sub-slice h of tile t of this position
-            // (the direction of this position, known here: no division per sub-slice)
+            // this warp's 16-token sub-slices of this position: sub-slice si is
+            // column block si % 8 of tile si / 8; the quadrant's warps take every
+            // kEpiPerQuad-th one (so no warp skips a tile)
             const bool rev_pos = (((kFinal ? p.pass : p.j + pi)) & 1) != 0;
-            const int col0 = vb + slice * 32;
-            auto sub_col = [&](int t, int h) { return col0 + (rev_pos ? (ntiles - 1 - t) : t) * BN + h * 16; };
+            const int nsub = ntiles * 8;
+            auto sub_col = [&](int si) {
+                const int t = si >> 3;
+                return vb + (rev_pos ? (ntiles - 1 - t) : t) * BN + (si & 7) * 16;
+            };
             // final draw: this thread's base / target values, one sub-slice ahead
             uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
-            if (kFinal && active && ntiles > 0) {
-                const int v = sub_col(0, 0);
+            if (kFinal && active && slice < nsub) {
+                const int v = sub_col(slice);
                 const int n = min(16, ve - v);
                 if (n > 0) {
                     load16_bf16(trow + v, n, nt_lo, nt_hi);
                     if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
                 }
             }
-            for (int t = 0; t < ntiles && ok; ++t) {
+            int waited = -1;  // the last tile whose accumulator this warp waited for
+#pragma unroll 1
+            for (int si = slice; si < nsub && ok; si += kEpiPerQuad) {
+                const int t = si >> 3;
                 const int tg = pi * ntiles + t;
                 const int a = tg % kAccBufs;
                 const uint32_t aph = (uint32_t)(tg / kAccBufs) & 1u;
-                // one copy of the sub-slice body (a second would overflow the
-                // instruction cache)
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    // The Philox words need nothing from the tensor cores.  The first
-                    // sub-slice draws them while the tile's UMMAs may still run; the
-                    // second issues its TMEM load first and draws them under its latency.
+                {
+                    // The Philox words need nothing from the tensor cores.
                     uint4 w[4];
                     uint32_t acc[16];
-                    const int vw = sub_col(t, h);
-                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + slice * 32 + h * 16;
-                    if (h == 0) {
+                    const int vw = sub_col(si);
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + (si & 7) * 16;
+                    if (t != waited) {
+                        // a new tile: draw the words while its UMMAs may still run
                         if (vw < ve) {
 #pragma unroll
                             for (int g = 0; g < 4; ++g)
@@ -703,8 +715,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             break;
                         }
                         tc_fence_after();
+                        waited = t;
                         tmem_ld16(taddr, acc);
                     } else {
+                        // the tile is ready: issue the TMEM load, draw under its latency
                         tmem_ld16(taddr, acc);
                         if (vw < ve) {
 #pragma unroll
@@ -713,11 +727,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         }
                     }
                     tmem_ld_wait16(acc);
-                    if (h == 1) {  // both halves are in registers: hand the accumulator back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty(a));
-                    }
+                    // this sub-slice is in registers: hand its part of the accumulator back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty(a));
                     const int v = vw;
                     const int n = min(16, ve - v);
                     if (!kFinal) {
@@ -768,10 +781,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         for (int i = 0; i < 16; ++i) z[i] = bf16_at(nu_lo, nu_hi, i) + __uint_as_float(acc[i]);
                         const uint4 ct_lo = nt_lo, ct_hi = nt_hi;
                         {
-                            const int tn = t + h, hn = h ^ 1;  // the next sub-slice
-                            const int vn = (tn < ntiles) ? sub_col(tn, hn) : ve;
+                            const int sn = si + kEpiPerQuad;  // this warp's next sub-slice
+                            const int vn = (sn < nsub) ? sub_col(sn) : ve;
                             const int nn = min(16, ve - vn);
-                            if (active && tn < ntiles && nn > 0) {
+                            if (active && sn < nsub && nn > 0) {
                                 load16_bf16(trow + vn, nn, nt_lo, nt_hi);
                                 if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
                             }
@@ -892,21 +905,21 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             // merge the four column slices of each row
             if (!kFinal) {
                 RowState *ms = reinterpret_cast<RowState *>(smem + kOffMerge);
-                ms[row * 4 + slice] = st;
+                ms[row * kEpiPerQuad + slice] = st;
             } else {
                 ResidualState *ms = reinterpret_cast<ResidualState *>(smem + kOffMerge);
-                ms[row * 4 + slice] = rs;
+                ms[row * kEpiPerQuad + slice] = rs;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
             if (slice == 0 && b < p.B) {
                 if (!kFinal) {
                     const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
-                    for (int s2 = 1; s2 < 4; ++s2) row_state_merge(st, ms[row * 4 + s2]);
+                    for (int s2 = 1; s2 < kEpiPerQuad; ++s2) row_state_merge(st, ms[row * kEpiPerQuad + s2]);
                     p.part[((size_t)jj * p.B + b) * p.nseg + seg] = st;
                     if (st.idx != INT32_MAX) atomicMax(best, best_encode(st.key, st.idx));
                 } else if (active) {
                     const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);
-                    for (int s2 = 1; s2 < 4; ++s2) residual_merge(rs, ms[row * 4 + s2]);
+                    for (int s2 = 1; s2 < kEpiPerQuad; ++s2) residual_merge(rs, ms[row * kEpiPerQuad + s2]);
                     p.rpart[(size_t)b * p.nseg + seg] = rs;
                 }
             }
