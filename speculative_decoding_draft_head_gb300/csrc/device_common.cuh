@@ -57,16 +57,39 @@ struct PhiloxRoundKeys {
     uint32_t k1[10];
 };
 
-// Philox4x32-10 for counter (x0, pos, rid, stream) with the parts of round 1
-// that do not depend on x0 precomputed per request:
-//   y0c = hi(M1 rid) ^ pos ^ k0[0],  y1c = lo(M1 rid),  sk = stream ^ k1[0].
-// Same words as philox4x32_10(make_uint4(x0, pos, rid, stream), k0, k1).
-__device__ __forceinline__ uint4 philox_folded(uint32_t x0, uint32_t y0c, uint32_t y1c, uint32_t sk,
-                                               const PhiloxRoundKeys &K) {
-    const uint64_t p = (uint64_t)kPhiloxM0 * x0;
-    uint32_t c0 = y0c, c1 = y1c, c2 = (uint32_t)(p >> 32) ^ sk, c3 = (uint32_t)p;
+// Philox4x32-10 for counter (x0, pos, rid, stream) with the parts that do not
+// depend on x0 precomputed per request and position (PhiloxRow).  After round 1
+// the words are (y0c, y1c, hi(M0 x0) ^ sk, lo(M0 x0)) with
+//   y0c = hi(M1 rid) ^ pos ^ k0[0],  y1c = lo(M1 rid),  sk = stream ^ k1[0];
+// round 2 multiplies the constant y0c, so hi(M0 y0c) ^ k1[1] and lo(M0 y0c)
+// are precomputed as well.  Same words as
+// philox4x32_10(make_uint4(x0, pos, rid, stream), k0, k1).
+struct PhiloxRow {
+    uint32_t sk;   // stream ^ k1[0]
+    uint32_t y1k;  // y1c ^ k0[1]
+    uint32_t y2h;  // hi(M0 y0c) ^ k1[1]
+    uint32_t y2l;  // lo(M0 y0c)
+};
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t rid, uint32_t pos, uint32_t stream, const PhiloxRoundKeys &K) {
+    const uint32_t y0c = __umulhi(kPhiloxM1, rid) ^ pos ^ K.k0[0];
+    const uint32_t y1c = kPhiloxM1 * rid;
+    const uint64_t p2 = (uint64_t)kPhiloxM0 * y0c;
+    PhiloxRow R;
+    R.sk = stream ^ K.k1[0];
+    R.y1k = y1c ^ K.k0[1];
+    R.y2h = (uint32_t)(p2 >> 32) ^ K.k1[1];
+    R.y2l = (uint32_t)p2;
+    return R;
+}
+__device__ __forceinline__ uint4 philox_folded(uint32_t x0, const PhiloxRow &R, const PhiloxRoundKeys &K) {
+    // round 1
+    const uint64_t p1 = (uint64_t)kPhiloxM0 * x0;
+    const uint32_t c2r1 = (uint32_t)(p1 >> 32) ^ R.sk, c3r1 = (uint32_t)p1;
+    // round 2: only the M1 product depends on x0
+    const uint64_t pb2 = (uint64_t)kPhiloxM1 * c2r1;
+    uint32_t c0 = (uint32_t)(pb2 >> 32) ^ R.y1k, c1 = (uint32_t)pb2, c2 = R.y2h ^ c3r1, c3 = R.y2l;
 #pragma unroll
-    for (int r = 1; r < 10; ++r) {
+    for (int r = 2; r < 10; ++r) {
         const uint64_t pa = (uint64_t)kPhiloxM0 * c0;
         const uint64_t pb = (uint64_t)kPhiloxM1 * c2;
         const uint32_t n0 = (uint32_t)(pb >> 32) ^ c1 ^ K.k0[r];

@@ -597,8 +597,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const int kind = kFinal ? (code >= 0 ? (code >> 16) : 0) : 0;
         const int fpos = kFinal ? (code & 0xFFFF) : 0;
         const uint32_t stream = kFinal ? (kind == 1 ? kStreamResidual : kStreamBonus) : kStreamDraft;
-        const uint32_t y1c = kPhiloxM1 * rid;
-        const uint32_t sk = stream ^ p.keys.k1[0];
+
         bool ok = true;
         for (int pi = 0; pi < npos && ok; ++pi) {
             const int jj = kFinal ? 0 : p.j + pi;
@@ -641,8 +640,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             }
             const bool active = kFinal ? (kind != 0) : (prev >= 0);
             const uint32_t pos = kFinal ? (uint32_t)fpos : (uint32_t)jj;
-            // round-1 constant of Philox for this request and position
-            const uint32_t y0c = __umulhi(kPhiloxM1, rid) ^ pos ^ p.keys.k0[0];
+            // the parts of Philox fixed by this request and position
+            const PhiloxRow prow = philox_row(rid, pos, stream, p.keys);
 
             RowState st = row_state_init();
             float Q = kQMax;
@@ -704,7 +703,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         if (vw < ve) {
 #pragma unroll
                             for (int g = 0; g < 4; ++g)
-                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, y0c, y1c, sk, p.keys);
+                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, prow, p.keys);
                         }
                         if (!uniform_wait(tfull(a), aph, abort)) {
                             if (lane == 0) {
@@ -723,7 +722,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         if (vw < ve) {
 #pragma unroll
                             for (int g = 0; g < 4; ++g)
-                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, y0c, y1c, sk, p.keys);
+                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, prow, p.keys);
                         }
                     }
                     tmem_ld_wait16(acc);
