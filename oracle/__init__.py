@@ -93,6 +93,11 @@ def lib():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _f64p, _f64p, _i32p, _f64p, _i32p, _f64p, _f64p]
             L.or_schedule.restype = ctypes.c_int
+            L.or_draft_sample_rnn.argtypes = [
+                _f64p, _f64p, _f64p, _f64p, _i32p, _f64p, nu,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
+                _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, nf]
+            L.or_draft_sample_rnn.restype = ctypes.c_int
             L.or_schedule_policy.argtypes = [
                 _f64p, _f64p, _f64p, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
@@ -189,6 +194,35 @@ def draft_sample(U, E_in, W_out, anchor, temp, rid=None, seed=0, want_z=False):
                                out["tokens"], out["lse"], out["logq"], out["gap"], out["top"], z)
     if rc != 0:
         raise ValueError("or_draft_sample failed: %d" % rc)
+    if want_z:
+        out["z"] = z
+    return out
+
+
+def draft_sample_rnn(U, E_in, W_h, W_out, anchor, temp, rid=None, seed=0, want_z=False):
+    """Draft a block with the recurrent head (see ``or_draft_sample_rnn``).
+
+    W_h [r,r] (row n: weights of state unit n).  Returns the keys of
+    ``draft_sample`` plus h [B,G,r] (the bf16 states) and h_margin [B,G]."""
+    U = _f64(U)
+    E_in = _f64(E_in)
+    W_h = _f64(W_h)
+    W_out = _f64(W_out)
+    B, G, V = U.shape
+    r = E_in.shape[1]
+    assert E_in.shape == (V, r) and W_out.shape == (V, r) and W_h.shape == (r, r)
+    anchor = _i32(anchor)
+    temp = _f64(temp)
+    rid = _u32(rid)
+    out = dict(tokens=np.zeros((B, G), np.int32), lse=np.zeros((B, G)),
+               logq=np.zeros((B, G)), gap=np.zeros((B, G)), top=np.zeros((B, G)),
+               h=np.zeros((B, G, r)), h_margin=np.zeros((B, G)))
+    z = np.zeros((B, G, V)) if want_z else None
+    rc = lib().or_draft_sample_rnn(U, E_in, W_h, W_out, anchor, temp, rid, B, G, V, r, seed,
+                                   out["tokens"], out["lse"], out["logq"], out["gap"], out["top"],
+                                   out["h"], out["h_margin"], z)
+    if rc != 0:
+        raise ValueError("or_draft_sample_rnn failed: %d" % rc)
     if want_z:
         out["z"] = z
     return out

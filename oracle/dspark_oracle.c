@@ -224,6 +224,93 @@ int or_draft_sample(const double *U, const double *E_in, const double *W_out,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The recurrent (RNN) head, the second sequential head the pages set beside  */
+/* the Markov head ([DSP-IT] "Un po' di autoregressione basta"; the aitalk   */
+/* overview "Un drafter...").  The pages do not give the cell; reading R12:   */
+/*   h_{-1} = 0, x_{-1} = anchor,                                             */
+/*   h_j = bf16( tanh( E_in[x_{j-1}] + W_h h_{j-1} ) )   (an Elman cell whose */
+/*         input term is the embedding of the previous token; the state is   */
+/*         kept in bf16, the storage type of the head's weights),           */
+/*   bias_j[v] = sum_k h_j[k] W_out[v][k],  z = fp32(U + bias).              */
+/* W_h is [r][r] with row n the weights of output unit n.  Everything else   */
+/* (temperature, Gumbel-max, streams) is as in or_draft_sample.             */
+/* h_out [B][G][r] receives the states; h_margin [B][G] the smallest relative */
+/* distance of a pre-rounding state value to a bf16 rounding boundary (a      */
+/* value on a boundary may round either way under another summation order). */
+/* ------------------------------------------------------------------------ */
+static double bf16_rne(double x, double *margin)
+{
+    if (x == 0.0 || !isfinite(x)) { if (margin) *margin = INFINITY; return x; }
+    int e;
+    double m = frexp(x, &e);          /* x = m 2^e, 0.5 <= |m| < 1 */
+    double sc = ldexp(m, 8);          /* 8 significant bits */
+    double fl = floor(sc);
+    if (margin) *margin = fabs((sc - fl) - 0.5) / fabs(sc);
+    double rn = nearbyint(sc);        /* round half to even (default mode) */
+    return ldexp(rn, e - 8);
+}
+
+int or_draft_sample_rnn(const double *U, const double *E_in, const double *W_h, const double *W_out,
+                        const int32_t *anchor, const double *temp, const uint32_t *rid,
+                        int B, int G, int V, int r, uint64_t seed,
+                        int32_t *tokens, double *lse, double *logq, double *gap, double *top,
+                        double *h_out, double *h_margin, double *z_out)
+{
+    double *z = (double *)malloc(sizeof(double) * (size_t)V);
+    double *s = (double *)malloc(sizeof(double) * (size_t)V);
+    double *h = (double *)malloc(sizeof(double) * (size_t)r);
+    double *hn = (double *)malloc(sizeof(double) * (size_t)r);
+    if (!z || !s || !h || !hn) { free(z); free(s); free(h); free(hn); return -2; }
+    for (int b = 0; b < B; ++b) {
+        uint32_t id = rid ? rid[b] : (uint32_t)b;
+        double T = temp[b];
+        int prev = anchor[b];
+        if (prev < 0 || prev >= V) { free(z); free(s); free(h); free(hn); return -1; }
+        for (int k = 0; k < r; ++k) h[k] = 0.0;
+        for (int j = 0; j < G; ++j) {
+            size_t o = (size_t)b * (size_t)G + (size_t)j;
+            /* the state update */
+            double mm = INFINITY;
+            for (int n = 0; n < r; ++n) {
+                double a = E_in[(size_t)prev * (size_t)r + n];
+                for (int k = 0; k < r; ++k) a += W_h[(size_t)n * (size_t)r + k] * h[k];
+                double mg;
+                hn[n] = bf16_rne(tanh(a), &mg);
+                if (mg < mm) mm = mg;
+            }
+            memcpy(h, hn, sizeof(double) * (size_t)r);
+            if (h_out) memcpy(h_out + o * (size_t)r, h, sizeof(double) * (size_t)r);
+            if (h_margin) h_margin[o] = mm;
+            /* the bias and the logits of this position */
+            const double *U_row = U + o * (size_t)V;
+            for (int v = 0; v < V; ++v) {
+                const double *w = W_out + (size_t)v * (size_t)r;
+                double bias = 0.0;
+                for (int k = 0; k < r; ++k) bias += h[k] * w[k];
+                z[v] = (double)(float)(U_row[v] + bias);
+            }
+            if (z_out) memcpy(z_out + o * (size_t)V, z, sizeof(double) * (size_t)V);
+            int x;
+            if (T > 0.0) {
+                for (int v = 0; v < V; ++v) s[v] = z[v] / T;
+                double l = row_logsumexp(s, V);
+                x = gumbel_max(s, NULL, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o]);
+                lse[o] = l;
+                logq[o] = s[x] - l;
+            } else {
+                x = row_argmax(z, V, &gap[o], &top[o]);
+                lse[o] = z[x];
+                logq[o] = 0.0;
+            }
+            tokens[o] = x;
+            prev = x;
+        }
+    }
+    free(z); free(s); free(h); free(hn);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Confidence calibration and prefix scheduler ([DSP-IT] "Verificare meglio, */
 /* non di piu'": c_k, a_j = prod_{i<=j} c_i, Theta = tau * SPS(B), greedy     */
 /* admission in a-order with the early stop), readings R7 and R8.             */
