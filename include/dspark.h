@@ -74,7 +74,8 @@ typedef enum dspark_dtype {
 enum {
     DSPARK_WS_DRAFT = 0,
     DSPARK_WS_SCHEDULE = 1,
-    DSPARK_WS_VERIFY = 2
+    DSPARK_WS_VERIFY = 2,
+    DSPARK_WS_DRAFT_RNN = 3
 };
 
 /* bits of the device flag word */
@@ -133,6 +134,36 @@ DSPARK_API dspark_status dspark_draft_sample(
     int B, int G, int V, int r, dspark_dtype dtype, uint64_t seed,
     int32_t *draft_tokens, float *draft_lse, float *draft_logq, float *draft_logits,
     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Draft sampling with the recurrent (RNN) head.
+ *
+ * "DSpark, la bozza che sa quando fermarsi" (paithon.it), section "Un po' di
+ * autoregressione basta", names a recurrent head beside the Markov head: the
+ * bias of position j comes from a state carried along the block instead of
+ * from x_{j-1} alone.  The pages give no cell; this one is an Elman cell
+ * driven by the previous token's embedding, its state kept in bf16:
+ *   h_{-1} = 0,  h_j[n] = bf16(tanh(e_in[prev][n] + sum_k w_h[n][k] h_{j-1}[k]))
+ *   z[v] = base_logits[b][j][v] + sum_k h_j[k] * w_out[v][k]          (fp32)
+ * with prev = anchor[b] (j = 0) or draft_tokens[b][j-1]; everything after z
+ * (temperature, Gumbel-max draw, lse, logq, greedy rows, streams) is exactly
+ * as in dspark_draft_sample.
+ *
+ * Arguments as in dspark_draft_sample, plus w_h [r][r] bf16 (row n holds the
+ * weights of state unit n) and h_states: [B][G][r] bf16 output of the states
+ * h_j, or NULL.  The state sum is compensated and tanh is taken in fp64, so
+ * h_j is the exactly rounded value except within ~1e-13 of a bf16 rounding
+ * boundary.  dtype must be DSPARK_BF16 (else DSPARK_ERR_UNSUPPORTED).  The
+ * workspace is DSPARK_WS_DRAFT_RNN.  Verify such a block with dspark_verify
+ * given the draft_logits this call stored (the draft distribution of the
+ * rejected position is then read, not recomputed).
+ */
+DSPARK_API dspark_status dspark_draft_sample_rnn(
+    const void *base_logits, const void *e_in, const void *w_h, const void *w_out,
+    const int32_t *anchor, const float *temperature, const uint32_t *request_id,
+    int B, int G, int V, int r, dspark_dtype dtype, uint64_t seed,
+    int32_t *draft_tokens, float *draft_lse, float *draft_logq, float *draft_logits,
+    void *h_states, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Confidence calibration and the load-aware prefix scheduler.

@@ -338,6 +338,22 @@ def draft_sample_parallel(U, E_in, W_out, anchor, temp, rid=None, seed=0, thread
     return _merge(res)
 
 
+def draft_sample_rnn_parallel(U, E_in, W_h, W_out, anchor, temp, rid=None, seed=0, threads=None,
+                              want_z=False):
+    """``draft_sample_rnn`` over request chunks on ``threads`` host threads."""
+    U = _f64(U); E_in = _f64(E_in); W_h = _f64(W_h); W_out = _f64(W_out)
+    anchor = _i32(anchor); temp = _f64(temp)
+    B = U.shape[0]
+    rid = _rid_or_default(rid, B)
+    threads = threads or os.cpu_count() or 1
+    parts = _chunks(B, threads)
+    with ThreadPoolExecutor(len(parts)) as ex:
+        res = list(ex.map(lambda ab: draft_sample_rnn(U[ab[0]:ab[1]], E_in, W_h, W_out, anchor[ab[0]:ab[1]],
+                                                      temp[ab[0]:ab[1]], rid[ab[0]:ab[1]], seed,
+                                                      want_z=want_z), parts))
+    return _merge(res)
+
+
 def verify_parallel(target, U, E_in, W_out, anchor, draft_tokens, verify_len, temp, rid=None,
                     seed=0, threads=None):
     """``verify`` over request chunks on ``threads`` host threads."""

@@ -19,7 +19,7 @@ from . import build as _build
 DSPARK_OK = 0
 DSPARK_BF16 = 0
 DSPARK_F32 = 1
-WS_DRAFT, WS_SCHEDULE, WS_VERIFY = 0, 1, 2
+WS_DRAFT, WS_SCHEDULE, WS_VERIFY, WS_DRAFT_RNN = 0, 1, 2, 3
 
 FLAG_BAD_TOKEN = 1
 FLAG_BAD_TEMPERATURE = 2
@@ -28,7 +28,7 @@ FLAG_BAD_POS_TEMP = 8
 
 EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
            "dspark_schedule_prefix", "dspark_schedule_policy", "dspark_verify", "dspark_read_device_flags",
-           "dspark_verify_noalloc")
+           "dspark_verify_noalloc", "dspark_draft_sample_rnn")
 
 _lib = None
 _lock = threading.Lock()
@@ -66,6 +66,9 @@ def load(build_if_missing: bool = True):
         L.dspark_draft_sample.restype = ctypes.c_int
         L.dspark_draft_sample.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, u64,
                                           vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_draft_sample_rnn.restype = ctypes.c_int
+        L.dspark_draft_sample_rnn.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, u64,
+                                              vp, vp, vp, vp, vp, vp, sz, vp]
         L.dspark_schedule_prefix.restype = ctypes.c_int
         L.dspark_schedule_prefix.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                              vp, sz, vp]
@@ -187,6 +190,40 @@ def draft_sample(base, e_in, w_out, anchor, temperature, request_id=None, seed=0
         B, G, V, r, _dtype_code(base), int(seed) & 0xFFFFFFFFFFFFFFFF,
         _ptr(out["tokens"]), _ptr(out["lse"]), _ptr(out["logq"]), _ptr(out.get("logits")),
         _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def draft_sample_rnn(base, e_in, w_h, w_out, anchor, temperature, request_id=None, seed=0, *,
+                     out=None, store_logits=False, store_states=False, workspace=None, stream=None):
+    """Draft one block per request with the recurrent head (bf16 weights).
+
+    Returns dict(tokens, lse, logq[, logits][, h]); ``h`` [B,G,r] bf16 are the
+    states h_j.  Verify the block with :func:`verify` and ``draft_logits``."""
+    lib = load()
+    B, G, V = base.shape
+    r = e_in.shape[1]
+    dev = base.device
+    _need(base, "base", dtype=torch.bfloat16, shape=(B, G, V), device=dev)
+    _need(e_in, "e_in", dtype=torch.bfloat16, shape=(V, r), device=dev)
+    _need(w_h, "w_h", dtype=torch.bfloat16, shape=(r, r), device=dev)
+    _need(w_out, "w_out", dtype=torch.bfloat16, shape=(V, r), device=dev)
+    _need(anchor, "anchor", dtype=torch.int32, shape=(B,), device=dev)
+    _need(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
+    rid = _rid(request_id, B, dev)
+    if out is None:
+        out = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
+                   lse=torch.empty((B, G), dtype=torch.float32, device=dev),
+                   logq=torch.empty((B, G), dtype=torch.float32, device=dev))
+        if store_logits:
+            out["logits"] = torch.empty((B, G, V), dtype=torch.float32, device=dev)
+        if store_states:
+            out["h"] = torch.empty((B, G, r), dtype=torch.bfloat16, device=dev)
+    ws = workspace if workspace is not None else _default_ws.get(WS_DRAFT_RNN, B, G, V, r, dev)
+    _check(lib.dspark_draft_sample_rnn(
+        _ptr(base), _ptr(e_in), _ptr(w_h), _ptr(w_out), _ptr(anchor), _ptr(temperature), _ptr(rid),
+        B, G, V, r, DSPARK_BF16, int(seed) & 0xFFFFFFFFFFFFFFFF,
+        _ptr(out["tokens"]), _ptr(out["lse"]), _ptr(out["logq"]), _ptr(out.get("logits")),
+        _ptr(out.get("h")), _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

@@ -68,6 +68,7 @@ size_t dspark_workspace_bytes(int which, int B, int G, int V, int r) {
             const size_t b = plan_draft(B, G, V, r, DSPARK_F32).ws_bytes;
             return a > b ? a : b;
         }
+        case DSPARK_WS_DRAFT_RNN: return plan_draft_rnn(B, G, V, r).ws_bytes;
         case DSPARK_WS_SCHEDULE: return kFlagBytes;
         case DSPARK_WS_VERIFY: {
             const size_t a = plan_verify(B, G, V, r, DSPARK_BF16).ws_bytes;
@@ -115,6 +116,48 @@ dspark_status dspark_draft_sample(const void *base_logits, const void *e_in, con
         e = launch_draft_finalize(a, plan, j, 1, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
     }
+    return DSPARK_OK;
+}
+
+dspark_status dspark_draft_sample_rnn(const void *base_logits, const void *e_in, const void *w_h,
+                                      const void *w_out, const int32_t *anchor, const float *temperature,
+                                      const uint32_t *request_id, int B, int G, int V, int r,
+                                      dspark_dtype dtype, uint64_t seed, int32_t *draft_tokens,
+                                      float *draft_lse, float *draft_logq, float *draft_logits,
+                                      void *h_states, void *workspace, size_t workspace_bytes, void *stream) {
+    dspark_status st = check_common(B, G, V, r, dtype);
+    if (st != DSPARK_OK) return st;
+    if (dtype != DSPARK_BF16) return fail(DSPARK_ERR_UNSUPPORTED, "the recurrent head runs on bf16 weights only");
+    if (!base_logits || !e_in || !w_h || !w_out || !anchor || !temperature || !draft_tokens || !draft_lse ||
+        !draft_logq)
+        return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned(base_logits, 16) || !aligned(e_in, 16) || !aligned(w_h, 16) || !aligned(w_out, 16) ||
+        (draft_logits && !aligned(draft_logits, 16)) || (h_states && !aligned(h_states, 2)))
+        return fail(DSPARK_ERR_INVALID_ARG, "logits and weights must be 16-byte aligned");
+    const RnnPlan plan = plan_draft_rnn(B, G, V, r);
+    if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    e = cudaMemsetAsync(ws + plan.draft.best_offset, 0, plan.draft.clear_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the row-wide best words");
+    DraftArgs a{base_logits, e_in, w_out, anchor, temperature, request_id, B, G, V, r, dtype, seed,
+                draft_tokens, draft_lse, draft_logq, draft_logits, ws};
+    __nv_bfloat16 *h_ws = reinterpret_cast<__nv_bfloat16 *>(ws + plan.h_offset);
+    RnnStateArgs ra{static_cast<const __nv_bfloat16 *>(e_in), static_cast<const __nv_bfloat16 *>(w_h), anchor,
+                    reinterpret_cast<const unsigned long long *>(ws + plan.draft.best_offset), h_ws,
+                    static_cast<__nv_bfloat16 *>(h_states), B, G, V, r};
+    // position j: the state from x_{j-1} and h_{j-1}, then the draw with h_j
+    // as the tensor-core A operand; the partials are merged once at the end
+    for (int j = 0; j < G; ++j) {
+        e = launch_rnn_state(ra, j, s);
+        if (e != cudaSuccess) return cuda_fail(e, "recurrent state launch");
+        e = launch_draft_tensor_rows(a, plan.draft, j, h_ws + (size_t)j * B * r, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft sample launch");
+    }
+    e = launch_draft_finalize(a, plan.draft, 0, G, s);
+    if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
     return DSPARK_OK;
 }
 

@@ -281,6 +281,20 @@ __device__ __forceinline__ uint32_t load_relaxed(const uint32_t *p) {
     return v;
 }
 
+// Row-wide best draw of a block position as one 64-bit word: the key's
+// order-preserving encoding above the complemented token id, so that
+// atomicMax keeps the largest key and, on an exact tie, the lowest id (the
+// merge rule of the partial states).  0 means "none".
+__device__ __forceinline__ unsigned long long best_encode(float key, int idx) {
+    return ((unsigned long long)key_to_ordered(key) << 32) | (unsigned long long)(~(uint32_t)idx);
+}
+__device__ __forceinline__ int best_token(unsigned long long w) { return w ? (int)~(uint32_t)w : -1; }
+__device__ __forceinline__ unsigned long long load_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Residual draw state: best key over {p > q} and, for the degenerate case
 // where no entry has p > q, the best key of a draw from p.
 struct ResidualState {

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/dspark.h"
@@ -32,6 +33,14 @@ struct DraftPlan {
     size_t ws_bytes;
 };
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt);
+// the recurrent head's workspace: a bf16 draft plan plus the [G][B][r] states
+// at h_offset
+struct RnnPlan {
+    DraftPlan draft;
+    size_t h_offset;
+    size_t ws_bytes;
+};
+RnnPlan plan_draft_rnn(int B, int G, int V, int r);
 
 struct DraftArgs {
     const void *base;
@@ -54,6 +63,22 @@ cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cud
 cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, int npos, cudaStream_t s);
 // every block position (one cooperative launch, else one launch per position)
 cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &p, cudaStream_t s);
+// recurrent head: h_j = bf16(tanh(E_in[x_{j-1}] + W_h h_{j-1})) into h_ws + j B r
+struct RnnStateArgs {
+    const __nv_bfloat16 *e_in;        // [V][r]
+    const __nv_bfloat16 *w_h;         // [r][r], row n = weights of state unit n
+    const int32_t *anchor;            // [B]
+    const unsigned long long *best;   // [G][B] row-wide best words of the draft launches
+    __nv_bfloat16 *h_ws;              // [G][B][r] states
+    __nv_bfloat16 *h_out;             // optional [B][G][r] copy of the states
+    int B, G, V, r;
+};
+int rnn_rows_per_block(int B);
+cudaError_t launch_rnn_state(const RnnStateArgs &a, int j, cudaStream_t s);
+// block position j alone, with the A operand of request b read from a_rows + b r
+// (bf16) instead of E_in[x_{j-1}]
+cudaError_t launch_draft_tensor_rows(const DraftArgs &a, const DraftPlan &p, int j, const void *a_rows,
+                                     cudaStream_t s);
 
 // tensor-core kernel geometry (bf16): 128-request row blocks x vocabulary segments
 int tc_row_blocks(int B);

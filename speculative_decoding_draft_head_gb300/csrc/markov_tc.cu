@@ -112,6 +112,7 @@ constexpr float kMargin = 1.0001f;
 
 struct TcParams {
     const __nv_bfloat16 *e_in;
+    const __nv_bfloat16 *a_rows;  // draft, one position: A row of request b at a_rows + b r (else E_in[x_{j-1}])
     const __nv_bfloat16 *base;
     const __nv_bfloat16 *target;
     const int32_t *anchor;
@@ -135,19 +136,6 @@ struct TcParams {
     float *z_out;
 };
 
-// Row-wide best draw of a block position as one 64-bit word: the key's
-// order-preserving encoding above the complemented token id, so that
-// atomicMax keeps the largest key and, on an exact tie, the lowest id (the
-// merge rule of the partial states).  0 means "none".
-__device__ __forceinline__ unsigned long long best_encode(float key, int idx) {
-    return ((unsigned long long)key_to_ordered(key) << 32) | (unsigned long long)(~(uint32_t)idx);
-}
-__device__ __forceinline__ int best_token(unsigned long long w) { return w ? (int)~(uint32_t)w : -1; }
-__device__ __forceinline__ unsigned long long load_relaxed_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
 __device__ __forceinline__ unsigned int load_acquire_u32(const unsigned int *p) {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -603,8 +591,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             const int jj = kFinal ? 0 : p.j + pi;
             // ---- A operand of this position: TMEM lane = request row, K in
             // pairs per 32-bit column; warp w writes K elements 64 (w / 4) .. + 63
-            // of the rows of its quadrant.  Every UMMA of the previous position
-            // is done: this warp has seen the tfull of its last tile.
+            // of the rows of its quadrant: E_in[x_{j-1}] (Markov head), or the
+            // request's own row of p.a_rows (the recurrent head's state h_j).
+            // Every UMMA of the previous position is done: this warp has seen
+            // the tfull of its last tile.
             int prev = -1;
             if (kFinal) {
                 prev = row_prev[row];
@@ -618,6 +608,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             }
             {
                 const int k0 = slice * 64;
+                const __nv_bfloat16 *a_src =
+                    (!kFinal && p.a_rows) ? p.a_rows + (size_t)b * p.r : p.e_in + (size_t)max(prev, 0) * p.r;
                 if (k0 < p.r) {
                     const int nk = min(64, p.r - k0);  // a multiple of 16
                     uint32_t av[32];
@@ -625,7 +617,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     for (int i = 0; i < 8; ++i) {
                         uint4 val = make_uint4(0u, 0u, 0u, 0u);
                         if (prev >= 0 && 8 * i < nk)
-                            val = __ldg(reinterpret_cast<const uint4 *>(p.e_in + (size_t)prev * p.r + k0) + i);
+                            val = __ldg(reinterpret_cast<const uint4 *>(a_src + k0) + i);
                         av[4 * i] = val.x;
                         av[4 * i + 1] = val.y;
                         av[4 * i + 2] = val.z;
@@ -1052,13 +1044,14 @@ int coop_capacity() {
 
 }  // namespace
 
-cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStream_t s) {
-    CUtensorMap mw, mu;
-    cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
+namespace {
+
+cudaError_t draft_setup(const DraftArgs &a, const DraftPlan &pl, CUtensorMap *mw, CUtensorMap *mu, TcParams &p) {
+    cudaError_t e = make_w_map(mw, a.w_out, a.V, a.r);
     if (e != cudaSuccess) return e;
-    if ((e = make_u_map(&mu, a.base, a.B, a.G, a.V, 64)) != cudaSuccess) return e;
+    if ((e = make_u_map(mu, a.base, a.B, a.G, a.V, 64)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
-    TcParams p{};
+    p = TcParams{};
     p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
     p.base = static_cast<const __nv_bfloat16 *>(a.base);
     p.anchor = a.anchor;
@@ -1076,6 +1069,16 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStr
     p.grid_bar = reinterpret_cast<unsigned int *>(a.ws + pl.bar_offset);
     p.flags = reinterpret_cast<uint32_t *>(a.ws);
     p.z_out = a.z_out;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStream_t s) {
+    CUtensorMap mw, mu;
+    TcParams p;
+    cudaError_t e = draft_setup(a, pl, &mw, &mu, p);
+    if (e != cudaSuccess) return e;
     const dim3 grid(pl.nsplit, pl.row_blocks);
     // all positions in one cooperative launch when every CTA fits at once
     if (a.G > 1 && (long)grid.x * grid.y <= (long)coop_capacity()) {
@@ -1094,6 +1097,19 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStr
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_draft_tensor_rows(const DraftArgs &a, const DraftPlan &pl, int j, const void *a_rows,
+                                     cudaStream_t s) {
+    CUtensorMap mw, mu;
+    TcParams p;
+    cudaError_t e = draft_setup(a, pl, &mw, &mu, p);
+    if (e != cudaSuccess) return e;
+    p.a_rows = static_cast<const __nv_bfloat16 *>(a_rows);
+    p.j = j;
+    p.j_end = j + 1;
+    markov_tc_kernel<false><<<dim3(pl.nsplit, pl.row_blocks), kThreads, kSmemBytes, s>>>(mw, mu, p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {

@@ -11,7 +11,11 @@ distributions follow the five workloads the library is measured on:
   highconc   B=1024 G=4   V=129280  r=256  bf16  T~U[0.3,1.2], t=U+N(0,sigma_b^2),
                                                   sigma_b~U[0.2,2], scheduler on
 
-E_in and W_out (both V x r; W_out row v scores token v) are N(0, 0.02^2).  Confidence logits are
+E_in and W_out (both V x r; W_out row v scores token v) are N(0, 0.02^2).  The
+recurrent head (make_rnn_head) draws its own, larger weights so that its state
+moves the logits: E_in ~ N(0, 0.5^2), W_h ~ N(0, (0.9 / sqrt(r))^2) (a
+contracting recurrence), W_out ~ N(0, 0.05^2), all rounded to bf16; the bias
+then has a spread of about 0.3 nats against the base logits' 3.  Confidence logits are
 N(1, 1); the per-position calibration temperatures are evenly spaced in
 [1, 2]; the batch-token throughput table is SPS(n) = 1 / (1 + n / 512).
 """
@@ -114,3 +118,16 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", request_id_base: int =
     return dict(base=base, target=target, e_in=e_in, w_out=w_out, anchor=anchor,
                 temperature=temperature, request_id=request_id, conf_logits=conf_logits,
                 pos_temp=pos_temp, sps=sps)
+
+
+def make_rnn_head(w: Workload, seed: int = 0, device="cpu") -> dict:
+    """Weights of a recurrent draft head for workload ``w`` (bf16):
+    e_in [V,r], w_h [r,r] (row n: weights of state unit n), w_out [V,r]."""
+    V, r = w.V, w.r
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000033 + 7 + zlib.crc32(w.name.encode()) % 991)
+    f32 = torch.float32
+    e_in = (torch.randn((V, r), generator=g, device=device, dtype=f32) * 0.5).to(torch.bfloat16)
+    w_h = (torch.randn((r, r), generator=g, device=device, dtype=f32) * (0.9 / r ** 0.5)).to(torch.bfloat16)
+    w_out = (torch.randn((V, r), generator=g, device=device, dtype=f32) * 0.05).to(torch.bfloat16)
+    return dict(e_in=e_in.contiguous(), w_h=w_h.contiguous(), w_out=w_out.contiguous())
