@@ -304,6 +304,28 @@ def run_ours(args, w):
     total_positions = _sum_over_ranks(positions, world)
     value = total_positions / (ms_max / 1000.0)
 
+    # the recurrent head's draft call on the same base logits (scope row f3;
+    # outside the timed step, which is the Markov head's round)
+    rnn_ms = None
+    if w.dtype == "bf16":
+        from speculative_decoding_draft_head_gb300.synth import make_rnn_head
+        head = make_rnn_head(w, args.seed + rank, device=dev)
+        ws_r = binding.default_workspace(binding.WS_DRAFT_RNN, B, G, V, r, dev)
+        r_out = {k: torch.empty_like(t) for k, t in d_out.items()}
+        e_r0, e_r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        samples = []
+        for i in range(3 + max(3, min(args.steps, 20))):
+            e_r0.record(stream)
+            binding.draft_sample_rnn(inp["base"], head["e_in"], head["w_h"], head["w_out"], inp["anchor"],
+                                     inp["temperature"], inp["request_id"], args.seed, out=r_out,
+                                     workspace=ws_r, stream=stream)
+            e_r1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                samples.append(e_r0.elapsed_time(e_r1))
+        rnn_ms = statistics.median(samples)
+        del head
+
     # end to end: per-round inputs from pinned host memory, emitted tokens back
     per_round = ("base", "target", "anchor", "temperature", "request_id", "conf_logits")
     host = {k: inp[k].cpu().pin_memory() for k in per_round}
@@ -394,6 +416,10 @@ def run_ours(args, w):
                               if dominant == "draft" else "verify call (%d launches)" % launches_per_call),
                       peak_source=peaks["source"]),
         calls_ms=dict(draft=d_ms, schedule=s_ms, verify=v_ms),
+        rnn_head=(None if rnn_ms is None else
+                  dict(draft_ms=rnn_ms, launches=2 * G + 1,
+                       note="recurrent-head draft call (state update + tensor-core draw per position, "
+                            "then finalize), not part of the timed round")),
         bias_gemm=dict(flops_per_round=bias_flops,
                        tflops_over_draft_time=bias_flops / (d_ms / 1000.0) / 1e12,
                        peak_tflops=peaks["bf16_tflops_sustained"]),

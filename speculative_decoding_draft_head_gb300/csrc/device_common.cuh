@@ -281,6 +281,15 @@ __device__ __forceinline__ uint32_t load_relaxed(const uint32_t *p) {
     return v;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start its
+// independent prologue (launch_dependents), and wait until every earlier
+// kernel of the stream has completed with its writes visible (wait).  Both
+// are no-ops when the launch carries no programmatic serialization attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Row-wide best draw of a block position as one 64-bit word: the key's
 // order-preserving encoding above the complemented token id, so that
 // atomicMax keeps the largest key and, on an exact tie, the lowest id (the

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -15,6 +16,27 @@ constexpr size_t kFlagBytes = 256;      // flag word region at the head of every
 constexpr int kMaxG = 64;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// A set-up call made once per device, such as raising a kernel's dynamic
+// shared-memory limit (a property of the function on each device).
+struct PerDeviceOnce {
+    std::mutex mu;
+    bool done[64] = {};
+    cudaError_t result[64] = {};
+    template <typename Fn>
+    cudaError_t run(Fn &&fn) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            result[dev] = fn();
+            done[dev] = true;
+        }
+        return result[dev];
+    }
+};
 
 // Record the message returned by dspark_last_error() and return `st`.
 dspark_status set_last_error(dspark_status st, const char *fmt, ...);

@@ -393,6 +393,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     uint32_t *row_rid = reinterpret_cast<uint32_t *>(misc + 4 + 2 * BM);
     int *row_code = misc + 4 + 3 * BM;  // final draw: kind << 16 | position; draft: temperature valid
 
+    // one position of the recurrent head: launched as a programmatic
+    // dependent of the state kernel, so the set-up and the first W_out and
+    // base-logit tiles overlap it; its outputs are waited for (griddep_wait)
+    // only where they are read, at the A operand build.  (No early trigger
+    // for the next state kernel: its blocks would crowd onto the first SMs
+    // this grid frees.)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWStages; ++s) mbar_init(empty_w(s), 1);  // released by the UMMAs
         for (int s = 0; s < kUStages; ++s) {
@@ -596,6 +602,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             // Every UMMA of the previous position is done: this warp has seen
             // the tfull of its last tile.
             int prev = -1;
+            if (!kFinal && p.a_rows && pi == 0) griddep_wait();
             if (kFinal) {
                 prev = row_prev[row];
             } else if (b < p.B && code) {
@@ -983,9 +990,11 @@ cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, in
 
 template <bool kFinal>
 cudaError_t set_smem_attr() {
-    static cudaError_t once = cudaFuncSetAttribute(markov_tc_kernel<kFinal>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    return once;
+    static PerDeviceOnce once;
+    return once.run([] {
+        return cudaFuncSetAttribute(markov_tc_kernel<kFinal>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+    });
 }
 
 PhiloxRoundKeys round_keys(uint64_t seed) {
@@ -1108,8 +1117,19 @@ cudaError_t launch_draft_tensor_rows(const DraftArgs &a, const DraftPlan &pl, in
     p.a_rows = static_cast<const __nv_bfloat16 *>(a_rows);
     p.j = j;
     p.j_end = j + 1;
-    markov_tc_kernel<false><<<dim3(pl.nsplit, pl.row_blocks), kThreads, kSmemBytes, s>>>(mw, mu, p);
-    return cudaGetLastError();
+    // overlap the launch, barrier set-up and the first W_out / base-logit
+    // tiles with the state kernel that writes a_rows
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(pl.nsplit, pl.row_blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, mw, mu, p);
 }
 
 cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {

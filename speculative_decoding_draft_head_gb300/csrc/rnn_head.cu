@@ -13,15 +13,20 @@
 // head's path unchanged.
 //
 // Precision.  The products of two bf16 values are exact in fp32; they are
-// summed with a compensated two-sum accumulator (error about 2^-48 of the sum
-// of magnitudes), tanh is taken in fp64 and the result is rounded once to
-// bf16 from fp64.  A state therefore differs from the exactly rounded one only
-// when its pre-rounding value lies within about 1e-13 (relative) of a bf16
-// rounding boundary.
+// summed with compensated two-sum chains (error about 2^-48 of the sum of
+// magnitudes).  tanh is taken in fp32 unless the result lies within a few
+// fp32 units of a bf16 rounding midpoint, where it is taken in fp64 and
+// rounded once to bf16 from fp64 (about 1 value in 4000; GB300's fp64 rate
+// makes an fp64 tanh for every value cost more than the whole dot product).
+// A state therefore differs from the exactly rounded one only when its
+// pre-rounding value lies within about 1e-13 (relative) of a rounding
+// boundary.  (A faster-issuing variant, FMA chains with a running error bound
+// and a two-sum recompute of the undecided values, measured no faster: the
+// kernel is bound by latency at one block per SM, not by issue.)
 //
 // Work per position is B r^2 multiply-adds (16.8 M at B = r = 256): a small
-// SIMT kernel, one thread per state unit and R requests per block, so that
-// each thread's W_h row is read once per block.
+// SIMT kernel, one thread per state unit and R requests per block, with W_h
+// staged once per block in shared memory.
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -51,16 +56,50 @@ __device__ __forceinline__ __nv_bfloat16 double_to_bf16_rne(double x) {
     return __float2bfloat16_rn((float)__longlong_as_double((long long)u));
 }
 
+// fp32 units (within a binade) between a tanhf result and the nearest bf16
+// rounding midpoint below which the fp64 path decides the rounding: tanhf is
+// within 2 ulp (CUDA's documented bound) and the fp32 argument adds at most
+// 1 ulp of the result (|d tanh / da| * |a| <= |tanh a|), so 8 leaves a factor
+// of two over the worst case
+constexpr int kTanhGuard = 8;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// W_h rows in shared memory: 2 r bytes + 16 of padding, so that the 16-byte
+// loads of eight consecutive threads (eight rows) fall on distinct banks
+__host__ __device__ constexpr int w_row_bytes(int r) { return 2 * r + 16; }
+size_t state_smem_bytes(int R, int r) { return (size_t)r * w_row_bytes(r) + sizeof(float) * (size_t)R * r; }
+
+// One block: R requests, thread n = state unit n.  W_h (all r rows) is
+// staged in shared memory with coalesced asynchronous copies; each thread
+// then reads its own row from there.
 template <int R>
 __global__ void __launch_bounds__(kRnnThreads)
 rnn_state_kernel(const __nv_bfloat16 *__restrict__ e_in, const __nv_bfloat16 *__restrict__ w_h,
                  const int32_t *__restrict__ anchor, const unsigned long long *__restrict__ best,
                  const __nv_bfloat16 *__restrict__ h_prev, __nv_bfloat16 *__restrict__ h_next,
                  __nv_bfloat16 *__restrict__ h_out, int B, int G, int V, int r, int j) {
-    extern __shared__ float hs[];  // [R][r]: h_{j-1} of the block's requests
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned char *wsm = smem;                                            // [r][w_row_bytes]
+    float *hs = reinterpret_cast<float *>(smem + (size_t)r * w_row_bytes(r));  // [R][r]: h_{j-1}
     __shared__ int prev_s[R];
-    const int b0 = blockIdx.x * R;
+    // the draw of this position (the next launch) may start its prologue
+    if (threadIdx.x == 0) griddep_launch_dependents();
     const int n = threadIdx.x;
+    if (j > 0) {
+        // W_h is an input: its copy may start before the previous kernel ends
+        const int parts = r / 8;  // 16-byte pieces per row
+        const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(wsm);
+        for (int idx = threadIdx.x; idx < r * parts; idx += blockDim.x) {
+            const int row = idx / parts, part = idx - row * parts;
+            cp_async16(wbase + (uint32_t)(row * w_row_bytes(r) + part * 16), w_h + (size_t)row * r + part * 8);
+        }
+    }
+    griddep_wait();
+    const int b0 = blockIdx.x * R;
     if (threadIdx.x < R) {
         const int b = b0 + threadIdx.x;
         int prev = -1;
@@ -77,23 +116,33 @@ rnn_state_kernel(const __nv_bfloat16 *__restrict__ e_in, const __nv_bfloat16 *__
         const int b = b0 + rr;
         hs[i] = (j > 0 && b < B) ? __bfloat162float(h_prev[(size_t)b * r + k]) : 0.f;
     }
+    cp_async_wait_all();
     __syncthreads();
     if (n >= r) return;
 
-    float s[R], c[R];
+    // four interleaved compensated sums per request (k mod 4) keep four
+    // independent dependency chains in flight; merged exactly at the end
+    float s[R][4], c[R][4];
 #pragma unroll
-    for (int i = 0; i < R; ++i) s[i] = c[i] = 0.f;
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s[i][q] = c[i][q] = 0.f;
     if (j > 0) {
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(w_h + (size_t)n * r);
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(wsm + (size_t)n * w_row_bytes(r));
+#pragma unroll 2
         for (int k8 = 0; k8 < r / 8; ++k8) {
-            const uint4 w4 = __ldg(wrow + k8);
+            const uint4 w4 = wrow[k8];
             const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float w = (e & 1) ? bf16_hi(ww[e >> 1]) : bf16_lo(ww[e >> 1]);
-                const int k = 8 * k8 + e;
+            for (int i = 0; i < R; ++i) {
+                const float4 h0 = *reinterpret_cast<const float4 *>(hs + i * r + 8 * k8);
+                const float4 h1 = *reinterpret_cast<const float4 *>(hs + i * r + 8 * k8 + 4);
+                const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-                for (int i = 0; i < R; ++i) two_sum_acc(s[i], c[i], __fmul_rn(w, hs[i * r + k]));
+                for (int e = 0; e < 8; ++e) {
+                    const float w = (e & 1) ? bf16_hi(ww[e >> 1]) : bf16_lo(ww[e >> 1]);
+                    two_sum_acc(s[i][e & 3], c[i][e & 3], __fmul_rn(w, hv[e]));
+                }
             }
         }
     }
@@ -104,8 +153,14 @@ rnn_state_kernel(const __nv_bfloat16 *__restrict__ e_in, const __nv_bfloat16 *__
         const int prev = prev_s[i];
         __nv_bfloat16 h = __float2bfloat16_rn(0.f);
         if (prev >= 0) {
-            const double a = (double)__bfloat162float(e_in[(size_t)prev * r + n]) + (double)s[i] + (double)c[i];
-            h = double_to_bf16_rne(tanh(a));
+            float sm = s[i][0], cm = c[i][0] + c[i][1] + c[i][2] + c[i][3];
+            two_sum_acc(sm, cm, s[i][1]);
+            two_sum_acc(sm, cm, s[i][2]);
+            two_sum_acc(sm, cm, s[i][3]);
+            const double a = (double)__bfloat162float(e_in[(size_t)prev * r + n]) + (double)sm + (double)cm;
+            const float t = tanhf((float)a);
+            const int mid = abs((int)(__float_as_uint(t) & 0xFFFFu) - 0x8000);
+            h = (mid > kTanhGuard) ? __float2bfloat16_rn(t) : double_to_bf16_rne(tanh(a));
         }
         h_next[(size_t)b * r + n] = h;
         if (h_out) h_out[((size_t)b * G + j) * r + n] = h;
@@ -114,8 +169,14 @@ rnn_state_kernel(const __nv_bfloat16 *__restrict__ e_in, const __nv_bfloat16 *__
 
 template <int R>
 cudaError_t launch_rnn_r(const RnnStateArgs &a, int j, cudaStream_t s) {
+    const size_t smem = state_smem_bytes(R, a.r);
+    static PerDeviceOnce once;  // the limit for the largest r
+    cudaError_t e = once.run([] {
+        return cudaFuncSetAttribute(rnn_state_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)state_smem_bytes(R, 256));
+    });
+    if (e != cudaSuccess) return e;
     const int blocks = (a.B + R - 1) / R;
-    const size_t smem = sizeof(float) * (size_t)R * (size_t)a.r;
     const __nv_bfloat16 *h_prev = a.h_ws + (size_t)(j > 0 ? j - 1 : 0) * a.B * a.r;
     rnn_state_kernel<R><<<blocks, kRnnThreads, smem, s>>>(a.e_in, a.w_h, a.anchor, a.best, h_prev,
                                                           a.h_ws + (size_t)j * a.B * a.r, a.h_out, a.B, a.G,
@@ -134,9 +195,10 @@ RnnPlan plan_draft_rnn(int B, int G, int V, int r) {
 }
 
 int rnn_rows_per_block(int B) {
-    // at least one block per SM where B allows, else fewer requests per block
-    int R = 8;
-    while (R > 1 && (B + R - 1) / R < kNumSMs) R >>= 1;
+    // a block fills an SM's shared memory with W_h: one wave of at most one
+    // block per SM, and as few W_h copies as that allows
+    int R = 1;
+    while (R < 8 && (B + R - 1) / R > kNumSMs) R <<= 1;
     return R;
 }
 
