@@ -86,7 +86,7 @@ def lib():
             L.or_draft_sample.argtypes = [
                 _f64p, _f64p, _f64p, _i32p, _f64p, nu,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
-                _i32p, _f64p, _f64p, _f64p, _f64p, nf]
+                _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, nf]
             L.or_draft_sample.restype = ctypes.c_int
             L.or_schedule.argtypes = [
                 _f64p, _f64p, _f64p, ctypes.c_int,
@@ -96,7 +96,7 @@ def lib():
             L.or_draft_sample_rnn.argtypes = [
                 _f64p, _f64p, _f64p, _f64p, _i32p, _f64p, nu,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
-                _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, nf]
+                _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, nf]
             L.or_draft_sample_rnn.restype = ctypes.c_int
             L.or_schedule_policy.argtypes = [
                 _f64p, _f64p, _f64p, ctypes.c_int,
@@ -175,8 +175,8 @@ def draft_sample(U, E_in, W_out, anchor, temp, rid=None, seed=0, want_z=False):
 
     U [B,G,V], E_in [V,r], W_out [V,r] (row v scores token v), anchor [B], temp [B],
     rid [B] or None.
-    Returns a dict of numpy arrays: tokens, lse, logq, gap, top (all [B,G]),
-    and z [B,G,V] when ``want_z``.
+    Returns a dict of numpy arrays: tokens, lse, logq, gap, top, cdf_margin
+    (all [B,G]), and z [B,G,V] when ``want_z``.
     """
     U = _f64(U)
     E_in = _f64(E_in)
@@ -188,10 +188,12 @@ def draft_sample(U, E_in, W_out, anchor, temp, rid=None, seed=0, want_z=False):
     temp = _f64(temp)
     rid = _u32(rid)
     out = dict(tokens=np.zeros((B, G), np.int32), lse=np.zeros((B, G)),
-               logq=np.zeros((B, G)), gap=np.zeros((B, G)), top=np.zeros((B, G)))
+               logq=np.zeros((B, G)), gap=np.zeros((B, G)), top=np.zeros((B, G)),
+               cdf_margin=np.zeros((B, G)))
     z = np.zeros((B, G, V)) if want_z else None
     rc = lib().or_draft_sample(U, E_in, W_out, anchor, temp, rid, B, G, V, r, seed,
-                               out["tokens"], out["lse"], out["logq"], out["gap"], out["top"], z)
+                               out["tokens"], out["lse"], out["logq"], out["gap"], out["top"],
+                               out["cdf_margin"], z)
     if rc != 0:
         raise ValueError("or_draft_sample failed: %d" % rc)
     if want_z:
@@ -216,11 +218,11 @@ def draft_sample_rnn(U, E_in, W_h, W_out, anchor, temp, rid=None, seed=0, want_z
     rid = _u32(rid)
     out = dict(tokens=np.zeros((B, G), np.int32), lse=np.zeros((B, G)),
                logq=np.zeros((B, G)), gap=np.zeros((B, G)), top=np.zeros((B, G)),
-               h=np.zeros((B, G, r)), h_margin=np.zeros((B, G)))
+               cdf_margin=np.zeros((B, G)), h=np.zeros((B, G, r)), h_margin=np.zeros((B, G)))
     z = np.zeros((B, G, V)) if want_z else None
     rc = lib().or_draft_sample_rnn(U, E_in, W_h, W_out, anchor, temp, rid, B, G, V, r, seed,
                                    out["tokens"], out["lse"], out["logq"], out["gap"], out["top"],
-                                   out["h"], out["h_margin"], z)
+                                   out["cdf_margin"], out["h"], out["h_margin"], z)
     if rc != 0:
         raise ValueError("or_draft_sample_rnn failed: %d" % rc)
     if want_z:

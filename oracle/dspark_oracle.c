@@ -158,6 +158,59 @@ static int gumbel_max(const double *s, const unsigned char *allowed, int V,
     return best;
 }
 
+/* Draw from softmax(s) in two stages (reading R2b): the vocabulary is cut into
+ * groups of DRAW_GROUP consecutive tokens (the last one ragged).  With
+ * (w0, w1, w2, w3) the Philox block at counter (g, j, rid, stream), i.e.
+ * u0 = or_uniform(.., 4 g, stream) and u1 = or_uniform(.., 4 g + 1, stream):
+ *   group key   K_g = log sum_{v in g} exp(s_v) + G(u0),  G(u) = -log(-log u);
+ *   winner      g* = argmax_g K_g (lowest g on exact ties);
+ *   token       the first v of g* whose running sum sum_{v' <= v} exp(s_v')
+ *               exceeds u1 * sum_{v in g*} exp(s_v) (inverse CDF in group order).
+ * The maximum of Gumbels is Gumbel at their log-sum-exp and its argmax is
+ * independent of its value, so the token has law softmax(s) exactly.
+ * gap / top: the top-two group keys' difference and the top key; cdf_margin:
+ * the smallest |running sum - u1 * group sum| / group sum over the group's
+ * boundaries (how close the in-group draw came to a neighbour). */
+#define DRAW_GROUP 16
+static int group_draw(const double *s, int V, uint64_t seed, uint32_t rid, uint32_t j, uint32_t stream,
+                      double *gap, double *top, double *cdf_margin)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) if (s[v] > m) m = s[v];
+    int gbest = -1;
+    double k1 = -INFINITY, k2 = -INFINITY;
+    for (int g0 = 0; g0 < V; g0 += DRAW_GROUP) {
+        int g1 = g0 + DRAW_GROUP < V ? g0 + DRAW_GROUP : V;
+        double sum = 0.0;
+        for (int v = g0; v < g1; ++v) sum += exp(s[v] - m);
+        if (!(sum > 0.0)) continue;
+        uint32_t g = (uint32_t)(g0 / DRAW_GROUP);
+        double key = m + log(sum) - log(-log(or_uniform(seed, rid, j, 4u * g, stream)));
+        if (gbest < 0 || key > k1) { k2 = k1; k1 = key; gbest = (int)g; }
+        else if (key > k2) { k2 = key; }
+    }
+    if (gap) *gap = k1 - k2;
+    if (top) *top = k1;
+    int g0 = gbest * DRAW_GROUP, g1 = g0 + DRAW_GROUP < V ? g0 + DRAW_GROUP : V;
+    double sum = 0.0;
+    for (int v = g0; v < g1; ++v) sum += exp(s[v] - m);
+    double target = or_uniform(seed, rid, j, 4u * (uint32_t)gbest + 1u, stream) * sum;
+    int x = -1;
+    double run = 0.0, margin = INFINITY;
+    for (int v = g0; v < g1; ++v) {
+        double e = exp(s[v] - m);
+        run += e;
+        if (e > 0.0) {
+            double d = fabs(run - target) / sum;
+            if (d < margin) margin = d;
+        }
+        if (x < 0 && run > target) x = v;
+    }
+    if (x < 0) for (int v = g1 - 1; v >= g0; --v) if (exp(s[v] - m) > 0.0) { x = v; break; }
+    if (cdf_margin) *cdf_margin = margin;
+    return x;
+}
+
 /* [DSP-IT] "Un po' di autoregressione basta", equation for p_k, with the
  * Markov head B = W1 W2 (R3, R4).  W1 = E_in is stored [V][r]; W2 is stored
  * transposed as W_out [V][r] (row v scores token v), so
@@ -180,15 +233,17 @@ static void markov_logits(const double *U_row, const double *E_in, const double 
 /* probability; the sampled token feeds the next position's bias).            */
 /*                                                                           */
 /* U [B][G][V], E_in [V][r], W_out [V][r], anchor [B], temp [B], rid [B]      */
-/* (NULL = 0..B-1).  Outputs [B][G]: tokens, lse (T = 0: max z), logq         */
-/* (T = 0: 0), gap / top of the deciding keys; z_out [B][G][V] optional.      */
+/* (NULL = 0..B-1).  Outputs [B][G]: tokens (group_draw, reading R2b), lse   */
+/* (T = 0: max z), logq (T = 0: 0), gap / top of the deciding group keys      */
+/* (T = 0: of the logits), cdf_margin of the in-group draw (T = 0: +inf);     */
+/* z_out [B][G][V] optional.                                                  */
 /* Returns 0, or -1 on an out-of-range anchor.                                */
 /* ------------------------------------------------------------------------ */
 int or_draft_sample(const double *U, const double *E_in, const double *W_out,
                     const int32_t *anchor, const double *temp, const uint32_t *rid,
                     int B, int G, int V, int r, uint64_t seed,
                     int32_t *tokens, double *lse, double *logq, double *gap, double *top,
-                    double *z_out)
+                    double *cdf_margin, double *z_out)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
     double *s = (double *)malloc(sizeof(double) * (size_t)V);
@@ -207,11 +262,12 @@ int or_draft_sample(const double *U, const double *E_in, const double *W_out,
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) s[v] = z[v] / T;
                 double l = row_logsumexp(s, V);
-                x = gumbel_max(s, NULL, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o]);
+                x = group_draw(s, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
                 lse[o] = l;
                 logq[o] = s[x] - l;
             } else {
                 x = row_argmax(z, V, &gap[o], &top[o]);
+                cdf_margin[o] = INFINITY;
                 lse[o] = z[x];
                 logq[o] = 0.0;
             }
@@ -254,7 +310,7 @@ int or_draft_sample_rnn(const double *U, const double *E_in, const double *W_h, 
                         const int32_t *anchor, const double *temp, const uint32_t *rid,
                         int B, int G, int V, int r, uint64_t seed,
                         int32_t *tokens, double *lse, double *logq, double *gap, double *top,
-                        double *h_out, double *h_margin, double *z_out)
+                        double *cdf_margin, double *h_out, double *h_margin, double *z_out)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
     double *s = (double *)malloc(sizeof(double) * (size_t)V);
@@ -294,11 +350,12 @@ int or_draft_sample_rnn(const double *U, const double *E_in, const double *W_h, 
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) s[v] = z[v] / T;
                 double l = row_logsumexp(s, V);
-                x = gumbel_max(s, NULL, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o]);
+                x = group_draw(s, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
                 lse[o] = l;
                 logq[o] = s[x] - l;
             } else {
                 x = row_argmax(z, V, &gap[o], &top[o]);
+                cdf_margin[o] = INFINITY;
                 lse[o] = z[x];
                 logq[o] = 0.0;
             }

@@ -240,21 +240,6 @@ __device__ __forceinline__ void softmax_push_group(RowState &st, const float (&s
     st.S += acc;
 }
 
-// Gumbel-max step for one token: exact key s2 - log2(-ln u).  The cheap test
-// first: since -ln u >= 1 - u, the token cannot beat the current best when
-// log2(1 - u) >= s2 - best (a 1e-4 margin covers the approximate log2).
-__device__ __forceinline__ void gumbel_push(RowState &st, float s2, uint32_t word, int v) {
-    const float w1 = word_to_one_minus_uniform(word);
-    if (fast_log2(w1) < s2 - st.key + 1e-4f) {
-        const float key = s2 - fast_log2(neg_log_uniform(word));
-        if (key > st.key || (key == st.key && v < st.idx)) {
-            st.key = key;
-            st.s_at = s2;
-            st.idx = v;
-        }
-    }
-}
-
 // Greedy step: key = value itself.
 __device__ __forceinline__ void argmax_push(RowState &st, float z, int v) {
     if (z > st.key || (z == st.key && v < st.idx)) {

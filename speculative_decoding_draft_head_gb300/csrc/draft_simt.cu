@@ -10,7 +10,9 @@
 // shared memory, forms the rank-r bias with register-tiled FMAs (4 vocabulary
 // entries x rows_per_block requests per thread, W_out rows read along r), adds
 // the base logits and streams every logit once through the online softmax and
-// the Gumbel-max argmax.  The per-(request, segment) partial states are merged
+// the two-stage group draw (a Gumbel on each 16-token group's log-sum-exp, an
+// inverse CDF inside the winning group; four lanes hold one group).  The
+// per-(request, segment) partial states are merged
 // by draft_finalize, which writes the token the next position reads.  bf16
 // weights take the tensor-core kernel (markov_tc.cu) instead.
 #include <climits>
@@ -23,6 +25,73 @@ namespace {
 
 constexpr int kSimtThreads = 256;
 constexpr int kSimtRows = 8;
+
+// The two-stage group draw of a 16-token group held by a quad of lanes (four
+// tokens each, lane & 3 = quarter of the group; v = this lane's first token).
+// Group key K_g = max + log2 sum 2^(s - max) - log2(-ln u0) (log2 units), and
+// inside the group the first token whose running sum of 2^(s - max) exceeds
+// u1 times the group's sum, with (u0, u1) = words 0 and 1 of the Philox block
+// at counter (group, j, rid, draft stream).  The quad's first lane records a
+// key that beats its partial state.  Every lane of the warp calls it.
+__device__ __forceinline__ void group_draw_quad(RowState &st, const float (&s2)[4], int v, bool valid, uint32_t rid,
+                                                int j, uint32_t k0, uint32_t k1) {
+    const int lane = threadIdx.x & 31;
+    float gm = fmaxf(fmaxf(s2[0], s2[1]), fmaxf(s2[2], s2[3]));
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+    float e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e[i] = (valid && gm > -INFINITY) ? exp2f(s2[i] - gm) : 0.f;
+    float gs = ((e[0] + e[1]) + e[2]) + e[3];
+    gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+    gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+    const bool leader = (lane & 3) == 0;
+    bool take = false;
+    float key = -INFINITY;
+    uint4 wd = make_uint4(0u, 0u, 0u, 0u);
+    if (leader && valid && gs > 0.f) {
+        wd = philox4x32_10(make_uint4((uint32_t)v >> 4, (uint32_t)j, rid, kStreamDraft), k0, k1);
+        key = gm + log2f(gs) - log2f(neg_log_uniform(wd.x));
+        take = key > st.key;  // an exact tie keeps the earlier, lower-numbered group
+    }
+    if (!__any_sync(0xffffffffu, take)) return;
+    // gather the quad's terms and scaled logits in the leader, in token order
+    float eq[16], sq[16];
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            eq[4 * qd + i] = __shfl_sync(0xffffffffu, e[i], (lane & ~3) + qd);
+            sq[4 * qd + i] = __shfl_sync(0xffffffffu, s2[i], (lane & ~3) + qd);
+        }
+    if (!take) return;
+    float run = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) run += eq[i];
+    const float target = word_to_uniform(wd.y) * run;
+    int x = -1, last = 0;
+    float sx = 0.f, sl = 0.f;
+    run = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        run += eq[i];
+        if (eq[i] > 0.f) {
+            last = i;
+            sl = sq[i];
+        }
+        if (x < 0 && run > target) {
+            x = i;
+            sx = sq[i];
+        }
+    }
+    if (x < 0) {  // target rounded up to the group's sum: its last token
+        x = last;
+        sx = sl;
+    }
+    st.key = key;
+    st.idx = v + x;
+    st.s_at = sx;
+}
 
 template <typename TIn>
 __global__ void __launch_bounds__(kSimtThreads)
@@ -73,15 +142,19 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
 #pragma unroll
     for (int rb = 0; rb < kSimtRows; ++rb) st[rb] = row_state_init();
 
-    const int vb = seg * chunk;
+    const int vb = seg * chunk;  // a multiple of 16: whole draw groups
     const int ve = min(V, vb + chunk);
-    for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kSimtThreads) {
+    // every thread runs the same iterations (the group draw votes and
+    // shuffles across the warp); lanes past the segment hold no tokens
+    for (int vbase = vb; vbase < ve; vbase += 4 * kSimtThreads) {
+        const int v = vbase + 4 * threadIdx.x;
+        const bool valid = v < ve;  // V % 8 == 0: all four tokens or none
         float acc[kSimtRows][4];
 #pragma unroll
         for (int rb = 0; rb < kSimtRows; ++rb)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[rb][e] = 0.f;
-        for (int k = 0; k < r; k += 4) {
+        for (int k = 0; valid && k < r; k += 4) {
             float4 w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) w[e] = load4(w_out + (size_t)(v + e) * r + k);
@@ -102,23 +175,23 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
 #pragma unroll
         for (int rb = 0; rb < kSimtRows; ++rb) {
             const int b = b0 + rb;
-            if (b >= B || prev_s[rb] < 0) continue;
+            if (b >= B || prev_s[rb] < 0) continue;  // uniform over the block
             const size_t row = (size_t)b * G + j;
-            const float4 u4 = load4(base + row * V + v);
             const float c2 = c2_s[rb];
-            float z[4];
+            float z[4] = {0.f, 0.f, 0.f, 0.f};
+            if (valid) {
+                const float4 u4 = load4(base + row * V + v);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[rb][e];
-            if (z_out) *reinterpret_cast<float4 *>(z_out + row * V + v) = make_float4(z[0], z[1], z[2], z[3]);
+                for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[rb][e];
+                if (z_out) *reinterpret_cast<float4 *>(z_out + row * V + v) = make_float4(z[0], z[1], z[2], z[3]);
+            }
             if (c2 > 0.f) {
                 float s2[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) s2[e] = z[e] * c2;
-                softmax_push_group<4>(st[rb], s2, 4);
-                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, rid_s[rb], kStreamDraft), k0, k1);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) gumbel_push(st[rb], s2[e], word_of(w4, e), v + e);
-            } else {
+                for (int e = 0; e < 4; ++e) s2[e] = valid ? z[e] * c2 : -INFINITY;
+                if (valid) softmax_push_group<4>(st[rb], s2, 4);
+                group_draw_quad(st[rb], s2, v, valid, rid_s[rb], j, k0, k1);
+            } else if (valid) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) argmax_push(st[rb], z[e], v + e);
             }
@@ -221,7 +294,7 @@ DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
         if (nsplit > max_split) nsplit = max_split;
         if (nsplit < 1) nsplit = 1;
         int chunk = (V + nsplit - 1) / nsplit;
-        chunk = (chunk + 3) / 4 * 4;
+        chunk = (chunk + 15) / 16 * 16;  // whole draw groups per segment
         p.nsplit = (V + chunk - 1) / chunk;
         p.chunk = chunk;
     }

@@ -47,7 +47,7 @@ struct DraftPlan {
     int rows_per_block;    // SIMT: requests per block
     int row_blocks;        // SIMT: ceil(B / rows_per_block); tensor path: M tiles
     int nsplit;            // vocabulary segments per row (partials per row)
-    int chunk;             // vocabulary entries per segment (multiple of 4)
+    int chunk;             // vocabulary entries per segment (SIMT; a multiple of 16, whole draw groups)
     size_t partial_offset; // byte offset of the per-(row, segment) partials ([G][B][nsplit] on the tensor path)
     size_t best_offset;    // [G][B] 64-bit row-wide best (key, token) words (tensor path), zeroed per call
     size_t bar_offset;     // [row_blocks] barrier counters between positions (tensor path), zeroed per call

@@ -161,7 +161,7 @@ __device__ __forceinline__ bool grid_sync(unsigned int *ctr, unsigned int target
 
 __device__ __forceinline__ int seg_begin(int s, int nseg, int V) {
     if (s >= nseg) return V;
-    return (int)(((long long)s * V / nseg) & ~7LL);
+    return (int)(((long long)s * V / nseg) & ~15LL);  // whole 16-token draw groups
 }
 
 __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
@@ -213,76 +213,48 @@ __device__ __forceinline__ float sum16(const float (&e)[16]) {
     return (s8[0] + s8[2]) + (s8[1] + s8[3]);
 }
 
-// Draft epilogue for 16 logits z of one row (T > 0, c2 = log2(e) / T), with
-// the draft-stream Philox words w of those tokens.  Every
-// lane of the warp calls it together (it votes across the warp); `on` is false
-// for rows that are greedy or inactive, which then change nothing.
+// Draft epilogue for the 16 logits z of one row (T > 0, c2 = log2(e) / T).
+// Every lane of the warp calls it together (it votes across the warp); `on`
+// is false for rows that are greedy or inactive, which then change nothing.
+//
+// One sub-slice of 16 tokens is one draw group (v is a multiple of 16; the
+// vocabulary's last group may be ragged, n < 16).  The row's draw is the
+// two-stage group draw: the group key K_g = log2 sum_g 2^s + G2(u0) with
+// G2(u) = -log2(-ln u), the largest key wins, and inside the winning group the
+// token is the first whose running sum of 2^s exceeds u1 times the group's
+// sum; w.x and w.y (words 0 and 1 of the group's Philox block) give u0 and u1.
 //
 // The softmax keeps a running reference m (log2 units) that may lag the true
-// maximum: terms 2^(z c2 - m) above 1 are fine, and a batch whose sum exceeds
-// 2^64 (or overflows) is redone against its own maximum.  The first batch of a
-// row segment takes its maximum as m and the exact key of that token as the
-// first best key, so later tokens face a tight threshold at once.  The
-// candidate test runs per Philox group of four tokens: the group's largest e
-// against its smallest 1 - u (largest word); only passing groups test their
-// tokens one by one.
-//
-// kbest is the best key known for the whole row: this thread's, or a larger
-// one another thread published in the row's best word (any token that cannot beat an
-// achieved key cannot be the row's Gumbel argmax, so it is skipped exactly).
-// A new best is published with atomicMax; readers see it a tile later.
-__device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
-                                               int n, int v, bool on, unsigned long long *best,
-                                               const uint4 (&w)[4]) {
+// maximum: terms 2^(z c2 - m) above 1 are fine, and a group whose sum exceeds
+// 2^64 (or overflows) is redone against its own maximum.  With Q = 2^(m - K),
+// K the best key known for the whole row (this thread's, or a larger one
+// another thread published in the row's best word), K_g > K needs
+// -ln u0 < sum Q, hence (1 - u0) < sum Q: a group that fails the conservative
+// form f1 < fl(sum Q + 1) cannot win and costs no logarithm.  A new best is
+// published with atomicMax; readers see it a sub-slice later.
+__device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
+                                              int n, int v, bool on, unsigned long long *best, const uint4 &w) {
     const bool full = (n == 16);  // warp-uniform
     float e[16];
+    float sum = 0.f;
     if (on) {
         if (st.m == -INFINITY) {
-            // exact keys of the top token of each group of four: the best of them
-            // seeds the threshold
-            float zm = -INFINITY, kb = -INFINITY, sb = 0.f;
-            int ib = INT32_MAX;
+            // the first group of this thread's row: its maximum is the reference
+            float zm = -INFINITY;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                float zg = -INFINITY;
-                int ig = 0;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int i = 4 * g + c;
-                    if ((full || i < n) && z[i] > zg) {
-                        zg = z[i];
-                        ig = c;
-                    }
-                }
-                if (zg == -INFINITY) continue;  // ragged tail: an empty group
-                zm = fmaxf(zm, zg);
-                const uint32_t word = ig == 0 ? w[g].x : (ig == 1 ? w[g].y : (ig == 2 ? w[g].z : w[g].w));
-                const float s2 = zg * c2;
-                const float key = s2 - fast_log2(neg_log_uniform(word));
-                if (key > kb) {
-                    kb = key;
-                    sb = s2;
-                    ib = v + 4 * g + ig;
-                }
-            }
+            for (int i = 0; i < 16; ++i)
+                if (full || i < n) zm = fmaxf(zm, z[i]);
             st.m = zm * c2;  // c2 > 0: the rounded product is monotone in z
-            if (kb > kbest) {
-                st.key = kb;
-                st.s_at = sb;
-                st.idx = ib;
-                kbest = kb;
-                atomicMax(best, best_encode(kb, ib));
-            }
             Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
-        if (full) {  // warp-uniform: only segment tails are ragged
+        if (full) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) e[i] = fast_exp2(fmaf(z[i], c2, -st.m));
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) e[i] = (i < n) ? fast_exp2(fmaf(z[i], c2, -st.m)) : 0.f;
         }
-        float sum = sum16(e);
+        sum = sum16(e);
         if (!(sum <= 0x1p64f)) {  // far above the reference (or overflow): renormalise
             float zm = -INFINITY;
 #pragma unroll
@@ -297,43 +269,43 @@ __device__ __forceinline__ void draft_sample16(RowState &st, float &Q, float &kb
             sum = sum16(e);
         }
         st.S += sum;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) e[i] = 0.f;  // threshold 1 <= f1: no candidate
     }
-    uint32_t gmask = 0;
+    const bool cand = on && sum > 0.f && one_minus_uniform_plus_one(w.x) < fmaf(sum, Q, 1.f);
+    if (__any_sync(0xffffffffu, cand) && cand) {
+        // rare: the group's exact key
+        const float key = st.m + fast_log2(sum) - fast_log2(neg_log_uniform(w.x));
+        if (key > kbest) {
+            // the token: inverse CDF in group order, on the sequential sums
+            float run = 0.f;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const float emax = fmaxf(fmaxf(e[4 * g], e[4 * g + 1]), fmaxf(e[4 * g + 2], e[4 * g + 3]));
-        const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
-        if (one_minus_uniform_plus_one(wmax) < fmaf(emax, Q, 1.f)) gmask |= 1u << g;
-    }
-    if (__any_sync(0xffffffffu, gmask != 0)) {
-        // rare: one pass per group, its values picked by value (no local memory)
-#pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
-            const bool mine = (gmask >> g) & 1u;
-            if (!(__any_sync(0xffffffffu, mine) && mine)) continue;
-            const uint4 wg = g == 0 ? w[0] : (g == 1 ? w[1] : (g == 2 ? w[2] : w[3]));
+            for (int i = 0; i < 16; ++i) run += e[i];
+            const float target = word_to_uniform(w.y) * run;
+            int x = -1, last = 0;
+            float zx = 0.f, zl = 0.f;
+            run = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float ei = g == 0 ? e[c] : (g == 1 ? e[4 + c] : (g == 2 ? e[8 + c] : e[12 + c]));
-                const float zi = g == 0 ? z[c] : (g == 1 ? z[4 + c] : (g == 2 ? z[8 + c] : z[12 + c]));
-                const uint32_t word = word_of(wg, c);
-                if (!(one_minus_uniform_plus_one(word) < fmaf(ei, Q, 1.f))) continue;
-                const float s2 = zi * c2;
-                const float key = s2 - fast_log2(neg_log_uniform(word));
-                if (key > kbest) {
-                    const int idx = v + 4 * g + c;
-                    st.key = key;
-                    st.s_at = s2;
-                    st.idx = idx;
-                    kbest = key;
-                    atomicMax(best, best_encode(key, idx));
+            for (int i = 0; i < 16; ++i) {
+                run += e[i];
+                if (e[i] > 0.f) {
+                    last = i;
+                    zl = z[i];
+                }
+                if (x < 0 && run > target) {
+                    x = i;
+                    zx = z[i];
                 }
             }
+            if (x < 0) {  // target rounded up to the group's sum: its last token
+                x = last;
+                zx = zl;
+            }
+            st.key = key;
+            st.s_at = zx * c2;
+            st.idx = v + x;
+            kbest = key;
+            atomicMax(best, best_encode(key, v + x));
+            Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
-        if (on) Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
     }
 }
 
@@ -684,6 +656,17 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
                 }
             }
+            // Philox words of a 16-token sub-slice: the draft's group block
+            // (counter = group index v / 16), or the final draw's per-token
+            // words (counters v / 4 .. v / 4 + 3)
+            auto draw_words = [&](uint4 (&w)[4], int vw, const PhiloxRow &pr, const PhiloxRoundKeys &K) {
+                if (!kFinal) {
+                    w[0] = philox_folded((uint32_t)vw >> 4, pr, K);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)vw >> 2) + g, pr, K);
+                }
+            };
             int waited = -1;  // the last tile whose accumulator this warp waited for
 #pragma unroll 1
             for (int si = slice; si < nsub && ok; si += kEpiPerQuad) {
@@ -699,11 +682,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + (si & 7) * 16;
                     if (t != waited) {
                         // a new tile: draw the words while its UMMAs may still run
-                        if (vw < ve) {
-#pragma unroll
-                            for (int g = 0; g < 4; ++g)
-                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, prow, p.keys);
-                        }
+                        if (vw < ve) draw_words(w, vw, prow, p.keys);
                         if (!uniform_wait(tfull(a), aph, abort)) {
                             if (lane == 0) {
                                 *abort = 1;
@@ -718,11 +697,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     } else {
                         // the tile is ready: issue the TMEM load, draw under its latency
                         tmem_ld16(taddr, acc);
-                        if (vw < ve) {
-#pragma unroll
-                            for (int g = 0; g < 4; ++g)
-                                w[g] = philox_folded(((uint32_t)vw >> 2) + g, prow, p.keys);
-                        }
+                        if (vw < ve) draw_words(w, vw, prow, p.keys);
                     }
                     tmem_ld_wait16(acc);
                     // this sub-slice is in registers: hand its part of the accumulator back
@@ -763,7 +738,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                                 Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
                             }
                         }
-                        draft_sample16(st, Q, kbest, z, c2, n, v, on, best, w);
+                        draft_group16(st, Q, kbest, z, c2, n, v, on, best, w[0]);
                         // reload it for the next sub-slice, after this one's publications
                         // (at the start of a position the other threads are publishing
                         // their first batches now)

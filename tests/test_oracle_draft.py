@@ -4,6 +4,13 @@ Sources: "DSpark, la bozza che sa quando fermarsi" (paithon.it), section
 "Un po' di autoregressione basta": the draft distribution at position k is
 softmax(U_k + B_k) with the Markov bias B = W1 W2 driven by the previous
 token, and the block is sampled left to right.
+
+The draw itself (the pages fix no sampler) is the two-stage group draw: a
+Gumbel on each 16-token group's log-sum-exp picks the group, an inverse CDF
+inside it picks the token.  Its pins: exact closed forms on constant rows
+(winner = the group with the largest group uniform, token = 16 g + floor(16 u1)),
+and chi-square agreement with softmax across several groups, a ragged last
+group, and the conditional law inside a dominant group.
 """
 import math
 
@@ -123,3 +130,58 @@ def test_request_id_and_seed_select_independent_streams():
     c = oracle.draft_sample(U, rid=[5, 5], seed=2, **kw)["tokens"]
     assert np.array_equal(a[0], a[1]) and np.array_equal(a[0], b[0])
     assert not np.array_equal(b[0], b[1]) and not np.array_equal(a[0], c[0])
+
+
+GROUP = 16
+
+
+def test_group_draw_closed_form_on_constant_rows():
+    # equal logits: every group has the same log-sum-exp, so the winner is the
+    # group with the largest group uniform u0 (word 0 of the group's Philox
+    # block, token slot 4 g), and the in-group inverse CDF on equal weights
+    # takes token floor(16 u1) (u1: word 1, slot 4 g + 1)
+    V, r, G = 64, 2, 3
+    U = np.full((5, G, V), -1.25)
+    rid = np.array([0, 3, 17, 1000, 77777], np.uint32)
+    for seed in (0, 9, 123456789):
+        d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((V, r)), np.zeros(5, np.int32),
+                                np.full(5, 0.6), rid=rid, seed=seed)
+        for b in range(5):
+            for j in range(G):
+                u0 = [oracle.uniform(seed, int(rid[b]), j, 4 * g, 0) for g in range(V // GROUP)]
+                gs = int(np.argmax(u0))
+                u1 = oracle.uniform(seed, int(rid[b]), j, 4 * gs + 1, 0)
+                assert d["tokens"][b, j] == GROUP * gs + int(math.floor(GROUP * u1))
+                assert d["logq"][b, j] == pytest.approx(-math.log(V), abs=1e-12)
+
+
+def test_group_draw_matches_softmax_across_groups_and_a_ragged_group():
+    V, r, N, T = 40, 2, 240000, 0.7      # groups of 16, 16 and 8 tokens
+    rng = np.random.default_rng(14)
+    row = rng.normal(0, 1.2, V)
+    U = np.broadcast_to(row, (N, 1, V)).copy()
+    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((V, r)), np.zeros(N, np.int32),
+                            np.full(N, T), rid=np.arange(N), seed=41)
+    p = _softmax(row / T)
+    ok, chi2 = _chi2_ok(np.bincount(d["tokens"][:, 0], minlength=V), p, N)
+    assert ok, chi2
+    # the group marginals alone (a sharper check of the first stage)
+    pg = np.add.reduceat(p, [0, 16, 32])
+    cg = np.bincount(d["tokens"][:, 0] // GROUP, minlength=3)
+    ok, chi2 = _chi2_ok(cg, pg, N)
+    assert ok, chi2
+
+
+def test_group_draw_inside_a_dominant_group_follows_the_conditional_law():
+    V, r, N = 64, 2, 160000
+    rng = np.random.default_rng(15)
+    row = rng.normal(0, 1.0, V) - 40.0
+    row[32:48] += 40.0                   # group 2 holds all the mass
+    U = np.broadcast_to(row, (N, 1, V)).copy()
+    d = oracle.draft_sample(U, np.zeros((V, r)), np.zeros((V, r)), np.zeros(N, np.int32),
+                            np.ones(N), rid=np.arange(N), seed=5)
+    tok = d["tokens"][:, 0]
+    assert np.all((tok >= 32) & (tok < 48))
+    ok, chi2 = _chi2_ok(np.bincount(tok - 32, minlength=16), _softmax(row[32:48]), N)
+    assert ok, chi2
+    assert np.all(d["cdf_margin"][:, 0] >= 0) and np.all(d["cdf_margin"][:, 0] <= 1)
