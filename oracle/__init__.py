@@ -106,7 +106,7 @@ def lib():
             L.or_verify.argtypes = [
                 _f64p, _f64p, _f64p, _f64p, _i32p, _i32p, ni, _f64p, nu,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
-                _i32p, _i32p, _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _i32p]
+                _i32p, _i32p, _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _i32p]
             L.or_verify.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -292,11 +292,12 @@ def verify(target, U, E_in, W_out, anchor, draft_tokens, verify_len, temp, rid=N
     out = dict(accept_len=np.zeros(B, np.int32), out_tokens=np.zeros((B, G + 1), np.int32),
                num_out=np.zeros(B, np.int32), target_lse=np.zeros((B, G + 1)),
                logp=np.zeros((B, G)), logq=np.zeros((B, G)), accept_margin=np.zeros((B, G)),
-               final_gap=np.zeros(B), final_top=np.zeros(B), final_kind=np.zeros(B, np.int32))
+               final_gap=np.zeros(B), final_top=np.zeros(B), final_cdf=np.zeros(B),
+               final_kind=np.zeros(B, np.int32))
     rc = lib().or_verify(target, U, E_in, W_out, anchor, dt, vl, temp, rid, B, G, V, r, seed,
                          out["accept_len"], out["out_tokens"], out["num_out"], out["target_lse"],
                          out["logp"], out["logq"], out["accept_margin"], out["final_gap"],
-                         out["final_top"], out["final_kind"])
+                         out["final_top"], out["final_cdf"], out["final_kind"])
     if rc != 0:
         raise ValueError("or_verify failed: %d" % rc)
     return out

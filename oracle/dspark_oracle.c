@@ -139,25 +139,6 @@ static int row_argmax(const double *s, int V, double *gap, double *top)
     return best;
 }
 
-/* Gumbel-max draw over keys s_v + g(u(seed, rid, j, v, stream)), restricted
- * to entries with allowed[v] != 0 when allowed is not NULL. */
-static int gumbel_max(const double *s, const unsigned char *allowed, int V,
-                      uint64_t seed, uint32_t rid, uint32_t j, uint32_t stream,
-                      double *gap, double *top)
-{
-    int best = -1;
-    double b1 = -INFINITY, b2 = -INFINITY;
-    for (int v = 0; v < V; ++v) {
-        if (allowed && !allowed[v]) continue;
-        double key = s[v] + or_gumbel(seed, rid, j, (uint32_t)v, stream);
-        if (best < 0 || key > b1) { b2 = b1; b1 = key; best = v; }
-        else if (key > b2) { b2 = key; }
-    }
-    if (gap) *gap = b1 - b2;
-    if (top) *top = b1;
-    return best;
-}
-
 /* Draw from softmax(s) in two stages (reading R2b): the vocabulary is cut into
  * groups of DRAW_GROUP consecutive tokens (the last one ragged).  With
  * (w0, w1, w2, w3) the Philox block at counter (g, j, rid, stream), i.e.
@@ -169,11 +150,14 @@ static int gumbel_max(const double *s, const unsigned char *allowed, int V,
  * The maximum of Gumbels is Gumbel at their log-sum-exp and its argmax is
  * independent of its value, so the token has law softmax(s) exactly.
  * gap / top: the top-two group keys' difference and the top key; cdf_margin:
- * the smallest |running sum - u1 * group sum| / group sum over the group's
- * boundaries (how close the in-group draw came to a neighbour). */
+ * the smallest |running sum - u1 * group sum| over the group's boundaries (how
+ * close the in-group draw came to a neighbour), divided by the group's sum of
+ * exp(s), or by the group's sum of err_scale (linear units, exp(s) measured
+ * against it) when err_scale is not NULL: a residual max(0, p - q) is computed
+ * on the device from p and q, whose size sets its absolute error. */
 #define DRAW_GROUP 16
-static int group_draw(const double *s, int V, uint64_t seed, uint32_t rid, uint32_t j, uint32_t stream,
-                      double *gap, double *top, double *cdf_margin)
+static int group_draw(const double *s, const double *err_scale, int V, uint64_t seed, uint32_t rid,
+                      uint32_t j, uint32_t stream, double *gap, double *top, double *cdf_margin)
 {
     double m = -INFINITY;
     for (int v = 0; v < V; ++v) if (s[v] > m) m = s[v];
@@ -195,13 +179,18 @@ static int group_draw(const double *s, int V, uint64_t seed, uint32_t rid, uint3
     double sum = 0.0;
     for (int v = g0; v < g1; ++v) sum += exp(s[v] - m);
     double target = or_uniform(seed, rid, j, 4u * (uint32_t)gbest + 1u, stream) * sum;
+    double norm = sum;
+    if (err_scale) {
+        norm = 0.0;
+        for (int v = g0; v < g1; ++v) norm += err_scale[v] * exp(-m);
+    }
     int x = -1;
     double run = 0.0, margin = INFINITY;
     for (int v = g0; v < g1; ++v) {
         double e = exp(s[v] - m);
         run += e;
         if (e > 0.0) {
-            double d = fabs(run - target) / sum;
+            double d = fabs(run - target) / norm;
             if (d < margin) margin = d;
         }
         if (x < 0 && run > target) x = v;
@@ -262,7 +251,7 @@ int or_draft_sample(const double *U, const double *E_in, const double *W_out,
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) s[v] = z[v] / T;
                 double l = row_logsumexp(s, V);
-                x = group_draw(s, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
+                x = group_draw(s, NULL, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
                 lse[o] = l;
                 logq[o] = s[x] - l;
             } else {
@@ -350,7 +339,7 @@ int or_draft_sample_rnn(const double *U, const double *E_in, const double *W_h, 
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) s[v] = z[v] / T;
                 double l = row_logsumexp(s, V);
-                x = group_draw(s, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
+                x = group_draw(s, NULL, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
                 lse[o] = l;
                 logq[o] = s[x] - l;
             } else {
@@ -582,7 +571,8 @@ int or_schedule_policy(const double *conf_logits, const double *pos_temp, const 
 /* l'echantillonnage par rejet": accept x with probability min(1, p/q), stop */
 /* at the first rejection and resample from the residual distribution;       */
 /* [DSP-ZH] "DSpark 是什么？": append a bonus token when the whole block is   */
-/* accepted), readings R5 and R6.                                            */
+/* accepted), readings R5 and R6; the residual, fallback and bonus draws    */
+/* are group draws (R2b) on streams 2, 2 and 3.                              */
 /*                                                                           */
 /* target [B][G+1][V]: row j is the target's logits for draft position j,    */
 /* row L_b gives the bonus.  The draft side is recomputed here from U, E_in, */
@@ -590,8 +580,9 @@ int or_schedule_policy(const double *conf_logits, const double *pos_temp, const 
 /* Outputs: accept_len [B], out_tokens [B][G+1] (-1 padded), num_out [B],    */
 /* target_lse [B][G+1] (NaN where not read; T = 0: max t), logp / logq       */
 /* [B][G] (NaN where not tested), accept_margin [B][G] = |u - min(1, p/q)|   */
-/* (NaN where not tested), final_gap / final_top [B] for the last draw,      */
-/* final_kind [B] = 0 bonus, 1 residual, 2 residual fell back to p,          */
+/* (NaN where not tested), final_gap / final_top / final_cdf [B] for the    */
+/* last draw (group_draw's gap, top and cdf_margin; greedy: the logits' gap */
+/* and +inf), final_kind [B] = 0 bonus, 1 residual, 2 residual fell back to p,*/
 /* 3 greedy correction.  Returns 0, -1 on invalid input.                     */
 /* ------------------------------------------------------------------------ */
 int or_verify(const double *target, const double *U, const double *E_in, const double *W_out,
@@ -600,14 +591,18 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
               int B, int G, int V, int r, uint64_t seed,
               int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
               double *target_lse, double *logp, double *logq, double *accept_margin,
-              double *final_gap, double *final_top, int32_t *final_kind)
+              double *final_gap, double *final_top, double *final_cdf, int32_t *final_kind)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
     double *s = (double *)malloc(sizeof(double) * (size_t)V);
     double *st = (double *)malloc(sizeof(double) * (size_t)V);
     double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    double *pq = (double *)malloc(sizeof(double) * (size_t)V);
     unsigned char *allowed = (unsigned char *)malloc((size_t)V);
-    if (!z || !s || !st || !w || !allowed) { free(z); free(s); free(st); free(w); free(allowed); return -2; }
+    if (!z || !s || !st || !w || !pq || !allowed) {
+        free(z); free(s); free(st); free(w); free(pq); free(allowed);
+        return -2;
+    }
     int rc = 0;
     for (int b = 0; b < B && rc == 0; ++b) {
         uint32_t id = rid ? rid[b] : (uint32_t)b;
@@ -629,7 +624,7 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
         int k = 0;         /* number of accepted draft tokens */
         int y = -1;        /* the final (resampled or bonus) token */
         int kind = 0;
-        double fgap = NAN, ftop = NAN;
+        double fgap = NAN, ftop = NAN, fcdf = INFINITY;
         for (int j = 0; j < L; ++j) {
             const double *t_row = target + ((size_t)b * (G + 1) + j) * (size_t)V;
             int x = draft_tokens[(size_t)b * G + j];
@@ -657,13 +652,14 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
                     double pv = exp(st[v] - lt), qv = exp(s[v] - lq);
                     allowed[v] = (unsigned char)(pv > qv);
                     w[v] = allowed[v] ? log(pv - qv) : -INFINITY;
+                    pq[v] = pv + qv;
                     any |= allowed[v];
                 }
                 if (any) {
-                    y = gumbel_max(w, allowed, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop);
+                    y = group_draw(w, pq, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop, &fcdf);
                     kind = 1;
                 } else {
-                    y = gumbel_max(st, NULL, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop);
+                    y = group_draw(st, NULL, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop, &fcdf);
                     kind = 2;
                 }
                 break;
@@ -683,7 +679,7 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
             const double *t_row = target + ((size_t)b * (G + 1) + L) * (size_t)V;
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) st[v] = t_row[v] / T;
-                y = gumbel_max(st, NULL, V, seed, id, (uint32_t)L, 3u, &fgap, &ftop);
+                y = group_draw(st, NULL, V, seed, id, (uint32_t)L, 3u, &fgap, &ftop, &fcdf);
             } else {
                 double top;
                 y = row_argmax(t_row, V, &fgap, &top);
@@ -698,8 +694,9 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
         num_out[b] = k + 1;
         final_gap[b] = fgap;
         final_top[b] = ftop;
+        final_cdf[b] = fcdf;
         final_kind[b] = kind;
     }
-    free(z); free(s); free(st); free(w); free(allowed);
+    free(z); free(s); free(st); free(w); free(pq); free(allowed);
     return rc;
 }

@@ -289,27 +289,21 @@ __device__ __forceinline__ unsigned long long load_relaxed_u64(const unsigned lo
     return v;
 }
 
-// Residual draw state: best key over {p > q} and, for the degenerate case
-// where no entry has p > q, the best key of a draw from p.
+// Final draw state (residual or bonus): the best group key and its token.
+// A residual row whose entries all have p <= q (impossible in exact
+// arithmetic after a rejection) keeps key -inf here and is redrawn from p by
+// the merge step.
 struct ResidualState {
     float key_res;
     int idx_res;
-    float key_p;
-    int idx_p;
 };
 
-__device__ __forceinline__ ResidualState residual_init() {
-    return ResidualState{-INFINITY, INT32_MAX, -INFINITY, INT32_MAX};
-}
+__device__ __forceinline__ ResidualState residual_init() { return ResidualState{-INFINITY, INT32_MAX}; }
 
 __device__ __forceinline__ void residual_merge(ResidualState &a, const ResidualState &b) {
     if (key_better(b.key_res, b.idx_res, a.key_res, a.idx_res)) {
         a.key_res = b.key_res;
         a.idx_res = b.idx_res;
-    }
-    if (key_better(b.key_p, b.idx_p, a.key_p, a.idx_p)) {
-        a.key_p = b.key_p;
-        a.idx_p = b.idx_p;
     }
 }
 

@@ -619,7 +619,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             float kbest = -INFINITY;  // best key of the row known to this thread
             unsigned long long *best = (kFinal || b >= p.B) ? nullptr : p.best + (size_t)jj * p.B + b;
             uint32_t kg_next = 0u;  // "none"
-            float Qr = kQMax;       // 2^-K for the residual candidate test (with margin)
             float kbest_r = -INFINITY;  // best residual key of the row known to this thread
             uint32_t kr_next = 0u;      // the row-wide word, loaded one sub-slice ahead ("none")
             uint32_t *res_best = (kFinal && active) ? p.res_best + b : nullptr;
@@ -656,17 +655,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
                 }
             }
-            // Philox words of a 16-token sub-slice: the draft's group block
-            // (counter = group index v / 16), or the final draw's per-token
-            // words (counters v / 4 .. v / 4 + 3)
-            auto draw_words = [&](uint4 (&w)[4], int vw, const PhiloxRow &pr, const PhiloxRoundKeys &K) {
-                if (!kFinal) {
-                    w[0] = philox_folded((uint32_t)vw >> 4, pr, K);
-                } else {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)vw >> 2) + g, pr, K);
-                }
-            };
             int waited = -1;  // the last tile whose accumulator this warp waited for
 #pragma unroll 1
             for (int si = slice; si < nsub && ok; si += kEpiPerQuad) {
@@ -675,14 +663,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 const int a = tg % kAccBufs;
                 const uint32_t aph = (uint32_t)(tg / kAccBufs) & 1u;
                 {
-                    // The Philox words need nothing from the tensor cores.
-                    uint4 w[4];
+                    // The group's Philox block (counter = group index v / 16) needs
+                    // nothing from the tensor cores.
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
                     uint32_t acc[16];
                     const int vw = sub_col(si);
                     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + (si & 7) * 16;
                     if (t != waited) {
                         // a new tile: draw the words while its UMMAs may still run
-                        if (vw < ve) draw_words(w, vw, prow, p.keys);
+                        if (vw < ve) w = philox_folded((uint32_t)vw >> 4, prow, p.keys);
                         if (!uniform_wait(tfull(a), aph, abort)) {
                             if (lane == 0) {
                                 *abort = 1;
@@ -697,7 +686,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     } else {
                         // the tile is ready: issue the TMEM load, draw under its latency
                         tmem_ld16(taddr, acc);
-                        if (vw < ve) draw_words(w, vw, prow, p.keys);
+                        if (vw < ve) w = philox_folded((uint32_t)vw >> 4, prow, p.keys);
                     }
                     tmem_ld_wait16(acc);
                     // this sub-slice is in registers: hand its part of the accumulator back
@@ -738,7 +727,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                                 Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
                             }
                         }
-                        draft_group16(st, Q, kbest, z, c2, n, v, on, best, w[0]);
+                        draft_group16(st, Q, kbest, z, c2, n, v, on, best, w);
                         // reload it for the next sub-slice, after this one's publications
                         // (at the start of a position the other threads are publishing
                         // their first batches now)
@@ -763,112 +752,72 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             }
                         }
                         if (n <= 0) continue;  // warp-uniform
-                        // Token v's key is log2(r_v) - log2(E_v) with r_v = p_v - q_v; a
-                        // bonus row is a residual row with q = 0 and unnormalised p
-                        // (lse_q2 = +inf, lse_t2 = 0).  It can beat the best key K only
-                        // if (1 - u_v) < r_v 2^-K.
-                        // upper bound of p - q under the approximate exponentials;
-                        // rb <= 0 gives a threshold <= 1 <= f1: no candidate
-                        auto rbound = [&](int i) -> float {
-                            const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -lse_t2));
+                        // One 16-token draw group (R2b; stream 2 residual, 3 bonus).  A
+                        // residual row weighs token v by r_v = p_v - q_v where positive,
+                        // with p and q normalised (reference 0); a bonus row by
+                        // 2^(t_v c2 - tref) with the group's own maximum as tref (q = 0:
+                        // lse_q2 = +inf).  Group key K_g = off + log2 sum r - log2(-ln u0),
+                        // off = tref for bonus rows, 0 for residual rows; it can beat the
+                        // best key K only if (1 - u0) < sum 2^(off - K).
+                        const bool bonus = (kind == 2);
+                        float tref = lse_t2, off = 0.f;
+                        if (active && bonus) {
+                            float tm = -INFINITY;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (i < n) tm = fmaxf(tm, bf16_at(ct_lo, ct_hi, i));
+                            tref = off = tm * c2;
+                        }
+                        // upper bound of the group's sum under the approximate exponentials
+                        float sum_up = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -tref));
                             const float qv = fast_exp2(fmaf(z[i], c2, -lse_q2));
-                            return (active && i < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
-                        };
-                        // exact residual key of a token with target logit ti and draft
-                        // logit zi (-inf where p <= q)
-                        auto rkey = [&](float ti, float zi, uint32_t word) -> float {
-                            // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
-                            // log2 q formed from the logit difference first (+inf for bonus rows)
-                            const float delta2 = fmaf(ti - zi, c2, lse_q2 - lse_t2);
-                            if (!(delta2 > 0.f)) return -INFINITY;
-                            const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
-                            return fmaf(ti, c2, -lse_t2) + l1 - fast_log2(neg_log_uniform(word));
-                        };
+                            const float ub = (pv - qv) + 4e-7f * (pv + qv);
+                            sum_up += (i < n && ub > 0.f) ? ub : 0.f;
+                        }
                         if (active) {
                             // the row-wide best key (one sub-slice old) tightens the threshold
                             const float kg = ordered_to_key(kr_next);
-                            if (kg > kbest_r) {
-                                kbest_r = kg;
-                                Qr = fminf(fast_exp2(-kbest_r), kQMax) * kMargin;
-                            }
-                            if (rs.key_res == -INFINITY && kbest_r == -INFINITY) {
-                                // first batch: exact keys of each group's most promising
-                                // token (largest bound) seed the threshold
-#pragma unroll
-                                for (int g = 0; g < 4; ++g) {
-                                    float rbm = 0.f, tm = 0.f, zm = 0.f;
-                                    int im = -1;
-                                    uint32_t word = 0;
-#pragma unroll
-                                    for (int c = 0; c < 4; ++c) {
-                                        const float r = rbound(4 * g + c);
-                                        if (r > rbm) {
-                                            rbm = r;
-                                            im = c;
-                                            tm = bf16_at(ct_lo, ct_hi, 4 * g + c);
-                                            zm = z[4 * g + c];
-                                            word = word_of(w[g], c);
-                                        }
-                                    }
-                                    if (im < 0) continue;
-                                    const float key = rkey(tm, zm, word);
-                                    if (key > rs.key_res) {
-                                        rs.key_res = key;
-                                        rs.idx_res = v + 4 * g + im;
-                                    }
-                                }
-                                if (rs.key_res > kbest_r) {
-                                    kbest_r = rs.key_res;
-                                    atomicMax(res_best, key_to_ordered(kbest_r));
-                                }
-                                Qr = fminf(fast_exp2(-kbest_r), kQMax) * kMargin;
-                            }
+                            if (kg > kbest_r) kbest_r = kg;
                         }
-                        uint32_t gmask = 0;
+                        const float Qg = fminf(fast_exp2(off - kbest_r), kQMax) * kMargin;
+                        const bool cand = active && sum_up > 0.f && one_minus_uniform_plus_one(w.x) < fmaf(sum_up, Qg, 1.f);
+                        if (__any_sync(0xffffffffu, cand) && cand) {
+                            // rare: the exact weights, r_v = p_v (1 - 2^-delta) with
+                            // delta = log2 p_v - log2 q_v formed from the logits first
+                            // (+inf for bonus rows), and the group's exact key
+                            float r[16];
+                            float R = 0.f;
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const float rmax = fmaxf(fmaxf(rbound(4 * g), rbound(4 * g + 1)),
-                                                     fmaxf(rbound(4 * g + 2), rbound(4 * g + 3)));
-                            const uint32_t wmax = max(max(w[g].x, w[g].y), max(w[g].z, w[g].w));
-                            if (one_minus_uniform_plus_one(wmax) < fmaf(rmax, Qr, 1.f)) gmask |= 1u << g;
-                        }
-                        if (__any_sync(0xffffffffu, gmask != 0)) {
-                            // rare: one pass per group, its values picked by value
-#pragma unroll 1
-                            for (int g = 0; g < 4; ++g) {
-                                const bool mine = (gmask >> g) & 1u;
-                                if (!(__any_sync(0xffffffffu, mine) && mine)) continue;
-                                const uint4 wg = g == 0 ? w[0] : (g == 1 ? w[1] : (g == 2 ? w[2] : w[3]));
+                            for (int i = 0; i < 16; ++i) {
+                                const float ti = bf16_at(ct_lo, ct_hi, i);
+                                const float delta2 = fmaf(ti - z[i], c2, lse_q2 - tref);
+                                const float ri = (i < n && delta2 > 0.f)
+                                                     ? exp2f(fmaf(ti, c2, -tref)) * (delta2 > 24.f ? 1.f : -expm1f(-delta2 * kLn2))
+                                                     : 0.f;
+                                r[i] = ri;
+                                R += ri;
+                            }
+                            const float key = off + log2f(R) - log2f(neg_log_uniform(w.x));
+                            if (R > 0.f && key > kbest_r) {
+                                // the token: inverse CDF in group order
+                                const float target = word_to_uniform(w.y) * R;
+                                int x = -1, last = 0;
+                                float run = 0.f;
 #pragma unroll
-                                for (int c = 0; c < 4; ++c) {
-                                    const int i0 = c, i1 = 4 + c, i2 = 8 + c, i3 = 12 + c;
-                                    const float ti = g == 0 ? bf16_at(ct_lo, ct_hi, i0)
-                                                            : (g == 1 ? bf16_at(ct_lo, ct_hi, i1)
-                                                                      : (g == 2 ? bf16_at(ct_lo, ct_hi, i2)
-                                                                                : bf16_at(ct_lo, ct_hi, i3)));
-                                    const float zi = g == 0 ? z[i0] : (g == 1 ? z[i1] : (g == 2 ? z[i2] : z[i3]));
-                                    const float pv = fast_exp2(fmaf(ti, c2, -lse_t2));
-                                    const float qv = fast_exp2(fmaf(zi, c2, -lse_q2));
-                                    const float rbi = (active && 4 * g + c < n) ? (pv - qv) + 4e-7f * (pv + qv) : 0.f;
-                                    const uint32_t word = word_of(wg, c);
-                                    if (!(one_minus_uniform_plus_one(word) < fmaf(rbi, Qr, 1.f))) continue;
-                                    // log2(p - q) = log2 p + log2(1 - 2^-delta), with delta = log2 p -
-                                    // log2 q formed from the logit difference first (+inf for bonus rows)
-                                    const float delta2 = fmaf(ti - zi, c2, lse_q2 - lse_t2);
-                                    if (!(delta2 > 0.f)) continue;
-                                    const float l1 = delta2 > 24.f ? 0.f : fast_log2(-expm1f(-delta2 * kLn2));
-                                    const float key = fmaf(ti, c2, -lse_t2) + l1 - fast_log2(neg_log_uniform(word));
-                                    if (key > rs.key_res) {
-                                        rs.key_res = key;
-                                        rs.idx_res = v + 4 * g + c;
-                                    }
+                                for (int i = 0; i < 16; ++i) {
+                                    run += r[i];
+                                    if (r[i] > 0.f) last = i;
+                                    if (x < 0 && run > target) x = i;
                                 }
+                                if (x < 0) x = last;  // target rounded up to the group's sum
+                                rs.key_res = key;
+                                rs.idx_res = v + x;
+                                kbest_r = key;
+                                atomicMax(res_best, key_to_ordered(key));
                             }
-                            if (rs.key_res > kbest_r) {
-                                kbest_r = rs.key_res;
-                                atomicMax(res_best, key_to_ordered(kbest_r));
-                            }
-                            Qr = fminf(fast_exp2(-kbest_r), kQMax) * kMargin;
                         }
                         // the row-wide word for the next sub-slice, after this one's publication
                         if (active) kr_next = load_relaxed(res_best);

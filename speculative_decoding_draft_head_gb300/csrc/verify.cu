@@ -38,8 +38,6 @@ __device__ __forceinline__ ResidualState residual_warp_merge(ResidualState s) {
         ResidualState o;
         o.key_res = __shfl_xor_sync(0xffffffffu, s.key_res, mask);
         o.idx_res = __shfl_xor_sync(0xffffffffu, s.idx_res, mask);
-        o.key_p = __shfl_xor_sync(0xffffffffu, s.key_p, mask);
-        o.idx_p = __shfl_xor_sync(0xffffffffu, s.idx_p, mask);
         residual_merge(s, o);
     }
     return s;
@@ -259,7 +257,7 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__
     const float c2 = kLog2e / temperature[b];
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     const bool residual = (kind == 1);
-    const float lse_q2 = residual ? draft_lse[(size_t)b * G + d] * kLog2e : 0.f;
+    const float lse_q2 = residual ? draft_lse[(size_t)b * G + d] * kLog2e : INFINITY;
     const float lse_t2 = residual ? lse_t_row[b] : 0.f;
     if (residual && !z_in) {
         const int prev = (d == 0) ? anchor[b] : draft_tokens[(size_t)b * G + d - 1];
@@ -269,14 +267,25 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__
     const size_t drow = (size_t)b * G + d;
     const TIn *t_row = target + ((size_t)b * (G + 1) + d) * V;
     const uint32_t stream = residual ? kStreamResidual : kStreamBonus;
-    const int vb = seg * chunk;
+    const int vb = seg * chunk;  // a multiple of 16: whole draw groups
     const int ve = min(V, vb + chunk);
+    const int lane = threadIdx.x & 31;
     ResidualState st = residual_init();
-    for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kResThreads) {
-        const float4 t4 = load4(t_row + v);
-        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, stream), k0, k1);
+    // One 16-token draw group (R2b) per quad of lanes, four tokens each.  A
+    // residual row weighs token v by r_v = p_v - q_v where positive (p and q
+    // normalised); a bonus row by 2^(t_v c2 - tref) with the group's maximum
+    // as tref.  Every thread runs the same iterations (the quads shuffle).
+    for (int vbase = vb; vbase < ve; vbase += 4 * kResThreads) {
+        const int v = vbase + 4 * threadIdx.x;
+        const bool valid = v < ve;  // V % 8 == 0: all four tokens or none
+        float t[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float z[4] = {0.f, 0.f, 0.f, 0.f};
-        if (residual) {
+        if (valid) {
+            const float4 t4 = load4(t_row + v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) t[e] = elem(t4, e);
+        }
+        if (valid && residual) {
             if (z_in) {
                 const float4 z4 = *reinterpret_cast<const float4 *>(z_in + drow * V + v);
                 z[0] = z4.x; z[1] = z4.y; z[2] = z4.z; z[3] = z4.w;
@@ -287,12 +296,12 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float4 w = load4(w_out + (size_t)(v + e) * r + k);
-                        float t = acc[e];
-                        t = fmaf(a.x, w.x, t);
-                        t = fmaf(a.y, w.y, t);
-                        t = fmaf(a.z, w.z, t);
-                        t = fmaf(a.w, w.w, t);
-                        acc[e] = t;
+                        float x = acc[e];
+                        x = fmaf(a.x, w.x, x);
+                        x = fmaf(a.y, w.y, x);
+                        x = fmaf(a.z, w.z, x);
+                        x = fmaf(a.w, w.w, x);
+                        acc[e] = x;
                     }
                 }
                 const float4 u4 = load4(base + drow * V + v);
@@ -300,46 +309,66 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__
                 for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[e];
             }
         }
+        float tref = lse_t2, off = 0.f;
+        if (!residual) {
+            float tm = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+            tref = off = tm * c2;
+        }
+        float w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float t = elem(t4, e);
-            const uint32_t word = word_of(w4, e);
-            const float lw = fast_log2(word_to_one_minus_uniform(word));
-            const float base_p = t * c2;
-            if (!residual) {  // bonus: Gumbel-max over t / T
-                if (lw < base_p - st.key_res + 1e-4f) {
-                    const float key = base_p - fast_log2(neg_log_uniform(word));
-                    if (key_better(key, v + e, st.key_res, st.idx_res)) {
-                        st.key_res = key;
-                        st.idx_res = v + e;
-                    }
-                }
-                continue;
-            }
-            // log2 p - log2 q, from the logit difference first
-            const float delta2 = fmaf(t - z[e], c2, lse_q2 - lse_t2);
-            if (delta2 > 0.f) {
-                const float l1 = delta2 > 20.f ? delta2 : fast_log2(expm1f(delta2 * kLn2));
-                const float base_r = fmaf(z[e], c2, -lse_q2) + l1;
-                if (lw < base_r - st.key_res + 1e-4f) {
-                    const float key = base_r - fast_log2(neg_log_uniform(word));
-                    if (key_better(key, v + e, st.key_res, st.idx_res)) {
-                        st.key_res = key;
-                        st.idx_res = v + e;
-                    }
+            float we = 0.f;
+            if (valid) {
+                if (residual) {
+                    // p (1 - 2^-delta), delta = log2 p - log2 q from the logits first
+                    const float delta2 = fmaf(t[e] - z[e], c2, lse_q2 - lse_t2);
+                    if (delta2 > 0.f)
+                        we = exp2f(fmaf(t[e], c2, -lse_t2)) * (delta2 > 24.f ? 1.f : -expm1f(-delta2 * kLn2));
+                } else {
+                    we = exp2f(fmaf(t[e], c2, -tref));
                 }
             }
-            if (lw < base_p - st.key_p + 1e-4f) {
-                const float key = base_p - fast_log2(neg_log_uniform(word));
-                if (key_better(key, v + e, st.key_p, st.idx_p)) {
-                    st.key_p = key;
-                    st.idx_p = v + e;
-                }
-            }
+            w4[e] = we;
         }
+        float gs = ((w4[0] + w4[1]) + w4[2]) + w4[3];
+        gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+        gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+        const bool leader = (lane & 3) == 0;
+        bool take = false;
+        float key = -INFINITY;
+        uint4 wd = make_uint4(0u, 0u, 0u, 0u);
+        if (leader && valid && gs > 0.f) {
+            wd = philox4x32_10(make_uint4((uint32_t)v >> 4, (uint32_t)d, id, stream), k0, k1);
+            key = off + log2f(gs) - log2f(neg_log_uniform(wd.x));
+            take = key > st.key_res;  // an exact tie keeps the earlier, lower-numbered group
+        }
+        if (!__any_sync(0xffffffffu, take)) continue;
+        float wq[16];
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) wq[4 * qd + e] = __shfl_sync(0xffffffffu, w4[e], (lane & ~3) + qd);
+        if (!take) continue;
+        float run = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) run += wq[i2];
+        const float target = word_to_uniform(wd.y) * run;
+        int x = -1, last = 0;
+        run = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) {
+            run += wq[i2];
+            if (wq[i2] > 0.f) last = i2;
+            if (x < 0 && run > target) x = i2;
+        }
+        if (x < 0) x = last;  // target rounded up to the group's sum
+        st.key_res = key;
+        st.idx_res = v + x;
     }
     st = residual_warp_merge(st);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     if (lane == 0) scratch[warp] = st;
     __syncthreads();
     if (warp == 0) {
@@ -352,7 +381,7 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__
 // One warp per request with a final draw: merge the partials, emit the token.
 // If a residual row had no entry with p > q at all (impossible in exact
 // arithmetic after a rejection), the token is drawn from p with the residual
-// stream instead, scanning the target row here.
+// stream instead (a group draw over the target row, here).
 template <typename TIn>
 __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part, int nsplit,
                                           const int32_t *__restrict__ final_code,
@@ -368,26 +397,54 @@ __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part
     ResidualState s = residual_init();
     for (int i = lane; i < nsplit; i += 32) residual_merge(s, part[(size_t)b * nsplit + i]);
     s = residual_warp_merge(s);
-    int y = (s.idx_res != INT32_MAX) ? s.idx_res : s.idx_p;
-    if (y == INT32_MAX) {  // degenerate residual: draw from p
+    int y = s.idx_res;
+    if (y == INT32_MAX) {  // degenerate residual: a group draw from p (stream 2)
         const int d = code & 0xFFFF;
         const float c2 = kLog2e / temperature[b];
         const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
         const TIn *t_row = target + ((size_t)b * (G + 1) + d) * V;
-        ResidualState f = residual_init();
-        for (int v = 4 * lane; v < V; v += 128) {
-            const uint4 w4 = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, kStreamResidual), k0, k1);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float key = to_f32(t_row[v + e]) * c2 - fast_log2(neg_log_uniform(word_of(w4, e)));
-                if (key_better(key, v + e, f.key_p, f.idx_p)) {
-                    f.key_p = key;
-                    f.idx_p = v + e;
-                }
+        // each lane keys its own groups, then the warp keeps the best (lowest
+        // group on ties) and resolves its token
+        float kb = -INFINITY;
+        int gb = INT32_MAX;
+        for (int g0 = 16 * lane; g0 < V; g0 += 16 * 32) {
+            const int g1 = min(g0 + 16, V);
+            float m = -INFINITY;
+            for (int v = g0; v < g1; ++v) m = fmaxf(m, to_f32(t_row[v]) * c2);
+            float S = 0.f;
+            for (int v = g0; v < g1; ++v) S += exp2f(fmaf(to_f32(t_row[v]), c2, -m));
+            const uint4 wd = philox4x32_10(make_uint4((uint32_t)g0 >> 4, (uint32_t)d, id, kStreamResidual), k0, k1);
+            const float key = m + log2f(S) - log2f(neg_log_uniform(wd.x));
+            if (key > kb) {
+                kb = key;
+                gb = g0;
             }
         }
-        f = residual_warp_merge(f);
-        y = f.idx_p;
+#pragma unroll
+        for (int mask = 16; mask > 0; mask >>= 1) {
+            const float ko = __shfl_xor_sync(0xffffffffu, kb, mask);
+            const int go = __shfl_xor_sync(0xffffffffu, gb, mask);
+            if (key_better(ko, go, kb, gb)) {
+                kb = ko;
+                gb = go;
+            }
+        }
+        const int g1 = min(gb + 16, V);
+        float m = -INFINITY;
+        for (int v = gb; v < g1; ++v) m = fmaxf(m, to_f32(t_row[v]) * c2);
+        float S = 0.f;
+        for (int v = gb; v < g1; ++v) S += exp2f(fmaf(to_f32(t_row[v]), c2, -m));
+        const uint4 wd = philox4x32_10(make_uint4((uint32_t)gb >> 4, (uint32_t)d, id, kStreamResidual), k0, k1);
+        const float tgt = word_to_uniform(wd.y) * S;
+        float run = 0.f;
+        y = g1 - 1;
+        for (int v = gb; v < g1; ++v) {
+            run += exp2f(fmaf(to_f32(t_row[v]), c2, -m));
+            if (run > tgt) {
+                y = v;
+                break;
+            }
+        }
     }
     if (lane == 0) out_tokens[(size_t)b * (G + 1) + accept_len[b]] = y;
 }
@@ -461,7 +518,7 @@ VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {
     long want_r = (2L * kNumSMs + B - 1) / B;
     int max_r = (V + 1023) / 1024;
     int rs = (int)(want_r < 1 ? 1 : (want_r > max_r ? max_r : want_r));
-    int rchunk = ((V + rs - 1) / rs + 3) / 4 * 4;
+    int rchunk = ((V + rs - 1) / rs + 15) / 16 * 16;  // whole draw groups per segment
     p.res_chunk = rchunk;
     p.res_split = (V + rchunk - 1) / rchunk;
     p.res_split_tc = p.tensor_residual ? tc_segments(B, V) : 0;

@@ -173,7 +173,7 @@ def compare_verify(g, o, temps, reqs, skip):
             t.failures.append("accepted prefix b=%d" % b)
         if go[b, ka] != o["out_tokens"][i, ko]:
             gap, top = o["final_gap"][i], o["final_top"][i]
-            if gap <= TIE_GUMBEL * max(1.0, abs(top)):
+            if gap <= TIE_GUMBEL * max(1.0, abs(top)) or o["final_cdf"][i] <= TIE_CDF:
                 t.exempt += 1
             else:
                 t.failures.append("final token b=%d gpu=%d oracle=%d kind=%d gap=%.3g" %

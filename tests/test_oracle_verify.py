@@ -279,3 +279,34 @@ def test_markov_head_fixes_the_multimodal_collision():
         results[head] = (v["accept_len"] == 2).mean()
     assert abs(results["parallel"] - 0.5) < 4 * math.sqrt(0.25 / N)
     assert results["markov"] == 1.0
+
+
+def test_first_emitted_token_is_distributed_as_target_across_draw_groups():
+    """Residual and bonus draws over several 16-token groups and a ragged one.
+
+    One draft position (L = 1): the first emitted token is the accepted draft
+    token or the residual draw, and must have law p0; when the draft token is
+    accepted, the second emitted token is the bonus draw from p1.  Both draws
+    are group draws on V = 40 (groups of 16, 16 and 8 tokens); p0 and q0 are
+    chosen so that the residual puts mass in every group.
+    """
+    V, N, seed = 40, 300000, 23
+    rng = np.random.default_rng(31)
+    p0 = _softmax(rng.normal(0, 1.0, V))
+    q0 = _softmax(rng.normal(0, 1.0, V))
+    p1 = _softmax(rng.normal(0, 1.5, V))
+    d, v = _run([p0, p1], [q0], N, seed, L=1)
+    first = v["out_tokens"][:, 0]
+    ok, chi2 = _chi2_ok(np.bincount(first, minlength=V), p0, N)
+    assert ok, chi2
+    resid = np.maximum(p0 - q0, 0)
+    assert all(resid[a:a + 16].sum() > 0.01 for a in (0, 16, 32))
+    acc = v["accept_len"] == 1
+    assert 0.3 < acc.mean() < 0.9
+    ok, chi2 = _chi2_ok(np.bincount(v["out_tokens"][acc, 1], minlength=V), p1, int(acc.sum()))
+    assert ok, chi2
+    rej = ~acc
+    ok, chi2 = _chi2_ok(np.bincount(first[rej], minlength=V), resid / resid.sum(), int(rej.sum()))
+    assert ok, chi2
+    assert np.all(v["final_kind"][rej] == 1) and np.all(v["final_kind"][acc] == 0)
+    assert np.all((v["final_cdf"] >= 0) & (v["final_cdf"] <= 1))
