@@ -101,7 +101,7 @@ constexpr uint32_t kOffBar = kOffMerge + kMergeBytes;
 constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs + 1;
 static_assert(kNumBars * 8 <= 256, "barrier region");
 constexpr uint32_t kOffMisc = kOffBar + 256;
-constexpr uint32_t kMiscBytes = 16 + BM * 16;
+constexpr uint32_t kMiscBytes = 16 + BM * 20;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kTmemA + 128 <= kTmemCols, "TMEM accumulators and A operand");
@@ -231,9 +231,12 @@ __device__ __forceinline__ float sum16(const float (&e)[16]) {
 // another thread published in the row's best word), K_g > K needs
 // -ln u0 < sum Q, hence (1 - u0) < sum Q: a group that fails the conservative
 // form f1 < fl(sum Q + 1) cannot win and costs no logarithm.  A new best is
-// published with atomicMax; readers see it a sub-slice later.
+// published with atomicMax twice: to the CTA's per-row word in shared memory
+// (read by the quadrant's warps before each sub-slice) and to the row-wide
+// word in global memory (read every other sub-slice).
 __device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
-                                              int n, int v, bool on, unsigned long long *best, const uint4 &w) {
+                                              int n, int v, bool on, unsigned long long *best, uint32_t *cta_best,
+                                              const uint4 &w) {
     const bool full = (n == 16);  // warp-uniform
     float e[16];
     float sum = 0.f;
@@ -303,6 +306,7 @@ __device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbe
             st.s_at = zx * c2;
             st.idx = v + x;
             kbest = key;
+            atomicMax(cta_best, key_to_ordered(key));
             atomicMax(best, best_encode(key, v + x));
             Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
@@ -364,6 +368,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     float *row_c2 = reinterpret_cast<float *>(misc + 4 + BM);
     uint32_t *row_rid = reinterpret_cast<uint32_t *>(misc + 4 + 2 * BM);
     int *row_code = misc + 4 + 3 * BM;  // final draw: kind << 16 | position; draft: temperature valid
+    // draft: the best key of each row found in this CTA during the position
+    // (ordered encoding, 0 = none), shared by the quadrant's four warps
+    uint32_t *row_kbest = reinterpret_cast<uint32_t *>(misc + 4 + 4 * BM);
 
     // one position of the recurrent head: launched as a programmatic
     // dependent of the state kernel, so the set-up and the first W_out and
@@ -426,6 +433,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         row_c2[threadIdx.x] = c2;
         row_rid[threadIdx.x] = id;
         row_code[threadIdx.x] = code;
+        row_kbest[threadIdx.x] = 0u;
     }
     if (!kFinal && warp < kEpiWarps && threadIdx.x < 16 * 8) {
         // identity row n (16 rows of 128 bytes): a single 1.0 at k = n;
@@ -719,19 +727,21 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         }
                         const bool on = active && c2 > 0.f;
                         if (on) {
-                            // the row-wide best key loaded one sub-slice earlier (the high
-                            // word of the row's best)
-                            const float kg = ordered_to_key(kg_next);
+                            // the best key known for the row: this CTA's (shared memory,
+                            // current) or the row-wide word's high half (global, loaded
+                            // two sub-slices earlier)
+                            const float kg = ordered_to_key(max(kg_next, *(volatile uint32_t *)(row_kbest + row)));
                             if (kg > kbest) {
                                 kbest = kg;
                                 Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
                             }
                         }
-                        draft_group16(st, Q, kbest, z, c2, n, v, on, best, w);
-                        // reload it for the next sub-slice, after this one's publications
-                        // (at the start of a position the other threads are publishing
-                        // their first batches now)
-                        if (on) kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
+                        draft_group16(st, Q, kbest, z, c2, n, v, on, best, row_kbest + row, w);
+                        // reload the row-wide word every other sub-slice of this warp,
+                        // after this one's publications (at the start of a position the
+                        // other CTAs are publishing their first groups now)
+                        if (on && ((si / kEpiPerQuad) & 1))
+                            kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
                     } else {
                         // take this sub-slice's prefetched values, then prefetch the next
                         // one's (before any skip: the skipped sub-slice may come first
@@ -839,6 +849,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     for (int s2 = 1; s2 < kEpiPerQuad; ++s2) row_state_merge(st, ms[row * kEpiPerQuad + s2]);
                     p.part[((size_t)jj * p.B + b) * p.nseg + seg] = st;
                     if (st.idx != INT32_MAX) atomicMax(best, best_encode(st.key, st.idx));
+                    row_kbest[row] = 0u;  // the next position's (every warp is past its last read)
                 } else if (active) {
                     const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);
                     for (int s2 = 1; s2 < kEpiPerQuad; ++s2) residual_merge(rs, ms[row * kEpiPerQuad + s2]);
