@@ -326,17 +326,41 @@ def run_ours(args, w):
         rnn_ms = statistics.median(samples)
         del head
 
-    # end to end: per-round inputs from pinned host memory, emitted tokens back
-    per_round = ("base", "target", "anchor", "temperature", "request_id", "conf_logits")
+    # End to end: every step's inputs come from pinned host memory and the
+    # emitted tokens go back.  The base logits and the small per-request inputs
+    # are copied whole (double-buffered: step i + 1's copies run on a copy
+    # stream while step i computes); of the target logits only the rows the
+    # scheduler admitted, rows 0 .. L_b of each request, cross the host link:
+    # dspark_pack_target gathers them from host memory on the device after the
+    # schedule, and verification reads the packed rows.  The host link (about
+    # 210 GB/s, copy engine or kernel reads alike) is the bound.
+    per_round = ("base", "anchor", "temperature", "request_id", "conf_logits")
     host = {k: inp[k].cpu().pin_memory() for k in per_round}
+    host_target = inp["target"].cpu().pin_memory()
     out_host = dict(out_tokens=torch.empty((B, G + 1), dtype=torch.int32).pin_memory(),
                     num_out=torch.empty((B,), dtype=torch.int32).pin_memory())
-    h2d = sum(host[k].numel() * host[k].element_size() for k in per_round)
+    target_rows = int((np.asarray(vl_host) + 1).sum()) if w.scheduler else B * (G + 1)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in per_round) + \
+        target_rows * V * host_target.element_size()
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    pk_out = dict(target=torch.empty((B * (G + 1), V), dtype=host_target.dtype, device=dev),
+                  row0=torch.empty((B,), dtype=torch.int64, device=dev),
+                  n_rows=torch.empty((1,), dtype=torch.int64, device=dev))
+    vl_full = torch.full((B,), G, dtype=torch.int32, device=dev)
 
-    # Double-buffered: the copies of step i + 1 run on a copy stream while step i
-    # computes (every step still copies its whole input from pinned host memory,
-    # inside the timed region; H2D is the bound at about 200 GB/s).
+    def step_e2e(x):
+        binding.draft_sample(x["base"], x["e_in"], x["w_out"], x["anchor"], x["temperature"],
+                             x["request_id"], args.seed, out=d_out, workspace=ws_d, stream=stream)
+        vl = vl_full
+        if w.scheduler:
+            binding.schedule_prefix(x["conf_logits"], x["pos_temp"], x["sps"], w.L_min, G, out=s_out,
+                                    workspace=ws_s, stream=stream)
+            vl = s_out["verify_len"]
+        binding.pack_target(host_target, vl, out=pk_out, stream=stream)
+        binding.verify(pk_out["target"], x["base"], x["e_in"], x["w_out"], x["anchor"], d_out, vl,
+                       x["temperature"], x["request_id"], args.seed, target_row0=pk_out["row0"], out=v_out,
+                       workspace=ws_v, stream=stream)
+
     copy_stream = torch.cuda.Stream(dev)
     bufs = [{k: (inp[k].clone() if k in per_round else inp[k]) for k in inp} for _ in range(2)]
     ev_copied = [torch.cuda.Event() for _ in range(2)]
@@ -361,7 +385,7 @@ def run_ours(args, w):
                 issue_copy(i + 1)
             b = i % 2
             stream.wait_event(ev_copied[b])
-            step(bufs[b])
+            step_e2e(bufs[b])
             ev_used[b].record(stream)
             used_recorded[b] = True
             out_host["out_tokens"].copy_(v_out["out_tokens"], non_blocking=True)
@@ -424,8 +448,11 @@ def run_ours(args, w):
                        tflops_over_draft_time=bias_flops / (d_ms / 1000.0) / 1e12,
                        peak_tflops=peaks["bf16_tflops_sustained"]),
         e2e=dict(value=e_value, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
-                 ms_per_step=e_ms, copies="pinned host -> device each step, overlapped with the previous "
-                                         "step's compute (two input buffers, a copy stream)"),
+                 ms_per_step=e_ms,
+                 copies="every step from pinned host memory: base logits and per-request inputs copied "
+                        "whole (overlapped with the previous step, two buffers, a copy stream); target "
+                        "logits only for the scheduled rows 0..L_b of each request (%d of %d rows), "
+                        "gathered on the device by dspark_pack_target" % (target_rows, B * (G + 1))),
         gpu_launches=args.steps * (launches_draft + (1 if w.scheduler else 0) + 4),
         clocks=clk,
     )

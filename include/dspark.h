@@ -84,7 +84,8 @@ enum {
     DSPARK_FLAG_BAD_TEMPERATURE = 2u,  /* a temperature that is negative, NaN or inf */
     DSPARK_FLAG_BAD_VERIFY_LEN = 4u,   /* a verify length outside [0, G] */
     DSPARK_FLAG_BAD_POS_TEMP = 8u,     /* a calibration temperature <= 0 or NaN */
-    DSPARK_FLAG_TIMEOUT = 16u          /* a bounded device-side wait gave up */
+    DSPARK_FLAG_TIMEOUT = 16u,         /* a bounded device-side wait gave up */
+    DSPARK_FLAG_BAD_TARGET_ROW = 32u   /* a packed target row outside the array */
 };
 
 /* Library version, major * 10000 + minor * 100 + patch. */
@@ -112,9 +113,13 @@ DSPARK_API size_t dspark_workspace_bytes(int which, int B, int G, int V, int r);
  * For each request b and j = 0 .. G-1, with prev = anchor[b] (j = 0) or
  * draft_tokens[b][j-1]:
  *   z[v]  = base_logits[b][j][v] + sum_k e_in[prev][k] * w_out[k][v]   (fp32)
- *   T > 0: s = z / T, lse = log sum exp s, x_j = argmax_v s[v] + g_v with
- *          g_v = -ln(-ln u(seed, request_id[b], j, v, stream 0)),
- *          logq = s[x_j] - lse
+ *   T > 0: s = z / T, lse = log sum exp s, x_j drawn from softmax(s) by the
+ *          group draw: with groups of 16 consecutive tokens (the last one may
+ *          be ragged) and u0 = u(seed, request_id[b], j, 4 g, stream 0),
+ *          u1 = u(.., 4 g + 1, stream 0) (words 0 and 1 of group g's Philox
+ *          block), the group g* with the largest log sum_{v in g} exp s[v] -
+ *          ln(-ln u0) wins and x_j is its first token whose running sum of
+ *          exp s exceeds u1 times the group's sum; logq = s[x_j] - lse
  *   T = 0: x_j = argmax_v z[v] (lowest id on ties), lse = max z, logq = 0
  *
  * base_logits [B][G][V] dtype   e_in [V][r] dtype   w_out [V][r] dtype (row v
@@ -246,12 +251,13 @@ DSPARK_API dspark_status dspark_schedule_policy(
  *   p_j = softmax(target[b][j] / T), q_j = the draft distribution (from the
  *   draft's logq and lse);
  *   accept x_j while u(seed, id, j, 0, stream 1) < min(1, p_j(x_j)/q_j(x_j));
- *   at the first rejection d: y = argmax over {v : p_d(v) > q_d(v)} of
- *   ln(p_d(v) - q_d(v)) + g(u(seed, id, d, v, stream 2))  (the draft logits
- *   of row d are recomputed from base_logits, e_in and w_out, or read from
- *   draft_logits when it is not NULL);
- *   if all L are accepted: y = argmax_v target[b][L][v] / T +
- *   g(u(seed, id, L, v, stream 3)).
+ *   at the first rejection d: y is drawn from normalise(max(0, p_d - q_d)) by
+ *   the group draw of dspark_draft_sample (weights max(0, p - q), stream 2;
+ *   from p_d itself if no entry has p > q) (the draft logits of row d are
+ *   recomputed from base_logits, e_in and w_out, or read from draft_logits
+ *   when it is not NULL);
+ *   if all L are accepted: y is drawn from softmax(target[b][L] / T) by the
+ *   group draw on stream 3.
  * T = 0: accept while x_j == argmax target[b][j]; y = that argmax at the first
  * mismatch, else argmax target[b][L].
  *
@@ -276,6 +282,47 @@ DSPARK_API dspark_status dspark_verify(
     int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
     float *target_lse, float *logp_sel,
     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * dspark_verify on a packed target: only the rows verification reads.
+ *
+ * The scheduler of "DSpark, la bozza che sa quando fermarsi" (paithon.it),
+ * section "Verificare meglio, non di piu'", sizes the target's batch by the
+ * verify lengths: request b needs target rows 0 .. L_b (L_b = verify_len[b]),
+ * sum_b (L_b + 1) rows in all, not B (G + 1).  Here request b's row j is row
+ * target_row0[b] + j of target_logits [n_target_rows][V]; rows 0 .. L_b must
+ * lie inside the array (else the request's outputs are marked as for a bad
+ * token and DSPARK_FLAG_BAD_TARGET_ROW is raised).  target_row0 [B] int64 is a
+ * device array.  Everything else, the results included, is dspark_verify's.
+ */
+DSPARK_API dspark_status dspark_verify_packed(
+    const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
+    const void *base_logits, const void *e_in, const void *w_out,
+    const float *draft_logits, const int32_t *anchor, const int32_t *draft_tokens,
+    const float *draft_lse, const float *draft_logq, const int32_t *verify_len,
+    const float *temperature, const uint32_t *request_id, int B, int G, int V, int r,
+    dspark_dtype dtype, uint64_t seed, int32_t *accept_len, int32_t *out_tokens,
+    int32_t *num_out, float *target_lse, float *logp_sel, void *workspace,
+    size_t workspace_bytes, void *stream);
+
+/*
+ * Gather the target rows verification reads into the packed layout.
+ *
+ * For each request b with L_b = verify_len[b] (G if verify_len is NULL),
+ * copies rows 0 .. L_b of target_logits [B][G+1][V] (dtype) to
+ * target_packed, requests in order: target_row0[b] = sum_{b' < b} (L_b' + 1),
+ * and n_rows[0] = sum_b (L_b + 1) when n_rows is not NULL.  A request with an
+ * invalid length contributes no row (dspark_verify_packed flags it).
+ * target_logits may be device memory or pinned host memory mapped into the
+ * device's address space; then only these rows cross the host link.
+ * target_packed needs room for B (G+1) rows; verify_len, target_row0
+ * ([B] int64) and n_rows ([1] int64) are device arrays.  Nothing is read back
+ * to the host: pass n_target_rows = B (G+1) (the buffer's size) to
+ * dspark_verify_packed.
+ */
+DSPARK_API dspark_status dspark_pack_target(
+    const void *target_logits, const int32_t *verify_len, int B, int G, int V, dspark_dtype dtype,
+    void *target_packed, int64_t *target_row0, int64_t *n_rows, void *stream);
 
 /*
  * dspark_verify without a workspace argument, for callers that cannot

@@ -25,10 +25,12 @@ FLAG_BAD_TOKEN = 1
 FLAG_BAD_TEMPERATURE = 2
 FLAG_BAD_VERIFY_LEN = 4
 FLAG_BAD_POS_TEMP = 8
+FLAG_TIMEOUT = 16
+FLAG_BAD_TARGET_ROW = 32
 
 EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
            "dspark_schedule_prefix", "dspark_schedule_policy", "dspark_verify", "dspark_read_device_flags",
-           "dspark_verify_noalloc", "dspark_draft_sample_rnn")
+           "dspark_verify_noalloc", "dspark_draft_sample_rnn", "dspark_verify_packed", "dspark_pack_target")
 
 _lib = None
 _lock = threading.Lock()
@@ -78,6 +80,10 @@ def load(build_if_missing: bool = True):
         L.dspark_verify.restype = ctypes.c_int
         L.dspark_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                     i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dspark_verify_packed.restype = ctypes.c_int
+        L.dspark_verify_packed.argtypes = [vp, vp, ctypes.c_int64] + L.dspark_verify.argtypes[1:]
+        L.dspark_pack_target.restype = ctypes.c_int
+        L.dspark_pack_target.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.dspark_verify_noalloc.restype = ctypes.c_int
         L.dspark_verify_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                             i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp]
@@ -258,16 +264,24 @@ def schedule_prefix(conf_logits, pos_temp, sps, L_min, L_max, *, policy=SCHED_EA
 
 
 def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, request_id=None,
-           seed=0, *, draft_logits=None, out=None, workspace=None, stream=None):
+           seed=0, *, draft_logits=None, target_row0=None, out=None, workspace=None, stream=None):
     """Verify one drafted block per request.
 
-    ``draft`` is the dict returned by :func:`draft_sample`.  Returns
-    dict(accept_len, out_tokens, num_out, target_lse, logp)."""
+    ``draft`` is the dict returned by :func:`draft_sample`.  ``target`` is
+    [B, G+1, V], or with ``target_row0`` ([B] int64) the packed rows [n, V]
+    (request b's row j at row target_row0[b] + j, see dspark_verify_packed).
+    Returns dict(accept_len, out_tokens, num_out, target_lse, logp)."""
     lib = load()
-    B, G1, V = target.shape
-    G = G1 - 1
+    B, G = draft["tokens"].shape
+    V = target.shape[-1]
     dev = target.device
-    _need(target, "target", device=dev)
+    if target_row0 is None:
+        _need(target, "target", shape=(B, G + 1, V), device=dev)
+    else:
+        _need(target, "target", device=dev)
+        if target.dim() != 2:
+            raise ValueError("a packed target is [rows, V]")
+        _need(target_row0, "target_row0", dtype=torch.int64, shape=(B,), device=dev)
     if draft_logits is None:
         _need(base, "base", dtype=target.dtype, shape=(B, G, V), device=dev)
         _need(e_in, "e_in", dtype=target.dtype, device=dev)
@@ -290,14 +304,43 @@ def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, re
                    target_lse=torch.empty((B, G + 1), dtype=torch.float32, device=dev),
                    logp=torch.empty((B, G), dtype=torch.float32, device=dev))
     ws = workspace if workspace is not None else _default_ws.get(WS_VERIFY, B, G, V, r, dev)
-    _check(lib.dspark_verify(
-        _ptr(target), _ptr(base), _ptr(e_in), _ptr(w_out), _ptr(draft_logits), _ptr(anchor),
-        _ptr(draft["tokens"]), _ptr(draft["lse"]), _ptr(draft["logq"]), _ptr(verify_len),
-        _ptr(temperature), _ptr(rid), B, G, V, r, _dtype_code(target),
-        int(seed) & 0xFFFFFFFFFFFFFFFF,
-        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["num_out"]),
-        _ptr(out.get("target_lse")), _ptr(out.get("logp")), _ptr(ws), ws.numel(),
-        _stream(stream)))
+    args = (_ptr(base), _ptr(e_in), _ptr(w_out), _ptr(draft_logits), _ptr(anchor),
+            _ptr(draft["tokens"]), _ptr(draft["lse"]), _ptr(draft["logq"]), _ptr(verify_len),
+            _ptr(temperature), _ptr(rid), B, G, V, r, _dtype_code(target),
+            int(seed) & 0xFFFFFFFFFFFFFFFF,
+            _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["num_out"]),
+            _ptr(out.get("target_lse")), _ptr(out.get("logp")), _ptr(ws), ws.numel(),
+            _stream(stream))
+    if target_row0 is None:
+        _check(lib.dspark_verify(_ptr(target), *args))
+    else:
+        _check(lib.dspark_verify_packed(_ptr(target), _ptr(target_row0), target.shape[0], *args))
+    return out
+
+
+def pack_target(target, verify_len, *, out=None, stream=None):
+    """Rows 0 .. L_b of every request of ``target`` [B, G+1, V] (device, or
+    pinned host memory, which the device reads directly) packed for
+    :func:`verify` with ``target_row0`` (dspark_pack_target).
+
+    Returns dict(target [B*(G+1), V] with the packed rows first, row0 [B]
+    int64, n_rows [1] int64), all on the device of ``verify_len``."""
+    lib = load()
+    B, G1, V = target.shape
+    dev = verify_len.device if verify_len is not None else torch.device("cuda", torch.cuda.current_device())
+    if not target.is_contiguous():
+        raise ValueError("target must be contiguous")
+    if target.device.type == "cpu" and not target.is_pinned():
+        raise ValueError("a host target must be in pinned memory")
+    if verify_len is not None:
+        _need(verify_len, "verify_len", dtype=torch.int32, shape=(B,), device=dev)
+    if out is None:
+        out = dict(target=torch.empty((B * G1, V), dtype=target.dtype, device=dev),
+                   row0=torch.empty((B,), dtype=torch.int64, device=dev),
+                   n_rows=torch.empty((1,), dtype=torch.int64, device=dev))
+    _check(lib.dspark_pack_target(_ptr(target), _ptr(verify_len), B, G1 - 1, V, _dtype_code(target),
+                                  _ptr(out["target"]), _ptr(out["row0"]), _ptr(out.get("n_rows")),
+                                  _stream(stream)))
     return out
 
 

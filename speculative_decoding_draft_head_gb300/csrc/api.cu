@@ -39,6 +39,40 @@ dspark_status check_ws(void *ws, size_t have, size_t need) {
     return DSPARK_OK;
 }
 
+
+dspark_status verify_impl(const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
+                          const void *base_logits, const void *e_in,
+                            const void *w_out, const float *draft_logits, const int32_t *anchor,
+                            const int32_t *draft_tokens, const float *draft_lse, const float *draft_logq,
+                            const int32_t *verify_len, const float *temperature,
+                            const uint32_t *request_id, int B, int G, int V, int r, dspark_dtype dtype,
+                            uint64_t seed, int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
+                            float *target_lse, float *logp_sel, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    dspark_status st = check_common(B, G, V, r, dtype);
+    if (st != DSPARK_OK) return st;
+    if (!target_logits || !anchor || !draft_tokens || !draft_lse || !draft_logq || !temperature ||
+        !accept_len || !out_tokens || !num_out)
+        return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!draft_logits && (!base_logits || !e_in || !w_out))
+        return fail(DSPARK_ERR_INVALID_ARG, "need draft_logits or (base_logits, e_in, w_out)");
+    if (!aligned(target_logits, 16) || (base_logits && !aligned(base_logits, 16)) ||
+        (e_in && !aligned(e_in, 16)) || (w_out && !aligned(w_out, 16)) ||
+        (draft_logits && !aligned(draft_logits, 16)))
+        return fail(DSPARK_ERR_INVALID_ARG, "logits and weights must be 16-byte aligned");
+    const VerifyPlan plan = plan_verify(B, G, V, r, dtype);
+    if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    VerifyArgs a{target_logits, target_row0, n_target_rows, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens, draft_lse,
+                 draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype, seed, accept_len,
+                 out_tokens, num_out, target_lse, logp_sel, static_cast<unsigned char *>(workspace)};
+    e = launch_verify(a, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+    return DSPARK_OK;
+}
+
 }  // namespace
 }  // namespace dspark
 
@@ -208,27 +242,44 @@ dspark_status dspark_verify(const void *target_logits, const void *base_logits, 
                             uint64_t seed, int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
                             float *target_lse, float *logp_sel, void *workspace, size_t workspace_bytes,
                             void *stream) {
-    dspark_status st = check_common(B, G, V, r, dtype);
-    if (st != DSPARK_OK) return st;
-    if (!target_logits || !anchor || !draft_tokens || !draft_lse || !draft_logq || !temperature ||
-        !accept_len || !out_tokens || !num_out)
+    return verify_impl(target_logits, nullptr, 0, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens,
+                       draft_lse, draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype, seed,
+                       accept_len, out_tokens, num_out, target_lse, logp_sel, workspace, workspace_bytes, stream);
+}
+
+dspark_status dspark_verify_packed(const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
+                                   const void *base_logits, const void *e_in, const void *w_out,
+                                   const float *draft_logits, const int32_t *anchor, const int32_t *draft_tokens,
+                                   const float *draft_lse, const float *draft_logq, const int32_t *verify_len,
+                                   const float *temperature, const uint32_t *request_id, int B, int G, int V, int r,
+                                   dspark_dtype dtype, uint64_t seed, int32_t *accept_len, int32_t *out_tokens,
+                                   int32_t *num_out, float *target_lse, float *logp_sel, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    if (!target_row0) return fail(DSPARK_ERR_INVALID_ARG, "target_row0 is NULL");
+    if (n_target_rows < 1) return fail(DSPARK_ERR_INVALID_ARG, "n_target_rows must be >= 1");
+    if (n_target_rows > (1LL << 40) / (V > 0 ? V : 1))
+        return fail(DSPARK_ERR_INVALID_ARG, "n_target_rows * V too large");
+    return verify_impl(target_logits, target_row0, n_target_rows, base_logits, e_in, w_out, draft_logits, anchor,
+                       draft_tokens, draft_lse, draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype,
+                       seed, accept_len, out_tokens, num_out, target_lse, logp_sel, workspace, workspace_bytes,
+                       stream);
+}
+
+dspark_status dspark_pack_target(const void *target_logits, const int32_t *verify_len, int B, int G, int V,
+                                 dspark_dtype dtype, void *target_packed, int64_t *target_row0, int64_t *n_rows,
+                                 void *stream) {
+    if (B < 1 || G < 1 || G > kMaxG) return fail(DSPARK_ERR_INVALID_ARG, "bad B=%d or G=%d", B, G);
+    if (V < 8 || V % 8 != 0) return fail(DSPARK_ERR_INVALID_ARG, "V must be a positive multiple of 8 (got %d)", V);
+    if (dtype != DSPARK_BF16 && dtype != DSPARK_F32) return fail(DSPARK_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if ((long)B * (G + 1) * (long)V > (1L << 40)) return fail(DSPARK_ERR_INVALID_ARG, "B*(G+1)*V too large");
+    if (!target_logits || !target_packed || !target_row0)
         return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
-    if (!draft_logits && (!base_logits || !e_in || !w_out))
-        return fail(DSPARK_ERR_INVALID_ARG, "need draft_logits or (base_logits, e_in, w_out)");
-    if (!aligned(target_logits, 16) || (base_logits && !aligned(base_logits, 16)) ||
-        (e_in && !aligned(e_in, 16)) || (w_out && !aligned(w_out, 16)) ||
-        (draft_logits && !aligned(draft_logits, 16)))
-        return fail(DSPARK_ERR_INVALID_ARG, "logits and weights must be 16-byte aligned");
-    const VerifyPlan plan = plan_verify(B, G, V, r, dtype);
-    if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
-    VerifyArgs a{target_logits, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens, draft_lse,
-                 draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype, seed, accept_len,
-                 out_tokens, num_out, target_lse, logp_sel, static_cast<unsigned char *>(workspace)};
-    e = launch_verify(a, plan, s);
-    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+    if (!aligned(target_logits, 16) || !aligned(target_packed, 16) || !aligned(target_row0, 8) ||
+        (n_rows && !aligned(n_rows, 8)))
+        return fail(DSPARK_ERR_INVALID_ARG, "target arrays must be 16-byte aligned");
+    cudaError_t e = launch_pack_target(target_logits, verify_len, B, G, V, dtype == DSPARK_BF16 ? 2 : 4,
+                                       target_packed, target_row0, n_rows, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     return DSPARK_OK;
 }
 

@@ -32,6 +32,18 @@ constexpr uint32_t kFlagBadTemperature = 2u;
 constexpr uint32_t kFlagBadVerifyLen = 4u;
 constexpr uint32_t kFlagBadPosTemp = 8u;
 constexpr uint32_t kFlagTimeout = 16u;
+constexpr uint32_t kFlagBadTargetRow = 32u;
+
+// Row j of request b's target logits: the dense layout [B][G+1][V], or the
+// packed one (request b's rows 0, 1, .. from row row0[b] of n_rows rows).
+// nullptr when a packed row falls outside the array.
+template <typename T>
+__device__ __forceinline__ const T *target_row(const T *target, const int64_t *row0, int64_t n_rows, int b, int G,
+                                               int j, int V) {
+    if (!row0) return target + ((size_t)b * (G + 1) + j) * (size_t)V;
+    const int64_t r = row0[b] + j;
+    return (row0[b] >= 0 && r < n_rows) ? target + (size_t)r * (size_t)V : nullptr;
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

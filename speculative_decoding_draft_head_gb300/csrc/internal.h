@@ -41,6 +41,10 @@ struct PerDeviceOnce {
 // Record the message returned by dspark_last_error() and return `st`.
 dspark_status set_last_error(dspark_status st, const char *fmt, ...);
 
+// ----------------------------------------------------------------- pack ----
+cudaError_t launch_pack_target(const void *src, const int32_t *verify_len, int B, int G, int V, size_t elem_bytes,
+                               void *dst, int64_t *row0, int64_t *n_rows, cudaStream_t s);
+
 // ---------------------------------------------------------------- draft ----
 struct DraftPlan {
     bool tensor_path;      // tcgen05 Markov-head kernel (bf16) vs SIMT kernel
@@ -112,6 +116,8 @@ size_t tc_residual_state_bytes();
 // (fully accepted, Gumbel-max over target row L)
 struct FinalArgs {
     const void *target;
+    const int64_t *target_row0;
+    int64_t n_target_rows;
     const void *base;
     const void *e_in;
     const void *w_out;
@@ -150,6 +156,8 @@ VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt);
 
 struct VerifyArgs {
     const void *target;
+    const int64_t *target_row0;  // packed target: request b's row 0 (nullptr: dense [B][G+1][V])
+    int64_t n_target_rows;
     const void *base;
     const void *e_in;
     const void *w_out;

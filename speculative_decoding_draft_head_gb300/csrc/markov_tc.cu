@@ -115,6 +115,8 @@ struct TcParams {
     const __nv_bfloat16 *a_rows;  // draft, one position: A row of request b at a_rows + b r (else E_in[x_{j-1}])
     const __nv_bfloat16 *base;
     const __nv_bfloat16 *target;
+    const int64_t *target_row0;  // final draw: packed target rows (nullptr: dense)
+    int64_t n_target_rows;
     const int32_t *anchor;
     const int32_t *tokens;
     const float *temperature;
@@ -634,7 +636,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             float lse_q2 = 0.f, lse_t2 = 0.f;
             const __nv_bfloat16 *urow = nullptr, *trow = nullptr;
             if (kFinal && active) {
-                trow = p.target + ((size_t)b * (p.G + 1) + fpos) * p.V;
+                trow = target_row(p.target, p.target_row0, p.n_target_rows, b, p.G, fpos, p.V);  // checked by decide
                 if (kind == 1) {
                     urow = p.base + ((size_t)b * p.G + fpos) * p.V;
                     lse_q2 = p.draft_lse[(size_t)b * p.G + fpos] * kLog2e;
@@ -1076,6 +1078,8 @@ cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
     p.base = static_cast<const __nv_bfloat16 *>(a.base);
     p.target = static_cast<const __nv_bfloat16 *>(a.target);
+    p.target_row0 = a.target_row0;
+    p.n_target_rows = a.n_target_rows;
     p.anchor = a.anchor;
     p.tokens = a.tokens;
     p.temperature = a.temperature;

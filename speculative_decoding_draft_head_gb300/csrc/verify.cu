@@ -65,7 +65,8 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
 // ---------------------------------------------------------------- pass 1 ----
 template <typename TIn>
 __global__ void __launch_bounds__(kRowThreads)
-verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ verify_len,
+verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ row0, int64_t n_rows,
+                   const int32_t *__restrict__ verify_len,
                    const float *__restrict__ temperature, int B, int G, int V, int chunk, int nsplit,
                    RowState *__restrict__ part) {
     __shared__ RowState scratch[kRowThreads / 32];
@@ -82,7 +83,8 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
     const int seg = blockIdx.y;
     const int vb = seg * chunk;
     const int ve = min(V, vb + chunk);
-    const TIn *t_row = target + ((size_t)b * (G + 1) + j) * V;
+    const TIn *t_row = target_row(target, row0, n_rows, b, G, j, V);
+    if (!t_row) return;  // flagged by the decide kernel
 
     RowState st = row_state_init();
     if (T > 0.f) {
@@ -120,7 +122,8 @@ verify_rows_kernel(const TIn *__restrict__ target, const int32_t *__restrict__ v
 
 // ---------------------------------------------------------------- pass 2 ----
 template <typename TIn>
-__global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowState *__restrict__ part,
+__global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ row0,
+                                     int64_t n_rows, const RowState *__restrict__ part,
                                      int nsplit, const int32_t *__restrict__ anchor,
                                      const int32_t *__restrict__ draft_tokens,
                                      const float *__restrict__ draft_logq,
@@ -156,6 +159,11 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         }
         if (bad && lane == 0) atomicOr(flags, kFlagBadToken);
     }
+    if (!bad && row0 && !target_row(target, row0, n_rows, b, G, L, V)) {
+        // rows 0 .. L of a packed target must all be inside the array
+        if (lane == 0) atomicOr(flags, kFlagBadTargetRow);
+        bad = true;
+    }
     // clear the per-row outputs of this request
     for (int j = lane; j <= G; j += 32) {
         out_tokens[(size_t)b * (G + 1) + j] = -1;
@@ -183,7 +191,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
         const int x = draft_tokens[(size_t)b * G + j];
         if (T > 0.f) {
             const float lse2 = s.m + log2f(s.S);
-            const float tx = to_f32(target[((size_t)b * (G + 1) + j) * V + x]);
+            const float tx = to_f32(target_row(target, row0, n_rows, b, G, j, V)[x]);
             const float logp = kLn2 * (fmaf(tx, c2, -s.m) - log2f(s.S));
             const float logq = draft_logq[(size_t)b * G + j];
             const uint4 w4 = philox4x32_10(make_uint4(0u, (uint32_t)j, id, kStreamAccept), k0, k1);
@@ -239,7 +247,8 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const RowSt
 // FMAs (fp32 weights); bonus rows draw from the target row L.
 template <typename TIn>
 __global__ void __launch_bounds__(kResThreads)
-verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__ base,
+verify_final_simt_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ row0, int64_t n_rows,
+                         const TIn *__restrict__ base,
                          const TIn *__restrict__ e_in, const TIn *__restrict__ w_out,
                          const float *__restrict__ z_in, const int32_t *__restrict__ anchor,
                          const int32_t *__restrict__ draft_tokens, const float *__restrict__ draft_lse,
@@ -265,7 +274,7 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const TIn *__restrict__
     }
     __syncthreads();
     const size_t drow = (size_t)b * G + d;
-    const TIn *t_row = target + ((size_t)b * (G + 1) + d) * V;
+    const TIn *t_row = target_row(target, row0, n_rows, b, G, d, V);  // checked by the decide kernel
     const uint32_t stream = residual ? kStreamResidual : kStreamBonus;
     const int vb = seg * chunk;  // a multiple of 16: whole draw groups
     const int ve = min(V, vb + chunk);
@@ -386,7 +395,8 @@ template <typename TIn>
 __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part, int nsplit,
                                           const int32_t *__restrict__ final_code,
                                           const int32_t *__restrict__ accept_len,
-                                          const TIn *__restrict__ target, const float *__restrict__ temperature,
+                                          const TIn *__restrict__ target, const int64_t *__restrict__ row0,
+                                          int64_t n_rows, const float *__restrict__ temperature,
                                           const uint32_t *__restrict__ request_id, int B, int G, int V,
                                           uint32_t k0, uint32_t k1, int32_t *__restrict__ out_tokens) {
     const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -402,7 +412,7 @@ __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part
         const int d = code & 0xFFFF;
         const float c2 = kLog2e / temperature[b];
         const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
-        const TIn *t_row = target + ((size_t)b * (G + 1) + d) * V;
+        const TIn *t_row = target_row(target, row0, n_rows, b, G, d, V);
         // each lane keys its own groups, then the warp keeps the best (lowest
         // group on ties) and resolves its token
         float kb = -INFINITY;
@@ -461,12 +471,12 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     const TIn *target = static_cast<const TIn *>(a.target);
 
     verify_rows_kernel<TIn><<<dim3(a.B * (a.G + 1), p.row_split), kRowThreads, 0, s>>>(
-        target, a.verify_len, a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split, row_part);
+        target, a.target_row0, a.n_target_rows, a.verify_len, a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split, row_part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int warps = 4;
     verify_decide_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
-        target, row_part, p.row_split, a.anchor, a.draft_tokens, a.draft_logq, a.verify_len, a.temperature,
+        target, a.target_row0, a.n_target_rows, row_part, p.row_split, a.anchor, a.draft_tokens, a.draft_logq, a.verify_len, a.temperature,
         a.request_id, a.B, a.G, a.V, k0, k1, a.accept_len, a.out_tokens, a.num_out, a.target_lse,
         a.logp_sel, final_code, lse_t_row, res_best, flags);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -474,14 +484,14 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     const int res_nsplit = tensor ? p.res_split_tc : p.res_split;
     if (tensor) {
         // the last draft launch (position G-1) walked in direction G-1: continue from its end
-        FinalArgs fa{a.target, a.base, a.e_in, a.w_out, a.anchor, a.draft_tokens, a.temperature,
+        FinalArgs fa{a.target, a.target_row0, a.n_target_rows, a.base, a.e_in, a.w_out, a.anchor, a.draft_tokens, a.temperature,
                      a.request_id, final_code, lse_t_row, a.draft_lse, a.B, a.G, a.V, a.r, res_nsplit,
                      a.G, a.seed, res_part, res_best, flags};
         e = launch_final_tensor(fa, s);
     } else {
         const size_t smem = sizeof(float) * (size_t)a.r;
         verify_final_simt_kernel<TIn><<<dim3(a.B, p.res_split), kResThreads, smem, s>>>(
-            target, static_cast<const TIn *>(a.base), static_cast<const TIn *>(a.e_in),
+            target, a.target_row0, a.n_target_rows, static_cast<const TIn *>(a.base), static_cast<const TIn *>(a.e_in),
             static_cast<const TIn *>(a.w_out), a.z_in, a.anchor, a.draft_tokens, a.draft_lse,
             a.temperature, a.request_id, final_code, lse_t_row, a.B, a.G, a.V, a.r, k0, k1, p.res_chunk,
             p.res_split, res_part);
@@ -489,7 +499,7 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     }
     if (e != cudaSuccess) return e;
     verify_final_merge_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
-        res_part, res_nsplit, final_code, a.accept_len, target, a.temperature, a.request_id, a.B, a.G,
+        res_part, res_nsplit, final_code, a.accept_len, target, a.target_row0, a.n_target_rows, a.temperature, a.request_id, a.B, a.G,
         a.V, k0, k1, a.out_tokens);
     return cudaGetLastError();
 }
