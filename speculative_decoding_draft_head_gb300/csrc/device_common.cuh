@@ -295,6 +295,17 @@ __device__ __forceinline__ unsigned long long best_encode(float key, int idx) {
     return ((unsigned long long)key_to_ordered(key) << 32) | (unsigned long long)(~(uint32_t)idx);
 }
 __device__ __forceinline__ int best_token(unsigned long long w) { return w ? (int)~(uint32_t)w : -1; }
+// Fire-and-forget maxima (no value returned, so the issuing warp does not
+// wait for the memory system).
+__device__ __forceinline__ void red_max_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_max_shared_u32(uint32_t *p, uint32_t v) {
+    asm volatile("red.shared.max.u32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_max_u32(uint32_t *p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long load_relaxed_u64(const unsigned long long *p) {
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

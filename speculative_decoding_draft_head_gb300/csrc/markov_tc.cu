@@ -233,7 +233,7 @@ __device__ __forceinline__ float sum16(const float (&e)[16]) {
 // another thread published in the row's best word), K_g > K needs
 // -ln u0 < sum Q, hence (1 - u0) < sum Q: a group that fails the conservative
 // form f1 < fl(sum Q + 1) cannot win and costs no logarithm.  A new best is
-// published with atomicMax twice: to the CTA's per-row word in shared memory
+// published with a max reduction twice: to the CTA's per-row word in shared memory
 // (read by the quadrant's warps before each sub-slice) and to the row-wide
 // word in global memory (read every fourth sub-slice).
 __device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
@@ -308,8 +308,8 @@ __device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbe
             st.s_at = zx * c2;
             st.idx = v + x;
             kbest = key;
-            atomicMax(cta_best, key_to_ordered(key));
-            atomicMax(best, best_encode(key, v + x));
+            red_max_shared_u32(cta_best, key_to_ordered(key));
+            red_max_u64(best, best_encode(key, v + x));
             Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
         }
     }
@@ -829,7 +829,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                                 rs.key_res = key;
                                 rs.idx_res = v + x;
                                 kbest_r = key;
-                                atomicMax(res_best, key_to_ordered(key));
+                                red_max_u32(res_best, key_to_ordered(key));
                             }
                         }
                         // the row-wide word for the next sub-slice, after this one's publication
@@ -851,7 +851,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
                     for (int s2 = 1; s2 < kEpiPerQuad; ++s2) row_state_merge(st, ms[row * kEpiPerQuad + s2]);
                     p.part[((size_t)jj * p.B + b) * p.nseg + seg] = st;
-                    if (st.idx != INT32_MAX) atomicMax(best, best_encode(st.key, st.idx));
+                    if (st.idx != INT32_MAX) red_max_u64(best, best_encode(st.key, st.idx));
                     row_kbest[row] = 0u;  // the next position's (every warp is past its last read)
                 } else if (active) {
                     const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);

@@ -21,7 +21,7 @@
 //     decide the lengths here and skip to 5;
 //  2. tau_0 and the candidate list (a, j, b) for L_min <= j < L_max;
 //  3. bitonic sort in shared memory by (a desc, j asc, b asc);
-//  4. block prefix sum of a in fp64, Theta before / after each admission, and
+//  4. block prefix sum of a in float-float, Theta before / after each admission, and
 //     the first candidate whose admission does not raise Theta (policy 0,
 //     block min) or the count with the largest Theta (policy 1, block argmax);
 //  5. scatter the admitted counts into the verify lengths, Theta of the result.
@@ -42,48 +42,93 @@ __device__ __forceinline__ unsigned long long cand_key(float a, int pay) {
     return ((unsigned long long)(~__float_as_uint(a)) << 32) | (unsigned int)pay;
 }
 
-__device__ double block_sum(double v, double *red) {
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+// tau and Theta in float-float arithmetic (an unevaluated sum hi + lo of two
+// floats, about 44 significant bits), on the fp32 pipes: GB300's fp64 rate
+// would make this one-block kernel wait on its fp64 unit.
+struct ff {
+    float hi, lo;
+};
+__device__ __forceinline__ ff ff_make(float x) { return ff{x, 0.f}; }
+// Knuth's two-sum of two floats, then renormalised (|lo| <= ulp(hi) / 2)
+__device__ __forceinline__ ff ff_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return ff{s, e};
+}
+__device__ __forceinline__ ff ff_fast_norm(float hi, float lo) {
+    const float s = __fadd_rn(hi, lo);
+    return ff{s, __fsub_rn(lo, __fsub_rn(s, hi))};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    const ff s = ff_two_sum(a.hi, b.hi);
+    return ff_fast_norm(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ ff ff_add_f(ff a, float b) {
+    const ff s = ff_two_sum(a.hi, b);
+    return ff_fast_norm(s.hi, __fadd_rn(s.lo, a.lo));
+}
+// a * b for a float b: the product's rounding error from an FMA
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+    const float p = __fmul_rn(a.hi, b);
+    const float e = __fmaf_rn(a.lo, b, __fmaf_rn(a.hi, b, -p));
+    return ff_fast_norm(p, e);
+}
+__device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ double ff_to_double(ff a) { return (double)a.hi + (double)a.lo; }
+__device__ __forceinline__ ff shfl_xor_ff(ff v, int o) {
+    return ff{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ ff shfl_up_ff(ff v, int o) {
+    return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+
+__device__ ff block_sum(ff v, ff *red) {
+    for (int o = 16; o > 0; o >>= 1) v = ff_add(v, shfl_xor_ff(v, o));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __syncthreads();
     if (lane == 0) red[warp] = v;
     __syncthreads();
-    double t = (lane < (int)(blockDim.x >> 5)) ? red[lane] : 0.0;
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    ff t = (lane < (int)(blockDim.x >> 5)) ? red[lane] : ff_make(0.f);
+    for (int o = 16; o > 0; o >>= 1) t = ff_add(t, shfl_xor_ff(t, o));
     return t;
 }
 
-// Exclusive prefix over threads of one double per thread.
-__device__ double block_exclusive_scan(double v, double *red) {
+// Exclusive prefix over threads of one float-float per thread.
+__device__ ff block_exclusive_scan(ff v, ff *red) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    double incl = v;
+    ff incl = v;
     for (int o = 1; o < 32; o <<= 1) {
-        const double n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+        const ff n = shfl_up_ff(incl, o);
+        if (lane >= o) incl = ff_add(incl, n);
     }
     __syncthreads();
     if (lane == 31) red[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        double w = (lane < (int)(blockDim.x >> 5)) ? red[lane] : 0.0;
-        double wi = w;
+        const ff w = (lane < (int)(blockDim.x >> 5)) ? red[lane] : ff_make(0.f);
+        ff wi = w;
         for (int o = 1; o < 32; o <<= 1) {
-            const double n = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += n;
+            const ff n = shfl_up_ff(wi, o);
+            if (lane >= o) wi = ff_add(wi, n);
         }
-        red[lane] = wi - w;  // exclusive prefix of warp totals
+        // exclusive prefix of the warp totals: the inclusive one of the lane before
+        const ff ex = shfl_up_ff(wi, 1);
+        red[lane] = (lane == 0) ? ff_make(0.f) : ex;
     }
     __syncthreads();
-    return red[warp] + (incl - v);
+    // exclusive within the warp: the inclusive value of the lane before
+    const ff before = shfl_up_ff(incl, 1);
+    return ff_add(red[warp], lane == 0 ? ff_make(0.f) : before);
 }
 
 // Block-wide argmax of (value, index): the larger value, on equal values the
 // smaller index.  Every thread gets the result.
-__device__ void block_argmax(double &v, int &n, double *redv, int *redn) {
+__device__ void block_argmax(ff &v, int &n, ff *redv, int *redn) {
     for (int o = 16; o > 0; o >>= 1) {
-        const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const ff v2 = shfl_xor_ff(v, o);
         const int n2 = __shfl_xor_sync(0xffffffffu, n, o);
-        if (v2 > v || (v2 == v && n2 < n)) {
+        if (ff_gt(v2, v) || (v2.hi == v.hi && v2.lo == v.lo && n2 < n)) {
             v = v2;
             n = n2;
         }
@@ -95,12 +140,12 @@ __device__ void block_argmax(double &v, int &n, double *redv, int *redn) {
         redn[warp] = n;
     }
     __syncthreads();
-    v = (lane < (int)(blockDim.x >> 5)) ? redv[lane] : -INFINITY;
+    v = (lane < (int)(blockDim.x >> 5)) ? redv[lane] : ff{-INFINITY, 0.f};
     n = (lane < (int)(blockDim.x >> 5)) ? redn[lane] : INT_MAX;
     for (int o = 16; o > 0; o >>= 1) {
-        const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const ff v2 = shfl_xor_ff(v, o);
         const int n2 = __shfl_xor_sync(0xffffffffu, n, o);
-        if (v2 > v || (v2 == v && n2 < n)) {
+        if (ff_gt(v2, v) || (v2.hi == v.hi && v2.lo == v.lo && n2 < n)) {
             v = v2;
             n = n2;
         }
@@ -116,7 +161,7 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
     extern __shared__ unsigned long long smem[];
     unsigned long long *key = smem;                       // [npow2] sort keys
     int *len_s = reinterpret_cast<int *>(key + npow2);    // [B]
-    __shared__ double red[32];
+    __shared__ ff red[32];
     __shared__ int redn[32];
     __shared__ unsigned long long xch[kSchedThreads];  // register-sort exchange
     __shared__ int first_fail;
@@ -148,10 +193,10 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
 
     // 1-2. calibrated confidences, prefix products, tau_0, candidates (policies
     // 2-3: the lengths, tau and the batch tokens of the result)
-    double tau_part = 0.0, tok_part = 0.0;
+    ff tau_part = ff_make(0.f), tok_part = ff_make(0.f);
     for (int b = tid; b < B; b += blockDim.x) {
         float prod = 1.f;
-        double t = 1.0;
+        ff t = ff_make(1.f);
         int L = L_min;
         bool run = true;
         for (int j = 0; j < G; ++j) {
@@ -165,25 +210,25 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
                     run = (policy == 2 ? prod : c) > threshold;
                     if (run) L = j + 1;
                 }
-                if (j < L) t += (double)prod;
+                if (j < L) t = ff_add_f(t, prod);
             } else {
-                if (j < L_min) t += (double)prod;
+                if (j < L_min) t = ff_add_f(t, prod);
                 if (j >= L_min && j < L_max) key[b * width + (j - L_min)] = cand_key(prod, j * B + b);
             }
         }
-        tau_part += t;
+        tau_part = ff_add(tau_part, t);
         len_s[b] = L;
-        tok_part += (double)(L + 1);
+        tok_part = ff_add_f(tok_part, (float)(L + 1));
     }
     if (policy >= 2) {
-        const double tau = block_sum(tau_part, red);
-        const double tok = block_sum(tok_part, red);
+        const ff tau = block_sum(tau_part, red);
+        const ff tok = block_sum(tok_part, red);  // an integer below 2^24: exact
         for (int b = tid; b < B; b += blockDim.x) verify_len[b] = len_s[b];
-        if (tid == 0 && theta_out) *theta_out = tau * (double)sps[(long)tok];
+        if (tid == 0 && theta_out) *theta_out = ff_to_double(tau) * (double)sps[(long)tok.hi];
         return;
     }
     for (int i = ncand + tid; i < npow2; i += blockDim.x) key[i] = ~0ull;
-    const double tau0 = block_sum(tau_part, red);
+    const ff tau0 = block_sum(tau_part, red);
     __syncthreads();
 
     // 3. bitonic sort: highest priority first (ascending keys)
@@ -232,33 +277,34 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
     const long n0 = (long)B * (L_min + 1);
     const int per = (ncand + blockDim.x - 1) / blockDim.x;
     const int lo = min(ncand, tid * per), hi = min(ncand, lo + per);
-    auto a_of = [&](int i) { return (double)__uint_as_float(~(unsigned int)(key[i] >> 32)); };
-    double local = 0.0;
-    for (int i = lo; i < hi; ++i) local += a_of(i);
-    const double before = block_exclusive_scan(local, red);
-    double run = tau0 + before;  // tau before candidate lo
+    auto a_of = [&](int i) { return __uint_as_float(~(unsigned int)(key[i] >> 32)); };
+    ff local = ff_make(0.f);
+    for (int i = lo; i < hi; ++i) local = ff_add_f(local, a_of(i));
+    const ff before = block_exclusive_scan(local, red);
+    ff run = ff_add(tau0, before);  // tau before candidate lo
     int nstar;
     if (policy == 0) {
         for (int i = lo; i < hi; ++i) {
-            const double a = a_of(i);
-            const double th_before = run * (double)sps[n0 + i];
-            const double th_after = (run + a) * (double)sps[n0 + i + 1];
-            if (!(th_after > th_before)) {
+            const float a = a_of(i);
+            const ff th_before = ff_mul_f(run, sps[n0 + i]);
+            const ff next = ff_add_f(run, a);
+            const ff th_after = ff_mul_f(next, sps[n0 + i + 1]);
+            if (!ff_gt(th_after, th_before)) {
                 atomicMin(&first_fail, i);
                 break;
             }
-            run += a;
+            run = next;
         }
         __syncthreads();
         nstar = first_fail;
     } else {
         // Theta after admitting the first n candidates, n = 0 .. ncand
-        double bv = (tid == 0) ? tau0 * (double)sps[n0] : -INFINITY;
+        ff bv = (tid == 0) ? ff_mul_f(tau0, sps[n0]) : ff{-INFINITY, 0.f};
         int bn = (tid == 0) ? 0 : INT_MAX;
         for (int i = lo; i < hi; ++i) {
-            run += a_of(i);
-            const double th = run * (double)sps[n0 + i + 1];
-            if (th > bv) {
+            run = ff_add_f(run, a_of(i));
+            const ff th = ff_mul_f(run, sps[n0 + i + 1]);
+            if (ff_gt(th, bv)) {
                 bv = th;
                 bn = i + 1;
             }
@@ -268,15 +314,15 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
         __syncthreads();
     }
     // tau after the admitted prefix, for Theta
-    double adm = 0.0;
-    for (int i = lo; i < min(hi, nstar); ++i) adm += a_of(i);
-    const double tau_final = tau0 + block_sum(adm, red);
+    ff adm = ff_make(0.f);
+    for (int i = lo; i < min(hi, nstar); ++i) adm = ff_add_f(adm, a_of(i));
+    const ff tau_final = ff_add(tau0, block_sum(adm, red));
 
     // 5. verify lengths
     for (int i = tid; i < nstar; i += blockDim.x) atomicAdd(&len_s[(int)(key[i] & 0xFFFFFFFFu) % B], 1);
     __syncthreads();
     for (int b = tid; b < B; b += blockDim.x) verify_len[b] = len_s[b];
-    if (tid == 0 && theta_out) *theta_out = tau_final * (double)sps[n0 + nstar];
+    if (tid == 0 && theta_out) *theta_out = ff_to_double(tau_final) * (double)sps[n0 + nstar];
 }
 
 }  // namespace
