@@ -12,8 +12,9 @@
 //                     of every sampled request once with 16-byte loads
 //                     (online softmax of t/T), and rows j <= L of greedy
 //                     requests (argmax);
-//  2. verify_decide   one warp per request: merges the row partials, runs the
-//                     sequential acceptance scan, writes the emitted tokens and
+//  2. verify_decide   one warp per request: merges the row partials and tests
+//                     every row at once (a lane per row; the first rejection is
+//                     a ballot), writes the emitted tokens and
 //                     marks the final draw: a residual at the rejected row or a
 //                     bonus from row L (sampled requests only);
 //  3. final draw      residual rows rebuild the draft logits of the rejected
@@ -182,41 +183,53 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
     }
     const float c2 = T > 0.f ? kLog2e / T : 0.f;
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
-    int k = 0, y = -1, d = -1;
-    for (int j = 0; j < L; ++j) {
-        RowState s = row_state_init();
-        const RowState *pr = part + ((size_t)b * (G + 1) + j) * nsplit;
-        for (int i = lane; i < nsplit; i += 32) row_state_merge(s, pr[i]);
-        s = warp_merge(s);
-        const int x = draft_tokens[(size_t)b * G + j];
-        if (T > 0.f) {
-            const float lse2 = s.m + log2f(s.S);
-            const float tx = to_f32(target_row(target, row0, n_rows, b, G, j, V)[x]);
-            const float logp = kLn2 * (fmaf(tx, c2, -s.m) - log2f(s.S));
-            const float logq = draft_logq[(size_t)b * G + j];
-            const uint4 w4 = philox4x32_10(make_uint4(0u, (uint32_t)j, id, kStreamAccept), k0, k1);
-            const float u = word_to_uniform(w4.x);
-            const bool accept = u < expf(logp - logq);
-            if (lane == 0) {
-                if (target_lse) target_lse[(size_t)b * (G + 1) + j] = kLn2 * lse2;
-                if (logp_sel) logp_sel[(size_t)b * G + j] = logp;
-            }
-            if (!accept) {
-                d = j;
-                if (lane == 0) lse_t_row[b] = lse2;
-                break;
-            }
-        } else {
-            if (lane == 0) {
-                if (target_lse) target_lse[(size_t)b * (G + 1) + j] = s.key;
-                if (logp_sel) logp_sel[(size_t)b * G + j] = (s.idx == x) ? 0.f : -INFINITY;
-            }
-            if (s.idx != x) {
-                y = s.idx;
-                break;
+    // Every tested row at once: lane j merges row j's partials (in segment
+    // order), reads the target logit of x_j and decides its acceptance; the
+    // first rejection (or greedy mismatch) is the lowest set bit of a ballot.
+    // Rows after it were never tested: their outputs stay NaN.
+    int k = L, y = -1, d = -1;
+    for (int j0 = 0; j0 < L; j0 += 32) {
+        const int j = j0 + lane;
+        const bool tested = j < L;
+        bool pass = true;
+        float lse_out = 0.f, logp = 0.f, lse2 = 0.f;
+        int amax = -1;
+        if (tested) {
+            RowState s = row_state_init();
+            const RowState *pr = part + ((size_t)b * (G + 1) + j) * nsplit;
+            for (int i = 0; i < nsplit; ++i) row_state_merge(s, pr[i]);
+            const int x = draft_tokens[(size_t)b * G + j];
+            if (T > 0.f) {
+                lse2 = s.m + log2f(s.S);
+                const float tx = to_f32(target_row(target, row0, n_rows, b, G, j, V)[x]);
+                logp = kLn2 * (fmaf(tx, c2, -s.m) - log2f(s.S));
+                const float logq = draft_logq[(size_t)b * G + j];
+                const uint4 w4 = philox4x32_10(make_uint4(0u, (uint32_t)j, id, kStreamAccept), k0, k1);
+                pass = word_to_uniform(w4.x) < expf(logp - logq);
+                lse_out = kLn2 * lse2;
+            } else {
+                lse_out = s.key;
+                logp = (s.idx == x) ? 0.f : -INFINITY;
+                pass = (s.idx == x);
+                amax = s.idx;
             }
         }
-        ++k;
+        const unsigned int fail = __ballot_sync(0xffffffffu, tested && !pass);
+        const int first = fail ? j0 + __ffs(fail) - 1 : INT_MAX;  // the first failing row
+        if (tested && j <= first) {
+            if (target_lse) target_lse[(size_t)b * (G + 1) + j] = lse_out;
+            if (logp_sel) logp_sel[(size_t)b * G + j] = logp;
+        }
+        if (fail) {
+            k = first;
+            if (T > 0.f) {
+                d = first;
+                if (j == first) lse_t_row[b] = lse2;
+            } else {
+                y = __shfl_sync(0xffffffffu, amax, first - j0);
+            }
+            break;
+        }
     }
     int code = -1;
     if (d >= 0) {
