@@ -655,15 +655,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 const int t = si >> 3;
                 return vb + (rev_pos ? (ntiles - 1 - t) : t) * BN + (si & 7) * 16;
             };
-            // final draw: this thread's base / target values, one sub-slice ahead
-            uint4 nu_lo = make_uint4(0, 0, 0, 0), nu_hi = nu_lo, nt_lo = nu_lo, nt_hi = nu_lo;
+            // final draw: this thread's target values, one sub-slice ahead (its
+            // base values are read only for the groups that pass the bound test)
+            uint4 nt_lo = make_uint4(0, 0, 0, 0), nt_hi = nt_lo;
             if (kFinal && active && slice < nsub) {
                 const int v = sub_col(slice);
                 const int n = min(16, ve - v);
-                if (n > 0) {
-                    load16_bf16(trow + v, n, nt_lo, nt_hi);
-                    if (kind == 1) load16_bf16(urow + v, n, nu_lo, nu_hi);
-                }
+                if (n > 0) load16_bf16(trow + v, n, nt_lo, nt_hi);
             }
             int waited = -1;  // the last tile whose accumulator this warp waited for
 #pragma unroll 1
@@ -746,23 +744,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         if (on && ((si / kEpiPerQuad) & 3) == 3)
                             kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
                     } else {
-                        // take this sub-slice's prefetched values, then prefetch the next
-                        // one's (before any skip: the skipped sub-slice may come first
-                        // when walking the segment backwards)
-                        // z = base + bias at once (the bias registers die), the target
-                        // kept packed as bf16 pairs
-                        float z[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) z[i] = bf16_at(nu_lo, nu_hi, i) + __uint_as_float(acc[i]);
+                        // take this sub-slice's prefetched target values (kept packed as
+                        // bf16 pairs), then prefetch the next one's (before any skip: the
+                        // skipped sub-slice may come first when walking the segment
+                        // backwards)
                         const uint4 ct_lo = nt_lo, ct_hi = nt_hi;
                         {
                             const int sn = si + kEpiPerQuad;  // this warp's next sub-slice
                             const int vn = (sn < nsub) ? sub_col(sn) : ve;
                             const int nn = min(16, ve - vn);
-                            if (active && sn < nsub && nn > 0) {
-                                load16_bf16(trow + vn, nn, nt_lo, nt_hi);
-                                if (kind == 1) load16_bf16(urow + vn, nn, nu_lo, nu_hi);
-                            }
+                            if (active && sn < nsub && nn > 0) load16_bf16(trow + vn, nn, nt_lo, nt_hi);
                         }
                         if (n <= 0) continue;  // warp-uniform
                         // One 16-token draw group (R2b; stream 2 residual, 3 bonus).  A
@@ -772,15 +763,35 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         // lse_q2 = +inf).  Group key K_g = off + log2 sum r - log2(-ln u0),
                         // off = tref for bonus rows, 0 for residual rows; it can beat the
                         // best key K only if (1 - u0) < sum 2^(off - K).
+                        // No normaliser is needed here (p and q are normalised by lse_t2
+                        // and lse_q2), only the candidate test, so a group is first
+                        // tested against a bound from its largest target logit alone:
+                        // every r_v <= p_v <= 2^(t_max c2 - tref).
                         const bool bonus = (kind == 2);
-                        float tref = lse_t2, off = 0.f;
-                        if (active && bonus) {
-                            float tm = -INFINITY;
+                        float tm = -INFINITY;
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (i < n) tm = fmaxf(tm, bf16_at(ct_lo, ct_hi, i));
-                            tref = off = tm * c2;
+                        for (int i = 0; i < 16; ++i)
+                            if (i < n) tm = fmaxf(tm, bf16_at(ct_lo, ct_hi, i));
+                        const float off = bonus ? tm * c2 : 0.f;
+                        const float tref = bonus ? off : lse_t2;
+                        if (active) {
+                            // the row-wide best key (one sub-slice old) tightens the threshold
+                            const float kg = ordered_to_key(kr_next);
+                            if (kg > kbest_r) kbest_r = kg;
                         }
+                        const float Qg = fminf(fast_exp2(off - kbest_r), kQMax) * kMargin;
+                        const float pmax = fast_exp2(fmaf(tm, c2, -tref));
+                        const bool maybe = active && one_minus_uniform_plus_one(w.x) < fmaf((float)n * pmax, Qg, 1.f);
+                        // the row-wide word for the next sub-slice (this thread's own
+                        // publications below are already in kbest_r)
+                        if (active) kr_next = load_relaxed(res_best);
+                        if (!__any_sync(0xffffffffu, maybe)) continue;
+                        // the draft logits z = base + bias of this group (residual rows)
+                        uint4 u_lo = make_uint4(0, 0, 0, 0), u_hi = u_lo;
+                        if (maybe && kind == 1) load16_bf16(urow + v, n, u_lo, u_hi);
+                        float z[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) z[i] = bf16_at(u_lo, u_hi, i) + __uint_as_float(acc[i]);
                         // upper bound of the group's sum under the approximate exponentials
                         float sum_up = 0.f;
 #pragma unroll
@@ -790,13 +801,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             const float ub = (pv - qv) + 4e-7f * (pv + qv);
                             sum_up += (i < n && ub > 0.f) ? ub : 0.f;
                         }
-                        if (active) {
-                            // the row-wide best key (one sub-slice old) tightens the threshold
-                            const float kg = ordered_to_key(kr_next);
-                            if (kg > kbest_r) kbest_r = kg;
-                        }
-                        const float Qg = fminf(fast_exp2(off - kbest_r), kQMax) * kMargin;
-                        const bool cand = active && sum_up > 0.f && one_minus_uniform_plus_one(w.x) < fmaf(sum_up, Qg, 1.f);
+                        const bool cand = maybe && sum_up > 0.f && one_minus_uniform_plus_one(w.x) < fmaf(sum_up, Qg, 1.f);
                         if (__any_sync(0xffffffffu, cand) && cand) {
                             // rare: the exact weights, r_v = p_v (1 - 2^-delta) with
                             // delta = log2 p_v - log2 q_v formed from the logits first
@@ -832,8 +837,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                                 red_max_u32(res_best, key_to_ordered(key));
                             }
                         }
-                        // the row-wide word for the next sub-slice, after this one's publication
-                        if (active) kr_next = load_relaxed(res_best);
                     }
                 }
             }
