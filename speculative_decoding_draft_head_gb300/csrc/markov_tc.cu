@@ -75,8 +75,8 @@ constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;      // and kMmaWarp + 1: even / odd tiles
 constexpr int kThreads = (kEpiWarps + 3) * 32;
 // registers per thread such that the warps of the busiest SM sub-partition fit its 16K
-constexpr int kMaxRegs = (16384 / (32 * ((kEpiWarps + 3 + 3) / 4))) / 8 * 8 > 96
-                             ? 96
+constexpr int kMaxRegs = (16384 / (32 * ((kEpiWarps + 3 + 3) / 4))) / 8 * 8 > 168
+                             ? 168
                              : (16384 / (32 * ((kEpiWarps + 3 + 3) / 4))) / 8 * 8;
 static_assert(kEpiWarps % 4 == 0 && kEpiPerQuad <= 8, "epilogue warps");
 constexpr int kWStages = 8;              // W ring: one 64-wide K atom of one tile per stage
@@ -371,7 +371,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     uint32_t *row_rid = reinterpret_cast<uint32_t *>(misc + 4 + 2 * BM);
     int *row_code = misc + 4 + 3 * BM;  // final draw: kind << 16 | position; draft: temperature valid
     // draft: the best key of each row found in this CTA during the position
-    // (ordered encoding, 0 = none), shared by the quadrant's four warps
+    // (ordered encoding, 0 = none), shared by the quadrant's warps
     uint32_t *row_kbest = reinterpret_cast<uint32_t *>(misc + 4 + 4 * BM);
 
     // one position of the recurrent head: launched as a programmatic
@@ -578,8 +578,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         for (int pi = 0; pi < npos && ok; ++pi) {
             const int jj = kFinal ? 0 : p.j + pi;
             // ---- A operand of this position: TMEM lane = request row, K in
-            // pairs per 32-bit column; warp w writes K elements 64 (w / 4) .. + 63
-            // of the rows of its quadrant: E_in[x_{j-1}] (Markov head), or the
+            // pairs per 32-bit column; the quadrant's warp `slice` writes the
+            // 64-element K blocks slice, slice + kEpiPerQuad, .. of its rows: E_in[x_{j-1}] (Markov head), or the
             // request's own row of p.a_rows (the recurrent head's state h_j).
             // Every UMMA of the previous position is done: this warp has seen
             // the tfull of its last tile.
@@ -596,10 +596,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 }
             }
             {
-                const int k0 = slice * 64;
                 const __nv_bfloat16 *a_src =
                     (!kFinal && p.a_rows) ? p.a_rows + (size_t)b * p.r : p.e_in + (size_t)max(prev, 0) * p.r;
-                if (k0 < p.r) {
+#pragma unroll 1
+                for (int k0 = slice * 64; k0 < p.r; k0 += kEpiPerQuad * 64) {
                     const int nk = min(64, p.r - k0);  // a multiple of 16
                     uint32_t av[32];
 #pragma unroll
@@ -612,7 +612,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         av[4 * i + 2] = val.z;
                         av[4 * i + 3] = val.w;
                     }
-                    tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(slice * 32), av);
+                    tmem_st32(tmem_base + ((uint32_t)(q * 32) << 16) + kTmemA + (uint32_t)(k0 / 2), av);
                     tmem_st_wait();
                 }
                 tc_fence_before();
