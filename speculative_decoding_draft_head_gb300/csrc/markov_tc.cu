@@ -737,11 +737,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             }
                         }
                         draft_group16(st, Q, kbest, z, c2, n, v, on, best, row_kbest + row, w);
-                        // reload the row-wide word every fourth sub-slice of this warp
-                        // (measured best: every second or eighth is slower, never is 10 %
-                        // slower), after this one's publications (at the start of a
-                        // position the other CTAs are publishing their first groups now)
-                        if (on && ((si / kEpiPerQuad) & 3) == 3)
+                        // reload the row-wide word after this warp's first sub-slice of
+                        // the position (by then every CTA has published its rows' first
+                        // groups, so the threshold is tight from the second sub-slice
+                        // on), then every fourth sub-slice, after this one's
+                        // publications.  Measured on GB300: 227 us against 238 us with
+                        // every fourth alone; every second, every eighth or a
+                        // threshold four sub-slices older are slower, never is 10 %
+                        // slower.
+                        if (on && (si < kEpiPerQuad || ((si / kEpiPerQuad) & 3) == 3))
                             kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
                     } else {
                         // take this sub-slice's prefetched target values (kept packed as
