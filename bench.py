@@ -276,6 +276,11 @@ def run_ours(args, w):
     vl_host = s_out["verify_len"].cpu().numpy() if w.scheduler else np.full(B, G)
     positions = int(vl_host.sum())
     n_rej = int((v_out["accept_len"] < (s_out["verify_len"] if w.scheduler else G)).sum().item())
+    # measured acceptance: accepted tests over tests (a request stops testing at
+    # its first rejection)
+    acc_h = v_out["accept_len"].cpu().numpy()
+    n_tests = int(np.minimum(acc_h + 1, vl_host).sum())
+    acceptance = float(acc_h.sum()) / max(1, n_tests)
 
     # per-call timing (events around each call), then the whole-step timing
     for _ in range(max(3, min(args.steps, 20))):
@@ -434,11 +439,15 @@ def run_ours(args, w):
         data="synthetic", config=_config(w),
         hbm_gbs=round_bytes / (ms / 1000.0) / 1e9,
         positions_per_step=positions,
+        drafted_positions_per_s=B * G / (d_ms / 1000.0),
+        acceptance=dict(accepted_over_tested=acceptance, tests=n_tests,
+                        note="per-test acceptance min(1, p/q) realised on the synthetic workload"),
         roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
                       frac=achieved / peaks["hbm_gbs"], traffic=traffic,
                       kernel=("draft call: markov_tc_kernel (all %d positions, one launch) + finalize" % G
                               if dominant == "draft" else "verify call (%d launches)" % launches_per_call),
-                      peak_source=peaks["source"]),
+                      peak_source=peaks["source"],
+                      dram_gbs=(None if traffic is None else traffic / (dom_ms / 1000.0) / 1e9)),
         calls_ms=dict(draft=d_ms, schedule=s_ms, verify=v_ms),
         rnn_head=(None if rnn_ms is None else
                   dict(draft_ms=rnn_ms, launches=2 * G + 1,

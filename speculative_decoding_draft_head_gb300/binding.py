@@ -263,6 +263,38 @@ def schedule_prefix(conf_logits, pos_temp, sps, L_min, L_max, *, policy=SCHED_EA
     return out
 
 
+class LaggedScheduler:
+    """The deployed scheduling mode: round t's verify lengths come from the
+    calibrated confidences of round t - ``lag`` ("DSpark, la bozza che sa quando
+    fermarsi", section "Che cosa resta da verificare": the production scheduler
+    works from confidences two rounds old and has no early stop), so the
+    schedule need not wait for the current round's confidence head.
+
+    Keeps a device ring of the last ``lag`` rounds' confidence logits [B, G];
+    until it has filled, a round is scheduled from its own logits.  Each
+    :meth:`step` runs one dspark_schedule_policy launch (policy ``policy``,
+    best prefix by default) and returns its outputs."""
+
+    def __init__(self, pos_temp, sps, L_min, L_max, *, lag=2, policy=SCHED_BEST_PREFIX, threshold=0.0):
+        if lag < 0:
+            raise ValueError("lag must be >= 0")
+        self.pos_temp, self.sps = pos_temp, sps
+        self.L_min, self.L_max = int(L_min), int(L_max)
+        self.lag, self.policy, self.threshold = int(lag), int(policy), float(threshold)
+        self._ring = []
+
+    def step(self, conf_logits, *, out=None, stream=None):
+        """Schedule this round; ``conf_logits`` [B, G] are this round's logits."""
+        src = self._ring[0] if len(self._ring) == self.lag and self.lag > 0 else conf_logits
+        res = schedule_prefix(src, self.pos_temp, self.sps, self.L_min, self.L_max, policy=self.policy,
+                              threshold=self.threshold, out=out, stream=stream)
+        if self.lag > 0:
+            self._ring.append(conf_logits.clone())
+            if len(self._ring) > self.lag:
+                self._ring.pop(0)
+        return res
+
+
 def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, request_id=None,
            seed=0, *, draft_logits=None, target_row0=None, out=None, workspace=None, stream=None):
     """Verify one drafted block per request.

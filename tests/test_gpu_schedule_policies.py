@@ -80,3 +80,24 @@ def test_unknown_policy_is_rejected():
     with pytest.raises(binding.DSparkError):
         binding.schedule_prefix(inp["conf_logits"], inp["pos_temp"], inp["sps"], w.L_min, w.G,
                                 policy=binding.SCHED_THRESHOLD_CUM, threshold=float("nan"))
+
+
+def test_lagged_scheduler_uses_the_confidences_of_two_rounds_back():
+    # the deployed mode: round t is scheduled (best prefix, no early stop) from
+    # round t - 2's calibrated confidences; the first two rounds use their own
+    w = WORKLOADS["dspark5"]
+    inp = make_inputs(w, 5, device="cuda")
+    sched = binding.LaggedScheduler(inp["pos_temp"], inp["sps"], w.L_min, w.G, lag=2)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    rounds = [1.0 + torch.randn((w.B, w.G), generator=gen, device="cuda") for _ in range(5)]
+    for t, cl in enumerate(rounds):
+        g = sched.step(cl)
+        torch.cuda.synchronize()
+        src = rounds[t - 2] if t >= 2 else cl
+        o = oracle.schedule_policy(src.cpu(), inp["pos_temp"].cpu(), inp["sps"].cpu(), w.L_min, w.G,
+                                   binding.SCHED_BEST_PREFIX)
+        _compare(g, o, False)
+        if t >= 2:  # and not from its own round
+            own = oracle.schedule_policy(cl.cpu(), inp["pos_temp"].cpu(), inp["sps"].cpu(), w.L_min, w.G,
+                                         binding.SCHED_BEST_PREFIX)
+            assert not np.array_equal(own["verify_len"], o["verify_len"])
