@@ -161,6 +161,22 @@ __device__ __forceinline__ bool grid_sync(unsigned int *ctr, unsigned int target
     return true;
 }
 
+// Named barrier `id` over `nthreads` threads that also returns the OR of every
+// participant's `pred`, so all of them take the same decision (a flag another
+// warp may raise at any time, read once per thread, could otherwise differ).
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ int seg_begin(int s, int nseg, int V) {
     if (s >= nseg) return V;
     return (int)(((long long)s * V / nseg) & ~15LL);  // whole 16-token draw groups
@@ -875,9 +891,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     *abort = 1;
                     atomicOr(p.flags, kFlagTimeout);
                 }
-                asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                // every epilogue warp leaves together if any part of the CTA gave up
+                if (named_barrier_or(1, kEpiWarps * 32, *abort != 0)) ok = false;
                 __threadfence();
-                if (*abort) ok = false;
             }
         }
     }
