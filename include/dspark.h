@@ -361,6 +361,17 @@ DSPARK_API dspark_status dspark_verify_noalloc(
 
 /* Copy the device flag word of a workspace to *flags (waits for `stream`).
  * Returns DSPARK_OK or DSPARK_ERR_CUDA. */
+/*
+ * Self-test of the bounded device-side waits (the library's failure
+ * detection): one block waits, with the helpers every kernel uses and a limit
+ * of limit_us microseconds (1 .. 10^6), on an mbarrier phase that nothing
+ * completes and on a device counter that nothing increments.  *result (host)
+ * receives bit 0 if the mbarrier wait gave up and bit 1 if the counter wait
+ * did: 3 when both report their timeout.  Synchronises the stream.  The
+ * context stays usable afterwards.
+ */
+DSPARK_API dspark_status dspark_selftest_bounded_wait(unsigned int limit_us, uint32_t *result, void *stream);
+
 DSPARK_API dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags);
 
 #ifdef __cplusplus

@@ -30,7 +30,8 @@ FLAG_BAD_TARGET_ROW = 32
 
 EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
            "dspark_schedule_prefix", "dspark_schedule_policy", "dspark_verify", "dspark_read_device_flags",
-           "dspark_verify_noalloc", "dspark_draft_sample_rnn", "dspark_verify_packed", "dspark_pack_target")
+           "dspark_verify_noalloc", "dspark_draft_sample_rnn", "dspark_verify_packed", "dspark_pack_target",
+           "dspark_selftest_bounded_wait")
 
 _lib = None
 _lock = threading.Lock()
@@ -82,6 +83,8 @@ def load(build_if_missing: bool = True):
                                     i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dspark_verify_packed.restype = ctypes.c_int
         L.dspark_verify_packed.argtypes = [vp, vp, ctypes.c_int64] + L.dspark_verify.argtypes[1:]
+        L.dspark_selftest_bounded_wait.restype = ctypes.c_int
+        L.dspark_selftest_bounded_wait.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_uint32), vp]
         L.dspark_pack_target.restype = ctypes.c_int
         L.dspark_pack_target.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.dspark_verify_noalloc.restype = ctypes.c_int
@@ -404,6 +407,14 @@ def verify_noalloc(target, base, e_in, w_out, anchor, draft, verify_len, tempera
         _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["num_out"]),
         _ptr(out.get("target_lse")), _ptr(out.get("logp")), _stream(stream)))
     return out
+
+
+def selftest_bounded_wait(limit_us=1000, stream=None) -> int:
+    """Run dspark_selftest_bounded_wait: 3 when both probe waits report their
+    timeout."""
+    val = ctypes.c_uint32(0)
+    _check(load().dspark_selftest_bounded_wait(int(limit_us), ctypes.byref(val), _stream(stream)))
+    return int(val.value)
 
 
 def read_device_flags(workspace, stream=None) -> int:

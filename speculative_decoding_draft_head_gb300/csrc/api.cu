@@ -283,6 +283,14 @@ dspark_status dspark_pack_target(const void *target_logits, const int32_t *verif
     return DSPARK_OK;
 }
 
+dspark_status dspark_selftest_bounded_wait(unsigned int limit_us, uint32_t *result, void *stream) {
+    if (!result) return fail(DSPARK_ERR_INVALID_ARG, "result is NULL");
+    if (limit_us < 1 || limit_us > 1000000) return fail(DSPARK_ERR_INVALID_ARG, "limit_us must be in [1, 1e6]");
+    cudaError_t e = run_bounded_wait_probe(limit_us, result, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test");
+    return DSPARK_OK;
+}
+
 dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags) {
     if (!workspace || !flags) return fail(DSPARK_ERR_INVALID_ARG, "NULL workspace or flags");
     cudaStream_t s = static_cast<cudaStream_t>(stream);

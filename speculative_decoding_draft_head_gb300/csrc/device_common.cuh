@@ -295,6 +295,26 @@ __device__ __forceinline__ unsigned long long best_encode(float key, int idx) {
     return ((unsigned long long)key_to_ordered(key) << 32) | (unsigned long long)(~(uint32_t)idx);
 }
 __device__ __forceinline__ int best_token(unsigned long long w) { return w ? (int)~(uint32_t)w : -1; }
+__device__ __forceinline__ unsigned int load_acquire_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until a global counter reaches `target` (the waiting half of a
+// grid barrier): gives up after about `limit` clock cycles or when *abort is
+// raised.  Returns whether the counter got there.
+__device__ __forceinline__ bool counter_wait(const unsigned int *ctr, unsigned int target, volatile int *abort,
+                                             long long limit) {
+    const long long t0 = clock64();
+    while (load_acquire_u32(ctr) < target) {
+        if (*abort) return false;
+        if (clock64() - t0 > limit) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
 // Fire-and-forget maxima (no value returned, so the issuing warp does not
 // wait for the memory system).
 __device__ __forceinline__ void red_max_u64(unsigned long long *p, unsigned long long v) {

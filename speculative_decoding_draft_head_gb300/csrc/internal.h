@@ -41,6 +41,9 @@ struct PerDeviceOnce {
 // Record the message returned by dspark_last_error() and return `st`.
 dspark_status set_last_error(dspark_status st, const char *fmt, ...);
 
+// ------------------------------------------------------------- selftest ----
+cudaError_t run_bounded_wait_probe(unsigned int limit_us, uint32_t *result, cudaStream_t s);
+
 // ----------------------------------------------------------------- pack ----
 cudaError_t launch_pack_target(const void *src, const int32_t *verify_len, int B, int G, int V, size_t elem_bytes,
                                void *dst, int64_t *row0, int64_t *n_rows, cudaStream_t s);

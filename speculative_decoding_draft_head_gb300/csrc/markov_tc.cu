@@ -138,11 +138,6 @@ struct TcParams {
     float *z_out;
 };
 
-__device__ __forceinline__ unsigned int load_acquire_u32(const unsigned int *p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // Grid-wide barrier between block positions (one thread per CTA; the launch
 // is cooperative, so every CTA is resident).  Bounded: gives up after about
@@ -151,12 +146,7 @@ __device__ __forceinline__ bool grid_sync(unsigned int *ctr, unsigned int target
                                           long long limit) {
     __threadfence();
     atomicAdd(ctr, 1u);
-    const long long t0 = clock64();
-    while (load_acquire_u32(ctr) < target) {
-        if (*abort) return false;
-        if (clock64() - t0 > limit) return false;
-        __nanosleep(64);
-    }
+    if (!counter_wait(ctr, target, abort, limit)) return false;
     __threadfence();
     return true;
 }
