@@ -71,54 +71,62 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
                    const float *__restrict__ temperature, int B, int G, int V, int chunk, int nsplit,
                    RowState *__restrict__ part) {
     __shared__ RowState scratch[kRowThreads / 32];
-    // rows along x (their count B (G + 1) can pass the 65535 limit of y)
-    const int row = blockIdx.x;
-    const int b = row / (G + 1);
-    const int j = row - b * (G + 1);
-    const int L = read_verify_len(verify_len, b, G);
-    const float T = temperature[b];
-    // sampled requests read rows j < L here (row L only for a bonus draw, in
-    // the final pass); greedy requests read rows j <= L
-    if (L < 0 || !temperature_ok(T) || j > L || (T > 0.f && j == L)) return;
-    const float c2 = T > 0.f ? kLog2e / T : 0.f;
-    const int seg = blockIdx.y;
-    const int vb = seg * chunk;
-    const int ve = min(V, vb + chunk);
-    const TIn *t_row = target_row(target, row0, n_rows, b, G, j, V);
-    if (!t_row) return;  // flagged by the decide kernel
+    // Unit u = seg * rows + row.  Launched as (rows, segments) every block takes
+    // one unit (rows along x: their count B (G + 1) can pass the 65535 limit of
+    // y); launched with fewer blocks (beside the draft kernel, one block per SM)
+    // the blocks walk the units.
+    const long rows = (long)B * (G + 1);
+    const long units = rows * nsplit;
+    const long stride = (long)gridDim.x * gridDim.y;
+    for (long u = (long)blockIdx.y * gridDim.x + blockIdx.x; u < units; u += stride) {
+        const int row = (int)(u % rows);
+        const int seg = (int)(u / rows);
+        const int b = row / (G + 1);
+        const int j = row - b * (G + 1);
+        const int L = read_verify_len(verify_len, b, G);
+        const float T = temperature[b];
+        // sampled requests read rows j < L here (row L only for a bonus draw, in
+        // the final pass); greedy requests read rows j <= L (uniform per unit)
+        if (L < 0 || !temperature_ok(T) || j > L || (T > 0.f && j == L)) continue;
+        const TIn *t_row = target_row(target, row0, n_rows, b, G, j, V);
+        if (!t_row) continue;  // flagged by the decide kernel
+        const float c2 = T > 0.f ? kLog2e / T : 0.f;
+        const int vb = seg * chunk;
+        const int ve = min(V, vb + chunk);
 
-    RowState st = row_state_init();
-    if (T > 0.f) {
-        int v = vb + 8 * threadIdx.x;
-        for (; v + 8 * kRowThreads < ve; v += 16 * kRowThreads) {  // two loads in flight
-            float x[8], y[8];
-            load8(t_row + v, x);
-            load8(t_row + v + 8 * kRowThreads, y);
+        RowState st = row_state_init();
+        if (T > 0.f) {
+            int v = vb + 8 * threadIdx.x;
+            for (; v + 8 * kRowThreads < ve; v += 16 * kRowThreads) {  // two loads in flight
+                float x[8], y[8];
+                load8(t_row + v, x);
+                load8(t_row + v + 8 * kRowThreads, y);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                x[e] *= c2;
-                y[e] *= c2;
+                for (int e = 0; e < 8; ++e) {
+                    x[e] *= c2;
+                    y[e] *= c2;
+                }
+                softmax_push_group<8>(st, x, 8);
+                softmax_push_group<8>(st, y, 8);
             }
-            softmax_push_group<8>(st, x, 8);
-            softmax_push_group<8>(st, y, 8);
-        }
-        if (v < ve) {
-            float x[8];
-            load8(t_row + v, x);
+            if (v < ve) {
+                float x[8];
+                load8(t_row + v, x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] *= c2;
-            softmax_push_group<8>(st, x, 8);
-        }
-    } else {  // greedy request
-        for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {
-            float x[8];
-            load8(t_row + v, x);
+                for (int e = 0; e < 8; ++e) x[e] *= c2;
+                softmax_push_group<8>(st, x, 8);
+            }
+        } else {  // greedy request
+            for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {
+                float x[8];
+                load8(t_row + v, x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) argmax_push(st, x[e], v + e);
+                for (int e = 0; e < 8; ++e) argmax_push(st, x[e], v + e);
+            }
         }
+        st = block_merge(st, scratch);
+        if (threadIdx.x == 0) part[(size_t)row * nsplit + seg] = st;
     }
-    st = block_merge(st, scratch);
-    if (threadIdx.x == 0) part[(size_t)row * nsplit + seg] = st;
 }
 
 // ---------------------------------------------------------------- pass 2 ----
@@ -472,8 +480,38 @@ __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part
     if (lane == 0) out_tokens[(size_t)b * (G + 1) + accept_len[b]] = y;
 }
 
+// Beside the draft kernel the blocks must share an SM with a draft CTA, which
+// runs with the largest shared-memory carveout; a block that reached an SM
+// first under a smaller carveout would keep the draft CTA off it.
 template <typename TIn>
-cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
+cudaError_t set_rows_carveout() {
+    static PerDeviceOnce once;
+    return once.run([] {
+        return cudaFuncSetAttribute(verify_rows_kernel<TIn>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    (int)cudaSharedmemCarveoutMaxShared);
+    });
+}
+
+template <typename TIn>
+cudaError_t launch_verify_rows_t(const VerifyArgs &a, const VerifyPlan &p, bool beside, cudaStream_t s) {
+    if (beside) {
+        const cudaError_t e = set_rows_carveout<TIn>();
+        if (e != cudaSuccess) return e;
+    }
+    RowState *row_part = reinterpret_cast<RowState *>(a.ws + p.row_part_offset);
+    const TIn *target = static_cast<const TIn *>(a.target);
+    const long units = (long)a.B * (a.G + 1) * p.row_split;
+    // beside the draft kernel: one block per SM, which fits next to a draft CTA
+    const dim3 grid = beside ? dim3((unsigned int)(units < kNumSMs ? units : kNumSMs))
+                             : dim3((unsigned int)(a.B * (a.G + 1)), (unsigned int)p.row_split);
+    verify_rows_kernel<TIn><<<grid, kRowThreads, 0, s>>>(target, a.target_row0, a.n_target_rows, a.verify_len,
+                                                         a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split,
+                                                         row_part);
+    return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t launch_verify_finish_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
     uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
     RowState *row_part = reinterpret_cast<RowState *>(a.ws + p.row_part_offset);
     int32_t *final_code = reinterpret_cast<int32_t *>(a.ws + p.res_row_offset);
@@ -483,10 +521,7 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
     const TIn *target = static_cast<const TIn *>(a.target);
 
-    verify_rows_kernel<TIn><<<dim3(a.B * (a.G + 1), p.row_split), kRowThreads, 0, s>>>(
-        target, a.target_row0, a.n_target_rows, a.verify_len, a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split, row_part);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     const int warps = 4;
     verify_decide_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
         target, a.target_row0, a.n_target_rows, row_part, p.row_split, a.anchor, a.draft_tokens, a.draft_logq, a.verify_len, a.temperature,
@@ -519,9 +554,20 @@ cudaError_t launch_verify_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream
 
 }  // namespace
 
+cudaError_t launch_verify_rows(const VerifyArgs &a, const VerifyPlan &p, bool beside, cudaStream_t s) {
+    if (a.dt == DSPARK_BF16) return launch_verify_rows_t<__nv_bfloat16>(a, p, beside, s);
+    return launch_verify_rows_t<float>(a, p, beside, s);
+}
+
+cudaError_t launch_verify_finish(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
+    if (a.dt == DSPARK_BF16) return launch_verify_finish_t<__nv_bfloat16>(a, p, s);
+    return launch_verify_finish_t<float>(a, p, s);
+}
+
 cudaError_t launch_verify(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
-    if (a.dt == DSPARK_BF16) return launch_verify_t<__nv_bfloat16>(a, p, s);
-    return launch_verify_t<float>(a, p, s);
+    cudaError_t e = launch_verify_rows(a, p, false, s);
+    if (e != cudaSuccess) return e;
+    return launch_verify_finish(a, p, s);
 }
 
 VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {
