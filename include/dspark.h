@@ -22,8 +22,13 @@
  *    allocates or frees memory.  Pointers to logits, E_in and W_out must be
  *    16-byte aligned; V must be a multiple of 8.
  *  - "dtype" arrays hold bf16 (DSPARK_BF16) or fp32 (DSPARK_F32) values; all
- *    arithmetic is fp32 on the device (the scheduler sums tau and Theta in
- *    fp64).
+ *    arithmetic is fp32 on the device (the scheduler accumulates tau and
+ *    Theta in float-float, an unevaluated sum of two floats of about 44
+ *    significant bits, and returns Theta as a double).
+ *  - Logits must be finite.  Mask a token with a large negative finite value
+ *    (-3e4, say): its probability is then 0 in fp32 and it is never drawn.
+ *    An IEEE -inf base logit is not supported on the bf16 path, whose base
+ *    add on the tensor cores multiplies every base logit of a tile by 0 or 1.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Calls only enqueue work: they do not synchronise.
  *  - `workspace` is caller-owned device scratch memory of at least
@@ -158,9 +163,9 @@ DSPARK_API dspark_status dspark_draft_sample(
  *
  * Arguments as in dspark_draft_sample, plus w_h [r][r] bf16 (row n holds the
  * weights of state unit n) and h_states: [B][G][r] bf16 output of the states
- * h_j, or NULL.  The state sum is compensated and tanh is taken in fp64, so
- * h_j is the exactly rounded value except within ~1e-13 of a bf16 rounding
- * boundary.  dtype must be DSPARK_BF16 (else DSPARK_ERR_UNSUPPORTED).  The
+ * h_j, or NULL.  The state sum is compensated, and tanh is taken in fp32 and
+ * redone in fp64 when the result lies near a bf16 rounding boundary, so h_j
+ * is the exactly rounded value except within ~1e-13 of such a boundary.  dtype must be DSPARK_BF16 (else DSPARK_ERR_UNSUPPORTED).  The
  * workspace is DSPARK_WS_DRAFT_RNN.  Verify such a block with dspark_verify
  * given the draft_logits this call stored (the draft distribution of the
  * rejected position is then read, not recomputed).
@@ -193,7 +198,8 @@ DSPARK_API dspark_status dspark_draft_sample_rnn(
  * B * (L_max + 1) + 1.  Outputs: conf, cum_conf [B][G] fp32, verify_len [B]
  * int32, theta_out [1] fp64 (final Theta) or NULL.
  * Limits: 0 <= L_min <= L_max <= G <= 64, B * G <= 16384.
- * c and a are computed in fp32; tau and Theta are accumulated in fp64.
+ * c and a are computed in fp32; tau and Theta are accumulated in float-float
+ * (about 44 significant bits).
  */
 DSPARK_API dspark_status dspark_schedule_prefix(
     const float *conf_logits, const float *pos_temp, const float *sps, int sps_len,

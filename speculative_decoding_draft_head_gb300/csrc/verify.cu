@@ -63,6 +63,38 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
+// Online softmax of 8 logits x scaled by c2 (log2 units) against a reference
+// m that may lag the running maximum, as in the draft: a term 2^(x c2 - m)
+// above 1 is fine, and only a group whose sum leaves [0, 2^64] (far above the
+// reference, or overflowed) is redone against its own maximum.  The result
+// m + log2 S is the same log-sum-exp; the common case costs one fused
+// multiply-add, one exp2 and one add per logit.
+__device__ __forceinline__ void softmax_push8_lagging(RowState &st, const float (&x)[8], float c2) {
+    if (st.m == -INFINITY) {  // this thread's first group: its maximum is the reference
+        float xm = x[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) xm = fmaxf(xm, x[i]);
+        st.m = xm * c2;
+        if (st.m == -INFINITY) return;  // every logit so far is -inf: nothing to add
+    }
+    float e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e[i] = fast_exp2(fmaf(x[i], c2, -st.m));
+    float acc = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+    if (!(acc <= 0x1p64f)) {
+        float xm = x[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) xm = fmaxf(xm, x[i]);
+        const float cm = fmaxf(st.m, xm * c2);
+        st.S *= fast_exp2(st.m - cm);
+        st.m = cm;
+        acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc += fast_exp2(fmaf(x[i], c2, -st.m));
+    }
+    st.S += acc;
+}
+
 // ---------------------------------------------------------------- pass 1 ----
 template <typename TIn>
 __global__ void __launch_bounds__(kRowThreads)
@@ -101,20 +133,13 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
                 float x[8], y[8];
                 load8(t_row + v, x);
                 load8(t_row + v + 8 * kRowThreads, y);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[e] *= c2;
-                    y[e] *= c2;
-                }
-                softmax_push_group<8>(st, x, 8);
-                softmax_push_group<8>(st, y, 8);
+                softmax_push8_lagging(st, x, c2);
+                softmax_push8_lagging(st, y, c2);
             }
             if (v < ve) {
                 float x[8];
                 load8(t_row + v, x);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] *= c2;
-                softmax_push_group<8>(st, x, 8);
+                softmax_push8_lagging(st, x, c2);
             }
         } else {  // greedy request
             for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {

@@ -12,7 +12,9 @@ Contract (fp32 device arithmetic against a double-precision oracle):
     counted; everything after a divergence in the same request is skipped.
   - log-sum-exps and calibrated confidences agree within REL (relative, with
     a floor of 1 on the scale); log-probabilities within REL absolute (that is,
-    probabilities within REL relative).
+    probabilities within REL relative) down to log p = -64, and within
+    REL |log p| / 64 below (p < 2^-92, masked tokens), where the spacing of
+    fp32 numbers near log p itself exceeds REL.
 """
 from __future__ import annotations
 
@@ -186,7 +188,9 @@ def compare_verify(g, o, temps, reqs, skip):
                 t.failures.append("target lse b=%d j=%d gpu=%.9g oracle=%.9g" % (b, j, glse[b, j], ol))
         for j in range(o["logp"].shape[1]):
             ol = o["logp"][i, j]
-            if np.isfinite(ol) and abs(glp[b, j] - ol) > REL:
+            # absolute below |log p| = 64; beyond (p < 2^-92, a masked token) the
+            # fp32 spacing of log p itself passes REL, so the bound scales with it
+            if np.isfinite(ol) and abs(glp[b, j] - ol) > REL * max(1.0, abs(ol) / 64.0):
                 t.failures.append("logp b=%d j=%d gpu=%.9g oracle=%.9g" % (b, j, glp[b, j], ol))
     return t
 
