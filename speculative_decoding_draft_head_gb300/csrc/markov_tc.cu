@@ -98,7 +98,7 @@ constexpr uint32_t kIBytes = 16 * 128;
 constexpr uint32_t kOffMerge = kOffI + kIBytes;
 constexpr uint32_t kMergeBytes = BM * kEpiPerQuad * 32;
 constexpr uint32_t kOffBar = kOffMerge + kMergeBytes;
-constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs + 1;
+constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs + 1 + 2;
 static_assert(kNumBars * 8 <= 256, "barrier region");
 constexpr uint32_t kOffMisc = kOffBar + 256;
 constexpr uint32_t kMiscBytes = 16 + BM * 20;
@@ -107,6 +107,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kTmemA + 128 <= kTmemCols, "TMEM accumulators and A operand");
 
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of clock cycles
+constexpr long long kDrainLimit = 200000000LL;  // ~0.1 s: copies and UMMAs in flight after a timeout
 constexpr float kQMax = 0x1p126f;
 constexpr float kMargin = 1.0001f;
 
@@ -321,6 +322,24 @@ __device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbe
     }
 }
 
+// A timed-out CTA, before its shared memory and TMEM are given up: the copies
+// it armed must land (bytes armed but never issued are counted as landed) and
+// the UMMAs it issued must finish; each wait is bounded again.  Out of line:
+// the path runs only after a timeout.
+static_assert(kUStages == 2, "drain_copies walks two tile slots");
+__device__ __noinline__ void drain_copies(uint32_t full0, uint32_t full1, int armed, uint32_t unissued,
+                                          volatile int *never) {
+    if (armed <= 0) return;
+    const int last = armed - 1;
+    if (unissued) mbar_complete_tx((last & 1) ? full1 : full0, unissued);
+    for (int t = armed > kUStages ? armed - kUStages : 0; t < armed; ++t)
+        mbar_wait((t & 1) ? full1 : full0, (uint32_t)(t / kUStages) & 1u, never, kDrainLimit);
+}
+__device__ __noinline__ void drain_ummas(uint32_t bar, volatile int *never) {
+    umma_commit(bar);
+    mbar_wait(bar, 0u, never, kDrainLimit);
+}
+
 // 18 warps: 5 share one SM sub-partition's 16K registers, so at most 96 each.
 // The warps of the busiest SM sub-partition share its 16K registers: kMaxRegs each.
 //
@@ -368,10 +387,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     auto tfull = [&](int a) { return bar(kWStages + 2 * kUStages + a); };
     auto tempty = [&](int a) { return bar(kWStages + 2 * kUStages + kAccBufs + a); };
     const uint32_t a_ready = bar(kWStages + 2 * kUStages + 2 * kAccBufs);
+    // drain(i): every UMMA of issuer i is done (used only after a timeout)
+    auto drain = [&](int i) { return bar(kWStages + 2 * kUStages + 2 * kAccBufs + 1 + i); };
 
     int *misc = reinterpret_cast<int *>(smem + kOffMisc);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
     volatile int *abort = misc + 1;
+    volatile int *never = misc + 2;  // stays 0: the abort flag of the drain's waits
     int *row_prev = misc + 4;  // final draw: the row's previous token
     float *row_c2 = reinterpret_cast<float *>(misc + 4 + BM);
     uint32_t *row_rid = reinterpret_cast<uint32_t *>(misc + 4 + 2 * BM);
@@ -397,7 +419,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             mbar_init(tempty(a), 32);  // one arrival per 16-column sub-slice of each quadrant
         }
         mbar_init(a_ready, kEpiWarps);
+        mbar_init(drain(0), 1);
+        mbar_init(drain(1), 1);
         *abort = 0;
+        *never = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -458,6 +483,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int n_katoms = (p.r + 63) >> 6;
+    // producer lane 0: tiles whose full_tile phase was armed, and the bytes armed
+    // for the last of them that were never issued (a timeout inside the tile)
+    int armed = 0;
+    uint32_t unissued = 0;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -486,14 +515,18 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             break;
                         }
                         mbar_arrive_expect_tx(full_tile(slot), n_katoms * kWChunk + u_bytes);
+                        armed = tg + 1;
+                        unissued = n_katoms * kWChunk + u_bytes;
                     }
                     tma_load_2d(sbase + kOffW + ws * kWChunk, &map_w, full_tile(slot), kb * 64, v0, pol_w);
+                    unissued -= kWChunk;
                 }
                 if (ok && !kFinal) {
                     tma_load_3d(sbase + kOffU + slot * kUBytes, &map_u, full_tile(slot), v0, jj, m0, pol_u);
                     if (two)
                         tma_load_3d(sbase + kOffU + slot * kUBytes + kUHalf, &map_u, full_tile(slot), v0 + 64, jj, m0,
                                     pol_u);
+                    unissued -= u_bytes;
                 }
             }
             if (!ok) {
@@ -889,6 +922,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     }
     tc_fence_before();
     __syncthreads();
+    if (*abort) {  // the same for every thread after the barrier
+        if (lane == 0) {
+            if (warp == kProducerWarp) drain_copies(full_tile(0), full_tile(1), armed, unissued, never);
+            if (warp == kMmaWarp || warp == kMmaWarp + 1) drain_ummas(drain(warp - kMmaWarp), never);
+        }
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
