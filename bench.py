@@ -272,27 +272,28 @@ def run_ours(args, w):
                        x["temperature"], x["request_id"], args.seed, rows_done=True, out=v_out,
                        workspace=ws_v, stream=stream)
 
-    def step(x, timed=False):
+    def step(x, timed=False, st=None):
         if not timed and args.overlap:
             return step_overlapped(x)
+        st = stream if st is None else st
         if timed:
             ev["draft"][0].record(stream)
         binding.draft_sample(x["base"], x["e_in"], x["w_out"], x["anchor"], x["temperature"],
-                             x["request_id"], args.seed, out=d_out, workspace=ws_d, stream=stream)
+                             x["request_id"], args.seed, out=d_out, workspace=ws_d, stream=st)
         if timed:
             ev["draft"][1].record(stream)
             ev["sched"][0].record(stream)
         vl = None
         if w.scheduler:
             binding.schedule_prefix(x["conf_logits"], x["pos_temp"], x["sps"], w.L_min, G, out=s_out,
-                                    workspace=ws_s, stream=stream)
+                                    workspace=ws_s, stream=st)
             vl = s_out["verify_len"]
         if timed:
             ev["sched"][1].record(stream)
             ev["verify"][0].record(stream)
         binding.verify(x["target"], x["base"], x["e_in"], x["w_out"], x["anchor"], d_out, vl,
                        x["temperature"], x["request_id"], args.seed, out=v_out, workspace=ws_v,
-                       stream=stream)
+                       stream=st)
         if timed:
             ev["verify"][1].record(stream)
 
@@ -315,6 +316,20 @@ def run_ours(args, w):
         for k in ev:
             call_ms[k].append(ev[k][0].elapsed_time(ev[k][1]))
 
+    # The timed rounds replay one CUDA graph of the round (its launches and
+    # flag clears, captured once on a side stream): the same kernels on the
+    # same resident buffers, without the per-launch gaps of eager issue.
+    graph = None
+    if not args.no_graph and not args.overlap:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            step(inp, st=cap)
+        stream.wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize()
+
     clocks = ClockSampler(dev.index)
     if rank == 0:
         clocks.start()
@@ -325,7 +340,10 @@ def run_ours(args, w):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        step(inp)
+        if graph is not None:
+            graph.replay()
+        else:
+            step(inp)
     t1.record(stream)
     torch.cuda.synchronize()
     _barrier(world)
@@ -477,7 +495,8 @@ def run_ours(args, w):
         calls_ms=dict(draft=d_ms, schedule=s_ms, verify=v_ms),
         step_order=("schedule; then draft beside dspark_verify_rows on a second stream; then "
                     "dspark_verify_finish (calls_ms timed serially)" if args.overlap else
-                    "draft, schedule, verify on one stream"),
+                    "draft, schedule, verify on one stream" +
+                    (", replayed from one CUDA graph (calls_ms timed eagerly)" if graph is not None else "")),
         rnn_head=(None if rnn_ms is None else
                   dict(draft_ms=rnn_ms, launches=2 * G + 1,
                        note="recurrent-head draft call (state update + tensor-core draw per position, "
@@ -523,6 +542,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue the timed rounds' calls eagerly instead of replaying a CUDA graph of the round")
     ap.add_argument("--overlap", action="store_true",
                     help="run dspark_verify_rows on a second stream beside the draft (measured slower: both "
                          "kernels are bound by the SMs' issue rate, not by HBM)")
