@@ -87,3 +87,30 @@ def test_schedule_and_verify_reject_bad_host_arguments():
     st = lib.dspark_verify(p, None, None, None, None, p, p, p, p, None, p, None,
                            4, 4, 1024, 16, 1, 0, p, p, p, None, None, p, 1 << 20, None)
     assert st == 1 and "draft_logits" in lib.dspark_last_error().decode()
+
+
+def test_split_verify_rejects_bad_host_arguments():
+    """dspark_verify_rows / dspark_verify_finish check their arguments on the
+    host before any launch, like dspark_verify."""
+    lib = binding.load()
+    vp = ctypes.c_void_p
+    p = vp(1 << 12)
+    err = lambda: lib.dspark_last_error().decode()
+    # rows half: B, G, V, r, dtype as dspark_verify; then pointers, packing, workspace
+    st = lib.dspark_verify_rows(p, None, 0, None, None, 4, 4, 1024, 16, 1, p, 1 << 20, None)
+    assert st == 1 and "NULL" in err()
+    st = lib.dspark_verify_rows(p, p, 0, None, p, 4, 4, 1024, 16, 1, p, 1 << 20, None)
+    assert st == 1 and "n_target_rows" in err()
+    st = lib.dspark_verify_rows(vp((1 << 12) + 4), None, 0, None, p, 4, 4, 1024, 16, 1, p, 1 << 20, None)
+    assert st == 1 and "aligned" in err()
+    st = lib.dspark_verify_rows(p, None, 0, None, p, 4, 4, 1024, 16, 1, p, 16, None)
+    assert st == 1 and "too small" in err()
+    st = lib.dspark_verify_rows(p, None, 0, None, p, 4, 0, 1024, 16, 1, p, 1 << 20, None)
+    assert st == 1 and "G must be" in err()
+    # finishing half: the packed-layout check, then dspark_verify's
+    st = lib.dspark_verify_finish(p, p, 0, p, p, p, None, p, p, p, p, None, p, None,
+                                  4, 4, 1024, 16, 1, 0, p, p, p, None, None, p, 1 << 20, None)
+    assert st == 1 and "n_target_rows" in err()
+    st = lib.dspark_verify_finish(p, None, 0, None, None, None, None, p, p, p, p, None, p, None,
+                                  4, 4, 1024, 16, 1, 0, p, p, p, None, None, p, 1 << 20, None)
+    assert st == 1 and "draft_logits" in err()
