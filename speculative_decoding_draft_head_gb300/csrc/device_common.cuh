@@ -114,18 +114,9 @@ __device__ __forceinline__ uint4 philox_folded(uint32_t x0, const PhiloxRow &R, 
     return make_uint4(c0, c1, c2, c3);
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4 &w, int e) {
-    return e == 0 ? w.x : (e == 1 ? w.y : (e == 2 ? w.z : w.w));
-}
-
 // u = ((w >> 9) + 1/2) * 2^-23, exact: 1 + k 2^-23 minus (1 - 2^-24).
 __device__ __forceinline__ float word_to_uniform(uint32_t w) {
     return __uint_as_float(0x3F800000u | (w >> 9)) - 0x1.fffffep-1f;
-}
-
-// 1 - u, exact: (2 - 2^-24) - (1 + k 2^-23).
-__device__ __forceinline__ float word_to_one_minus_uniform(uint32_t w) {
-    return 0x1.fffffep+0f - __uint_as_float(0x3F800000u | (w >> 9));
 }
 
 // f1 = 1 + k' 2^-23 with k' = 0x7FFFFF - (w >> 9), which equals
