@@ -185,3 +185,34 @@ def test_group_draw_inside_a_dominant_group_follows_the_conditional_law():
     ok, chi2 = _chi2_ok(np.bincount(tok - 32, minlength=16), _softmax(row[32:48]), N)
     assert ok, chi2
     assert np.all(d["cdf_margin"][:, 0] >= 0) and np.all(d["cdf_margin"][:, 0] <= 1)
+
+
+def test_masked_tokens_are_never_drawn_and_leave_lse_unchanged():
+    """A masked token (logit -3e4) has probability exp(-3e4 / T) = 0 in double
+    precision: the draft never draws it and lse is the log-sum-exp over the
+    unmasked tokens alone, also for rows whose first groups are all masked."""
+    V, r, B, G = 96, 4, 6, 2
+    rng = np.random.default_rng(3)
+    U = rng.normal(0, 2, (B, G, V))
+    mask = np.zeros(V, bool)
+    mask[:40] = True          # the first two 16-token groups and half of the third
+    mask[-12:] = True
+    U[..., mask] = -3.0e4
+    E = rng.normal(0, 0.3, (V, r))
+    W = rng.normal(0, 0.3, (V, r))
+    anchor = np.array([50, 60, 41, 77, 3, 95], np.int32)
+    temps = np.array([1.0, 0.7, 1.3, 0.0, 1.0, 2.0])
+    d = oracle.draft_sample(U, E, W, anchor, temps, seed=11)
+    assert not mask[d["tokens"]].any()
+    for b in range(B):
+        prev = anchor[b]
+        for j in range(G):
+            z = (U[b, j] + W @ E[prev]).astype(np.float32).astype(np.float64)  # fp32 logits, as drawn
+            zu = z[~mask]
+            if temps[b] > 0:
+                s = zu / temps[b]
+                want = s.max() + math.log(np.exp(s - s.max()).sum())
+            else:
+                want = zu.max()
+            assert d["lse"][b, j] == pytest.approx(want, rel=1e-12, abs=1e-9)
+            prev = d["tokens"][b, j]

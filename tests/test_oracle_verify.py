@@ -310,3 +310,31 @@ def test_first_emitted_token_is_distributed_as_target_across_draw_groups():
     assert ok, chi2
     assert np.all(v["final_kind"][rej] == 1) and np.all(v["final_kind"][acc] == 0)
     assert np.all((v["final_cdf"] >= 0) & (v["final_cdf"] <= 1))
+
+
+def test_target_masked_tokens_are_rejected_and_never_emitted():
+    """Tokens the target masks (logit -3e4, probability 0) are rejected when
+    drafted (p = 0 < u q) and never emitted by the residual or bonus draw."""
+    V, G, r, B = 64, 3, 2, 400
+    rng = np.random.default_rng(21)
+    U = rng.normal(0, 1.5, (B, G, V))
+    tgt = np.concatenate([U, rng.normal(0, 1.5, (B, 1, V))], axis=1) + rng.normal(0, 0.5, (B, G + 1, V))
+    banned = np.zeros(V, bool)
+    banned[rng.choice(V, 20, replace=False)] = True
+    tgt[..., banned] = -3.0e4
+    E, W = rng.normal(0, 0.2, (V, r)), rng.normal(0, 0.2, (V, r))
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    temps = np.where(np.arange(B) % 4 == 0, 0.0, 1.0)
+    d = oracle.draft_sample(U, E, W, anchor, temps, rid=np.arange(B), seed=5)
+    v = oracle.verify(tgt, U, E, W, anchor, d["tokens"], None, temps, rid=np.arange(B), seed=5)
+    drafted_banned = 0
+    for b in range(B):
+        k = v["accept_len"][b]
+        out = v["out_tokens"][b, : v["num_out"][b]]
+        assert not banned[out].any()
+        # the first drafted banned token is never accepted
+        hit = np.flatnonzero(banned[d["tokens"][b]])
+        if hit.size:
+            drafted_banned += 1
+            assert k <= hit[0]
+    assert drafted_banned > 20  # the case is exercised
