@@ -211,6 +211,7 @@ __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsp
                                       const float *__restrict__ temperature, int B, int G, int j0, int npos,
                                       int32_t *__restrict__ tokens, float *__restrict__ lse,
                                       float *__restrict__ logq) {
+    griddep_wait();  // a programmatic dependent: the previous launch's writes are visible after this
     const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= B * npos) return;
@@ -269,9 +270,8 @@ cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j,
     if (p.tensor_path) part += (size_t)j * pos_stride;
     const int warps = 4;
     const int rows = a.B * npos;
-    draft_finalize_kernel<<<(rows + warps - 1) / warps, 32 * warps, 0, s>>>(
-        part, p.nsplit, pos_stride, a.temperature, a.B, a.G, j, npos, a.tokens, a.lse, a.logq);
-    return cudaGetLastError();
+    return launch_dependent(draft_finalize_kernel, dim3((rows + warps - 1) / warps), dim3(32 * warps), 0, s, part,
+                            p.nsplit, pos_stride, a.temperature, a.B, a.G, j, npos, a.tokens, a.lse, a.logq);
 }
 
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -206,5 +207,25 @@ struct ScheduleArgs {
 constexpr int kScheduleMaxCells = 16384;  // B * G
 size_t schedule_smem_bytes(int B, int G, int L_min, int L_max);
 cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s);
+
+// Launch `kernel` as a programmatic dependent of the stream's previous kernel:
+// its blocks may be scheduled while that kernel drains, and every kernel
+// launched this way starts with griddepcontrol.wait (griddep_wait), which
+// returns once the previous kernel has completed and its writes are visible.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace dspark

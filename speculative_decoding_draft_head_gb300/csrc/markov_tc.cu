@@ -434,6 +434,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         tma_prefetch_desc(&map_w);
         if (!kFinal) tma_prefetch_desc(&map_u);
     }
+    // the final draw is launched as a dependent of the decide pass: its set-up
+    // above overlaps that pass, whose outputs are read from here on
+    if (kFinal) griddep_wait();
     if (threadIdx.x < BM) {
         const int b = m0 + threadIdx.x;
         int prev = -1, code = 0;
@@ -1155,8 +1158,8 @@ cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     p.res_best = a.res_best;
     p.flags = a.flags;
     // the final draw reads its base rows directly: map_u is unused
-    markov_tc_kernel<true><<<dim3(a.nseg, tc_row_blocks(a.B)), kThreads, kSmemBytes, s>>>(mw, mw, p);
-    return cudaGetLastError();
+    return launch_dependent(markov_tc_kernel<true>, dim3(a.nseg, tc_row_blocks(a.B)), dim3(kThreads), kSmemBytes, s,
+                            mw, mw, p);
 }
 
 }  // namespace dspark

@@ -169,6 +169,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
                                      float *__restrict__ target_lse, float *__restrict__ logp_sel,
                                      int32_t *__restrict__ final_code, float *__restrict__ lse_t_row,
                                      uint32_t *__restrict__ res_best, uint32_t *__restrict__ flags) {
+    griddep_wait();  // a programmatic dependent: the previous launch's writes are visible after this
     const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -445,6 +446,7 @@ __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part
                                           int64_t n_rows, const float *__restrict__ temperature,
                                           const uint32_t *__restrict__ request_id, int B, int G, int V,
                                           uint32_t k0, uint32_t k1, int32_t *__restrict__ out_tokens) {
+    griddep_wait();  // a programmatic dependent: the previous launch's writes are visible after this
     const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -548,11 +550,12 @@ cudaError_t launch_verify_finish_t(const VerifyArgs &a, const VerifyPlan &p, cud
 
     cudaError_t e;
     const int warps = 4;
-    verify_decide_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
-        target, a.target_row0, a.n_target_rows, row_part, p.row_split, a.anchor, a.draft_tokens, a.draft_logq, a.verify_len, a.temperature,
-        a.request_id, a.B, a.G, a.V, k0, k1, a.accept_len, a.out_tokens, a.num_out, a.target_lse,
-        a.logp_sel, final_code, lse_t_row, res_best, flags);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_dependent(verify_decide_kernel<TIn>, dim3((a.B + warps - 1) / warps), dim3(32 * warps), 0, s,
+                         target, a.target_row0, a.n_target_rows, (const RowState *)row_part, p.row_split, a.anchor,
+                         a.draft_tokens, a.draft_logq, a.verify_len, a.temperature, a.request_id, a.B, a.G, a.V, k0,
+                         k1, a.accept_len, a.out_tokens, a.num_out, a.target_lse, a.logp_sel, final_code, lse_t_row,
+                         res_best, flags);
+    if (e != cudaSuccess) return e;
     const bool tensor = p.tensor_residual && !a.z_in;
     const int res_nsplit = tensor ? p.res_split_tc : p.res_split;
     if (tensor) {
@@ -571,10 +574,10 @@ cudaError_t launch_verify_finish_t(const VerifyArgs &a, const VerifyPlan &p, cud
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    verify_final_merge_kernel<TIn><<<(a.B + warps - 1) / warps, 32 * warps, 0, s>>>(
-        res_part, res_nsplit, final_code, a.accept_len, target, a.target_row0, a.n_target_rows, a.temperature, a.request_id, a.B, a.G,
-        a.V, k0, k1, a.out_tokens);
-    return cudaGetLastError();
+    return launch_dependent(verify_final_merge_kernel<TIn>, dim3((a.B + warps - 1) / warps), dim3(32 * warps), 0, s,
+                            (const ResidualState *)res_part, res_nsplit, (const int32_t *)final_code,
+                            (const int32_t *)a.accept_len, target, a.target_row0, a.n_target_rows, a.temperature,
+                            a.request_id, a.B, a.G, a.V, k0, k1, a.out_tokens);
 }
 
 }  // namespace
