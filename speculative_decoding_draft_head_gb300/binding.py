@@ -305,8 +305,8 @@ class LaggedScheduler:
 def verify_rows(target, verify_len, temperature, G, *, target_row0=None, r=16, workspace=None, stream=None):
     """The target-row statistics of verification alone (dspark_verify_rows),
     one block per SM so that it can run beside the draft kernel on another
-    stream.  Finish with :func:`verify` and ``rows_done=True`` on the same
-    workspace.  Returns the workspace."""
+    stream.  Finish with :func:`verify` and ``rows_done=True``, passing the
+    workspace this returns.  Returns the workspace."""
     lib = load()
     V = target.shape[-1]
     B = temperature.shape[0]
@@ -337,6 +337,10 @@ def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, re
     With ``rows_done`` only the second half runs (dspark_verify_finish) on a
     workspace that :func:`verify_rows` filled.
     Returns dict(accept_len, out_tokens, num_out, target_lse, logp)."""
+    if rows_done and workspace is None:
+        # the first half's results live in its workspace: name it (the default
+        # workspaces of the two calls need not be the same tensor)
+        raise ValueError("rows_done=True needs the workspace that verify_rows returned")
     lib = load()
     B, G = draft["tokens"].shape
     V = target.shape[-1]

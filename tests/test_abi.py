@@ -114,3 +114,15 @@ def test_split_verify_rejects_bad_host_arguments():
     st = lib.dspark_verify_finish(p, None, 0, None, None, None, None, p, p, p, p, None, p, None,
                                   4, 4, 1024, 16, 1, 0, p, p, p, None, None, p, 1 << 20, None)
     assert st == 1 and "draft_logits" in err()
+
+
+def test_finishing_half_needs_the_rows_workspace():
+    """verify(rows_done=True) must be given the workspace verify_rows filled;
+    the binding refuses before touching the device."""
+    import torch
+    B, G, V = 2, 3, 16
+    z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt)
+    draft = dict(tokens=z(B, G, dt=torch.int32), lse=z(B, G), logq=z(B, G))
+    with pytest.raises(ValueError, match="rows_done"):
+        binding.verify(z(B, G + 1, V), z(B, G, V), z(V, 16), z(V, 16), z(B, dt=torch.int32), draft, None,
+                       z(B), rows_done=True)
