@@ -61,7 +61,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -70,9 +70,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def stop(self):
+    def stop(self, region=None):
+        """Summary of the samples; with region = (t0, t1) (time.monotonic of the
+        timed region's start and end), of those read inside it."""
         if self.proc is None:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
         self.proc.terminate()
@@ -80,9 +82,19 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return summarize_clocks(self.lines, region)
+
+
+def summarize_clocks(lines, region=None):
+    """Median SM clock, maximum clock and active slowdown reasons of nvidia-smi
+    csv samples [(host time, line)].  With region = (t0, t1), only the samples
+    read inside it (plus one 25 ms sampling period after t1, the reader's lag)
+    count when there are any; `samples_in_region` says how many there were."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def parse(sel):
         sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for _, ln in sel:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -94,8 +106,15 @@ class ClockSampler:
             for n, p in zip(names, parts[3:7]):
                 if p.lower() == "active":
                     reasons.add(n)
-        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
-                    reasons=sorted(reasons), samples=len(sm))
+        return sm, smax, reasons
+
+    inside = [] if region is None else [x for x in lines if region[0] <= x[0] <= region[1] + 0.025]
+    sm, smax, reasons = parse(inside)
+    n_in = len(sm)
+    if not sm:  # the region was shorter than the sampling period
+        sm, smax, reasons = parse(lines)
+    return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
+                reasons=sorted(reasons), samples=len(sm), samples_in_region=n_in)
 
 
 def _dist_init(n):
@@ -156,7 +175,9 @@ def oracle_sample(w, h, seed, budget_s=12.0, threads=None):
     n = min(w.B, max(threads, 8))
     elapsed, done, positions = 0.0, 0, 0
     rid_all = h["request_id"].numpy().astype(np.uint32)
-    e_in, w_out = oracle._f64(h["e_in"]), oracle._f64(h["w_out"])
+    if "_f64" not in h:  # the weights in the oracle's input precision, converted once
+        h["_f64"] = (oracle._f64(h["e_in"]), oracle._f64(h["w_out"]))
+    e_in, w_out = h["_f64"]
     while done < w.B:
         reqs = np.arange(done, min(w.B, done + n))
         t0 = time.perf_counter()
@@ -189,7 +210,8 @@ def run_reference(args, w):
     vals = []
     info = None
     for i in range(args.warmup + args.steps):
-        budget = max(2.0, 60.0 / max(1, args.warmup + args.steps))
+        # about 90 s in all; a step is at least one batch of requests
+        budget = max(0.05, 90.0 / max(1, args.warmup + args.steps))
         r = oracle_sample(w, h, args.seed, budget_s=budget)
         if i >= args.warmup:
             vals.append(r["value"])
@@ -338,6 +360,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.monotonic()
     t0.record(stream)
     for _ in range(args.steps):
         if graph is not None:
@@ -346,9 +369,10 @@ def run_ours(args, w):
             step(inp)
     t1.record(stream)
     torch.cuda.synchronize()
+    h1 = time.monotonic()
     _barrier(world)
     ms = t0.elapsed_time(t1) / args.steps
-    clk = clocks.stop() if rank == 0 else None
+    clk = clocks.stop(region=(h0, h1)) if rank == 0 else None
     ms_max = _max_over_ranks(ms, world)
     total_positions = _sum_over_ranks(positions, world)
     value = total_positions / (ms_max / 1000.0)
@@ -535,7 +559,9 @@ def _read_traffic(w, kernel):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    # about a tenth of a second of timed rounds: several clock samples (every
+    # 25 ms) fall inside it
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dspark5")
