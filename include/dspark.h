@@ -119,7 +119,7 @@ DSPARK_API size_t dspark_workspace_bytes(int which, int B, int G, int V, int r);
  *
  * For each request b and j = 0 .. G-1, with prev = anchor[b] (j = 0) or
  * draft_tokens[b][j-1]:
- *   z[v]  = base_logits[b][j][v] + sum_k e_in[prev][k] * w_out[k][v]   (fp32)
+ *   z[v]  = base_logits[b][j][v] + sum_k e_in[prev][k] * w_out[v][k]   (fp32)
  *   T > 0: s = z / T, lse = log sum exp s, x_j drawn from softmax(s) by the
  *          group draw: with groups of 16 consecutive tokens (the last one may
  *          be ragged) and u0 = u(seed, request_id[b], j, 4 g, stream 0),
@@ -165,8 +165,9 @@ DSPARK_API dspark_status dspark_draft_sample(
  * weights of state unit n) and h_states: [B][G][r] bf16 output of the states
  * h_j, or NULL.  The state sum is compensated, and tanh is taken in fp32 and
  * redone in fp64 when the result lies near a bf16 rounding boundary, so h_j
- * is the exactly rounded value except within ~1e-13 of such a boundary.  dtype must be DSPARK_BF16 (else DSPARK_ERR_UNSUPPORTED).  The
- * workspace is DSPARK_WS_DRAFT_RNN.  Verify such a block with dspark_verify
+ * is the exactly rounded value except within ~1e-13 of such a boundary.
+ * dtype must be DSPARK_BF16 (else DSPARK_ERR_UNSUPPORTED).  The workspace is
+ * DSPARK_WS_DRAFT_RNN.  Verify such a block with dspark_verify
  * given the draft_logits this call stored (the draft distribution of the
  * rejected position is then read, not recomputed).
  */
