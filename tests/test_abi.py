@@ -126,3 +126,21 @@ def test_finishing_half_needs_the_rows_workspace():
     with pytest.raises(ValueError, match="rows_done"):
         binding.verify(z(B, G + 1, V), z(B, G, V), z(V, 16), z(V, 16), z(B, dt=torch.int32), draft, None,
                        z(B), rows_done=True)
+
+
+def test_pack_target_rejects_bad_host_arguments():
+    lib = binding.load()
+    vp = ctypes.c_void_p
+    p = vp(1 << 12)
+    err = lambda: lib.dspark_last_error().decode()
+    cases = [
+        ((p, None, 0, 4, 1024, 0, p, p, p, None), "bad B"),
+        ((p, None, 4, 65, 1024, 0, p, p, p, None), "bad B"),
+        ((p, None, 4, 4, 1001, 0, p, p, p, None), "multiple of 8"),
+        ((p, None, 4, 4, 1024, 7, p, p, p, None), "unknown dtype"),
+        ((None, None, 4, 4, 1024, 0, p, p, p, None), "NULL"),
+        ((p, None, 4, 4, 1024, 0, vp((1 << 12) + 8), p, p, None), "aligned"),
+    ]
+    for args, needle in cases:
+        st = lib.dspark_pack_target(*args)
+        assert st == 1 and needle in err(), (args, st, err())
