@@ -144,3 +144,20 @@ def test_pack_target_rejects_bad_host_arguments():
     for args, needle in cases:
         st = lib.dspark_pack_target(*args)
         assert st == 1 and needle in err(), (args, st, err())
+
+
+def test_recurrent_draft_rejects_bad_host_arguments():
+    lib = binding.load()
+    vp = ctypes.c_void_p
+    p = vp(1 << 12)
+    err = lambda: lib.dspark_last_error().decode()
+
+    def call(dt=0, r=16, wh=p, ws=p, wsb=1 << 24, hs=None):
+        return lib.dspark_draft_sample_rnn(p, p, wh, p, p, p, None, 4, 3, 1024, r, dt, 0, p, p, p, None, hs,
+                                           ws, wsb, None)
+    assert call(dt=1, r=16) == 2 and "bf16" in err()          # fp32 weights: unsupported
+    assert call(r=24) == 1 and "r % 16" in err()
+    assert call(wh=None) == 1 and "NULL" in err()
+    assert call(wh=vp((1 << 12) + 8)) == 1 and "aligned" in err()
+    assert call(hs=vp((1 << 12) + 1)) == 1 and "aligned" in err()
+    assert call(wsb=16) == 1 and "too small" in err()
