@@ -161,3 +161,20 @@ def test_recurrent_draft_rejects_bad_host_arguments():
     assert call(wh=vp((1 << 12) + 8)) == 1 and "aligned" in err()
     assert call(hs=vp((1 << 12) + 1)) == 1 and "aligned" in err()
     assert call(wsb=16) == 1 and "too small" in err()
+
+
+def test_selftest_and_noalloc_reject_on_the_host():
+    lib = binding.load()
+    vp = ctypes.c_void_p
+    p = vp(1 << 12)
+    err = lambda: lib.dspark_last_error().decode()
+    res = ctypes.cast(vp(1 << 12), ctypes.POINTER(ctypes.c_uint32))
+    assert lib.dspark_selftest_bounded_wait(0, res, None) == 1 and "limit_us" in err()
+    assert lib.dspark_selftest_bounded_wait(2000000, res, None) == 1 and "limit_us" in err()
+    assert lib.dspark_selftest_bounded_wait(10, None, None) == 1 and "NULL" in err()
+    # a verification whose scratch exceeds the fixed array: unsupported, no launch
+    args = [p] * 12 + [20096, 16, 129280, 256, 0, 0] + [p] * 6
+    assert lib.dspark_verify_noalloc(*args) == 2 and "fixed" in err()
+    # an invalid size is reported as dspark_verify reports it
+    args = [p] * 12 + [4, 0, 1024, 16, 0, 0] + [p] * 6
+    assert lib.dspark_verify_noalloc(*args) == 1 and "G must be" in err()
