@@ -10,13 +10,16 @@ marshals numpy arrays into it.
 Parity status per function (what pins each one is listed in the test suite):
   philox4x32_10 / uniform / gumbel : pinned (cuRAND host generator, uniformity,
                                      range bounds)
-  draft_sample                     : pinned (chi-square vs softmax, closed-form
-                                     rows, textbook matmul, Markov toy)
+  draft_sample                     : pinned (per-token Gumbel-max: argmax of the
+                                     uniforms on constant rows, chi-square vs
+                                     softmax over 10^6 draws, textbook matmul,
+                                     Markov toy)
   schedule                         : pinned (brute force over length vectors,
                                      closed-form threshold, sigmoid identities)
   verify                           : pinned (1 - TV acceptance, expected tokens
-                                     per pass, exact output distribution by
-                                     enumeration and chi-square, greedy limit)
+                                     per pass, the exact output law by brute-force
+                                     enumeration against 10^6 oracle rounds,
+                                     residual and bonus laws, greedy limit)
 """
 from __future__ import annotations
 
@@ -86,7 +89,7 @@ def lib():
             L.or_draft_sample.argtypes = [
                 _f64p, _f64p, _f64p, _i32p, _f64p, nu,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
-                _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, nf]
+                _i32p, _f64p, _f64p, _f64p, _f64p, nf]
             L.or_draft_sample.restype = ctypes.c_int
             L.or_schedule.argtypes = [
                 _f64p, _f64p, _f64p, ctypes.c_int,
@@ -96,7 +99,7 @@ def lib():
             L.or_draft_sample_rnn.argtypes = [
                 _f64p, _f64p, _f64p, _f64p, _i32p, _f64p, nu,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
-                _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, nf]
+                _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, nf]
             L.or_draft_sample_rnn.restype = ctypes.c_int
             L.or_schedule_policy.argtypes = [
                 _f64p, _f64p, _f64p, ctypes.c_int,
@@ -106,7 +109,7 @@ def lib():
             L.or_verify.argtypes = [
                 _f64p, _f64p, _f64p, _f64p, _i32p, _i32p, ni, _f64p, nu,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
-                _i32p, _i32p, _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _i32p]
+                _i32p, _i32p, _i32p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _i32p]
             L.or_verify.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -175,8 +178,8 @@ def draft_sample(U, E_in, W_out, anchor, temp, rid=None, seed=0, want_z=False):
 
     U [B,G,V], E_in [V,r], W_out [V,r] (row v scores token v), anchor [B], temp [B],
     rid [B] or None.
-    Returns a dict of numpy arrays: tokens, lse, logq, gap, top, cdf_margin
-    (all [B,G]), and z [B,G,V] when ``want_z``.
+    Returns a dict of numpy arrays: tokens, lse, logq, gap, top (all [B,G]),
+    and z [B,G,V] when ``want_z``.
     """
     U = _f64(U)
     E_in = _f64(E_in)
@@ -188,12 +191,10 @@ def draft_sample(U, E_in, W_out, anchor, temp, rid=None, seed=0, want_z=False):
     temp = _f64(temp)
     rid = _u32(rid)
     out = dict(tokens=np.zeros((B, G), np.int32), lse=np.zeros((B, G)),
-               logq=np.zeros((B, G)), gap=np.zeros((B, G)), top=np.zeros((B, G)),
-               cdf_margin=np.zeros((B, G)))
+               logq=np.zeros((B, G)), gap=np.zeros((B, G)), top=np.zeros((B, G)))
     z = np.zeros((B, G, V)) if want_z else None
     rc = lib().or_draft_sample(U, E_in, W_out, anchor, temp, rid, B, G, V, r, seed,
-                               out["tokens"], out["lse"], out["logq"], out["gap"], out["top"],
-                               out["cdf_margin"], z)
+                               out["tokens"], out["lse"], out["logq"], out["gap"], out["top"], z)
     if rc != 0:
         raise ValueError("or_draft_sample failed: %d" % rc)
     if want_z:
@@ -218,11 +219,11 @@ def draft_sample_rnn(U, E_in, W_h, W_out, anchor, temp, rid=None, seed=0, want_z
     rid = _u32(rid)
     out = dict(tokens=np.zeros((B, G), np.int32), lse=np.zeros((B, G)),
                logq=np.zeros((B, G)), gap=np.zeros((B, G)), top=np.zeros((B, G)),
-               cdf_margin=np.zeros((B, G)), h=np.zeros((B, G, r)), h_margin=np.zeros((B, G)))
+               h=np.zeros((B, G, r)), h_margin=np.zeros((B, G)))
     z = np.zeros((B, G, V)) if want_z else None
     rc = lib().or_draft_sample_rnn(U, E_in, W_h, W_out, anchor, temp, rid, B, G, V, r, seed,
                                    out["tokens"], out["lse"], out["logq"], out["gap"], out["top"],
-                                   out["cdf_margin"], out["h"], out["h_margin"], z)
+                                   out["h"], out["h_margin"], z)
     if rc != 0:
         raise ValueError("or_draft_sample_rnn failed: %d" % rc)
     if want_z:
@@ -292,12 +293,11 @@ def verify(target, U, E_in, W_out, anchor, draft_tokens, verify_len, temp, rid=N
     out = dict(accept_len=np.zeros(B, np.int32), out_tokens=np.zeros((B, G + 1), np.int32),
                num_out=np.zeros(B, np.int32), target_lse=np.zeros((B, G + 1)),
                logp=np.zeros((B, G)), logq=np.zeros((B, G)), accept_margin=np.zeros((B, G)),
-               final_gap=np.zeros(B), final_top=np.zeros(B), final_cdf=np.zeros(B),
-               final_kind=np.zeros(B, np.int32))
+               final_gap=np.zeros(B), final_top=np.zeros(B), final_kind=np.zeros(B, np.int32))
     rc = lib().or_verify(target, U, E_in, W_out, anchor, dt, vl, temp, rid, B, G, V, r, seed,
                          out["accept_len"], out["out_tokens"], out["num_out"], out["target_lse"],
                          out["logp"], out["logq"], out["accept_margin"], out["final_gap"],
-                         out["final_top"], out["final_cdf"], out["final_kind"])
+                         out["final_top"], out["final_kind"])
     if rc != 0:
         raise ValueError("or_verify failed: %d" % rc)
     return out

@@ -139,65 +139,28 @@ static int row_argmax(const double *s, int V, double *gap, double *top)
     return best;
 }
 
-/* Draw from softmax(s) in two stages (reading R2b): the vocabulary is cut into
- * groups of DRAW_GROUP consecutive tokens (the last one ragged).  With
- * (w0, w1, w2, w3) the Philox block at counter (g, j, rid, stream), i.e.
- * u0 = or_uniform(.., 4 g, stream) and u1 = or_uniform(.., 4 g + 1, stream):
- *   group key   K_g = log sum_{v in g} exp(s_v) + G(u0),  G(u) = -log(-log u);
- *   winner      g* = argmax_g K_g (lowest g on exact ties);
- *   token       the first v of g* whose running sum sum_{v' <= v} exp(s_v')
- *               exceeds u1 * sum_{v in g*} exp(s_v) (inverse CDF in group order).
- * The maximum of Gumbels is Gumbel at their log-sum-exp and its argmax is
- * independent of its value, so the token has law softmax(s) exactly.
- * gap / top: the top-two group keys' difference and the top key; cdf_margin:
- * the smallest |running sum - u1 * group sum| over the group's boundaries (how
- * close the in-group draw came to a neighbour), divided by the group's sum of
- * exp(s), or by the group's sum of err_scale (linear units, exp(s) measured
- * against it) when err_scale is not NULL: a residual max(0, p - q) is computed
- * on the device from p and q, whose size sets its absolute error. */
-#define DRAW_GROUP 16
-static int group_draw(const double *s, const double *err_scale, int V, uint64_t seed, uint32_t rid,
-                      uint32_t j, uint32_t stream, double *gap, double *top, double *cdf_margin)
+/* Gumbel-max draw with one random word per token, keyed on (seed, request,
+ * position, token, stream) (reading R1):
+ *   x = argmax_v ( w_v + g(u_{stream, j, v}) ),  g(u) = -log(-log u),
+ * over the entries with w_v > -inf, the lowest id on exact ties.  With w the
+ * logits s = z / T this draws x with probability softmax(s)_x exactly; with
+ * w_v = log r_v it draws from r normalised.  Every token takes its own word
+ * (or_uniform at token v).  gap / top: the difference of the two largest keys
+ * and the largest key (how close the draw came to a tie). */
+static int gumbel_max(const double *w, int V, uint64_t seed, uint32_t rid, uint32_t j, uint32_t stream,
+                      double *gap, double *top)
 {
-    double m = -INFINITY;
-    for (int v = 0; v < V; ++v) if (s[v] > m) m = s[v];
-    int gbest = -1;
+    int best = -1;
     double k1 = -INFINITY, k2 = -INFINITY;
-    for (int g0 = 0; g0 < V; g0 += DRAW_GROUP) {
-        int g1 = g0 + DRAW_GROUP < V ? g0 + DRAW_GROUP : V;
-        double sum = 0.0;
-        for (int v = g0; v < g1; ++v) sum += exp(s[v] - m);
-        if (!(sum > 0.0)) continue;
-        uint32_t g = (uint32_t)(g0 / DRAW_GROUP);
-        double key = m + log(sum) - log(-log(or_uniform(seed, rid, j, 4u * g, stream)));
-        if (gbest < 0 || key > k1) { k2 = k1; k1 = key; gbest = (int)g; }
+    for (int v = 0; v < V; ++v) {
+        if (w[v] == -INFINITY) continue;
+        double key = w[v] + or_gumbel(seed, rid, j, (uint32_t)v, stream);
+        if (best < 0 || key > k1) { k2 = k1; k1 = key; best = v; }
         else if (key > k2) { k2 = key; }
     }
     if (gap) *gap = k1 - k2;
     if (top) *top = k1;
-    int g0 = gbest * DRAW_GROUP, g1 = g0 + DRAW_GROUP < V ? g0 + DRAW_GROUP : V;
-    double sum = 0.0;
-    for (int v = g0; v < g1; ++v) sum += exp(s[v] - m);
-    double target = or_uniform(seed, rid, j, 4u * (uint32_t)gbest + 1u, stream) * sum;
-    double norm = sum;
-    if (err_scale) {
-        norm = 0.0;
-        for (int v = g0; v < g1; ++v) norm += err_scale[v] * exp(-m);
-    }
-    int x = -1;
-    double run = 0.0, margin = INFINITY;
-    for (int v = g0; v < g1; ++v) {
-        double e = exp(s[v] - m);
-        run += e;
-        if (e > 0.0) {
-            double d = fabs(run - target) / norm;
-            if (d < margin) margin = d;
-        }
-        if (x < 0 && run > target) x = v;
-    }
-    if (x < 0) for (int v = g1 - 1; v >= g0; --v) if (exp(s[v] - m) > 0.0) { x = v; break; }
-    if (cdf_margin) *cdf_margin = margin;
-    return x;
+    return best;
 }
 
 /* [DSP-IT] "Un po' di autoregressione basta", equation for p_k, with the
@@ -222,17 +185,16 @@ static void markov_logits(const double *U_row, const double *E_in, const double 
 /* probability; the sampled token feeds the next position's bias).            */
 /*                                                                           */
 /* U [B][G][V], E_in [V][r], W_out [V][r], anchor [B], temp [B], rid [B]      */
-/* (NULL = 0..B-1).  Outputs [B][G]: tokens (group_draw, reading R2b), lse   */
-/* (T = 0: max z), logq (T = 0: 0), gap / top of the deciding group keys      */
-/* (T = 0: of the logits), cdf_margin of the in-group draw (T = 0: +inf);     */
-/* z_out [B][G][V] optional.                                                  */
+/* (NULL = 0..B-1).  Outputs [B][G]: tokens (Gumbel-max on stream 0), lse     */
+/* (T = 0: max z), logq (T = 0: 0), gap / top of the two largest keys (T = 0: */
+/* of the logits); z_out [B][G][V] optional.                                  */
 /* Returns 0, or -1 on an out-of-range anchor.                                */
 /* ------------------------------------------------------------------------ */
 int or_draft_sample(const double *U, const double *E_in, const double *W_out,
                     const int32_t *anchor, const double *temp, const uint32_t *rid,
                     int B, int G, int V, int r, uint64_t seed,
                     int32_t *tokens, double *lse, double *logq, double *gap, double *top,
-                    double *cdf_margin, double *z_out)
+                    double *z_out)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
     double *s = (double *)malloc(sizeof(double) * (size_t)V);
@@ -251,12 +213,11 @@ int or_draft_sample(const double *U, const double *E_in, const double *W_out,
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) s[v] = z[v] / T;
                 double l = row_logsumexp(s, V);
-                x = group_draw(s, NULL, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
+                x = gumbel_max(s, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o]);
                 lse[o] = l;
                 logq[o] = s[x] - l;
             } else {
                 x = row_argmax(z, V, &gap[o], &top[o]);
-                cdf_margin[o] = INFINITY;
                 lse[o] = z[x];
                 logq[o] = 0.0;
             }
@@ -299,7 +260,7 @@ int or_draft_sample_rnn(const double *U, const double *E_in, const double *W_h, 
                         const int32_t *anchor, const double *temp, const uint32_t *rid,
                         int B, int G, int V, int r, uint64_t seed,
                         int32_t *tokens, double *lse, double *logq, double *gap, double *top,
-                        double *cdf_margin, double *h_out, double *h_margin, double *z_out)
+                        double *h_out, double *h_margin, double *z_out)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
     double *s = (double *)malloc(sizeof(double) * (size_t)V);
@@ -339,12 +300,11 @@ int or_draft_sample_rnn(const double *U, const double *E_in, const double *W_h, 
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) s[v] = z[v] / T;
                 double l = row_logsumexp(s, V);
-                x = group_draw(s, NULL, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o], &cdf_margin[o]);
+                x = gumbel_max(s, V, seed, id, (uint32_t)j, 0u, &gap[o], &top[o]);
                 lse[o] = l;
                 logq[o] = s[x] - l;
             } else {
                 x = row_argmax(z, V, &gap[o], &top[o]);
-                cdf_margin[o] = INFINITY;
                 lse[o] = z[x];
                 logq[o] = 0.0;
             }
@@ -572,7 +532,7 @@ int or_schedule_policy(const double *conf_logits, const double *pos_temp, const 
 /* at the first rejection and resample from the residual distribution;       */
 /* [DSP-ZH] "DSpark 是什么？": append a bonus token when the whole block is   */
 /* accepted), readings R5 and R6; the residual, fallback and bonus draws    */
-/* are group draws (R2b) on streams 2, 2 and 3.                              */
+/* are Gumbel-max draws on streams 2, 2 and 3.                               */
 /*                                                                           */
 /* target [B][G+1][V]: row j is the target's logits for draft position j,    */
 /* row L_b gives the bonus.  The draft side is recomputed here from U, E_in, */
@@ -580,9 +540,9 @@ int or_schedule_policy(const double *conf_logits, const double *pos_temp, const 
 /* Outputs: accept_len [B], out_tokens [B][G+1] (-1 padded), num_out [B],    */
 /* target_lse [B][G+1] (NaN where not read; T = 0: max t), logp / logq       */
 /* [B][G] (NaN where not tested), accept_margin [B][G] = |u - min(1, p/q)|   */
-/* (NaN where not tested), final_gap / final_top / final_cdf [B] for the    */
-/* last draw (group_draw's gap, top and cdf_margin; greedy: the logits' gap */
-/* and +inf), final_kind [B] = 0 bonus, 1 residual, 2 residual fell back to p,*/
+/* (NaN where not tested), final_gap / final_top [B] for the last draw (the  */
+/* two largest Gumbel keys' gap and the largest; greedy: of the logits),     */
+/* final_kind [B] = 0 bonus, 1 residual, 2 residual fell back to p,          */
 /* 3 greedy correction.  Returns 0, -1 on invalid input.                     */
 /* ------------------------------------------------------------------------ */
 int or_verify(const double *target, const double *U, const double *E_in, const double *W_out,
@@ -591,16 +551,15 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
               int B, int G, int V, int r, uint64_t seed,
               int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
               double *target_lse, double *logp, double *logq, double *accept_margin,
-              double *final_gap, double *final_top, double *final_cdf, int32_t *final_kind)
+              double *final_gap, double *final_top, int32_t *final_kind)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)V);
     double *s = (double *)malloc(sizeof(double) * (size_t)V);
     double *st = (double *)malloc(sizeof(double) * (size_t)V);
     double *w = (double *)malloc(sizeof(double) * (size_t)V);
-    double *pq = (double *)malloc(sizeof(double) * (size_t)V);
     unsigned char *allowed = (unsigned char *)malloc((size_t)V);
-    if (!z || !s || !st || !w || !pq || !allowed) {
-        free(z); free(s); free(st); free(w); free(pq); free(allowed);
+    if (!z || !s || !st || !w || !allowed) {
+        free(z); free(s); free(st); free(w); free(allowed);
         return -2;
     }
     int rc = 0;
@@ -624,7 +583,7 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
         int k = 0;         /* number of accepted draft tokens */
         int y = -1;        /* the final (resampled or bonus) token */
         int kind = 0;
-        double fgap = NAN, ftop = NAN, fcdf = INFINITY;
+        double fgap = NAN, ftop = NAN;
         for (int j = 0; j < L; ++j) {
             const double *t_row = target + ((size_t)b * (G + 1) + j) * (size_t)V;
             int x = draft_tokens[(size_t)b * G + j];
@@ -652,14 +611,13 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
                     double pv = exp(st[v] - lt), qv = exp(s[v] - lq);
                     allowed[v] = (unsigned char)(pv > qv);
                     w[v] = allowed[v] ? log(pv - qv) : -INFINITY;
-                    pq[v] = pv + qv;
                     any |= allowed[v];
                 }
                 if (any) {
-                    y = group_draw(w, pq, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop, &fcdf);
+                    y = gumbel_max(w, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop);
                     kind = 1;
                 } else {
-                    y = group_draw(st, NULL, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop, &fcdf);
+                    y = gumbel_max(st, V, seed, id, (uint32_t)j, 2u, &fgap, &ftop);
                     kind = 2;
                 }
                 break;
@@ -679,7 +637,7 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
             const double *t_row = target + ((size_t)b * (G + 1) + L) * (size_t)V;
             if (T > 0.0) {
                 for (int v = 0; v < V; ++v) st[v] = t_row[v] / T;
-                y = group_draw(st, NULL, V, seed, id, (uint32_t)L, 3u, &fgap, &ftop, &fcdf);
+                y = gumbel_max(st, V, seed, id, (uint32_t)L, 3u, &fgap, &ftop);
             } else {
                 double top;
                 y = row_argmax(t_row, V, &fgap, &top);
@@ -694,9 +652,8 @@ int or_verify(const double *target, const double *U, const double *E_in, const d
         num_out[b] = k + 1;
         final_gap[b] = fgap;
         final_top[b] = ftop;
-        final_cdf[b] = fcdf;
         final_kind[b] = kind;
     }
-    free(z); free(s); free(st); free(w); free(pq); free(allowed);
+    free(z); free(s); free(st); free(w); free(allowed);
     return rc;
 }
