@@ -24,6 +24,7 @@ dspark_status check_common(int B, int G, int V, int r, dspark_dtype dt) {
     if (B < 1) return fail(DSPARK_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
     if (G < 1 || G > kMaxG) return fail(DSPARK_ERR_INVALID_ARG, "G must be in [1, %d] (got %d)", kMaxG, G);
     if (V < 8 || V % 8 != 0) return fail(DSPARK_ERR_INVALID_ARG, "V must be a positive multiple of 8 (got %d)", V);
+    if (V > kMaxV) return fail(DSPARK_ERR_UNSUPPORTED, "V must be at most %d (got %d)", kMaxV, V);
     if (dt != DSPARK_BF16 && dt != DSPARK_F32) return fail(DSPARK_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
     if (r < 1 || r > 256) return fail(DSPARK_ERR_INVALID_ARG, "r must be in [1, 256] (got %d)", r);
     if (dt == DSPARK_BF16 && r % 16 != 0) return fail(DSPARK_ERR_INVALID_ARG, "bf16 needs r %% 16 == 0 (got %d)", r);

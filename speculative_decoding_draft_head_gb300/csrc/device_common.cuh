@@ -6,9 +6,14 @@
 // top 23 bits of the word and centres it in its cell: u = (k + 1/2) 2^-23.
 //
 // Scores are kept in log2 units: s2 = z * log2(e) / T.  The online softmax
-// holds (m, S) with S = sum 2^(s2 - m), so lse = ln 2 * (m + log2 S); the
-// Gumbel-max key of token v is s2_v - log2(E_v) with E_v = -ln u_v, which
-// orders tokens exactly as the natural-log key s_v - ln(E_v) = s_v + g_v.
+// holds (m, S) with S = sum 2^(s2 - m) and an integer reference m, so that
+// rescaling a partial sum is an exact power-of-two scaling and lse =
+// ln 2 * (m + log2 S).  The Gumbel-max key of token v is s_v + g(u_v) with
+// s_v = z_v / T and g(u) = -ln(-ln u).  Tokens are screened in fp32 (log2
+// units, no logarithm for almost all of them); the few that can still win get
+// their key in float-float arithmetic (about 44 significant bits), so the
+// winner agrees with an fp64 evaluation of the same keys except on ties far
+// below fp32 rounding.
 #pragma once
 
 #include <cstdint>
@@ -47,6 +52,19 @@ __device__ __forceinline__ const T *target_row(const T *target, const int64_t *r
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// c2 = log2(e) / T as float-float (hi, lo).  A logit's exponent z c2 - m is
+// formed as fmaf(z, lo, fmaf(z, hi, -m)): rounding c2 to fp32 alone would
+// shift every exponent by about 6e-8 |z c2| (3e-6 nats at |z / T| = 50).
+__device__ __forceinline__ float2 c2_split(float T) {
+    constexpr float kLog2eHi = 1.44269502162933349609375f;  // fp32(log2 e)
+    constexpr float kLog2eLo = 1.925963e-08f;               // log2 e - kLog2eHi
+    const float hi = __fdiv_rn(kLog2eHi, T);
+    const float rem = fmaf(-hi, T, kLog2eHi);               // exact
+    return make_float2(hi, __fdiv_rn(rem + kLog2eLo, T));
+}
+// 2^(z c2 - m) with c2 = (c2h, c2l) from c2_split.
+__device__ __forceinline__ float term_exp2(float z, float c2h, float c2l, float m);
 
 // Ten rounds of the Philox4x32 bijection.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
@@ -161,15 +179,149 @@ __device__ __forceinline__ float elem(const float4 &f, int e) {
     return e == 0 ? f.x : (e == 1 ? f.y : (e == 2 ? f.z : f.w));
 }
 
-// Running state of one row segment: online softmax (m, S) and the best key.
-// T > 0: m = max s2, S = sum 2^(s2 - m), key = best s2 - log2(E), s_at = s2
-// at the best token.  T = 0: key = m = max z, s_at = z at the best token.
+// ------------------------------------------------------------ keys ----
+// Float keys as unsigned integers whose order is the float order, so that a
+// row-wide running best can be kept with atomicMax.  0 encodes "none" (-inf).
+__device__ __forceinline__ uint32_t key_to_ordered(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ordered_to_key(uint32_t o) {
+    if (o == 0u) return -INFINITY;
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+// A float-float number hi + lo with |lo| <= ulp(hi) / 2.
+struct FF {
+    float hi, lo;
+};
+
+// a + b exactly (Knuth's two-sum).
+__device__ __forceinline__ FF two_sum(float a, float b) {
+    const float s = a + b;
+    const float bv = s - a;
+    const float av = s - bv;
+    return FF{s, (a - av) + (b - bv)};
+}
+// a + b exactly when |a| >= |b| (or a == 0): the normalising step.
+__device__ __forceinline__ FF quick_two_sum(float a, float b) {
+    const float s = a + b;
+    return FF{s, b - (s - a)};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const FF s = two_sum(a.hi, b.hi);
+    return quick_two_sum(s.hi, s.lo + (a.lo + b.lo));
+}
+__device__ __forceinline__ FF ff_neg(FF a) { return FF{-a.hi, -a.lo}; }
+
+// Natural logarithm of a positive normal float as float-float, from
+// ln x = e ln 2 + ln m with m in [sqrt(1/2), sqrt(2)) and
+// ln m = 2 atanh(t), t = (m - 1) / (m + 1), |t| <= 0.1716:
+// 2 atanh(t) = 2t + t^3 (2/3 + 2/5 t^2 + 2/7 t^4 + ...) (the Taylor series of
+// atanh).  t is formed in float-float; the series tail (below 0.0034) in fp32.
+// Absolute error about 1e-10 for the arguments used here.
+__device__ __forceinline__ FF ln_ff(float x) {
+    const uint32_t ix = __float_as_uint(x);
+    int e = (int)((ix >> 23) & 0xFFu) - 127;
+    uint32_t mb = (ix & 0x7FFFFFu) | 0x3F800000u;  // m in [1, 2)
+    if (mb > 0x3FB504F3u) {                         // m > sqrt(2): halve it
+        mb -= 0x00800000u;
+        e += 1;
+    }
+    const float m = __uint_as_float(mb);
+    const float f = m - 1.f;             // exact (Sterbenz)
+    const FF d = two_sum(m, 1.f);        // m + 1
+    const float rd = __frcp_rn(d.hi);
+    const float t_hi = f * rd;
+    float rem = fmaf(-t_hi, d.hi, f);    // f - t_hi (d.hi + d.lo)
+    rem = fmaf(-t_hi, d.lo, rem);
+    const float t_lo = rem * rd;
+    const float t2 = t_hi * t_hi;
+    float P = 2.f / 13.f;
+    P = fmaf(P, t2, 2.f / 11.f);
+    P = fmaf(P, t2, 2.f / 9.f);
+    P = fmaf(P, t2, 2.f / 7.f);
+    P = fmaf(P, t2, 2.f / 5.f);
+    P = fmaf(P, t2, 2.f / 3.f);
+    const float tail = t_hi * t2 * P;
+    // ln 2 split so that e * kLn2Hi is exact for |e| < 256
+    constexpr float kLn2Hi = 0.693145751953125f;        // 0x3F317200
+    constexpr float kLn2Lo = 1.4286068203094172e-06f;   // ln 2 - kLn2Hi
+    const float fe = (float)e;
+    const FF a = two_sum(fe * kLn2Hi, 2.f * t_hi);
+    return quick_two_sum(a.hi, a.lo + fmaf(fe, kLn2Lo, fmaf(2.f, t_lo, tail)));
+}
+
+// s = z / T as float-float (rT = fl(1 / T); the residual z - s_hi T is exact).
+__device__ __forceinline__ FF div_ff(float z, float T, float rT) {
+    const float hi = z * rT;
+    const float lo = fmaf(-hi, T, z) * rT;
+    return quick_two_sum(hi, lo);
+}
+
+// g(u) = -ln(-ln u) for the uniform of word w, as float-float.
+__device__ __forceinline__ FF gumbel_ff(uint32_t w) {
+    const FF l = ln_ff(word_to_uniform(w));         // ln u < 0, u exact in fp32
+    const FF L = ln_ff(-l.hi);                       // ln E, E = -ln u = -(l.hi + l.lo)
+    // ln(E_hi + E_lo) = ln E_hi + E_lo / E_hi (|E_lo / E_hi| <= 2^-24)
+    const float corr = -l.lo * __frcp_rn(-l.hi);
+    return quick_two_sum(-L.hi, -(L.lo + corr));
+}
+
+// The row-wide best draw as one 64-bit word whose unsigned order is the order
+// of the keys, the lowest token id winning an exact tie: the key's high part
+// in the order-preserving encoding (32 bits), its low part as a signed
+// fraction of ulp(hi) in 12 bits, and the complemented token id in 20 bits
+// (vocabularies up to 2^20).  0 means "none".
+constexpr int kTokenBits = 20;
+constexpr uint32_t kTokenMask = (1u << kTokenBits) - 1u;
+__device__ __forceinline__ unsigned long long key_word(FF k, int idx) {
+    const uint32_t oh = key_to_ordered(k.hi);
+    uint32_t q = 2048u;
+    const uint32_t e = (__float_as_uint(k.hi) >> 23) & 0xFFu;
+    if (e >= 35u && e < 255u) {
+        // lo / ulp(hi) * 4096 = lo * 2^(162 - e), in [-2048, 2048]
+        const int qi = __float2int_rn(k.lo * __uint_as_float((289u - e) << 23));
+        q = (uint32_t)(min(2047, max(-2047, qi)) + 2048);
+    }
+    return ((unsigned long long)oh << 32) | ((unsigned long long)q << kTokenBits) |
+           (unsigned long long)(~(uint32_t)idx & kTokenMask);
+}
+__device__ __forceinline__ int word_token(unsigned long long w) {
+    return w ? (int)(~(uint32_t)w & kTokenMask) : -1;
+}
+// The key's high part (natural-log units) of a word, -inf for "none".
+__device__ __forceinline__ float word_key_hi(unsigned long long w) { return ordered_to_key((uint32_t)(w >> 32)); }
+
+// The screening factor Q = 2^(m - K log2 e) (capped at 2^126) times a margin
+// that covers the fp32 rounding of the exponents (relative 4e-7 of their
+// size); K = -inf (no key yet) lets every token with mass through.
+__device__ __forceinline__ float screen_q(float m, float kbest) {
+    if (kbest == -INFINITY) return INFINITY;
+    const float K2 = kbest * kLog2e;
+    return fminf(fast_exp2(m - K2), 0x1p126f) * (1.f + 4e-7f * (fabsf(K2) + fabsf(m) + 64.f));
+}
+
+// Tolerance of an fp32 key (log2 units) against the threshold K2: the
+// rounding of z c2, of c2 itself, of -ln u and lg2, and of K2.
+__device__ __forceinline__ float key_tol2(float k2, float K2) {
+    return 4e-7f * (fabsf(k2) + fabsf(K2)) + 2e-6f;
+}
+
+// 2^k for an integer-valued float k (exact power of two; 0 below 2^-149).
+__device__ __forceinline__ float scale_pow2(float S, float k) {
+    return (k < -300.f) ? 0.f : ldexpf(S, (int)k);
+}
+
+// Running state of one row segment: online softmax (m, S) and the best draw.
+// T > 0: m an integer reference (log2 units), S = sum 2^(s2 - m), best the
+// best key word, z_at the logit z of that token.  T = 0: m = max z, best the
+// word of (max z, lowest id), z_at = max z.
 struct RowState {
     float m;
     float S;
-    float key;
-    float s_at;
-    int idx;      // best index, INT32_MAX if none
+    unsigned long long best;
+    float z_at;
     int pad0, pad1, pad2;
 };
 static_assert(sizeof(RowState) == 32, "RowState is stored as two 16-byte words");
@@ -178,30 +330,24 @@ __device__ __forceinline__ RowState row_state_init() {
     RowState st;
     st.m = -INFINITY;
     st.S = 0.f;
-    st.key = -INFINITY;
-    st.s_at = 0.f;
-    st.idx = INT32_MAX;
+    st.best = 0ull;
+    st.z_at = 0.f;
     st.pad0 = st.pad1 = st.pad2 = 0;
     return st;
 }
 
-__device__ __forceinline__ bool key_better(float ka, int ia, float kb, int ib) {
-    return ka > kb || (ka == kb && ia < ib);
-}
-
-// Merge b into a (associative; ties on the key go to the lower index).
+// Merge b into a (associative; the larger word wins).
 __device__ __forceinline__ void row_state_merge(RowState &a, const RowState &b) {
     const float m = fmaxf(a.m, b.m);
     if (m != -INFINITY) {
-        const float sa = (a.m == -INFINITY) ? 0.f : a.S * exp2f(a.m - m);
-        const float sb = (b.m == -INFINITY) ? 0.f : b.S * exp2f(b.m - m);
+        const float sa = (a.m == -INFINITY) ? 0.f : scale_pow2(a.S, a.m - m);
+        const float sb = (b.m == -INFINITY) ? 0.f : scale_pow2(b.S, b.m - m);
         a.S = sa + sb;
         a.m = m;
     }
-    if (key_better(b.key, b.idx, a.key, a.idx)) {
-        a.key = b.key;
-        a.s_at = b.s_at;
-        a.idx = b.idx;
+    if (b.best > a.best) {
+        a.best = b.best;
+        a.z_at = b.z_at;
     }
 }
 
@@ -209,9 +355,8 @@ __device__ __forceinline__ RowState shfl_xor_state(const RowState &s, int mask) 
     RowState o;
     o.m = __shfl_xor_sync(0xffffffffu, s.m, mask);
     o.S = __shfl_xor_sync(0xffffffffu, s.S, mask);
-    o.key = __shfl_xor_sync(0xffffffffu, s.key, mask);
-    o.s_at = __shfl_xor_sync(0xffffffffu, s.s_at, mask);
-    o.idx = __shfl_xor_sync(0xffffffffu, s.idx, mask);
+    o.best = __shfl_xor_sync(0xffffffffu, s.best, mask);
+    o.z_at = __shfl_xor_sync(0xffffffffu, s.z_at, mask);
     o.pad0 = o.pad1 = o.pad2 = 0;
     return o;
 }
@@ -225,44 +370,78 @@ __device__ __forceinline__ RowState warp_merge(RowState s) {
     return s;
 }
 
-// Online-softmax step with a group of n scores (log2 units), n <= 16.
-template <int N>
-__device__ __forceinline__ void softmax_push_group(RowState &st, const float (&s2)[N], int n) {
-    float cm = -INFINITY;
+// The natural-log log-sum-exp of partial states (m_i, S_i) of one row, in
+// double: the partial sums are rescaled exactly (integer references) and
+// added in double.  Every lane of the warp calls it; lane i reads partials
+// i, i + 32, ...  Returns -inf for an empty row.
+__device__ __forceinline__ double warp_lse_of_partials(const RowState *part, int n) {
+    float m = -INFINITY;
+    for (int i = threadIdx.x & 31; i < n; i += 32) m = fmaxf(m, part[i].m);
 #pragma unroll
-    for (int i = 0; i < N; ++i)
-        if (i < n) cm = fmaxf(cm, s2[i]);
-    if (cm > st.m) {
-        st.S = (st.m == -INFINITY) ? 0.f : st.S * fast_exp2(st.m - cm);
-        st.m = cm;
+    for (int k = 16; k > 0; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+    if (m == -INFINITY) return -INFINITY;
+    double S = 0.0;
+    for (int i = threadIdx.x & 31; i < n; i += 32) {
+        const RowState &p = part[i];
+        if (p.m != -INFINITY && p.S > 0.f) S += ldexp((double)p.S, (int)fmaxf(p.m - m, -1100.f));
+    }
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) S += __shfl_xor_sync(0xffffffffu, S, k);
+    return 0.6931471805599453 * ((double)m + log2(S));
+}
+
+__device__ __forceinline__ float term_exp2(float z, float c2h, float c2l, float m) {
+    return fast_exp2(fmaf(z, c2l, fmaf(z, c2h, -m)));
+}
+
+// Online-softmax step with the logits z[0..N) of one row (c2 = (c2h, c2l)),
+// against an integer reference m (log2 units) that may lag the maximum
+// (terms above 1 are fine; a group whose sum leaves [0, 2^64] is redone
+// against its own maximum, an exact power-of-two rescaling).  e[i] receives
+// the terms 2^(z c2 - m) against the final m.
+template <int N>
+__device__ __forceinline__ void softmax_push_group(RowState &st, const float (&z)[N], float c2h, float c2l,
+                                                   float (&e)[N]) {
+    if (st.m == -INFINITY) {
+        float zm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < N; ++i) zm = fmaxf(zm, z[i]);
+        if (zm == -INFINITY) return;
+        st.m = ceilf(zm * c2h);  // c2 > 0: the rounded product is monotone in z
     }
     float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < N; ++i)
-        if (i < n) acc += fast_exp2(s2[i] - st.m);
+    for (int i = 0; i < N; ++i) {
+        e[i] = term_exp2(z[i], c2h, c2l, st.m);
+        acc += e[i];
+    }
+    if (!(acc <= 0x1p64f)) {
+        float zm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < N; ++i) zm = fmaxf(zm, z[i]);
+        const float nm = ceilf(fmaxf(st.m, zm * c2h));
+        st.S = scale_pow2(st.S, st.m - nm);
+        st.m = nm;
+        acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            e[i] = term_exp2(z[i], c2h, c2l, st.m);
+            acc += e[i];
+        }
+    }
     st.S += acc;
 }
 
-// Greedy step: key = value itself.
+// Greedy step: the key is the logit itself (lowest id on exact ties).
 __device__ __forceinline__ void argmax_push(RowState &st, float z, int v) {
-    if (z > st.key || (z == st.key && v < st.idx)) {
-        st.key = z;
-        st.s_at = z;
-        st.idx = v;
+    const unsigned long long w = key_word(FF{z, 0.f}, v);
+    if (w > st.best) {
+        st.best = w;
+        st.z_at = z;
     }
     st.m = fmaxf(st.m, z);
 }
 
-// Float keys as unsigned integers whose order is the float order, so that a
-// row-wide running best can be kept with atomicMax.  0 encodes "none" (-inf).
-__device__ __forceinline__ uint32_t key_to_ordered(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float ordered_to_key(uint32_t o) {
-    if (o == 0u) return -INFINITY;
-    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
-}
 __device__ __forceinline__ uint32_t load_relaxed(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -278,14 +457,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Row-wide best draw of a block position as one 64-bit word: the key's
-// order-preserving encoding above the complemented token id, so that
-// atomicMax keeps the largest key and, on an exact tie, the lowest id (the
-// merge rule of the partial states).  0 means "none".
-__device__ __forceinline__ unsigned long long best_encode(float key, int idx) {
-    return ((unsigned long long)key_to_ordered(key) << 32) | (unsigned long long)(~(uint32_t)idx);
-}
-__device__ __forceinline__ int best_token(unsigned long long w) { return w ? (int)~(uint32_t)w : -1; }
 __device__ __forceinline__ unsigned int load_acquire_u32(const unsigned int *p) {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -323,23 +494,13 @@ __device__ __forceinline__ unsigned long long load_relaxed_u64(const unsigned lo
     return v;
 }
 
-// Final draw state (residual or bonus): the best group key and its token.
-// A residual row whose entries all have p <= q (impossible in exact
-// arithmetic after a rejection) keeps key -inf here and is redrawn from p by
-// the merge step.
+// Final draw state (residual or bonus): the best key word (key_word) of a
+// row segment, 0 = none.  A residual row whose entries all have p <= q
+// (impossible in exact arithmetic after a rejection) keeps 0 here and is
+// redrawn from p by the merge step.
 struct ResidualState {
-    float key_res;
-    int idx_res;
+    unsigned long long best;
 };
-
-__device__ __forceinline__ ResidualState residual_init() { return ResidualState{-INFINITY, INT32_MAX}; }
-
-__device__ __forceinline__ void residual_merge(ResidualState &a, const ResidualState &b) {
-    if (key_better(b.key_res, b.idx_res, a.key_res, a.idx_res)) {
-        a.key_res = b.key_res;
-        a.idx_res = b.idx_res;
-    }
-}
 
 // Block-wide merge of one RowState per thread; the result is valid in thread 0.
 // `scratch` holds blockDim.x / 32 states.

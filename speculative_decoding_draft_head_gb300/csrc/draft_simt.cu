@@ -10,11 +10,10 @@
 // shared memory, forms the rank-r bias with register-tiled FMAs (4 vocabulary
 // entries x rows_per_block requests per thread, W_out rows read along r), adds
 // the base logits and streams every logit once through the online softmax and
-// the two-stage group draw (a Gumbel on each 16-token group's log-sum-exp, an
-// inverse CDF inside the winning group; four lanes hold one group).  The
-// per-(request, segment) partial states are merged
-// by draft_finalize, which writes the token the next position reads.  bf16
-// weights take the tensor-core kernel (markov_tc.cu) instead.
+// the per-token Gumbel-max draw (one Philox block gives the words of a
+// thread's four tokens).  The per-(request, segment) partial states are
+// merged by draft_finalize, which writes the token the next position reads.
+// bf16 weights take the tensor-core kernel (markov_tc.cu) instead.
 #include <climits>
 
 #include "device_common.cuh"
@@ -26,71 +25,33 @@ namespace {
 constexpr int kSimtThreads = 256;
 constexpr int kSimtRows = 8;
 
-// The two-stage group draw of a 16-token group held by a quad of lanes (four
-// tokens each, lane & 3 = quarter of the group; v = this lane's first token).
-// Group key K_g = max + log2 sum 2^(s - max) - log2(-ln u0) (log2 units), and
-// inside the group the first token whose running sum of 2^(s - max) exceeds
-// u1 times the group's sum, with (u0, u1) = words 0 and 1 of the Philox block
-// at counter (group, j, rid, draft stream).  The quad's first lane records a
-// key that beats its partial state.  Every lane of the warp calls it.
-__device__ __forceinline__ void group_draw_quad(RowState &st, const float (&s2)[4], int v, bool valid, uint32_t rid,
-                                                int j, uint32_t k0, uint32_t k1) {
-    const int lane = threadIdx.x & 31;
-    float gm = fmaxf(fmaxf(s2[0], s2[1]), fmaxf(s2[2], s2[3]));
-    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
-    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+// Online softmax and per-token Gumbel-max for four consecutive tokens
+// v .. v + 3 of one row (T > 0, c2 = log2(e) / T, rT = fl(1 / T)); w holds
+// their draft-stream words.  A token is screened without a logarithm
+// against the best key K this thread has seen for the row, (1 - u) < e Q with
+// e = 2^(s2 - m) and Q = 2^(m - K log2 e) (E = -ln u >= 1 - u, so no winner is
+// lost); a survivor's fp32 key decides whether its float-float key is formed,
+// and the key words decide.
+__device__ __forceinline__ void simt_draw4(RowState &st, float &kbest, const float (&z)[4], float2 c2, float T,
+                                           float rT, int v, const uint4 &w) {
     float e[4];
+    softmax_push_group<4>(st, z, c2.x, c2.y, e);
+    const float Q = screen_q(st.m, kbest);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) e[i] = (valid && gm > -INFINITY) ? exp2f(s2[i] - gm) : 0.f;
-    float gs = ((e[0] + e[1]) + e[2]) + e[3];
-    gs += __shfl_xor_sync(0xffffffffu, gs, 1);
-    gs += __shfl_xor_sync(0xffffffffu, gs, 2);
-    const bool leader = (lane & 3) == 0;
-    bool take = false;
-    float key = -INFINITY;
-    uint4 wd = make_uint4(0u, 0u, 0u, 0u);
-    if (leader && valid && gs > 0.f) {
-        wd = philox4x32_10(make_uint4((uint32_t)v >> 4, (uint32_t)j, rid, kStreamDraft), k0, k1);
-        key = gm + log2f(gs) - log2f(neg_log_uniform(wd.x));
-        take = key > st.key;  // an exact tie keeps the earlier, lower-numbered group
-    }
-    if (!__any_sync(0xffffffffu, take)) return;
-    // gather the quad's terms and scaled logits in the leader, in token order
-    float eq[16], sq[16];
-#pragma unroll
-    for (int qd = 0; qd < 4; ++qd)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            eq[4 * qd + i] = __shfl_sync(0xffffffffu, e[i], (lane & ~3) + qd);
-            sq[4 * qd + i] = __shfl_sync(0xffffffffu, s2[i], (lane & ~3) + qd);
-        }
-    if (!take) return;
-    float run = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) run += eq[i];
-    const float target = word_to_uniform(wd.y) * run;
-    int x = -1, last = 0;
-    float sx = 0.f, sl = 0.f;
-    run = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        run += eq[i];
-        if (eq[i] > 0.f) {
-            last = i;
-            sl = sq[i];
-        }
-        if (x < 0 && run > target) {
-            x = i;
-            sx = sq[i];
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t wi = i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
+        if (!(one_minus_uniform_plus_one(wi) < fmaf(e[i], Q, 1.f))) continue;
+        const float k2 = fmaf(z[i], c2.x, -fast_log2(neg_log_uniform(wi)));
+        const float K2 = kbest * kLog2e;
+        if (!(k2 > K2 - key_tol2(k2, K2))) continue;
+        const FF key = ff_add(div_ff(z[i], T, rT), gumbel_ff(wi));
+        const unsigned long long word = key_word(key, v + i);
+        if (word > st.best) {
+            st.best = word;
+            st.z_at = z[i];
+            kbest = fmaxf(kbest, key.hi);
         }
     }
-    if (x < 0) {  // target rounded up to the group's sum: its last token
-        x = last;
-        sx = sl;
-    }
-    st.key = key;
-    st.idx = v + x;
-    st.s_at = sx;
 }
 
 template <typename TIn>
@@ -103,7 +64,8 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
                   uint32_t *__restrict__ flags, float *__restrict__ z_out) {
     extern __shared__ float a_rows[];  // [kSimtRows][r]
     __shared__ int prev_s[kSimtRows];
-    __shared__ float c2_s[kSimtRows];
+    __shared__ float2 c2_s[kSimtRows];
+    __shared__ float T_s[kSimtRows];
     __shared__ uint32_t rid_s[kSimtRows];
     __shared__ RowState scratch[kSimtThreads / 32];
 
@@ -112,7 +74,7 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
     if (threadIdx.x < kSimtRows) {
         const int b = b0 + threadIdx.x;
         int prev = -1;
-        float c2 = 0.f;
+        float2 c2 = make_float2(0.f, 0.f);
         uint32_t id = 0;
         if (b < B) {
             prev = (j == 0) ? anchor[b] : tokens[(size_t)b * G + j - 1];
@@ -124,10 +86,11 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
             const bool t_ok = T >= 0.f && !isinf(T);
             if (!t_ok && seg == 0 && j == 0) atomicOr(flags, kFlagBadTemperature);
             if (bad_prev || !t_ok) prev = -1;
-            c2 = (T > 0.f) ? kLog2e / T : 0.f;
+            if (T > 0.f && t_ok) c2 = c2_split(T);
         }
         prev_s[threadIdx.x] = prev;
         c2_s[threadIdx.x] = c2;
+        T_s[threadIdx.x] = (b < B) ? temperature[b] : 1.f;
         rid_s[threadIdx.x] = id;
     }
     __syncthreads();
@@ -139,13 +102,15 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
     __syncthreads();
 
     RowState st[kSimtRows];
+    float kbest[kSimtRows];
 #pragma unroll
-    for (int rb = 0; rb < kSimtRows; ++rb) st[rb] = row_state_init();
+    for (int rb = 0; rb < kSimtRows; ++rb) {
+        st[rb] = row_state_init();
+        kbest[rb] = -INFINITY;
+    }
 
-    const int vb = seg * chunk;  // a multiple of 16: whole draw groups
+    const int vb = seg * chunk;  // a multiple of 16
     const int ve = min(V, vb + chunk);
-    // every thread runs the same iterations (the group draw votes and
-    // shuffles across the warp); lanes past the segment hold no tokens
     for (int vbase = vb; vbase < ve; vbase += 4 * kSimtThreads) {
         const int v = vbase + 4 * threadIdx.x;
         const bool valid = v < ve;  // V % 8 == 0: all four tokens or none
@@ -177,7 +142,7 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
             const int b = b0 + rb;
             if (b >= B || prev_s[rb] < 0) continue;  // uniform over the block
             const size_t row = (size_t)b * G + j;
-            const float c2 = c2_s[rb];
+            const float2 c2 = c2_s[rb];
             float z[4] = {0.f, 0.f, 0.f, 0.f};
             if (valid) {
                 const float4 u4 = load4(base + row * V + v);
@@ -185,12 +150,13 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
                 for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[rb][e];
                 if (z_out) *reinterpret_cast<float4 *>(z_out + row * V + v) = make_float4(z[0], z[1], z[2], z[3]);
             }
-            if (c2 > 0.f) {
-                float s2[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s2[e] = valid ? z[e] * c2 : -INFINITY;
-                if (valid) softmax_push_group<4>(st[rb], s2, 4);
-                group_draw_quad(st[rb], s2, v, valid, rid_s[rb], j, k0, k1);
+            if (c2.x > 0.f) {
+                if (valid) {
+                    const float T = T_s[rb];
+                    const uint4 w = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, rid_s[rb], kStreamDraft),
+                                                  k0, k1);
+                    simt_draw4(st[rb], kbest[rb], z, c2, T, __frcp_rn(T), v, w);
+                }
             } else if (valid) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) argmax_push(st[rb], z[e], v + e);
@@ -207,6 +173,9 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
 
 // One warp per (request, position): merge the segment partials, write token,
 // lse, logq.  Position j0 + k reads its partials at part + k * pos_stride.
+// The token is the largest key word; lse is the partial sums rescaled
+// exactly and added in double, and log q = z_x / T - lse in double, each
+// rounded once to fp32.
 __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsplit, size_t pos_stride,
                                       const float *__restrict__ temperature, int B, int G, int j0, int npos,
                                       int32_t *__restrict__ tokens, float *__restrict__ lse,
@@ -214,28 +183,41 @@ __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsp
     griddep_wait();  // a programmatic dependent: the previous launch's writes are visible after this
     const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (gw >= B * npos) return;
+    if (gw >= B * npos) return;  // warp-uniform
     const int k = gw / B, b = gw - k * B, j = j0 + k;
-    const RowState *pr = part + (size_t)k * pos_stride;
-    RowState s = row_state_init();
-    for (int i = lane; i < nsplit; i += 32) row_state_merge(s, pr[(size_t)b * nsplit + i]);
-    s = warp_merge(s);
+    const RowState *pr = part + (size_t)k * pos_stride + (size_t)b * nsplit;
+    const float T = temperature[b];
+    const double lse_d = (T > 0.f) ? warp_lse_of_partials(pr, nsplit) : 0.0;
+    unsigned long long bw = 0ull;
+    float zat = 0.f;
+    for (int i = lane; i < nsplit; i += 32)
+        if (pr[i].best > bw) {
+            bw = pr[i].best;
+            zat = pr[i].z_at;
+        }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        const unsigned long long ob = __shfl_xor_sync(0xffffffffu, bw, m);
+        const float oz = __shfl_xor_sync(0xffffffffu, zat, m);
+        if (ob > bw) {
+            bw = ob;
+            zat = oz;
+        }
+    }
     if (lane != 0) return;
     const size_t o = (size_t)b * G + j;
-    const float T = temperature[b];
-    if (s.idx == INT32_MAX) {  // request flagged invalid
+    if (bw == 0ull) {  // request flagged invalid
         tokens[o] = -1;
         lse[o] = __int_as_float(0x7fc00000);
         logq[o] = __int_as_float(0x7fc00000);
         return;
     }
-    tokens[o] = s.idx;
+    tokens[o] = word_token(bw);
     if (T > 0.f) {
-        const float l2 = log2f(s.S);
-        lse[o] = kLn2 * (s.m + l2);
-        logq[o] = kLn2 * ((s.s_at - s.m) - l2);
+        lse[o] = (float)lse_d;
+        logq[o] = (float)((double)zat / (double)T - lse_d);
     } else {
-        lse[o] = s.key;
+        lse[o] = zat;
         logq[o] = 0.f;
     }
 }
@@ -294,7 +276,7 @@ DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
         if (nsplit > max_split) nsplit = max_split;
         if (nsplit < 1) nsplit = 1;
         int chunk = (V + nsplit - 1) / nsplit;
-        chunk = (chunk + 15) / 16 * 16;  // whole draw groups per segment
+        chunk = (chunk + 15) / 16 * 16;
         p.nsplit = (V + chunk - 1) / chunk;
         p.chunk = chunk;
     }

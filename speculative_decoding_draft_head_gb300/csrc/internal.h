@@ -15,6 +15,7 @@ namespace dspark {
 constexpr int kNumSMs = 152;            // GB300: 2 dies x 76 SMs
 constexpr size_t kFlagBytes = 256;      // flag word region at the head of every workspace
 constexpr int kMaxG = 64;
+constexpr int kMaxV = 1 << 20;         // token ids fit the 20-bit field of the key words
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -55,7 +56,7 @@ struct DraftPlan {
     int rows_per_block;    // SIMT: requests per block
     int row_blocks;        // SIMT: ceil(B / rows_per_block); tensor path: M tiles
     int nsplit;            // vocabulary segments per row (partials per row)
-    int chunk;             // vocabulary entries per segment (SIMT; a multiple of 16, whole draw groups)
+    int chunk;             // vocabulary entries per segment (SIMT; a multiple of 16)
     size_t partial_offset; // byte offset of the per-(row, segment) partials ([G][B][nsplit] on the tensor path)
     size_t best_offset;    // [G][B] 64-bit row-wide best (key, token) words (tensor path), zeroed per call
     size_t bar_offset;     // [row_blocks] barrier counters between positions (tensor path), zeroed per call
@@ -130,7 +131,7 @@ struct FinalArgs {
     const float *temperature;
     const uint32_t *request_id;
     const int32_t *final_code; // [B]: -1, (1 << 16) | d residual, (2 << 16) | L bonus
-    const float *lse_t_row;    // [B] target lse of the rejected row, log2 units
+    const float2 *lse_t_row;   // [B] target lse of the rejected row, natural log as float-float (hi, lo)
     const float *draft_lse;    // [B][G] natural log
     int B, G, V, r, nseg;
     int pass;                  // traversal direction of the vocabulary segments (odd: backwards)
@@ -151,7 +152,7 @@ struct VerifyPlan {
     int res_split_tc;       // segments per residual row, tensor-core kernel (0 = unused)
     size_t row_part_offset; // [B][G+1][row_split] RowState
     size_t res_row_offset;  // [B] int32: rejected position or -1
-    size_t lse_t_offset;    // [B] fp32: target lse of the rejected row
+    size_t lse_t_offset;    // [B] float2: target lse of the rejected row (natural log, hi + lo)
     size_t res_part_offset; // [B][res_split] ResidualState
     size_t res_best_offset; // [B] uint32 row-wide best residual key of the tensor-core final draw
     size_t ws_bytes;

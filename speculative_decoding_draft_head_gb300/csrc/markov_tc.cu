@@ -101,7 +101,7 @@ constexpr uint32_t kOffBar = kOffMerge + kMergeBytes;
 constexpr int kNumBars = kWStages + 2 * kUStages + 2 * kAccBufs + 1 + 2;
 static_assert(kNumBars * 8 <= 256, "barrier region");
 constexpr uint32_t kOffMisc = kOffBar + 256;
-constexpr uint32_t kMiscBytes = 16 + BM * 20;
+constexpr uint32_t kMiscBytes = 16 + BM * 28;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kTmemA + 128 <= kTmemCols, "TMEM accumulators and A operand");
@@ -109,7 +109,6 @@ static_assert(kTmemA + 128 <= kTmemCols, "TMEM accumulators and A operand");
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of clock cycles
 constexpr long long kDrainLimit = 200000000LL;  // ~0.1 s: copies and UMMAs in flight after a timeout
 constexpr float kQMax = 0x1p126f;
-constexpr float kMargin = 1.0001f;
 
 struct TcParams {
     const __nv_bfloat16 *e_in;
@@ -123,7 +122,7 @@ struct TcParams {
     const float *temperature;
     const uint32_t *request_id;
     const int32_t *final_code;  // [B]: -1, or (kind << 16) | position
-    const float *lse_t_row;     // [B] target lse of the rejected row, log2 units
+    const float2 *lse_t_row;    // [B] target lse of the rejected row, natural log, float-float
     const float *draft_lse;     // [B][G] natural log
     int B, G, V, r;
     int j, j_end;               // draft: block positions j .. j_end - 1 in this launch
@@ -131,7 +130,7 @@ struct TcParams {
     int pass;                   // final draw: odd passes walk the segment backwards
     PhiloxRoundKeys keys;
     RowState *part;             // draft: [G][B][nseg] softmax / key partials
-    unsigned long long *best;   // draft: [G][B] row-wide best (key, token), see best_encode
+    unsigned long long *best;   // draft: [G][B] row-wide best (key, token) words, see key_word
     unsigned int *grid_bar;     // draft, several positions: [row blocks] arrival counters of the barrier
     ResidualState *rpart;
     uint32_t *res_best;         // final draw: [B] row-wide best residual key (ordered encoding)
@@ -222,49 +221,71 @@ __device__ __forceinline__ float sum16(const float (&e)[16]) {
     return (s8[0] + s8[2]) + (s8[1] + s8[3]);
 }
 
-// Draft epilogue for the 16 logits z of one row (T > 0, c2 = log2(e) / T).
-// Every lane of the warp calls it together (it votes across the warp); `on`
-// is false for rows that are greedy or inactive, which then change nothing.
+// Word i (a compile-time constant after unrolling) of four Philox blocks.
+__device__ __forceinline__ uint32_t word_at(const uint4 (&w)[4], int i) {
+    const uint4 &b = w[i >> 2];
+    switch (i & 3) {
+        case 0: return b.x;
+        case 1: return b.y;
+        case 2: return b.z;
+        default: return b.w;
+    }
+}
+
+// The largest of the 16 words (the smallest 1 - u of the sub-slice).
+__device__ __forceinline__ uint32_t max_word16(const uint4 (&w)[4]) {
+    uint32_t a = max(max(w[0].x, w[0].y), max(w[0].z, w[0].w));
+    const uint32_t b = max(max(w[1].x, w[1].y), max(w[1].z, w[1].w));
+    const uint32_t c = max(max(w[2].x, w[2].y), max(w[2].z, w[2].w));
+    const uint32_t d = max(max(w[3].x, w[3].y), max(w[3].z, w[3].w));
+    return max(max(a, b), max(c, d));
+}
+
+// Draft epilogue for the 16 logits z of one row (T > 0, c2 = log2(e) / T,
+// rT = fl(1 / T)), tokens v .. v + n - 1, with their draft-stream words w
+// (word i of token v + i).  Every lane of the warp calls it together (it
+// votes across the warp); `on` is false for rows that are greedy or inactive,
+// which then change nothing.
 //
-// One sub-slice of 16 tokens is one draw group (v is a multiple of 16; the
-// vocabulary's last group may be ragged, n < 16).  The row's draw is the
-// two-stage group draw: the group key K_g = log2 sum_g 2^s + G2(u0) with
-// G2(u) = -log2(-ln u), the largest key wins, and inside the winning group the
-// token is the first whose running sum of 2^s exceeds u1 times the group's
-// sum; w.x and w.y (words 0 and 1 of the group's Philox block) give u0 and u1.
+// Per-token Gumbel-max: token v beats the best key K known for the row iff
+// E_v = -ln u_v < e^(s_v - K) = e_v Q / margin, where e_v = 2^(s2_v - m) is
+// the softmax term already computed and Q = screen_q(m, K).  Since
+// E >= 1 - u, the test (1 - u_v) < e_v Q (conservative form f1 < fl(e Q + 1))
+// never loses a winner.  Most sub-slices are decided by one test: the
+// largest word of the 16 against the sub-slice's sum (sum >= every e_v).  A
+// sub-slice that passes tests its tokens one by one; the survivors get an
+// fp32 key (log2 units), and those within rounding of the threshold get the
+// float-float key, whose word (key_word) decides against the row's best.
 //
-// The softmax keeps a running reference m (log2 units) that may lag the true
+// The softmax keeps an integer reference m (log2 units) that may lag the
 // maximum: terms 2^(z c2 - m) above 1 are fine, and a group whose sum exceeds
-// 2^64 (or overflows) is redone against its own maximum.  With Q = 2^(m - K),
-// K the best key known for the whole row (this thread's, or a larger one
-// another thread published in the row's best word), K_g > K needs
-// -ln u0 < sum Q, hence (1 - u0) < sum Q: a group that fails the conservative
-// form f1 < fl(sum Q + 1) cannot win and costs no logarithm.  A new best is
-// published with a max reduction twice: to the CTA's per-row word in shared memory
-// (read by the quadrant's warps before each sub-slice) and to the row-wide
-// word in global memory (read every fourth sub-slice).
-__device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
-                                              int n, int v, bool on, unsigned long long *best, uint32_t *cta_best,
-                                              const uint4 &w) {
+// 2^64 (or overflows) is redone against its own maximum.  A new best is
+// published with a max reduction twice: to the CTA's per-row word in shared
+// memory (read by the quadrant's warps before each sub-slice) and to the
+// row-wide word in global memory (read every fourth sub-slice).
+__device__ __forceinline__ void draft_tokens16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
+                                               float c2l, float T, float rT, int n, int v, bool on,
+                                               unsigned long long *best,
+                                               uint32_t *cta_best, const uint4 (&w)[4]) {
     const bool full = (n == 16);  // warp-uniform
     float e[16];
     float sum = 0.f;
     if (on) {
         if (st.m == -INFINITY) {
-            // the first group of this thread's row: its maximum is the reference
+            // the first group of this thread's row: the reference is its maximum, rounded up
             float zm = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 if (full || i < n) zm = fmaxf(zm, z[i]);
-            st.m = zm * c2;  // c2 > 0: the rounded product is monotone in z
-            Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
+            st.m = ceilf(zm * c2);  // c2 > 0: the rounded product is monotone in z
+            Q = screen_q(st.m, kbest);
         }
         if (full) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) e[i] = fast_exp2(fmaf(z[i], c2, -st.m));
+            for (int i = 0; i < 16; ++i) e[i] = term_exp2(z[i], c2, c2l, st.m);
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) e[i] = (i < n) ? fast_exp2(fmaf(z[i], c2, -st.m)) : 0.f;
+            for (int i = 0; i < 16; ++i) e[i] = (i < n) ? term_exp2(z[i], c2, c2l, st.m) : 0.f;
         }
         sum = sum16(e);
         if (!(sum <= 0x1p64f)) {  // far above the reference (or overflow): renormalise
@@ -272,52 +293,59 @@ __device__ __forceinline__ void draft_group16(RowState &st, float &Q, float &kbe
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 if (full || i < n) zm = fmaxf(zm, z[i]);
-            const float cm = fmaxf(st.m, zm * c2);
-            st.S *= fast_exp2(st.m - cm);
+            const float cm = ceilf(fmaxf(st.m, zm * c2));
+            st.S = scale_pow2(st.S, st.m - cm);
             st.m = cm;
-            Q = fminf(fast_exp2(cm - kbest), kQMax) * kMargin;
+            Q = screen_q(st.m, kbest);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) e[i] = (full || i < n) ? fast_exp2(fmaf(z[i], c2, -st.m)) : 0.f;
+            for (int i = 0; i < 16; ++i) e[i] = (full || i < n) ? term_exp2(z[i], c2, c2l, st.m) : 0.f;
             sum = sum16(e);
         }
         st.S += sum;
     }
-    const bool cand = on && sum > 0.f && one_minus_uniform_plus_one(w.x) < fmaf(sum, Q, 1.f);
-    if (__any_sync(0xffffffffu, cand) && cand) {
-        // rare: the group's exact key
-        const float key = st.m + fast_log2(sum) - fast_log2(neg_log_uniform(w.x));
-        if (key > kbest) {
-            // the token: inverse CDF in group order, on the sequential sums
-            float run = 0.f;
+    const bool grp = on && sum > 0.f && one_minus_uniform_plus_one(max_word16(w)) < fmaf(sum, Q, 1.f);
+    if (!(__any_sync(0xffffffffu, grp) && grp)) return;
+    // rare: the tokens one by one; survivors' fp32 keys replace their terms in e
 #pragma unroll
-            for (int i = 0; i < 16; ++i) run += e[i];
-            const float target = word_to_uniform(w.y) * run;
-            int x = -1, last = 0;
-            float zx = 0.f, zl = 0.f;
-            run = 0.f;
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t wi = word_at(w, i);
+        float k2 = -INFINITY;
+        if (one_minus_uniform_plus_one(wi) < fmaf(e[i], Q, 1.f))
+            k2 = fmaf(z[i], c2, -fast_log2(neg_log_uniform(wi)));
+        e[i] = k2;
+    }
+#pragma unroll 1
+    while (true) {
+        float kb2 = -INFINITY;
+        int ib = -1;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                run += e[i];
-                if (e[i] > 0.f) {
-                    last = i;
-                    zl = z[i];
-                }
-                if (x < 0 && run > target) {
-                    x = i;
-                    zx = z[i];
-                }
+        for (int i = 0; i < 16; ++i)
+            if (e[i] > kb2) {
+                kb2 = e[i];
+                ib = i;
             }
-            if (x < 0) {  // target rounded up to the group's sum: its last token
-                x = last;
-                zx = zl;
+        const float K2 = kbest * kLog2e;
+        if (ib < 0 || !(kb2 > K2 - key_tol2(kb2, K2))) break;
+        float zb = 0.f;
+        uint32_t wb = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i == ib) {
+                zb = z[i];
+                wb = word_at(w, i);
+                e[i] = -INFINITY;
             }
-            st.key = key;
-            st.s_at = zx * c2;
-            st.idx = v + x;
-            kbest = key;
-            red_max_shared_u32(cta_best, key_to_ordered(key));
-            red_max_u64(best, best_encode(key, v + x));
-            Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
+        const FF key = ff_add(div_ff(zb, T, rT), gumbel_ff(wb));
+        const unsigned long long word = key_word(key, v + ib);
+        if (word > st.best) {
+            st.best = word;
+            st.z_at = zb;
+            if (key.hi >= kbest) {
+                kbest = key.hi;
+                red_max_shared_u32(cta_best, key_to_ordered(key.hi));
+                red_max_u64(best, word);
+                Q = screen_q(st.m, kbest);
+            }
         }
     }
 }
@@ -401,6 +429,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     // draft: the best key of each row found in this CTA during the position
     // (ordered encoding, 0 = none), shared by the quadrant's warps
     uint32_t *row_kbest = reinterpret_cast<uint32_t *>(misc + 4 + 4 * BM);
+    float *row_T = reinterpret_cast<float *>(misc + 4 + 5 * BM);  // the row's temperature
+    float *row_c2l = reinterpret_cast<float *>(misc + 4 + 6 * BM);  // low part of c2 (c2_split)
 
     // one position of the recurrent head: launched as a programmatic
     // dependent of the state kernel, so the set-up and the first W_out and
@@ -440,7 +470,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     if (threadIdx.x < BM) {
         const int b = m0 + threadIdx.x;
         int prev = -1, code = 0;
-        float c2 = 0.f;
+        float c2 = 0.f, c2l = 0.f;
         uint32_t id = 0;
         if (b < p.B) {
             const float T = p.temperature[b];
@@ -453,7 +483,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     if (!t_ok) atomicOr(p.flags, kFlagBadTemperature);
                 }
                 code = t_ok ? 1 : 0;
-                c2 = (T > 0.f) ? kLog2e / T : 0.f;
+                if (T > 0.f && t_ok) {
+                    const float2 cs = c2_split(T);
+                    c2 = cs.x;
+                    c2l = cs.y;
+                }
             } else {
                 code = p.final_code[b];  // validated by the decide kernel
                 if (code >= 0) {
@@ -467,9 +501,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         }
         row_prev[threadIdx.x] = prev;
         row_c2[threadIdx.x] = c2;
+        row_c2l[threadIdx.x] = c2l;
         row_rid[threadIdx.x] = id;
         row_code[threadIdx.x] = code;
         row_kbest[threadIdx.x] = 0u;
+        row_T[threadIdx.x] = (b < p.B) ? p.temperature[b] : 1.f;
     }
     if (!kFinal && warp < kEpiWarps && threadIdx.x < 16 * 8) {
         // identity row n (16 rows of 128 bytes): a single 1.0 at k = n;
@@ -610,6 +646,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const int row = q * 32 + lane;
         const int b = m0 + row;
         const float c2 = row_c2[row];
+        const float c2l = row_c2l[row];
+        const float Trow = row_T[row];
+        const float rT = (Trow > 0.f) ? __frcp_rn(Trow) : 0.f;
         const uint32_t rid = row_rid[row];
         const int code = row_code[row];
         const int kind = kFinal ? (code >= 0 ? (code >> 16) : 0) : 0;
@@ -634,7 +673,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     prev = p.anchor[b];
                     if (prev < 0 || prev >= p.V) prev = -1;
                 } else {
-                    prev = best_token(load_relaxed_u64(p.best + (size_t)(jj - 1) * p.B + b));
+                    prev = word_token(load_relaxed_u64(p.best + (size_t)(jj - 1) * p.B + b));
                 }
             }
             {
@@ -674,15 +713,19 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             float kbest_r = -INFINITY;  // best residual key of the row known to this thread
             uint32_t kr_next = 0u;      // the row-wide word, loaded one sub-slice ahead ("none")
             uint32_t *res_best = (kFinal && active) ? p.res_best + b : nullptr;
-            ResidualState rs = residual_init();
-            float lse_q2 = 0.f, lse_t2 = 0.f;
+            ResidualState rs{0ull};
+            float lse_q2 = 0.f, lse_t2 = 0.f, lse_q = 0.f;
+            FF lse_t{0.f, 0.f};
             const __nv_bfloat16 *urow = nullptr, *trow = nullptr;
             if (kFinal && active) {
                 trow = target_row(p.target, p.target_row0, p.n_target_rows, b, p.G, fpos, p.V);  // checked by decide
                 if (kind == 1) {
                     urow = p.base + ((size_t)b * p.G + fpos) * p.V;
-                    lse_q2 = p.draft_lse[(size_t)b * p.G + fpos] * kLog2e;
-                    lse_t2 = p.lse_t_row[b];
+                    lse_q = p.draft_lse[(size_t)b * p.G + fpos];
+                    lse_q2 = lse_q * kLog2e;
+                    const float2 lt = p.lse_t_row[b];
+                    lse_t = FF{lt.x, lt.y};
+                    lse_t2 = lt.x * kLog2e;
                 } else {
                     lse_q2 = INFINITY;  // q = 0
                     lse_t2 = 0.f;       // unnormalised p: the same argmax
@@ -713,15 +756,19 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 const int a = tg % kAccBufs;
                 const uint32_t aph = (uint32_t)(tg / kAccBufs) & 1u;
                 {
-                    // The group's Philox block (counter = group index v / 16) needs
-                    // nothing from the tensor cores.
-                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    // The sub-slice's 16 token words (four Philox blocks, counters
+                    // v / 4 .. v / 4 + 3) need nothing from the tensor cores.
+                    uint4 w[4];
                     uint32_t acc[16];
                     const int vw = sub_col(si);
                     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + (si & 7) * 16;
+                    auto draw_words = [&]() {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)vw >> 2) + g, prow, p.keys);
+                    };
                     if (t != waited) {
                         // a new tile: draw the words while its UMMAs may still run
-                        if (vw < ve) w = philox_folded((uint32_t)vw >> 4, prow, p.keys);
+                        draw_words();
                         if (!uniform_wait(tfull(a), aph, abort)) {
                             if (lane == 0) {
                                 *abort = 1;
@@ -736,7 +783,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     } else {
                         // the tile is ready: issue the TMEM load, draw under its latency
                         tmem_ld16(taddr, acc);
-                        if (vw < ve) w = philox_folded((uint32_t)vw >> 4, prow, p.keys);
+                        draw_words();
                     }
                     tmem_ld_wait16(acc);
                     // this sub-slice is in registers: hand its part of the accumulator back
@@ -775,10 +822,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             const float kg = ordered_to_key(max(kg_next, *(volatile uint32_t *)(row_kbest + row)));
                             if (kg > kbest) {
                                 kbest = kg;
-                                Q = fminf(fast_exp2(st.m - kbest), kQMax) * kMargin;
+                                Q = screen_q(st.m, kbest);
                             }
                         }
-                        draft_group16(st, Q, kbest, z, c2, n, v, on, best, row_kbest + row, w);
+                        draft_tokens16(st, Q, kbest, z, c2, c2l, Trow, rT, n, v, on, best, row_kbest + row, w);
                         // reload the row-wide word after this warp's first sub-slice of
                         // the position (by then every CTA has published its rows' first
                         // groups, so the threshold is tight from the second sub-slice
@@ -802,17 +849,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             if (active && sn < nsub && nn > 0) load16_bf16(trow + vn, nn, nt_lo, nt_hi);
                         }
                         if (n <= 0) continue;  // warp-uniform
-                        // One 16-token draw group (R2b; stream 2 residual, 3 bonus).  A
-                        // residual row weighs token v by r_v = p_v - q_v where positive,
-                        // with p and q normalised (reference 0); a bonus row by
-                        // 2^(t_v c2 - tref) with the group's own maximum as tref (q = 0:
-                        // lse_q2 = +inf).  Group key K_g = off + log2 sum r - log2(-ln u0),
-                        // off = tref for bonus rows, 0 for residual rows; it can beat the
-                        // best key K only if (1 - u0) < sum 2^(off - K).
-                        // No normaliser is needed here (p and q are normalised by lse_t2
-                        // and lse_q2), only the candidate test, so a group is first
-                        // tested against a bound from its largest target logit alone:
-                        // every r_v <= p_v <= 2^(t_max c2 - tref).
+                        // Per-token Gumbel-max (stream 2 residual, 3 bonus).  A residual
+                        // row weighs token v by r_v = p_v - q_v where positive, with p
+                        // and q normalised (reference 0); a bonus row by
+                        // 2^(t_v c2 - tref) with the sub-slice's largest scaled logit as
+                        // tref (q = 0: lse_q2 = +inf).  Token v can beat the best key K
+                        // only if (1 - u_v) < r_v 2^(off - K), off = tref for bonus
+                        // rows, 0 for residual rows.  The sub-slice is first tested
+                        // with its largest word against a bound from its largest target
+                        // logit alone: every r_v <= p_v <= 2^(t_max c2 - tref).
                         const bool bonus = (kind == 2);
                         float tm = -INFINITY;
 #pragma unroll
@@ -825,62 +870,81 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             const float kg = ordered_to_key(kr_next);
                             if (kg > kbest_r) kbest_r = kg;
                         }
-                        const float Qg = fminf(fast_exp2(off - kbest_r), kQMax) * kMargin;
+                        const float Qg = screen_q(off, kbest_r);
                         const float pmax = fast_exp2(fmaf(tm, c2, -tref));
-                        const bool maybe = active && one_minus_uniform_plus_one(w.x) < fmaf((float)n * pmax, Qg, 1.f);
+                        const bool maybe = active && one_minus_uniform_plus_one(max_word16(w)) < fmaf(pmax, Qg, 1.f);
                         // the row-wide word for the next sub-slice (this thread's own
                         // publications below are already in kbest_r)
                         if (active) kr_next = load_relaxed(res_best);
                         if (!__any_sync(0xffffffffu, maybe)) continue;
-                        // the draft logits z = base + bias of this group (residual rows)
+                        // the draft logits z = base + bias of this sub-slice (residual rows)
                         uint4 u_lo = make_uint4(0, 0, 0, 0), u_hi = u_lo;
                         if (maybe && kind == 1) load16_bf16(urow + v, n, u_lo, u_hi);
                         float z[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) z[i] = bf16_at(u_lo, u_hi, i) + __uint_as_float(acc[i]);
-                        // upper bound of the group's sum under the approximate exponentials
-                        float sum_up = 0.f;
+                        // per token: screen with an upper bound of r_v under the
+                        // approximate exponentials; a survivor's fp32 key (log2 units,
+                        // from that bound, so never below the true key by more than
+                        // rounding) goes to k2[]
+                        float k2[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -tref));
-                            const float qv = fast_exp2(fmaf(z[i], c2, -lse_q2));
-                            const float ub = (pv - qv) + 4e-7f * (pv + qv);
-                            sum_up += (i < n && ub > 0.f) ? ub : 0.f;
-                        }
-                        const bool cand = maybe && sum_up > 0.f && one_minus_uniform_plus_one(w.x) < fmaf(sum_up, Qg, 1.f);
-                        if (__any_sync(0xffffffffu, cand) && cand) {
-                            // rare: the exact weights, r_v = p_v (1 - 2^-delta) with
-                            // delta = log2 p_v - log2 q_v formed from the logits first
-                            // (+inf for bonus rows), and the group's exact key
-                            float r[16];
-                            float R = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float ti = bf16_at(ct_lo, ct_hi, i);
-                                const float delta2 = fmaf(ti - z[i], c2, lse_q2 - tref);
-                                const float ri = (i < n && delta2 > 0.f)
-                                                     ? exp2f(fmaf(ti, c2, -tref)) * (delta2 > 24.f ? 1.f : -expm1f(-delta2 * kLn2))
-                                                     : 0.f;
-                                r[i] = ri;
-                                R += ri;
+                            float kk = -INFINITY;
+                            if (maybe && i < n) {
+                                const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -tref));
+                                const float qv = fast_exp2(fmaf(z[i], c2, -lse_q2));
+                                const float ub = (pv - qv) + 4e-7f * (pv + qv);
+                                const uint32_t wi = word_at(w, i);
+                                if (ub > 0.f && one_minus_uniform_plus_one(wi) < fmaf(ub, Qg, 1.f))
+                                    kk = off + fast_log2(ub) - fast_log2(neg_log_uniform(wi));
                             }
-                            const float key = off + log2f(R) - log2f(neg_log_uniform(w.x));
-                            if (R > 0.f && key > kbest_r) {
-                                // the token: inverse CDF in group order
-                                const float target = word_to_uniform(w.y) * R;
-                                int x = -1, last = 0;
-                                float run = 0.f;
+                            k2[i] = kk;
+                        }
+                        // contenders, best first: the float-float key decides
+#pragma unroll 1
+                        while (true) {
+                            float kb2 = -INFINITY;
+                            int ib = -1;
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    run += r[i];
-                                    if (r[i] > 0.f) last = i;
-                                    if (x < 0 && run > target) x = i;
+                            for (int i = 0; i < 16; ++i)
+                                if (k2[i] > kb2) {
+                                    kb2 = k2[i];
+                                    ib = i;
                                 }
-                                if (x < 0) x = last;  // target rounded up to the group's sum
-                                rs.key_res = key;
-                                rs.idx_res = v + x;
-                                kbest_r = key;
-                                red_max_u32(res_best, key_to_ordered(key));
+                            const float K2 = kbest_r * kLog2e;
+                            if (ib < 0 || !(kb2 > K2 - key_tol2(kb2, K2))) break;
+                            float zb = 0.f, tb = 0.f;
+                            uint32_t wb = 0u;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (i == ib) {
+                                    zb = z[i];
+                                    tb = bf16_at(ct_lo, ct_hi, i);
+                                    wb = word_at(w, i);
+                                    k2[i] = -INFINITY;
+                                }
+                            FF key;
+                            if (bonus) {
+                                key = div_ff(tb, Trow, rT);  // t / T: the bonus key before its noise
+                            } else {
+                                // ln r = ln p + ln(1 - q / p), ln q - ln p formed in
+                                // float-float from the logits and the two lse
+                                const FF lp = ff_add(div_ff(tb, Trow, rT), ff_neg(lse_t));
+                                const FF dl = ff_add(ff_add(div_ff(zb, Trow, rT), FF{-lse_q, 0.f}), ff_neg(lp));
+                                const float d = dl.hi + dl.lo;
+                                if (!(d < 0.f)) continue;  // p <= q: no residual mass
+                                const float l1m = (d > -0.6931472f) ? logf(-expm1f(d)) : log1pf(-expf(d));
+                                key = ff_add(lp, FF{l1m, 0.f});
+                            }
+                            key = ff_add(key, gumbel_ff(wb));
+                            const unsigned long long word = key_word(key, v + ib);
+                            if (word > rs.best) {
+                                rs.best = word;
+                                if (key.hi >= kbest_r) {
+                                    kbest_r = key.hi;
+                                    red_max_u32(res_best, key_to_ordered(key.hi));
+                                }
                             }
                         }
                     }
@@ -900,11 +964,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
                     for (int s2 = 1; s2 < kEpiPerQuad; ++s2) row_state_merge(st, ms[row * kEpiPerQuad + s2]);
                     p.part[((size_t)jj * p.B + b) * p.nseg + seg] = st;
-                    if (st.idx != INT32_MAX) red_max_u64(best, best_encode(st.key, st.idx));
+                    if (st.best) red_max_u64(best, st.best);
                     row_kbest[row] = 0u;  // the next position's (every warp is past its last read)
                 } else if (active) {
                     const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);
-                    for (int s2 = 1; s2 < kEpiPerQuad; ++s2) residual_merge(rs, ms[row * kEpiPerQuad + s2]);
+                    for (int s2 = 1; s2 < kEpiPerQuad; ++s2) rs.best = max(rs.best, ms[row * kEpiPerQuad + s2].best);
                     p.rpart[(size_t)b * p.nseg + seg] = rs;
                 }
             }

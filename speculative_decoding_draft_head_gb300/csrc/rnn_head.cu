@@ -106,7 +106,7 @@ rnn_state_kernel(const __nv_bfloat16 *__restrict__ e_in, const __nv_bfloat16 *__
         if (b < B) {
             // x_{j-1}: the anchor, else the token drawn at position j - 1 (the
             // row-wide best word of the previous draft launch)
-            prev = (j == 0) ? anchor[b] : best_token(best[(size_t)(j - 1) * B + b]);
+            prev = (j == 0) ? anchor[b] : word_token(best[(size_t)(j - 1) * B + b]);
             if (prev < 0 || prev >= V) prev = -1;
         }
         prev_s[threadIdx.x] = prev;

@@ -33,15 +33,10 @@ namespace {
 constexpr int kRowThreads = 256;
 constexpr int kResThreads = 256;
 
-__device__ __forceinline__ ResidualState residual_warp_merge(ResidualState s) {
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long w) {
 #pragma unroll
-    for (int mask = 16; mask > 0; mask >>= 1) {
-        ResidualState o;
-        o.key_res = __shfl_xor_sync(0xffffffffu, s.key_res, mask);
-        o.idx_res = __shfl_xor_sync(0xffffffffu, s.idx_res, mask);
-        residual_merge(s, o);
-    }
-    return s;
+    for (int mask = 16; mask > 0; mask >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, mask));
+    return w;
 }
 
 __device__ __forceinline__ int read_verify_len(const int32_t *verify_len, int b, int G) {
@@ -63,34 +58,35 @@ __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-// Online softmax of 8 logits x scaled by c2 (log2 units) against a reference
-// m that may lag the running maximum, as in the draft: a term 2^(x c2 - m)
-// above 1 is fine, and only a group whose sum leaves [0, 2^64] (far above the
-// reference, or overflowed) is redone against its own maximum.  The result
-// m + log2 S is the same log-sum-exp; the common case costs one fused
-// multiply-add, one exp2 and one add per logit.
-__device__ __forceinline__ void softmax_push8_lagging(RowState &st, const float (&x)[8], float c2) {
-    if (st.m == -INFINITY) {  // this thread's first group: its maximum is the reference
+// Online softmax of 8 logits x scaled by c2 (log2 units) against an integer
+// reference m that may lag the running maximum, as in the draft: a term
+// 2^(x c2 - m) above 1 is fine, and only a group whose sum leaves [0, 2^64]
+// (far above the reference, or overflowed) is redone against its own maximum
+// (an exact power-of-two rescaling of the sum).  The result m + log2 S is the
+// same log-sum-exp; the common case costs one fused multiply-add, one exp2
+// and one add per logit.
+__device__ __forceinline__ void softmax_push8_lagging(RowState &st, const float (&x)[8], float c2, float c2l) {
+    if (st.m == -INFINITY) {  // this thread's first group: its maximum, rounded up, is the reference
         float xm = x[0];
 #pragma unroll
         for (int i = 1; i < 8; ++i) xm = fmaxf(xm, x[i]);
-        st.m = xm * c2;
+        st.m = ceilf(xm * c2);
         if (st.m == -INFINITY) return;  // every logit so far is -inf: nothing to add
     }
     float e[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) e[i] = fast_exp2(fmaf(x[i], c2, -st.m));
+    for (int i = 0; i < 8; ++i) e[i] = term_exp2(x[i], c2, c2l, st.m);
     float acc = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
     if (!(acc <= 0x1p64f)) {
         float xm = x[0];
 #pragma unroll
         for (int i = 1; i < 8; ++i) xm = fmaxf(xm, x[i]);
-        const float cm = fmaxf(st.m, xm * c2);
-        st.S *= fast_exp2(st.m - cm);
+        const float cm = ceilf(fmaxf(st.m, xm * c2));
+        st.S = scale_pow2(st.S, st.m - cm);
         st.m = cm;
         acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc += fast_exp2(fmaf(x[i], c2, -st.m));
+        for (int i = 0; i < 8; ++i) acc += term_exp2(x[i], c2, c2l, st.m);
     }
     st.S += acc;
 }
@@ -122,7 +118,8 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
         if (L < 0 || !temperature_ok(T) || j > L || (T > 0.f && j == L)) continue;
         const TIn *t_row = target_row(target, row0, n_rows, b, G, j, V);
         if (!t_row) continue;  // flagged by the decide kernel
-        const float c2 = T > 0.f ? kLog2e / T : 0.f;
+        const float2 c2s = T > 0.f ? c2_split(T) : make_float2(0.f, 0.f);
+        const float c2 = c2s.x, c2l = c2s.y;
         const int vb = seg * chunk;
         const int ve = min(V, vb + chunk);
 
@@ -133,13 +130,13 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
                 float x[8], y[8];
                 load8(t_row + v, x);
                 load8(t_row + v + 8 * kRowThreads, y);
-                softmax_push8_lagging(st, x, c2);
-                softmax_push8_lagging(st, y, c2);
+                softmax_push8_lagging(st, x, c2, c2l);
+                softmax_push8_lagging(st, y, c2, c2l);
             }
             if (v < ve) {
                 float x[8];
                 load8(t_row + v, x);
-                softmax_push8_lagging(st, x, c2);
+                softmax_push8_lagging(st, x, c2, c2l);
             }
         } else {  // greedy request
             for (int v = vb + 8 * threadIdx.x; v < ve; v += 8 * kRowThreads) {
@@ -155,6 +152,33 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
 }
 
 // ---------------------------------------------------------------- pass 2 ----
+// The natural-log log-sum-exp of one row's partial states (m_i, S_i) in
+// double: the integer references make the rescaling exact.  -inf if empty.
+__device__ __forceinline__ double lse_of_partials(const RowState *part, int n) {
+    float m = -INFINITY;
+    for (int i = 0; i < n; ++i) m = fmaxf(m, part[i].m);
+    if (m == -INFINITY) return -INFINITY;
+    double S = 0.0;
+    for (int i = 0; i < n; ++i) {
+        const RowState &q = part[i];
+        if (q.m != -INFINITY && q.S > 0.f) S += ldexp((double)q.S, (int)fmaxf(q.m - m, -1100.f));
+    }
+    return 0.6931471805599453 * ((double)m + log2(S));
+}
+
+// The greedy argmax of one row from its partials: the largest key word.
+__device__ __forceinline__ unsigned long long best_of_partials(const RowState *part, int n, float *z_at) {
+    unsigned long long w = 0ull;
+    float z = 0.f;
+    for (int i = 0; i < n; ++i)
+        if (part[i].best > w) {
+            w = part[i].best;
+            z = part[i].z_at;
+        }
+    *z_at = z;
+    return w;
+}
+
 template <typename TIn>
 __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ row0,
                                      int64_t n_rows, const RowState *__restrict__ part,
@@ -167,7 +191,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
                                      uint32_t k0, uint32_t k1, int32_t *__restrict__ accept_len,
                                      int32_t *__restrict__ out_tokens, int32_t *__restrict__ num_out,
                                      float *__restrict__ target_lse, float *__restrict__ logp_sel,
-                                     int32_t *__restrict__ final_code, float *__restrict__ lse_t_row,
+                                     int32_t *__restrict__ final_code, float2 *__restrict__ lse_t_row,
                                      uint32_t *__restrict__ res_best, uint32_t *__restrict__ flags) {
     griddep_wait();  // a programmatic dependent: the previous launch's writes are visible after this
     const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -215,50 +239,55 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
         }
         return;
     }
-    const float c2 = T > 0.f ? kLog2e / T : 0.f;
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     // Every tested row at once: lane j merges row j's partials (in segment
-    // order), reads the target logit of x_j and decides its acceptance; the
-    // first rejection (or greedy mismatch) is the lowest set bit of a ballot.
-    // Rows after it were never tested: their outputs stay NaN.
+    // order), reads the target logit of x_j and decides its acceptance in
+    // double: log p = t_x / T - lse_t, accept iff u < min(1, exp(log p - log q));
+    // the first rejection (or greedy mismatch) is the lowest set bit of a
+    // ballot.  Rows after it were never tested: their outputs stay NaN.
     int k = L, y = -1, d = -1;
     for (int j0 = 0; j0 < L; j0 += 32) {
         const int j = j0 + lane;
         const bool tested = j < L;
         bool pass = true;
-        float lse_out = 0.f, logp = 0.f, lse2 = 0.f;
+        float lse_out = 0.f, logp_out = 0.f;
+        double lse_d = 0.0;
         int amax = -1;
         if (tested) {
-            RowState s = row_state_init();
             const RowState *pr = part + ((size_t)b * (G + 1) + j) * nsplit;
-            for (int i = 0; i < nsplit; ++i) row_state_merge(s, pr[i]);
             const int x = draft_tokens[(size_t)b * G + j];
             if (T > 0.f) {
-                lse2 = s.m + log2f(s.S);
+                lse_d = lse_of_partials(pr, nsplit);
                 const float tx = to_f32(target_row(target, row0, n_rows, b, G, j, V)[x]);
-                logp = kLn2 * (fmaf(tx, c2, -s.m) - log2f(s.S));
-                const float logq = draft_logq[(size_t)b * G + j];
+                const double logp = (double)tx / (double)T - lse_d;
+                const double logq = (double)draft_logq[(size_t)b * G + j];
                 const uint4 w4 = philox4x32_10(make_uint4(0u, (uint32_t)j, id, kStreamAccept), k0, k1);
-                pass = word_to_uniform(w4.x) < expf(logp - logq);
-                lse_out = kLn2 * lse2;
+                pass = (logp >= logq) || ((double)word_to_uniform(w4.x) < exp(logp - logq));
+                lse_out = (float)lse_d;
+                logp_out = (float)logp;
             } else {
-                lse_out = s.key;
-                logp = (s.idx == x) ? 0.f : -INFINITY;
-                pass = (s.idx == x);
-                amax = s.idx;
+                float zmax;
+                const unsigned long long bw = best_of_partials(pr, nsplit, &zmax);
+                amax = word_token(bw);
+                lse_out = zmax;
+                logp_out = (amax == x) ? 0.f : -INFINITY;
+                pass = (amax == x);
             }
         }
         const unsigned int fail = __ballot_sync(0xffffffffu, tested && !pass);
         const int first = fail ? j0 + __ffs(fail) - 1 : INT_MAX;  // the first failing row
         if (tested && j <= first) {
             if (target_lse) target_lse[(size_t)b * (G + 1) + j] = lse_out;
-            if (logp_sel) logp_sel[(size_t)b * G + j] = logp;
+            if (logp_sel) logp_sel[(size_t)b * G + j] = logp_out;
         }
         if (fail) {
             k = first;
             if (T > 0.f) {
                 d = first;
-                if (j == first) lse_t_row[b] = lse2;
+                if (j == first) {
+                    const float hi = (float)lse_d;
+                    lse_t_row[b] = make_float2(hi, (float)(lse_d - (double)hi));
+                }
             } else {
                 y = __shfl_sync(0xffffffffu, amax, first - j0);
             }
@@ -271,12 +300,19 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
     } else if (y < 0 && T > 0.f) {
         code = (2 << 16) | L;              // bonus draw from row L
     } else if (y < 0) {                    // greedy bonus: argmax of row L
-        RowState s = row_state_init();
         const RowState *pr = part + ((size_t)b * (G + 1) + L) * nsplit;
-        for (int i = lane; i < nsplit; i += 32) row_state_merge(s, pr[i]);
-        s = warp_merge(s);
-        y = s.idx;
-        if (lane == 0 && target_lse) target_lse[(size_t)b * (G + 1) + L] = s.key;
+        unsigned long long bw = 0ull;
+        float zb = 0.f;
+        for (int i = lane; i < nsplit; i += 32)
+            if (pr[i].best > bw) {
+                bw = pr[i].best;
+                zb = pr[i].z_at;
+            }
+        const unsigned long long mw = warp_max_u64(bw);
+        y = word_token(mw);
+        const unsigned int own = __ballot_sync(0xffffffffu, bw == mw);
+        const float zmax = __shfl_sync(0xffffffffu, zb, __ffs(own) - 1);
+        if (lane == 0 && target_lse) target_lse[(size_t)b * (G + 1) + L] = zmax;
     }
     for (int j = lane; j < k; j += 32) out_tokens[(size_t)b * (G + 1) + j] = draft_tokens[(size_t)b * G + j];
     if (lane == 0) {
@@ -289,9 +325,55 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
 }
 
 // ------------------------------------------------- pass 3 (SIMT / stored) ----
+// The screened per-token Gumbel-max step of the final draw for one token with
+// word w, against the best key kbest this thread has seen (natural-log units).
+// Residual rows (lse_q < +inf): weight r = p - q with p = exp(t/T - lse_t),
+// q = exp(z/T - lse_q), key ln r + g(u) where r > 0; bonus and fallback rows
+// (lse_q = +inf): key t/T + g(u).  The screen (1 - u) < (weight bound) 2^-K
+// loses no winner; survivors within rounding of the threshold get the
+// float-float key, and the key words decide.
+__device__ __forceinline__ void final_token_step(unsigned long long &best, float &kbest, float t, float z, float T,
+                                                 float rT, float c2, FF lse_t, float lse_q, uint32_t w, int v) {
+    const bool residual = lse_q != INFINITY;
+    const float K2 = kbest * kLog2e;
+    float k2;
+    if (residual) {
+        const float pv = exp2f(fmaf(t, c2, -lse_t.hi * kLog2e));
+        const float qv = exp2f(fmaf(z, c2, -lse_q * kLog2e));
+        const float ub = (pv - qv) + 4e-7f * (pv + qv);
+        if (!(ub > 0.f)) return;
+        if (!(one_minus_uniform_plus_one(w) < fmaf(ub, screen_q(0.f, kbest), 1.f))) return;
+        k2 = log2f(ub) - log2f(neg_log_uniform(w));
+    } else {
+        const float s2 = t * c2;
+        if (!(one_minus_uniform_plus_one(w) < screen_q(s2, kbest) + 1.f)) return;
+        k2 = s2 - log2f(neg_log_uniform(w));
+    }
+    if (!(k2 > K2 - key_tol2(k2, K2))) return;
+    FF key;
+    if (residual) {
+        // ln r = ln p + ln(1 - q / p), ln q - ln p in float-float
+        const FF lp = ff_add(div_ff(t, T, rT), ff_neg(lse_t));
+        const FF dl = ff_add(ff_add(div_ff(z, T, rT), FF{-lse_q, 0.f}), ff_neg(lp));
+        const float d = dl.hi + dl.lo;
+        if (!(d < 0.f)) return;  // p <= q: no residual mass
+        const float l1m = (d > -0.6931472f) ? logf(-expm1f(d)) : log1pf(-expf(d));
+        key = ff_add(lp, FF{l1m, 0.f});
+    } else {
+        key = div_ff(t, T, rT);
+    }
+    key = ff_add(key, gumbel_ff(w));
+    const unsigned long long word = key_word(key, v);
+    if (word > best) {
+        best = word;
+        kbest = fmaxf(kbest, key.hi);
+    }
+}
+
 // Final draw with CUDA cores: residual rows take the draft logits of the
 // rejected row from the stored draft logits (any dtype) or rebuild them with
-// FMAs (fp32 weights); bonus rows draw from the target row L.
+// FMAs (fp32 weights); bonus rows draw from the target row L.  Each thread
+// takes four tokens at a time (one Philox block).
 template <typename TIn>
 __global__ void __launch_bounds__(kResThreads)
 verify_final_simt_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ row0, int64_t n_rows,
@@ -300,21 +382,26 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const int64_t *__restri
                          const float *__restrict__ z_in, const int32_t *__restrict__ anchor,
                          const int32_t *__restrict__ draft_tokens, const float *__restrict__ draft_lse,
                          const float *__restrict__ temperature, const uint32_t *__restrict__ request_id,
-                         const int32_t *__restrict__ final_code, const float *__restrict__ lse_t_row,
+                         const int32_t *__restrict__ final_code, const float2 *__restrict__ lse_t_row,
                          int B, int G, int V, int r, uint32_t k0, uint32_t k1, int chunk, int nsplit,
                          ResidualState *__restrict__ part) {
     extern __shared__ float a_row[];  // [r]
-    __shared__ ResidualState scratch[kResThreads / 32];
+    __shared__ unsigned long long scratch[kResThreads / 32];
     const int b = blockIdx.x;  // requests along x, segments along y
     const int code = final_code[b];
     if (code < 0) return;
     const int kind = code >> 16, d = code & 0xFFFF;
     const int seg = blockIdx.y;
-    const float c2 = kLog2e / temperature[b];
+    const float T = temperature[b];
+    const float c2 = kLog2e / T, rT = __frcp_rn(T);
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     const bool residual = (kind == 1);
-    const float lse_q2 = residual ? draft_lse[(size_t)b * G + d] * kLog2e : INFINITY;
-    const float lse_t2 = residual ? lse_t_row[b] : 0.f;
+    const float lse_q = residual ? draft_lse[(size_t)b * G + d] : INFINITY;
+    FF lse_t{0.f, 0.f};
+    if (residual) {
+        const float2 lt = lse_t_row[b];
+        lse_t = FF{lt.x, lt.y};
+    }
     if (residual && !z_in) {
         const int prev = (d == 0) ? anchor[b] : draft_tokens[(size_t)b * G + d - 1];
         for (int k = threadIdx.x; k < r; k += blockDim.x) a_row[k] = to_f32(e_in[(size_t)prev * r + k]);
@@ -323,25 +410,16 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const int64_t *__restri
     const size_t drow = (size_t)b * G + d;
     const TIn *t_row = target_row(target, row0, n_rows, b, G, d, V);  // checked by the decide kernel
     const uint32_t stream = residual ? kStreamResidual : kStreamBonus;
-    const int vb = seg * chunk;  // a multiple of 16: whole draw groups
+    const int vb = seg * chunk;  // a multiple of 16
     const int ve = min(V, vb + chunk);
-    const int lane = threadIdx.x & 31;
-    ResidualState st = residual_init();
-    // One 16-token draw group (R2b) per quad of lanes, four tokens each.  A
-    // residual row weighs token v by r_v = p_v - q_v where positive (p and q
-    // normalised); a bonus row by 2^(t_v c2 - tref) with the group's maximum
-    // as tref.  Every thread runs the same iterations (the quads shuffle).
-    for (int vbase = vb; vbase < ve; vbase += 4 * kResThreads) {
-        const int v = vbase + 4 * threadIdx.x;
-        const bool valid = v < ve;  // V % 8 == 0: all four tokens or none
-        float t[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        float z[4] = {0.f, 0.f, 0.f, 0.f};
-        if (valid) {
-            const float4 t4 = load4(t_row + v);
+    unsigned long long best = 0ull;
+    float kbest = -INFINITY;
+    for (int v = vb + 4 * threadIdx.x; v < ve; v += 4 * kResThreads) {  // V % 8 == 0: four tokens at once
+        float t[4], z[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4 t4 = load4(t_row + v);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) t[e] = elem(t4, e);
-        }
-        if (valid && residual) {
+        for (int e = 0; e < 4; ++e) t[e] = elem(t4, e);
+        if (residual) {
             if (z_in) {
                 const float4 z4 = *reinterpret_cast<const float4 *>(z_in + drow * V + v);
                 z[0] = z4.x; z[1] = z4.y; z[2] = z4.z; z[3] = z4.w;
@@ -365,79 +443,27 @@ verify_final_simt_kernel(const TIn *__restrict__ target, const int64_t *__restri
                 for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[e];
             }
         }
-        float tref = lse_t2, off = 0.f;
-        if (!residual) {
-            float tm = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
-            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
-            tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
-            tref = off = tm * c2;
-        }
-        float w4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float we = 0.f;
-            if (valid) {
-                if (residual) {
-                    // p (1 - 2^-delta), delta = log2 p - log2 q from the logits first
-                    const float delta2 = fmaf(t[e] - z[e], c2, lse_q2 - lse_t2);
-                    if (delta2 > 0.f)
-                        we = exp2f(fmaf(t[e], c2, -lse_t2)) * (delta2 > 24.f ? 1.f : -expm1f(-delta2 * kLn2));
-                } else {
-                    we = exp2f(fmaf(t[e], c2, -tref));
-                }
-            }
-            w4[e] = we;
-        }
-        float gs = ((w4[0] + w4[1]) + w4[2]) + w4[3];
-        gs += __shfl_xor_sync(0xffffffffu, gs, 1);
-        gs += __shfl_xor_sync(0xffffffffu, gs, 2);
-        const bool leader = (lane & 3) == 0;
-        bool take = false;
-        float key = -INFINITY;
-        uint4 wd = make_uint4(0u, 0u, 0u, 0u);
-        if (leader && valid && gs > 0.f) {
-            wd = philox4x32_10(make_uint4((uint32_t)v >> 4, (uint32_t)d, id, stream), k0, k1);
-            key = off + log2f(gs) - log2f(neg_log_uniform(wd.x));
-            take = key > st.key_res;  // an exact tie keeps the earlier, lower-numbered group
-        }
-        if (!__any_sync(0xffffffffu, take)) continue;
-        float wq[16];
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) wq[4 * qd + e] = __shfl_sync(0xffffffffu, w4[e], (lane & ~3) + qd);
-        if (!take) continue;
-        float run = 0.f;
-#pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) run += wq[i2];
-        const float target = word_to_uniform(wd.y) * run;
-        int x = -1, last = 0;
-        run = 0.f;
-#pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) {
-            run += wq[i2];
-            if (wq[i2] > 0.f) last = i2;
-            if (x < 0 && run > target) x = i2;
-        }
-        if (x < 0) x = last;  // target rounded up to the group's sum
-        st.key_res = key;
-        st.idx_res = v + x;
+        const uint4 wd = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, stream), k0, k1);
+        final_token_step(best, kbest, t[0], z[0], T, rT, c2, lse_t, lse_q, wd.x, v);
+        final_token_step(best, kbest, t[1], z[1], T, rT, c2, lse_t, lse_q, wd.y, v + 1);
+        final_token_step(best, kbest, t[2], z[2], T, rT, c2, lse_t, lse_q, wd.z, v + 2);
+        final_token_step(best, kbest, t[3], z[3], T, rT, c2, lse_t, lse_q, wd.w, v + 3);
     }
-    st = residual_warp_merge(st);
-    const int warp = threadIdx.x >> 5;
-    if (lane == 0) scratch[warp] = st;
+    best = warp_max_u64(best);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) scratch[warp] = best;
     __syncthreads();
     if (warp == 0) {
-        st = (lane < kResThreads / 32) ? scratch[lane] : residual_init();
-        st = residual_warp_merge(st);
-        if (lane == 0) part[(size_t)b * nsplit + seg] = st;
+        best = (lane < kResThreads / 32) ? scratch[lane] : 0ull;
+        best = warp_max_u64(best);
+        if (lane == 0) part[(size_t)b * nsplit + seg].best = best;
     }
 }
 
 // One warp per request with a final draw: merge the partials, emit the token.
 // If a residual row had no entry with p > q at all (impossible in exact
 // arithmetic after a rejection), the token is drawn from p with the residual
-// stream instead (a group draw over the target row, here).
+// stream instead (a per-token Gumbel-max over the target row, here).
 template <typename TIn>
 __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part, int nsplit,
                                           const int32_t *__restrict__ final_code,
@@ -452,59 +478,27 @@ __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part
     if (b >= B) return;
     const int code = final_code[b];
     if (code < 0) return;
-    ResidualState s = residual_init();
-    for (int i = lane; i < nsplit; i += 32) residual_merge(s, part[(size_t)b * nsplit + i]);
-    s = residual_warp_merge(s);
-    int y = s.idx_res;
-    if (y == INT32_MAX) {  // degenerate residual: a group draw from p (stream 2)
+    unsigned long long w = 0ull;
+    for (int i = lane; i < nsplit; i += 32) w = max(w, part[(size_t)b * nsplit + i].best);
+    w = warp_max_u64(w);
+    if (w == 0ull) {  // degenerate residual: a draw from p (stream 2)
         const int d = code & 0xFFFF;
-        const float c2 = kLog2e / temperature[b];
+        const float T = temperature[b];
+        const float c2 = kLog2e / T, rT = __frcp_rn(T);
         const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
         const TIn *t_row = target_row(target, row0, n_rows, b, G, d, V);
-        // each lane keys its own groups, then the warp keeps the best (lowest
-        // group on ties) and resolves its token
-        float kb = -INFINITY;
-        int gb = INT32_MAX;
-        for (int g0 = 16 * lane; g0 < V; g0 += 16 * 32) {
-            const int g1 = min(g0 + 16, V);
-            float m = -INFINITY;
-            for (int v = g0; v < g1; ++v) m = fmaxf(m, to_f32(t_row[v]) * c2);
-            float S = 0.f;
-            for (int v = g0; v < g1; ++v) S += exp2f(fmaf(to_f32(t_row[v]), c2, -m));
-            const uint4 wd = philox4x32_10(make_uint4((uint32_t)g0 >> 4, (uint32_t)d, id, kStreamResidual), k0, k1);
-            const float key = m + log2f(S) - log2f(neg_log_uniform(wd.x));
-            if (key > kb) {
-                kb = key;
-                gb = g0;
-            }
+        float kbest = -INFINITY;
+        for (int v = 4 * lane; v < V; v += 4 * 32) {
+            const float4 t4 = load4(t_row + v);
+            const uint4 wd = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)d, id, kStreamResidual), k0, k1);
+            final_token_step(w, kbest, t4.x, 0.f, T, rT, c2, FF{0.f, 0.f}, INFINITY, wd.x, v);
+            final_token_step(w, kbest, t4.y, 0.f, T, rT, c2, FF{0.f, 0.f}, INFINITY, wd.y, v + 1);
+            final_token_step(w, kbest, t4.z, 0.f, T, rT, c2, FF{0.f, 0.f}, INFINITY, wd.z, v + 2);
+            final_token_step(w, kbest, t4.w, 0.f, T, rT, c2, FF{0.f, 0.f}, INFINITY, wd.w, v + 3);
         }
-#pragma unroll
-        for (int mask = 16; mask > 0; mask >>= 1) {
-            const float ko = __shfl_xor_sync(0xffffffffu, kb, mask);
-            const int go = __shfl_xor_sync(0xffffffffu, gb, mask);
-            if (key_better(ko, go, kb, gb)) {
-                kb = ko;
-                gb = go;
-            }
-        }
-        const int g1 = min(gb + 16, V);
-        float m = -INFINITY;
-        for (int v = gb; v < g1; ++v) m = fmaxf(m, to_f32(t_row[v]) * c2);
-        float S = 0.f;
-        for (int v = gb; v < g1; ++v) S += exp2f(fmaf(to_f32(t_row[v]), c2, -m));
-        const uint4 wd = philox4x32_10(make_uint4((uint32_t)gb >> 4, (uint32_t)d, id, kStreamResidual), k0, k1);
-        const float tgt = word_to_uniform(wd.y) * S;
-        float run = 0.f;
-        y = g1 - 1;
-        for (int v = gb; v < g1; ++v) {
-            run += exp2f(fmaf(to_f32(t_row[v]), c2, -m));
-            if (run > tgt) {
-                y = v;
-                break;
-            }
-        }
+        w = warp_max_u64(w);
     }
-    if (lane == 0) out_tokens[(size_t)b * (G + 1) + accept_len[b]] = y;
+    if (lane == 0) out_tokens[(size_t)b * (G + 1) + accept_len[b]] = word_token(w);
 }
 
 // Beside the draft kernel the blocks must share an SM with a draft CTA, which
@@ -542,7 +536,7 @@ cudaError_t launch_verify_finish_t(const VerifyArgs &a, const VerifyPlan &p, cud
     uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
     RowState *row_part = reinterpret_cast<RowState *>(a.ws + p.row_part_offset);
     int32_t *final_code = reinterpret_cast<int32_t *>(a.ws + p.res_row_offset);
-    float *lse_t_row = reinterpret_cast<float *>(a.ws + p.lse_t_offset);
+    float2 *lse_t_row = reinterpret_cast<float2 *>(a.ws + p.lse_t_offset);
     ResidualState *res_part = reinterpret_cast<ResidualState *>(a.ws + p.res_part_offset);
     uint32_t *res_best = reinterpret_cast<uint32_t *>(a.ws + p.res_best_offset);
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
@@ -615,7 +609,7 @@ VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {
     long want_r = (2L * kNumSMs + B - 1) / B;
     int max_r = (V + 1023) / 1024;
     int rs = (int)(want_r < 1 ? 1 : (want_r > max_r ? max_r : want_r));
-    int rchunk = ((V + rs - 1) / rs + 15) / 16 * 16;  // whole draw groups per segment
+    int rchunk = ((V + rs - 1) / rs + 15) / 16 * 16;
     p.res_chunk = rchunk;
     p.res_split = (V + rchunk - 1) / rchunk;
     p.res_split_tc = p.tensor_residual ? tc_segments(B, V) : 0;
@@ -626,7 +620,7 @@ VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {
     p.res_row_offset = off;
     off = align_up(off + sizeof(int32_t) * (size_t)B, 256);
     p.lse_t_offset = off;
-    off = align_up(off + sizeof(float) * (size_t)B, 256);
+    off = align_up(off + sizeof(float2) * (size_t)B, 256);
     p.res_part_offset = off;
     off = align_up(off + sizeof(ResidualState) * (size_t)B * res_slots, 256);
     p.res_best_offset = off;

@@ -4,12 +4,11 @@ them under the parity contract.
 Contract (fp32 device arithmetic against a double-precision oracle):
   - token ids, accepted lengths and verify lengths are bit-exact, except for a
     decision the oracle itself places on a near-tie: a Gumbel (or greedy)
-    top-two gap <= TIE_GUMBEL * max(1, |top key|), a draft's in-group inverse
-    CDF that lands within TIE_CDF (relative to the group's mass) of a
-    neighbouring token's boundary, an acceptance uniform within
-    TIE_ACCEPT of min(1, p/q), or a scheduler step whose Theta change or
-    candidate order is within TIE_THETA (relative).  Such mismatches are
-    counted; everything after a divergence in the same request is skipped.
+    top-two gap <= TIE_GUMBEL * max(1, |top key|), an acceptance uniform
+    within TIE_ACCEPT of min(1, p/q), or a scheduler step whose Theta change
+    or candidate order is within TIE_THETA (relative).  Such mismatches are
+    counted (``exempt``, out of ``decisions``); everything after a divergence
+    in the same request is skipped.  A mismatch on any other decision fails.
   - log-sum-exps and calibrated confidences agree within REL (relative, with
     a floor of 1 on the scale); log-probabilities within REL absolute (that is,
     probabilities within REL relative) down to log p = -64, and within
@@ -31,10 +30,9 @@ from speculative_decoding_draft_head_gb300.synth import make_inputs
 REL = 1e-5
 TIE_GUMBEL = 1e-5
 TIE_ACCEPT = 1e-6
-# the device's in-group running sums use ex2.approx values (relative error
-# about 2^-22 each), so they sit within about 1.2e-6 of the group's mass
-TIE_CDF = 4e-6
 TIE_THETA = 1e-6
+# exempt (near-tie) mismatches allowed per decision: the parity bar
+EXEMPT_RATE = 1e-6
 
 
 @dataclasses.dataclass
@@ -50,6 +48,24 @@ class Tally:
 
     def check(self):
         assert not self.failures, "\n".join(self.failures[:20])
+
+    def allowed_exempt(self):
+        """Exempt mismatches a test of this many decisions may see at the
+        parity bar (EXEMPT_RATE per decision): the count below which a
+        Poisson count at that rate stays with probability 1 - 1e-3."""
+        lam = EXEMPT_RATE * self.decisions
+        k, p, cdf = 0, math.exp(-lam), math.exp(-lam)
+        while cdf < 1.0 - 1e-3:
+            k += 1
+            p *= lam / k
+            cdf += p
+        return k
+
+    def check_rate(self):
+        self.check()
+        assert self.exempt <= self.allowed_exempt(), (
+            "%d exempt near-tie mismatches in %d decisions (allowed %d at %.0e per decision)"
+            % (self.exempt, self.decisions, self.allowed_exempt(), EXEMPT_RATE))
 
 
 def to_host(d):
@@ -111,7 +127,7 @@ def compare_draft(g, o, temps, reqs):
             t.decisions += 1
             if gt[b, j] != o["tokens"][i, j]:
                 gap, top = o["gap"][i, j], o["top"][i, j]
-                if gap <= TIE_GUMBEL * max(1.0, abs(top)) or o["cdf_margin"][i, j] <= TIE_CDF:
+                if gap <= TIE_GUMBEL * max(1.0, abs(top)):
                     t.exempt += 1
                     diverged[i] = True
                     break
@@ -175,7 +191,7 @@ def compare_verify(g, o, temps, reqs, skip):
             t.failures.append("accepted prefix b=%d" % b)
         if go[b, ka] != o["out_tokens"][i, ko]:
             gap, top = o["final_gap"][i], o["final_top"][i]
-            if gap <= TIE_GUMBEL * max(1.0, abs(top)) or o["final_cdf"][i] <= TIE_CDF:
+            if gap <= TIE_GUMBEL * max(1.0, abs(top)):
                 t.exempt += 1
             else:
                 t.failures.append("final token b=%d gpu=%d oracle=%d kind=%d gap=%.3g" %

@@ -67,7 +67,7 @@ def test_masked_tokens_match_oracle_and_are_never_emitted(case, seed):
         skip |= g["sched"]["verify_len"].numpy() != o["sched"]["verify_len"]
     t.add(compare_verify(g["verify"], o["verify"], temps, o["reqs"], skip))
     t.check()
-    assert t.exempt <= max(1, t.decisions // 1000)
+    assert t.exempt <= t.allowed_exempt()
     # a masked token has probability 2^-40000 or less: never drafted, never emitted
     tok = g["draft"]["tokens"].numpy()
     out = g["verify"]["out_tokens"].numpy()

@@ -1,32 +1,38 @@
-"""Parity by volume: about a million decisions against the oracle.
+"""Parity by volume: a few million decisions against the oracle.
 
-Two oracle-cheap workloads with many requests: the tiny one (fp32 weights, the
-CUDA-core path) and dspark5 with a small vocabulary (bf16 weights, the
-tensor-core path, scheduler on).  Every decision must match the oracle except
-those the oracle places on a near-tie (counted as exempt), and the exempt
-count must stay below 2e-5 of all decisions (the fp32 device arithmetic
-against fp64: ex2.approx terms in the in-group running sums, group keys within
-about 1e-6 of each other).  The observed rate is printed.
+Oracle-cheap workloads with many requests: the tiny one (fp32 weights, the
+CUDA-core path), and dspark5, highconc and largev with small vocabularies
+(bf16 weights, the tensor-core path; the scheduler on; per-request
+temperatures; greedy and sampled rows mixed).  Every decision (a draft draw,
+an acceptance test, a residual or bonus draw, a scheduler admission) must
+match the oracle, except those the oracle places on a near-tie, and those
+exempt mismatches must stay at or below 1e-6 of all decisions (the fp32 device
+arithmetic against fp64; the draws' keys are formed in float-float, so the
+mismatches come from ties far below fp32 rounding and from the fp32
+log-probabilities passed between the calls).  The observed rate is printed.
 """
 import pytest
 
 from speculative_decoding_draft_head_gb300.synth import WORKLOADS
 
-from parity import Tally, full_parity
+from parity import EXEMPT_RATE, Tally, full_parity
 
 pytestmark = pytest.mark.gpu
 
 
-def test_a_million_decisions():
+def test_millions_of_decisions():
     total = Tally()
-    runs = [(WORKLOADS["tiny"].scaled(B=16384), range(8)),
-            (WORKLOADS["dspark5"].scaled(B=2048, V=2056), range(8))]
+    runs = [(WORKLOADS["tiny"].scaled(B=16384), range(16)),
+            (WORKLOADS["dspark5"].scaled(B=2048, V=2056), range(8)),
+            (WORKLOADS["highconc"].scaled(B=2048, V=1032), range(8)),
+            (WORKLOADS["largev"].scaled(B=1024, V=4104), range(4))]
     for w, seeds in runs:
         for seed in seeds:
             t, _, _, _ = full_parity(w, seed)
             total.add(t)
     total.check()
     rate = total.exempt / total.decisions
-    print("parity volume: %d decisions, %d exempt near-ties (%.2e)" % (total.decisions, total.exempt, rate))
-    assert total.decisions >= 1_000_000
-    assert rate < 2e-5
+    print("parity volume: %d decisions, %d exempt near-tie mismatches (%.2e)" %
+          (total.decisions, total.exempt, rate))
+    assert total.decisions >= 2_000_000
+    assert rate <= EXEMPT_RATE
