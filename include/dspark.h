@@ -46,7 +46,15 @@
  *    (seed mod 2^32, seed >> 32) and counter = (v >> 2, j, request_id,
  *    stream), output word v & 3; u = ((w >> 9) + 0.5) * 2^-23.  Streams:
  *    0 draft Gumbel noise, 1 acceptance uniform, 2 residual Gumbel noise,
- *    3 bonus Gumbel noise.  A call is reproducible from (seed, request ids).
+ *    3 bonus Gumbel noise; each token v of a Gumbel-max draw takes its own
+ *    word.  A call is reproducible from (seed, request ids).
+ *  - Precision: the arithmetic is fp32 on fp32 or bf16 data.  The kernels
+ *    screen tokens in fp32 and form the Gumbel keys of the few tokens that
+ *    can still win in float-float arithmetic (about 44 significant bits), and
+ *    the small merge and decision kernels work in double, so a draw or an
+ *    acceptance differs from an exact evaluation only on a tie far below fp32
+ *    rounding (about 1e-7 of decisions or fewer, in the test suite none in
+ *    2.5 million).
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -120,13 +128,10 @@ DSPARK_API size_t dspark_workspace_bytes(int which, int B, int G, int V, int r);
  * For each request b and j = 0 .. G-1, with prev = anchor[b] (j = 0) or
  * draft_tokens[b][j-1]:
  *   z[v]  = base_logits[b][j][v] + sum_k e_in[prev][k] * w_out[v][k]   (fp32)
- *   T > 0: s = z / T, lse = log sum exp s, x_j drawn from softmax(s) by the
- *          group draw: with groups of 16 consecutive tokens (the last one may
- *          be ragged) and u0 = u(seed, request_id[b], j, 4 g, stream 0),
- *          u1 = u(.., 4 g + 1, stream 0) (words 0 and 1 of group g's Philox
- *          block), the group g* with the largest log sum_{v in g} exp s[v] -
- *          ln(-ln u0) wins and x_j is its first token whose running sum of
- *          exp s exceeds u1 times the group's sum; logq = s[x_j] - lse
+ *   T > 0: s = z / T, lse = log sum exp s, x_j drawn from softmax(s) by
+ *          per-token Gumbel-max: x_j = argmax_v s[v] - ln(-ln u_v) with
+ *          u_v = u(seed, request_id[b], j, v, stream 0), the lowest id on an
+ *          exact tie; logq = s[x_j] - lse
  *   T = 0: x_j = argmax_v z[v] (lowest id on ties), lse = max z, logq = 0
  *
  * base_logits [B][G][V] dtype   e_in [V][r] dtype   w_out [V][r] dtype (row v
@@ -135,7 +140,9 @@ DSPARK_API size_t dspark_workspace_bytes(int which, int B, int G, int V, int r);
  * request_id [B] uint32 or NULL (then request b uses id b)
  * outputs: draft_tokens [B][G] int32, draft_lse [B][G] fp32,
  *          draft_logq [B][G] fp32, draft_logits [B][G][V] fp32 z or NULL.
- * Limits: 1 <= B, 1 <= G <= 64, 8 <= V < 2^31 with V % 8 == 0,
+ * Limits: 1 <= B, 1 <= G <= 64, 8 <= V <= 2^20 with V % 8 == 0 (the token id
+ *         shares a 64-bit key word with the key; larger V returns
+ *         DSPARK_ERR_UNSUPPORTED),
  *         16 <= r <= 256 with r % 16 == 0 (bf16) or 4 <= r <= 256 with
  *         r % 4 == 0 (fp32).  bf16 runs the bias on the tcgen05 tensor cores;
  *         fp32 runs it with CUDA-core FMAs (no TF32 rounding).
@@ -261,12 +268,13 @@ DSPARK_API dspark_status dspark_schedule_policy(
  *   draft's logq and lse);
  *   accept x_j while u(seed, id, j, 0, stream 1) < min(1, p_j(x_j)/q_j(x_j));
  *   at the first rejection d: y is drawn from normalise(max(0, p_d - q_d)) by
- *   the group draw of dspark_draft_sample (weights max(0, p - q), stream 2;
- *   from p_d itself if no entry has p > q) (the draft logits of row d are
- *   recomputed from base_logits, e_in and w_out, or read from draft_logits
- *   when it is not NULL);
- *   if all L are accepted: y is drawn from softmax(target[b][L] / T) by the
- *   group draw on stream 3.
+ *   per-token Gumbel-max on stream 2, y = argmax over {v: p_v > q_v} of
+ *   ln(p_v - q_v) - ln(-ln u(seed, id, d, v, stream 2)) (from p_d itself if no
+ *   entry has p > q) (the draft logits of row d are recomputed from
+ *   base_logits, e_in and w_out, or read from draft_logits when it is not
+ *   NULL);
+ *   if all L are accepted: y is drawn from softmax(target[b][L] / T) by
+ *   per-token Gumbel-max on stream 3.
  * T = 0: accept while x_j == argmax target[b][j]; y = that argmax at the first
  * mismatch, else argmax target[b][L].
  *
@@ -376,14 +384,16 @@ DSPARK_API dspark_status dspark_pack_target(
  * Scratch: a fixed DSPARK_NOALLOC_SCRATCH_BYTES array in the library's device
  * image, held by every GPU that loads the library until the process exits.
  * Its device address is looked up on the first call on each device (with that
- * device current): make that first call before any stream capture begins.
+ * device current) and kept for the life of the process, so a cudaDeviceReset
+ * invalidates it: make that first call before any stream capture begins, and
+ * do not use this entry point after a device reset.
  * Every call shares the array and finds the previous call's contents in it
  * (the flag word is cleared on each call); calls whose GPU work overlaps
  * (other streams, unordered host threads) race on it and must be avoided.
  * Sizes whose verify scratch exceeds the array return DSPARK_ERR_UNSUPPORTED
  * with a message in dspark_last_error().  No call allocates or frees memory.
- * The device flag word can be read with dspark_read_device_flags() only
- * through dspark_verify's own workspace, not for this entry point.
+ * The device flag word of the array (invalid inputs, a timeout, a packed row
+ * outside its array) is read with dspark_read_noalloc_flags().
  */
 #define DSPARK_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 
@@ -397,8 +407,12 @@ DSPARK_API dspark_status dspark_verify_noalloc(
     int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
     float *target_lse, float *logp_sel, void *stream);
 
-/* Copy the device flag word of a workspace to *flags (waits for `stream`).
- * Returns DSPARK_OK or DSPARK_ERR_CUDA. */
+/* Copy the device flag word of dspark_verify_noalloc's fixed array to *flags
+ * (waits for `stream`; the word of the last call, subject to the same race
+ * between overlapping calls).  Returns DSPARK_OK, DSPARK_ERR_INVALID_ARG for a
+ * NULL flags pointer, or DSPARK_ERR_CUDA. */
+DSPARK_API dspark_status dspark_read_noalloc_flags(void *stream, uint32_t *flags);
+
 /*
  * Self-test of the bounded device-side waits (the library's failure
  * detection): one block waits, with the helpers every kernel uses and a limit
@@ -410,6 +424,8 @@ DSPARK_API dspark_status dspark_verify_noalloc(
  */
 DSPARK_API dspark_status dspark_selftest_bounded_wait(unsigned int limit_us, uint32_t *result, void *stream);
 
+/* Copy the device flag word of a workspace to *flags (waits for `stream`).
+ * Returns DSPARK_OK or DSPARK_ERR_CUDA. */
 DSPARK_API dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags);
 
 #ifdef __cplusplus

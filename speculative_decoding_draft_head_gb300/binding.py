@@ -31,7 +31,8 @@ FLAG_BAD_TARGET_ROW = 32
 EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
            "dspark_schedule_prefix", "dspark_schedule_policy", "dspark_verify", "dspark_read_device_flags",
            "dspark_verify_noalloc", "dspark_draft_sample_rnn", "dspark_verify_packed", "dspark_pack_target",
-           "dspark_selftest_bounded_wait", "dspark_verify_rows", "dspark_verify_finish")
+           "dspark_selftest_bounded_wait", "dspark_verify_rows", "dspark_verify_finish",
+           "dspark_read_noalloc_flags")
 
 _lib = None
 _lock = threading.Lock()
@@ -96,6 +97,8 @@ def load(build_if_missing: bool = True):
                                             i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp]
         L.dspark_read_device_flags.restype = ctypes.c_int
         L.dspark_read_device_flags.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.dspark_read_noalloc_flags.restype = ctypes.c_int
+        L.dspark_read_noalloc_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         _lib = L
         return L
 
@@ -458,6 +461,13 @@ def selftest_bounded_wait(limit_us=1000, stream=None) -> int:
 def read_device_flags(workspace, stream=None) -> int:
     val = ctypes.c_uint32(0)
     _check(load().dspark_read_device_flags(_ptr(workspace), _stream(stream), ctypes.byref(val)))
+    return int(val.value)
+
+
+def read_noalloc_flags(stream=None) -> int:
+    """The flag word of the last :func:`verify_noalloc` call."""
+    val = ctypes.c_uint32(0)
+    _check(load().dspark_read_noalloc_flags(_stream(stream), ctypes.byref(val)))
     return int(val.value)
 
 

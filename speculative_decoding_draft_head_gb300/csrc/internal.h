@@ -43,6 +43,13 @@ struct PerDeviceOnce {
 // Record the message returned by dspark_last_error() and return `st`.
 dspark_status set_last_error(dspark_status st, const char *fmt, ...);
 
+// dspark_verify's host-side checks of sizes, pointers and alignment.
+dspark_status verify_check_args(const void *target_logits, const void *base_logits, const void *e_in,
+                                const void *w_out, const float *draft_logits, const int32_t *anchor,
+                                const int32_t *draft_tokens, const float *draft_lse, const float *draft_logq,
+                                const float *temperature, int B, int G, int V, int r, dspark_dtype dtype,
+                                const int32_t *accept_len, const int32_t *out_tokens, const int32_t *num_out);
+
 // ------------------------------------------------------------- selftest ----
 cudaError_t run_bounded_wait_probe(unsigned int limit_us, uint32_t *result, cudaStream_t s);
 

@@ -241,32 +241,58 @@ __device__ __forceinline__ uint32_t max_word16(const uint4 (&w)[4]) {
     return max(max(a, b), max(c, d));
 }
 
-// Draft epilogue for the 16 logits z of one row (T > 0, c2 = log2(e) / T,
-// rT = fl(1 / T)), tokens v .. v + n - 1, with their draft-stream words w
-// (word i of token v + i).  Every lane of the warp calls it together (it
-// votes across the warp); `on` is false for rows that are greedy or inactive,
-// which then change nothing.
+// A lane's running draw of one row in one block position: the two largest
+// screened fp32 keys k = z c2 - log2(-ln u) (log2 units) with their logits,
+// words and token ids.
+struct Top2 {
+    float k1, k2;
+    float z1, z2;
+    uint32_t w1, w2;
+    int v1, v2;
+};
+__device__ __forceinline__ Top2 top2_init() { return Top2{-INFINITY, -INFINITY, 0.f, 0.f, 0u, 0u, -1, -1}; }
+
+// Error bound of a screened key k (log2 units): log2(-ln u) within about
+// 1e-5 (log2_neg_log_uniform_fast), the fp32 roundings of z c2 and of k.
+__device__ __forceinline__ float screen_tol(float k) { return 2e-5f + 4e-7f * fabsf(k); }
+
+// The screening factor for a threshold K2 in log2 units (see screen_q).
+__device__ __forceinline__ float screen_q2(float m, float K2) {
+    if (K2 == -INFINITY) return INFINITY;
+    return fminf(fast_exp2(m - K2), kQMax) * (1.f + 4e-7f * (fabsf(K2) + fabsf(m) + 64.f));
+}
+
+// A published lower bound (natural log) in log2 units, rounded down.
+__device__ __forceinline__ float lower_to_log2(float kn) {
+    return (kn == -INFINITY) ? -INFINITY : fmaf(kn, kLog2e, -fabsf(kn) * 0x1p-21f);
+}
+
+// Draft epilogue for the 16 logits z of one row (T > 0, c2 = (c2, c2l) =
+// log2(e) / T), tokens v .. v + n - 1, with their draft-stream words w (word
+// i of token v + i).  Every lane of the warp calls it together (it votes
+// across the warp); `on` is false for rows that are greedy or inactive, which
+// then change nothing.
 //
-// Per-token Gumbel-max: token v beats the best key K known for the row iff
+// Per-token Gumbel-max: token v can reach a key above a threshold K only if
 // E_v = -ln u_v < e^(s_v - K) = e_v Q / margin, where e_v = 2^(s2_v - m) is
-// the softmax term already computed and Q = screen_q(m, K).  Since
+// the softmax term already computed and Q = screen_q2(m, K log2 e).  Since
 // E >= 1 - u, the test (1 - u_v) < e_v Q (conservative form f1 < fl(e Q + 1))
-// never loses a winner.  Most sub-slices are decided by one test: the
-// largest word of the 16 against the sub-slice's sum (sum >= every e_v).  A
-// sub-slice that passes tests its tokens one by one; the survivors get an
-// fp32 key (log2 units), and those within rounding of the threshold get the
-// float-float key, whose word (key_word) decides against the row's best.
+// never loses a token that can reach K.  Most sub-slices are decided by one
+// test: the largest word of the 16 against the sub-slice's sum (sum >= every
+// e_v).  A sub-slice that passes tests its tokens one by one and gives each
+// survivor an fp32 key k (within screen_tol of the exact one); the lane keeps
+// its two largest.  K is the largest lower bound known for the row: the
+// lane's own k1 - screen_tol(k1), or one another lane published (in natural
+// log, to the CTA's per-row word in shared memory and the row-wide word's high
+// half in global memory).  The exact (float-float) keys are formed once, at
+// the end of the position (draft_top2_word).
 //
 // The softmax keeps an integer reference m (log2 units) that may lag the
 // maximum: terms 2^(z c2 - m) above 1 are fine, and a group whose sum exceeds
-// 2^64 (or overflows) is redone against its own maximum.  A new best is
-// published with a max reduction twice: to the CTA's per-row word in shared
-// memory (read by the quadrant's warps before each sub-slice) and to the
-// row-wide word in global memory (read every fourth sub-slice).
-__device__ __forceinline__ void draft_tokens16(RowState &st, float &Q, float &kbest, const float (&z)[16], float c2,
-                                               float c2l, float T, float rT, int n, int v, bool on,
-                                               unsigned long long *best,
-                                               uint32_t *cta_best, const uint4 (&w)[4]) {
+// 2^64 (or overflows) is redone against its own maximum.
+__device__ __forceinline__ void draft_tokens16(RowState &st, Top2 &tp, float &Q, float &K2, const float (&z)[16],
+                                               float c2, float c2l, int n, int v, bool on,
+                                               unsigned long long *best, uint32_t *cta_best, const uint4 (&w)[4]) {
     const bool full = (n == 16);  // warp-uniform
     float e[16];
     float sum = 0.f;
@@ -278,7 +304,7 @@ __device__ __forceinline__ void draft_tokens16(RowState &st, float &Q, float &kb
             for (int i = 0; i < 16; ++i)
                 if (full || i < n) zm = fmaxf(zm, z[i]);
             st.m = ceilf(zm * c2);  // c2 > 0: the rounded product is monotone in z
-            Q = screen_q(st.m, kbest);
+            Q = screen_q2(st.m, K2);
         }
         if (full) {
 #pragma unroll
@@ -296,7 +322,7 @@ __device__ __forceinline__ void draft_tokens16(RowState &st, float &Q, float &kb
             const float cm = ceilf(fmaxf(st.m, zm * c2));
             st.S = scale_pow2(st.S, st.m - cm);
             st.m = cm;
-            Q = screen_q(st.m, kbest);
+            Q = screen_q2(st.m, K2);
 #pragma unroll
             for (int i = 0; i < 16; ++i) e[i] = (full || i < n) ? term_exp2(z[i], c2, c2l, st.m) : 0.f;
             sum = sum16(e);
@@ -305,49 +331,62 @@ __device__ __forceinline__ void draft_tokens16(RowState &st, float &Q, float &kb
     }
     const bool grp = on && sum > 0.f && one_minus_uniform_plus_one(max_word16(w)) < fmaf(sum, Q, 1.f);
     if (!(__any_sync(0xffffffffu, grp) && grp)) return;
-    // rare: the tokens one by one; survivors' fp32 keys replace their terms in e
+    // rare: the tokens one by one (e_v = 0 for tokens past n fails the test)
+    const float k1_before = tp.k1;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const uint32_t wi = word_at(w, i);
-        float k2 = -INFINITY;
-        if (one_minus_uniform_plus_one(wi) < fmaf(e[i], Q, 1.f))
-            k2 = fmaf(z[i], c2, -fast_log2(neg_log_uniform(wi)));
-        e[i] = k2;
-    }
-#pragma unroll 1
-    while (true) {
-        float kb2 = -INFINITY;
-        int ib = -1;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (e[i] > kb2) {
-                kb2 = e[i];
-                ib = i;
-            }
-        const float K2 = kbest * kLog2e;
-        if (ib < 0 || !(kb2 > K2 - key_tol2(kb2, K2))) break;
-        float zb = 0.f;
-        uint32_t wb = 0u;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (i == ib) {
-                zb = z[i];
-                wb = word_at(w, i);
-                e[i] = -INFINITY;
-            }
-        const FF key = ff_add(div_ff(zb, T, rT), gumbel_ff(wb));
-        const unsigned long long word = key_word(key, v + ib);
-        if (word > st.best) {
-            st.best = word;
-            st.z_at = zb;
-            if (key.hi >= kbest) {
-                kbest = key.hi;
-                red_max_shared_u32(cta_best, key_to_ordered(key.hi));
-                red_max_u64(best, word);
-                Q = screen_q(st.m, kbest);
+        if (one_minus_uniform_plus_one(wi) < fmaf(e[i], Q, 1.f)) {
+            const float k = fmaf(z[i], c2l, fmaf(z[i], c2, -log2_neg_log_uniform_fast(wi)));
+            if (k > tp.k2) {
+                if (k > tp.k1) {
+                    tp.k2 = tp.k1;
+                    tp.z2 = tp.z1;
+                    tp.w2 = tp.w1;
+                    tp.v2 = tp.v1;
+                    tp.k1 = k;
+                    tp.z1 = z[i];
+                    tp.w1 = wi;
+                    tp.v1 = v + i;
+                } else {
+                    tp.k2 = k;
+                    tp.z2 = z[i];
+                    tp.w2 = wi;
+                    tp.v2 = v + i;
+                }
             }
         }
     }
+    if (tp.k1 > k1_before) {
+        const float lower = tp.k1 - screen_tol(tp.k1);  // <= the exact key of token v1 (log2 units)
+        if (lower > K2) {
+            K2 = lower;
+            Q = screen_q2(st.m, K2);
+            // publish it in natural log, rounded down
+            const float kn = fmaf(lower, kLn2, -fabsf(lower) * 0x1p-21f);
+            red_max_shared_u32(cta_best, key_to_ordered(kn));
+            red_max_u64(best, (unsigned long long)key_to_ordered(kn) << 32);
+        }
+    }
+}
+
+// The exact key word of a lane's draw: the float-float key of its best
+// screened token, and of the second when the two fp32 keys are within their
+// error bounds of each other (then the larger word wins).  0 if none.
+__device__ __forceinline__ unsigned long long draft_top2_word(const Top2 &tp, float T, float rT, float *z_at) {
+    unsigned long long wb = 0ull;
+    if (tp.k1 > -INFINITY) {
+        wb = key_word(ff_add(div_ff(tp.z1, T, rT), gumbel_ff(tp.w1)), tp.v1);
+        *z_at = tp.z1;
+        if (tp.k2 >= tp.k1 - screen_tol(tp.k1) - screen_tol(tp.k2)) {
+            const unsigned long long w2 = key_word(ff_add(div_ff(tp.z2, T, rT), gumbel_ff(tp.w2)), tp.v2);
+            if (w2 > wb) {
+                wb = w2;
+                *z_at = tp.z2;
+            }
+        }
+    }
+    return wb;
 }
 
 // A timed-out CTA, before its shared memory and TMEM are given up: the copies
@@ -707,7 +746,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 
             RowState st = row_state_init();
             float Q = kQMax;
-            float kbest = -INFINITY;  // best key of the row known to this thread
+            float K2 = -INFINITY;  // the largest lower bound of an achieved key of the row (log2 units)
+            Top2 tp = top2_init();
             unsigned long long *best = (kFinal || b >= p.B) ? nullptr : p.best + (size_t)jj * p.B + b;
             uint32_t kg_next = 0u;  // "none"
             float kbest_r = -INFINITY;  // best residual key of the row known to this thread
@@ -762,10 +802,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     uint32_t acc[16];
                     const int vw = sub_col(si);
                     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + (si & 7) * 16;
-                    auto draw_words = [&]() {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) w[g] = philox_folded(((uint32_t)vw >> 2) + g, prow, p.keys);
-                    };
+                    auto draw_words = [&]() { philox_folded4((uint32_t)vw >> 2, prow, p.keys, w); };
                     if (t != waited) {
                         // a new tile: draw the words while its UMMAs may still run
                         draw_words();
@@ -819,13 +856,14 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             // the best key known for the row: this CTA's (shared memory,
                             // current) or the row-wide word's high half (global, loaded
                             // up to four sub-slices earlier)
-                            const float kg = ordered_to_key(max(kg_next, *(volatile uint32_t *)(row_kbest + row)));
-                            if (kg > kbest) {
-                                kbest = kg;
-                                Q = screen_q(st.m, kbest);
+                            const float kg = lower_to_log2(
+                                ordered_to_key(max(kg_next, *(volatile uint32_t *)(row_kbest + row))));
+                            if (kg > K2) {
+                                K2 = kg;
+                                Q = screen_q2(st.m, K2);
                             }
                         }
-                        draft_tokens16(st, Q, kbest, z, c2, c2l, Trow, rT, n, v, on, best, row_kbest + row, w);
+                        draft_tokens16(st, tp, Q, K2, z, c2, c2l, n, v, on, best, row_kbest + row, w);
                         // reload the row-wide word after this warp's first sub-slice of
                         // the position (by then every CTA has published its rows' first
                         // groups, so the threshold is tight from the second sub-slice
@@ -952,6 +990,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             }
             // merge the four column slices of each row
             if (!kFinal) {
+                if (c2 > 0.f) {  // sampled rows: the exact key word of the lane's draw
+                    float zb = 0.f;
+                    st.best = draft_top2_word(tp, Trow, rT, &zb);
+                    st.z_at = zb;
+                }
                 RowState *ms = reinterpret_cast<RowState *>(smem + kOffMerge);
                 ms[row * kEpiPerQuad + slice] = st;
             } else {

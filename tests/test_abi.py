@@ -178,3 +178,10 @@ def test_selftest_and_noalloc_reject_on_the_host():
     # an invalid size is reported as dspark_verify reports it
     args = [p] * 12 + [4, 0, 1024, 16, 0, 0] + [p] * 6
     assert lib.dspark_verify_noalloc(*args) == 1 and "G must be" in err()
+    # argument errors come before the scratch-size check, as in dspark_verify
+    args = [p] * 5 + [None] + [p] * 6 + [20096, 16, 129280, 256, 0, 0] + [p] * 6
+    assert lib.dspark_verify_noalloc(*args) == 1 and "NULL" in err()
+    args = [vp((1 << 12) + 4)] + [p] * 11 + [20096, 16, 129280, 256, 0, 0] + [p] * 6
+    assert lib.dspark_verify_noalloc(*args) == 1 and "aligned" in err()
+    # the flag reader wants somewhere to put the word
+    assert lib.dspark_read_noalloc_flags(None, None) == 1 and "NULL" in err()

@@ -59,3 +59,23 @@ def test_noalloc_rejects_sizes_beyond_the_fixed_array():
                                    4096, 64, 1024, 16, 1, 0, p, p, p, None, None, None)
     assert st == 2
     assert "scratch" in lib.dspark_last_error().decode()
+
+
+@pytest.mark.gpu
+def test_noalloc_flag_word_reports_invalid_device_inputs():
+    """An out-of-range verify length raises its bit in the fixed array's flag
+    word, which dspark_read_noalloc_flags returns; the next valid call clears
+    it."""
+    w = WORKLOADS["dspark5"].scaled(B=8, V=2056, scheduler=False)
+    inp = make_inputs(w, 5, device="cuda")
+    d = binding.draft_sample(inp["base"], inp["e_in"], inp["w_out"], inp["anchor"], inp["temperature"],
+                             inp["request_id"], 5)
+    vl = torch.full((w.B,), w.G, dtype=torch.int32, device="cuda")
+    vl[3] = w.G + 7
+    args = (inp["target"], inp["base"], inp["e_in"], inp["w_out"], inp["anchor"], d)
+    got = binding.verify_noalloc(*args, vl, inp["temperature"], inp["request_id"], 5)
+    assert binding.read_noalloc_flags() & binding.FLAG_BAD_VERIFY_LEN
+    assert int(got["accept_len"][3]) == -1
+    vl[3] = w.G
+    binding.verify_noalloc(*args, vl, inp["temperature"], inp["request_id"], 5)
+    assert binding.read_noalloc_flags() == 0
