@@ -202,6 +202,34 @@ def oracle_sample(w, h, seed, budget_s=12.0, threads=None):
                 seconds=total, positions=positions)
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baseline_line(w, h, seed, budget_s):
+    """The oracle on all host cores (the reported baseline) and on one core."""
+    cb = oracle_sample(w, h, seed, budget_s=budget_s)
+    c1 = oracle_sample(w, h, seed, budget_s=max(2.0, budget_s / 3), threads=1)
+    return dict(value=cb["value"], unit=UNIT, cores=cb["cores"], kind="oracle", sample=cb["sample"],
+                cpu_model=cpu_model(),
+                single_thread=dict(value=c1["value"], unit=UNIT, cores=1, sample=c1["sample"]))
+
+
 def run_reference(args, w):
     if int(os.environ.get("RANK", "0")) != 0:
         return
@@ -222,7 +250,7 @@ def run_reference(args, w):
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
                 config=_config(w),
                 cpu_baseline=dict(value=value, unit=UNIT, cores=info["cores"], kind="oracle",
-                                  sample=info["sample"]),
+                                  sample=info["sample"], cpu_model=cpu_model()),
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line))
 
@@ -478,6 +506,10 @@ def run_ours(args, w):
     e_ms = _max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
     e_value = total_positions / (e_ms / 1000.0)
 
+    # the device's Philox4x32-10 rate with the draft's own word code (the ALU
+    # roof of the per-token draw), measured here on this GPU
+    philox_peak = max(binding.selftest_philox_rate(2048) for _ in range(3))
+
     if rank != 0:
         return
     peaks = _peaks()
@@ -501,6 +533,26 @@ def run_ours(args, w):
     achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
     bias_flops = 2.0 * B * G * V * r
     traffic = _read_traffic(w, dominant)
+    # the ALU roof: one Philox4x32-10 block per four tokens of a draw; the
+    # draft draws B G V tokens, the final draw of verification one row per
+    # request (B V)
+    draft_blocks = B * G * ((V + 3) // 4)
+    final_blocks = B * ((V + 3) // 4)
+
+    def roof(nbytes, blocks, ms_call, dram=None):
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+        t_alu = blocks / philox_peak
+        hbm = dict(achieved=nbytes / (ms_call / 1000.0) / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
+                   frac=nbytes / (ms_call / 1000.0) / 1e9 / peaks["hbm_gbs"], floor_us=t_hbm * 1e6)
+        alu = dict(achieved=blocks / (ms_call / 1000.0) / 1e9, peak=philox_peak / 1e9,
+                   unit="G Philox4x32-10 blocks/s", frac=blocks / (ms_call / 1000.0) / philox_peak,
+                   floor_us=t_alu * 1e6)
+        return dict(bound="alu" if t_alu > t_hbm else "hbm", hbm=hbm, alu=alu)
+
+    r_draft = roof(draft_bytes, draft_blocks, d_ms)
+    r_verify = roof(verify_bytes + residual_bytes, final_blocks, v_ms)
+    r_dom = r_draft if dominant == "draft" else r_verify
+    dom_roof = r_dom[r_dom["bound"]]
     line = dict(
         metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=ms_max, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f32",
@@ -510,12 +562,20 @@ def run_ours(args, w):
         drafted_positions_per_s=B * G / (d_ms / 1000.0),
         acceptance=dict(accepted_over_tested=acceptance, tests=n_tests,
                         note="per-test acceptance min(1, p/q) realised on the synthetic workload"),
-        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
-                      frac=achieved / peaks["hbm_gbs"], traffic=traffic,
+        roofline=dict(bound=r_dom["bound"], achieved=dom_roof["achieved"], peak=dom_roof["peak"],
+                      unit=dom_roof["unit"], frac=dom_roof["frac"], traffic=traffic,
                       kernel=("draft call: markov_tc_kernel (all %d positions, one launch) + finalize" % G
                               if dominant == "draft" else "verify call (%d launches)" % launches_per_call),
-                      peak_source=peaks["source"],
+                      peak_source=("measured live: dspark_selftest_philox_rate (the draft's Philox code, "
+                                   "2048 threads per SM), best of 3" if r_dom["bound"] == "alu" else
+                                   peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"),
+                      hbm_frac=r_dom["hbm"]["frac"], alu_frac=r_dom["alu"]["frac"],
                       dram_gbs=(None if traffic is None else traffic / (dom_ms / 1000.0) / 1e9)),
+        rooflines=dict(draft=r_draft, verify=r_verify,
+                       note="per call (events around the call, eager issue): hbm = algorithmic bytes "
+                            "over the call time against the measured copy bandwidth; alu = Philox "
+                            "blocks (one per four drawn tokens) over the call time against the "
+                            "device's measured Philox rate; bound = the roof with the longer floor"),
         calls_ms=dict(draft=d_ms, schedule=s_ms, verify=v_ms),
         step_order=("schedule; then draft beside dspark_verify_rows on a second stream; then "
                     "dspark_verify_finish (calls_ms timed serially)" if args.overlap else
@@ -539,9 +599,7 @@ def run_ours(args, w):
     )
     if not args.no_cpu_baseline and world == 1:
         h = {k: t.cpu() for k, t in inp.items()}
-        cb = oracle_sample(w, h, args.seed, budget_s=args.cpu_budget)
-        line["cpu_baseline"] = dict(value=cb["value"], unit=UNIT, cores=cb["cores"], kind="oracle",
-                                    sample=cb["sample"])
+        line["cpu_baseline"] = cpu_baseline_line(w, h, args.seed, args.cpu_budget)
     print(json.dumps(line))
 
 

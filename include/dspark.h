@@ -424,6 +424,20 @@ DSPARK_API dspark_status dspark_read_noalloc_flags(void *stream, uint32_t *flags
  */
 DSPARK_API dspark_status dspark_selftest_bounded_wait(unsigned int limit_us, uint32_t *result, void *stream);
 
+/*
+ * The device's rate for the draw's random words: a grid of 2048 threads per
+ * SM draws Philox4x32-10 blocks with the same code as the draft kernel's
+ * per-token words (four consecutive counters per step, the parts fixed by
+ * request and position precomputed), iters x 4 blocks per thread, and
+ * *blocks_per_second receives the measured rate (CUDA events on `stream`;
+ * synchronises it).  This is the ALU roof of the per-token Gumbel-max draw,
+ * which needs one block per four tokens.  workspace: device scratch of at
+ * least 256 bytes per SM (the words are folded into it so that none is
+ * optimised away), 256-byte aligned; 1 <= iters <= 2^20.
+ */
+DSPARK_API dspark_status dspark_selftest_philox_rate(void *workspace, size_t workspace_bytes, int iters,
+                                                     double *blocks_per_second, void *stream);
+
 /* Copy the device flag word of a workspace to *flags (waits for `stream`).
  * Returns DSPARK_OK or DSPARK_ERR_CUDA. */
 DSPARK_API dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags);

@@ -32,7 +32,7 @@ EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dsp
            "dspark_schedule_prefix", "dspark_schedule_policy", "dspark_verify", "dspark_read_device_flags",
            "dspark_verify_noalloc", "dspark_draft_sample_rnn", "dspark_verify_packed", "dspark_pack_target",
            "dspark_selftest_bounded_wait", "dspark_verify_rows", "dspark_verify_finish",
-           "dspark_read_noalloc_flags")
+           "dspark_read_noalloc_flags", "dspark_selftest_philox_rate")
 
 _lib = None
 _lock = threading.Lock()
@@ -97,6 +97,8 @@ def load(build_if_missing: bool = True):
                                             i32, i32, i32, i32, i32, u64, vp, vp, vp, vp, vp, vp]
         L.dspark_read_device_flags.restype = ctypes.c_int
         L.dspark_read_device_flags.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.dspark_selftest_philox_rate.restype = ctypes.c_int
+        L.dspark_selftest_philox_rate.argtypes = [vp, sz, i32, ctypes.POINTER(ctypes.c_double), vp]
         L.dspark_read_noalloc_flags.restype = ctypes.c_int
         L.dspark_read_noalloc_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         _lib = L
@@ -456,6 +458,17 @@ def selftest_bounded_wait(limit_us=1000, stream=None) -> int:
     val = ctypes.c_uint32(0)
     _check(load().dspark_selftest_bounded_wait(int(limit_us), ctypes.byref(val), _stream(stream)))
     return int(val.value)
+
+
+def selftest_philox_rate(iters=2048, stream=None) -> float:
+    """Philox4x32-10 blocks per second of the draft's word code on this
+    device (dspark_selftest_philox_rate)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sink = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
+    val = ctypes.c_double(0.0)
+    _check(load().dspark_selftest_philox_rate(_ptr(sink), sink.numel(), int(iters), ctypes.byref(val),
+                                              _stream(stream)))
+    return float(val.value)
 
 
 def read_device_flags(workspace, stream=None) -> int:

@@ -367,6 +367,21 @@ dspark_status dspark_selftest_bounded_wait(unsigned int limit_us, uint32_t *resu
     return DSPARK_OK;
 }
 
+dspark_status dspark_selftest_philox_rate(void *workspace, size_t workspace_bytes, int iters, double *blocks_per_second,
+                                         void *stream) {
+    if (!blocks_per_second) return fail(DSPARK_ERR_INVALID_ARG, "blocks_per_second is NULL");
+    if (iters < 1 || iters > (1 << 20)) return fail(DSPARK_ERR_INVALID_ARG, "iters must be in [1, 2^20]");
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    dspark_status st = check_ws(workspace, workspace_bytes, philox_probe_sink_bytes(sms));
+    if (st != DSPARK_OK) return st;
+    e = run_philox_probe(workspace, sms, iters, blocks_per_second, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "Philox rate probe");
+    return DSPARK_OK;
+}
+
 dspark_status dspark_read_device_flags(const void *workspace, void *stream, uint32_t *flags) {
     if (!workspace || !flags) return fail(DSPARK_ERR_INVALID_ARG, "NULL workspace or flags");
     cudaStream_t s = static_cast<cudaStream_t>(stream);

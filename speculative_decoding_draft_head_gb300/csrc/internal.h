@@ -52,6 +52,8 @@ dspark_status verify_check_args(const void *target_logits, const void *base_logi
 
 // ------------------------------------------------------------- selftest ----
 cudaError_t run_bounded_wait_probe(unsigned int limit_us, uint32_t *result, cudaStream_t s);
+size_t philox_probe_sink_bytes(int sms);
+cudaError_t run_philox_probe(void *sink, int sms, int iters, double *blocks_per_s, cudaStream_t s);
 
 // ----------------------------------------------------------------- pack ----
 cudaError_t launch_pack_target(const void *src, const int32_t *verify_len, int B, int G, int V, size_t elem_bytes,

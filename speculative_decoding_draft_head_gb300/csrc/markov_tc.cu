@@ -79,8 +79,14 @@ constexpr int kMaxRegs = (16384 / (32 * ((kEpiWarps + 3 + 3) / 4))) / 8 * 8 > 16
                              ? 168
                              : (16384 / (32 * ((kEpiWarps + 3 + 3) / 4))) / 8 * 8;
 static_assert(kEpiWarps % 4 == 0 && kEpiPerQuad <= 8, "epilogue warps");
-constexpr int kWStages = 8;              // W ring: one 64-wide K atom of one tile per stage
-constexpr int kUStages = 2;              // = tile slots: tile t fills slot t % 2
+#ifndef DSPARK_W_STAGES
+#define DSPARK_W_STAGES 8
+#endif
+#ifndef DSPARK_U_STAGES
+#define DSPARK_U_STAGES 2
+#endif
+constexpr int kWStages = DSPARK_W_STAGES;  // W ring: one 64-wide K atom of one tile per stage
+constexpr int kUStages = DSPARK_U_STAGES;  // tile slots: tile t fills slot t % kUStages
 constexpr int kAccBufs = 3;
 constexpr uint32_t kTmemCols = 512;      // 3 x 128 accumulator columns + A, power-of-two allocation
 constexpr uint32_t kTmemA = kAccBufs * BN;  // A operand: columns 384.. (r/2 columns, <= 128)
@@ -262,9 +268,30 @@ __device__ __forceinline__ float screen_q2(float m, float K2) {
     return fminf(fast_exp2(m - K2), kQMax) * (1.f + 4e-7f * (fabsf(K2) + fabsf(m) + 64.f));
 }
 
+// The smallest Gumbel noise a word can give, g(2^-24) = -ln(24 ln 2), in log2
+// units and rounded down: every token's key is at least s2_v + kGminLog2, so a
+// lane's largest scaled logit alone bounds the row's best key from below.
+constexpr float kGminLog2 = -4.0563f;   // -2.81148 nats * log2(e) = -4.05615
+
 // A published lower bound (natural log) in log2 units, rounded down.
 __device__ __forceinline__ float lower_to_log2(float kn) {
     return (kn == -INFINITY) ? -INFINITY : fmaf(kn, kLog2e, -fabsf(kn) * 0x1p-21f);
+}
+
+// Raise the threshold K2 (log2 units) to a lower bound of the row's best key
+// and publish it in natural log, rounded down, to the CTA's per-row word and
+// the row-wide word's high half.
+__device__ __forceinline__ void publish_lower(float &K2, float lower, unsigned long long *best, uint32_t *cta_best) {
+    K2 = lower;
+    const float kn = fmaf(lower, kLn2, -fabsf(lower) * 0x1p-21f);
+    red_max_shared_u32(cta_best, key_to_ordered(kn));
+    red_max_u64(best, (unsigned long long)key_to_ordered(kn) << 32);
+}
+// The bound from a scaled logit s2 alone: its token's key is at least
+// s2 + kGminLog2 (less the rounding of s2 = z c2).
+__device__ __forceinline__ void raise_floor(float &K2, float s2, unsigned long long *best, uint32_t *cta_best) {
+    const float lower = s2 + kGminLog2 - 4e-7f * fabsf(s2);
+    if (lower > K2) publish_lower(K2, lower, best, cta_best);
 }
 
 // Draft epilogue for the 16 logits z of one row (T > 0, c2 = (c2, c2l) =
@@ -304,6 +331,7 @@ __device__ __forceinline__ void draft_tokens16(RowState &st, Top2 &tp, float &Q,
             for (int i = 0; i < 16; ++i)
                 if (full || i < n) zm = fmaxf(zm, z[i]);
             st.m = ceilf(zm * c2);  // c2 > 0: the rounded product is monotone in z
+            raise_floor(K2, zm * c2, best, cta_best);
             Q = screen_q2(st.m, K2);
         }
         if (full) {
@@ -322,6 +350,7 @@ __device__ __forceinline__ void draft_tokens16(RowState &st, Top2 &tp, float &Q,
             const float cm = ceilf(fmaxf(st.m, zm * c2));
             st.S = scale_pow2(st.S, st.m - cm);
             st.m = cm;
+            raise_floor(K2, zm * c2, best, cta_best);
             Q = screen_q2(st.m, K2);
 #pragma unroll
             for (int i = 0; i < 16; ++i) e[i] = (full || i < n) ? term_exp2(z[i], c2, c2l, st.m) : 0.f;
@@ -360,12 +389,8 @@ __device__ __forceinline__ void draft_tokens16(RowState &st, Top2 &tp, float &Q,
     if (tp.k1 > k1_before) {
         const float lower = tp.k1 - screen_tol(tp.k1);  // <= the exact key of token v1 (log2 units)
         if (lower > K2) {
-            K2 = lower;
+            publish_lower(K2, lower, best, cta_best);
             Q = screen_q2(st.m, K2);
-            // publish it in natural log, rounded down
-            const float kn = fmaf(lower, kLn2, -fabsf(lower) * 0x1p-21f);
-            red_max_shared_u32(cta_best, key_to_ordered(kn));
-            red_max_u64(best, (unsigned long long)key_to_ordered(kn) << 32);
         }
     }
 }
@@ -393,14 +418,13 @@ __device__ __forceinline__ unsigned long long draft_top2_word(const Top2 &tp, fl
 // it armed must land (bytes armed but never issued are counted as landed) and
 // the UMMAs it issued must finish; each wait is bounded again.  Out of line:
 // the path runs only after a timeout.
-static_assert(kUStages == 2, "drain_copies walks two tile slots");
-__device__ __noinline__ void drain_copies(uint32_t full0, uint32_t full1, int armed, uint32_t unissued,
-                                          volatile int *never) {
+// full0: the full_tile barrier of slot 0 (the slots' barriers are 8 bytes apart).
+__device__ __noinline__ void drain_copies(uint32_t full0, int armed, uint32_t unissued, volatile int *never) {
     if (armed <= 0) return;
     const int last = armed - 1;
-    if (unissued) mbar_complete_tx((last & 1) ? full1 : full0, unissued);
+    if (unissued) mbar_complete_tx(full0 + 8u * (uint32_t)(last % kUStages), unissued);
     for (int t = armed > kUStages ? armed - kUStages : 0; t < armed; ++t)
-        mbar_wait((t & 1) ? full1 : full0, (uint32_t)(t / kUStages) & 1u, never, kDrainLimit);
+        mbar_wait(full0 + 8u * (uint32_t)(t % kUStages), (uint32_t)(t / kUStages) & 1u, never, kDrainLimit);
 }
 __device__ __noinline__ void drain_ummas(uint32_t bar, volatile int *never) {
     umma_commit(bar);
@@ -633,7 +657,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             for (int tg = par; tg < total; tg += 2) {
                 const int pi = tg / ntiles;
                 const int a = tg % kAccBufs;
-                const int slot = tg % kUStages;  // = par
+                const int slot = tg % kUStages;
                 // the A operand of this position is in TMEM.  Every phase of
                 // a_ready is waited for in order, also those of positions with no
                 // tile of this warp (one tile per segment): a parity wait more
@@ -1034,7 +1058,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     __syncthreads();
     if (*abort) {  // the same for every thread after the barrier
         if (lane == 0) {
-            if (warp == kProducerWarp) drain_copies(full_tile(0), full_tile(1), armed, unissued, never);
+            if (warp == kProducerWarp) drain_copies(full_tile(0), armed, unissued, never);
             if (warp == kMmaWarp || warp == kMmaWarp + 1) drain_ummas(drain(warp - kMmaWarp), never);
         }
         __syncwarp();

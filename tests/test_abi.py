@@ -185,3 +185,7 @@ def test_selftest_and_noalloc_reject_on_the_host():
     assert lib.dspark_verify_noalloc(*args) == 1 and "aligned" in err()
     # the flag reader wants somewhere to put the word
     assert lib.dspark_read_noalloc_flags(None, None) == 1 and "NULL" in err()
+    # the Philox rate probe checks its arguments before any launch
+    rate = ctypes.c_double(0.0)
+    assert lib.dspark_selftest_philox_rate(p, 1 << 16, 16, None, None) == 1 and "NULL" in err()
+    assert lib.dspark_selftest_philox_rate(p, 1 << 16, 0, ctypes.byref(rate), None) == 1 and "iters" in err()

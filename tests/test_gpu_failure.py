@@ -40,3 +40,4 @@ def test_selftest_rejects_bad_limits():
         binding.selftest_bounded_wait(0)
     with pytest.raises(binding.DSparkError):
         binding.selftest_bounded_wait(2_000_000)
+
