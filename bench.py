@@ -401,6 +401,11 @@ def run_ours(args, w):
     _barrier(world)
     ms = t0.elapsed_time(t1) / args.steps
     clk = clocks.stop(region=(h0, h1)) if rank == 0 else None
+    # every call of the timed region must have completed cleanly: no invalid
+    # input and no bounded wait that ran out
+    flags = dict(draft=binding.read_device_flags(ws_d), verify=binding.read_device_flags(ws_v))
+    if any(flags.values()):
+        raise RuntimeError("device flags raised in the timed region: %s" % flags)
     ms_max = _max_over_ranks(ms, world)
     total_positions = _sum_over_ranks(positions, world)
     value = total_positions / (ms_max / 1000.0)
@@ -595,6 +600,7 @@ def run_ours(args, w):
                         "logits only for the scheduled rows 0..L_b of each request (%d of %d rows), "
                         "gathered on the device by dspark_pack_target" % (target_rows, B * (G + 1))),
         gpu_launches=args.steps * (launches_draft + (1 if w.scheduler else 0) + 4),
+        device_flags=flags,
         clocks=clk,
     )
     if not args.no_cpu_baseline and world == 1:

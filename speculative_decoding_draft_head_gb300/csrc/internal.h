@@ -122,6 +122,7 @@ cudaError_t launch_draft_tensor_rows(const DraftArgs &a, const DraftPlan &p, int
 
 // tensor-core kernel geometry (bf16): 128-request row blocks x vocabulary segments
 int tc_row_blocks(int B);
+int tc_row_replication(int B);
 int tc_segments(int B, int V);
 size_t tc_residual_state_bytes();
 

@@ -133,6 +133,7 @@ struct TcParams {
     int B, G, V, r;
     int j, j_end;               // draft: block positions j .. j_end - 1 in this launch
     int nseg;
+    int rep;                    // row replication for small batches: TMEM row i holds request m0 + i % (128 / rep)
     int pass;                   // final draw: odd passes walk the segment backwards
     PhiloxRoundKeys keys;
     RowState *part;             // draft: [G][B][nseg] softmax / key partials
@@ -509,7 +510,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         }
         for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), 32);  // one arrival per 16-column sub-slice of each quadrant
+            mbar_init(tempty(a), 32 / p.rep);  // one arrival per 16-column sub-slice each quadrant processes
         }
         mbar_init(a_ready, kEpiWarps);
         mbar_init(drain(0), 1);
@@ -530,8 +531,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     // the final draw is launched as a dependent of the decide pass: its set-up
     // above overlaps that pass, whose outputs are read from here on
     if (kFinal) griddep_wait();
+    // Small batches (B <= 32 or 64) replicate their requests over the 128
+    // TMEM rows, 4 or 2 times, and each replica (a set of lane quadrants)
+    // processes its own share of every tile's columns: the epilogue then runs
+    // on every SM sub-partition (a warp reads only its own lane quadrant).
+    const int rows_q = BM / p.rep;  // distinct requests in the tile
     if (threadIdx.x < BM) {
-        const int b = m0 + threadIdx.x;
+        const int b = m0 + (int)threadIdx.x % rows_q;
         int prev = -1, code = 0;
         float c2 = 0.f, c2l = 0.f;
         uint32_t id = 0;
@@ -624,10 +630,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     unissued -= kWChunk;
                 }
                 if (ok && !kFinal) {
-                    tma_load_3d(sbase + kOffU + slot * kUBytes, &map_u, full_tile(slot), v0, jj, m0, pol_u);
-                    if (two)
-                        tma_load_3d(sbase + kOffU + slot * kUBytes + kUHalf, &map_u, full_tile(slot), v0 + 64, jj, m0,
-                                    pol_u);
+                    // one box of rows_q requests per replica (128-byte rows: the
+                    // swizzle phase of a replica at a multiple of 8 rows is unchanged)
+                    for (int k = 0; k < p.rep; ++k) {
+                        const uint32_t dst = sbase + kOffU + slot * kUBytes + (uint32_t)(k * rows_q * 128);
+                        tma_load_3d(dst, &map_u, full_tile(slot), v0, jj, m0, pol_u);
+                        if (two) tma_load_3d(dst + kUHalf, &map_u, full_tile(slot), v0 + 64, jj, m0, pol_u);
+                    }
                     unissued -= u_bytes;
                 }
             }
@@ -707,7 +716,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         // ------------------------------------------------------ epilogue ----
         const int q = warp & 3, slice = warp >> 2;  // quadrant, index within the quadrant's warps
         const int row = q * 32 + lane;
-        const int b = m0 + row;
+        const int rq = row % rows_q;  // the request slot of this row (replicas share it)
+        const int b = m0 + rq;
+        // this quadrant's share of each tile's 8 column blocks: spt = 8 / rep
+        // consecutive blocks from cb0 (shifts: rep is 1 or 2)
+        const int spt_sh = (p.rep == 2) ? 2 : 3;
+        const int spt = 1 << spt_sh;
+        const int cb0 = (p.rep == 2) ? (q >> 1) * 4 : 0;
         const float c2 = row_c2[row];
         const float c2l = row_c2l[row];
         const float Trow = row_T[row];
@@ -764,6 +779,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 if (lane == 0) mbar_arrive(a_ready);
             }
             const bool active = kFinal ? (kind != 0) : (prev >= 0);
+            // only rows that draw need words: a warp whose rows are all padding,
+            // inactive or greedy skips the Philox blocks (warp-uniform)
+            const bool need_words = __any_sync(0xffffffffu, active && c2 > 0.f);
             const uint32_t pos = kFinal ? (uint32_t)fpos : (uint32_t)jj;
             // the parts of Philox fixed by this request and position
             const PhiloxRow prow = philox_row(rid, pos, stream, p.keys);
@@ -799,10 +817,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             // column block si % 8 of tile si / 8; the quadrant's warps take every
             // kEpiPerQuad-th one (so no warp skips a tile)
             const bool rev_pos = (((kFinal ? p.pass : p.j + pi)) & 1) != 0;
-            const int nsub = ntiles * 8;
+            const int nsub = ntiles * spt;
             auto sub_col = [&](int si) {
-                const int t = si >> 3;
-                return vb + (rev_pos ? (ntiles - 1 - t) : t) * BN + (si & 7) * 16;
+                const int t = si >> spt_sh;
+                return vb + (rev_pos ? (ntiles - 1 - t) : t) * BN + (cb0 + (si & (spt - 1))) * 16;
             };
             // final draw: this thread's target values, one sub-slice ahead (its
             // base values are read only for the groups that pass the bound test)
@@ -815,7 +833,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
             int waited = -1;  // the last tile whose accumulator this warp waited for
 #pragma unroll 1
             for (int si = slice; si < nsub && ok; si += kEpiPerQuad) {
-                const int t = si >> 3;
+                const int t = si >> spt_sh;
                 const int tg = pi * ntiles + t;
                 const int a = tg % kAccBufs;
                 const uint32_t aph = (uint32_t)(tg / kAccBufs) & 1u;
@@ -825,8 +843,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     uint4 w[4];
                     uint32_t acc[16];
                     const int vw = sub_col(si);
-                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + (si & 7) * 16;
-                    auto draw_words = [&]() { philox_folded4((uint32_t)vw >> 2, prow, p.keys, w); };
+                    const uint32_t taddr =
+                        tmem_base + ((uint32_t)(q * 32) << 16) + a * BN + (uint32_t)(cb0 + (si & (spt - 1))) * 16;
+                    auto draw_words = [&]() {
+                        if (need_words) {
+                            philox_folded4((uint32_t)vw >> 2, prow, p.keys, w);
+                        } else {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) w[g] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    };
                     if (t != waited) {
                         // a new tile: draw the words while its UMMAs may still run
                         draw_words();
@@ -881,13 +907,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             // current) or the row-wide word's high half (global, loaded
                             // up to four sub-slices earlier)
                             const float kg = lower_to_log2(
-                                ordered_to_key(max(kg_next, *(volatile uint32_t *)(row_kbest + row))));
+                                ordered_to_key(max(kg_next, *(volatile uint32_t *)(row_kbest + rq))));
                             if (kg > K2) {
                                 K2 = kg;
                                 Q = screen_q2(st.m, K2);
                             }
                         }
-                        draft_tokens16(st, tp, Q, K2, z, c2, c2l, n, v, on, best, row_kbest + row, w);
+                        draft_tokens16(st, tp, Q, K2, z, c2, c2l, n, v, on, best, row_kbest + rq, w);
                         // reload the row-wide word after this warp's first sub-slice of
                         // the position (by then every CTA has published its rows' first
                         // groups, so the threshold is tight from the second sub-slice
@@ -1026,16 +1052,21 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 ms[row * kEpiPerQuad + slice] = rs;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-            if (slice == 0 && b < p.B) {
+            // one thread per request merges its row's slices and replicas
+            if (slice == 0 && row < rows_q && b < p.B) {
                 if (!kFinal) {
                     const RowState *ms = reinterpret_cast<const RowState *>(smem + kOffMerge);
-                    for (int s2 = 1; s2 < kEpiPerQuad; ++s2) row_state_merge(st, ms[row * kEpiPerQuad + s2]);
+                    for (int k = 0; k < p.rep; ++k)
+                        for (int s2 = (k == 0 ? 1 : 0); s2 < kEpiPerQuad; ++s2)
+                            row_state_merge(st, ms[(row + k * rows_q) * kEpiPerQuad + s2]);
                     p.part[((size_t)jj * p.B + b) * p.nseg + seg] = st;
                     if (st.best) red_max_u64(best, st.best);
-                    row_kbest[row] = 0u;  // the next position's (every warp is past its last read)
+                    row_kbest[rq] = 0u;  // the next position's (every warp is past its last read)
                 } else if (active) {
                     const ResidualState *ms = reinterpret_cast<const ResidualState *>(smem + kOffMerge);
-                    for (int s2 = 1; s2 < kEpiPerQuad; ++s2) rs.best = max(rs.best, ms[row * kEpiPerQuad + s2].best);
+                    for (int k = 0; k < p.rep; ++k)
+                        for (int s2 = (k == 0 ? 1 : 0); s2 < kEpiPerQuad; ++s2)
+                            rs.best = max(rs.best, ms[(row + k * rows_q) * kEpiPerQuad + s2].best);
                     p.rpart[(size_t)b * p.nseg + seg] = rs;
                 }
             }
@@ -1100,13 +1131,14 @@ cudaError_t make_w_map(CUtensorMap *m, const void *w_out, int V, int r) {
 }
 
 // Base logits [B][G][V] as a 3-D tensor (V, G, B), boxes of 64 columns x
-// 128 requests in the 128-byte swizzled layout (two boxes per tile).
-cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, int box_cols = 64) {
+// 128 requests (box_rows: 128 / the row replication) in the 128-byte swizzled
+// layout (two boxes per tile and replica).
+cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, int box_cols = 64, int box_rows = BM) {
     auto fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)G, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)G * V * 2};
-    cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)BM};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     const bool tile = (box_cols == 64);
     CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -1139,6 +1171,14 @@ PhiloxRoundKeys round_keys(uint64_t seed) {
 }  // namespace
 
 int tc_row_blocks(int B) { return (B + BM - 1) / BM; }
+
+// Row replication of the tensor-core kernels: a batch of at most 64 requests
+// fills the 128 accumulator rows twice.  At most 8 / kEpiPerQuad replicas:
+// each epilogue warp must take part in every tile (its quadrant's share of
+// the tile has at least kEpiPerQuad sub-slices), or it would skip phases of
+// the accumulators' mbarriers and a later parity wait could alias.
+int tc_row_replication(int B) { return B <= 64 ? 2 : 1; }
+static_assert(kEpiPerQuad <= 4, "two replicas give each warp of a quadrant a sub-slice of every tile");
 
 int tc_segments(int B, int V) {
     const int mb = tc_row_blocks(B);
@@ -1185,7 +1225,8 @@ namespace {
 cudaError_t draft_setup(const DraftArgs &a, const DraftPlan &pl, CUtensorMap *mw, CUtensorMap *mu, TcParams &p) {
     cudaError_t e = make_w_map(mw, a.w_out, a.V, a.r);
     if (e != cudaSuccess) return e;
-    if ((e = make_u_map(mu, a.base, a.B, a.G, a.V, 64)) != cudaSuccess) return e;
+    const int rep = tc_row_replication(a.B);
+    if ((e = make_u_map(mu, a.base, a.B, a.G, a.V, 64, BM / rep)) != cudaSuccess) return e;
     if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
     p = TcParams{};
     p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
@@ -1199,6 +1240,7 @@ cudaError_t draft_setup(const DraftArgs &a, const DraftPlan &pl, CUtensorMap *mw
     p.V = a.V;
     p.r = a.r;
     p.nseg = pl.nsplit;
+    p.rep = rep;
     p.keys = round_keys(a.seed);
     p.part = reinterpret_cast<RowState *>(a.ws + pl.partial_offset);
     p.best = reinterpret_cast<unsigned long long *>(a.ws + pl.best_offset);
@@ -1282,6 +1324,7 @@ cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     p.V = a.V;
     p.r = a.r;
     p.j = 0;
+    p.rep = tc_row_replication(a.B);
     p.pass = a.pass;
     p.nseg = a.nseg;
     p.keys = round_keys(a.seed);

@@ -73,18 +73,26 @@ def to_host(d):
 
 
 def gpu_round(inp, w, seed, scheduler=None, store_logits=False):
-    """draft -> schedule (if the workload uses it) -> verify on the GPU."""
+    """draft -> schedule (if the workload uses it) -> verify on the GPU; the
+    device flag words of the calls must stay clear (no invalid input, no
+    bounded wait that ran out)."""
     scheduler = w.scheduler if scheduler is None else scheduler
+    dev = inp["base"].device
+    ws_d = binding.default_workspace(binding.WS_DRAFT, w.B, w.G, w.V, w.r, dev)
+    ws_v = binding.default_workspace(binding.WS_VERIFY, w.B, w.G, w.V, w.r, dev)
     d = binding.draft_sample(inp["base"], inp["e_in"], inp["w_out"], inp["anchor"],
-                             inp["temperature"], inp["request_id"], seed, store_logits=store_logits)
+                             inp["temperature"], inp["request_id"], seed, store_logits=store_logits,
+                             workspace=ws_d)
+    assert binding.read_device_flags(ws_d) == 0, "draft flags %d" % binding.read_device_flags(ws_d)
     sch = None
     vl = None
     if scheduler:
         sch = binding.schedule_prefix(inp["conf_logits"], inp["pos_temp"], inp["sps"], w.L_min, w.G)
         vl = sch["verify_len"]
     v = binding.verify(inp["target"], inp["base"], inp["e_in"], inp["w_out"], inp["anchor"], d, vl,
-                       inp["temperature"], inp["request_id"], seed)
+                       inp["temperature"], inp["request_id"], seed, workspace=ws_v)
     torch.cuda.synchronize()
+    assert binding.read_device_flags(ws_v) == 0, "verify flags %d" % binding.read_device_flags(ws_v)
     return dict(draft=to_host(d), sched=None if sch is None else to_host(sch), verify=to_host(v))
 
 
