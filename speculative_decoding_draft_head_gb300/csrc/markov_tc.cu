@@ -98,6 +98,16 @@ constexpr uint32_t kOffU = kOffW + kWStages * kWChunk;
 // 16 x 16 bf16 identity in the B-operand layout: eight N = 16 UMMAs per tile
 // add the base-logit tile (as an A operand) onto the bias accumulator
 constexpr uint32_t kOffI = kOffU + kUStages * kUBytes;
+// The final draw's target values: each epilogue thread owns kTargetAhead
+// slots of 32 bytes (16 bf16) in the base-logit ring, which the final draw
+// does not use; the low and high 16-byte halves lie in two arrays, so a warp's
+// reads of one half are contiguous.
+constexpr int kTargetAhead = 4;
+constexpr uint32_t kTargetHalf = kTargetAhead * kEpiWarps * 32 * 16;
+static_assert(2 * kTargetHalf <= kUStages * kUBytes, "target slots fit in the base-logit ring");
+__device__ __forceinline__ uint32_t target_slot(uint32_t sbase, int k, int tid) {
+    return sbase + kOffU + (uint32_t)(((k % kTargetAhead) * (kEpiWarps * 32) + tid) * 16);
+}
 constexpr uint32_t kIBytes = 16 * 128;
 // per-row merge of the four column slices (the W ring keeps streaming the
 // next block position meanwhile)
@@ -239,6 +249,43 @@ __device__ __forceinline__ uint32_t word_at(const uint4 (&w)[4], int i) {
     }
 }
 
+// Element i (a run-time index) of 16 values held in registers: a tree of
+// selects on the bits of i, so the values stay in registers.
+__device__ __forceinline__ float select16(const float (&z)[16], int i) {
+    float a[8], b[4], c[2];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = (i & 8) ? z[k + 8] : z[k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) b[k] = (i & 4) ? a[k + 4] : a[k];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) c[k] = (i & 2) ? b[k + 2] : b[k];
+    return (i & 1) ? c[1] : c[0];
+}
+// Element i (a run-time index) of 16 raw 32-bit values.
+__device__ __forceinline__ uint32_t select16(const uint32_t (&z)[16], int i) {
+    uint32_t a[8], b[4], c[2];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = (i & 8) ? z[k + 8] : z[k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) b[k] = (i & 4) ? a[k + 4] : a[k];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) c[k] = (i & 2) ? b[k + 2] : b[k];
+    return (i & 1) ? c[1] : c[0];
+}
+// Element i (a run-time index) of 16 packed bf16.
+__device__ __forceinline__ float select16_bf16(const uint4 &lo, const uint4 &hi, int i) {
+    const uint4 a = (i & 8) ? hi : lo;
+    const uint32_t b0 = (i & 4) ? a.z : a.x, b1 = (i & 4) ? a.w : a.y;
+    const uint32_t wd = (i & 2) ? b1 : b0;
+    return (i & 1) ? bf16_hi(wd) : bf16_lo(wd);
+}
+// Word i (a run-time index) of four Philox blocks.
+__device__ __forceinline__ uint32_t select16(const uint4 (&w)[4], int i) {
+    const uint4 a = (i & 8) ? ((i & 4) ? w[3] : w[2]) : ((i & 4) ? w[1] : w[0]);
+    const uint32_t b0 = (i & 2) ? a.z : a.x, b1 = (i & 2) ? a.w : a.y;
+    return (i & 1) ? b1 : b0;
+}
+
 // The largest of the 16 words (the smallest 1 - u of the sub-slice).
 __device__ __forceinline__ uint32_t max_word16(const uint4 (&w)[4]) {
     uint32_t a = max(max(w[0].x, w[0].y), max(w[0].z, w[0].w));
@@ -361,29 +408,37 @@ __device__ __forceinline__ void draft_tokens16(RowState &st, Top2 &tp, float &Q,
     }
     const bool grp = on && sum > 0.f && one_minus_uniform_plus_one(max_word16(w)) < fmaf(sum, Q, 1.f);
     if (!(__any_sync(0xffffffffu, grp) && grp)) return;
-    // rare: the tokens one by one (e_v = 0 for tokens past n fails the test)
+    // rare: the tokens one by one (e_v = 0 for tokens past n fails the test).
+    // The per-token tests give a mask; only its tokens, in increasing order,
+    // take a key (a lane has about four the first time, one or two later, and
+    // the warp runs its lanes' largest count instead of all 16).
     const float k1_before = tp.k1;
+    uint32_t mask = 0u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t wi = word_at(w, i);
-        if (one_minus_uniform_plus_one(wi) < fmaf(e[i], Q, 1.f)) {
-            const float k = fmaf(z[i], c2l, fmaf(z[i], c2, -log2_neg_log_uniform_fast(wi)));
-            if (k > tp.k2) {
-                if (k > tp.k1) {
-                    tp.k2 = tp.k1;
-                    tp.z2 = tp.z1;
-                    tp.w2 = tp.w1;
-                    tp.v2 = tp.v1;
-                    tp.k1 = k;
-                    tp.z1 = z[i];
-                    tp.w1 = wi;
-                    tp.v1 = v + i;
-                } else {
-                    tp.k2 = k;
-                    tp.z2 = z[i];
-                    tp.w2 = wi;
-                    tp.v2 = v + i;
-                }
+    for (int i = 0; i < 16; ++i)
+        if (one_minus_uniform_plus_one(word_at(w, i)) < fmaf(e[i], Q, 1.f)) mask |= 1u << i;
+#pragma unroll 1
+    while (mask) {
+        const int i = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const float zi = select16(z, i);
+        const uint32_t wi = select16(w, i);
+        const float k = fmaf(zi, c2l, fmaf(zi, c2, -log2_neg_log_uniform_fast(wi)));
+        if (k > tp.k2) {
+            if (k > tp.k1) {
+                tp.k2 = tp.k1;
+                tp.z2 = tp.z1;
+                tp.w2 = tp.w1;
+                tp.v2 = tp.v1;
+                tp.k1 = k;
+                tp.z1 = zi;
+                tp.w1 = wi;
+                tp.v1 = v + i;
+            } else {
+                tp.k2 = k;
+                tp.z2 = zi;
+                tp.w2 = wi;
+                tp.v2 = v + i;
             }
         }
     }
@@ -413,6 +468,32 @@ __device__ __forceinline__ unsigned long long draft_top2_word(const Top2 &tp, fl
         }
     }
     return wb;
+}
+
+// The exact key word of a final-draw contender: token tok with target logit
+// tb, draft logit zb and word wb; 0 when a residual row gives it no mass
+// (p <= q).  key_hi receives the float-float key's high part.  Out of line:
+// it runs for a few tokens per row, and inlined its registers would spill in
+// the sub-slice loop.
+__device__ __noinline__ unsigned long long final_key_word(float tb, float zb, uint32_t wb, int tok, bool bonus,
+                                                          float T, float rT, FF lse_t, float lse_q,
+                                                          float *key_hi) {
+    FF key;
+    if (bonus) {
+        key = div_ff(tb, T, rT);  // t / T: the bonus key before its noise
+    } else {
+        // ln r = ln p + ln(1 - q / p), ln q - ln p formed in float-float from
+        // the logits and the two lse
+        const FF lp = ff_add(div_ff(tb, T, rT), ff_neg(lse_t));
+        const FF dl = ff_add(ff_add(div_ff(zb, T, rT), FF{-lse_q, 0.f}), ff_neg(lp));
+        const float d = dl.hi + dl.lo;
+        if (!(d < 0.f)) return 0ull;  // p <= q: no residual mass
+        const float l1m = (d > -0.6931472f) ? logf(-expm1f(d)) : log1pf(-expf(d));
+        key = ff_add(lp, FF{l1m, 0.f});
+    }
+    key = ff_add(key, gumbel_ff(wb));
+    *key_hi = key.hi;
+    return key_word(key, tok);
 }
 
 // A timed-out CTA, before its shared memory and TMEM are given up: the copies
@@ -822,17 +903,31 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                 const int t = si >> spt_sh;
                 return vb + (rev_pos ? (ntiles - 1 - t) : t) * BN + (cb0 + (si & (spt - 1))) * 16;
             };
-            // final draw: this thread's target values, one sub-slice ahead (its
-            // base values are read only for the groups that pass the bound test)
-            uint4 nt_lo = make_uint4(0, 0, 0, 0), nt_hi = nt_lo;
-            if (kFinal && active && slice < nsub) {
-                const int v = sub_col(slice);
-                const int n = min(16, ve - v);
-                if (n > 0) load16_bf16(trow + v, n, nt_lo, nt_hi);
+            // final draw: this thread's target values arrive by cp.async into
+            // its own slots of the (otherwise unused) base-logit ring,
+            // kTargetAhead - 1 sub-slices ahead (its base values are read only
+            // for the groups that pass the bound test).  One commit group per
+            // sub-slice, empty where nothing is copied.
+            auto prefetch_target = [&](int k) {
+                const int sn = slice + k * kEpiPerQuad;
+                if (active && sn < nsub) {
+                    const int vn = sub_col(sn);
+                    const int nn = min(16, ve - vn);
+                    if (nn > 0) {
+                        const uint32_t dst = target_slot(sbase, k, threadIdx.x);
+                        cp_async_16(dst, trow + vn, 2 * min(nn, 8));
+                        cp_async_16(dst + kTargetHalf, nn > 8 ? trow + vn + 8 : trow + vn, 2 * max(nn - 8, 0));
+                    }
+                }
+                cp_async_commit();
+            };
+            if (kFinal) {
+#pragma unroll
+                for (int k = 0; k < kTargetAhead - 1; ++k) prefetch_target(k);
             }
             int waited = -1;  // the last tile whose accumulator this warp waited for
 #pragma unroll 1
-            for (int si = slice; si < nsub && ok; si += kEpiPerQuad) {
+            for (int si = slice, k = 0; si < nsub && ok; si += kEpiPerQuad, ++k) {
                 const int t = si >> spt_sh;
                 const int tg = pi * ntiles + t;
                 const int a = tg % kAccBufs;
@@ -925,18 +1020,19 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         if (on && (si < kEpiPerQuad || ((si / kEpiPerQuad) & 3) == 3))
                             kg_next = load_relaxed(reinterpret_cast<const uint32_t *>(best) + 1);
                     } else {
-                        // take this sub-slice's prefetched target values (kept packed as
-                        // bf16 pairs), then prefetch the next one's (before any skip: the
-                        // skipped sub-slice may come first when walking the segment
-                        // backwards)
-                        const uint4 ct_lo = nt_lo, ct_hi = nt_hi;
-                        {
-                            const int sn = si + kEpiPerQuad;  // this warp's next sub-slice
-                            const int vn = (sn < nsub) ? sub_col(sn) : ve;
-                            const int nn = min(16, ve - vn);
-                            if (active && sn < nsub && nn > 0) load16_bf16(trow + vn, nn, nt_lo, nt_hi);
-                        }
+                        // start the copy kTargetAhead - 1 sub-slices ahead (before any
+                        // skip: the skipped sub-slice may come first when walking the
+                        // segment backwards; its slot was read last sub-slice), then take
+                        // this sub-slice's target values (packed bf16 pairs)
+                        prefetch_target(k + kTargetAhead - 1);
                         if (n <= 0) continue;  // warp-uniform
+                        cp_async_wait<kTargetAhead - 1>();
+                        uint4 ct_lo, ct_hi;
+                        {
+                            const uint32_t src = target_slot(sbase, k, threadIdx.x);
+                            ct_lo = ld_shared_v4(src);
+                            ct_hi = ld_shared_v4(src + kTargetHalf);
+                        }
                         // Per-token Gumbel-max (stream 2 residual, 3 bonus).  A residual
                         // row weighs token v by r_v = p_v - q_v where positive, with p
                         // and q normalised (reference 0); a bonus row by
@@ -968,76 +1064,78 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         // the draft logits z = base + bias of this sub-slice (residual rows)
                         uint4 u_lo = make_uint4(0, 0, 0, 0), u_hi = u_lo;
                         if (maybe && kind == 1) load16_bf16(urow + v, n, u_lo, u_hi);
-                        float z[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) z[i] = bf16_at(u_lo, u_hi, i) + __uint_as_float(acc[i]);
                         // per token: screen with an upper bound of r_v under the
-                        // approximate exponentials; a survivor's fp32 key (log2 units,
-                        // from that bound, so never below the true key by more than
-                        // rounding) goes to k2[]
-                        float k2[16];
+                        // approximate exponentials; the survivors form a mask
+                        uint32_t mask = 0u;
+                        if (maybe) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float kk = -INFINITY;
-                            if (maybe && i < n) {
-                                const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -tref));
-                                const float qv = fast_exp2(fmaf(z[i], c2, -lse_q2));
-                                const float ub = (pv - qv) + 4e-7f * (pv + qv);
-                                const uint32_t wi = word_at(w, i);
-                                if (ub > 0.f && one_minus_uniform_plus_one(wi) < fmaf(ub, Qg, 1.f))
-                                    kk = off + fast_log2(ub) - fast_log2(neg_log_uniform(wi));
+                            for (int i = 0; i < 16; ++i) {
+                                if (i < n) {
+                                    const float zi = bf16_at(u_lo, u_hi, i) + __uint_as_float(acc[i]);
+                                    const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -tref));
+                                    const float qv = fast_exp2(fmaf(zi, c2, -lse_q2));
+                                    const float ub = (pv - qv) + 4e-7f * (pv + qv);
+                                    if (ub > 0.f && one_minus_uniform_plus_one(word_at(w, i)) < fmaf(ub, Qg, 1.f))
+                                        mask |= 1u << i;
+                                }
                             }
-                            k2[i] = kk;
                         }
-                        // contenders, best first: the float-float key decides
+                        // a survivor's fp32 key (log2 units, from the bound, so never
+                        // below the true key by more than rounding)
+                        auto fp32_key = [&](int i, float &tb, float &zb, uint32_t &wb) {
+                            tb = select16_bf16(ct_lo, ct_hi, i);
+                            zb = select16_bf16(u_lo, u_hi, i) + __uint_as_float(select16(acc, i));
+                            wb = select16(w, i);
+                            const float pv = fast_exp2(fmaf(tb, c2, -tref));
+                            const float qv = fast_exp2(fmaf(zb, c2, -lse_q2));
+                            const float ub = (pv - qv) + 4e-7f * (pv + qv);
+                            return off + fast_log2(ub) - fast_log2(neg_log_uniform(wb));
+                        };
+                        // the survivor with the largest fp32 key goes first, so that its
+                        // float-float key raises the row's best before the others are
+                        // tested against it (the largest key word wins, whatever the order)
+                        int first = -1;
+                        if (mask & (mask - 1u)) {
+                            float kb = -INFINITY;
 #pragma unroll 1
-                        while (true) {
-                            float kb2 = -INFINITY;
-                            int ib = -1;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (k2[i] > kb2) {
-                                    kb2 = k2[i];
-                                    ib = i;
+                            for (uint32_t m2 = mask; m2; m2 &= m2 - 1u) {
+                                const int i = __ffs(m2) - 1;
+                                float tb, zb;
+                                uint32_t wb;
+                                const float kk = fp32_key(i, tb, zb, wb);
+                                if (kk > kb) {
+                                    kb = kk;
+                                    first = i;
                                 }
-                            const float K2 = kbest_r * kLog2e;
-                            if (ib < 0 || !(kb2 > K2 - key_tol2(kb2, K2))) break;
-                            float zb = 0.f, tb = 0.f;
-                            uint32_t wb = 0u;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (i == ib) {
-                                    zb = z[i];
-                                    tb = bf16_at(ct_lo, ct_hi, i);
-                                    wb = word_at(w, i);
-                                    k2[i] = -INFINITY;
-                                }
-                            FF key;
-                            if (bonus) {
-                                key = div_ff(tb, Trow, rT);  // t / T: the bonus key before its noise
-                            } else {
-                                // ln r = ln p + ln(1 - q / p), ln q - ln p formed in
-                                // float-float from the logits and the two lse
-                                const FF lp = ff_add(div_ff(tb, Trow, rT), ff_neg(lse_t));
-                                const FF dl = ff_add(ff_add(div_ff(zb, Trow, rT), FF{-lse_q, 0.f}), ff_neg(lp));
-                                const float d = dl.hi + dl.lo;
-                                if (!(d < 0.f)) continue;  // p <= q: no residual mass
-                                const float l1m = (d > -0.6931472f) ? logf(-expm1f(d)) : log1pf(-expf(d));
-                                key = ff_add(lp, FF{l1m, 0.f});
                             }
-                            key = ff_add(key, gumbel_ff(wb));
-                            const unsigned long long word = key_word(key, v + ib);
+                        }
+#pragma unroll 1
+                        while (mask) {
+                            const int i = (first >= 0) ? first : __ffs(mask) - 1;
+                            first = -1;
+                            mask &= ~(1u << i);
+                            float tb, zb;
+                            uint32_t wb;
+                            const float kk = fp32_key(i, tb, zb, wb);
+                            const float K2 = kbest_r * kLog2e;
+                            if (!(kk > K2 - key_tol2(kk, K2))) continue;
+                            float key_hi;
+                            const unsigned long long word =
+                                final_key_word(tb, zb, wb, v + i, bonus, Trow, rT, lse_t, lse_q, &key_hi);
                             if (word > rs.best) {
                                 rs.best = word;
-                                if (key.hi >= kbest_r) {
-                                    kbest_r = key.hi;
-                                    red_max_u32(res_best, key_to_ordered(key.hi));
+                                if (key_hi >= kbest_r) {
+                                    kbest_r = key_hi;
+                                    red_max_u32(res_best, key_to_ordered(key_hi));
                                 }
                             }
                         }
                     }
                 }
             }
+            // no copy may still be landing in the target slots (a timed-out
+            // warp leaves the loop early)
+            if (kFinal) cp_async_wait_all();
             // merge the four column slices of each row
             if (!kFinal) {
                 if (c2 > 0.f) {  // sampled rows: the exact key word of the lane's draw
