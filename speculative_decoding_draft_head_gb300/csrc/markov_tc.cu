@@ -9,46 +9,51 @@
 // TMEM epilogue so that each logit is produced and consumed on chip.
 //
 // Two uses share the kernel:
-//  - draft: rows = 128 requests at block position j; base-logit tiles come
-//    by TMA; the kernel writes per-(request, segment) softmax/argmax partials
-//    (draft_finalize merges them and writes x_j, which the next position's
-//    launch gathers);
+//  - draft: rows = 128 requests (a batch of at most 64 is replicated twice
+//    over the 128 rows, each replica taking half of every tile's columns);
+//    base-logit tiles come by TMA; one cooperative launch walks all block
+//    positions, meeting the other CTAs of its row block at a bounded grid
+//    barrier between positions, where each row's best (key, token) word gives
+//    x_j for the next position's A operand.  Per-(request, segment) softmax
+//    partials go to the workspace for draft_finalize (lse, log q);
 //  - final draw of verification ("Les mathematiques derriere l'acceleration",
 //    section "La garantie de l'echantillonnage par rejet", and "DeepSeek发布
 //    DSpark", section "DSpark 是什么？"): each row is a request that either
 //    rejected at position d (draw from max(0, p_d - q_d), q rebuilt from base
 //    logits + Markov bias) or accepted its whole block (bonus draw from p_L);
-//    other rows idle.  Base and target rows are read directly, one tile ahead.
+//    other rows idle.  Target rows stream by cp.async into per-thread slots
+//    three sub-slices ahead; base rows are read only where a group passes the
+//    bound test.
 //
-// CTA layout (one CTA per SM, 608 threads, ~199 KB shared memory):
-//   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant of
-//               rows) and columns 32*(w/4).. of each 128-column tile, as two
-//               16-column sub-slices;
-//   warp 16     TMA producer: W_out chunks (128 tokens x 64 of r, 128-byte
+// CTA layout (one CTA per SM, 480 threads, ~200 KB shared memory):
+//   warps 0-11  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant of
+//               rows); the 8 sixteen-column sub-slices of each 128-column
+//               tile are dealt round-robin to the quadrant's three warps;
+//   warp 12     TMA producer: W_out chunks (128 tokens x 64 of r, 128-byte
 //               swizzle, L2 evict-last) and base-logit tiles (two boxes of
 //               128 requests x 64 tokens, evict-first);
-//   warps 17-18 UMMA issuers for even / odd tiles (M=128, N=128, K=16 steps);
-//               warp 17 also allocates TMEM.
+//   warps 13-14 UMMA issuers for even / odd tiles (M=128, N=128, K=16 steps);
+//               warp 13 also allocates TMEM.
 // The A operand (the 128 gathered E_in rows, 128 x r bf16) is written once per
-// CTA into TMEM (columns 384..) and read from there by the bias UMMAs, which
-// leaves shared memory to the streams.  Rings: 8 W chunks (two tiles), 2 base
-// tiles (tile slots), 3 TMEM accumulators of 128 columns.  Tiles are as wide as a single
-// UMMA allows at this shape because every tcgen05.mma costs a roughly fixed
-// issue time whatever its N: wide tiles cut the instructions per token.  In
-// the draft the base-logit tile joins the contraction: after the r/16 bias
-// steps, eight N=16 UMMAs multiply 16-token slices of the tile (128 requests
-// x 128 tokens, already in the K-major A layout as TMA writes it) by a 16 x 16
-// identity into the matching accumulator columns, so TMEM holds z = U + bias
-// and the epilogue reads nothing from shared memory.  (U * 1 and U * 0 are
-// exact; base logits must be finite, since inf * 0 would poison the other
-// columns of its 16-wide step.)  Every wait is bounded; a timeout sets the
-// timeout bit of the flag word and the CTA unwinds.
+// position into TMEM (columns 384..) and read from there by the bias UMMAs,
+// which leaves shared memory to the streams.  Rings: 8 W chunks (two tiles),
+// 2 base tiles (tile slots), 3 TMEM accumulators of 128 columns.  Tiles are as
+// wide as a single UMMA allows at this shape because every tcgen05.mma costs a
+// roughly fixed issue time whatever its N: wide tiles cut the instructions per
+// token.  In the draft the base-logit tile joins the contraction: after the
+// r/16 bias steps, eight N=16 UMMAs multiply 16-token slices of the tile (128
+// requests x 128 tokens, already in the K-major A layout as TMA writes it) by
+// a 16 x 16 identity into the matching accumulator columns, so TMEM holds
+// z = U + bias and the epilogue reads nothing from shared memory.  (U * 1 and
+// U * 0 are exact; base logits must be finite, since inf * 0 would poison the
+// other columns of its 16-wide step.)  Every wait is bounded; a timeout sets
+// the timeout bit of the flag word and the CTA unwinds.
 //
-// Gumbel-max without a logarithm per token: token v beats the running best
-// key K iff E_v < 2^(s2_v - K) = e_v * 2^(m - K), where e_v = 2^(s2_v - m) is
-// the softmax term already computed and E_v = -ln u_v >= 1 - u_v.  So the test
-// (1 - u_v) < e_v * Q with Q = 2^(m - K) (plus a 1e-4 margin) rejects almost
-// every token exactly; only the survivors evaluate -ln u_v and the exact key.
+// Per-token Gumbel-max without a logarithm per token: token v can beat a key K
+// only if E_v < 2^(s2_v - K) = e_v * 2^(m - K), where e_v = 2^(s2_v - m) is the
+// softmax term already computed and E_v = -ln u_v >= 1 - u_v.  So the test
+// (1 - u_v) < e_v * Q with Q = 2^(m - K) (with a rounding margin) rejects
+// almost every token; only the survivors evaluate -ln u_v and a key.
 #include <climits>
 #include <mutex>
 
@@ -67,7 +72,7 @@ using namespace tc;
 constexpr int BM = 128;
 constexpr int BN = 128;                  // tokens per tile: the UMMA N
 #ifndef DSPARK_EPI_WARPS
-#define DSPARK_EPI_WARPS 16
+#define DSPARK_EPI_WARPS 12
 #endif
 constexpr int kEpiWarps = DSPARK_EPI_WARPS;  // a multiple of 4: one group per TMEM lane quadrant
 constexpr int kEpiPerQuad = kEpiWarps / 4;   // warps sharing a quadrant's 16-column sub-slices
@@ -513,8 +518,8 @@ __device__ __noinline__ void drain_ummas(uint32_t bar, volatile int *never) {
     mbar_wait(bar, 0u, never, kDrainLimit);
 }
 
-// 18 warps: 5 share one SM sub-partition's 16K registers, so at most 96 each.
-// The warps of the busiest SM sub-partition share its 16K registers: kMaxRegs each.
+// The warps of the busiest SM sub-partition share its 16K registers: kMaxRegs
+// each (15 warps: 4 per sub-partition, 128 registers).
 //
 // The draft form walks block positions p.j .. p.j_end - 1 in one launch when
 // the launch is cooperative: between positions every CTA publishes its rows'
