@@ -298,33 +298,7 @@ def run_ours(args, w):
           for k in ("draft", "sched", "verify")}
     call_ms = {k: [] for k in ev}
 
-    side = torch.cuda.Stream(dev)
-    ev_sched, ev_rows = torch.cuda.Event(), torch.cuda.Event()
-
-    def step_overlapped(x):
-        # The target-row statistics (dspark_verify_rows) need only the target
-        # logits and the verify lengths: after the schedule they run on a side
-        # stream, one block per SM beside the draft kernel's CTAs; the rest of
-        # the verification (dspark_verify_finish) waits for both.
-        vl = None
-        if w.scheduler:
-            binding.schedule_prefix(x["conf_logits"], x["pos_temp"], x["sps"], w.L_min, G, out=s_out,
-                                    workspace=ws_s, stream=stream)
-            vl = s_out["verify_len"]
-        ev_sched.record(stream)
-        side.wait_event(ev_sched)
-        binding.verify_rows(x["target"], vl, x["temperature"], G, r=r, workspace=ws_v, stream=side)
-        ev_rows.record(side)
-        binding.draft_sample(x["base"], x["e_in"], x["w_out"], x["anchor"], x["temperature"],
-                             x["request_id"], args.seed, out=d_out, workspace=ws_d, stream=stream)
-        stream.wait_event(ev_rows)
-        binding.verify(x["target"], x["base"], x["e_in"], x["w_out"], x["anchor"], d_out, vl,
-                       x["temperature"], x["request_id"], args.seed, rows_done=True, out=v_out,
-                       workspace=ws_v, stream=stream)
-
     def step(x, timed=False, st=None):
-        if not timed and args.overlap:
-            return step_overlapped(x)
         st = stream if st is None else st
         if timed:
             ev["draft"][0].record(stream)
@@ -370,7 +344,7 @@ def run_ours(args, w):
     # flag clears, captured once on a side stream): the same kernels on the
     # same resident buffers, without the per-launch gaps of eager issue.
     graph = None
-    if not args.no_graph and not args.overlap:
+    if not args.no_graph:
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -582,9 +556,7 @@ def run_ours(args, w):
                             "blocks (one per four drawn tokens) over the call time against the "
                             "device's measured Philox rate; bound = the roof with the longer floor"),
         calls_ms=dict(draft=d_ms, schedule=s_ms, verify=v_ms),
-        step_order=("schedule; then draft beside dspark_verify_rows on a second stream; then "
-                    "dspark_verify_finish (calls_ms timed serially)" if args.overlap else
-                    "draft, schedule, verify on one stream" +
+        step_order=("draft, schedule, verify on one stream" +
                     (", replayed from one CUDA graph (calls_ms timed eagerly)" if graph is not None else "")),
         rnn_head=(None if rnn_ms is None else
                   dict(draft_ms=rnn_ms, launches=2 * G + 1,
@@ -634,9 +606,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed rounds' calls eagerly instead of replaying a CUDA graph of the round")
-    ap.add_argument("--overlap", action="store_true",
-                    help="run dspark_verify_rows on a second stream beside the draft (measured slower: both "
-                         "kernels are bound by the SMs' issue rate, not by HBM)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

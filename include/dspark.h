@@ -12,9 +12,7 @@
  *                           (dspark_schedule_policy: other policies);
  *   dspark_verify           lossless rejection-sampling verification against
  *                           the target logits, with residual resampling or a
- *                           bonus token (dspark_verify_rows and
- *                           dspark_verify_finish: the same in two halves, the
- *                           first of which may run beside the draft).
+ *                           bonus token.
  *
  * Conventions shared by every entry point
  *  - Every array argument is a DEVICE pointer owned by the caller, row-major
@@ -287,7 +285,9 @@ DSPARK_API dspark_status dspark_schedule_policy(
  * tokens then the resampled or bonus token, padded with -1; num_out [B] =
  * accept_len + 1; target_lse [B][G+1] fp32 or NULL (lse of rows j < L at
  * T > 0, max of the row at T = 0; NaN where not computed); logp_sel [B][G]
- * fp32 or NULL (log p_j(x_j) of the tested rows, NaN elsewhere).
+ * fp32 or NULL (log p_j(x_j) of the tested rows, NaN elsewhere).  There is
+ * no q output: log q_j(x_j) is the caller's draft_logq input, which the
+ * acceptance test uses as given.
  */
 DSPARK_API dspark_status dspark_verify(
     const void *target_logits, const void *base_logits, const void *e_in, const void *w_out,
@@ -313,35 +313,6 @@ DSPARK_API dspark_status dspark_verify(
  * device array.  Everything else, the results included, is dspark_verify's.
  */
 DSPARK_API dspark_status dspark_verify_packed(
-    const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
-    const void *base_logits, const void *e_in, const void *w_out,
-    const float *draft_logits, const int32_t *anchor, const int32_t *draft_tokens,
-    const float *draft_lse, const float *draft_logq, const int32_t *verify_len,
-    const float *temperature, const uint32_t *request_id, int B, int G, int V, int r,
-    dspark_dtype dtype, uint64_t seed, int32_t *accept_len, int32_t *out_tokens,
-    int32_t *num_out, float *target_lse, float *logp_sel, void *workspace,
-    size_t workspace_bytes, void *stream);
-
-/*
- * dspark_verify in two halves, so that the first can run beside the draft.
- *
- * The target-row statistics of verification (the log-sum-exp of t/T of every
- * tested row, or its argmax at T = 0) need only the target logits and the
- * verify lengths, not the draft.  dspark_verify_rows computes them into the
- * verify workspace (and clears its flag word); launched as one block per SM,
- * it fits next to a CTA of the draft kernel, so a caller may run it on another
- * stream while dspark_draft_sample runs.  dspark_verify_finish then does the
- * rest of dspark_verify (acceptance, final draw, emit) on the same workspace,
- * after both.  target_row0 = NULL means the dense layout [B][G+1][V];
- * otherwise the packed layout of dspark_verify_packed.  The results equal
- * dspark_verify's (dspark_verify_packed's) bit for bit.
- */
-DSPARK_API dspark_status dspark_verify_rows(
-    const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
-    const int32_t *verify_len, const float *temperature, int B, int G, int V, int r, dspark_dtype dtype,
-    void *workspace, size_t workspace_bytes, void *stream);
-
-DSPARK_API dspark_status dspark_verify_finish(
     const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
     const void *base_logits, const void *e_in, const void *w_out,
     const float *draft_logits, const int32_t *anchor, const int32_t *draft_tokens,

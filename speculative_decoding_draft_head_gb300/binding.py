@@ -31,8 +31,7 @@ FLAG_BAD_TARGET_ROW = 32
 EXPORTS = ("dspark_version", "dspark_last_error", "dspark_workspace_bytes", "dspark_draft_sample",
            "dspark_schedule_prefix", "dspark_schedule_policy", "dspark_verify", "dspark_read_device_flags",
            "dspark_verify_noalloc", "dspark_draft_sample_rnn", "dspark_verify_packed", "dspark_pack_target",
-           "dspark_selftest_bounded_wait", "dspark_verify_rows", "dspark_verify_finish",
-           "dspark_read_noalloc_flags", "dspark_selftest_philox_rate")
+           "dspark_selftest_bounded_wait", "dspark_read_noalloc_flags", "dspark_selftest_philox_rate")
 
 _lib = None
 _lock = threading.Lock()
@@ -86,10 +85,6 @@ def load(build_if_missing: bool = True):
         L.dspark_verify_packed.argtypes = [vp, vp, ctypes.c_int64] + L.dspark_verify.argtypes[1:]
         L.dspark_selftest_bounded_wait.restype = ctypes.c_int
         L.dspark_selftest_bounded_wait.argtypes = [ctypes.c_uint, ctypes.POINTER(ctypes.c_uint32), vp]
-        L.dspark_verify_rows.restype = ctypes.c_int
-        L.dspark_verify_rows.argtypes = [vp, vp, ctypes.c_int64, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]
-        L.dspark_verify_finish.restype = ctypes.c_int
-        L.dspark_verify_finish.argtypes = L.dspark_verify_packed.argtypes
         L.dspark_pack_target.restype = ctypes.c_int
         L.dspark_pack_target.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.dspark_verify_noalloc.restype = ctypes.c_int
@@ -307,45 +302,14 @@ class LaggedScheduler:
         return res
 
 
-def verify_rows(target, verify_len, temperature, G, *, target_row0=None, r=16, workspace=None, stream=None):
-    """The target-row statistics of verification alone (dspark_verify_rows),
-    one block per SM so that it can run beside the draft kernel on another
-    stream.  Finish with :func:`verify` and ``rows_done=True``, passing the
-    workspace this returns.  Returns the workspace."""
-    lib = load()
-    V = target.shape[-1]
-    B = temperature.shape[0]
-    dev = target.device
-    _need(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
-    if verify_len is not None:
-        _need(verify_len, "verify_len", dtype=torch.int32, shape=(B,), device=dev)
-    if target_row0 is None:
-        _need(target, "target", shape=(B, G + 1, V), device=dev)
-    else:
-        _need(target_row0, "target_row0", dtype=torch.int64, shape=(B,), device=dev)
-    ws = workspace if workspace is not None else _default_ws.get(WS_VERIFY, B, G, V, r, dev)
-    _check(lib.dspark_verify_rows(_ptr(target), _ptr(target_row0),
-                                  target.shape[0] if target_row0 is not None else 0, _ptr(verify_len),
-                                  _ptr(temperature), B, G, V, r, _dtype_code(target), _ptr(ws), ws.numel(),
-                                  _stream(stream)))
-    return ws
-
-
 def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, request_id=None,
-           seed=0, *, draft_logits=None, target_row0=None, rows_done=False, out=None, workspace=None,
-           stream=None):
+           seed=0, *, draft_logits=None, target_row0=None, out=None, workspace=None, stream=None):
     """Verify one drafted block per request.
 
     ``draft`` is the dict returned by :func:`draft_sample`.  ``target`` is
     [B, G+1, V], or with ``target_row0`` ([B] int64) the packed rows [n, V]
     (request b's row j at row target_row0[b] + j, see dspark_verify_packed).
-    With ``rows_done`` only the second half runs (dspark_verify_finish) on a
-    workspace that :func:`verify_rows` filled.
     Returns dict(accept_len, out_tokens, num_out, target_lse, logp)."""
-    if rows_done and workspace is None:
-        # the first half's results live in its workspace: name it (the default
-        # workspaces of the two calls need not be the same tensor)
-        raise ValueError("rows_done=True needs the workspace that verify_rows returned")
     lib = load()
     B, G = draft["tokens"].shape
     V = target.shape[-1]
@@ -386,10 +350,7 @@ def verify(target, base, e_in, w_out, anchor, draft, verify_len, temperature, re
             _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["num_out"]),
             _ptr(out.get("target_lse")), _ptr(out.get("logp")), _ptr(ws), ws.numel(),
             _stream(stream))
-    if rows_done:  # dspark_verify_rows already ran on this workspace
-        n_rows = target.shape[0] if target_row0 is not None else 0
-        _check(lib.dspark_verify_finish(_ptr(target), _ptr(target_row0), n_rows, *args))
-    elif target_row0 is None:
+    if target_row0 is None:
         _check(lib.dspark_verify(_ptr(target), *args))
     else:
         _check(lib.dspark_verify_packed(_ptr(target), _ptr(target_row0), target.shape[0], *args))

@@ -74,7 +74,7 @@ dspark_status verify_impl(const void *target_logits, const int64_t *target_row0,
                             const uint32_t *request_id, int B, int G, int V, int r, dspark_dtype dtype,
                             uint64_t seed, int32_t *accept_len, int32_t *out_tokens, int32_t *num_out,
                             float *target_lse, float *logp_sel, void *workspace, size_t workspace_bytes,
-                            void *stream, bool finish_only = false) {
+                            void *stream) {
     dspark_status st = verify_check_args(target_logits, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens,
                                          draft_lse, draft_logq, temperature, B, G, V, r, dtype, accept_len,
                                          out_tokens, num_out);
@@ -82,15 +82,12 @@ dspark_status verify_impl(const void *target_logits, const int64_t *target_row0,
     const VerifyPlan plan = plan_verify(B, G, V, r, dtype);
     if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaSuccess;
-    if (!finish_only) {  // (dspark_verify_rows cleared it for a finish)
-        e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
-    }
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
     VerifyArgs a{target_logits, target_row0, n_target_rows, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens, draft_lse,
                  draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype, seed, accept_len,
                  out_tokens, num_out, target_lse, logp_sel, static_cast<unsigned char *>(workspace)};
-    e = finish_only ? launch_verify_finish(a, plan, s) : launch_verify(a, plan, s);
+    e = launch_verify(a, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "verify launch");
     return DSPARK_OK;
 }
@@ -293,52 +290,6 @@ dspark_status dspark_verify_packed(const void *target_logits, const int64_t *tar
                        draft_tokens, draft_lse, draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype,
                        seed, accept_len, out_tokens, num_out, target_lse, logp_sel, workspace, workspace_bytes,
                        stream);
-}
-
-dspark_status dspark_verify_rows(const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
-                                 const int32_t *verify_len, const float *temperature, int B, int G, int V, int r,
-                                 dspark_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
-    dspark_status st = check_common(B, G, V, r, dtype);
-    if (st != DSPARK_OK) return st;
-    if (!target_logits || !temperature) return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
-    if (!aligned(target_logits, 16)) return fail(DSPARK_ERR_INVALID_ARG, "target logits must be 16-byte aligned");
-    if ((st = check_packed(target_row0, n_target_rows, V)) != DSPARK_OK) return st;
-    const VerifyPlan plan = plan_verify(B, G, V, r, dtype);
-    if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
-    VerifyArgs a{};
-    a.target = target_logits;
-    a.target_row0 = target_row0;
-    a.n_target_rows = n_target_rows;
-    a.verify_len = verify_len;
-    a.temperature = temperature;
-    a.B = B;
-    a.G = G;
-    a.V = V;
-    a.r = r;
-    a.dt = dtype;
-    a.ws = static_cast<unsigned char *>(workspace);
-    e = launch_verify_rows(a, plan, true, s);
-    if (e != cudaSuccess) return cuda_fail(e, "verify rows launch");
-    return DSPARK_OK;
-}
-
-dspark_status dspark_verify_finish(const void *target_logits, const int64_t *target_row0, int64_t n_target_rows,
-                                   const void *base_logits, const void *e_in, const void *w_out,
-                                   const float *draft_logits, const int32_t *anchor, const int32_t *draft_tokens,
-                                   const float *draft_lse, const float *draft_logq, const int32_t *verify_len,
-                                   const float *temperature, const uint32_t *request_id, int B, int G, int V, int r,
-                                   dspark_dtype dtype, uint64_t seed, int32_t *accept_len, int32_t *out_tokens,
-                                   int32_t *num_out, float *target_lse, float *logp_sel, void *workspace,
-                                   size_t workspace_bytes, void *stream) {
-    dspark_status st = check_packed(target_row0, n_target_rows, V);
-    if (st != DSPARK_OK) return st;
-    return verify_impl(target_logits, target_row0, n_target_rows, base_logits, e_in, w_out, draft_logits, anchor,
-                       draft_tokens, draft_lse, draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype,
-                       seed, accept_len, out_tokens, num_out, target_lse, logp_sel, workspace, workspace_bytes,
-                       stream, true);
 }
 
 dspark_status dspark_pack_target(const void *target_logits, const int32_t *verify_len, int B, int G, int V,

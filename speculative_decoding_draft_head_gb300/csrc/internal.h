@@ -195,10 +195,6 @@ struct VerifyArgs {
     unsigned char *ws;
 };
 cudaError_t launch_verify(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s);
-// the two halves of launch_verify: the target-row statistics (beside: one
-// block per SM, to run next to the draft kernel), then decide, final draw, merge
-cudaError_t launch_verify_rows(const VerifyArgs &a, const VerifyPlan &p, bool beside, cudaStream_t s);
-cudaError_t launch_verify_finish(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s);
 
 // ------------------------------------------------------------- schedule ----
 struct ScheduleArgs {

@@ -99,10 +99,9 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
                    const float *__restrict__ temperature, int B, int G, int V, int chunk, int nsplit,
                    RowState *__restrict__ part) {
     __shared__ RowState scratch[kRowThreads / 32];
-    // Unit u = seg * rows + row.  Launched as (rows, segments) every block takes
+    // Unit u = seg * rows + row; launched as (rows, segments), every block takes
     // one unit (rows along x: their count B (G + 1) can pass the 65535 limit of
-    // y); launched with fewer blocks (beside the draft kernel, one block per SM)
-    // the blocks walk the units.
+    // y).
     const long rows = (long)B * (G + 1);
     const long units = rows * nsplit;
     const long stride = (long)gridDim.x * gridDim.y;
@@ -501,30 +500,11 @@ __global__ void verify_final_merge_kernel(const ResidualState *__restrict__ part
     if (lane == 0) out_tokens[(size_t)b * (G + 1) + accept_len[b]] = word_token(w);
 }
 
-// Beside the draft kernel the blocks must share an SM with a draft CTA, which
-// runs with the largest shared-memory carveout; a block that reached an SM
-// first under a smaller carveout would keep the draft CTA off it.
 template <typename TIn>
-cudaError_t set_rows_carveout() {
-    static PerDeviceOnce once;
-    return once.run([] {
-        return cudaFuncSetAttribute(verify_rows_kernel<TIn>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                    (int)cudaSharedmemCarveoutMaxShared);
-    });
-}
-
-template <typename TIn>
-cudaError_t launch_verify_rows_t(const VerifyArgs &a, const VerifyPlan &p, bool beside, cudaStream_t s) {
-    if (beside) {
-        const cudaError_t e = set_rows_carveout<TIn>();
-        if (e != cudaSuccess) return e;
-    }
+cudaError_t launch_verify_rows_t(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
     RowState *row_part = reinterpret_cast<RowState *>(a.ws + p.row_part_offset);
     const TIn *target = static_cast<const TIn *>(a.target);
-    const long units = (long)a.B * (a.G + 1) * p.row_split;
-    // beside the draft kernel: one block per SM, which fits next to a draft CTA
-    const dim3 grid = beside ? dim3((unsigned int)(units < kNumSMs ? units : kNumSMs))
-                             : dim3((unsigned int)(a.B * (a.G + 1)), (unsigned int)p.row_split);
+    const dim3 grid((unsigned int)(a.B * (a.G + 1)), (unsigned int)p.row_split);
     verify_rows_kernel<TIn><<<grid, kRowThreads, 0, s>>>(target, a.target_row0, a.n_target_rows, a.verify_len,
                                                          a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split,
                                                          row_part);
@@ -576,20 +556,10 @@ cudaError_t launch_verify_finish_t(const VerifyArgs &a, const VerifyPlan &p, cud
 
 }  // namespace
 
-cudaError_t launch_verify_rows(const VerifyArgs &a, const VerifyPlan &p, bool beside, cudaStream_t s) {
-    if (a.dt == DSPARK_BF16) return launch_verify_rows_t<__nv_bfloat16>(a, p, beside, s);
-    return launch_verify_rows_t<float>(a, p, beside, s);
-}
-
-cudaError_t launch_verify_finish(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
-    if (a.dt == DSPARK_BF16) return launch_verify_finish_t<__nv_bfloat16>(a, p, s);
-    return launch_verify_finish_t<float>(a, p, s);
-}
-
 cudaError_t launch_verify(const VerifyArgs &a, const VerifyPlan &p, cudaStream_t s) {
-    cudaError_t e = launch_verify_rows(a, p, false, s);
+    cudaError_t e = (a.dt == DSPARK_BF16) ? launch_verify_rows_t<__nv_bfloat16>(a, p, s) : launch_verify_rows_t<float>(a, p, s);
     if (e != cudaSuccess) return e;
-    return launch_verify_finish(a, p, s);
+    return (a.dt == DSPARK_BF16) ? launch_verify_finish_t<__nv_bfloat16>(a, p, s) : launch_verify_finish_t<float>(a, p, s);
 }
 
 VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {

@@ -89,43 +89,19 @@ def test_schedule_and_verify_reject_bad_host_arguments():
     assert st == 1 and "draft_logits" in lib.dspark_last_error().decode()
 
 
-def test_split_verify_rejects_bad_host_arguments():
-    """dspark_verify_rows / dspark_verify_finish check their arguments on the
-    host before any launch, like dspark_verify."""
+def test_packed_verify_rejects_bad_host_arguments():
+    """dspark_verify_packed checks the packed layout, then dspark_verify's
+    arguments, on the host before any launch."""
     lib = binding.load()
     vp = ctypes.c_void_p
     p = vp(1 << 12)
     err = lambda: lib.dspark_last_error().decode()
-    # rows half: B, G, V, r, dtype as dspark_verify; then pointers, packing, workspace
-    st = lib.dspark_verify_rows(p, None, 0, None, None, 4, 4, 1024, 16, 1, p, 1 << 20, None)
-    assert st == 1 and "NULL" in err()
-    st = lib.dspark_verify_rows(p, p, 0, None, p, 4, 4, 1024, 16, 1, p, 1 << 20, None)
-    assert st == 1 and "n_target_rows" in err()
-    st = lib.dspark_verify_rows(vp((1 << 12) + 4), None, 0, None, p, 4, 4, 1024, 16, 1, p, 1 << 20, None)
-    assert st == 1 and "aligned" in err()
-    st = lib.dspark_verify_rows(p, None, 0, None, p, 4, 4, 1024, 16, 1, p, 16, None)
-    assert st == 1 and "too small" in err()
-    st = lib.dspark_verify_rows(p, None, 0, None, p, 4, 0, 1024, 16, 1, p, 1 << 20, None)
-    assert st == 1 and "G must be" in err()
-    # finishing half: the packed-layout check, then dspark_verify's
-    st = lib.dspark_verify_finish(p, p, 0, p, p, p, None, p, p, p, p, None, p, None,
+    st = lib.dspark_verify_packed(p, p, 0, p, p, p, None, p, p, p, p, None, p, None,
                                   4, 4, 1024, 16, 1, 0, p, p, p, None, None, p, 1 << 20, None)
     assert st == 1 and "n_target_rows" in err()
-    st = lib.dspark_verify_finish(p, None, 0, None, None, None, None, p, p, p, p, None, p, None,
+    st = lib.dspark_verify_packed(p, p, 8, None, None, None, None, p, p, p, p, None, p, None,
                                   4, 4, 1024, 16, 1, 0, p, p, p, None, None, p, 1 << 20, None)
     assert st == 1 and "draft_logits" in err()
-
-
-def test_finishing_half_needs_the_rows_workspace():
-    """verify(rows_done=True) must be given the workspace verify_rows filled;
-    the binding refuses before touching the device."""
-    import torch
-    B, G, V = 2, 3, 16
-    z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt)
-    draft = dict(tokens=z(B, G, dt=torch.int32), lse=z(B, G), logq=z(B, G))
-    with pytest.raises(ValueError, match="rows_done"):
-        binding.verify(z(B, G + 1, V), z(B, G, V), z(V, 16), z(V, 16), z(B, dt=torch.int32), draft, None,
-                       z(B), rows_done=True)
 
 
 def test_pack_target_rejects_bad_host_arguments():
