@@ -49,7 +49,8 @@
  *  - Precision: the arithmetic is fp32 on fp32 or bf16 data.  The kernels
  *    screen tokens in fp32 and form the Gumbel keys of the few tokens that
  *    can still win in float-float arithmetic (about 44 significant bits), and
- *    the small merge and decision kernels work in double, so a draw or an
+ *    the merges of row partials (log-sum-exp, log q, log p) and the acceptance
+ *    test work in float-float as well, so a draw or an
  *    acceptance differs from an exact evaluation only on a tie far below fp32
  *    rounding (about 1e-7 of decisions or fewer, in the test suite none in
  *    2.5 million).

@@ -92,14 +92,6 @@ dspark_status verify_impl(const void *target_logits, const int64_t *target_row0,
     return DSPARK_OK;
 }
 
-dspark_status check_packed(const int64_t *target_row0, int64_t n_target_rows, int V) {
-    if (!target_row0) return DSPARK_OK;
-    if (n_target_rows < 1) return fail(DSPARK_ERR_INVALID_ARG, "n_target_rows must be >= 1");
-    if (n_target_rows > (1LL << 40) / (V > 0 ? V : 1))
-        return fail(DSPARK_ERR_INVALID_ARG, "n_target_rows * V too large");
-    return DSPARK_OK;
-}
-
 }  // namespace
 }  // namespace dspark
 

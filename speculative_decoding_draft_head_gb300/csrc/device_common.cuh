@@ -327,6 +327,33 @@ __device__ __forceinline__ unsigned long long key_word(FF k, int idx) {
     return ((unsigned long long)oh << 32) | ((unsigned long long)q << kTokenBits) |
            (unsigned long long)(~(uint32_t)idx & kTokenMask);
 }
+
+// The exact key word of a final-draw contender: token tok with target logit
+// tb, draft logit zb and word wb; 0 when a residual row gives it no mass
+// (p <= q).  key_hi receives the float-float key's high part.  Out of line:
+// it runs for a few tokens per row; inlined at every call site it would
+// spill registers (tensor-core kernel) or bloat the code (SIMT kernel).
+static __device__ __noinline__ unsigned long long final_key_word(float tb, float zb, uint32_t wb, int tok, bool bonus,
+                                                          float T, float rT, FF lse_t, float lse_q,
+                                                          float *key_hi) {
+    FF key;
+    if (bonus) {
+        key = div_ff(tb, T, rT);  // t / T: the bonus key before its noise
+    } else {
+        // ln r = ln p + ln(1 - q / p), ln q - ln p formed in float-float from
+        // the logits and the two lse
+        const FF lp = ff_add(div_ff(tb, T, rT), ff_neg(lse_t));
+        const FF dl = ff_add(ff_add(div_ff(zb, T, rT), FF{-lse_q, 0.f}), ff_neg(lp));
+        const float d = dl.hi + dl.lo;
+        if (!(d < 0.f)) return 0ull;  // p <= q: no residual mass
+        const float l1m = (d > -0.6931472f) ? logf(-expm1f(d)) : log1pf(-expf(d));
+        key = ff_add(lp, FF{l1m, 0.f});
+    }
+    key = ff_add(key, gumbel_ff(wb));
+    *key_hi = key.hi;
+    return key_word(key, tok);
+}
+
 __device__ __forceinline__ int word_token(unsigned long long w) {
     return w ? (int)(~(uint32_t)w & kTokenMask) : -1;
 }
@@ -410,24 +437,52 @@ __device__ __forceinline__ RowState warp_merge(RowState s) {
     return s;
 }
 
-// The natural-log log-sum-exp of partial states (m_i, S_i) of one row, in
-// double: the partial sums are rescaled exactly (integer references) and
-// added in double.  Every lane of the warp calls it; lane i reads partials
-// i, i + 32, ...  Returns -inf for an empty row.
-__device__ __forceinline__ double warp_lse_of_partials(const RowState *part, int n) {
+// ln x of a positive float-float x = hi + lo: ln hi + lo / hi (the next
+// term, (lo / hi)^2 / 2, is below 2^-49).
+__device__ __forceinline__ FF ln_of_ff(FF x) {
+    const FF l = ln_ff(x.hi);
+    return quick_two_sum(l.hi, l.lo + x.lo * __frcp_rn(x.hi));
+}
+// m ln 2 as float-float for an integer-valued float m: the fp32 product, its
+// exact rounding error, and m times the part of ln 2 that fp32 drops.
+__device__ __forceinline__ FF mul_ln2_ff(float m) {
+    constexpr float kLn2Tail = -1.9046542999577683e-09f;  // ln 2 - fl(ln 2)
+    const float p = m * kLn2;
+    return quick_two_sum(p, fmaf(m, kLn2Tail, fmaf(m, kLn2, -p)));
+}
+// Sum of partial sums S_i 2^(m_i - m) (m the largest reference): each term is
+// an exact power-of-two rescaling, added in float-float.
+__device__ __forceinline__ FF add_scaled_partial(FF S, const RowState &p, float m) {
+    if (p.m != -INFINITY && p.S > 0.f) S = ff_add(S, FF{scale_pow2(p.S, p.m - m), 0.f});
+    return S;
+}
+
+// The natural-log log-sum-exp of the partial states (m_i, S_i) of one row, as
+// float-float (about 44 bits): m ln 2 + ln sum_i S_i 2^(m_i - m), the partial
+// sums rescaled exactly by their integer references.  Every lane of the warp
+// calls it; lane i reads partials i, i + 32, ...  Returns -inf for an empty
+// row.
+__device__ __forceinline__ FF warp_lse_of_partials(const RowState *part, int n) {
     float m = -INFINITY;
     for (int i = threadIdx.x & 31; i < n; i += 32) m = fmaxf(m, part[i].m);
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
-    if (m == -INFINITY) return -INFINITY;
-    double S = 0.0;
-    for (int i = threadIdx.x & 31; i < n; i += 32) {
-        const RowState &p = part[i];
-        if (p.m != -INFINITY && p.S > 0.f) S += ldexp((double)p.S, (int)fmaxf(p.m - m, -1100.f));
-    }
+    if (m == -INFINITY) return FF{-INFINITY, 0.f};
+    FF S{0.f, 0.f};
+    for (int i = threadIdx.x & 31; i < n; i += 32) S = add_scaled_partial(S, part[i], m);
 #pragma unroll
-    for (int k = 16; k > 0; k >>= 1) S += __shfl_xor_sync(0xffffffffu, S, k);
-    return 0.6931471805599453 * ((double)m + log2(S));
+    for (int k = 16; k > 0; k >>= 1)
+        S = ff_add(S, FF{__shfl_xor_sync(0xffffffffu, S.hi, k), __shfl_xor_sync(0xffffffffu, S.lo, k)});
+    return ff_add(mul_ln2_ff(m), ln_of_ff(S));
+}
+// The same for one thread reading all n partials in order.
+__device__ __forceinline__ FF lse_of_partials(const RowState *part, int n) {
+    float m = -INFINITY;
+    for (int i = 0; i < n; ++i) m = fmaxf(m, part[i].m);
+    if (m == -INFINITY) return FF{-INFINITY, 0.f};
+    FF S{0.f, 0.f};
+    for (int i = 0; i < n; ++i) S = add_scaled_partial(S, part[i], m);
+    return ff_add(mul_ln2_ff(m), ln_of_ff(S));
 }
 
 __device__ __forceinline__ float term_exp2(float z, float c2h, float c2l, float m) {

@@ -25,35 +25,73 @@ namespace {
 constexpr int kSimtThreads = 256;
 constexpr int kSimtRows = 8;
 
+// The exact key word of draft token v with logit z and word w: z / T + g(u)
+// in float-float.  Out of line: it runs for few tokens, and inlined at each of
+// the kernel's unrolled call sites it would bloat the code (a launch fetches
+// its instructions cold).
+static __device__ __noinline__ unsigned long long draft_key_word(float z, float T, float rT, uint32_t w, int v,
+                                                                 float *key_hi) {
+    const FF key = ff_add(div_ff(z, T, rT), gumbel_ff(w));
+    *key_hi = key.hi;
+    return key_word(key, v);
+}
+
 // Online softmax and per-token Gumbel-max for four consecutive tokens
 // v .. v + 3 of one row (T > 0, c2 = log2(e) / T, rT = fl(1 / T)); w holds
-// their draft-stream words.  A token is screened without a logarithm
-// against the best key K this thread has seen for the row, (1 - u) < e Q with
-// e = 2^(s2 - m) and Q = 2^(m - K log2 e) (E = -ln u >= 1 - u, so no winner is
-// lost); a survivor's fp32 key decides whether its float-float key is formed,
-// and the key words decide.
+// their draft-stream words; lanes with valid = false hold no tokens.  Every
+// lane of the warp calls it together (it reduces across the warp).  A token is
+// screened without a logarithm against the best key K this thread knows for
+// the row, (1 - u) < e Q with e = 2^(s2 - m) and Q = 2^(m - K log2 e)
+// (E = -ln u >= 1 - u, so no winner is lost).  A survivor gets an fp32 key;
+// the warp's largest fp32 key, less its error bound, is a lower bound of an
+// exact key that its own lane forms below, so only tokens that can reach it
+// form a float-float key, and the key words decide.
 __device__ __forceinline__ void simt_draw4(RowState &st, float &kbest, const float (&z)[4], float2 c2, float T,
-                                           float rT, int v, const uint4 &w) {
+                                           float rT, int v, const uint4 &w, bool valid) {
     float e[4];
-    softmax_push_group<4>(st, z, c2.x, c2.y, e);
+    if (valid) softmax_push_group<4>(st, z, c2.x, c2.y, e);
     const float Q = screen_q(st.m, kbest);
+    float k2[4];
+    float wm = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t wi = i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
-        if (!(one_minus_uniform_plus_one(wi) < fmaf(e[i], Q, 1.f))) continue;
-        const float k2 = fmaf(z[i], c2.x, -fast_log2(neg_log_uniform(wi)));
-        const float K2 = kbest * kLog2e;
-        if (!(k2 > K2 - key_tol2(k2, K2))) continue;
-        const FF key = ff_add(div_ff(z[i], T, rT), gumbel_ff(wi));
-        const unsigned long long word = key_word(key, v + i);
+        k2[i] = -INFINITY;
+        if (valid && one_minus_uniform_plus_one(wi) < fmaf(e[i], Q, 1.f)) {
+            k2[i] = fmaf(z[i], c2.x, -fast_log2(neg_log_uniform(wi)));
+            wm = fmaxf(wm, k2[i]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+    const float wlow = wm - key_tol2(wm, wm);  // log2 units; -inf when no lane has a survivor
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float K2 = fmaxf(kbest * kLog2e, wlow);
+        if (!(k2[i] > K2 - key_tol2(k2[i], K2))) continue;
+        const uint32_t wi = i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
+        float key_hi;
+        const unsigned long long word = draft_key_word(z[i], T, rT, wi, v + i, &key_hi);
         if (word > st.best) {
             st.best = word;
             st.z_at = z[i];
-            kbest = fmaxf(kbest, key.hi);
+            kbest = fmaxf(kbest, key_hi);
         }
     }
+    // the warp's bound, in natural-log units, screens this thread's next tokens
+    if (wlow > -INFINITY) kbest = fmaxf(kbest, wlow * kLn2 - 1e-6f * fabsf(wlow));
 }
 
+static_assert(kSimtThreads / 32 == kSimtRows, "one warp draws each row of the block");
+
+// Two phases per 4 kSimtThreads tokens of the segment: every thread forms the
+// logits of four tokens for all rows of the block (the rank-r bias
+// register-tiled over the rows, so each W_out row is read once per block) into
+// shared memory; then warp w draws row w over those tokens (softmax and
+// per-token Gumbel-max), its lanes taking groups of four tokens in turn.  One
+// copy of the draw code serves every row: the kernel is small enough that a
+// launch does not wait on instruction fetch, and each row's state stays in its
+// warp's registers.
 template <typename TIn>
 __global__ void __launch_bounds__(kSimtThreads)
 draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
@@ -62,15 +100,17 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
                   const uint32_t *__restrict__ request_id, int B, int G, int V, int r, int j,
                   uint32_t k0, uint32_t k1, int chunk, int nsplit, RowState *__restrict__ part,
                   uint32_t *__restrict__ flags, float *__restrict__ z_out) {
-    extern __shared__ float a_rows[];  // [kSimtRows][r]
+    extern __shared__ float smem_f[];
+    float *a_rows = smem_f;                       // [kSimtRows][r]
+    float *zs = smem_f + (size_t)kSimtRows * r;   // [kSimtRows][4 kSimtThreads] logits of the current tokens
     __shared__ int prev_s[kSimtRows];
     __shared__ float2 c2_s[kSimtRows];
     __shared__ float T_s[kSimtRows];
     __shared__ uint32_t rid_s[kSimtRows];
-    __shared__ RowState scratch[kSimtThreads / 32];
 
     const int b0 = blockIdx.y * kSimtRows;
     const int seg = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x < kSimtRows) {
         const int b = b0 + threadIdx.x;
         int prev = -1;
@@ -101,81 +141,100 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
     }
     __syncthreads();
 
-    RowState st[kSimtRows];
-    float kbest[kSimtRows];
-#pragma unroll
-    for (int rb = 0; rb < kSimtRows; ++rb) {
-        st[rb] = row_state_init();
-        kbest[rb] = -INFINITY;
-    }
+    // this warp's row
+    const int b_w = b0 + warp;
+    const bool row_on = b_w < B && prev_s[warp] >= 0;  // uniform over the warp
+    const float2 c2w = c2_s[warp];
+    const float T_w = T_s[warp];
+    const float rT_w = __frcp_rn(T_w);
+    const uint32_t rid_w = rid_s[warp];
+    RowState st = row_state_init();
+    float kbest = -INFINITY;
 
     const int vb = seg * chunk;  // a multiple of 16
     const int ve = min(V, vb + chunk);
     for (int vbase = vb; vbase < ve; vbase += 4 * kSimtThreads) {
-        const int v = vbase + 4 * threadIdx.x;
-        const bool valid = v < ve;  // V % 8 == 0: all four tokens or none
-        float acc[kSimtRows][4];
+        // phase 1: the logits of tokens v .. v + 3 for every row of the block
+        {
+            const int v = vbase + 4 * threadIdx.x;
+            if (v < ve) {  // V % 8 == 0: all four tokens or none
+                float acc[kSimtRows][4];
 #pragma unroll
-        for (int rb = 0; rb < kSimtRows; ++rb)
+                for (int rb = 0; rb < kSimtRows; ++rb)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[rb][e] = 0.f;
-        for (int k = 0; valid && k < r; k += 4) {
-            float4 w[4];
+                    for (int e = 0; e < 4; ++e) acc[rb][e] = 0.f;
+                for (int k = 0; k < r; k += 4) {
+                    float4 w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = load4(w_out + (size_t)(v + e) * r + k);
+                    for (int e = 0; e < 4; ++e) w[e] = load4(w_out + (size_t)(v + e) * r + k);
 #pragma unroll
-            for (int rb = 0; rb < kSimtRows; ++rb) {
-                const float4 a = *reinterpret_cast<const float4 *>(a_rows + rb * r + k);
+                    for (int rb = 0; rb < kSimtRows; ++rb) {
+                        const float4 a = *reinterpret_cast<const float4 *>(a_rows + rb * r + k);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float t = acc[rb][e];
-                    t = fmaf(a.x, w[e].x, t);
-                    t = fmaf(a.y, w[e].y, t);
-                    t = fmaf(a.z, w[e].z, t);
-                    t = fmaf(a.w, w[e].w, t);
-                    acc[rb][e] = t;
+                        for (int e = 0; e < 4; ++e) {
+                            float t = acc[rb][e];
+                            t = fmaf(a.x, w[e].x, t);
+                            t = fmaf(a.y, w[e].y, t);
+                            t = fmaf(a.z, w[e].z, t);
+                            t = fmaf(a.w, w[e].w, t);
+                            acc[rb][e] = t;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int rb = 0; rb < kSimtRows; ++rb) {
+                    const int b = b0 + rb;
+                    if (b >= B || prev_s[rb] < 0) continue;  // uniform over the block
+                    const size_t row = (size_t)b * G + j;
+                    const float4 u4 = load4(base + row * V + v);
+                    const float4 z4 = make_float4(u4.x + acc[rb][0], u4.y + acc[rb][1], u4.z + acc[rb][2],
+                                                  u4.w + acc[rb][3]);
+                    *reinterpret_cast<float4 *>(zs + rb * (4 * kSimtThreads) + 4 * threadIdx.x) = z4;
+                    if (z_out) *reinterpret_cast<float4 *>(z_out + row * V + v) = z4;
                 }
             }
         }
-#pragma unroll
-        for (int rb = 0; rb < kSimtRows; ++rb) {
-            const int b = b0 + rb;
-            if (b >= B || prev_s[rb] < 0) continue;  // uniform over the block
-            const size_t row = (size_t)b * G + j;
-            const float2 c2 = c2_s[rb];
-            float z[4] = {0.f, 0.f, 0.f, 0.f};
-            if (valid) {
-                const float4 u4 = load4(base + row * V + v);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) z[e] = elem(u4, e) + acc[rb][e];
-                if (z_out) *reinterpret_cast<float4 *>(z_out + row * V + v) = make_float4(z[0], z[1], z[2], z[3]);
-            }
-            if (c2.x > 0.f) {
+        __syncthreads();
+        // phase 2: warp w draws row w over these tokens
+        if (row_on) {
+#pragma unroll 1
+            for (int g = lane; g < kSimtThreads; g += 32) {
+                const int v = vbase + 4 * g;
+                const bool valid = v < ve;
+                float z[4] = {0.f, 0.f, 0.f, 0.f};
                 if (valid) {
-                    const float T = T_s[rb];
-                    const uint4 w = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, rid_s[rb], kStreamDraft),
-                                                  k0, k1);
-                    simt_draw4(st[rb], kbest[rb], z, c2, T, __frcp_rn(T), v, w);
+                    const float4 z4 = *reinterpret_cast<const float4 *>(zs + warp * (4 * kSimtThreads) + 4 * g);
+                    z[0] = z4.x;
+                    z[1] = z4.y;
+                    z[2] = z4.z;
+                    z[3] = z4.w;
                 }
-            } else if (valid) {
+                if (c2w.x > 0.f) {  // uniform over the warp: every lane draws
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (valid)
+                        w = philox4x32_10(make_uint4((uint32_t)v >> 2, (uint32_t)j, rid_w, kStreamDraft), k0, k1);
+                    simt_draw4(st, kbest, z, c2w, T_w, rT_w, v, w, valid);
+                } else if (valid) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) argmax_push(st[rb], z[e], v + e);
+                    for (int e = 0; e < 4; ++e) argmax_push(st, z[e], v + e);
+                }
             }
         }
+        __syncthreads();  // the next tokens' logits overwrite zs
     }
-#pragma unroll
-    for (int rb = 0; rb < kSimtRows; ++rb) {
-        RowState m = block_merge(st[rb], scratch);
-        const int b = b0 + rb;
-        if (threadIdx.x == 0 && b < B) part[(size_t)b * nsplit + seg] = m;
+    if (row_on) {
+        const RowState m = warp_merge(st);
+        if (lane == 0) part[(size_t)b_w * nsplit + seg] = m;
+    } else if (b_w < B && lane == 0) {
+        part[(size_t)b_w * nsplit + seg] = row_state_init();
     }
 }
 
 // One warp per (request, position): merge the segment partials, write token,
 // lse, logq.  Position j0 + k reads its partials at part + k * pos_stride.
 // The token is the largest key word; lse is the partial sums rescaled
-// exactly and added in double, and log q = z_x / T - lse in double, each
-// rounded once to fp32.
+// exactly and added in float-float (about 44 bits), and log q = z_x / T - lse
+// in float-float, each rounded once to fp32.
 __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsplit, size_t pos_stride,
                                       const float *__restrict__ temperature, int B, int G, int j0, int npos,
                                       int32_t *__restrict__ tokens, float *__restrict__ lse,
@@ -187,7 +246,7 @@ __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsp
     const int k = gw / B, b = gw - k * B, j = j0 + k;
     const RowState *pr = part + (size_t)k * pos_stride + (size_t)b * nsplit;
     const float T = temperature[b];
-    const double lse_d = (T > 0.f) ? warp_lse_of_partials(pr, nsplit) : 0.0;
+    const FF lse_ff = (T > 0.f) ? warp_lse_of_partials(pr, nsplit) : FF{0.f, 0.f};
     unsigned long long bw = 0ull;
     float zat = 0.f;
     for (int i = lane; i < nsplit; i += 32)
@@ -214,8 +273,8 @@ __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsp
     }
     tokens[o] = word_token(bw);
     if (T > 0.f) {
-        lse[o] = (float)lse_d;
-        logq[o] = (float)((double)zat / (double)T - lse_d);
+        lse[o] = lse_ff.hi;
+        logq[o] = ff_add(div_ff(zat, T, __frcp_rn(T)), ff_neg(lse_ff)).hi;
     } else {
         lse[o] = zat;
         logq[o] = 0.f;
@@ -226,7 +285,7 @@ __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsp
 
 cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s) {
     const dim3 grid(p.nsplit, p.row_blocks);
-    const size_t smem = sizeof(float) * kSimtRows * (size_t)a.r;
+    const size_t smem = sizeof(float) * kSimtRows * ((size_t)a.r + 4 * kSimtThreads);
     uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
     RowState *part = reinterpret_cast<RowState *>(a.ws + p.partial_offset);
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);

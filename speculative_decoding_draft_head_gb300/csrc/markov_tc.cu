@@ -475,32 +475,6 @@ __device__ __forceinline__ unsigned long long draft_top2_word(const Top2 &tp, fl
     return wb;
 }
 
-// The exact key word of a final-draw contender: token tok with target logit
-// tb, draft logit zb and word wb; 0 when a residual row gives it no mass
-// (p <= q).  key_hi receives the float-float key's high part.  Out of line:
-// it runs for a few tokens per row, and inlined its registers would spill in
-// the sub-slice loop.
-__device__ __noinline__ unsigned long long final_key_word(float tb, float zb, uint32_t wb, int tok, bool bonus,
-                                                          float T, float rT, FF lse_t, float lse_q,
-                                                          float *key_hi) {
-    FF key;
-    if (bonus) {
-        key = div_ff(tb, T, rT);  // t / T: the bonus key before its noise
-    } else {
-        // ln r = ln p + ln(1 - q / p), ln q - ln p formed in float-float from
-        // the logits and the two lse
-        const FF lp = ff_add(div_ff(tb, T, rT), ff_neg(lse_t));
-        const FF dl = ff_add(ff_add(div_ff(zb, T, rT), FF{-lse_q, 0.f}), ff_neg(lp));
-        const float d = dl.hi + dl.lo;
-        if (!(d < 0.f)) return 0ull;  // p <= q: no residual mass
-        const float l1m = (d > -0.6931472f) ? logf(-expm1f(d)) : log1pf(-expf(d));
-        key = ff_add(lp, FF{l1m, 0.f});
-    }
-    key = ff_add(key, gumbel_ff(wb));
-    *key_hi = key.hi;
-    return key_word(key, tok);
-}
-
 // A timed-out CTA, before its shared memory and TMEM are given up: the copies
 // it armed must land (bytes armed but never issued are counted as landed) and
 // the UMMAs it issued must finish; each wait is bounded again.  Out of line:

@@ -151,20 +151,6 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
 }
 
 // ---------------------------------------------------------------- pass 2 ----
-// The natural-log log-sum-exp of one row's partial states (m_i, S_i) in
-// double: the integer references make the rescaling exact.  -inf if empty.
-__device__ __forceinline__ double lse_of_partials(const RowState *part, int n) {
-    float m = -INFINITY;
-    for (int i = 0; i < n; ++i) m = fmaxf(m, part[i].m);
-    if (m == -INFINITY) return -INFINITY;
-    double S = 0.0;
-    for (int i = 0; i < n; ++i) {
-        const RowState &q = part[i];
-        if (q.m != -INFINITY && q.S > 0.f) S += ldexp((double)q.S, (int)fmaxf(q.m - m, -1100.f));
-    }
-    return 0.6931471805599453 * ((double)m + log2(S));
-}
-
 // The greedy argmax of one row from its partials: the largest key word.
 __device__ __forceinline__ unsigned long long best_of_partials(const RowState *part, int n, float *z_at) {
     unsigned long long w = 0ull;
@@ -241,29 +227,31 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
     const uint32_t id = request_id ? request_id[b] : (uint32_t)b;
     // Every tested row at once: lane j merges row j's partials (in segment
     // order), reads the target logit of x_j and decides its acceptance in
-    // double: log p = t_x / T - lse_t, accept iff u < min(1, exp(log p - log q));
-    // the first rejection (or greedy mismatch) is the lowest set bit of a
-    // ballot.  Rows after it were never tested: their outputs stay NaN.
+    // float-float: log p = t_x / T - lse_t, accept iff log p >= log q or
+    // ln u < log p - log q (u < min(1, p / q) without an exponential); the
+    // first rejection (or greedy mismatch) is the lowest set bit of a ballot.
+    // Rows after it were never tested: their outputs stay NaN.
     int k = L, y = -1, d = -1;
     for (int j0 = 0; j0 < L; j0 += 32) {
         const int j = j0 + lane;
         const bool tested = j < L;
         bool pass = true;
         float lse_out = 0.f, logp_out = 0.f;
-        double lse_d = 0.0;
+        FF lse{0.f, 0.f};
         int amax = -1;
         if (tested) {
             const RowState *pr = part + ((size_t)b * (G + 1) + j) * nsplit;
             const int x = draft_tokens[(size_t)b * G + j];
             if (T > 0.f) {
-                lse_d = lse_of_partials(pr, nsplit);
+                lse = lse_of_partials(pr, nsplit);
                 const float tx = to_f32(target_row(target, row0, n_rows, b, G, j, V)[x]);
-                const double logp = (double)tx / (double)T - lse_d;
-                const double logq = (double)draft_logq[(size_t)b * G + j];
+                const FF logp = ff_add(div_ff(tx, T, __frcp_rn(T)), ff_neg(lse));
+                const FF diff = ff_add(logp, FF{-draft_logq[(size_t)b * G + j], 0.f});  // log p - log q
                 const uint4 w4 = philox4x32_10(make_uint4(0u, (uint32_t)j, id, kStreamAccept), k0, k1);
-                pass = (logp >= logq) || ((double)word_to_uniform(w4.x) < exp(logp - logq));
-                lse_out = (float)lse_d;
-                logp_out = (float)logp;
+                // (a normalised float-float has the sign of its high part)
+                pass = diff.hi >= 0.f || ff_add(diff, ff_neg(ln_ff(word_to_uniform(w4.x)))).hi > 0.f;
+                lse_out = lse.hi;
+                logp_out = logp.hi;
             } else {
                 float zmax;
                 const unsigned long long bw = best_of_partials(pr, nsplit, &zmax);
@@ -283,10 +271,7 @@ __global__ void verify_decide_kernel(const TIn *__restrict__ target, const int64
             k = first;
             if (T > 0.f) {
                 d = first;
-                if (j == first) {
-                    const float hi = (float)lse_d;
-                    lse_t_row[b] = make_float2(hi, (float)(lse_d - (double)hi));
-                }
+                if (j == first) lse_t_row[b] = make_float2(lse.hi, lse.lo);
             } else {
                 y = __shfl_sync(0xffffffffu, amax, first - j0);
             }
@@ -349,23 +334,11 @@ __device__ __forceinline__ void final_token_step(unsigned long long &best, float
         k2 = s2 - log2f(neg_log_uniform(w));
     }
     if (!(k2 > K2 - key_tol2(k2, K2))) return;
-    FF key;
-    if (residual) {
-        // ln r = ln p + ln(1 - q / p), ln q - ln p in float-float
-        const FF lp = ff_add(div_ff(t, T, rT), ff_neg(lse_t));
-        const FF dl = ff_add(ff_add(div_ff(z, T, rT), FF{-lse_q, 0.f}), ff_neg(lp));
-        const float d = dl.hi + dl.lo;
-        if (!(d < 0.f)) return;  // p <= q: no residual mass
-        const float l1m = (d > -0.6931472f) ? logf(-expm1f(d)) : log1pf(-expf(d));
-        key = ff_add(lp, FF{l1m, 0.f});
-    } else {
-        key = div_ff(t, T, rT);
-    }
-    key = ff_add(key, gumbel_ff(w));
-    const unsigned long long word = key_word(key, v);
+    float key_hi;
+    const unsigned long long word = final_key_word(t, z, w, v, !residual, T, rT, lse_t, lse_q, &key_hi);
     if (word > best) {
         best = word;
-        kbest = fmaxf(kbest, key.hi);
+        kbest = fmaxf(kbest, key_hi);
     }
 }
 
@@ -567,7 +540,8 @@ VerifyPlan plan_verify(int B, int G, int V, int r, dspark_dtype dt) {
     VerifyPlan p{};
     const long rows = (long)B * (G + 1);
     // target rows: aim for ~8 blocks per SM among the rows that are read
-    // (about half of them with scheduled lengths), segments >= 4096 entries
+    // (about half of them with scheduled lengths), segments >= 4096 entries;
+    // twice as many segments measured slower (dspark5, qwen3, largev)
     long want = (16L * kNumSMs + rows - 1) / rows;
     int max_split = (V + 4095) / 4096;
     int split = (int)(want < 1 ? 1 : (want > max_split ? max_split : want));
