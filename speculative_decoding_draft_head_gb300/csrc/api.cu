@@ -166,6 +166,7 @@ dspark_status dspark_draft_sample(const void *base_logits, const void *e_in, con
     for (int j = 0; j < G; ++j) {
         e = launch_draft_simt(a, plan, j, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft sample launch");
+        if (simt_writes_rows(plan)) continue;
         e = launch_draft_finalize(a, plan, j, 1, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
     }

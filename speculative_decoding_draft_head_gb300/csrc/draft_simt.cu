@@ -84,6 +84,27 @@ __device__ __forceinline__ void simt_draw4(RowState &st, float &kbest, const flo
 
 static_assert(kSimtThreads / 32 == kSimtRows, "one warp draws each row of the block");
 
+// x_j, lse_j and log q_j of one request from its merged draw: bw the largest
+// key word (0: the request was flagged invalid), zat its token's logit, lse_ff
+// the row's log-sum-exp of z/T (T > 0).
+__device__ __forceinline__ void write_draft_row(unsigned long long bw, float zat, FF lse_ff, float T, size_t o,
+                                                int32_t *tokens, float *lse, float *logq) {
+    if (bw == 0ull) {
+        tokens[o] = -1;
+        lse[o] = __int_as_float(0x7fc00000);
+        logq[o] = __int_as_float(0x7fc00000);
+        return;
+    }
+    tokens[o] = word_token(bw);
+    if (T > 0.f) {
+        lse[o] = lse_ff.hi;
+        logq[o] = ff_add(div_ff(zat, T, __frcp_rn(T)), ff_neg(lse_ff)).hi;
+    } else {
+        lse[o] = zat;
+        logq[o] = 0.f;
+    }
+}
+
 // Two phases per 4 kSimtThreads tokens of the segment: every thread forms the
 // logits of four tokens for all rows of the block (the rank-r bias
 // register-tiled over the rows, so each W_out row is read once per block) into
@@ -99,7 +120,8 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
                   const int32_t *__restrict__ tokens, const float *__restrict__ temperature,
                   const uint32_t *__restrict__ request_id, int B, int G, int V, int r, int j,
                   uint32_t k0, uint32_t k1, int chunk, int nsplit, RowState *__restrict__ part,
-                  uint32_t *__restrict__ flags, float *__restrict__ z_out) {
+                  uint32_t *__restrict__ flags, float *__restrict__ z_out, int32_t *__restrict__ tokens_out,
+                  float *__restrict__ lse_out, float *__restrict__ logq_out) {
     extern __shared__ float smem_f[];
     float *a_rows = smem_f;                       // [kSimtRows][r]
     float *zs = smem_f + (size_t)kSimtRows * r;   // [kSimtRows][4 kSimtThreads] logits of the current tokens
@@ -222,11 +244,15 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
         }
         __syncthreads();  // the next tokens' logits overwrite zs
     }
-    if (row_on) {
-        const RowState m = warp_merge(st);
-        if (lane == 0) part[(size_t)b_w * nsplit + seg] = m;
-    } else if (b_w < B && lane == 0) {
-        part[(size_t)b_w * nsplit + seg] = row_state_init();
+    const RowState m = row_on ? warp_merge(st) : row_state_init();
+    if (b_w < B && lane == 0) {
+        if (!tokens_out) {
+            part[(size_t)b_w * nsplit + seg] = m;
+        } else {
+            // one segment covers the row: this warp holds the row's whole draw
+            const FF lse_ff = (row_on && T_w > 0.f) ? lse_of_partials(&m, 1) : FF{0.f, 0.f};
+            write_draft_row(m.best, m.z_at, lse_ff, T_w, (size_t)b_w * G + j, tokens_out, lse_out, logq_out);
+        }
     }
 }
 
@@ -264,28 +290,18 @@ __global__ void draft_finalize_kernel(const RowState *__restrict__ part, int nsp
         }
     }
     if (lane != 0) return;
-    const size_t o = (size_t)b * G + j;
-    if (bw == 0ull) {  // request flagged invalid
-        tokens[o] = -1;
-        lse[o] = __int_as_float(0x7fc00000);
-        logq[o] = __int_as_float(0x7fc00000);
-        return;
-    }
-    tokens[o] = word_token(bw);
-    if (T > 0.f) {
-        lse[o] = lse_ff.hi;
-        logq[o] = ff_add(div_ff(zat, T, __frcp_rn(T)), ff_neg(lse_ff)).hi;
-    } else {
-        lse[o] = zat;
-        logq[o] = 0.f;
-    }
+    write_draft_row(bw, zat, lse_ff, T, (size_t)b * G + j, tokens, lse, logq);
 }
 
 }  // namespace
 
+bool simt_writes_rows(const DraftPlan &p) { return !p.tensor_path && p.nsplit == 1; }
+
 cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s) {
     const dim3 grid(p.nsplit, p.row_blocks);
     const size_t smem = sizeof(float) * kSimtRows * ((size_t)a.r + 4 * kSimtThreads);
+    // one segment per row: the kernel writes x_j, lse_j and log q_j itself
+    const bool direct = simt_writes_rows(p);
     uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
     RowState *part = reinterpret_cast<RowState *>(a.ws + p.partial_offset);
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
@@ -293,12 +309,12 @@ cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cud
         draft_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, smem, s>>>(
             (const __nv_bfloat16 *)a.base, (const __nv_bfloat16 *)a.e_in, (const __nv_bfloat16 *)a.w_out,
             a.anchor, a.tokens, a.temperature, a.request_id, a.B, a.G, a.V, a.r, j, k0, k1, p.chunk,
-            p.nsplit, part, flags, a.z_out);
+            p.nsplit, part, flags, a.z_out, direct ? a.tokens : nullptr, a.lse, a.logq);
     } else {
         draft_simt_kernel<float><<<grid, kSimtThreads, smem, s>>>(
             (const float *)a.base, (const float *)a.e_in, (const float *)a.w_out, a.anchor, a.tokens,
             a.temperature, a.request_id, a.B, a.G, a.V, a.r, j, k0, k1, p.chunk, p.nsplit, part, flags,
-            a.z_out);
+            a.z_out, direct ? a.tokens : nullptr, a.lse, a.logq);
     }
     return cudaGetLastError();
 }

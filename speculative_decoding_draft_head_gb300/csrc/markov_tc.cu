@@ -1040,16 +1040,32 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         // publications below are already in kbest_r)
                         if (active) kr_next = load_relaxed(res_best);
                         if (!__any_sync(0xffffffffu, maybe)) continue;
-                        // the draft logits z = base + bias of this sub-slice (residual rows)
-                        uint4 u_lo = make_uint4(0, 0, 0, 0), u_hi = u_lo;
-                        if (maybe && kind == 1) load16_bf16(urow + v, n, u_lo, u_hi);
-                        // per token: screen with an upper bound of r_v under the
-                        // approximate exponentials; the survivors form a mask
-                        uint32_t mask = 0u;
+                        // per token against p alone (r_v <= p_v, with a margin for the
+                        // approximate exponential; exact for bonus rows): most lanes
+                        // drop out here, before any base value is read
+                        uint32_t pmask = 0u;
                         if (maybe) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 if (i < n) {
+                                    const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -tref));
+                                    if (one_minus_uniform_plus_one(word_at(w, i)) < fmaf(pv * (1.f + 1e-6f), Qg, 1.f))
+                                        pmask |= 1u << i;
+                                }
+                            }
+                        }
+                        if (!__any_sync(0xffffffffu, pmask != 0u)) continue;
+                        // the draft logits z = base + bias of this sub-slice (residual rows)
+                        uint4 u_lo = make_uint4(0, 0, 0, 0), u_hi = u_lo;
+                        if (pmask && kind == 1) load16_bf16(urow + v, n, u_lo, u_hi);
+                        // then per token with an upper bound of r_v = p_v - q_v under the
+                        // approximate exponentials (where p and q are close, most
+                        // tokens stop here); the survivors form a mask
+                        uint32_t mask = 0u;
+                        if (pmask) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if ((pmask >> i) & 1u) {
                                     const float zi = bf16_at(u_lo, u_hi, i) + __uint_as_float(acc[i]);
                                     const float pv = fast_exp2(fmaf(bf16_at(ct_lo, ct_hi, i), c2, -tref));
                                     const float qv = fast_exp2(fmaf(zi, c2, -lse_q2));
@@ -1059,8 +1075,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                                 }
                             }
                         }
-                        // a survivor's fp32 key (log2 units, from the bound, so never
-                        // below the true key by more than rounding)
+                        // a survivor's fp32 key (log2 units) from an upper bound of r_v
+                        // under the approximate exponentials, so never below the true
+                        // key by more than rounding; -inf where the bound is not
+                        // positive (p <= q: no residual mass)
                         auto fp32_key = [&](int i, float &tb, float &zb, uint32_t &wb) {
                             tb = select16_bf16(ct_lo, ct_hi, i);
                             zb = select16_bf16(u_lo, u_hi, i) + __uint_as_float(select16(acc, i));
@@ -1068,7 +1086,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             const float pv = fast_exp2(fmaf(tb, c2, -tref));
                             const float qv = fast_exp2(fmaf(zb, c2, -lse_q2));
                             const float ub = (pv - qv) + 4e-7f * (pv + qv);
-                            return off + fast_log2(ub) - fast_log2(neg_log_uniform(wb));
+                            return ub > 0.f ? off + fast_log2(ub) - fast_log2(neg_log_uniform(wb)) : -INFINITY;
                         };
                         // the survivor with the largest fp32 key goes first, so that its
                         // float-float key raises the row's best before the others are
