@@ -1236,9 +1236,12 @@ cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, in
     cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     const bool tile = (box_cols == 64);
+    // no L2 promotion: the base logits are read once, and promoted sectors
+    // only crowd W_out out of L2 (cold-cache DRAM reads of a dspark5 draft
+    // launch 554 -> 512 MB, same time)
     CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, tile ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
