@@ -205,8 +205,12 @@ def test_minimal_sizes():
     tally.check()
 
 
-def test_invalid_device_inputs_are_flagged_not_read():
-    w = SCALED["tiny"].scaled(B=4)
+@pytest.mark.parametrize("name", ["tiny", "dspark5"])
+def test_invalid_device_inputs_are_flagged_not_read(name):
+    """fp32 weights (SIMT draft writing its rows itself) and bf16 weights
+    (tensor-core draft + finalize): flagged requests get token -1 and NaN lse
+    and log q at every position, the others are drawn."""
+    w = SCALED[name].scaled(B=4, scheduler=False)
     inp = make_inputs(w, 0, device="cuda")
     anchor = inp["anchor"].clone()
     anchor[1] = w.V + 5
@@ -219,6 +223,9 @@ def test_invalid_device_inputs_are_flagged_not_read():
     tok = d["tokens"].cpu().numpy()
     assert np.all(tok[1] == -1) and np.all(tok[2] == -1)
     assert np.all(tok[0] >= 0) and np.all(tok[3] >= 0)
+    lse, logq = d["lse"].cpu().numpy(), d["logq"].cpu().numpy()
+    assert np.all(np.isnan(lse[1:3])) and np.all(np.isnan(logq[1:3]))
+    assert np.all(np.isfinite(lse[[0, 3]])) and np.all(np.isfinite(logq[[0, 3]]))
     vl = torch.tensor([2, 9, 1, 0], dtype=torch.int32, device="cuda")
     wsv = binding.default_workspace(binding.WS_VERIFY, w.B, w.G, w.V, w.r, anchor.device)
     v = binding.verify(inp["target"], inp["base"], inp["e_in"], inp["w_out"], anchor, d, vl, temp, None, 0,
@@ -228,7 +235,8 @@ def test_invalid_device_inputs_are_flagged_not_read():
     acc = v["accept_len"].cpu().numpy()
     assert acc[1] == -1 and acc[2] == -1 and acc[0] >= 0 and acc[3] == 0
     cl = inp["conf_logits"]
-    pt = torch.tensor([1.0, 0.0, 1.0, 1.0], device="cuda")
+    pt = torch.ones(w.G, device="cuda")
+    pt[1] = 0.0  # a position temperature must be > 0
     wss = binding.default_workspace(binding.WS_SCHEDULE, w.B, w.G, 8, 1, anchor.device)
     binding.schedule_prefix(cl, pt, inp["sps"], 1, w.G, workspace=wss)
     assert binding.read_device_flags(wss) & binding.FLAG_BAD_POS_TEMP
