@@ -22,8 +22,8 @@
 //    rejected at position d (draw from max(0, p_d - q_d), q rebuilt from base
 //    logits + Markov bias) or accepted its whole block (bonus draw from p_L);
 //    other rows idle.  Target rows stream by cp.async into per-thread slots
-//    three sub-slices ahead; base rows are read only where a group passes the
-//    bound test.
+//    three sub-slices ahead; base values are read only for lanes with a token
+//    that passes the per-token test against p.
 //
 // CTA layout (one CTA per SM, 480 threads, ~200 KB shared memory):
 //   warps 0-11  epilogue: warp w reads TMEM lanes 32*(w%4).. (its quadrant of
@@ -191,7 +191,7 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
 
 __device__ __forceinline__ int seg_begin(int s, int nseg, int V) {
     if (s >= nseg) return V;
-    return (int)(((long long)s * V / nseg) & ~15LL);  // whole 16-token draw groups
+    return (int)(((long long)s * V / nseg) & ~15LL);  // whole 16-token sub-slices
 }
 
 __device__ __forceinline__ bool uniform_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
