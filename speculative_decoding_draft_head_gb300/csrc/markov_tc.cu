@@ -502,7 +502,9 @@ __device__ __noinline__ void drain_ummas(uint32_t bar, volatile int *never) {
 // TMEM A operand and release the MMA warps (a_ready), while the producer has
 // already been streaming the next position's W_out and base-logit tiles.
 // Tile, ring and accumulator counters run on across positions.
-template <bool kFinal>
+// kQuad: the four-replica form (batches of at most 32 requests), in which
+// epilogue warps also pass the tiles where they have no sub-slice.
+template <bool kFinal, bool kQuad>
 __global__ void __maxnreg__(kMaxRegs)
 markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
                  const __grid_constant__ TcParams p) {
@@ -570,7 +572,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         }
         for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), 32 / p.rep);  // one arrival per 16-column sub-slice each quadrant processes
+            // one arrival per 16-column sub-slice each quadrant processes; in the
+            // four-replica form one per epilogue warp and tile
+            mbar_init(tempty(a), kQuad ? kEpiWarps : 32 / p.rep);
         }
         mbar_init(a_ready, kEpiWarps);
         mbar_init(drain(0), 1);
@@ -779,10 +783,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const int rq = row % rows_q;  // the request slot of this row (replicas share it)
         const int b = m0 + rq;
         // this quadrant's share of each tile's 8 column blocks: spt = 8 / rep
-        // consecutive blocks from cb0 (shifts: rep is 1 or 2)
-        const int spt_sh = (p.rep == 2) ? 2 : 3;
+        // consecutive blocks from cb0; a replica spans 4 / rep whole quadrants
+        // (rep is 1 or 2; kQuad: 4, one replica per quadrant)
+        const int spt_sh = kQuad ? 1 : (p.rep == 2) ? 2 : 3;
         const int spt = 1 << spt_sh;
-        const int cb0 = (p.rep == 2) ? (q >> 1) * 4 : 0;
+        const int cb0 = kQuad ? q * 2 : (p.rep == 2) ? (q >> 1) * 4 : 0;
         const float c2 = row_c2[row];
         const float c2l = row_c2l[row];
         const float Trow = row_T[row];
@@ -794,6 +799,22 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const uint32_t stream = kFinal ? (kind == 1 ? kStreamResidual : kStreamBonus) : kStreamDraft;
 
         bool ok = true;
+        // With one or two replicas every epilogue warp has a sub-slice in every
+        // tile (a quadrant's share is 8 or 4 sub-slices for kEpiPerQuad = 3
+        // warps) and hands back each one.  With four replicas (kQuad) a
+        // quadrant's share of a tile is two sub-slices for three warps, so every
+        // warp takes part in every tile, in order: it waits for the tile's
+        // accumulator and hands it back once (one arrival per warp), also for a
+        // tile in which it has no sub-slice.  Either way the UMMAs never run more
+        // than one phase of an accumulator ahead of any warp, and no parity wait
+        // can alias.  waited_g: the last tile (counted over all positions) this
+        // warp has waited for.
+        int waited_g = -1;
+        auto pass_tile = [&](int tw) {  // wait for tile tw and hand it straight back
+            const bool r = uniform_wait(tfull(tw % kAccBufs), (uint32_t)(tw / kAccBufs) & 1u, abort);
+            if (r && lane == 0) mbar_arrive(tempty(tw % kAccBufs));
+            return r;
+        };
         for (int pi = 0; pi < npos && ok; ++pi) {
             const int jj = kFinal ? 0 : p.j + pi;
             // ---- A operand of this position: TMEM lane = request row, K in
@@ -930,7 +951,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     if (t != waited) {
                         // a new tile: draw the words while its UMMAs may still run
                         draw_words();
-                        if (!uniform_wait(tfull(a), aph, abort)) {
+                        bool w_ok = true;
+                        if (kQuad)
+                            for (int tw = waited_g + 1; tw < tg && w_ok; ++tw) w_ok = pass_tile(tw);  // no sub-slice
+                        if (!w_ok || !uniform_wait(tfull(a), aph, abort)) {
                             if (lane == 0) {
                                 *abort = 1;
                                 atomicOr(p.flags, kFlagTimeout);
@@ -940,6 +964,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         }
                         tc_fence_after();
                         waited = t;
+                        if (kQuad) waited_g = tg;
                         tmem_ld16(taddr, acc);
                     } else {
                         // the tile is ready: issue the TMEM load, draw under its latency
@@ -947,10 +972,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         draw_words();
                     }
                     tmem_ld_wait16(acc);
-                    // this sub-slice is in registers: hand its part of the accumulator back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty(a));
+                    // this sub-slice (kQuad: this warp's last of the tile) is in
+                    // registers: hand its part of the accumulator back
+                    if (!kQuad || si + kEpiPerQuad >= nsub || ((si + kEpiPerQuad) >> spt_sh) != t) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty(a));
+                    }
                     const int v = vw;
                     const int n = min(16, ve - v);
                     if (!kFinal) {
@@ -1130,6 +1158,19 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                     }
                 }
             }
+            // the position's last tiles in which this warp has no sub-slice (or all
+            // of them, for a warp with none in this position)
+            for (int tw = waited_g + 1; kQuad && ok && tw < (pi + 1) * ntiles; ++tw) {
+                if (pass_tile(tw)) {
+                    waited_g = tw;
+                } else {
+                    if (lane == 0) {
+                        *abort = 1;
+                        atomicOr(p.flags, kFlagTimeout);
+                    }
+                    ok = false;
+                }
+            }
             // no copy may still be landing in the target slots (a timed-out
             // warp leaves the loop early)
             if (kFinal) cp_async_wait_all();
@@ -1245,13 +1286,22 @@ cudaError_t make_u_map(CUtensorMap *m, const void *base, int B, int G, int V, in
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kFinal>
+template <bool kFinal, bool kQuad>
 cudaError_t set_smem_attr() {
     static PerDeviceOnce once;
     return once.run([] {
-        return cudaFuncSetAttribute(markov_tc_kernel<kFinal>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(markov_tc_kernel<kFinal, kQuad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kSmemBytes);
     });
+}
+// the kernel form for a row replication (four replicas: kQuad)
+template <bool kFinal>
+auto tc_kernel(int rep) -> decltype(&markov_tc_kernel<kFinal, false>) {
+    return rep == 4 ? &markov_tc_kernel<kFinal, true> : &markov_tc_kernel<kFinal, false>;
+}
+template <bool kFinal>
+cudaError_t set_smem_attrs(int rep) {
+    return rep == 4 ? set_smem_attr<kFinal, true>() : set_smem_attr<kFinal, false>();
 }
 
 PhiloxRoundKeys round_keys(uint64_t seed) {
@@ -1271,12 +1321,12 @@ PhiloxRoundKeys round_keys(uint64_t seed) {
 int tc_row_blocks(int B) { return (B + BM - 1) / BM; }
 
 // Row replication of the tensor-core kernels: a batch of at most 64 requests
-// fills the 128 accumulator rows twice.  At most 8 / kEpiPerQuad replicas:
-// each epilogue warp must take part in every tile (its quadrant's share of
-// the tile has at least kEpiPerQuad sub-slices), or it would skip phases of
-// the accumulators' mbarriers and a later parity wait could alias.
-int tc_row_replication(int B) { return B <= 64 ? 2 : 1; }
-static_assert(kEpiPerQuad <= 4, "two replicas give each warp of a quadrant a sub-slice of every tile");
+// fills the 128 accumulator rows twice, one of at most 32 four times, each
+// replica taking its share of every tile's column blocks.  A replica spans
+// whole TMEM lane quadrants (one TMEM load reads the same columns for all 32
+// lanes of a warp), so at most 4.  A warp whose quadrant share of a tile holds
+// no sub-slice for it still waits on that tile's accumulator phase.
+int tc_row_replication(int B) { return B <= 32 ? 4 : (B <= 64 ? 2 : 1); }
 
 int tc_segments(int B, int V) {
     const int mb = tc_row_blocks(B);
@@ -1305,7 +1355,7 @@ int coop_capacity() {
         int coop = 0, sms = 0, per_sm = 0;
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, markov_tc_kernel<false>, kThreads,
+        if (coop && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, markov_tc_kernel<false, false>, kThreads,
                                                                  kSmemBytes) == cudaSuccess)
             cached[dev] = per_sm * sms;
         else
@@ -1325,7 +1375,7 @@ cudaError_t draft_setup(const DraftArgs &a, const DraftPlan &pl, CUtensorMap *mw
     if (e != cudaSuccess) return e;
     const int rep = tc_row_replication(a.B);
     if ((e = make_u_map(mu, a.base, a.B, a.G, a.V, 64, BM / rep)) != cudaSuccess) return e;
-    if ((e = set_smem_attr<false>()) != cudaSuccess) return e;
+    if ((e = set_smem_attrs<false>(rep)) != cudaSuccess) return e;
     p = TcParams{};
     p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
     p.base = static_cast<const __nv_bfloat16 *>(a.base);
@@ -1361,7 +1411,7 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStr
         p.j = 0;
         p.j_end = a.G;
         void *args[] = {(void *)&mw, (void *)&mu, (void *)&p};
-        e = cudaLaunchCooperativeKernel((const void *)markov_tc_kernel<false>, grid, dim3(kThreads), args, kSmemBytes,
+        e = cudaLaunchCooperativeKernel((const void *)tc_kernel<false>(p.rep), grid, dim3(kThreads), args, kSmemBytes,
                                         s);
         if (e != cudaErrorCooperativeLaunchTooLarge) return e;
         cudaGetLastError();  // not resident after all: one launch per position
@@ -1369,7 +1419,7 @@ cudaError_t launch_draft_tensor(const DraftArgs &a, const DraftPlan &pl, cudaStr
     for (int j = 0; j < a.G; ++j) {
         p.j = j;
         p.j_end = j + 1;
-        markov_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(mw, mu, p);
+        tc_kernel<false>(p.rep)<<<grid, kThreads, kSmemBytes, s>>>(mw, mu, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -1396,14 +1446,15 @@ cudaError_t launch_draft_tensor_rows(const DraftArgs &a, const DraftPlan &pl, in
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, markov_tc_kernel<false>, mw, mu, p);
+    return cudaLaunchKernelEx(&cfg, tc_kernel<false>(p.rep), mw, mu, p);
 }
 
 cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     CUtensorMap mw;
     cudaError_t e = make_w_map(&mw, a.w_out, a.V, a.r);
     if (e != cudaSuccess) return e;
-    if ((e = set_smem_attr<true>()) != cudaSuccess) return e;
+    const int rep = tc_row_replication(a.B);
+    if ((e = set_smem_attrs<true>(rep)) != cudaSuccess) return e;
     TcParams p{};
     p.e_in = static_cast<const __nv_bfloat16 *>(a.e_in);
     p.base = static_cast<const __nv_bfloat16 *>(a.base);
@@ -1422,7 +1473,7 @@ cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     p.V = a.V;
     p.r = a.r;
     p.j = 0;
-    p.rep = tc_row_replication(a.B);
+    p.rep = rep;
     p.pass = a.pass;
     p.nseg = a.nseg;
     p.keys = round_keys(a.seed);
@@ -1430,7 +1481,7 @@ cudaError_t launch_final_tensor(const FinalArgs &a, cudaStream_t s) {
     p.res_best = a.res_best;
     p.flags = a.flags;
     // the final draw reads its base rows directly: map_u is unused
-    return launch_dependent(markov_tc_kernel<true>, dim3(a.nseg, tc_row_blocks(a.B)), dim3(kThreads), kSmemBytes, s,
+    return launch_dependent(tc_kernel<true>(rep), dim3(a.nseg, tc_row_blocks(a.B)), dim3(kThreads), kSmemBytes, s,
                             mw, mw, p);
 }
 
