@@ -163,10 +163,14 @@ dspark_status dspark_draft_sample(const void *base_logits, const void *e_in, con
         if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
         return DSPARK_OK;
     }
+    if (simt_writes_rows(plan)) {  // one segment per row: every position in one launch
+        e = launch_draft_simt(a, plan, 0, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draft sample launch");
+        return DSPARK_OK;
+    }
     for (int j = 0; j < G; ++j) {
         e = launch_draft_simt(a, plan, j, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft sample launch");
-        if (simt_writes_rows(plan)) continue;
         e = launch_draft_finalize(a, plan, j, 1, s);
         if (e != cudaSuccess) return cuda_fail(e, "draft finalize launch");
     }

@@ -121,11 +121,12 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
                   const uint32_t *__restrict__ request_id, int B, int G, int V, int r, int j,
                   uint32_t k0, uint32_t k1, int chunk, int nsplit, RowState *__restrict__ part,
                   uint32_t *__restrict__ flags, float *__restrict__ z_out, int32_t *__restrict__ tokens_out,
-                  float *__restrict__ lse_out, float *__restrict__ logq_out) {
+                  float *__restrict__ lse_out, float *__restrict__ logq_out, int j_end) {
     extern __shared__ float smem_f[];
     float *a_rows = smem_f;                       // [kSimtRows][r]
     float *zs = smem_f + (size_t)kSimtRows * r;   // [kSimtRows][4 kSimtThreads] logits of the current tokens
     __shared__ int prev_s[kSimtRows];
+    __shared__ int next_s[kSimtRows];             // each row's token of the position just drawn
     __shared__ float2 c2_s[kSimtRows];
     __shared__ float T_s[kSimtRows];
     __shared__ uint32_t rid_s[kSimtRows];
@@ -133,13 +134,18 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
     const int b0 = blockIdx.y * kSimtRows;
     const int seg = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Positions j0 .. j_end - 1: more than one only when this block's segment
+    // covers the whole row (tokens_out set), so the block draws each next token
+    // itself; it passes it on through shared memory (tokens is read-only here).
+    const int j0 = j;
+    for (j = j0; j < j_end; ++j) {
     if (threadIdx.x < kSimtRows) {
         const int b = b0 + threadIdx.x;
         int prev = -1;
         float2 c2 = make_float2(0.f, 0.f);
         uint32_t id = 0;
         if (b < B) {
-            prev = (j == 0) ? anchor[b] : tokens[(size_t)b * G + j - 1];
+            prev = (j == 0) ? anchor[b] : (j > j0 ? next_s[threadIdx.x] : tokens[(size_t)b * G + j - 1]);
             const float T = temperature[b];
             id = request_id ? request_id[b] : (uint32_t)b;
             const bool bad_prev = prev < 0 || prev >= V;
@@ -252,7 +258,10 @@ draft_simt_kernel(const TIn *__restrict__ base, const TIn *__restrict__ e_in,
             // one segment covers the row: this warp holds the row's whole draw
             const FF lse_ff = (row_on && T_w > 0.f) ? lse_of_partials(&m, 1) : FF{0.f, 0.f};
             write_draft_row(m.best, m.z_at, lse_ff, T_w, (size_t)b_w * G + j, tokens_out, lse_out, logq_out);
+            next_s[warp] = word_token(m.best);  // -1 for a flagged request
         }
+    }
+    __syncthreads();  // next_s is complete; prev_s, a_rows and zs may be overwritten
     }
 }
 
@@ -300,8 +309,10 @@ bool simt_writes_rows(const DraftPlan &p) { return !p.tensor_path && p.nsplit ==
 cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s) {
     const dim3 grid(p.nsplit, p.row_blocks);
     const size_t smem = sizeof(float) * kSimtRows * ((size_t)a.r + 4 * kSimtThreads);
-    // one segment per row: the kernel writes x_j, lse_j and log q_j itself
+    // one segment per row: the kernel writes x_j, lse_j and log q_j itself,
+    // and walks every position from j in one launch
     const bool direct = simt_writes_rows(p);
+    const int j_end = direct ? a.G : j + 1;
     uint32_t *flags = reinterpret_cast<uint32_t *>(a.ws);
     RowState *part = reinterpret_cast<RowState *>(a.ws + p.partial_offset);
     const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFu), k1 = (uint32_t)(a.seed >> 32);
@@ -309,12 +320,12 @@ cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cud
         draft_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, smem, s>>>(
             (const __nv_bfloat16 *)a.base, (const __nv_bfloat16 *)a.e_in, (const __nv_bfloat16 *)a.w_out,
             a.anchor, a.tokens, a.temperature, a.request_id, a.B, a.G, a.V, a.r, j, k0, k1, p.chunk,
-            p.nsplit, part, flags, a.z_out, direct ? a.tokens : nullptr, a.lse, a.logq);
+            p.nsplit, part, flags, a.z_out, direct ? a.tokens : nullptr, a.lse, a.logq, j_end);
     } else {
         draft_simt_kernel<float><<<grid, kSimtThreads, smem, s>>>(
             (const float *)a.base, (const float *)a.e_in, (const float *)a.w_out, a.anchor, a.tokens,
             a.temperature, a.request_id, a.B, a.G, a.V, a.r, j, k0, k1, p.chunk, p.nsplit, part, flags,
-            a.z_out, direct ? a.tokens : nullptr, a.lse, a.logq);
+            a.z_out, direct ? a.tokens : nullptr, a.lse, a.logq, j_end);
     }
     return cudaGetLastError();
 }

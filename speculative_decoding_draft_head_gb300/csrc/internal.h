@@ -99,8 +99,9 @@ struct DraftArgs {
     unsigned char *ws;
 };
 cudaError_t launch_draft_simt(const DraftArgs &a, const DraftPlan &p, int j, cudaStream_t s);
-// whether the SIMT launch of a position writes its tokens, lse and log q
-// itself (one vocabulary segment per row: no finalize launch)
+// whether the SIMT launch writes its tokens, lse and log q itself (one
+// vocabulary segment per row: no finalize launch, and one launch from position
+// j to the last)
 bool simt_writes_rows(const DraftPlan &p);
 // merges the partials of positions j .. j + npos - 1 into tokens, lse and log q
 cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j, int npos, cudaStream_t s);
