@@ -502,8 +502,9 @@ def run_ours(args, w):
     s_ms = statistics.median(call_ms["sched"])
     dominant = "draft" if d_ms >= v_ms else "verify"
     # the bf16 draft runs one launch for all positions (+ finalize); fp32 weights
-    # take the SIMT kernel, one launch pair per position
-    launches_draft = 2 if w.dtype == "bf16" else 2 * G
+    # take the SIMT kernel: one launch pair per position, or one launch for all
+    # positions when a single vocabulary segment covers each row
+    launches_draft = 2 if w.dtype == "bf16" else _simt_draft_launches(B, G, V)
     dom_bytes = draft_bytes if dominant == "draft" else verify_bytes + residual_bytes
     dom_ms = d_ms if dominant == "draft" else v_ms
     # draft: one (cooperative) launch of the Markov-head kernel for all block
@@ -579,6 +580,16 @@ def run_ours(args, w):
         h = {k: t.cpu() for k, t in inp.items()}
         line["cpu_baseline"] = cpu_baseline_line(w, h, args.seed, args.cpu_budget)
     print(json.dumps(line))
+
+
+def _simt_draft_launches(B, G, V):
+    """Launches of a draft call with fp32 weights: one per position and its
+    finalize, or a single launch for all positions when one vocabulary
+    segment covers each row (the library's SIMT plan: 8 requests per block,
+    about two blocks per SM, segments of at least 1024 tokens)."""
+    row_blocks = (B + 7) // 8
+    nsplit = max(1, min((2 * 152 + row_blocks - 1) // row_blocks, (V + 1023) // 1024))
+    return 1 if nsplit == 1 else 2 * G
 
 
 def _read_traffic(w, kernel):
