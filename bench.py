@@ -380,6 +380,27 @@ def run_ours(args, w):
     flags = dict(draft=binding.read_device_flags(ws_d), verify=binding.read_device_flags(ws_v))
     if any(flags.values()):
         raise RuntimeError("device flags raised in the timed region: %s" % flags)
+    # the spread of single rounds: a separate pass after the timed region, one
+    # event pair around each round (events recorded back to back, no sync)
+    n_spread = min(args.steps, 100)
+    sp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(n_spread)]
+    for a, b in sp_ev:
+        a.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            step(inp)
+        b.record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(a.elapsed_time(b) for a, b in sp_ev)
+
+    def _pct(q):
+        return per_step[min(len(per_step) - 1, int(q * len(per_step)))]
+
+    step_spread = dict(n=n_spread, min=per_step[0], p10=_pct(0.1), median=_pct(0.5), p90=_pct(0.9),
+                       max=per_step[-1],
+                       note="ms per round, one event pair around each round, a pass after the timed region")
     ms_max = _max_over_ranks(ms, world)
     total_positions = _sum_over_ranks(positions, world)
     value = total_positions / (ms_max / 1000.0)
@@ -556,6 +577,7 @@ def run_ours(args, w):
                             "over the call time against the measured copy bandwidth; alu = Philox "
                             "blocks (one per four drawn tokens) over the call time against the "
                             "device's measured Philox rate; bound = the roof with the longer floor"),
+        step_ms=step_spread,
         calls_ms=dict(draft=d_ms, schedule=s_ms, verify=v_ms),
         step_order=("draft, schedule, verify on one stream" +
                     (", replayed from one CUDA graph (calls_ms timed eagerly)" if graph is not None else "")),

@@ -244,16 +244,15 @@ dspark_status dspark_schedule_policy(const float *conf_logits, const float *pos_
         return fail(DSPARK_ERR_INVALID_ARG, "sps_len must be >= B*(L_max+1)+1 = %ld", (long)B * (L_max + 1) + 1);
     if (!conf_logits || !pos_temp || !sps || !conf || !cum_conf || !verify_len)
         return fail(DSPARK_ERR_INVALID_ARG, "a required pointer is NULL");
-    if (schedule_smem_bytes(B, G, L_min, L_max) > 200 * 1024)
+    if (schedule_smem_bytes(B, G, L_min, L_max) > (size_t)kScheduleMaxSmem)
         return fail(DSPARK_ERR_UNSUPPORTED, "too many scheduler candidates");
     dspark_status st = check_ws(workspace, workspace_bytes, kFlagBytes);
     if (st != DSPARK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    // (the kernel clears the flag words itself)
     ScheduleArgs a{conf_logits, pos_temp, sps, sps_len, B, G, L_min, L_max, conf, cum_conf, verify_len,
                    theta_out, static_cast<unsigned char *>(workspace), policy, threshold};
-    e = launch_schedule(a, s);
+    const cudaError_t e = launch_schedule(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
     return DSPARK_OK;
 }

@@ -216,6 +216,7 @@ struct ScheduleArgs {
     float threshold;   // policies 2 and 3
 };
 constexpr int kScheduleMaxCells = 16384;  // B * G
+constexpr int kScheduleMaxSmem = 200 * 1024;  // dynamic shared memory of the scheduler's block, at most
 size_t schedule_smem_bytes(int B, int G, int L_min, int L_max);
 cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s);
 

@@ -20,11 +20,14 @@
 //  1. c, a per request in fp32 (a fixed left-to-right product); policies 2-3
 //     decide the lengths here and skip to 5;
 //  2. tau_0 and the candidate list (a, j, b) for L_min <= j < L_max;
-//  3. bitonic sort in shared memory by (a desc, j asc, b asc);
+//  3. sort by (a desc, j asc, b asc): E <= 8 keys per thread in registers,
+//     a bitonic network within each warp, then merge levels through shared
+//     memory (a bitonic network in shared memory beyond 8192 candidates);
 //  4. block prefix sum of a in float-float, Theta before / after each admission, and
 //     the first candidate whose admission does not raise Theta (policy 0,
 //     block min) or the count with the largest Theta (policy 1, block argmax);
 //  5. scatter the admitted counts into the verify lengths, Theta of the result.
+#include <algorithm>
 #include <climits>
 
 #include "device_common.cuh"
@@ -34,6 +37,8 @@ namespace dspark {
 namespace {
 
 constexpr int kSchedThreads = 1024;
+// keys per thread of the register sort, at most (more sort in shared memory)
+constexpr int kSortRegE = 8;
 
 // Sort key of a candidate: a >= 0 is fp32, so its bit pattern orders like
 // its value; (~bits) puts larger a first, the payload j * B + b breaks ties
@@ -152,6 +157,110 @@ __device__ void block_argmax(ff &v, int &n, ff *redv, int *redn) {
     }
 }
 
+__device__ __forceinline__ void prefetch_l1(const float *p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+
+// (a, b) <- (min, max) when up, else (max, min)
+__device__ __forceinline__ void cmpx(unsigned long long &a, unsigned long long &b, bool up) {
+    const unsigned long long lo = min(a, b), hi = max(a, b);
+    a = up ? lo : hi;
+    b = up ? hi : lo;
+}
+
+// Ascending sort of key[0 .. E * blockDim.x) (padding included), E consecutive
+// keys per thread (thread t holds keys t E .. t E + E - 1):
+//  1. each warp sorts its 32 E keys in registers with a bitonic network
+//     (partners within a thread swapped in registers, across lanes by
+//     shuffle), every warp's run ascending;
+//  2. five merge levels through shared memory join the 32 runs: at run length
+//     L each thread finds where its E outputs start on the merge path of its
+//     pair of runs (a binary search over the diagonal, ties taken from the
+//     first run) and merges E keys from there.
+// key[] holds the sorted keys on return.
+template <int E>
+__device__ void sort_keys(unsigned long long *key) {
+    constexpr int n = E * kSchedThreads;
+    const int t = threadIdx.x, lane = t & 31;
+    unsigned long long v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = key[t * E + e];
+    // 1. bitonic sort of the warp's run (index lane E + e within the run)
+#pragma unroll
+    for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
+        for (int jj = k >> 1; jj >= E; jj >>= 1) {
+            const int d = jj / E;  // partner lane distance
+            const bool take_min = (((lane * E) & k) == 0) == ((lane & d) == 0);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[e], d);
+                v[e] = take_min ? min(v[e], o) : max(v[e], o);
+            }
+        }
+#pragma unroll
+        for (int jl = E >> 1; jl >= 1; jl >>= 1) {
+            if (jl < k) {
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    if ((e & jl) == 0) cmpx(v[e], v[e | jl], ((lane * E + e) & k) == 0);
+            }
+        }
+    }
+    // 2. merge levels
+#pragma unroll 1
+    for (int L = 32 * E; L < n; L <<= 1) {
+        __syncthreads();  // the previous level's reads are done
+#pragma unroll
+        for (int e = 0; e < E; ++e) key[t * E + e] = v[e];
+        __syncthreads();
+        const int base = (t * E) & ~(2 * L - 1);  // the pair of runs [base, base + L), [base + L, base + 2 L)
+        const int diag = t * E - base;
+        const unsigned long long *ra = key + base, *rb = key + base + L;
+        int lo = max(0, diag - L), hi = min(diag, L);
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (ra[mid] <= rb[diag - 1 - mid]) lo = mid + 1;
+            else hi = mid;
+        }
+        int i = lo, j = diag - lo;
+        unsigned long long ka = ra[min(i, L - 1)], kb = rb[min(j, L - 1)];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const bool take_a = j >= L || (i < L && ka <= kb);
+            v[e] = take_a ? ka : kb;
+            if (e + 1 < E) {
+                if (take_a) ka = ra[min(++i, L - 1)];
+                else kb = rb[min(++j, L - 1)];
+            }
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) key[t * E + e] = v[e];
+    __syncthreads();
+}
+
+// A bitonic network on keys in shared memory, one compare-exchange per thread
+// and loop step, a block barrier per stage: for more than kSortRegE keys per
+// thread, where the register form would spill.
+__device__ void bitonic_sort_shared(unsigned long long *key, int n) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int ixj = i ^ jj;
+                if (ixj > i) {
+                    const unsigned long long ki = key[i], kx = key[ixj];
+                    const bool up = (i & k) == 0;
+                    if (up ? (kx < ki) : (ki < kx)) {
+                        key[i] = kx;
+                        key[ixj] = ki;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kSchedThreads)
 schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__ pos_temp,
                 const float *__restrict__ sps, int B, int G, int L_min, int L_max, int npow2, int policy,
@@ -159,11 +268,13 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
                 int32_t *__restrict__ verify_len, double *__restrict__ theta_out,
                 uint32_t *__restrict__ flags) {
     extern __shared__ unsigned long long smem[];
-    unsigned long long *key = smem;                       // [npow2] sort keys
-    int *len_s = reinterpret_cast<int *>(key + npow2);    // [B]
+    // the sort runs over nsort keys: the candidates' power of two, at least one per thread
+    const int nsort = max(npow2, kSchedThreads);
+    unsigned long long *key = smem;                       // [nsort] sort keys
+    int *len_s = reinterpret_cast<int *>(key + nsort);    // [B]
     __shared__ ff red[32];
     __shared__ int redn[32];
-    __shared__ unsigned long long xch[kSchedThreads];  // register-sort exchange
+    __shared__ float pt_s[kMaxG];  // position temperatures
     __shared__ int first_fail;
     __shared__ int bad_temp;
 
@@ -174,9 +285,12 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
         first_fail = ncand;
         bad_temp = 0;
     }
+    // the call's flag words start clear (this block is their only writer)
+    if (tid < (int)(kFlagBytes / sizeof(uint32_t))) flags[tid] = 0u;
     __syncthreads();
     for (int j = tid; j < G; j += blockDim.x) {
         const float T = pos_temp[j];
+        pt_s[j] = T;
         if (!(T > 0.f) || isinf(T)) atomicOr(&bad_temp, 1);
     }
     __syncthreads();
@@ -199,21 +313,30 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
         ff t = ff_make(1.f);
         int L = L_min;
         bool run = true;
-        for (int j = 0; j < G; ++j) {
-            const float l = conf_logits[(size_t)b * G + j];
-            const float c = 1.f / (1.f + expf(-l / pos_temp[j]));
-            prod *= c;
-            conf[(size_t)b * G + j] = c;
-            cum_conf[(size_t)b * G + j] = prod;
-            if (policy >= 2) {
-                if (run && j >= L_min && j < L_max) {
-                    run = (policy == 2 ? prod : c) > threshold;
-                    if (run) L = j + 1;
+        const float *lrow = conf_logits + (size_t)b * G;
+        // the row's logits eight at a time (the loads in flight together)
+        for (int j0 = 0; j0 < G; j0 += 8) {
+            float lg[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) lg[u] = (j0 + u < G) ? lrow[j0 + u] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                if (j >= G) break;
+                const float c = 1.f / (1.f + expf(-lg[u] / pt_s[j]));
+                prod *= c;
+                conf[(size_t)b * G + j] = c;
+                cum_conf[(size_t)b * G + j] = prod;
+                if (policy >= 2) {
+                    if (run && j >= L_min && j < L_max) {
+                        run = (policy == 2 ? prod : c) > threshold;
+                        if (run) L = j + 1;
+                    }
+                    if (j < L) t = ff_add_f(t, prod);
+                } else {
+                    if (j < L_min) t = ff_add_f(t, prod);
+                    if (j >= L_min && j < L_max) key[b * width + (j - L_min)] = cand_key(prod, j * B + b);
                 }
-                if (j < L) t = ff_add_f(t, prod);
-            } else {
-                if (j < L_min) t = ff_add_f(t, prod);
-                if (j >= L_min && j < L_max) key[b * width + (j - L_min)] = cand_key(prod, j * B + b);
             }
         }
         tau_part = ff_add(tau_part, t);
@@ -227,56 +350,26 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
         if (tid == 0 && theta_out) *theta_out = ff_to_double(tau) * (double)sps[(long)tok.hi];
         return;
     }
-    for (int i = ncand + tid; i < npow2; i += blockDim.x) key[i] = ~0ull;
+    for (int i = ncand + tid; i < nsort; i += blockDim.x) key[i] = ~0ull;
     const ff tau0 = block_sum(tau_part, red);
     __syncthreads();
 
     // 3. bitonic sort: highest priority first (ascending keys)
-    if (npow2 <= kSchedThreads) {
-        // one key per thread (padding sorts last): partners closer than a warp
-        // are exchanged by shuffle, the others through shared memory
-        unsigned long long kv = (tid < npow2) ? key[tid] : ~0ull;
-        for (int k = 2; k <= kSchedThreads; k <<= 1) {
-            for (int jj = k >> 1; jj > 0; jj >>= 1) {
-                unsigned long long other;
-                if (jj >= 32) {
-                    __syncthreads();
-                    xch[tid] = kv;
-                    __syncthreads();
-                    other = xch[tid ^ jj];
-                } else {
-                    other = __shfl_xor_sync(0xffffffffu, kv, jj);
-                }
-                const bool up = (tid & k) == 0, lower = (tid & jj) == 0;
-                kv = (up == lower) ? min(kv, other) : max(kv, other);
-            }
-        }
-        __syncthreads();
-        if (tid < npow2) key[tid] = kv;
-        __syncthreads();
-    } else {
-        for (int k = 2; k <= npow2; k <<= 1) {
-            for (int jj = k >> 1; jj > 0; jj >>= 1) {
-                for (int i = tid; i < npow2; i += blockDim.x) {
-                    const int ixj = i ^ jj;
-                    if (ixj > i) {
-                        const unsigned long long ki = key[i], kx = key[ixj];
-                        const bool up = (i & k) == 0;
-                        if (up ? (kx < ki) : (ki < kx)) {
-                            key[i] = kx;
-                            key[ixj] = ki;
-                        }
-                    }
-                }
-                __syncthreads();
-            }
-        }
+    switch (nsort / kSchedThreads) {
+        case 1: sort_keys<1>(key); break;
+        case 2: sort_keys<2>(key); break;
+        case 4: sort_keys<4>(key); break;
+        case kSortRegE: sort_keys<kSortRegE>(key); break;
+        default: bitonic_sort_shared(key, nsort); break;
     }
 
     // 4. prefix sums and the first admission that does not raise Theta
     const long n0 = (long)B * (L_min + 1);
     const int per = (ncand + blockDim.x - 1) / blockDim.x;
     const int lo = min(ncand, tid * per), hi = min(ncand, lo + per);
+    // this thread's entries of the SPS table into L1 while the scan runs
+    for (int i = lo; i < hi; ++i) prefetch_l1(sps + n0 + i + 1);
+    if (lo < hi) prefetch_l1(sps + n0 + lo);
     auto a_of = [&](int i) { return __uint_as_float(~(unsigned int)(key[i] >> 32)); };
     ff local = ff_make(0.f);
     for (int i = lo; i < hi; ++i) local = ff_add_f(local, a_of(i));
@@ -332,7 +425,7 @@ size_t schedule_smem_bytes(int B, int G, int L_min, int L_max) {
     const long ncand = (long)B * (L_max - L_min);
     long npow2 = 1;
     while (npow2 < ncand) npow2 <<= 1;
-    return (size_t)npow2 * sizeof(unsigned long long) + sizeof(int) * (size_t)B;
+    return (size_t)std::max(npow2, (long)kSchedThreads) * sizeof(unsigned long long) + sizeof(int) * (size_t)B;
 }
 
 cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
@@ -341,8 +434,15 @@ cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
     int npow2 = 1;
     while (npow2 < ncand) npow2 <<= 1;
     const size_t smem = schedule_smem_bytes(a.B, a.G, a.L_min, a.L_max);
-    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the dynamic shared-memory limit is raised once per device, to the most
+    // the entry points accept
+    static PerDeviceOnce attr;
+    cudaError_t e = attr.run([] {
+        return cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kScheduleMaxSmem);
+    });
     if (e != cudaSuccess) return e;
+    if (smem > (size_t)kScheduleMaxSmem) return cudaErrorInvalidValue;
     schedule_kernel<<<1, kSchedThreads, smem, s>>>(a.conf_logits, a.pos_temp, a.sps, a.B, a.G, a.L_min,
                                                     a.L_max, npow2, a.policy, a.threshold, a.conf, a.cum_conf,
                                                     a.verify_len, a.theta_out, reinterpret_cast<uint32_t *>(a.ws));
