@@ -254,6 +254,18 @@ __device__ __forceinline__ uint32_t word_at(const uint4 (&w)[4], int i) {
     }
 }
 
+// The largest of 16 packed bf16 values (lo: elements 0-7, hi: 8-15), by
+// packed maxima (exact: a maximum needs no rounding).
+__device__ __forceinline__ float max16_bf16(const uint4 &lo, const uint4 &hi) {
+    auto mx = [](uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    };
+    const uint32_t m = mx(mx(mx(lo.x, lo.y), mx(lo.z, lo.w)), mx(mx(hi.x, hi.y), mx(hi.z, hi.w)));
+    return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
 // Element i (a run-time index) of 16 values held in registers: a tree of
 // selects on the bits of i, so the values stay in registers.
 __device__ __forceinline__ float select16(const float (&z)[16], int i) {
@@ -1051,9 +1063,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         // logit alone: every r_v <= p_v <= 2^(t_max c2 - tref).
                         const bool bonus = (kind == 2);
                         float tm = -INFINITY;
+                        if (n == 16) {
+                            tm = max16_bf16(ct_lo, ct_hi);
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (i < n) tm = fmaxf(tm, bf16_at(ct_lo, ct_hi, i));
+                            for (int i = 0; i < 16; ++i)
+                                if (i < n) tm = fmaxf(tm, bf16_at(ct_lo, ct_hi, i));
+                        }
                         const float off = bonus ? tm * c2 : 0.f;
                         const float tref = bonus ? off : lse_t2;
                         if (active) {
