@@ -82,12 +82,11 @@ dspark_status verify_impl(const void *target_logits, const int64_t *target_row0,
     const VerifyPlan plan = plan_verify(B, G, V, r, dtype);
     if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    // (the first launch clears the flag words)
     VerifyArgs a{target_logits, target_row0, n_target_rows, base_logits, e_in, w_out, draft_logits, anchor, draft_tokens, draft_lse,
                  draft_logq, verify_len, temperature, request_id, B, G, V, r, dtype, seed, accept_len,
                  out_tokens, num_out, target_lse, logp_sel, static_cast<unsigned char *>(workspace)};
-    e = launch_verify(a, plan, s);
+    const cudaError_t e = launch_verify(a, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "verify launch");
     return DSPARK_OK;
 }
@@ -148,13 +147,13 @@ dspark_status dspark_draft_sample(const void *base_logits, const void *e_in, con
     const DraftPlan plan = plan_draft(B, G, V, r, dtype);
     if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
+    // the flag words, and on the tensor path the row-wide best words and the
+    // barrier counters after them, in one clear
+    cudaError_t e = cudaMemsetAsync(workspace, 0, plan.clear_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag words, best words and barrier counters");
     DraftArgs a{base_logits, e_in, w_out, anchor, temperature, request_id, B, G, V, r, dtype, seed,
                 draft_tokens, draft_lse, draft_logq, draft_logits, static_cast<unsigned char *>(workspace)};
     if (plan.tensor_path) {
-        e = cudaMemsetAsync(static_cast<unsigned char *>(workspace) + plan.best_offset, 0, plan.clear_bytes, s);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the row-wide best words and barrier counters");
         // the tokens feed the next position through the best words; the
         // partials of every position are merged once at the end
         e = launch_draft_tensor(a, plan, s);
@@ -196,10 +195,9 @@ dspark_status dspark_draft_sample_rnn(const void *base_logits, const void *e_in,
     if ((st = check_ws(workspace, workspace_bytes, plan.ws_bytes)) != DSPARK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    cudaError_t e = cudaMemsetAsync(workspace, 0, kFlagBytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag word");
-    e = cudaMemsetAsync(ws + plan.draft.best_offset, 0, plan.draft.clear_bytes, s);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the row-wide best words");
+    // the flag words, the row-wide best words and the barrier counters in one clear
+    cudaError_t e = cudaMemsetAsync(workspace, 0, plan.draft.clear_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the flag words and best words");
     DraftArgs a{base_logits, e_in, w_out, anchor, temperature, request_id, B, G, V, r, dtype, seed,
                 draft_tokens, draft_lse, draft_logq, draft_logits, ws};
     __nv_bfloat16 *h_ws = reinterpret_cast<__nv_bfloat16 *>(ws + plan.h_offset);

@@ -345,7 +345,6 @@ cudaError_t launch_draft_finalize(const DraftArgs &a, const DraftPlan &p, int j,
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
     (void)r;
     DraftPlan p{};
-    p.partial_offset = kFlagBytes;
     if (dt == DSPARK_BF16) {
         p.tensor_path = true;
         p.rows_per_block = 128;
@@ -366,13 +365,17 @@ DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt) {
         p.nsplit = (V + chunk - 1) / chunk;
         p.chunk = chunk;
     }
+    // flag words, then (tensor path) the best words and barrier counters, so
+    // that one clear of clear_bytes from offset 0 covers all three, then the
+    // partials
     const size_t npart = (size_t)B * p.nsplit * (p.tensor_path ? (size_t)G : 1);
-    p.best_offset = align_up(p.partial_offset + sizeof(RowState) * npart, 256);
+    p.best_offset = kFlagBytes;
     const size_t words = p.tensor_path ? sizeof(unsigned long long) * (size_t)B * (size_t)G : 0;
     p.bar_offset = p.best_offset + words;  // 8-byte aligned
     const size_t bars = p.tensor_path ? sizeof(unsigned int) * (size_t)p.row_blocks : 0;
-    p.clear_bytes = words + bars;
-    p.ws_bytes = align_up(p.bar_offset + bars, 256);
+    p.clear_bytes = p.bar_offset + bars;
+    p.partial_offset = align_up(p.clear_bytes, 256);
+    p.ws_bytes = align_up(p.partial_offset + sizeof(RowState) * npart, 256);
     return p;
 }
 

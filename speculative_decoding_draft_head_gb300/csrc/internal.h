@@ -67,9 +67,9 @@ struct DraftPlan {
     int nsplit;            // vocabulary segments per row (partials per row)
     int chunk;             // vocabulary entries per segment (SIMT; a multiple of 16)
     size_t partial_offset; // byte offset of the per-(row, segment) partials ([G][B][nsplit] on the tensor path)
-    size_t best_offset;    // [G][B] 64-bit row-wide best (key, token) words (tensor path), zeroed per call
-    size_t bar_offset;     // [row_blocks] barrier counters between positions (tensor path), zeroed per call
-    size_t clear_bytes;    // bytes from best_offset to zero per call (words + counters)
+    size_t best_offset;    // [G][B] 64-bit row-wide best (key, token) words (tensor path), right after the flags
+    size_t bar_offset;     // [row_blocks] barrier counters between positions (tensor path), after the words
+    size_t clear_bytes;    // bytes from offset 0 zeroed per call: flag words (+ best words + counters)
     size_t ws_bytes;
 };
 DraftPlan plan_draft(int B, int G, int V, int r, dspark_dtype dt);

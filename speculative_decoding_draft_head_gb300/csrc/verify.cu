@@ -97,8 +97,12 @@ __global__ void __launch_bounds__(kRowThreads)
 verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ row0, int64_t n_rows,
                    const int32_t *__restrict__ verify_len,
                    const float *__restrict__ temperature, int B, int G, int V, int chunk, int nsplit,
-                   RowState *__restrict__ part) {
+                   RowState *__restrict__ part, uint32_t *__restrict__ flags) {
     __shared__ RowState scratch[kRowThreads / 32];
+    // the call's flag words start clear: this pass, the call's first launch,
+    // raises none, and every later launch of the call reads or raises them
+    // only after waiting for the launch before it
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < kFlagBytes / sizeof(uint32_t)) flags[threadIdx.x] = 0u;
     // Unit u = seg * rows + row; launched as (rows, segments), every block takes
     // one unit (rows along x: their count B (G + 1) can pass the 65535 limit of
     // y).
@@ -480,7 +484,7 @@ cudaError_t launch_verify_rows_t(const VerifyArgs &a, const VerifyPlan &p, cudaS
     const dim3 grid((unsigned int)(a.B * (a.G + 1)), (unsigned int)p.row_split);
     verify_rows_kernel<TIn><<<grid, kRowThreads, 0, s>>>(target, a.target_row0, a.n_target_rows, a.verify_len,
                                                          a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split,
-                                                         row_part);
+                                                         row_part, reinterpret_cast<uint32_t *>(a.ws));
     return cudaGetLastError();
 }
 
