@@ -267,6 +267,7 @@ schedule_kernel(const float *__restrict__ conf_logits, const float *__restrict__
                 float threshold, float *__restrict__ conf, float *__restrict__ cum_conf,
                 int32_t *__restrict__ verify_len, double *__restrict__ theta_out,
                 uint32_t *__restrict__ flags) {
+    griddep_wait();  // a programmatic dependent: the previous launch's writes are visible after this
     extern __shared__ unsigned long long smem[];
     // the sort runs over nsort keys: the candidates' power of two, at least one per thread
     const int nsort = max(npow2, kSchedThreads);
@@ -443,10 +444,11 @@ cudaError_t launch_schedule(const ScheduleArgs &a, cudaStream_t s) {
     });
     if (e != cudaSuccess) return e;
     if (smem > (size_t)kScheduleMaxSmem) return cudaErrorInvalidValue;
-    schedule_kernel<<<1, kSchedThreads, smem, s>>>(a.conf_logits, a.pos_temp, a.sps, a.B, a.G, a.L_min,
-                                                    a.L_max, npow2, a.policy, a.threshold, a.conf, a.cum_conf,
-                                                    a.verify_len, a.theta_out, reinterpret_cast<uint32_t *>(a.ws));
-    return cudaGetLastError();
+    // a programmatic dependent of the launch before it (the kernel waits for
+    // that launch before its first access)
+    return launch_dependent(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, s, a.conf_logits, a.pos_temp,
+                            a.sps, a.B, a.G, a.L_min, a.L_max, npow2, a.policy, a.threshold, a.conf, a.cum_conf,
+                            a.verify_len, a.theta_out, reinterpret_cast<uint32_t *>(a.ws));
 }
 
 }  // namespace dspark

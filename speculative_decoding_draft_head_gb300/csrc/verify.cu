@@ -99,6 +99,7 @@ verify_rows_kernel(const TIn *__restrict__ target, const int64_t *__restrict__ r
                    const float *__restrict__ temperature, int B, int G, int V, int chunk, int nsplit,
                    RowState *__restrict__ part, uint32_t *__restrict__ flags) {
     __shared__ RowState scratch[kRowThreads / 32];
+    griddep_wait();  // a programmatic dependent: the previous launch's writes are visible after this
     // the call's flag words start clear: this pass, the call's first launch,
     // raises none, and every later launch of the call reads or raises them
     // only after waiting for the launch before it
@@ -482,10 +483,9 @@ cudaError_t launch_verify_rows_t(const VerifyArgs &a, const VerifyPlan &p, cudaS
     RowState *row_part = reinterpret_cast<RowState *>(a.ws + p.row_part_offset);
     const TIn *target = static_cast<const TIn *>(a.target);
     const dim3 grid((unsigned int)(a.B * (a.G + 1)), (unsigned int)p.row_split);
-    verify_rows_kernel<TIn><<<grid, kRowThreads, 0, s>>>(target, a.target_row0, a.n_target_rows, a.verify_len,
-                                                         a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split,
-                                                         row_part, reinterpret_cast<uint32_t *>(a.ws));
-    return cudaGetLastError();
+    return launch_dependent(verify_rows_kernel<TIn>, grid, dim3(kRowThreads), 0, s, target, a.target_row0,
+                            a.n_target_rows, a.verify_len, a.temperature, a.B, a.G, a.V, p.row_chunk, p.row_split,
+                            row_part, reinterpret_cast<uint32_t *>(a.ws));
 }
 
 template <typename TIn>
