@@ -11,6 +11,8 @@ arithmetic against fp64; the draws' keys are formed in float-float, so the
 mismatches come from ties far below fp32 rounding and from the fp32
 log-probabilities passed between the calls).  The observed rate is printed.
 """
+import os
+
 import pytest
 
 from speculative_decoding_draft_head_gb300.synth import WORKLOADS
@@ -19,13 +21,22 @@ from parity import EXEMPT_RATE, Tally, full_parity
 
 pytestmark = pytest.mark.gpu
 
+# DSPARK_PARITY_VOLUME=k runs k times the seeds (new seeds each time), for a
+# longer run than the default suite's
+VOLUME = max(1, int(os.environ.get("DSPARK_PARITY_VOLUME", "1")))
+
 
 def test_millions_of_decisions():
     total = Tally()
-    runs = [(WORKLOADS["tiny"].scaled(B=16384), range(16)),
-            (WORKLOADS["dspark5"].scaled(B=2048, V=2056), range(8)),
-            (WORKLOADS["highconc"].scaled(B=2048, V=1032), range(8)),
-            (WORKLOADS["largev"].scaled(B=1024, V=4104), range(4))]
+    k = VOLUME
+    runs = [(WORKLOADS["tiny"].scaled(B=16384), range(16 * k)),
+            (WORKLOADS["dspark5"].scaled(B=2048, V=2056), range(8 * k)),
+            (WORKLOADS["highconc"].scaled(B=2048, V=1032), range(8 * k)),
+            (WORKLOADS["largev"].scaled(B=1024, V=4104), range(4 * k)),
+            # batches replicated twice (B <= 64, block of 16) and four times
+            # (B <= 32) over the accumulator rows
+            (WORKLOADS["qwen3"].scaled(B=64, V=4104), range(8 * k)),
+            (WORKLOADS["largev"].scaled(B=32, V=4104), range(8 * k))]
     for w, seeds in runs:
         for seed in seeds:
             t, _, _, _ = full_parity(w, seed)
@@ -34,5 +45,5 @@ def test_millions_of_decisions():
     rate = total.exempt / total.decisions
     print("parity volume: %d decisions, %d exempt near-tie mismatches (%.2e)" %
           (total.decisions, total.exempt, rate))
-    assert total.decisions >= 2_000_000
+    assert total.decisions >= 2_000_000 * k
     assert rate <= EXEMPT_RATE
