@@ -205,6 +205,24 @@ def test_minimal_sizes():
     tally.check()
 
 
+# the largest vocabulary the entry points take: token ids fill the 20-bit
+# field of the 64-bit key words (ids up to 2^20 - 1)
+MAX_V = 1 << 20
+
+
+@pytest.mark.parametrize("name,B,reqs", [("dspark5", 4, None),             # bf16, four replicas
+                                         ("dspark5", 40, [0, 13, 27, 39]),  # bf16, two replicas
+                                         ("tiny", 4, None)])                # fp32 weights, SIMT path
+def test_maximum_vocabulary(name, B, reqs):
+    w = WORKLOADS[name].scaled(B=B, G=2, V=MAX_V, r=16)
+    tally, g, o, _ = full_parity(w, 3, reqs=reqs)
+    tally.check_rate()
+    # every drafted token is a valid id, the top ones included
+    toks = g["draft"]["tokens"].numpy()
+    assert toks.min() >= 0 and toks.max() < MAX_V
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", ["tiny", "dspark5"])
 def test_invalid_device_inputs_are_flagged_not_read(name):
     """fp32 weights (SIMT draft writing its rows itself) and bf16 weights
