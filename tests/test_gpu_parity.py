@@ -205,6 +205,21 @@ def test_minimal_sizes():
     tally.check()
 
 
+# the longest block the entry points take (G = 64): 64 positions in one
+# cooperative launch (or one SIMT launch), verification over 65 target rows,
+# the scheduler over 63 candidates per request
+@pytest.mark.parametrize("name,B,sched", [("dspark5", 16, True),    # scheduled lengths
+                                          ("dspark5", 100, False),  # every request verifies all 64
+                                          ("tiny", 4, False)])
+def test_longest_block(name, B, sched):
+    w = WORKLOADS[name].scaled(B=B, G=64, V=2056, r=16, scheduler=sched)
+    total = Tally()
+    for seed in range(2):
+        tally, *_ = full_parity(w, 60 + seed)
+        total.add(tally)
+    total.check_rate()
+
+
 # the largest vocabulary the entry points take: token ids fill the 20-bit
 # field of the 64-bit key words (ids up to 2^20 - 1)
 MAX_V = 1 << 20
