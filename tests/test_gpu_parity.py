@@ -14,7 +14,7 @@ from speculative_decoding_draft_head_gb300 import binding
 from speculative_decoding_draft_head_gb300.synth import WORKLOADS, make_inputs
 
 from parity import (REL, Tally, compare_draft, compare_verify, full_parity, gpu_round, host_inputs,
-                    oracle_round)
+                    logq_tolerance_low_temperature, oracle_round)
 
 pytestmark = pytest.mark.gpu
 
@@ -203,6 +203,27 @@ def test_minimal_sizes():
     w2 = WORKLOADS["dspark5"].scaled(B=1, G=1, V=8, r=16, scheduler=False)
     tally, *_ = full_parity(w2, 0)
     tally.check()
+
+
+# temperatures far from 1: per-request T spread geometrically over
+# [0.02, 20] (very peaked to nearly flat draws), every 16th request greedy.
+# Tokens, acceptance and residual draws stay exact against the oracle; log q
+# is held to 1e-5 plus the fp32 representation of the logits over T
+# (logq_tolerance_low_temperature), which passes 1e-5 below T of about 0.1.
+@pytest.mark.parametrize("name", ["dspark5", "tiny"])
+def test_extreme_temperatures(name):
+    w = WORKLOADS[name].scaled(B=64, V=4104) if name != "tiny" else WORKLOADS["tiny"].scaled(B=64)
+
+    def edit(inp):
+        T = torch.logspace(np.log10(0.02), np.log10(20.0), w.B, dtype=torch.float64)
+        T[::16] = 0.0
+        inp["temperature"].copy_(T.to(torch.float32))
+
+    total = Tally()
+    for seed in range(3):
+        tally, *_ = full_parity(w, 70 + seed, edit=edit, logq_tol=logq_tolerance_low_temperature)
+        total.add(tally)
+    total.check_rate()
 
 
 # the longest block the entry points take (G = 64): 64 positions in one
