@@ -241,6 +241,20 @@ def test_longest_block(name, B, sched):
     total.check_rate()
 
 
+# ranks r whose last 64-wide K block is partial (tensor path: W_out boxes
+# zero-filled past r, a partial A-operand block, UMMA steps skipped past r),
+# and an fp32 rank that is not a multiple of 16
+@pytest.mark.parametrize("name,r", [("dspark5", 80), ("dspark5", 208), ("tiny", 52)])
+def test_ranks_with_partial_k_blocks(name, r):
+    w = (WORKLOADS[name].scaled(B=64, V=2056, r=r) if name != "tiny"
+         else WORKLOADS["tiny"].scaled(B=32, r=r))
+    total = Tally()
+    for seed in range(2):
+        tally, *_ = full_parity(w, 80 + seed)
+        total.add(tally)
+    total.check_rate()
+
+
 # the largest vocabulary the entry points take: token ids fill the 20-bit
 # field of the 64-bit key words (ids up to 2^20 - 1)
 MAX_V = 1 << 20
