@@ -987,13 +987,36 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                             for (int g = 0; g < 4; ++g) w[g] = make_uint4(0u, 0u, 0u, 0u);
                         }
                     };
-                    if (t != waited) {
+                    if constexpr (kQuad) {
+                        // four replicas: one copy of the word code.  On a tile already
+                        // waited for, the TMEM load goes first and the words are drawn
+                        // under its latency; on a new tile the words are drawn while
+                        // its UMMAs may still run, then the accumulator is waited for
+                        // and loaded (largev round 531 -> 502 us; the same form in
+                        // the one- and two-replica kernel was slower)
+                        const bool new_tile = (t != waited);
+                        if (!new_tile) tmem_ld16(taddr, acc);
+                        draw_words();
+                        if (new_tile) {
+                            bool w_ok = true;
+                            for (int tw = waited_g + 1; tw < tg && w_ok; ++tw) w_ok = pass_tile(tw);  // no sub-slice
+                            if (!w_ok || !uniform_wait(tfull(a), aph, abort)) {
+                                if (lane == 0) {
+                                    *abort = 1;
+                                    atomicOr(p.flags, kFlagTimeout);
+                                }
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            waited = t;
+                            waited_g = tg;
+                            tmem_ld16(taddr, acc);
+                        }
+                    } else if (t != waited) {
                         // a new tile: draw the words while its UMMAs may still run
                         draw_words();
-                        bool w_ok = true;
-                        if (kQuad)
-                            for (int tw = waited_g + 1; tw < tg && w_ok; ++tw) w_ok = pass_tile(tw);  // no sub-slice
-                        if (!w_ok || !uniform_wait(tfull(a), aph, abort)) {
+                        if (!uniform_wait(tfull(a), aph, abort)) {
                             if (lane == 0) {
                                 *abort = 1;
                                 atomicOr(p.flags, kFlagTimeout);
@@ -1003,7 +1026,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
                         }
                         tc_fence_after();
                         waited = t;
-                        if (kQuad) waited_g = tg;
                         tmem_ld16(taddr, acc);
                     } else {
                         // the tile is ready: issue the TMEM load, draw under its latency
